@@ -1,0 +1,176 @@
+/*
+ * dsmoe.h — C ABI of libdsmoe.so: the decode-step hot path of a speculative-verify
+ * Q4 Mixture-of-Experts layer and of the compressed-attention block selection beside it,
+ * for one GB300 (sm_103a).
+ *
+ * Sources (the pages about a DeepSeek V4.1 Flash Q4 fork with a native multi-token drafter):
+ *   - "DeepSeek V4.1F Q4 on M3 Ultra with native DSpark MTP (40tps / 800tps)", paragraph
+ *     "Decode": the 384-expert router as one dispatch, the shared expert's gate+up+SwiGLU
+ *     as one kernel, BF16 rounding done inside the producing kernels.
+ *   - same page, paragraph "DSpark": with the drafter on, a decode step is a 6-row verify,
+ *     and the 6 verify rows share one weight stream.
+ *   - same page, paragraph "Decode at depth": compressed attention picks 512 blocks per
+ *     layer; layers score only the blocks their mask admits, compact the admitted index
+ *     once per row, and take the top 512 with a bounded radix select.
+ *   The sizes, the Q4 block format, the score formula and the tie-break are the
+ *   workload definitions this library is built against (stated beside each call).
+ *
+ * Conventions shared by every call:
+ *   - Every pointer argument is DEVICE memory owned by the caller (for instance the
+ *     storage of a torch tensor), except the argument structs themselves, which live on
+ *     the host and are only read during the call. The library allocates nothing and keeps
+ *     no global state; its only state is the header of the caller's workspace.
+ *   - Calls are asynchronous on `stream` and never synchronise the host, except
+ *     ds_workspace_status(), which does.
+ *   - Arguments are validated on the host before anything is enqueued. A failed check
+ *     returns its ds_status and enqueues nothing. A failed launch returns DS_ERR_CUDA.
+ *     No C++ exception crosses this boundary.
+ *   - Calls are re-entrant provided concurrent calls use distinct workspaces.
+ *   - bf16 and fp16 values are passed as their raw 16-bit patterns (uint16_t).
+ */
+#ifndef DSMOE_H
+#define DSMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so that C callers need no CUDA header.
+ * NULL means the legacy default stream. */
+typedef struct CUstream_st* ds_stream_t;
+
+typedef enum {
+  DS_OK = 0,
+  DS_ERR_INVALID_ARG = 1,   /* null pointer, size out of range, bad alignment          */
+  DS_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement             */
+  DS_ERR_WORKSPACE = 3,     /* workspace null, misaligned or smaller than required     */
+  DS_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed             */
+  DS_ERR_TIMEOUT = 5,       /* a device-side bounded wait gave up (reported by status) */
+  DS_ERR_DEVICE_CHECK = 6   /* a device-side consistency check failed (by status)      */
+} ds_status;
+
+/* ------------------------------------------------------------------------------------
+ * Q4 weight matrix (the pages' "Q4 weights"; format as defined for this workload):
+ * a logical [rows][K] matrix in blocks of 32 consecutive values along K. Each value is
+ * an int4 q in [-8, 7]; each block has one fp16 scale; the dequantised value is
+ * scale * q (no offset, no minimum).
+ *   qs : uint8 [rows][K/2]. Block b of a row occupies bytes 16b .. 16b+15. Byte j of a
+ *        block holds value 2j in its low nibble and value 2j+1 in its high nibble, each
+ *        stored as q + 8 (0..15).
+ *   sc : fp16 bits [rows][K/32].
+ * For a stack of E experts the arrays are [E][rows][...], expert-major.
+ * qs must be 16-byte aligned; sc must be 2-byte aligned.
+ * ---------------------------------------------------------------------------------- */
+typedef struct {
+  const uint8_t* qs;
+  const uint16_t* sc;
+} ds_q4;
+
+/* One MoE layer: E routed experts + 1 shared expert, each with gate and up [I][H] and
+ * down [H][I], and a bf16 router [E][H].
+ * Limits of this build: H and I multiples of 32, 32 <= H <= 16384, 32 <= I <= 8192,
+ * 1 <= top_k <= 16, top_k <= E <= 1024. */
+typedef struct {
+  int32_t hidden;      /* H                                                   */
+  int32_t n_experts;   /* E (routed)                                          */
+  int32_t inter;       /* I (expert intermediate size)                        */
+  int32_t top_k;       /* k                                                   */
+  const uint16_t* router_w;     /* bf16 [E][H]                                */
+  ds_q4 gate, up, down;         /* routed: gate, up [E][I][H]; down [E][H][I] */
+  ds_q4 sh_gate, sh_up, sh_down;/* shared: gate, up [I][H]; down [H][I]      */
+} ds_moe_layer;
+
+/* Bytes of workspace ds_moe_verify_forward needs for this layer and R rows, or 0 when
+ * the layer or R is invalid. The workspace must be 256-byte aligned. */
+size_t ds_moe_workspace_size(const ds_moe_layer* layer, int32_t R);
+
+/* One speculative-verify step of one MoE layer for R = 1..6 rows (the pages' 6-row
+ * verify, paragraph "DSpark"). For every row r:
+ *   z_e = sum_i x[r][i] * router_w[e][i]  (fp32 accumulation), s_e = sigmoid(z_e);
+ *   the k experts with the largest s_e (ties to the lower index) in rank order, with
+ *   weights w_j = s_j / sum of the k selected s;
+ *   for the shared expert and each selected expert e:
+ *     h = bf16_rne( silu(Wg_e x_r) * (Wu_e x_r) ),   o = Wd_e h   (fp32 accumulation);
+ *   y[r] = bf16_rne( o_shared + sum_j w_j * o_j ), summed in rank order.
+ * Every Q4 weight byte of the shared expert and of the union of the experts selected by
+ * the R rows is read from HBM once per call and applied to every row that uses it.
+ * A row's results do not depend on R or on the other rows: an R-row call writes the same
+ * bytes as R one-row calls.
+ *   x        : bf16 [R][H]                        (input)
+ *   y        : bf16 [R][H]                        (output)
+ *   topk_idx : int32 [R][k], expert ids in rank order (output)
+ *   topk_w   : fp32 [R][k], renormalised weights  (output)
+ *   workspace: >= ds_moe_workspace_size bytes, 256-byte aligned; its contents on entry
+ *              are ignored and it must not be used by another call in flight.
+ * Errors: DS_ERR_INVALID_ARG (null pointer, R outside 1..6, sizes outside the limits,
+ * misaligned qs/x/y), DS_ERR_WORKSPACE, DS_ERR_CUDA. */
+ds_status ds_moe_verify_forward(const ds_moe_layer* layer, const uint16_t* x, int32_t R,
+                                uint16_t* y, int32_t* topk_idx, float* topk_w,
+                                void* workspace, size_t ws_bytes, ds_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Block selection for compressed sparse attention (the pages' paragraph "Decode at
+ * depth"), batched over L layers and R query rows. For layer l and row r, block b is
+ * admitted when b < limit[l][r] and bit (b % 32) of mask[l][r][b / 32] is set. For every
+ * admitted block the score is
+ *   d_h = fmaf chain over i = 0..D-1 ascending of q[l][r][h][i] * key[l][b][i], from 0.0f;
+ *   s   = fmaf chain over h = 0..Hh-1 ascending of head_w[l][r][h] * max(d_h, +0.0f),
+ *         from +0.0f;
+ * (bf16 inputs widened exactly to fp32; every step one correctly rounded fp32 fma).
+ * The selection is the top_k admitted blocks by (s descending, b ascending), with -0.0
+ * equal to +0.0, written in ascending b; when fewer than top_k blocks are admitted, all
+ * of them are selected and the rest of the row is -1.
+ * Limits: 1 <= L, 1 <= R <= 8, 1 <= Hh <= 16, D == 128, 1 <= N <= 2^24,
+ * 1 <= top_k <= 2048, 0 <= limit <= N. NaN inputs are a caller error (not checked).
+ * ---------------------------------------------------------------------------------- */
+typedef struct {
+  int32_t n_layers;      /* L                     */
+  int32_t n_rows;        /* R                     */
+  int32_t n_heads;       /* Hh                    */
+  int32_t head_dim;      /* D (must be 128)       */
+  int32_t n_blocks;      /* N                     */
+  int32_t top_k;         /* 512 in the workload   */
+  const uint16_t* keys;  /* bf16 [L][N][D], layer l at keys + l * key_layer_stride elements */
+  int64_t key_layer_stride; /* elements between layers, >= N * D, multiple of 8            */
+  const uint16_t* q;     /* bf16 [L][R][Hh][D]     */
+  const float* head_w;   /* fp32 [L][R][Hh]        */
+  const uint32_t* mask;  /* uint32 [L][R][ceil(N/32)] */
+  const int32_t* limit;  /* int32 [L][R]           */
+} ds_select_args;
+
+/* Bytes of workspace ds_select_blocks needs, or 0 when the arguments are invalid. */
+size_t ds_select_workspace_size(const ds_select_args* args);
+
+/* Runs scoring of admitted blocks, compaction of the admitted index once per row and the
+ * bounded radix top-k for all L x R (layer, row) pairs in one call.
+ *   sel    : int32 [L][R][top_k], selected blocks ascending, -1 padded (output)
+ *   nsel   : int32 [L][R], min(top_k, admitted count)                  (output)
+ *   cidx   : int32 [L][R][N], admitted blocks ascending (output; may be NULL)
+ *   ccount : int32 [L][R], admitted count                (output; may be NULL)
+ * cidx and ccount must be both NULL or both non-NULL.
+ * Errors: DS_ERR_INVALID_ARG (null pointer, sizes outside the limits, keys not 16-byte
+ * aligned), DS_ERR_WORKSPACE, DS_ERR_CUDA. */
+ds_status ds_select_blocks(const ds_select_args* args, int32_t* sel, int32_t* nsel,
+                           int32_t* cidx, int32_t* ccount, void* workspace,
+                           size_t ws_bytes, ds_stream_t stream);
+
+/* Synchronises `stream`, then reads the status word that the kernels of the last call on
+ * this workspace left in its header: DS_OK, DS_ERR_TIMEOUT (a bounded device wait gave
+ * up) or DS_ERR_DEVICE_CHECK (a device consistency check failed, e.g. an index out of
+ * range; the offending access was skipped). DS_ERR_CUDA when the synchronise fails.
+ * The word is reset at the start of every call that uses the workspace. */
+ds_status ds_workspace_status(const void* workspace, ds_stream_t stream);
+
+/* Static, NUL-terminated name of a status code. */
+const char* ds_status_string(ds_status s);
+
+/* Library version string, e.g. "dsmoe 0.1 sm_103a". */
+const char* ds_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSMOE_H */

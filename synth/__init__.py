@@ -1,0 +1,157 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the benchmark.
+
+This module draws random numbers and packs them into the input layouts; it holds none of
+the method's arithmetic (no routing, no dequantisation, no scoring, no selection). Both the
+oracle side and the CUDA side receive the same bytes from here.
+
+Workloads (the pages' model is private; these stand in for it, with the shapes and value
+distributions of the workload definitions):
+  - MoE layer: router bf16 N(0, 0.02); Q4 values uniform in [-8, 7] (uniform random bytes:
+    two uniform nibbles each); fp16 scales |N(0, 0.02)|; activations bf16 N(0, 1).
+  - Block select: keys and queries bf16 N(0, 1); per-head fp32 weights N(0, 1); causal limit
+    of row r at position T - R + r with T = 4N tokens (blocks of 4 tokens), i.e.
+    limit_r = floor((T - R + r + 1) / 4); the last 32 blocks below the limit always
+    admitted, the rest Bernoulli(0.7), drawn per (layer, block) and shared by the rows
+    (default) or drawn per (layer, row, block). Mask bits at or above the limit are random
+    too, so a consumer must honour the limit.
+  - Speculative acceptance: Bernoulli(a) per draft, seeded.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class MoeShape:
+    H: int   # hidden
+    E: int   # routed experts
+    I: int   # expert intermediate
+    k: int   # top-k
+
+
+@dataclass(frozen=True)
+class SelectShape:
+    L: int     # layers
+    R: int     # query rows
+    Hh: int    # index heads
+    N: int     # candidate blocks
+    topk: int
+    D: int = 128
+
+
+# The workload sizes (one MoE layer of the tiny and of the single-layer verify case; the
+# block-select cases at 64 blocks, 8k context and 300k context).
+TINY_MOE = MoeShape(H=512, E=16, I=256, k=2)
+VERIFY_MOE = MoeShape(H=4096, E=384, I=1024, k=8)
+TINY_SELECT = SelectShape(L=1, R=1, Hh=1, N=64, topk=8)
+SELECT_8K = SelectShape(L=1, R=6, Hh=8, N=2048, topk=512)
+SELECT_64K = SelectShape(L=43, R=6, Hh=8, N=16000, topk=512)
+SELECT_300K = SelectShape(L=43, R=6, Hh=8, N=75000, topk=512)
+
+SLIDING_WINDOW = 32
+P_ADMIT = 0.7
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def q4_matrix(lead: tuple, rows: int, K: int, g: torch.Generator, device):
+    """Random Q4 matrix: qs uint8 [*lead, rows, K/2] (uniform bytes), sc fp16 |N(0,0.02)|."""
+    qs = torch.randint(0, 256, (*lead, rows, K // 2), dtype=torch.uint8, generator=g, device=device)
+    sc = torch.randn((*lead, rows, K // 32), generator=g, device=device).mul_(0.02).abs_()
+    return qs, sc.to(torch.float16)
+
+
+def moe_layer(shape: MoeShape, seed: int = 0, device="cpu") -> dict:
+    """Tensors of one MoE layer (routed experts stacked expert-major + shared expert)."""
+    g = _gen(seed, device)
+    H, E, I = shape.H, shape.E, shape.I
+    d = {"router_w": torch.randn((E, H), generator=g, device=device).mul_(0.02).to(torch.bfloat16)}
+    d["gate_qs"], d["gate_sc"] = q4_matrix((E,), I, H, g, device)
+    d["up_qs"], d["up_sc"] = q4_matrix((E,), I, H, g, device)
+    d["down_qs"], d["down_sc"] = q4_matrix((E,), H, I, g, device)
+    d["sh_gate_qs"], d["sh_gate_sc"] = q4_matrix((), I, H, g, device)
+    d["sh_up_qs"], d["sh_up_sc"] = q4_matrix((), I, H, g, device)
+    d["sh_down_qs"], d["sh_down_sc"] = q4_matrix((), H, I, g, device)
+    return d
+
+
+def activations(R: int, H: int, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Verify rows: bf16 N(0, 1) [R, H]."""
+    g = _gen(seed + 1_000_003, device)
+    return torch.randn((R, H), generator=g, device=device).to(torch.bfloat16)
+
+
+def causal_limits(N: int, R: int) -> np.ndarray:
+    """limit_r = floor((p_r + 1) / 4) with p_r = 4N - R + r (row r's token position)."""
+    T = 4 * N
+    return np.array([(T - R + r + 1) // 4 for r in range(R)], dtype=np.int32)
+
+
+def pack_bits(bits: np.ndarray) -> np.ndarray:
+    """bool [..., n] -> uint32 [..., ceil(n/32)], bit b%32 of word b//32 (little-endian)."""
+    n = bits.shape[-1]
+    W = (n + 31) // 32
+    pad = np.zeros(bits.shape[:-1] + (W * 32,), dtype=bool)
+    pad[..., :n] = bits
+    by = np.packbits(pad.reshape(bits.shape[:-1] + (W * 4, 8)), axis=-1, bitorder="little")
+    return by.reshape(bits.shape[:-1] + (W * 4,)).view("<u4").astype(np.uint32)
+
+
+def admission_mask(shape: SelectShape, seed: int = 0, shared: bool = True,
+                   p: float = P_ADMIT, window: int = SLIDING_WINDOW):
+    """(mask uint32 [L,R,W], limit int32 [L,R]) on the host."""
+    rng = np.random.Generator(np.random.PCG64(seed + 7_000_001))
+    L, R, N = shape.L, shape.R, shape.N
+    lim = causal_limits(N, R)
+    if shared:
+        draw = rng.random((L, 1, N)) < p
+        bits = np.repeat(draw, R, axis=1)
+    else:
+        bits = rng.random((L, R, N)) < p
+    b = np.arange(N)
+    for r in range(R):
+        win = (b >= lim[r] - window) & (b < lim[r])
+        bits[:, r, :] |= win[None, :]
+    limit = np.broadcast_to(lim[None, :], (L, R)).astype(np.int32).copy()
+    return pack_bits(bits), limit
+
+
+def select_inputs(shape: SelectShape, seed: int = 0, device="cpu", shared_mask: bool = True) -> dict:
+    """keys bf16 [L,N,D], q bf16 [L,R,Hh,D], head_w f32 [L,R,Hh], mask int32 [L,R,W]
+    (uint32 bit patterns), limit int32 [L,R]."""
+    g = _gen(seed + 5_000_011, device)
+    L, R, Hh, N, D = shape.L, shape.R, shape.Hh, shape.N, shape.D
+    keys = torch.empty((L, N, D), dtype=torch.bfloat16, device=device)
+    for l in range(L):
+        keys[l] = torch.randn((N, D), generator=g, device=device).to(torch.bfloat16)
+    q = torch.randn((L, R, Hh, D), generator=g, device=device).to(torch.bfloat16)
+    head_w = torch.randn((L, R, Hh), generator=g, device=device)
+    mask, limit = admission_mask(shape, seed, shared=shared_mask)
+    return {
+        "keys": keys, "q": q, "head_w": head_w,
+        "mask": torch.from_numpy(mask.view(np.int32).copy()).to(device),
+        "limit": torch.from_numpy(limit).to(device),
+    }
+
+
+def draft_acceptance(n_steps: int, R: int, a: float, seed: int = 0) -> np.ndarray:
+    """uint8 [n_steps, R-1]: 1 where draft j of step t is accepted (Bernoulli(a))."""
+    rng = np.random.Generator(np.random.PCG64(seed + 9_000_007))
+    return (rng.random((n_steps, max(R - 1, 0))) < a).astype(np.uint8)
+
+
+def to_numpy_bits(t: torch.Tensor) -> np.ndarray:
+    """Host copy of a tensor's raw bits (bf16/fp16 -> uint16, int32 mask -> uint32)."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.int32:
+        return t.numpy()
+    return t.numpy()

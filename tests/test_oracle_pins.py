@@ -1,0 +1,399 @@
+"""Pins of the CPU oracle against things other than itself (no GPU needed).
+
+Each pin would fail under a plausible mistake in the oracle: a wrong nibble order or sign
+offset (Q4 golden blocks, one-hot columns), a double rounding or wrong tie rule (bf16
+golden cases, torch's converter), a transposed operand or dropped term (dequantise-then-
+numpy-matmul layer check), a wrong selection order or tie-break (full sorts, all-equal
+scores), a wrong summation order in the block score (hand-worked fp32 cases).
+"""
+import json
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+# ------------------------------------------------------------------- helpers (tests) --
+
+
+def np_dequant(qs: np.ndarray, sc: np.ndarray) -> np.ndarray:
+    """Independent numpy dequantisation of a Q4 matrix: [..., rows, K/2] bytes and fp16-bit
+    scales [..., rows, K/32] -> fp64 [..., rows, K]."""
+    lo = (qs & 15).astype(np.int64) - 8
+    hi = (qs >> 4).astype(np.int64) - 8
+    q = np.stack([lo, hi], axis=-1).reshape(qs.shape[:-1] + (qs.shape[-1] * 2,))
+    s = sc.view(np.float16).astype(np.float64)
+    return q.astype(np.float64) * np.repeat(s, 32, axis=-1)
+
+
+def bf16_to_np(bits: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+
+
+def layer_numpy(d: dict) -> dict:
+    out = {}
+    for k, v in d.items():
+        v = v.contiguous()
+        if v.dtype in (torch.bfloat16, torch.float16):
+            out[k] = v.view(torch.int16).numpy().view(np.uint16)
+        else:
+            out[k] = v.numpy()
+    return out
+
+
+# ------------------------------------------------------------------- number formats --
+
+
+def test_f16_decode_matches_numpy_all_patterns():
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = h.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_f64(int(b)) for b in h])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_bf16_decode_matches_torch():
+    b = np.arange(0, 65536, 97, dtype=np.uint32).astype(np.uint16)
+    ref = bf16_to_np(b)
+    got = np.array([oracle.bf16_to_f64(int(x)) for x in b])
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def test_bf16_rne_golden(golden_dir):
+    d = json.loads((golden_dir / "bf16_rne.json").read_text())
+    for c in d["cases"]:
+        assert oracle.bf16_rne(c["value"]) == int(c["bits"], 16), c
+
+
+def test_bf16_rne_matches_torch_on_fp32_values():
+    # torch rounds fp32 -> bf16 to nearest even; on fp32 inputs there is no double rounding.
+    rng = np.random.default_rng(1)
+    v = np.concatenate([rng.standard_normal(4000), rng.standard_normal(2000) * 1e-38,
+                        rng.standard_normal(2000) * 1e30]).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.bf16_rne(float(x)) for x in v], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------------- Q4 format ----
+
+
+def test_q4_golden_blocks(golden_dir):
+    d = json.loads((golden_dir / "q4_block.json").read_text())
+    for blk in d["blocks"]:
+        qs = np.frombuffer(bytes.fromhex(blk["bytes_hex"]), dtype=np.uint8).reshape(1, 16)
+        sc = np.array([[int(blk["scale_f16_hex"], 16)]], dtype=np.uint16)
+        for k in range(32):
+            assert oracle.q4_value(qs, sc, 32, 0, k) == blk["scale"] * blk["q"][k]
+        # the numpy helper used by the other pins agrees with the hand-worked values too
+        assert np.array_equal(np_dequant(qs, sc)[0], blk["scale"] * np.array(blk["q"]))
+
+
+# ------------------------------------------------------------------------- router ----
+
+
+def test_router_onehot_closed_form():
+    # x = e_i gives z_e = Wr[e, i] exactly; top-2 of column i.
+    E, H, k = 4, 32, 2
+    wr = np.zeros((E, H), np.float32)
+    wr[:, 5] = [0.5, -1.0, 2.0, 0.25]
+    x = np.zeros((1, H), np.float32)
+    x[0, 5] = 1.0
+    to_bits = lambda a: torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    idx, w, s = oracle.router(to_bits(x), to_bits(wr), k)
+    assert idx.tolist() == [[2, 0]]
+    sig = lambda z: 1.0 / (1.0 + math.exp(-z))
+    assert s[0].tolist() == pytest.approx([sig(0.5), sig(-1.0), sig(2.0), sig(0.25)], abs=1e-15)
+    tot = sig(2.0) + sig(0.5)
+    assert w[0].tolist() == pytest.approx([sig(2.0) / tot, sig(0.5) / tot], abs=1e-15)
+
+
+def test_router_all_equal_scores_take_lowest_indices():
+    E, H, k = 16, 64, 5
+    x = synth.to_numpy_bits(synth.activations(3, H, seed=4))
+    wr = np.zeros((E, H), np.uint16)
+    idx, w, _ = oracle.router(x, wr, k)
+    assert idx.tolist() == [list(range(k))] * 3
+    assert np.all(w == 1.0 / k)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_router_full_sort_and_library_matmul(seed):
+    shape = synth.TINY_MOE
+    d = layer_numpy(synth.moe_layer(shape, seed=seed))
+    x = synth.to_numpy_bits(synth.activations(4, shape.H, seed=seed))
+    idx, w, s = oracle.router(x, d["router_w"], shape.k)
+    z = bf16_to_np(x) @ bf16_to_np(d["router_w"]).T          # library matmul, fp64
+    ref_s = 1.0 / (1.0 + np.exp(-z))
+    assert np.allclose(s, ref_s, rtol=0, atol=1e-14)
+    for r in range(x.shape[0]):
+        order = np.lexsort((np.arange(shape.E), -s[r]))    # full sort: score desc, index asc
+        assert idx[r].tolist() == order[: shape.k].tolist()
+        assert len(set(idx[r].tolist())) == shape.k
+        assert w[r].sum() == pytest.approx(1.0, abs=1e-12)
+        assert np.allclose(w[r], s[r, idx[r]] / s[r, idx[r]].sum(), rtol=1e-15)
+        # monotone: the same experts rank first by logit
+        assert set(np.argsort(-z[r], kind="stable")[: shape.k].tolist()) == set(idx[r].tolist())
+
+
+def test_router_brute_force_subsets():
+    # Among all k-subsets, the oracle's choice has the largest score sum.
+    import itertools
+    E, H, k = 7, 32, 3
+    d = layer_numpy(synth.moe_layer(synth.MoeShape(H=H, E=E, I=32, k=k), seed=11))
+    x = synth.to_numpy_bits(synth.activations(2, H, seed=11))
+    idx, _, s = oracle.router(x, d["router_w"], k)
+    for r in range(2):
+        best = max(itertools.combinations(range(E), k), key=lambda c: sum(s[r, list(c)]))
+        assert sorted(best) == sorted(idx[r].tolist())
+
+
+# ------------------------------------------------------------------ expert / layer ----
+
+
+def _onehot_layer(H=64, E=4, I=32, k=2, seed=3):
+    d = layer_numpy(synth.moe_layer(synth.MoeShape(H=H, E=E, I=I, k=k), seed=seed))
+    return d, H, E, I, k
+
+
+def test_expert_onehot_input_gives_dequantised_column():
+    d, H, E, I, k = _onehot_layer()
+    col = 37
+    x = np.zeros((1, H), np.uint16)
+    x[0, col] = 0x3F80  # 1.0
+    out = oracle.moe_forward(d, x, k, want_h=True)
+    g = np_dequant(d["sh_gate_qs"], d["sh_gate_sc"])[:, col]
+    u = np_dequant(d["sh_up_qs"], d["sh_up_sc"])[:, col]
+    want = [oracle.bf16_rne(gi / (1.0 + math.exp(-gi)) * ui) for gi, ui in zip(g, u)]
+    assert out["h"][0, 0].tolist() == want
+    for j in range(k):
+        e = out["idx"][0, j]
+        g = np_dequant(d["gate_qs"][e], d["gate_sc"][e])[:, col]
+        u = np_dequant(d["up_qs"][e], d["up_sc"][e])[:, col]
+        want = [oracle.bf16_rne(gi / (1.0 + math.exp(-gi)) * ui) for gi, ui in zip(g, u)]
+        assert out["h"][0, 1 + j].tolist() == want
+
+
+def test_expert_all_ones_weights_sum_inputs():
+    # q = 1 everywhere (nibble 9, bytes 0x99), scale 1: g = u = sum(x) for every output row.
+    d, H, E, I, k = _onehot_layer()
+    for nm in ("sh_gate", "sh_up"):
+        d[nm + "_qs"] = np.full_like(d[nm + "_qs"], 0x99)
+        d[nm + "_sc"] = np.full_like(d[nm + "_sc"], 0x3C00)  # fp16 1.0
+    x = synth.to_numpy_bits(synth.activations(1, H, seed=8))
+    out = oracle.moe_forward(d, x, k, want_h=True)
+    sx = math.fsum(bf16_to_np(x)[0])
+    want = oracle.bf16_rne(sx / (1.0 + math.exp(-sx)) * sx)
+    assert np.all(out["h"][0, 0] == want)
+
+
+@pytest.mark.parametrize("seed,R", [(0, 1), (1, 3)])
+def test_layer_matches_dequantise_then_numpy_matmul(seed, R):
+    shape = synth.TINY_MOE
+    d = layer_numpy(synth.moe_layer(shape, seed=seed))
+    x = synth.to_numpy_bits(synth.activations(R, shape.H, seed=seed))
+    out = oracle.moe_forward(d, x, shape.k, want_h=True)
+    xf = bf16_to_np(x)
+    z = xf @ bf16_to_np(d["router_w"]).T
+    s = 1.0 / (1.0 + np.exp(-z))
+
+    def expert(gq, gs, uq, us, dq, dsc, xr):
+        g = np_dequant(gq, gs) @ xr
+        u = np_dequant(uq, us) @ xr
+        hv = g / (1.0 + np.exp(-g)) * u
+        hb = torch.from_numpy(hv.astype(np.float32)).to(torch.bfloat16).double().numpy()
+        return hb, np_dequant(dq, dsc) @ hb
+
+    for r in range(R):
+        order = np.lexsort((np.arange(shape.E), -s[r]))[: shape.k]
+        wts = s[r, order] / s[r, order].sum()
+        hsh, acc = expert(d["sh_gate_qs"], d["sh_gate_sc"], d["sh_up_qs"], d["sh_up_sc"],
+                          d["sh_down_qs"], d["sh_down_sc"], xf[r])
+        hs = [hsh]
+        for j, e in enumerate(order):
+            he, o = expert(d["gate_qs"][e], d["gate_sc"][e], d["up_qs"][e], d["up_sc"][e],
+                           d["down_qs"][e], d["down_sc"][e], xf[r])
+            hs.append(he)
+            acc = acc + wts[j] * o
+        assert out["idx"][r].tolist() == order.tolist()
+        # h: the reference rounds through fp32, so allow one bf16 ulp on rare ties
+        got_h = bf16_to_np(out["h"][r])
+        want_h = np.stack(hs)
+        ulp = np.abs(want_h) * 2.0 ** -7 + 1e-30
+        assert np.all(np.abs(got_h - want_h) <= ulp)
+        assert np.mean(got_h == want_h) > 0.999
+        got_y = bf16_to_np(out["y"][r])
+        ulp_y = np.maximum(np.abs(acc) * 2.0 ** -7, 1e-6)
+        assert np.all(np.abs(got_y - acc) <= 2 * ulp_y)
+
+
+def test_layer_rows_independent():
+    shape = synth.TINY_MOE
+    d = layer_numpy(synth.moe_layer(shape, seed=5))
+    x = synth.to_numpy_bits(synth.activations(3, shape.H, seed=5))
+    full = oracle.moe_forward(d, x, shape.k)
+    for r in range(3):
+        one = oracle.moe_forward(d, x[r:r + 1], shape.k)
+        assert np.array_equal(one["y"][0], full["y"][r])
+        assert np.array_equal(one["idx"][0], full["idx"][r])
+
+
+def test_layer_idx_override_reweights_from_scores():
+    shape = synth.TINY_MOE
+    d = layer_numpy(synth.moe_layer(shape, seed=6))
+    x = synth.to_numpy_bits(synth.activations(1, shape.H, seed=6))
+    base = oracle.moe_forward(d, x, shape.k)
+    swapped = base["idx"][:, ::-1].copy()
+    alt = oracle.moe_forward(d, x, shape.k, idx_in=swapped)
+    assert alt["idx"].tolist() == swapped.tolist()
+    assert np.allclose(alt["w"], base["w"][:, ::-1], rtol=1e-15)
+
+
+# ---------------------------------------------------------------------- block select --
+
+
+def _bf16_bits(vals) -> np.ndarray:
+    return torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_block_score_golden_order(golden_dir):
+    d = json.loads((golden_dir / "canonical_score.json").read_text())
+    for c in d["cases"]:
+        Hh = len(c["heads"])
+        q = np.zeros((Hh, 128), np.float32)
+        for h, vals in enumerate(c["heads"]):
+            q[h, : len(vals)] = vals
+        key = np.zeros(128, np.float32)
+        key[: len(c["key"])] = c["key"]
+        got = oracle.block_score(_bf16_bits(q), _bf16_bits(key), np.array(c["w"], np.float32))
+        assert got == c["score"], c["name"]
+
+
+def test_block_score_integer_inputs_exact():
+    # small integers: every product and partial sum is exact in fp32, so the canonical
+    # score equals the exact integer value.
+    rng = np.random.default_rng(7)
+    for _ in range(50):
+        Hh = int(rng.integers(1, 9))
+        q = rng.integers(-4, 5, (Hh, 128))
+        k = rng.integers(-4, 5, 128)
+        w = rng.integers(-3, 4, Hh)
+        exact = int(sum(int(w[h]) * max(0, int(q[h] @ k)) for h in range(Hh)))
+        got = oracle.block_score(_bf16_bits(q.astype(np.float32)), _bf16_bits(k.astype(np.float32)),
+                                 w.astype(np.float32))
+        assert got == exact
+
+
+def _unpack(mask: np.ndarray, N: int) -> np.ndarray:
+    by = mask.astype("<u4").view(np.uint8)
+    return np.unpackbits(by.reshape(mask.shape[:-1] + (-1,)), axis=-1, bitorder="little")[..., :N].astype(bool)
+
+
+@pytest.mark.parametrize("shared", [True, False])
+def test_select_compaction_and_full_sort(shared):
+    shape = synth.SelectShape(L=2, R=3, Hh=4, N=333, topk=40)
+    inp = synth.select_inputs(shape, seed=2, shared_mask=shared)
+    keys, q = synth.to_numpy_bits(inp["keys"]), synth.to_numpy_bits(inp["q"])
+    hw, mask, limit = inp["head_w"].numpy(), inp["mask"].numpy().view(np.uint32), inp["limit"].numpy()
+    out = oracle.select(keys, q, hw, mask, limit, shape.topk)
+    bits = _unpack(mask, shape.N)
+    for l in range(shape.L):
+        for r in range(shape.R):
+            adm = np.flatnonzero(bits[l, r] & (np.arange(shape.N) < limit[l, r]))
+            n = out["ccount"][l, r]
+            assert n == len(adm)
+            assert out["cidx"][l, r, :n].tolist() == adm.tolist()
+            sc = out["cscore"][l, r, :n]
+            for j in (0, n // 2, n - 1):
+                assert sc[j] == oracle.block_score(q[l, r], keys[l, adm[j]], hw[l, r])
+            order = np.lexsort((adm, -sc.astype(np.float64)))[: shape.topk]
+            want = np.sort(adm[order])
+            m = min(shape.topk, n)
+            assert out["nsel"][l, r] == m
+            assert out["sel"][l, r, :m].tolist() == want.tolist()
+            assert np.all(out["sel"][l, r, m:] == -1)
+
+
+def test_select_fp64_sanity():
+    # every selected block scores (in fp64) at least as high as every unselected one,
+    # up to the fp32 rounding of the canonical order.
+    shape = synth.SelectShape(L=1, R=2, Hh=8, N=2048, topk=512)
+    inp = synth.select_inputs(shape, seed=9)
+    keys, q = synth.to_numpy_bits(inp["keys"]), synth.to_numpy_bits(inp["q"])
+    hw, mask, limit = inp["head_w"].numpy(), inp["mask"].numpy().view(np.uint32), inp["limit"].numpy()
+    out = oracle.select(keys, q, hw, mask, limit, shape.topk)
+    kf, qf = bf16_to_np(keys), bf16_to_np(q)
+    for r in range(shape.R):
+        n = out["ccount"][0, r]
+        adm = out["cidx"][0, r, :n]
+        d = np.einsum("hd,nd->nh", qf[0, r], kf[0, adm])
+        s64 = np.maximum(d, 0.0) @ hw[0, r].astype(np.float64)
+        scale = np.abs(hw[0, r]).sum() * np.abs(d).max()
+        chosen = np.isin(adm, out["sel"][0, r])
+        assert s64[chosen].min() >= s64[~chosen].max() - 1e-5 * scale
+
+
+def test_select_ties_take_lowest_indices():
+    # identical keys: every admitted block has the same score -> the lowest admitted ones.
+    shape = synth.SelectShape(L=1, R=2, Hh=2, N=200, topk=16)
+    inp = synth.select_inputs(shape, seed=1)
+    keys = np.tile(synth.to_numpy_bits(inp["keys"])[:, :1, :], (1, shape.N, 1))
+    q = synth.to_numpy_bits(inp["q"])
+    hw, mask, limit = inp["head_w"].numpy(), inp["mask"].numpy().view(np.uint32), inp["limit"].numpy()
+    out = oracle.select(keys, q, hw, mask, limit, shape.topk)
+    for r in range(shape.R):
+        assert out["sel"][0, r].tolist() == out["cidx"][0, r, : shape.topk].tolist()
+
+
+def test_select_fewer_admitted_than_k_pads():
+    shape = synth.SelectShape(L=1, R=1, Hh=1, N=64, topk=8)
+    inp = synth.select_inputs(shape, seed=0)
+    keys, q = synth.to_numpy_bits(inp["keys"]), synth.to_numpy_bits(inp["q"])
+    hw, limit = inp["head_w"].numpy(), inp["limit"].numpy()
+    mask = np.zeros((1, 1, 2), np.uint32)
+    mask[0, 0, 0] = (1 << 3) | (1 << 17) | (1 << 30)
+    out = oracle.select(keys, q, hw, mask, limit, shape.topk)
+    assert out["sel"][0, 0].tolist() == [3, 17, 30, -1, -1, -1, -1, -1]
+    assert out["nsel"][0, 0] == 3
+
+
+def test_select_single_head_is_partial_sort_of_relu_dot():
+    # tiny workload: one head, w = 1: score = relu(q . k) (about half exactly 0) and the
+    # selection is a textbook partial sort with the lower index first among equals.
+    shape = synth.TINY_SELECT
+    inp = synth.select_inputs(shape, seed=0)
+    keys, q = synth.to_numpy_bits(inp["keys"]), synth.to_numpy_bits(inp["q"])
+    hw = np.ones((1, 1, 1), np.float32)
+    mask, limit = inp["mask"].numpy().view(np.uint32), inp["limit"].numpy()
+    out = oracle.select(keys, q, hw, mask, limit, shape.topk)
+    bits = _unpack(mask, shape.N)[0, 0] & (np.arange(shape.N) < limit[0, 0])
+    adm = np.flatnonzero(bits)
+    dots = (bf16_to_np(keys)[0, adm] @ bf16_to_np(q)[0, 0, 0]).astype(np.float64)
+    sc = out["cscore"][0, 0, : len(adm)]
+    assert np.allclose(sc, np.maximum(dots, 0), rtol=1e-5, atol=1e-4)
+    assert np.sum(sc == 0) > 0
+    pairs = sorted(zip((-sc).tolist(), adm.tolist()))[: shape.topk]
+    assert out["sel"][0, 0].tolist() == sorted(b for _, b in pairs)
+
+
+# ------------------------------------------------------------- speculative bookkeeping --
+
+
+def test_committed_tokens_small_cases():
+    assert oracle.committed_tokens(np.array([1, 1, 0, 1, 1], np.uint8), 6) == 3
+    assert oracle.committed_tokens(np.array([0, 1, 1, 1, 1], np.uint8), 6) == 1
+    assert oracle.committed_tokens(np.ones(5, np.uint8), 6) == 6
+    assert oracle.committed_tokens(np.zeros(0, np.uint8), 1) == 1
+
+
+@pytest.mark.parametrize("a,R", [(0.5, 6), (0.7, 6), (0.9, 6), (0.7, 2)])
+def test_committed_tokens_bernoulli_mean_closed_form(a, R):
+    acc = synth.draft_acceptance(20000, R, a, seed=0)
+    mean = np.mean([oracle.committed_tokens(acc[t], R) for t in range(acc.shape[0])])
+    assert mean == pytest.approx((1 - a ** R) / (1 - a), rel=0.01)
