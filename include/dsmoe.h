@@ -41,6 +41,8 @@ extern "C" {
 /* Same object as cudaStream_t; declared here so that C callers need no CUDA header.
  * NULL means the legacy default stream. */
 typedef struct CUstream_st* ds_stream_t;
+/* Same object as cudaEvent_t. */
+typedef struct CUevent_st* ds_event_t;
 
 typedef enum {
   DS_OK = 0,
@@ -111,6 +113,16 @@ ds_status ds_moe_verify_forward(const ds_moe_layer* layer, const uint16_t* x, in
                                 uint16_t* y, int32_t* topk_idx, float* topk_w,
                                 void* workspace, size_t ws_bytes, ds_stream_t stream);
 
+/* Same as ds_moe_verify_forward, and in addition records caller-created events on
+ * `stream` right after each kernel of the call, for per-kernel timing:
+ *   marks[0] after the router, marks[1] after gate+up+SwiGLU, marks[2] after down+combine.
+ * `marks` may be NULL and any entry may be NULL (skipped). The events must belong to the
+ * stream's device. Errors as ds_moe_verify_forward; DS_ERR_CUDA if recording fails. */
+ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t* x,
+                                       int32_t R, uint16_t* y, int32_t* topk_idx,
+                                       float* topk_w, void* workspace, size_t ws_bytes,
+                                       ds_stream_t stream, const ds_event_t marks[3]);
+
 /* ------------------------------------------------------------------------------------
  * Block selection for compressed sparse attention (the pages' paragraph "Decode at
  * depth"), batched over L layers and R query rows. For layer l and row r, block b is
@@ -156,6 +168,14 @@ size_t ds_select_workspace_size(const ds_select_args* args);
 ds_status ds_select_blocks(const ds_select_args* args, int32_t* sel, int32_t* nsel,
                            int32_t* cidx, int32_t* ccount, void* workspace,
                            size_t ws_bytes, ds_stream_t stream);
+
+/* Same as ds_select_blocks, and in addition records caller-created events on `stream`
+ * right after each kernel: marks[0] after compaction, marks[1] after scoring, marks[2]
+ * after the top-k select. NULL array or entries are skipped. */
+ds_status ds_select_blocks_marked(const ds_select_args* args, int32_t* sel, int32_t* nsel,
+                                  int32_t* cidx, int32_t* ccount, void* workspace,
+                                  size_t ws_bytes, ds_stream_t stream,
+                                  const ds_event_t marks[3]);
 
 /* Synchronises `stream`, then reads the status word that the kernels of the last call on
  * this workspace left in its header: DS_OK, DS_ERR_TIMEOUT (a bounded device wait gave

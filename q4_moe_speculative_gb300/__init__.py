@@ -1,0 +1,190 @@
+"""GB300-native speculative-verify Q4 MoE layer and compressed-attention block selection.
+
+Thin Python binding over libdsmoe.so (include/dsmoe.h). Every step of the computation runs
+in the library's CUDA kernels; this module only checks tensors and passes pointers, sizes
+and the current CUDA stream. PyTorch provides device memory and streams.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _native as N
+
+__all__ = [
+    "MoeLayer", "moe_workspace_size", "moe_verify_forward", "select_workspace_size",
+    "select_blocks", "workspace_status", "version", "DsmoeError",
+]
+
+DsmoeError = N.DsmoeError
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)} (got {tuple(t.shape)})")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _check(status: int, what: str):
+    if status != N.DS_OK:
+        raise N.DsmoeError(status, what)
+
+
+@dataclass
+class MoeLayer:
+    """One MoE layer on the device (layout of include/dsmoe.h):
+    router_w bf16 [E,H]; routed gate/up qs uint8 [E,I,H/2], sc fp16 [E,I,H/32];
+    routed down qs [E,H,I/2], sc [E,H,I/32]; shared expert the same without the E axis."""
+    router_w: torch.Tensor
+    gate_qs: torch.Tensor
+    gate_sc: torch.Tensor
+    up_qs: torch.Tensor
+    up_sc: torch.Tensor
+    down_qs: torch.Tensor
+    down_sc: torch.Tensor
+    sh_gate_qs: torch.Tensor
+    sh_gate_sc: torch.Tensor
+    sh_up_qs: torch.Tensor
+    sh_up_sc: torch.Tensor
+    sh_down_qs: torch.Tensor
+    sh_down_sc: torch.Tensor
+    top_k: int
+
+    @property
+    def hidden(self) -> int:
+        return self.router_w.shape[1]
+
+    @property
+    def n_experts(self) -> int:
+        return self.router_w.shape[0]
+
+    @property
+    def inter(self) -> int:
+        return self.gate_qs.shape[1]
+
+    def validate(self):
+        E, H, I = self.n_experts, self.hidden, self.inter
+        _need(self.router_w, "router_w", torch.bfloat16, (E, H))
+        for nm, rows, K, stack in (("gate", I, H, True), ("up", I, H, True), ("down", H, I, True),
+                                   ("sh_gate", I, H, False), ("sh_up", I, H, False),
+                                   ("sh_down", H, I, False)):
+            lead = (E,) if stack else ()
+            _need(getattr(self, nm + "_qs"), nm + "_qs", torch.uint8, lead + (rows, K // 2))
+            _need(getattr(self, nm + "_sc"), nm + "_sc", torch.float16, lead + (rows, K // 32))
+
+    def struct(self) -> N.DsMoeLayer:
+        q4 = lambda a, b: N.DsQ4(_ptr(a), _ptr(b))  # noqa: E731
+        return N.DsMoeLayer(
+            self.hidden, self.n_experts, self.inter, self.top_k, _ptr(self.router_w),
+            q4(self.gate_qs, self.gate_sc), q4(self.up_qs, self.up_sc),
+            q4(self.down_qs, self.down_sc), q4(self.sh_gate_qs, self.sh_gate_sc),
+            q4(self.sh_up_qs, self.sh_up_sc), q4(self.sh_down_qs, self.sh_down_sc))
+
+    @staticmethod
+    def from_dict(d: dict, top_k: int) -> "MoeLayer":
+        keys = ("router_w gate_qs gate_sc up_qs up_sc down_qs down_sc sh_gate_qs sh_gate_sc "
+                "sh_up_qs sh_up_sc sh_down_qs sh_down_sc").split()
+        return MoeLayer(**{k: d[k] for k in keys}, top_k=top_k)
+
+
+def version() -> str:
+    return N.load().ds_version().decode()
+
+
+def moe_workspace_size(layer: MoeLayer, R: int) -> int:
+    st = layer.struct()
+    return int(N.load().ds_moe_workspace_size(st, R))
+
+
+def moe_verify_forward(layer: MoeLayer, x: torch.Tensor, *, y=None, topk_idx=None, topk_w=None,
+                       workspace=None, stream=None, validate: bool = True):
+    """One verify step of one MoE layer for R = x.shape[0] rows (1..6).
+    Returns (y bf16 [R,H], topk_idx int32 [R,k], topk_w fp32 [R,k])."""
+    lib = N.load()
+    R, H = x.shape
+    k = layer.top_k
+    if validate:
+        layer.validate()
+        _need(x, "x", torch.bfloat16, (R, layer.hidden))
+    dev = x.device
+    y = torch.empty((R, H), dtype=torch.bfloat16, device=dev) if y is None else y
+    topk_idx = torch.empty((R, k), dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
+    topk_w = torch.empty((R, k), dtype=torch.float32, device=dev) if topk_w is None else topk_w
+    if validate:
+        _need(y, "y", torch.bfloat16, (R, H))
+        _need(topk_idx, "topk_idx", torch.int32, (R, k))
+        _need(topk_w, "topk_w", torch.float32, (R, k))
+    st = layer.struct()
+    if workspace is None:
+        workspace = torch.empty(int(lib.ds_moe_workspace_size(st, R)), dtype=torch.uint8, device=dev)
+    status = lib.ds_moe_verify_forward(st, _ptr(x), R, _ptr(y), _ptr(topk_idx), _ptr(topk_w),
+                                       _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(status, "ds_moe_verify_forward")
+    return y, topk_idx, topk_w
+
+
+def _select_struct(keys, q, head_w, mask, limit, top_k, key_layer_stride=None) -> N.DsSelectArgs:
+    L, Nb, D = keys.shape
+    _, R, Hh, _ = q.shape
+    stride = keys.stride(0) if key_layer_stride is None else key_layer_stride
+    return N.DsSelectArgs(L, R, Hh, D, Nb, top_k, _ptr(keys), stride, _ptr(q), _ptr(head_w),
+                          _ptr(mask), _ptr(limit))
+
+
+def select_workspace_size(keys, q, head_w, mask, limit, top_k: int) -> int:
+    return int(N.load().ds_select_workspace_size(_select_struct(keys, q, head_w, mask, limit, top_k)))
+
+
+def select_blocks(keys, q, head_w, mask, limit, top_k: int = 512, *, sel=None, nsel=None,
+                  cidx=None, ccount=None, want_compacted: bool = False, workspace=None,
+                  stream=None, validate: bool = True):
+    """Block selection for L layers x R rows.
+    keys bf16 [L,N,128]; q bf16 [L,R,Hh,128]; head_w fp32 [L,R,Hh]; mask int32 [L,R,ceil(N/32)]
+    (bit patterns); limit int32 [L,R]. Returns (sel [L,R,top_k], nsel [L,R], cidx, ccount),
+    the last two None unless want_compacted or passed in."""
+    lib = N.load()
+    L, Nb, D = keys.shape
+    R, Hh = q.shape[1], q.shape[2]
+    W = (Nb + 31) // 32
+    if validate:
+        _need(keys, "keys", torch.bfloat16, (L, Nb, D))
+        _need(q, "q", torch.bfloat16, (L, R, Hh, D))
+        _need(head_w, "head_w", torch.float32, (L, R, Hh))
+        _need(mask, "mask", torch.int32, (L, R, W))
+        _need(limit, "limit", torch.int32, (L, R))
+    dev = keys.device
+    sel = torch.empty((L, R, top_k), dtype=torch.int32, device=dev) if sel is None else sel
+    nsel = torch.empty((L, R), dtype=torch.int32, device=dev) if nsel is None else nsel
+    if want_compacted and cidx is None:
+        cidx = torch.empty((L, R, Nb), dtype=torch.int32, device=dev)
+        ccount = torch.empty((L, R), dtype=torch.int32, device=dev)
+    args = _select_struct(keys, q, head_w, mask, limit, top_k)
+    if workspace is None:
+        workspace = torch.empty(int(lib.ds_select_workspace_size(args)), dtype=torch.uint8, device=dev)
+    status = lib.ds_select_blocks(args, _ptr(sel), _ptr(nsel), _ptr(cidx), _ptr(ccount),
+                                  _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(status, "ds_select_blocks")
+    return sel, nsel, cidx, ccount
+
+
+def workspace_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns the device status code left in the workspace."""
+    return int(N.load().ds_workspace_status(_ptr(workspace), _stream(stream)))

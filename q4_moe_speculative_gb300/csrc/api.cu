@@ -1,0 +1,208 @@
+// api.cu — the C ABI of libdsmoe.so: host-side validation, workspace carving and the
+// launch sequence of each call. Nothing here allocates memory or synchronises, except
+// ds_workspace_status(), which synchronises the stream to read the device status word.
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dsmoe {
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace dsmoe
+
+using namespace dsmoe;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool q4_ok(const ds_q4& w) { return w.qs && w.sc && aligned(w.qs, 16) && aligned(w.sc, 2); }
+
+ds_status check_layer(const ds_moe_layer* L, int32_t R) {
+  if (!L) return DS_ERR_INVALID_ARG;
+  if (R < 1 || R > kMaxRows) return DS_ERR_INVALID_ARG;
+  if (L->hidden < 32 || L->hidden > 16384 || L->hidden % 32) return DS_ERR_INVALID_ARG;
+  if (L->inter < 32 || L->inter > 8192 || L->inter % 32) return DS_ERR_INVALID_ARG;
+  if (L->top_k < 1 || L->top_k > kMaxTopK) return DS_ERR_INVALID_ARG;
+  if (L->n_experts < L->top_k || L->n_experts > kMaxExperts) return DS_ERR_INVALID_ARG;
+  if (!L->router_w || !aligned(L->router_w, 16)) return DS_ERR_INVALID_ARG;
+  if (!q4_ok(L->gate) || !q4_ok(L->up) || !q4_ok(L->down) || !q4_ok(L->sh_gate) ||
+      !q4_ok(L->sh_up) || !q4_ok(L->sh_down))
+    return DS_ERR_INVALID_ARG;
+  return DS_OK;
+}
+
+MoeDims dims_of(const ds_moe_layer* L, int32_t R) {
+  return MoeDims{R, L->hidden, L->n_experts, L->inter, L->top_k};
+}
+
+ds_status check_select(const ds_select_args* a) {
+  if (!a) return DS_ERR_INVALID_ARG;
+  if (a->n_layers < 1 || a->n_rows < 1 || a->n_rows > 8) return DS_ERR_INVALID_ARG;
+  if (a->n_heads < 1 || a->n_heads > 16 || a->head_dim != 128) return DS_ERR_INVALID_ARG;
+  if (a->n_blocks < 1 || a->n_blocks > (1 << 24)) return DS_ERR_INVALID_ARG;
+  if (a->top_k < 1 || a->top_k > 2048) return DS_ERR_INVALID_ARG;
+  if (a->key_layer_stride < (int64_t)a->n_blocks * a->head_dim || a->key_layer_stride % 8)
+    return DS_ERR_INVALID_ARG;
+  if (!a->keys || !aligned(a->keys, 16) || !a->q || !aligned(a->q, 4) || !a->head_w ||
+      !a->mask || !a->limit)
+    return DS_ERR_INVALID_ARG;
+  return DS_OK;
+}
+
+// Records marks[i] on s when present; false if recording failed.
+bool mark(const ds_event_t* marks, int i, cudaStream_t s) {
+  if (!marks || !marks[i]) return true;
+  return cudaEventRecord(reinterpret_cast<cudaEvent_t>(marks[i]), s) == cudaSuccess;
+}
+
+SelDims sdims_of(const ds_select_args* a) {
+  return SelDims{a->n_layers, a->n_rows, a->n_heads, a->head_dim, a->n_blocks, a->top_k,
+                 a->key_layer_stride};
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ds_moe_workspace_size(const ds_moe_layer* layer, int32_t R) {
+  if (!layer || R < 1 || R > kMaxRows || layer->hidden < 32 || layer->inter < 32 ||
+      layer->top_k < 1 || layer->top_k > kMaxTopK || layer->n_experts < layer->top_k ||
+      layer->n_experts > kMaxExperts)
+    return 0;
+  return moe_layout(dims_of(layer, R)).total;
+}
+
+ds_status ds_moe_verify_forward(const ds_moe_layer* layer, const uint16_t* x, int32_t R,
+                                uint16_t* y, int32_t* topk_idx, float* topk_w,
+                                void* workspace, size_t ws_bytes, ds_stream_t stream) {
+  return ds_moe_verify_forward_marked(layer, x, R, y, topk_idx, topk_w, workspace, ws_bytes,
+                                      stream, nullptr);
+}
+
+ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t* x,
+                                       int32_t R, uint16_t* y, int32_t* topk_idx,
+                                       float* topk_w, void* workspace, size_t ws_bytes,
+                                       ds_stream_t stream, const ds_event_t marks[3]) {
+  ds_status st = check_layer(layer, R);
+  if (st != DS_OK) return st;
+  if (!x || !y || !topk_idx || !topk_w || !aligned(x, 16) || !aligned(y, 4) ||
+      !aligned(topk_idx, 4) || !aligned(topk_w, 4))
+    return DS_ERR_INVALID_ARG;
+  const MoeDims d = dims_of(layer, R);
+  const MoeLayout L = moe_layout(d);
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return DS_ERR_WORKSPACE;
+
+  char* base = static_cast<char*>(workspace);
+  MoeWorkspace ws{};
+  ws.header = reinterpret_cast<uint32_t*>(base + L.header);
+  ws.tile_count = reinterpret_cast<uint32_t*>(base + L.tile_count);
+  ws.logits = reinterpret_cast<float*>(base + L.logits);
+  ws.route = reinterpret_cast<RouteInfo*>(base + L.route);
+  ws.h = reinterpret_cast<uint16_t*>(base + L.h);
+  ws.opart = reinterpret_cast<float*>(base + L.opart);
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(base, 0, L.zero_bytes, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (launch_router(d, x, layer->router_w, topk_idx, topk_w, ws, s) != cudaSuccess)
+    return DS_ERR_CUDA;
+  if (!mark(marks, 0, s)) return DS_ERR_CUDA;
+  const Q4Ptr gate{layer->gate.qs, layer->gate.sc}, up{layer->up.qs, layer->up.sc};
+  const Q4Ptr down{layer->down.qs, layer->down.sc};
+  const Q4Ptr sg{layer->sh_gate.qs, layer->sh_gate.sc}, su{layer->sh_up.qs, layer->sh_up.sc};
+  const Q4Ptr sd{layer->sh_down.qs, layer->sh_down.sc};
+  if (launch_gate_up(d, x, gate, up, sg, su, ws, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (!mark(marks, 1, s)) return DS_ERR_CUDA;
+  if (launch_down(d, down, sd, topk_w, y, ws, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (!mark(marks, 2, s)) return DS_ERR_CUDA;
+  return DS_OK;
+}
+
+size_t ds_select_workspace_size(const ds_select_args* args) {
+  if (check_select(args) != DS_OK) return 0;
+  // Sized for the case where the caller does not pass cidx / ccount.
+  return sel_layout(sdims_of(args), false).total;
+}
+
+ds_status ds_select_blocks(const ds_select_args* a, int32_t* sel, int32_t* nsel, int32_t* cidx,
+                           int32_t* ccount, void* workspace, size_t ws_bytes,
+                           ds_stream_t stream) {
+  return ds_select_blocks_marked(a, sel, nsel, cidx, ccount, workspace, ws_bytes, stream,
+                                 nullptr);
+}
+
+ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t* nsel,
+                                  int32_t* cidx, int32_t* ccount, void* workspace,
+                                  size_t ws_bytes, ds_stream_t stream,
+                                  const ds_event_t marks[3]) {
+  ds_status st = check_select(a);
+  if (st != DS_OK) return st;
+  if (!sel || !nsel || (cidx == nullptr) != (ccount == nullptr) || !aligned(sel, 4) ||
+      !aligned(nsel, 4))
+    return DS_ERR_INVALID_ARG;
+  const SelDims d = sdims_of(a);
+  const bool caller = cidx != nullptr;
+  const SelLayout L = sel_layout(d, caller);
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return DS_ERR_WORKSPACE;
+
+  char* base = static_cast<char*>(workspace);
+  SelWorkspace ws{};
+  ws.header = reinterpret_cast<uint32_t*>(base + L.header);
+  ws.wordoff = reinterpret_cast<int32_t*>(base + L.wordoff);
+  ws.cidx = caller ? cidx : reinterpret_cast<int32_t*>(base + L.cidx);
+  ws.ccount = caller ? ccount : reinterpret_cast<int32_t*>(base + L.ccount);
+  ws.cscore = reinterpret_cast<float*>(base + L.cscore);
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(base, 0, 256, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (launch_compact(d, a->mask, a->limit, ws, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (!mark(marks, 0, s)) return DS_ERR_CUDA;
+  if (launch_score(d, a->keys, a->q, a->head_w, a->mask, a->limit, ws, s) != cudaSuccess)
+    return DS_ERR_CUDA;
+  if (!mark(marks, 1, s)) return DS_ERR_CUDA;
+  if (launch_topk(d, sel, nsel, ws, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (!mark(marks, 2, s)) return DS_ERR_CUDA;
+  return DS_OK;
+}
+
+ds_status ds_workspace_status(const void* workspace, ds_stream_t stream) {
+  if (!workspace || !aligned(workspace, 256)) return DS_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DS_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DS_ERR_CUDA;
+  if (word & kStatusTimeout) return DS_ERR_TIMEOUT;
+  if (word & kStatusCheck) return DS_ERR_DEVICE_CHECK;
+  return DS_OK;
+}
+
+const char* ds_status_string(ds_status s) {
+  switch (s) {
+    case DS_OK: return "DS_OK";
+    case DS_ERR_INVALID_ARG: return "DS_ERR_INVALID_ARG";
+    case DS_ERR_UNSUPPORTED: return "DS_ERR_UNSUPPORTED";
+    case DS_ERR_WORKSPACE: return "DS_ERR_WORKSPACE";
+    case DS_ERR_CUDA: return "DS_ERR_CUDA";
+    case DS_ERR_TIMEOUT: return "DS_ERR_TIMEOUT";
+    case DS_ERR_DEVICE_CHECK: return "DS_ERR_DEVICE_CHECK";
+  }
+  return "DS_ERR_UNKNOWN";
+}
+
+const char* ds_version(void) { return "dsmoe 0.1 sm_103a"; }
+
+}  // extern "C"

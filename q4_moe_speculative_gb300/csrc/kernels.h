@@ -1,0 +1,88 @@
+// kernels.h — internal interface between the host API (api.cu) and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace dsmoe {
+
+constexpr int kMaxRows = 6;        // verify rows per MoE call
+constexpr int kMaxTopK = 16;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxUnion = kMaxRows * kMaxTopK;
+
+// Routing result shared by K1 (writer) and K3/K4 (readers); lives in the workspace.
+struct RouteInfo {
+  int32_t n_union;                  // distinct routed experts over the R rows
+  int32_t pad[3];
+  int32_t expert[kMaxUnion];        // ascending expert id
+  uint32_t rowmask[kMaxUnion];      // bit r: row r selected this expert
+  int8_t slot[kMaxUnion][8];        // rank + 1 of the expert in row r (slot 0 = shared)
+};
+
+struct Q4Ptr {
+  const uint8_t* qs;
+  const uint16_t* sc;
+};
+
+struct MoeDims {
+  int R, H, E, I, k;
+};
+
+struct MoeWorkspace {
+  uint32_t* header;        // WsHeader
+  uint32_t* tile_count;    // K4 arrivals per H tile
+  float* logits;           // [R][E]
+  RouteInfo* route;
+  uint16_t* h;             // bf16 [R][1+k][I]
+  float* opart;            // [R][1+k][H]
+};
+
+// K4 processes H in tiles of this many output rows.
+constexpr int kDownTileH = 64;
+
+struct MoeLayout {
+  size_t header, tile_count, logits, route, h, opart, total, zero_bytes;
+};
+MoeLayout moe_layout(const MoeDims& d);
+
+cudaError_t launch_router(const MoeDims& d, const uint16_t* x, const uint16_t* router_w,
+                          int32_t* topk_idx, float* topk_w, const MoeWorkspace& ws,
+                          cudaStream_t s);
+cudaError_t launch_gate_up(const MoeDims& d, const uint16_t* x, Q4Ptr gate, Q4Ptr up,
+                           Q4Ptr sh_gate, Q4Ptr sh_up, const MoeWorkspace& ws,
+                           cudaStream_t s);
+cudaError_t launch_down(const MoeDims& d, Q4Ptr down, Q4Ptr sh_down, const float* topk_w,
+                        uint16_t* y, const MoeWorkspace& ws, cudaStream_t s);
+
+// ------------------------------------------------------------------ block select ----
+struct SelDims {
+  int L, R, Hh, D, N, topk;
+  int64_t key_stride;
+};
+
+struct SelWorkspace {
+  uint32_t* header;
+  int32_t* wordoff;   // [L][R][W] exclusive prefix of admitted counts per mask word
+  int32_t* cidx;      // [L][R][N] (caller's array or workspace)
+  int32_t* ccount;    // [L][R]
+  float* cscore;      // [L][R][N] scores aligned with cidx
+};
+
+struct SelLayout {
+  size_t header, wordoff, cidx, ccount, cscore, total;
+};
+SelLayout sel_layout(const SelDims& d, bool caller_cidx);
+
+cudaError_t launch_compact(const SelDims& d, const uint32_t* mask, const int32_t* limit,
+                           const SelWorkspace& ws, cudaStream_t s);
+cudaError_t launch_score(const SelDims& d, const uint16_t* keys, const uint16_t* q,
+                         const float* head_w, const uint32_t* mask, const int32_t* limit,
+                         const SelWorkspace& ws, cudaStream_t s);
+cudaError_t launch_topk(const SelDims& d, int32_t* sel, int32_t* nsel, const SelWorkspace& ws,
+                        cudaStream_t s);
+
+// Cached device properties of the current device.
+int device_sm_count();
+
+}  // namespace dsmoe

@@ -62,8 +62,18 @@ def _gen(seed: int, device) -> torch.Generator:
 
 
 def q4_matrix(lead: tuple, rows: int, K: int, g: torch.Generator, device):
-    """Random Q4 matrix: qs uint8 [*lead, rows, K/2] (uniform bytes), sc fp16 |N(0,0.02)|."""
-    qs = torch.randint(0, 256, (*lead, rows, K // 2), dtype=torch.uint8, generator=g, device=device)
+    """Random Q4 matrix: qs uint8 [*lead, rows, K/2] (uniform bytes), sc fp16 |N(0,0.02)|.
+    On the host the bytes come from numpy (PCG64 seeded from `g`), which is much faster
+    than torch's host generator for gigabyte stacks; on a GPU from torch's device
+    generator. Same distributions, different bytes."""
+    shape = (*lead, rows, K // 2)
+    if torch.device(device).type == "cpu":
+        seed = int(torch.randint(0, 2**62, (1,), generator=g).item())
+        n = int(np.prod(shape))
+        words = np.random.PCG64(seed).random_raw((n + 7) // 8)   # uniform 64-bit outputs
+        qs = torch.from_numpy(words.view(np.uint8)[:n].reshape(shape).copy())
+    else:
+        qs = torch.randint(0, 256, shape, dtype=torch.uint8, generator=g, device=device)
     sc = torch.randn((*lead, rows, K // 32), generator=g, device=device).mul_(0.02).abs_()
     return qs, sc.to(torch.float16)
 

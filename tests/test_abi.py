@@ -1,0 +1,135 @@
+"""The C-ABI library loads, exports every symbol include/dsmoe.h declares, and rejects bad
+arguments on the host before anything reaches a GPU (no compute calls here)."""
+import ctypes as C
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from q4_moe_speculative_gb300.build import build_library
+    build_library()
+    from q4_moe_speculative_gb300 import _native
+    return _native.load()
+
+
+def declared_functions():
+    text = (ROOT / "include" / "dsmoe.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ds_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for n in ("ds_moe_verify_forward", "ds_select_blocks", "ds_moe_workspace_size",
+              "ds_select_workspace_size", "ds_workspace_status", "ds_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from q4_moe_speculative_gb300 import _native
+    names = declared_functions()
+    assert sorted(_native.EXPORTS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    for code, name in {0: "DS_OK", 1: "DS_ERR_INVALID_ARG", 3: "DS_ERR_WORKSPACE",
+                       5: "DS_ERR_TIMEOUT", 6: "DS_ERR_DEVICE_CHECK"}.items():
+        assert lib.ds_status_string(code).decode() == name
+    assert b"sm_103a" in lib.ds_version()
+
+
+FAKE = 1 << 20  # a 256-aligned address that is never dereferenced: validation fails first
+
+
+def fake_layer(H=4096, E=384, I=1024, k=8):
+    from q4_moe_speculative_gb300 import _native as N
+    q = N.DsQ4(FAKE, FAKE)
+    return N.DsMoeLayer(H, E, I, k, FAKE, q, q, q, q, q, q)
+
+
+def test_moe_workspace_size_host_only(lib):
+    st = fake_layer()
+    s6 = lib.ds_moe_workspace_size(st, 6)
+    s1 = lib.ds_moe_workspace_size(st, 1)
+    assert s6 > s1 > 0
+    # h [R][1+k][I] bf16 and fp32 partials [R][1+k][H] dominate
+    assert s6 >= 6 * 9 * 1024 * 2 + 6 * 9 * 4096 * 4
+    assert lib.ds_moe_workspace_size(st, 0) == 0
+    assert lib.ds_moe_workspace_size(st, 7) == 0
+
+
+@pytest.mark.parametrize("mutate,R,expect", [
+    (lambda s: None, 0, 1),
+    (lambda s: None, 7, 1),
+    (lambda s: setattr(s, "hidden", 4010), 6, 1),        # not a multiple of 32
+    (lambda s: setattr(s, "inter", 1000), 6, 1),
+    (lambda s: setattr(s, "top_k", 0), 6, 1),
+    (lambda s: setattr(s, "top_k", 17), 6, 1),
+    (lambda s: setattr(s, "n_experts", 4), 6, 1),        # E < k
+    (lambda s: setattr(s, "router_w", None), 6, 1),
+    (lambda s: setattr(s.gate, "qs", FAKE + 8), 6, 1),   # qs not 16-byte aligned
+    (lambda s: setattr(s.sh_down, "sc", None), 6, 1),
+])
+def test_moe_forward_rejects_bad_arguments(lib, mutate, R, expect):
+    st = fake_layer()
+    mutate(st)
+    r = lib.ds_moe_verify_forward(st, FAKE, R, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert r == expect
+
+
+def test_moe_forward_rejects_small_workspace(lib):
+    st = fake_layer()
+    need = lib.ds_moe_workspace_size(st, 6)
+    assert lib.ds_moe_verify_forward(st, FAKE, 6, FAKE, FAKE, FAKE, FAKE, need - 1, None) == 3
+    assert lib.ds_moe_verify_forward(st, FAKE, 6, FAKE, FAKE, FAKE, None, need, None) == 3
+    assert lib.ds_moe_verify_forward(st, FAKE, 6, FAKE, FAKE, FAKE, FAKE + 16, need, None) == 3
+
+
+def test_moe_forward_rejects_null_io(lib):
+    st = fake_layer()
+    assert lib.ds_moe_verify_forward(st, None, 6, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == 1
+    assert lib.ds_moe_verify_forward(st, FAKE, 6, None, FAKE, FAKE, FAKE, 1 << 40, None) == 1
+    assert lib.ds_moe_verify_forward(st, FAKE + 2, 6, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == 1
+
+
+def fake_select(**kw):
+    from q4_moe_speculative_gb300 import _native as N
+    a = dict(n_layers=43, n_rows=6, n_heads=8, head_dim=128, n_blocks=75000, top_k=512,
+             keys=FAKE, key_layer_stride=75000 * 128, q=FAKE, head_w=FAKE, mask=FAKE, limit=FAKE)
+    a.update(kw)
+    return N.DsSelectArgs(**a)
+
+
+def test_select_workspace_size_host_only(lib):
+    s = lib.ds_select_workspace_size(fake_select())
+    LRN = 43 * 6 * 75000
+    assert s >= LRN * 8  # compacted index + scores
+    assert lib.ds_select_workspace_size(fake_select(head_dim=64)) == 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(head_dim=64), dict(n_rows=0), dict(n_rows=9), dict(n_heads=17), dict(n_blocks=0),
+    dict(top_k=0), dict(top_k=4096), dict(key_layer_stride=100), dict(keys=FAKE + 8),
+    dict(keys=None), dict(mask=None), dict(limit=None), dict(head_w=None), dict(q=None),
+])
+def test_select_rejects_bad_arguments(lib, kw):
+    a = fake_select(**kw)
+    assert lib.ds_select_blocks(a, FAKE, FAKE, None, None, FAKE, 1 << 40, None) == 1
+
+
+def test_select_rejects_half_compacted_outputs_and_small_workspace(lib):
+    a = fake_select()
+    assert lib.ds_select_blocks(a, FAKE, FAKE, FAKE, None, FAKE, 1 << 40, None) == 1
+    need = lib.ds_select_workspace_size(a)
+    assert lib.ds_select_blocks(a, FAKE, FAKE, None, None, FAKE, need - 1, None) == 3
+
+
+def test_status_query_rejects_null(lib):
+    assert lib.ds_workspace_status(None, None) == 1
