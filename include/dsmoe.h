@@ -123,6 +123,13 @@ ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t
                                        float* topk_w, void* workspace, size_t ws_bytes,
                                        ds_stream_t stream, const ds_event_t marks[3]);
 
+/* Byte offset, inside a workspace sized by ds_moe_workspace_size(layer, R), of the bf16
+ * array h [R][1 + k][I] that ds_moe_verify_forward leaves there (slot 0 = shared expert,
+ * slot j + 1 = the row's rank-j expert): the rounded SwiGLU activations, kept for
+ * inspection. Valid once the call has completed on its stream and until the workspace is
+ * reused. Returns (size_t)-1 when the layer or R is invalid. */
+size_t ds_moe_workspace_h_offset(const ds_moe_layer* layer, int32_t R);
+
 /* ------------------------------------------------------------------------------------
  * Block selection for compressed sparse attention (the pages' paragraph "Decode at
  * depth"), batched over L layers and R query rows. For layer l and row r, block b is
@@ -151,7 +158,13 @@ typedef struct {
   const float* head_w;   /* fp32 [L][R][Hh]        */
   const uint32_t* mask;  /* uint32 [L][R][ceil(N/32)] */
   const int32_t* limit;  /* int32 [L][R]           */
+  int32_t flags;         /* 0, or DS_SELECT_CANONICAL_SCORES                        */
 } ds_select_args;
+
+/* ds_select_args.flags: compute every admitted block's score in the canonical order on
+ * CUDA cores instead of the default tensor-core scoring with exact re-scoring of the
+ * candidates near the threshold. Both give the same selection; the default is faster. */
+#define DS_SELECT_CANONICAL_SCORES 1
 
 /* Bytes of workspace ds_select_blocks needs, or 0 when the arguments are invalid. */
 size_t ds_select_workspace_size(const ds_select_args* args);

@@ -49,6 +49,8 @@ def lib() -> C.CDLL:
         L.orc_router.restype = None
         L.orc_moe_forward.argtypes = [P, P, C.c_int32, P, P, P, P, P, P]
         L.orc_moe_forward.restype = None
+        L.orc_moe_down_combine.argtypes = [P, C.c_int32, P, P, P, P]
+        L.orc_moe_down_combine.restype = None
         L.orc_block_score.argtypes = [P, P, P, C.c_int32, C.c_int32]
         L.orc_block_score.restype = C.c_float
         L.orc_select.argtypes = [C.c_int32] * 6 + [P, C.c_int64, P, P, P, P, C.c_int32,
@@ -110,6 +112,41 @@ def router(x: np.ndarray, wr: np.ndarray, k: int):
 
 
 # ----------------------------------------------------------------------- MoE layer --
+def _layer_struct(layer: dict, k: int):
+    keep = {}
+
+    def arr(name, dtype):
+        a = np.ascontiguousarray(layer[name])
+        assert a.dtype == dtype, (name, a.dtype)
+        keep[name] = a
+        return a.ctypes.data
+
+    E, H = layer["router_w"].shape
+    I = layer["gate_qs"].shape[1]
+    st = _OrcMoeLayer(H, E, I, k, arr("router_w", np.uint16),
+                      arr("gate_qs", np.uint8), arr("gate_sc", np.uint16),
+                      arr("up_qs", np.uint8), arr("up_sc", np.uint16),
+                      arr("down_qs", np.uint8), arr("down_sc", np.uint16),
+                      arr("sh_gate_qs", np.uint8), arr("sh_gate_sc", np.uint16),
+                      arr("sh_up_qs", np.uint8), arr("sh_up_sc", np.uint16),
+                      arr("sh_down_qs", np.uint8), arr("sh_down_sc", np.uint16))
+    return st, keep, (H, E, I)
+
+
+def moe_down_combine(layer: dict, k: int, idx: np.ndarray, w: np.ndarray, h: np.ndarray) -> np.ndarray:
+    """y bf16 bits [R,H] from given activations h bf16 bits [R,1+k,I], experts idx [R,k]
+    and weights w [R,k] (the layer's second half, fp64)."""
+    st, keep, (H, E, I) = _layer_struct(layer, k)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    h = _u16(h)
+    R = idx.shape[0]
+    assert h.shape == (R, 1 + k, I)
+    y = np.empty((R, H), np.uint16)
+    lib().orc_moe_down_combine(C.byref(st), R, _p(idx), _p(w), _p(h), _p(y))
+    return y
+
+
 def moe_forward(layer: dict, x: np.ndarray, k: int, idx_in: np.ndarray | None = None,
                 want_h: bool = False):
     """layer: dict of numpy arrays (router_w, gate/up/down, sh_gate/sh_up/sh_down qs and sc,

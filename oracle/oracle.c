@@ -225,6 +225,33 @@ void orc_moe_forward(const orc_moe_layer* L, const uint16_t* x, int32_t R,
   free(xr); free(acc); free(o); free(g); free(u); free(h); free(s_all);
 }
 
+/* Down projection and combine from given activations (the second half of the layer):
+ *   y[r] = bf16( Wd_shared h[r][0] + sum_j w[r][j] Wd_{idx[r][j]} h[r][1+j] ),  fp64.
+ * h_in: bf16 [R][1+k][I]. Used to compare a device's y with the oracle applied to the
+ * device's own h, which separates the two bf16 rounding points. */
+void orc_moe_down_combine(const orc_moe_layer* L, int32_t R, const int32_t* idx, const double* w,
+                          const uint16_t* h_in, uint16_t* y) {
+  const int32_t H = L->H, I = L->I, k = L->k;
+  const int64_t d_stride = (int64_t)H * I / 2, d_sstride = (int64_t)H * I / 32;
+  double* h = (double*)malloc(sizeof(double) * (size_t)I);
+  double* o = (double*)malloc(sizeof(double) * (size_t)H);
+  double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+  for (int32_t r = 0; r < R; ++r) {
+    for (int32_t i = 0; i < I; ++i) h[i] = orc_bf16_to_f64(h_in[((int64_t)r * (1 + k)) * I + i]);
+    q4_matvec(L->sd_qs, L->sd_sc, H, I, h, acc);
+    for (int32_t j = 0; j < k; ++j) {
+      int64_t e = idx[(int64_t)r * k + j];
+      for (int32_t i = 0; i < I; ++i)
+        h[i] = orc_bf16_to_f64(h_in[((int64_t)r * (1 + k) + 1 + j) * I + i]);
+      q4_matvec(L->down_qs + e * d_stride, L->down_sc + e * d_sstride, H, I, h, o);
+      double wj = w[(int64_t)r * k + j];
+      for (int32_t i = 0; i < H; ++i) acc[i] += wj * o[i];
+    }
+    for (int32_t i = 0; i < H; ++i) y[(int64_t)r * H + i] = orc_bf16_rne(acc[i]);
+  }
+  free(h); free(o); free(acc);
+}
+
 /* ------------------------------------------------------------------ block select ---- */
 
 /* Canonical fp32 score of one block for one row (reading of the score formula

@@ -141,12 +141,14 @@ def moe_verify_forward(layer: MoeLayer, x: torch.Tensor, *, y=None, topk_idx=Non
     return y, topk_idx, topk_w
 
 
-def _select_struct(keys, q, head_w, mask, limit, top_k, key_layer_stride=None) -> N.DsSelectArgs:
+def _select_struct(keys, q, head_w, mask, limit, top_k, key_layer_stride=None,
+                   canonical: bool = False) -> N.DsSelectArgs:
     L, Nb, D = keys.shape
     _, R, Hh, _ = q.shape
     stride = keys.stride(0) if key_layer_stride is None else key_layer_stride
+    flags = N.DS_SELECT_CANONICAL_SCORES if canonical else 0
     return N.DsSelectArgs(L, R, Hh, D, Nb, top_k, _ptr(keys), stride, _ptr(q), _ptr(head_w),
-                          _ptr(mask), _ptr(limit))
+                          _ptr(mask), _ptr(limit), flags)
 
 
 def select_workspace_size(keys, q, head_w, mask, limit, top_k: int) -> int:
@@ -155,11 +157,12 @@ def select_workspace_size(keys, q, head_w, mask, limit, top_k: int) -> int:
 
 def select_blocks(keys, q, head_w, mask, limit, top_k: int = 512, *, sel=None, nsel=None,
                   cidx=None, ccount=None, want_compacted: bool = False, workspace=None,
-                  stream=None, validate: bool = True):
+                  stream=None, validate: bool = True, canonical: bool = False):
     """Block selection for L layers x R rows.
     keys bf16 [L,N,128]; q bf16 [L,R,Hh,128]; head_w fp32 [L,R,Hh]; mask int32 [L,R,ceil(N/32)]
     (bit patterns); limit int32 [L,R]. Returns (sel [L,R,top_k], nsel [L,R], cidx, ccount),
-    the last two None unless want_compacted or passed in."""
+    the last two None unless want_compacted or passed in. canonical=True scores every admitted
+    block in the canonical order on CUDA cores (same selection, slower)."""
     lib = N.load()
     L, Nb, D = keys.shape
     R, Hh = q.shape[1], q.shape[2]
@@ -176,13 +179,21 @@ def select_blocks(keys, q, head_w, mask, limit, top_k: int = 512, *, sel=None, n
     if want_compacted and cidx is None:
         cidx = torch.empty((L, R, Nb), dtype=torch.int32, device=dev)
         ccount = torch.empty((L, R), dtype=torch.int32, device=dev)
-    args = _select_struct(keys, q, head_w, mask, limit, top_k)
+    args = _select_struct(keys, q, head_w, mask, limit, top_k, canonical=canonical)
     if workspace is None:
         workspace = torch.empty(int(lib.ds_select_workspace_size(args)), dtype=torch.uint8, device=dev)
     status = lib.ds_select_blocks(args, _ptr(sel), _ptr(nsel), _ptr(cidx), _ptr(ccount),
                                   _ptr(workspace), workspace.numel(), _stream(stream))
     _check(status, "ds_select_blocks")
     return sel, nsel, cidx, ccount
+
+
+def moe_workspace_h(layer: MoeLayer, R: int, workspace: torch.Tensor) -> torch.Tensor:
+    """View of the bf16 SwiGLU activations h [R, 1+k, I] that the last call left in
+    `workspace` (slot 0 = shared expert, slot j+1 = the row's rank-j expert)."""
+    off = int(N.load().ds_moe_workspace_h_offset(layer.struct(), R))
+    n = R * (1 + layer.top_k) * layer.inter
+    return workspace[off: off + 2 * n].view(torch.bfloat16).view(R, 1 + layer.top_k, layer.inter)
 
 
 def workspace_status(workspace: torch.Tensor, stream=None) -> int:

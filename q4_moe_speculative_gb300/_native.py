@@ -19,8 +19,10 @@ STATUS_NAMES = {
 EXPORTS = (
     "ds_moe_workspace_size", "ds_moe_verify_forward", "ds_select_workspace_size",
     "ds_select_blocks", "ds_workspace_status", "ds_status_string", "ds_version",
-    "ds_moe_verify_forward_marked", "ds_select_blocks_marked",
+    "ds_moe_verify_forward_marked", "ds_select_blocks_marked", "ds_moe_workspace_h_offset",
 )
+
+DS_SELECT_CANONICAL_SCORES = 1
 
 
 class DsQ4(C.Structure):
@@ -42,7 +44,7 @@ class DsSelectArgs(C.Structure):
         ("head_dim", C.c_int32), ("n_blocks", C.c_int32), ("top_k", C.c_int32),
         ("keys", C.c_void_p), ("key_layer_stride", C.c_int64),
         ("q", C.c_void_p), ("head_w", C.c_void_p),
-        ("mask", C.c_void_p), ("limit", C.c_void_p),
+        ("mask", C.c_void_p), ("limit", C.c_void_p), ("flags", C.c_int32),
     ]
 
 
@@ -73,6 +75,8 @@ def load() -> C.CDLL:
     lib.ds_moe_verify_forward.restype = C.c_int
     lib.ds_moe_verify_forward_marked.argtypes = lib.ds_moe_verify_forward.argtypes + [C.c_void_p]
     lib.ds_moe_verify_forward_marked.restype = C.c_int
+    lib.ds_moe_workspace_h_offset.argtypes = [C.POINTER(DsMoeLayer), C.c_int32]
+    lib.ds_moe_workspace_h_offset.restype = C.c_size_t
     lib.ds_select_workspace_size.argtypes = [C.POINTER(DsSelectArgs)]
     lib.ds_select_workspace_size.restype = C.c_size_t
     lib.ds_select_blocks.argtypes = [

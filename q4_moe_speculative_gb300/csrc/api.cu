@@ -60,6 +60,7 @@ ds_status check_select(const ds_select_args* a) {
   if (!a->keys || !aligned(a->keys, 16) || !a->q || !aligned(a->q, 4) || !a->head_w ||
       !a->mask || !a->limit)
     return DS_ERR_INVALID_ARG;
+  if (a->flags & ~DS_SELECT_CANONICAL_SCORES) return DS_ERR_INVALID_ARG;
   return DS_OK;
 }
 
@@ -131,6 +132,11 @@ ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t
   return DS_OK;
 }
 
+size_t ds_moe_workspace_h_offset(const ds_moe_layer* layer, int32_t R) {
+  if (ds_moe_workspace_size(layer, R) == 0) return (size_t)-1;
+  return moe_layout(dims_of(layer, R)).h;
+}
+
 size_t ds_select_workspace_size(const ds_select_args* args) {
   if (check_select(args) != DS_OK) return 0;
   // Sized for the case where the caller does not pass cidx / ccount.
@@ -165,15 +171,19 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
   ws.cidx = caller ? cidx : reinterpret_cast<int32_t*>(base + L.cidx);
   ws.ccount = caller ? ccount : reinterpret_cast<int32_t*>(base + L.ccount);
   ws.cscore = reinterpret_cast<float*>(base + L.cscore);
+  ws.chi = reinterpret_cast<float*>(base + L.chi);
+  const bool tc = !(a->flags & DS_SELECT_CANONICAL_SCORES) &&
+                  tc_scoring_supported(d, a->keys, a->q);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(base, 0, 256, s) != cudaSuccess) return DS_ERR_CUDA;
   if (launch_compact(d, a->mask, a->limit, ws, s) != cudaSuccess) return DS_ERR_CUDA;
   if (!mark(marks, 0, s)) return DS_ERR_CUDA;
-  if (launch_score(d, a->keys, a->q, a->head_w, a->mask, a->limit, ws, s) != cudaSuccess)
+  if (launch_score(d, a->keys, a->q, a->head_w, a->mask, a->limit, ws, tc, s) != cudaSuccess)
     return DS_ERR_CUDA;
   if (!mark(marks, 1, s)) return DS_ERR_CUDA;
-  if (launch_topk(d, sel, nsel, ws, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (launch_topk(d, a->keys, a->q, a->head_w, sel, nsel, ws, tc, s) != cudaSuccess)
+    return DS_ERR_CUDA;
   if (!mark(marks, 2, s)) return DS_ERR_CUDA;
   return DS_OK;
 }

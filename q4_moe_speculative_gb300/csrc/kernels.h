@@ -66,21 +66,25 @@ struct SelWorkspace {
   int32_t* wordoff;   // [L][R][W] exclusive prefix of admitted counts per mask word
   int32_t* cidx;      // [L][R][N] (caller's array or workspace)
   int32_t* ccount;    // [L][R]
-  float* cscore;      // [L][R][N] scores aligned with cidx
+  float* cscore;      // [L][R][N] aligned with cidx: canonical scores, or (tensor-core
+                      // scoring) order keys of the lower bounds of the scores
+  float* chi;         // [L][R][N] aligned with cidx: upper bounds (tensor-core scoring)
 };
 
 struct SelLayout {
-  size_t header, wordoff, cidx, ccount, cscore, total;
+  size_t header, wordoff, cidx, ccount, cscore, chi, total;
 };
 SelLayout sel_layout(const SelDims& d, bool caller_cidx);
+bool tc_scoring_supported(const SelDims& d, const uint16_t* keys, const uint16_t* q);
 
 cudaError_t launch_compact(const SelDims& d, const uint32_t* mask, const int32_t* limit,
                            const SelWorkspace& ws, cudaStream_t s);
 cudaError_t launch_score(const SelDims& d, const uint16_t* keys, const uint16_t* q,
                          const float* head_w, const uint32_t* mask, const int32_t* limit,
-                         const SelWorkspace& ws, cudaStream_t s);
-cudaError_t launch_topk(const SelDims& d, int32_t* sel, int32_t* nsel, const SelWorkspace& ws,
-                        cudaStream_t s);
+                         const SelWorkspace& ws, bool tc, cudaStream_t s);
+cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* q,
+                        const float* head_w, int32_t* sel, int32_t* nsel,
+                        const SelWorkspace& ws, bool tc, cudaStream_t s);
 
 // Cached device properties of the current device.
 int device_sm_count();

@@ -31,21 +31,31 @@ def host_layer(d: dict) -> dict:
     return {k: synth.to_numpy_bits(v) for k, v in d.items()}
 
 
-def check_case(dsm, d_dev, host, x_dev, k, y=None, idx=None, w=None):
+def check_case(dsm, d_dev, host, x_dev, k):
+    """Router (exact up to permitted near-ties), weights, h (the first bf16 rounding point:
+    exact or a budget of one-ulp flips), and y against the oracle's down projection and
+    combine applied to the device's h."""
     layer = dsm.MoeLayer.from_dict(d_dev, k)
-    if y is None:
-        y, idx, w = dsm.moe_verify_forward(layer, x_dev)
+    R = x_dev.shape[0]
+    ws = torch.empty(dsm.moe_workspace_size(layer, R), dtype=torch.uint8, device="cuda")
+    y, idx, w = dsm.moe_verify_forward(layer, x_dev, workspace=ws)
     torch.cuda.synchronize()
+    h_dev = synth.to_numpy_bits(dsm.moe_workspace_h(layer, R, ws))
     x = synth.to_numpy_bits(x_dev)
     y_b, idx_n, w_n = synth.to_numpy_bits(y), idx.cpu().numpy(), w.cpu().numpy()
-    ref = oracle.moe_forward(host, x, k)
+    ref = oracle.moe_forward(host, x, k, want_h=True)
     rep = compare.routing_report(idx_n, ref["idx"], ref["s"])
     assert not rep["rows_bad"], rep
     if rep["rows_swapped"]:
-        ref = oracle.moe_forward(host, x, k, idx_in=idx_n)
+        ref = oracle.moe_forward(host, x, k, idx_in=idx_n, want_h=True)
     assert compare.weights_ok(w_n, ref["w"])
-    yr = compare.y_report(y_b, ref["y"])
+    hr = compare.h_report(h_dev, ref["h"])
+    assert hr["ok"], hr
+    y_from_h = oracle.moe_down_combine(host, k, ref["idx"], ref["w"], h_dev)
+    yr = compare.y_report(y_b, y_from_h)
     assert yr["fail"] == 0, yr
+    yr["vs_full_oracle"] = compare.y_report(y_b, ref["y"])
+    yr["h"] = hr
     return yr
 
 
@@ -59,7 +69,7 @@ def test_tiny_config(dsm):
     shape = synth.TINY_MOE
     d, x = make(shape, 1, 0)
     yr = check_case(dsm, d, host_layer(d), x, shape.k)
-    assert yr["exact"] >= 0.95 * yr["n"]
+    assert yr["vs_full_oracle"]["exact"] >= 0.95 * yr["n"]
 
 
 @pytest.mark.parametrize("R", [1, 4, 6])
@@ -93,7 +103,8 @@ def verify_case(dsm):
 def test_verify_config_r6_matches_oracle(dsm, verify_case):
     shape, d, x = verify_case
     yr = check_case(dsm, d, host_layer(d), x, shape.k)
-    assert yr["exact"] >= 0.9 * yr["n"]
+    assert yr["vs_full_oracle"]["exact"] >= 0.9 * yr["n"]
+    assert yr["h"]["exact"] >= 0.99 * yr["h"]["n"]
 
 
 def test_r_rows_equal_single_row_calls(dsm, verify_case):

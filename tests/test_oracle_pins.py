@@ -233,6 +233,18 @@ def test_layer_matches_dequantise_then_numpy_matmul(seed, R):
         assert np.all(np.abs(got_y - acc) <= 2 * ulp_y)
 
 
+def test_down_combine_from_own_h_reproduces_y():
+    shape = synth.TINY_MOE
+    d = layer_numpy(synth.moe_layer(shape, seed=7))
+    x = synth.to_numpy_bits(synth.activations(3, shape.H, seed=7))
+    out = oracle.moe_forward(d, x, shape.k, want_h=True)
+    y = oracle.moe_down_combine(d, shape.k, out["idx"], out["w"], out["h"])
+    assert np.array_equal(y, out["y"])
+    # and it is linear in h: zero activations give zero output
+    assert np.all(oracle.moe_down_combine(d, shape.k, out["idx"], out["w"],
+                                          np.zeros_like(out["h"])) == 0)
+
+
 def test_layer_rows_independent():
     shape = synth.TINY_MOE
     d = layer_numpy(synth.moe_layer(shape, seed=5))

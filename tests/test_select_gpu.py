@@ -25,9 +25,10 @@ def to_dev(inp: dict) -> dict:
     return {k: v.to("cuda") for k, v in inp.items()}
 
 
-def run_dev(dsm, inp, topk):
+def run_dev(dsm, inp, topk, canonical=False):
     sel, nsel, cidx, ccount = dsm.select_blocks(inp["keys"], inp["q"], inp["head_w"], inp["mask"],
-                                                inp["limit"], topk, want_compacted=True)
+                                                inp["limit"], topk, want_compacted=True,
+                                                canonical=canonical)
     torch.cuda.synchronize()
     return sel.cpu().numpy(), nsel.cpu().numpy(), cidx.cpu().numpy(), ccount.cpu().numpy()
 
@@ -52,8 +53,8 @@ def assert_equal_rows(dev, ref, layers):
             assert np.array_equal(cidx[l, r, :n], ref["cidx"][l, r, :n]), (l, r)
 
 
-def check(dsm, inp, topk, layers=None):
-    dev = run_dev(dsm, to_dev(inp), topk)
+def check(dsm, inp, topk, layers=None, canonical=False):
+    dev = run_dev(dsm, to_dev(inp), topk, canonical=canonical)
     L = inp["keys"].shape[0]
     rng = (0, L) if layers is None else layers
     ref = run_ref(inp, topk, layers=rng)
@@ -69,11 +70,12 @@ def test_tiny_single_head(dsm):
     assert dev[1][0, 0] == shape.topk
 
 
+@pytest.mark.parametrize("canonical", [False, True])
 @pytest.mark.parametrize("shared", [True, False])
-def test_8k_context(dsm, shared):
+def test_8k_context(dsm, shared, canonical):
     shape = synth.SELECT_8K
     inp = synth.select_inputs(shape, seed=3, shared_mask=shared)
-    check(dsm, inp, shape.topk)
+    check(dsm, inp, shape.topk, canonical=canonical)
 
 
 def test_ragged_sizes(dsm):
@@ -96,22 +98,42 @@ def test_exact_admitted_counts(dsm, count):
     assert np.all(dev[1] == min(count, 512))
 
 
-def test_all_equal_scores_take_lowest_indices(dsm):
+@pytest.mark.parametrize("canonical", [False, True])
+def test_all_equal_scores_take_lowest_indices(dsm, canonical):
     # every key identical: all admitted scores tie; a bucket far above the shared-memory
     # residual bound (thousands of equal keys) exercises the global-memory passes.
     shape = synth.SelectShape(L=1, R=3, Hh=8, N=20000, topk=512)
     inp = synth.select_inputs(shape, seed=6)
     inp["keys"] = inp["keys"][:, :1, :].expand(-1, shape.N, -1).contiguous()
-    dev, ref = check(dsm, inp, shape.topk)
+    dev, ref = check(dsm, inp, shape.topk, canonical=canonical)
     for r in range(3):
         assert np.array_equal(dev[0][0, r], dev[2][0, r, :512])
 
 
-def test_zero_score_ties_single_head(dsm):
+@pytest.mark.parametrize("canonical", [False, True])
+def test_zero_score_ties_single_head(dsm, canonical):
     # one head, w = 1: score = relu(q.k), about half exactly +0; top-k reaches into the zeros
     shape = synth.SelectShape(L=2, R=2, Hh=1, N=4000, topk=1500)
     inp = synth.select_inputs(shape, seed=7)
     inp["head_w"] = torch.ones_like(inp["head_w"])
+    check(dsm, inp, shape.topk, canonical=canonical)
+
+
+def test_many_heads_and_rows(dsm):
+    # R * Hh = 128 (the widest tensor-core tile) and a layer stride with padding
+    shape = synth.SelectShape(L=2, R=8, Hh=16, N=3000, topk=256)
+    inp = synth.select_inputs(shape, seed=12)
+    check(dsm, inp, shape.topk)
+
+
+def test_candidate_band_overflow_falls_back(dsm):
+    # keys in 3 distinct values: thousands of near-equal tensor-core scores around the
+    # threshold overflow the candidate bound; the row is re-scored canonically.
+    shape = synth.SelectShape(L=1, R=2, Hh=8, N=30000, topk=512)
+    inp = synth.select_inputs(shape, seed=13)
+    base = inp["keys"][:, :3, :]
+    pick = torch.from_numpy(np.random.default_rng(0).integers(0, 3, shape.N))
+    inp["keys"] = base[:, pick, :].contiguous()
     check(dsm, inp, shape.topk)
 
 
@@ -131,7 +153,13 @@ def test_layers_batched_equal_single_layer_calls(dsm):
         assert np.array_equal(one[0][0], full[0][l])
         assert np.array_equal(one[1][0], full[1][l])
     again = run_dev(dsm, inp, shape.topk)
-    assert all(np.array_equal(a, b) for a, b in zip(full, again))
+    for a, b in zip(full[:2], again[:2]):           # sel, nsel
+        assert np.array_equal(a, b)
+    assert np.array_equal(full[3], again[3])        # ccount
+    for l in range(shape.L):                        # cidx up to the admitted count
+        for r in range(shape.R):
+            n = full[3][l, r]
+            assert np.array_equal(full[2][l, r, :n], again[2][l, r, :n])
 
 
 def test_300k_context_sampled_layers(dsm):
