@@ -230,7 +230,7 @@ def run_ours(args, world, rank, local):
     xs1 = [synth.activations(1, shape.H, seed=args.seed + 200 + i, device=dev) for i in range(n_x)]
     ws_moe = torch.empty(lib.ds_moe_workspace_size(structs[0], R_VERIFY), dtype=torch.uint8, device=dev)
 
-    sshape = synth.SELECT_300K
+    sshape = synth.SelectShape(L=args.select_layers, R=6, Hh=8, N=75000, topk=512)
     sel_host = synth.select_inputs(sshape, seed=args.seed, device="cpu")
     sel_in = {k: v.to(dev) for k, v in sel_host.items()}
     sargs = dsm._select_struct(sel_in["keys"], sel_in["q"], sel_in["head_w"], sel_in["mask"],
@@ -318,68 +318,71 @@ def run_ours(args, world, rank, local):
     moe_bytes = [moe_weight_bytes(shape, u) for u in unions]
     y0_sha = hashlib.sha256(y.view(torch.int16).cpu().numpy().tobytes()).hexdigest()[:16]
 
-    # R = 1 figure (same rotation, separate timed loop)
-    y1 = torch.empty((1, shape.H), dtype=torch.bfloat16, device=dev)
-    ws1 = torch.empty(lib.ds_moe_workspace_size(structs[0], 1), dtype=torch.uint8, device=dev)
-    idx1 = torch.empty((K, 1, shape.k), dtype=torch.int32, device=dev)
-    w1 = torch.empty((1, shape.k), dtype=torch.float32, device=dev)
-    r1_ev = [(ev(), ev()) for _ in range(K)]
-    for i in range(W + K):
-        li = i % nl
-        if i >= W:
-            r1_ev[i - W][0].record(stream)
-        lib.ds_moe_verify_forward(structs[li], xs1[i % n_x].data_ptr(), 1, y1.data_ptr(),
-                                  idx1[(i - W) % K].data_ptr(), w1.data_ptr(), ws1.data_ptr(),
-                                  ws1.numel(), sptr)
-        if i >= W:
-            r1_ev[i - W][1].record(stream)
-    torch.cuda.synchronize()
-    r1_ms = [a.elapsed_time(b) for a, b in r1_ev]
-    idx1_np = idx1.cpu().numpy()
-    r1_bytes = [moe_weight_bytes(shape, union_size(idx1_np[i])) for i in range(K)]
+    if args.skip_extras:   # profiling runs: only the timed step
+        r1_bytes, r1_ms, e2e_bytes, e2e_moe, e2e_sel, h2d, d2h = [1.0], [1.0], [1.0], [1.0], [1.0], 0, 0
+    else:
+        # R = 1 figure (same rotation, separate timed loop)
+        y1 = torch.empty((1, shape.H), dtype=torch.bfloat16, device=dev)
+        ws1 = torch.empty(lib.ds_moe_workspace_size(structs[0], 1), dtype=torch.uint8, device=dev)
+        idx1 = torch.empty((K, 1, shape.k), dtype=torch.int32, device=dev)
+        w1 = torch.empty((1, shape.k), dtype=torch.float32, device=dev)
+        r1_ev = [(ev(), ev()) for _ in range(K)]
+        for i in range(W + K):
+            li = i % nl
+            if i >= W:
+                r1_ev[i - W][0].record(stream)
+            lib.ds_moe_verify_forward(structs[li], xs1[i % n_x].data_ptr(), 1, y1.data_ptr(),
+                                      idx1[(i - W) % K].data_ptr(), w1.data_ptr(), ws1.data_ptr(),
+                                      ws1.numel(), sptr)
+            if i >= W:
+                r1_ev[i - W][1].record(stream)
+        torch.cuda.synchronize()
+        r1_ms = [a.elapsed_time(b) for a, b in r1_ev]
+        idx1_np = idx1.cpu().numpy()
+        r1_bytes = [moe_weight_bytes(shape, union_size(idx1_np[i])) for i in range(K)]
 
-    # end to end through the C ABI with pinned host buffers, copies inside the timed region
-    hx = [x.cpu().pin_memory() for x in xs6]
-    hq = {k: sel_host[k].pin_memory() for k in ("q", "head_w", "mask", "limit")}
-    dq = {k: torch.empty_like(sel_in[k]) for k in hq}
-    hy = torch.empty((R_VERIFY, shape.H), dtype=torch.bfloat16).pin_memory()
-    hidx = torch.empty((R_VERIFY, shape.k), dtype=torch.int32).pin_memory()
-    hw_ = torch.empty((R_VERIFY, shape.k), dtype=torch.float32).pin_memory()
-    hsel = torch.empty_like(sel, device="cpu").pin_memory()
-    hnsel = torch.empty_like(nsel, device="cpu").pin_memory()
-    dx = torch.empty_like(xs6[0])
-    sargs_e = dsm._select_struct(sel_in["keys"], dq["q"], dq["head_w"], dq["mask"], dq["limit"],
-                                 sshape.topk)
-    e2e_moe, e2e_sel = [], []
-    e2e_idx = []
-    for i in range(W + K):
-        a, b, c = ev(), ev(), ev()
-        a.record(stream)
-        dx.copy_(hx[i % n_x], non_blocking=True)
-        st = lib.ds_moe_verify_forward(structs[i % nl], dx.data_ptr(), R_VERIFY, y.data_ptr(),
-                                       scratch_idx.data_ptr(), scratch_w.data_ptr(),
-                                       ws_moe.data_ptr(), ws_moe.numel(), sptr)
-        hy.copy_(y, non_blocking=True)
-        hidx.copy_(scratch_idx, non_blocking=True)
-        hw_.copy_(scratch_w, non_blocking=True)
-        b.record(stream)
-        for k_ in hq:
-            dq[k_].copy_(hq[k_], non_blocking=True)
-        st |= lib.ds_select_blocks(sargs_e, sel.data_ptr(), nsel.data_ptr(), None, None,
-                                   ws_sel.data_ptr(), ws_sel.numel(), sptr)
-        hsel.copy_(sel, non_blocking=True)
-        hnsel.copy_(nsel, non_blocking=True)
-        c.record(stream)
-        c.synchronize()
-        if st:
-            raise RuntimeError("e2e call failed")
-        if i >= W:
-            e2e_moe.append(a.elapsed_time(b))
-            e2e_sel.append(b.elapsed_time(c))
-            e2e_idx.append(hidx.numpy().copy())
-    e2e_bytes = [moe_weight_bytes(shape, union_size(ix)) for ix in e2e_idx]
-    h2d = hx[0].numel() * 2 + sum(v.numel() * v.element_size() for v in hq.values())
-    d2h = hy.numel() * 2 + hidx.numel() * 4 + hw_.numel() * 4 + hsel.numel() * 4 + hnsel.numel() * 4
+        # end to end through the C ABI with pinned host buffers, copies inside the timed region
+        hx = [x.cpu().pin_memory() for x in xs6]
+        hq = {k: sel_host[k].pin_memory() for k in ("q", "head_w", "mask", "limit")}
+        dq = {k: torch.empty_like(sel_in[k]) for k in hq}
+        hy = torch.empty((R_VERIFY, shape.H), dtype=torch.bfloat16).pin_memory()
+        hidx = torch.empty((R_VERIFY, shape.k), dtype=torch.int32).pin_memory()
+        hw_ = torch.empty((R_VERIFY, shape.k), dtype=torch.float32).pin_memory()
+        hsel = torch.empty_like(sel, device="cpu").pin_memory()
+        hnsel = torch.empty_like(nsel, device="cpu").pin_memory()
+        dx = torch.empty_like(xs6[0])
+        sargs_e = dsm._select_struct(sel_in["keys"], dq["q"], dq["head_w"], dq["mask"], dq["limit"],
+                                     sshape.topk)
+        e2e_moe, e2e_sel = [], []
+        e2e_idx = []
+        for i in range(W + K):
+            a, b, c = ev(), ev(), ev()
+            a.record(stream)
+            dx.copy_(hx[i % n_x], non_blocking=True)
+            st = lib.ds_moe_verify_forward(structs[i % nl], dx.data_ptr(), R_VERIFY, y.data_ptr(),
+                                           scratch_idx.data_ptr(), scratch_w.data_ptr(),
+                                           ws_moe.data_ptr(), ws_moe.numel(), sptr)
+            hy.copy_(y, non_blocking=True)
+            hidx.copy_(scratch_idx, non_blocking=True)
+            hw_.copy_(scratch_w, non_blocking=True)
+            b.record(stream)
+            for k_ in hq:
+                dq[k_].copy_(hq[k_], non_blocking=True)
+            st |= lib.ds_select_blocks(sargs_e, sel.data_ptr(), nsel.data_ptr(), None, None,
+                                       ws_sel.data_ptr(), ws_sel.numel(), sptr)
+            hsel.copy_(sel, non_blocking=True)
+            hnsel.copy_(nsel, non_blocking=True)
+            c.record(stream)
+            c.synchronize()
+            if st:
+                raise RuntimeError("e2e call failed")
+            if i >= W:
+                e2e_moe.append(a.elapsed_time(b))
+                e2e_sel.append(b.elapsed_time(c))
+                e2e_idx.append(hidx.numpy().copy())
+        e2e_bytes = [moe_weight_bytes(shape, union_size(ix)) for ix in e2e_idx]
+        h2d = hx[0].numel() * 2 + sum(v.numel() * v.element_size() for v in hq.values())
+        d2h = hy.numel() * 2 + hidx.numel() * 4 + hw_.numel() * 4 + hsel.numel() * 4 + hnsel.numel() * 4
 
     # whole-job aggregation (replicas): sum of bytes / max of times
     moe_s = allreduce(sum(moe_ms) / 1e3, world, "max")
@@ -447,6 +450,11 @@ def run_ours(args, world, rank, local):
         "gpu_launches": 6 * K,
         "sha256": {"y_last_step": y0_sha},
     }
+    out["config"]["select_layers"] = args.select_layers
+    if args.skip_extras:
+        out["e2e"] = None
+        for k_ in ("moe_r1_gbs", "moe_r1_us_median", "moe_r1_pct_of_hbm_peak"):
+            out["components"][k_] = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(layers[0], xs6[0], sel_host, shape, sshape)
     return out
@@ -528,6 +536,8 @@ def main():
     ap.add_argument("--layers", type=int, default=8, help="distinct MoE layers rotated")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--select-layers", type=int, default=43, help="layers of the 300k select")
+    ap.add_argument("--skip-extras", action="store_true", help="no R=1 and end-to-end loops")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -64,7 +64,7 @@ typedef enum {
  *        stored as q + 8 (0..15).
  *   sc : fp16 bits [rows][K/32].
  * For a stack of E experts the arrays are [E][rows][...], expert-major.
- * qs must be 16-byte aligned; sc must be 2-byte aligned.
+ * qs must be 16-byte aligned; sc must be 4-byte aligned.
  * ---------------------------------------------------------------------------------- */
 typedef struct {
   const uint8_t* qs;
@@ -73,8 +73,10 @@ typedef struct {
 
 /* One MoE layer: E routed experts + 1 shared expert, each with gate and up [I][H] and
  * down [H][I], and a bf16 router [E][H].
- * Limits of this build: H and I multiples of 32, 32 <= H <= 16384, 32 <= I <= 8192,
- * 1 <= top_k <= 16, top_k <= E <= 1024. */
+ * Limits of this build: H and I multiples of 64, 64 <= H <= 16384, 64 <= I <= 8192,
+ * 1 <= top_k <= 16, top_k <= E <= 1024; the R verify rows are staged in shared memory,
+ * R * (2H + 64) bytes, which must fit beside the weight ring (e.g. H <= 6976 at R = 6;
+ * otherwise DS_ERR_UNSUPPORTED). */
 typedef struct {
   int32_t hidden;      /* H                                                   */
   int32_t n_experts;   /* E (routed)                                          */
@@ -108,7 +110,8 @@ size_t ds_moe_workspace_size(const ds_moe_layer* layer, int32_t R);
  *   workspace: >= ds_moe_workspace_size bytes, 256-byte aligned; its contents on entry
  *              are ignored and it must not be used by another call in flight.
  * Errors: DS_ERR_INVALID_ARG (null pointer, R outside 1..6, sizes outside the limits,
- * misaligned qs/x/y), DS_ERR_WORKSPACE, DS_ERR_CUDA. */
+ * misaligned qs/sc/x/y), DS_ERR_WORKSPACE, DS_ERR_UNSUPPORTED (R * H too large for the
+ * shared-memory staging), DS_ERR_CUDA. */
 ds_status ds_moe_verify_forward(const ds_moe_layer* layer, const uint16_t* x, int32_t R,
                                 uint16_t* y, int32_t* topk_idx, float* topk_w,
                                 void* workspace, size_t ws_bytes, ds_stream_t stream);

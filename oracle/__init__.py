@@ -47,9 +47,11 @@ def lib() -> C.CDLL:
         L.orc_q4_value.restype = C.c_double
         L.orc_router.argtypes = [P, C.c_int32, C.c_int32, P, C.c_int32, C.c_int32, P, P, P]
         L.orc_router.restype = None
-        L.orc_moe_forward.argtypes = [P, P, C.c_int32, P, P, P, P, P, P]
+        L.orc_moe_forward.argtypes = [P, P, C.c_int32, P, P, P, P, P, P, P]
         L.orc_moe_forward.restype = None
-        L.orc_moe_down_combine.argtypes = [P, C.c_int32, P, P, P, P]
+        L.orc_moe_down_combine.argtypes = [P, C.c_int32, P, P, P, P, P]
+        L.orc_bf16_rne_array.argtypes = [P, P, C.c_int64]
+        L.orc_bf16_rne_array.restype = None
         L.orc_moe_down_combine.restype = None
         L.orc_block_score.argtypes = [P, P, P, C.c_int32, C.c_int32]
         L.orc_block_score.restype = C.c_float
@@ -133,9 +135,11 @@ def _layer_struct(layer: dict, k: int):
     return st, keep, (H, E, I)
 
 
-def moe_down_combine(layer: dict, k: int, idx: np.ndarray, w: np.ndarray, h: np.ndarray) -> np.ndarray:
+def moe_down_combine(layer: dict, k: int, idx: np.ndarray, w: np.ndarray, h: np.ndarray,
+                     want_aux: bool = False):
     """y bf16 bits [R,H] from given activations h bf16 bits [R,1+k,I], experts idx [R,k]
-    and weights w [R,k] (the layer's second half, fp64)."""
+    and weights w [R,k] (the layer's second half, fp64). With want_aux, also returns
+    yaux [R,H,2] = (y before rounding, sum of the absolute values of its terms)."""
     st, keep, (H, E, I) = _layer_struct(layer, k)
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     w = np.ascontiguousarray(w, dtype=np.float64)
@@ -143,15 +147,24 @@ def moe_down_combine(layer: dict, k: int, idx: np.ndarray, w: np.ndarray, h: np.
     R = idx.shape[0]
     assert h.shape == (R, 1 + k, I)
     y = np.empty((R, H), np.uint16)
-    lib().orc_moe_down_combine(C.byref(st), R, _p(idx), _p(w), _p(h), _p(y))
-    return y
+    yaux = np.empty((R, H, 2), np.float64) if want_aux else None
+    lib().orc_moe_down_combine(C.byref(st), R, _p(idx), _p(w), _p(h), _p(y), _p(yaux))
+    return (y, yaux) if want_aux else y
+
+
+def bf16_rne_array(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, np.uint16)
+    lib().orc_bf16_rne_array(_p(v), _p(out), v.size)
+    return out
 
 
 def moe_forward(layer: dict, x: np.ndarray, k: int, idx_in: np.ndarray | None = None,
                 want_h: bool = False):
     """layer: dict of numpy arrays (router_w, gate/up/down, sh_gate/sh_up/sh_down qs and sc,
     bf16/fp16 as uint16). x bf16 bits [R,H].
-    Returns dict(y uint16 [R,H], idx, w, s, h uint16 [R,1+k,I] or None)."""
+    Returns dict(y uint16 [R,H], idx, w, s, h uint16 [R,1+k,I] or None, aux f64
+    [R,1+k,I,4] = (g, u, sum|g terms|, sum|u terms|) or None)."""
     keep = {}
 
     def arr(name, dtype):
@@ -176,9 +189,11 @@ def moe_forward(layer: dict, x: np.ndarray, k: int, idx_in: np.ndarray | None = 
     w = np.empty((R, k), np.float64)
     s = np.empty((R, E), np.float64)
     h = np.empty((R, 1 + k, I), np.uint16) if want_h else None
+    aux = np.empty((R, 1 + k, I, 4), np.float64) if want_h else None
     idx_in_a = None if idx_in is None else np.ascontiguousarray(idx_in, dtype=np.int32)
-    lib().orc_moe_forward(C.byref(st), _p(x), R, _p(idx_in_a), _p(y), _p(idx), _p(w), _p(s), _p(h))
-    return {"y": y, "idx": idx, "w": w, "s": s, "h": h}
+    lib().orc_moe_forward(C.byref(st), _p(x), R, _p(idx_in_a), _p(y), _p(idx), _p(w), _p(s), _p(h),
+                          _p(aux))
+    return {"y": y, "idx": idx, "w": w, "s": s, "h": h, "aux": aux}
 
 
 # -------------------------------------------------------------------- block select --

@@ -9,11 +9,15 @@ Tolerances are the workload's acceptance rules:
   - bf16 outputs: per element |dy| <= 2 bf16 ulp of y_ref, or |dy| <= 1e-2 |y_ref|;
     an element with |y_ref| < 1e-3 * rms(row) (cancellation near zero) that fails both is
     judged against 1e-2 * 1e-3 * rms(row) instead, and counted.
-  - the intermediate bf16 activations h (the first of the two rounding points): every
-    element equal to the oracle's or one bf16 ulp away (fp32 accumulation can land on the
-    other side of a rounding midpoint than fp64), at most H_FLIP_BUDGET of them; y is then
-    compared with the oracle's down projection and combine applied to the device's h, so
-    that a legitimate flip of h is not counted against y.
+  - the intermediate bf16 activations h (the first of the two rounding points) and y
+    near cancellation: the device accumulates in fp32 where the oracle uses fp64, so a
+    result may round to a different bf16 neighbour. An element passes if it is the bf16
+    rounding of some value within the fp32 accumulation band of the oracle's exact value:
+    |g_dev - g| <= ACC_REL * sum|g terms| (same for u and y), propagated through
+    silu(g) * u with silu's Lipschitz constant 1.1, plus the fp32 evaluation of silu and
+    the product (FP32_EVAL relative). y is compared with the oracle's down projection and
+    combine applied to the device's own h, so a legitimate difference in h is not counted
+    against y.
 """
 from __future__ import annotations
 
@@ -22,6 +26,8 @@ import torch
 
 TIE_GAP = 1e-5
 H_FLIP_BUDGET = 0.01
+ACC_REL = 2.0 ** -14       # fp32 accumulation over <= 16384 terms in ~150 sequential steps
+FP32_EVAL = 2.0 ** -20     # expf, division and products of the fp32 epilogue
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -87,3 +93,42 @@ def h_report(h_dev_bits: np.ndarray, h_ref_bits: np.ndarray) -> dict:
     n = int(d.size)
     return {"n": n, "exact": int(np.sum(d == 0)), "one_ulp": int(np.sum(d == 1)),
             "worse": int(np.sum(d > 1)), "ok": bool(np.all(d <= 1) and np.sum(d == 1) <= H_FLIP_BUDGET * n)}
+
+
+def _in_band(dev_bits: np.ndarray, lo: np.ndarray, hi: np.ndarray) -> np.ndarray:
+    """True where the device's bf16 value lies between bf16_rne(lo) and bf16_rne(hi)."""
+    import oracle
+    v = bf16_bits_to_f64(dev_bits)
+    vlo = bf16_bits_to_f64(oracle.bf16_rne_array(lo))
+    vhi = bf16_bits_to_f64(oracle.bf16_rne_array(hi))
+    return (v >= vlo) & (v <= vhi)
+
+
+def h_band_report(h_dev_bits: np.ndarray, aux: np.ndarray) -> dict:
+    """h from the device against the fp32 band around the oracle's exact silu(g) * u.
+    aux [..., 4] = (g, u, sum|g terms|, sum|u terms|) from oracle.moe_forward."""
+    g, u, ag, au = aux[..., 0], aux[..., 1], aux[..., 2], aux[..., 3]
+    sig = 1.0 / (1.0 + np.exp(-g))
+    silu = g * sig
+    h = silu * u
+    dg, du = ACC_REL * ag, ACC_REL * au
+    B = 1.1 * dg * (np.abs(u) + du) + np.abs(silu) * du + FP32_EVAL * np.abs(h)
+    ok = _in_band(h_dev_bits, h - B, h + B)
+    return {"n": int(ok.size), "outside": int(np.sum(~ok)), "ok": bool(np.all(ok))}
+
+
+def y_band_report(y_dev_bits: np.ndarray, y_ref_bits: np.ndarray, yaux: np.ndarray) -> dict:
+    """y from the device against the oracle applied to the device's h: the stated tolerance
+    (2 bf16 ulp or 1e-2 relative), or inside the fp32 accumulation band.
+    yaux [..., 2] = (y before rounding, sum of the absolute values of its terms)."""
+    rep = y_report(y_dev_bits, y_ref_bits)
+    y = bf16_bits_to_f64(y_dev_bits)
+    r = bf16_bits_to_f64(y_ref_bits)
+    d = np.abs(y - r)
+    tol_ok = (d <= 2 * bf16_ulp(r)) | (d <= 1e-2 * np.abs(r))
+    yraw, ay = yaux[..., 0], yaux[..., 1]
+    band_ok = _in_band(y_dev_bits, yraw - ACC_REL * ay, yraw + ACC_REL * ay)
+    ok = tol_ok | band_ok
+    rep.update({"band_only": int(np.sum(band_ok & ~tol_ok)), "outside": int(np.sum(~ok)),
+                "ok": bool(np.all(ok))})
+    return rep

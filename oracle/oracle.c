@@ -84,14 +84,26 @@ double orc_q4_value(const uint8_t* qs, const uint16_t* sc, int64_t K, int64_t ro
   return s * (double)q;
 }
 
-/* y[i] = sum_k W[i][k] * x[k] for the dequantised Q4 matrix W [rows][K], fp64. */
+/* y[i] = sum_k W[i][k] * x[k] for the dequantised Q4 matrix W [rows][K], fp64.
+ * If a is non-NULL, a[i] = sum_k |W[i][k] * x[k]| (the scale of the terms, used to bound
+ * the rounding error of a lower-precision evaluation of the same sum). */
+static void q4_matvec_abs(const uint8_t* qs, const uint16_t* sc, int64_t rows, int64_t K,
+                          const double* x, double* y, double* a) {
+  for (int64_t i = 0; i < rows; ++i) {
+    double acc = 0.0, aacc = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      double t = orc_q4_value(qs, sc, K, i, k) * x[k];
+      acc += t;
+      aacc += fabs(t);
+    }
+    y[i] = acc;
+    if (a) a[i] = aacc;
+  }
+}
+
 static void q4_matvec(const uint8_t* qs, const uint16_t* sc, int64_t rows, int64_t K,
                       const double* x, double* y) {
-  for (int64_t i = 0; i < rows; ++i) {
-    double acc = 0.0;
-    for (int64_t k = 0; k < K; ++k) acc += orc_q4_value(qs, sc, K, i, k) * x[k];
-    y[i] = acc;
-  }
+  q4_matvec_abs(qs, sc, rows, K, x, y, NULL);
 }
 
 /* ----------------------------------------------------------------------- router ----- */
@@ -151,16 +163,24 @@ typedef struct {
   const uint8_t* sd_qs;   const uint16_t* sd_sc;     /* shared [H][I] */
 } orc_moe_layer;
 
-/* One expert on one row: h = bf16(silu(Wg x) * (Wu x)), o = Wd h (fp64). */
+/* One expert on one row: h = bf16(silu(Wg x) * (Wu x)), o = Wd h (fp64).
+ * aux (may be NULL): per intermediate element i, {g, u, sum|Wg x terms|, sum|Wu x terms|}. */
 static void expert_forward(const uint8_t* gq, const uint16_t* gs, const uint8_t* uq,
                            const uint16_t* us, const uint8_t* dq, const uint16_t* ds,
                            int32_t H, int32_t I, const double* x, double* o,
-                           double* g, double* u, double* h) {
-  q4_matvec(gq, gs, I, H, x, g);
-  q4_matvec(uq, us, I, H, x, u);
+                           double* g, double* u, double* h, double* ag, double* au,
+                           double* aux) {
+  q4_matvec_abs(gq, gs, I, H, x, g, ag);
+  q4_matvec_abs(uq, us, I, H, x, u, au);
   for (int32_t i = 0; i < I; ++i) {
     double silu = g[i] / (1.0 + exp(-g[i]));   /* silu(g) = g * sigmoid(g) */
     h[i] = orc_bf16_to_f64(orc_bf16_rne(silu * u[i]));  /* rounding point 1 */
+    if (aux) {
+      aux[4 * i + 0] = g[i];
+      aux[4 * i + 1] = u[i];
+      aux[4 * i + 2] = ag[i];
+      aux[4 * i + 3] = au[i];
+    }
   }
   q4_matvec(dq, ds, H, I, h, o);
 }
@@ -173,7 +193,7 @@ static void expert_forward(const uint8_t* gq, const uint16_t* gs, const uint8_t*
  * h_out (may be NULL) receives the rounded h as bf16 [R][1+k][I], slot 0 = shared. */
 void orc_moe_forward(const orc_moe_layer* L, const uint16_t* x, int32_t R,
                      const int32_t* idx_in, uint16_t* y, int32_t* idx, double* w,
-                     double* s, uint16_t* h_out) {
+                     double* s, uint16_t* h_out, double* aux) {
   const int32_t H = L->H, E = L->E, I = L->I, k = L->k;
   double* s_all = (double*)malloc(sizeof(double) * (size_t)R * E);
   orc_router(x, R, H, L->router_w, E, k, idx, w, s_all);
@@ -196,6 +216,8 @@ void orc_moe_forward(const orc_moe_layer* L, const uint16_t* x, int32_t R,
   double* g = (double*)malloc(sizeof(double) * (size_t)I);
   double* u = (double*)malloc(sizeof(double) * (size_t)I);
   double* h = (double*)malloc(sizeof(double) * (size_t)I);
+  double* ag = (double*)malloc(sizeof(double) * (size_t)I);
+  double* au = (double*)malloc(sizeof(double) * (size_t)I);
   const int64_t gu_stride = (int64_t)I * H / 2, gu_sstride = (int64_t)I * H / 32;
   const int64_t d_stride = (int64_t)H * I / 2, d_sstride = (int64_t)H * I / 32;
 
@@ -203,7 +225,7 @@ void orc_moe_forward(const orc_moe_layer* L, const uint16_t* x, int32_t R,
     for (int32_t i = 0; i < H; ++i) xr[i] = orc_bf16_to_f64(x[(int64_t)r * H + i]);
     /* shared expert, weight 1 */
     expert_forward(L->sg_qs, L->sg_sc, L->su_qs, L->su_sc, L->sd_qs, L->sd_sc, H, I, xr,
-                   acc, g, u, h);
+                   acc, g, u, h, ag, au, aux ? aux + ((int64_t)r * (1 + k)) * I * 4 : NULL);
     if (h_out)
       for (int32_t i = 0; i < I; ++i)
         h_out[((int64_t)r * (1 + k) + 0) * I + i] = orc_bf16_rne(h[i]);
@@ -213,7 +235,8 @@ void orc_moe_forward(const orc_moe_layer* L, const uint16_t* x, int32_t R,
       expert_forward(L->gate_qs + e * gu_stride, L->gate_sc + e * gu_sstride,
                      L->up_qs + e * gu_stride, L->up_sc + e * gu_sstride,
                      L->down_qs + e * d_stride, L->down_sc + e * d_sstride, H, I, xr, o,
-                     g, u, h);
+                     g, u, h, ag, au,
+                     aux ? aux + ((int64_t)r * (1 + k) + 1 + j) * I * 4 : NULL);
       if (h_out)
         for (int32_t i = 0; i < I; ++i)
           h_out[((int64_t)r * (1 + k) + 1 + j) * I + i] = orc_bf16_rne(h[i]);
@@ -222,7 +245,7 @@ void orc_moe_forward(const orc_moe_layer* L, const uint16_t* x, int32_t R,
     }
     for (int32_t i = 0; i < H; ++i) y[(int64_t)r * H + i] = orc_bf16_rne(acc[i]); /* point 2 */
   }
-  free(xr); free(acc); free(o); free(g); free(u); free(h); free(s_all);
+  free(xr); free(acc); free(o); free(g); free(u); free(h); free(ag); free(au); free(s_all);
 }
 
 /* Down projection and combine from given activations (the second half of the layer):
@@ -230,26 +253,42 @@ void orc_moe_forward(const orc_moe_layer* L, const uint16_t* x, int32_t R,
  * h_in: bf16 [R][1+k][I]. Used to compare a device's y with the oracle applied to the
  * device's own h, which separates the two bf16 rounding points. */
 void orc_moe_down_combine(const orc_moe_layer* L, int32_t R, const int32_t* idx, const double* w,
-                          const uint16_t* h_in, uint16_t* y) {
+                          const uint16_t* h_in, uint16_t* y, double* yaux) {
   const int32_t H = L->H, I = L->I, k = L->k;
   const int64_t d_stride = (int64_t)H * I / 2, d_sstride = (int64_t)H * I / 32;
   double* h = (double*)malloc(sizeof(double) * (size_t)I);
   double* o = (double*)malloc(sizeof(double) * (size_t)H);
+  double* ao = (double*)malloc(sizeof(double) * (size_t)H);
   double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+  double* aacc = (double*)malloc(sizeof(double) * (size_t)H);
   for (int32_t r = 0; r < R; ++r) {
     for (int32_t i = 0; i < I; ++i) h[i] = orc_bf16_to_f64(h_in[((int64_t)r * (1 + k)) * I + i]);
-    q4_matvec(L->sd_qs, L->sd_sc, H, I, h, acc);
+    q4_matvec_abs(L->sd_qs, L->sd_sc, H, I, h, acc, aacc);
     for (int32_t j = 0; j < k; ++j) {
       int64_t e = idx[(int64_t)r * k + j];
       for (int32_t i = 0; i < I; ++i)
         h[i] = orc_bf16_to_f64(h_in[((int64_t)r * (1 + k) + 1 + j) * I + i]);
-      q4_matvec(L->down_qs + e * d_stride, L->down_sc + e * d_sstride, H, I, h, o);
+      q4_matvec_abs(L->down_qs + e * d_stride, L->down_sc + e * d_sstride, H, I, h, o, ao);
       double wj = w[(int64_t)r * k + j];
-      for (int32_t i = 0; i < H; ++i) acc[i] += wj * o[i];
+      for (int32_t i = 0; i < H; ++i) {
+        acc[i] += wj * o[i];
+        aacc[i] += fabs(wj) * ao[i];
+      }
     }
-    for (int32_t i = 0; i < H; ++i) y[(int64_t)r * H + i] = orc_bf16_rne(acc[i]);
+    for (int32_t i = 0; i < H; ++i) {
+      y[(int64_t)r * H + i] = orc_bf16_rne(acc[i]);
+      if (yaux) {
+        yaux[((int64_t)r * H + i) * 2 + 0] = acc[i];   /* y before rounding */
+        yaux[((int64_t)r * H + i) * 2 + 1] = aacc[i];  /* scale of its terms */
+      }
+    }
   }
-  free(h); free(o); free(acc);
+  free(h); free(o); free(ao); free(acc); free(aacc);
+}
+
+/* Elementwise orc_bf16_rne over n doubles. */
+void orc_bf16_rne_array(const double* in, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_rne(in[i]);
 }
 
 /* ------------------------------------------------------------------ block select ---- */

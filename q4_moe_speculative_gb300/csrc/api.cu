@@ -21,6 +21,19 @@ int device_sm_count() {
   return cached[dev];
 }
 
+int device_max_smem_optin() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      n = 48 * 1024;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 }  // namespace dsmoe
 
 using namespace dsmoe;
@@ -29,13 +42,13 @@ namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool q4_ok(const ds_q4& w) { return w.qs && w.sc && aligned(w.qs, 16) && aligned(w.sc, 2); }
+bool q4_ok(const ds_q4& w) { return w.qs && w.sc && aligned(w.qs, 16) && aligned(w.sc, 4); }
 
 ds_status check_layer(const ds_moe_layer* L, int32_t R) {
   if (!L) return DS_ERR_INVALID_ARG;
   if (R < 1 || R > kMaxRows) return DS_ERR_INVALID_ARG;
-  if (L->hidden < 32 || L->hidden > 16384 || L->hidden % 32) return DS_ERR_INVALID_ARG;
-  if (L->inter < 32 || L->inter > 8192 || L->inter % 32) return DS_ERR_INVALID_ARG;
+  if (L->hidden < 64 || L->hidden > 16384 || L->hidden % 64) return DS_ERR_INVALID_ARG;
+  if (L->inter < 64 || L->inter > 8192 || L->inter % 64) return DS_ERR_INVALID_ARG;
   if (L->top_k < 1 || L->top_k > kMaxTopK) return DS_ERR_INVALID_ARG;
   if (L->n_experts < L->top_k || L->n_experts > kMaxExperts) return DS_ERR_INVALID_ARG;
   if (!L->router_w || !aligned(L->router_w, 16)) return DS_ERR_INVALID_ARG;
@@ -80,7 +93,7 @@ SelDims sdims_of(const ds_select_args* a) {
 extern "C" {
 
 size_t ds_moe_workspace_size(const ds_moe_layer* layer, int32_t R) {
-  if (!layer || R < 1 || R > kMaxRows || layer->hidden < 32 || layer->inter < 32 ||
+  if (!layer || R < 1 || R > kMaxRows || layer->hidden < 64 || layer->inter < 64 ||
       layer->top_k < 1 || layer->top_k > kMaxTopK || layer->n_experts < layer->top_k ||
       layer->n_experts > kMaxExperts)
     return 0;
@@ -106,15 +119,19 @@ ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t
   const MoeDims d = dims_of(layer, R);
   const MoeLayout L = moe_layout(d);
   if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return DS_ERR_WORKSPACE;
+  // The verify rows are staged in shared memory: R * (2H + 64) bytes beside the weight ring.
+  if (gate_up_smem_bytes(d) > (size_t)device_max_smem_optin()) return DS_ERR_UNSUPPORTED;
 
   char* base = static_cast<char*>(workspace);
   MoeWorkspace ws{};
   ws.header = reinterpret_cast<uint32_t*>(base + L.header);
   ws.tile_count = reinterpret_cast<uint32_t*>(base + L.tile_count);
+  ws.part_count = reinterpret_cast<uint32_t*>(base + L.part_count);
   ws.logits = reinterpret_cast<float*>(base + L.logits);
   ws.route = reinterpret_cast<RouteInfo*>(base + L.route);
   ws.h = reinterpret_cast<uint16_t*>(base + L.h);
   ws.opart = reinterpret_cast<float*>(base + L.opart);
+  ws.part = reinterpret_cast<float*>(base + L.part);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(base, 0, L.zero_bytes, s) != cudaSuccess) return DS_ERR_CUDA;
@@ -170,6 +187,9 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
   ws.wordoff = reinterpret_cast<int32_t*>(base + L.wordoff);
   ws.cidx = caller ? cidx : reinterpret_cast<int32_t*>(base + L.cidx);
   ws.ccount = caller ? ccount : reinterpret_cast<int32_t*>(base + L.ccount);
+  ws.uidx = reinterpret_cast<int32_t*>(base + L.uidx);
+  ws.ucount = reinterpret_cast<int32_t*>(base + L.ucount);
+  ws.urows = reinterpret_cast<uint8_t*>(base + L.urows);
   ws.cscore = reinterpret_cast<float*>(base + L.cscore);
   ws.chi = reinterpret_cast<float*>(base + L.chi);
   const bool tc = !(a->flags & DS_SELECT_CANONICAL_SCORES) &&

@@ -30,21 +30,23 @@ struct MoeDims {
 };
 
 struct MoeWorkspace {
-  uint32_t* header;        // WsHeader
-  uint32_t* tile_count;    // K4 arrivals per H tile
+  uint32_t* header;        // WsHeader; words 2 and 3 are the K3 / K4 work counters
+  uint32_t* tile_count;    // K4 arrivals per 16-row tile of H
+  uint32_t* part_count;    // K3 arrivals per (expert slot, 16-row tile of I)
   float* logits;           // [R][E]
   RouteInfo* route;
   uint16_t* h;             // bf16 [R][1+k][I]
   float* opart;            // [R][1+k][H]
+  float* part;             // K3 partial sums per K part
 };
-
-// K4 processes H in tiles of this many output rows.
-constexpr int kDownTileH = 64;
 
 struct MoeLayout {
-  size_t header, tile_count, logits, route, h, opart, total, zero_bytes;
+  size_t header, tile_count, part_count, logits, route, h, opart, part, total, zero_bytes;
 };
 MoeLayout moe_layout(const MoeDims& d);
+int gate_up_kparts(int H);
+// Dynamic shared memory of the gate/up kernel for these sizes (bytes).
+size_t gate_up_smem_bytes(const MoeDims& d);
 
 cudaError_t launch_router(const MoeDims& d, const uint16_t* x, const uint16_t* router_w,
                           int32_t* topk_idx, float* topk_w, const MoeWorkspace& ws,
@@ -63,16 +65,19 @@ struct SelDims {
 
 struct SelWorkspace {
   uint32_t* header;
-  int32_t* wordoff;   // [L][R][W] exclusive prefix of admitted counts per mask word
+  int32_t* wordoff;   // [L][W] exclusive prefix of union-admitted counts per mask word
   int32_t* cidx;      // [L][R][N] (caller's array or workspace)
   int32_t* ccount;    // [L][R]
-  float* cscore;      // [L][R][N] aligned with cidx: canonical scores, or (tensor-core
+  int32_t* uidx;      // [L][N] union of the rows' admitted blocks, ascending
+  int32_t* ucount;    // [L]
+  uint8_t* urows;     // [L][N] bit r: row r admits the union entry
+  float* cscore;      // [L][R][N] by union entry: canonical scores, or (tensor-core
                       // scoring) order keys of the lower bounds of the scores
-  float* chi;         // [L][R][N] aligned with cidx: upper bounds (tensor-core scoring)
+  float* chi;         // [L][R][N] by union entry: upper bounds (tensor-core scoring)
 };
 
 struct SelLayout {
-  size_t header, wordoff, cidx, ccount, cscore, chi, total;
+  size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, chi, total;
 };
 SelLayout sel_layout(const SelDims& d, bool caller_cidx);
 bool tc_scoring_supported(const SelDims& d, const uint16_t* keys, const uint16_t* q);
@@ -88,5 +93,6 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
 
 // Cached device properties of the current device.
 int device_sm_count();
+int device_max_smem_optin();
 
 }  // namespace dsmoe

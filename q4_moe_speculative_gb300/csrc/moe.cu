@@ -6,11 +6,22 @@
 //     gate+up+SwiGLU is one kernel; BF16 rounding happens inside the producing kernels.
 //   paragraph "DSpark": the decode step is a 6-row verify and the rows share one weight
 //     stream.
+//
 // Every Q4 weight byte of the shared expert and of the union of routed experts is loaded
-// once per call (streaming loads, no reuse across CTAs needed) and applied to every row
-// that uses it. All reductions run in a fixed order that does not depend on R or on the
-// other rows, so an R-row call writes the same bytes as R one-row calls.
+// from HBM once per call and applied to every row that uses it. All reductions run in a
+// fixed order that does not depend on R or on the other rows, so an R-row call writes the
+// same bytes as R one-row calls.
+//
+// Q4 dot products (K3, K4) run on the tensor cores as mma.sync m16n8k16 (bf16 in, fp32
+// accumulate) with the weights dequantised in registers: the M dimension is 16 weight rows,
+// N = 8 is the (up to 6) verify rows, K = 16 values of one 32-value Q4 block, so each
+// block's fp16 scale is applied exactly to that block's two MMAs. Widening a 32-bit word
+// of 8 nibbles costs three shifts, four AND-ORs that put nibbles in the mantissa of the
+// bf16 number 128 + nibble, and four bf16x2 subtractions of 136 (exact q = nibble - 8).
+// Weight tiles stream through a per-warp cp.async ring in shared memory (4 stages), so no
+// register holds data in flight; units of work are taken from a counter (work stealing).
 #include <climits>
+#include <utility>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -19,8 +30,9 @@ namespace dsmoe {
 namespace {
 
 constexpr int kRouterWarps = 4;
-constexpr int kGateUpThreads = 256;
-constexpr int kDownThreads = 256;
+constexpr int kMmaWarps = 16;
+constexpr int kMmaThreads = kMmaWarps * 32;
+constexpr int kStages = 4;
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -28,88 +40,82 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// ---------------------------------------------------------------------------------
-// Activation staging for the Q4 dot products.
-//
-// A Q4 block is 32 values in 16 bytes: byte j holds value 2j (low nibble) and 2j+1
-// (high nibble). The kernels widen a 32-bit word w (values 8m..8m+7) with
-//   lo = w & 0x0F0F0F0F  -> values 8m+0, 8m+2, 8m+4, 8m+6
-//   hi = (w >> 4) & 0x0F0F0F0F -> values 8m+1, 8m+3, 8m+5, 8m+7
-// and one byte-permute per value that builds the fp32 number 128 + nibble exactly
-// (exponent byte 0x43, nibble in the top mantissa byte). The activations are therefore
-// staged in shared memory in the same order: "chunk" 2m holds the even values of word m
-// and chunk 2m+1 the odd ones, 4 floats per chunk, 8 chunks per block. Chunk c of block
-// b is stored at chunk position c ^ (b & 7), so that 8 lanes reading 8 consecutive
-// blocks with 128-bit loads touch 8 different bank groups.
-//
-// Because the weights enter as 128 + nibble = q + 136, each block's dot product is
-// corrected by 136 * (sum of the block's activations), staged next to the activations.
-// ---------------------------------------------------------------------------------
-__device__ __forceinline__ int stage_pos(int k) {
-  const int blk = k >> 5, w = k & 31;
-  const int m = w >> 3, j = (w >> 1) & 3, p = w & 1;
-  const int c = 2 * m + p;
-  return (blk << 5) + ((c ^ (blk & 7)) << 2) + j;
+// ---------------------------------------------------------------- PTX helpers --------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Stages bf16 row `src` (K values) as fp32 into dst (K floats) and 136 * block sums into
-// csum (K / 32 floats). Called by all threads of the CTA; caller synchronises.
-__device__ __forceinline__ void stage_row(const uint16_t* __restrict__ src, int K, float* dst,
-                                          float* csum, int tid, int nthreads) {
-  const uint32_t* s2 = reinterpret_cast<const uint32_t*>(src);
-  for (int i = tid; i < K / 2; i += nthreads) {
-    const uint32_t w = s2[i];
-    dst[stage_pos(2 * i)] = bf16_lo(w);
-    dst[stage_pos(2 * i + 1)] = bf16_hi(w);
-  }
-  for (int blk = tid; blk < K / 32; blk += nthreads) {
-    const uint4* p = reinterpret_cast<const uint4*>(src + blk * 32);
-    float s = 0.0f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint4 v = p[c];
-      s = __fadd_rn(s, bf16_lo(v.x)); s = __fadd_rn(s, bf16_hi(v.x));
-      s = __fadd_rn(s, bf16_lo(v.y)); s = __fadd_rn(s, bf16_hi(v.y));
-      s = __fadd_rn(s, bf16_lo(v.z)); s = __fadd_rn(s, bf16_hi(v.z));
-      s = __fadd_rn(s, bf16_lo(v.w)); s = __fadd_rn(s, bf16_hi(v.w));
-    }
-    csum[blk] = __fmul_rn(136.0f, s);
-  }
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// 16-byte async copy global -> shared; zero-fill (no global read) when !valid.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// 8 nibbles of w -> 8 floats (128 + nibble), in staged chunk order (even values, odd).
-__device__ __forceinline__ void widen8(uint32_t w, float f[8]) {
-  const uint32_t lo = w & 0x0F0F0F0Fu;
-  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
-  const uint32_t magic = 0x43000000u;
-  f[0] = __uint_as_float(__byte_perm(lo, magic, 0x7044));
-  f[1] = __uint_as_float(__byte_perm(lo, magic, 0x7144));
-  f[2] = __uint_as_float(__byte_perm(lo, magic, 0x7244));
-  f[3] = __uint_as_float(__byte_perm(lo, magic, 0x7344));
-  f[4] = __uint_as_float(__byte_perm(hi, magic, 0x7044));
-  f[5] = __uint_as_float(__byte_perm(hi, magic, 0x7144));
-  f[6] = __uint_as_float(__byte_perm(hi, magic, 0x7244));
-  f[7] = __uint_as_float(__byte_perm(hi, magic, 0x7344));
+// bf16 pair (q_lo, q_hi) of the nibbles at bits 0-3 and 16-19 of w: (w & 0x000F000F) |
+// 0x43004300 is the bf16 pair (128 + n_lo, 128 + n_hi); minus 136 gives n - 8 exactly.
+__device__ __forceinline__ uint32_t q4_pair(uint32_t w) {
+  uint32_t p, d;
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(p) : "r"(w));
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(p), "r"(0x43084308u));
+  return d;
 }
 
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
-  return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
+// D = A (16x16 bf16) * B (16x8 bf16) + C, fp32.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1,
+                                         const float (&c)[4]) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+        "f"(c[2]), "f"(c[3]));
 }
 
-// acc += dot(f[0..7], staged chunks 2m, 2m+1 of block at xb with swizzle sw)
-__device__ __forceinline__ float dot8(const float f[8], const float* xb, int m, int sw,
-                                      float acc) {
-  const float4 a = *reinterpret_cast<const float4*>(xb + (((2 * m) ^ sw) << 2));
-  const float4 b = *reinterpret_cast<const float4*>(xb + (((2 * m + 1) ^ sw) << 2));
-  acc = __fmaf_rn(f[0], a.x, acc);
-  acc = __fmaf_rn(f[1], a.y, acc);
-  acc = __fmaf_rn(f[2], a.z, acc);
-  acc = __fmaf_rn(f[3], a.w, acc);
-  acc = __fmaf_rn(f[4], b.x, acc);
-  acc = __fmaf_rn(f[5], b.y, acc);
-  acc = __fmaf_rn(f[6], b.z, acc);
-  acc = __fmaf_rn(f[7], b.w, acc);
-  return acc;
+// One Q4 block for the 16 rows of a tile: w_lo / w_hi are word q (values 8q..8q+7 of the
+// block) of rows g and g+8 of this lane (g = lane/4, q = lane%4); X holds the matching
+// activations of verify row g as bf16 pairs (v0,v4),(v1,v5),(v2,v6),(v3,v7). The block's
+// two MMAs use the K order (8q+0, 8q+4 | 8q+1, 8q+5) and (8q+2, 8q+6 | 8q+3, 8q+7), a
+// permutation within the block shared by A and B. Returns the raw block dot products
+// D[row g / g+8][col 2q, 2q+1] (before the block scale).
+__device__ __forceinline__ void q4_block_mma(uint32_t w_lo, uint32_t w_hi, const uint4& X,
+                                             float (&d)[4]) {
+  const float z[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint32_t p0 = q4_pair(w_lo), p1 = q4_pair(w_lo >> 4);
+  const uint32_t r0 = q4_pair(w_hi), r1 = q4_pair(w_hi >> 4);
+  mma16816(d, p0, r0, p1, r1, X.x, X.y, z);
+  const uint32_t p2 = q4_pair(w_lo >> 8), p3 = q4_pair(w_lo >> 12);
+  const uint32_t r2 = q4_pair(w_hi >> 8), r3 = q4_pair(w_hi >> 12);
+  mma16816(d, p2, r2, p3, r3, X.z, X.w, d);
+}
+
+// Natural-order bf16 values v0..v7 (as 4 packed words) -> MMA pair order.
+__device__ __forceinline__ uint4 pair_order(const uint4& v) {
+  return make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
+                    __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
+}
+
+// Four packed fp16 scales (blocks j = 0..3) -> fp32.
+__device__ __forceinline__ void widen_scales(uint2 s, float (&f)[4]) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&s.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&s.y));
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
 }
 
 // ---------------------------------------------------------------------------------
@@ -122,7 +128,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     k1_router(const uint16_t* __restrict__ x, int R, int H, const uint16_t* __restrict__ wr,
               int E, int k, float* __restrict__ logits, int32_t* __restrict__ topk_idx,
               float* __restrict__ topk_w, RouteInfo* __restrict__ route, WsHeader* hdr) {
-  extern __shared__ float smem[];  // x as fp32 [R][H]; then sigmoid scores [R][E]
+  extern __shared__ float smem_f[];  // x as fp32 [R][H]; then sigmoid scores [R][E]
   __shared__ int s_is_last;
   __shared__ int32_t sel_e[kMaxRows][kMaxTopK];
   __shared__ float sel_s[kMaxRows][kMaxTopK];
@@ -132,13 +138,19 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   __shared__ int8_t u_slot[kMaxUnion][8];
   __shared__ int s_nunion;
 
+  pdl_trigger();   // the gate/up kernel may launch now; it waits for this grid's results
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   {
-    const uint32_t* x2 = reinterpret_cast<const uint32_t*>(x);
-    for (int i = tid; i < R * H / 2; i += blockDim.x) {
-      const uint32_t w = x2[i];
-      smem[2 * i] = bf16_lo(w);
-      smem[2 * i + 1] = bf16_hi(w);
+    // 8 values per 16-byte load; loads of an unrolled batch are independent, so the CTA
+    // has many in flight instead of one load -> store round trip at a time.
+    const uint4* x8 = reinterpret_cast<const uint4*>(x);
+    const int n8 = R * H / 8;
+#pragma unroll 4
+    for (int i = tid; i < n8; i += blockDim.x) {
+      const uint4 v = __ldg(x8 + i);
+      float4* d = reinterpret_cast<float4*>(smem_f + 8 * i);
+      d[0] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+      d[1] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
     }
   }
   __syncthreads();
@@ -149,21 +161,33 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.0f;
     const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)e * H);
-    for (int c = lane; c < H / 8; c += 32) {
-      const uint4 wv = __ldcs(wrow + c);
-      const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
-                           bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+    const int nc = H / 8;
+    for (int c0 = 0; c0 < nc; c0 += 4 * 32) {
+      uint4 wv[4];
 #pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
-        if (r < R) {
-          const float4 a = *reinterpret_cast<const float4*>(smem + r * H + c * 8);
-          const float4 b = *reinterpret_cast<const float4*>(smem + r * H + c * 8 + 4);
-          float t = acc[r];
-          t = __fmaf_rn(wf[0], a.x, t); t = __fmaf_rn(wf[1], a.y, t);
-          t = __fmaf_rn(wf[2], a.z, t); t = __fmaf_rn(wf[3], a.w, t);
-          t = __fmaf_rn(wf[4], b.x, t); t = __fmaf_rn(wf[5], b.y, t);
-          t = __fmaf_rn(wf[6], b.z, t); t = __fmaf_rn(wf[7], b.w, t);
-          acc[r] = t;
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + u * 32 + lane;
+        wv[u] = c < nc ? __ldcs(wrow + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c >= nc) continue;
+        const float wf[8] = {bf16_lo(wv[u].x), bf16_hi(wv[u].x), bf16_lo(wv[u].y),
+                             bf16_hi(wv[u].y), bf16_lo(wv[u].z), bf16_hi(wv[u].z),
+                             bf16_lo(wv[u].w), bf16_hi(wv[u].w)};
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) {
+          if (r < R) {
+            const float4 a = *reinterpret_cast<const float4*>(smem_f + r * H + c * 8);
+            const float4 b = *reinterpret_cast<const float4*>(smem_f + r * H + c * 8 + 4);
+            float t = acc[r];
+            t = __fmaf_rn(wf[0], a.x, t); t = __fmaf_rn(wf[1], a.y, t);
+            t = __fmaf_rn(wf[2], a.z, t); t = __fmaf_rn(wf[3], a.w, t);
+            t = __fmaf_rn(wf[4], b.x, t); t = __fmaf_rn(wf[5], b.y, t);
+            t = __fmaf_rn(wf[6], b.z, t); t = __fmaf_rn(wf[7], b.w, t);
+            acc[r] = t;
+          }
         }
       }
     }
@@ -187,7 +211,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   if (!s_is_last) return;
   __threadfence();
 
-  float* s_sm = smem;  // [R][E] sigmoid scores
+  float* s_sm = smem_f;  // [R][E] sigmoid scores
   for (int i = tid; i < R * E; i += blockDim.x) {
     const float z = __ldcg(logits + i);
     s_sm[i] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
@@ -277,134 +301,249 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 }
 
 // ---------------------------------------------------------------------------------
-// K3: gate + up + SwiGLU for the shared expert (all rows) and every routed expert of the
-// union (its rows). Work unit = (expert slot u, 8 consecutive output rows i), one warp
-// per row; lane l reads blocks l, l+32, l+64, l+96 of the gate row and of the up row
-// (128-bit streaming loads, each byte once) and applies them to each of the expert's
-// rows. h = bf16_rne(silu(g) * u) is written by the producing warp.
+// K3: gate + up + SwiGLU. Unit of work = (expert slot u, 16 rows of I, one of KP parts of
+// K); expert slot 0 is the shared expert (all rows), slot u >= 1 the u-th expert of the
+// union (its rows). A warp streams its unit's gate and up rows in tiles of 4 Q4 blocks
+// through its cp.async ring and accumulates D[16 rows][8 cols] with mma.sync; the
+// activations sit in shared memory as bf16 in MMA pair order (staged once per CTA).
+// The last of the KP parts to arrive (atomic count) adds the parts in a fixed order and
+// writes h = bf16_rne(silu(g) * u) for the expert's rows.
 // ---------------------------------------------------------------------------------
+struct GuStage {
+  uint32_t a[2][4][16][4];   // [gate/up][block j][row][word]
+  uint32_t s[2][16][2];      // [gate/up][row][4 fp16 scales]
+};
+
 struct GateUpArgs {
   const uint16_t* x;
   int R, H, I, k;
   Q4Ptr gate, up, sh_gate, sh_up;
   const RouteInfo* route;
   uint16_t* h;
+  float* part;               // [(1+R*k) * (I/16) * KP][32 lanes][8]
+  uint32_t* part_count;      // [(1+R*k) * (I/16)]
+  uint32_t* unit_counter;
 };
 
-__global__ void __launch_bounds__(kGateUpThreads, 2) k3_gate_up(GateUpArgs a) {
-  extern __shared__ float smem[];
-  const int R = a.R, H = a.H, I = a.I;
-  const int nb = H >> 5;
-  float* xs = smem;            // [R][H] staged activations
-  float* cs = smem + R * H;    // [R][nb] 136 * block sums
+
+__global__ void __launch_bounds__(kMmaThreads, 1) k3_gate_up(GateUpArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int R = a.R, H = a.H, I = a.I, k = a.k;
+  const int nb = H >> 5;                        // Q4 blocks per row
+  const int T = (nb + 3) >> 2;                  // tiles of 4 blocks
+  const int TP = (T + 3) >> 2;                  // tiles per K part
+  const int KP = (T + TP - 1) / TP;             // K parts (<= 4)
+  const int RT = I >> 4;                        // 16-row tiles
+  const int xstride = H * 2 + 64;               // bytes per staged activation row
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, q = lane & 3;
 
-  for (int r = 0; r < R; ++r)
-    stage_row(a.x + (size_t)r * H, H, xs + r * H, cs + r * nb, tid, blockDim.x);
+  uint8_t* xs = smem;
+  GuStage* stages = reinterpret_cast<GuStage*>(smem + ((R * xstride + 127) & ~127)) + warp * kStages;
+  int* wdesc = reinterpret_cast<int*>(reinterpret_cast<GuStage*>(smem + ((R * xstride + 127) & ~127)) +
+                                      kMmaWarps * kStages) + warp * (2 * kStages);
+
+  // Activations -> shared memory, bf16 in MMA pair order (independent of the router).
+#pragma unroll 4
+  for (int i = tid; i < R * (H >> 3); i += blockDim.x) {
+    const int r = i / (H >> 3), grp = i - r * (H >> 3);
+    const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)r * H + grp * 8);
+    *reinterpret_cast<uint4*>(xs + r * xstride + (grp >> 2) * 64 + (grp & 3) * 16) = pair_order(v);
+  }
   __syncthreads();
+  pdl_wait();   // the route produced by the router grid is visible from here on
 
-  const int n_union = a.route->n_union;
-  const int tiles = (I + 7) / 8;
-  const int n_units = (1 + n_union) * tiles;
-  const size_t row_qs = (size_t)H / 2, row_sc = (size_t)H / 32;
+  const RouteInfo* rt_info = a.route;
+  const int n_union = rt_info->n_union;
+  const int n_units = (1 + n_union) * RT * KP;
+  const size_t row_qs = (size_t)H / 2, row_sc = (size_t)nb;
 
-  for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-    const int u = unit / tiles;
-    const int i = (unit - u * tiles) * 8 + warp;
-    if (i >= I) continue;
-    uint32_t rowmask;
-    const uint8_t *gq, *uq;
-    const uint16_t *gs, *us;
-    if (u == 0) {
-      rowmask = (1u << R) - 1u;
-      gq = a.sh_gate.qs + (size_t)i * row_qs;
-      uq = a.sh_up.qs + (size_t)i * row_qs;
-      gs = a.sh_gate.sc + (size_t)i * row_sc;
-      us = a.sh_up.sc + (size_t)i * row_sc;
-    } else {
-      const size_t e = (size_t)a.route->expert[u - 1];
-      rowmask = a.route->rowmask[u - 1];
-      const size_t row = e * I + i;
-      gq = a.gate.qs + row * row_qs;
-      uq = a.up.qs + row * row_qs;
-      gs = a.gate.sc + row * row_sc;
-      us = a.up.sc + row * row_sc;
+  // Issue cursor (warp-uniform). A unit is decoded once, when the warp takes it; each
+  // further tile only advances the source pointers.
+  int iu = -1, it = 0, itiles = 0, iblk = 0;
+  bool exhausted = false;
+  const uint8_t *igq = nullptr, *iuq = nullptr;
+  const uint16_t *igs = nullptr, *ius = nullptr;
+
+  auto issue = [&](int stage) {
+    int unit = -1, tile = 0;
+    if (!exhausted && (iu < 0 || it >= itiles)) {
+      int nu = 0;
+      if (lane == 0) nu = (int)atomicAdd(a.unit_counter, 1u);
+      nu = __shfl_sync(0xffffffffu, nu, 0);
+      if (nu >= n_units) {
+        exhausted = true;
+      } else {
+        iu = nu;
+        it = 0;
+        const int u = nu / (RT * KP);
+        const int rem = nu - u * RT * KP;
+        const int rti = rem / KP, kp = rem - rti * KP;
+        itiles = min(TP, T - kp * TP);
+        iblk = kp * TP * 4;
+        const size_t row0 = (size_t)rti * 16;
+        if (u == 0) {
+          igq = a.sh_gate.qs + row0 * row_qs; iuq = a.sh_up.qs + row0 * row_qs;
+          igs = a.sh_gate.sc + row0 * row_sc; ius = a.sh_up.sc + row0 * row_sc;
+        } else {
+          const size_t e = (size_t)rt_info->expert[u - 1];
+          igq = a.gate.qs + (e * I + row0) * row_qs; iuq = a.up.qs + (e * I + row0) * row_qs;
+          igs = a.gate.sc + (e * I + row0) * row_sc; ius = a.up.sc + (e * I + row0) * row_sc;
+        }
+      }
     }
-
-    float ga[kMaxRows], ua[kMaxRows];
+    if (!exhausted) {
+      unit = iu;
+      tile = it++;
+    }
+    if (lane == 0) {
+      wdesc[2 * stage] = unit;
+      wdesc[2 * stage + 1] = tile;
+    }
+    if (unit >= 0) {
+      const int blk0 = iblk + tile * 4;
+      GuStage& S = stages[stage];
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) { ga[r] = 0.0f; ua[r] = 0.0f; }
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int pp = lane + 32 * h2;
+        const int row = pp & 15, j = pp >> 4;
+        const bool v = blk0 + j < nb;
+        const size_t off = row * row_qs + (size_t)(blk0 + j) * 16;
+        cp_async16(&S.a[0][j][row][0], v ? igq + off : igq, v);
+        cp_async16(&S.a[1][j][row][0], v ? iuq + off : iuq, v);
+      }
+      {
+        const int row = lane >> 1, hf = lane & 1;
+        const bool v = blk0 + 2 * hf < nb;
+        const size_t off = row * row_sc + blk0 + 2 * hf;
+        cp_async4(&S.s[0][row][hf], v ? igs + off : igs, v);
+        cp_async4(&S.s[1][row][hf], v ? ius + off : ius, v);
+      }
+    }
+    cp_async_commit();
+  };
 
-    for (int cb = 0; cb < nb; cb += 128) {
-      uint4 qg[4], qu[4];
+  float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) issue(s);
+
+  // Compute cursor: the unit of the tile being computed, decoded once per unit.
+  int cu = -1, u = 0, rti = 0, kp = 0, tiles = 0;
+  uint32_t rowmask = 0;
+  bool member = false;
+  for (int t = 0;; ++t) {
+    issue((t + kStages - 1) % kStages);
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const int stage = t % kStages;
+    const int unit = wdesc[2 * stage], tile = wdesc[2 * stage + 1];
+    if (unit < 0) break;
+    if (unit != cu) {
+      cu = unit;
+      u = unit / (RT * KP);
+      const int rem = unit - u * RT * KP;
+      rti = rem / KP;
+      kp = rem - rti * KP;
+      tiles = min(TP, T - kp * TP);
+      rowmask = (u == 0) ? ((1u << R) - 1u) : rt_info->rowmask[u - 1];
+      member = (g < R) && ((rowmask >> g) & 1u);
+    }
+    if (tile == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { ag[i] = 0.f; au[i] = 0.f; }
+    }
+    const GuStage& S = stages[stage];
+    const int blk0 = (kp * TP + tile) * 4;
+    // fp16 scales of this lane's rows g and g+8 for the tile's 4 blocks, widened once
+    const uint2 sgv0 = *reinterpret_cast<const uint2*>(&S.s[0][g][0]);
+    const uint2 sgv8 = *reinterpret_cast<const uint2*>(&S.s[0][g + 8][0]);
+    const uint2 suv0 = *reinterpret_cast<const uint2*>(&S.s[1][g][0]);
+    const uint2 suv8 = *reinterpret_cast<const uint2*>(&S.s[1][g + 8][0]);
+    float sg0[4], sg8[4], su0[4], su8[4];
+    widen_scales(sgv0, sg0); widen_scales(sgv8, sg8);
+    widen_scales(suv0, su0); widen_scales(suv8, su8);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int blk = blk0 + j;
+      if (blk < nb) {
+        const uint4 X = member ? *reinterpret_cast<const uint4*>(xs + g * xstride + blk * 64 + q * 16)
+                               : make_uint4(0, 0, 0, 0);
+        float d[4];
+        q4_block_mma(S.a[0][j][g][q], S.a[0][j][g + 8][q], X, d);
+        ag[0] = __fmaf_rn(sg0[j], d[0], ag[0]); ag[1] = __fmaf_rn(sg0[j], d[1], ag[1]);
+        ag[2] = __fmaf_rn(sg8[j], d[2], ag[2]); ag[3] = __fmaf_rn(sg8[j], d[3], ag[3]);
+        q4_block_mma(S.a[1][j][g][q], S.a[1][j][g + 8][q], X, d);
+        au[0] = __fmaf_rn(su0[j], d[0], au[0]); au[1] = __fmaf_rn(su0[j], d[1], au[1]);
+        au[2] = __fmaf_rn(su8[j], d[2], au[2]); au[3] = __fmaf_rn(su8[j], d[3], au[3]);
+      }
+    }
+    __syncwarp();
+
+    if (tile == tiles - 1) {
+      // All K parts of (u, row tile) in a fixed order, then the SwiGLU epilogue.
       float sg[4], su[4];
+      bool last = true;
+      const int ut = u * RT + rti;
+      if (KP > 1) {
+        float* mine = a.part + ((size_t)ut * KP + kp) * 256 + lane * 8;
+        *reinterpret_cast<float4*>(mine) = make_float4(ag[0], ag[1], ag[2], ag[3]);
+        *reinterpret_cast<float4*>(mine + 4) = make_float4(au[0], au[1], au[2], au[3]);
+        __threadfence();
+        __syncwarp();
+        unsigned prev = 0;
+        if (lane == 0) prev = atomicAdd(a.part_count + ut, 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        last = (prev == (unsigned)(KP - 1));
+        if (last) {
+          __threadfence();
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int blk = cb + 32 * t + lane;
-        if (blk < nb) {
-          qg[t] = ldg_stream(gq + (size_t)blk * 16);
-          qu[t] = ldg_stream(uq + (size_t)blk * 16);
-          sg[t] = f16_bits_to_f32(__ldcs(gs + blk));
-          su[t] = f16_bits_to_f32(__ldcs(us + blk));
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int blk = cb + 32 * t + lane;
-        if (blk < nb) {
-          const int sw = blk & 7;
-          float bg[kMaxRows], bu[kMaxRows];
-#pragma unroll
-          for (int r = 0; r < kMaxRows; ++r) { bg[r] = 0.0f; bu[r] = 0.0f; }
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            float fg[8], fu[8];
-            widen8(word_of(qg[t], m), fg);
-            widen8(word_of(qu[t], m), fu);
-#pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) {
-              if (rowmask & (1u << r)) {
-                const float* xb = xs + r * H + blk * 32;
-                bg[r] = dot8(fg, xb, m, sw, bg[r]);
-                bu[r] = dot8(fu, xb, m, sw, bu[r]);
-              }
-            }
-          }
-#pragma unroll
-          for (int r = 0; r < kMaxRows; ++r) {
-            if (rowmask & (1u << r)) {
-              const float c = cs[r * nb + blk];
-              ga[r] = __fmaf_rn(sg[t], __fsub_rn(bg[r], c), ga[r]);
-              ua[r] = __fmaf_rn(su[t], __fsub_rn(bu[r], c), ua[r]);
-            }
+          for (int i = 0; i < 4; ++i) { sg[i] = 0.f; su[i] = 0.f; }
+          for (int p = 0; p < KP; ++p) {
+            const float* src = a.part + ((size_t)ut * KP + p) * 256 + lane * 8;
+            const float4 g4 = __ldcg(reinterpret_cast<const float4*>(src));
+            const float4 u4 = __ldcg(reinterpret_cast<const float4*>(src + 4));
+            sg[0] = __fadd_rn(sg[0], g4.x); sg[1] = __fadd_rn(sg[1], g4.y);
+            sg[2] = __fadd_rn(sg[2], g4.z); sg[3] = __fadd_rn(sg[3], g4.w);
+            su[0] = __fadd_rn(su[0], u4.x); su[1] = __fadd_rn(su[1], u4.y);
+            su[2] = __fadd_rn(su[2], u4.z); su[3] = __fadd_rn(su[3], u4.w);
           }
         }
-      }
-    }
-
+      } else {
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
-      if (rowmask & (1u << r)) {
-        const float g = warp_sum(ga[r]);
-        const float uu = warp_sum(ua[r]);
-        if (lane == r) {
-          const int slot = (u == 0) ? 0 : a.route->slot[u - 1][r];
-          const float silu = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
-          a.h[((size_t)r * (1 + a.k) + slot) * I + i] = f32_to_bf16_rne(__fmul_rn(silu, uu));
+        for (int i = 0; i < 4; ++i) { sg[i] = ag[i]; su[i] = au[i]; }
+      }
+      if (last) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 2 * q + (e & 1);
+          const int row = rti * 16 + g + ((e & 2) ? 8 : 0);
+          if (c < R && ((rowmask >> c) & 1u)) {
+            const int slot = (u == 0) ? 0 : rt_info->slot[u - 1][c];
+            const float gv = sg[e];
+            const float silu = __fdiv_rn(gv, __fadd_rn(1.0f, expf(-gv)));
+            a.h[((size_t)c * (1 + k) + slot) * I + row] = f32_to_bf16_rne(__fmul_rn(silu, su[e]));
+          }
         }
       }
     }
   }
+  cp_async_wait<0>();
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------------
-// K4: down projection + combine. Work unit = (expert slot u, tile of 64 output rows of
-// H). The CTA stages h of the expert's rows (fp32, same layout as K3's activations);
-// each warp computes 8 output rows, 4 at a time with 8 lanes per row (lane j of a group
-// reads blocks j, j+8, j+16, j+24 of its row), and writes fp32 partials per (row, slot).
-// The last unit to finish a tile (arrival count, no waiting) forms
+// K4: down projection + combine. Unit of work = (expert slot u, 16 rows of H), all of K
+// = I. The warp streams the down rows and the expert's h (its rows' slots, in the same
+// ring) and accumulates D[16 rows][8 cols] with mma.sync; it writes fp32 partials per
+// (row, slot). The last unit to finish a 16-row tile (arrival count, no waiting) forms
 //   y = bf16_rne(o_shared + sum_j w_j o_j)   in rank order j.
 // ---------------------------------------------------------------------------------
+struct DnStage {
+  uint32_t a[4][16][4];      // [block j][row][word]
+  uint32_t s[16][2];         // [row][4 fp16 scales]
+  uint4 b[4][32];            // [block j][lane]: h values 8q..8q+7 of verify row g
+};
+
 struct DownArgs {
   const uint16_t* h;
   int R, H, I, k;
@@ -412,149 +551,165 @@ struct DownArgs {
   const RouteInfo* route;
   const float* topk_w;
   float* opart;
-  uint32_t* tile_count;
+  uint32_t* tile_count;      // [H/16]
+  uint32_t* unit_counter;
   uint16_t* y;
 };
 
-__global__ void __launch_bounds__(kDownThreads) k4_down(DownArgs a) {
-  extern __shared__ float smem[];
-  __shared__ int s_last;
+__global__ void __launch_bounds__(kMmaThreads, 1) k4_down(DownArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
   const int R = a.R, H = a.H, I = a.I, k = a.k;
   const int nb = I >> 5;
-  float* hs = smem;            // [R][I]
-  float* cs = smem + R * I;    // [R][nb]
+  const int T = (nb + 3) >> 2;
+  const int RT = H >> 4;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int grp = lane >> 3, gl = lane & 7;
+  const int g = lane >> 2, q = lane & 3;
+  DnStage* stages = reinterpret_cast<DnStage*>(smem) + warp * kStages;
+  int* wdesc = reinterpret_cast<int*>(reinterpret_cast<DnStage*>(smem) + kMmaWarps * kStages) +
+               warp * (2 * kStages);
 
-  const int n_exp = 1 + a.route->n_union;
-  const int tiles = (H + kDownTileH - 1) / kDownTileH;
-  const int n_units = n_exp * tiles;
-  const int beg = (int)(((long long)blockIdx.x * n_units) / gridDim.x);
-  const int end = (int)(((long long)(blockIdx.x + 1) * n_units) / gridDim.x);
-  const size_t row_qs = (size_t)I / 2, row_sc = (size_t)I / 32;
+  pdl_wait();   // h and the route are complete from here on
+  const RouteInfo* rt_info = a.route;
+  const int n_exp = 1 + rt_info->n_union;
+  const int n_units = n_exp * RT;
+  const size_t row_qs = (size_t)I / 2, row_sc = (size_t)nb;
 
-  int staged = -1;
-  uint32_t rowmask = 0;
-  int slot[kMaxRows];
-  for (int unit = beg; unit < end; ++unit) {
-    const int u = unit / tiles;
-    const int tile = unit - u * tiles;
-    if (u != staged) {
-      __syncthreads();
-      if (u == 0) {
-        rowmask = (1u << R) - 1u;
-#pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) slot[r] = 0;
+  int iu = -1, it = 0;
+  bool exhausted = false;
+  const uint8_t* idq = nullptr;
+  const uint16_t* ids = nullptr;
+  const uint16_t* ihrow = nullptr;
+  bool imember = false;
+  auto issue = [&](int stage) {
+    int unit = -1, tile = 0;
+    if (!exhausted && (iu < 0 || it >= T)) {
+      int nu = 0;
+      if (lane == 0) nu = (int)atomicAdd(a.unit_counter, 1u);
+      nu = __shfl_sync(0xffffffffu, nu, 0);
+      if (nu >= n_units) {
+        exhausted = true;
       } else {
-        rowmask = a.route->rowmask[u - 1];
-#pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) slot[r] = a.route->slot[u - 1][r];
+        iu = nu;
+        it = 0;
+        const int u = nu / RT, rti = nu - u * RT;
+        const size_t row0 = (size_t)rti * 16;
+        uint32_t rowmask;
+        int slot_g = 0;
+        if (u == 0) {
+          idq = a.sh_down.qs + row0 * row_qs;
+          ids = a.sh_down.sc + row0 * row_sc;
+          rowmask = (1u << R) - 1u;
+        } else {
+          const size_t e = (size_t)rt_info->expert[u - 1];
+          idq = a.down.qs + (e * H + row0) * row_qs;
+          ids = a.down.sc + (e * H + row0) * row_sc;
+          rowmask = rt_info->rowmask[u - 1];
+          slot_g = rt_info->slot[u - 1][g];
+        }
+        imember = (g < R) && ((rowmask >> g) & 1u);
+        ihrow = a.h + ((size_t)g * (1 + k) + (imember ? slot_g : 0)) * I;
       }
-      for (int r = 0; r < R; ++r)
-        if (rowmask & (1u << r))
-          stage_row(a.h + ((size_t)r * (1 + k) + slot[r]) * I, I, hs + r * I, cs + r * nb,
-                    tid, blockDim.x);
-      __syncthreads();
-      staged = u;
     }
-    const uint8_t* dq;
-    const uint16_t* dsc;
-    if (u == 0) {
-      dq = a.sh_down.qs;
-      dsc = a.sh_down.sc;
-    } else {
-      const size_t e = (size_t)a.route->expert[u - 1];
-      dq = a.down.qs + e * H * row_qs;
-      dsc = a.down.sc + e * H * row_sc;
+    if (!exhausted) {
+      unit = iu;
+      tile = it++;
     }
-    const int hr0 = tile * kDownTileH + warp * 8;
+    if (lane == 0) {
+      wdesc[2 * stage] = unit;
+      wdesc[2 * stage + 1] = tile;
+    }
+    if (unit >= 0) {
+      const int blk0 = tile * 4;
+      DnStage& S = stages[stage];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int pp = lane + 32 * h2;
+        const int row = pp & 15, j = pp >> 4;
+        const bool v = blk0 + j < nb;
+        cp_async16(&S.a[j][row][0], v ? idq + row * row_qs + (size_t)(blk0 + j) * 16 : idq, v);
+      }
+      {
+        const int row = lane >> 1, hf = lane & 1;
+        const bool v = blk0 + 2 * hf < nb;
+        cp_async4(&S.s[row][hf], v ? ids + row * row_sc + blk0 + 2 * hf : ids, v);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool v = imember && (blk0 + j < nb);
+        cp_async16(&S.b[j][lane], v ? ihrow + (blk0 + j) * 32 + q * 8 : a.h, v);
+      }
+    }
+    cp_async_commit();
+  };
 
-    float acc[2][kMaxRows];
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int s = 0; s < 2; ++s)
-#pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) acc[s][r] = 0.0f;
+  for (int s = 0; s < kStages - 1; ++s) issue(s);
 
-    for (int cb = 0; cb < nb; cb += 32) {
-      uint4 q[2][4];
-      float sc[2][4];
+  int cu = -1, u = 0, rti = 0;
+  for (int t = 0;; ++t) {
+    issue((t + kStages - 1) % kStages);
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const int stage = t % kStages;
+    const int unit = wdesc[2 * stage], tile = wdesc[2 * stage + 1];
+    if (unit < 0) break;
+    if (unit != cu) {
+      cu = unit;
+      u = unit / RT;
+      rti = unit - u * RT;
+    }
+    if (tile == 0) {
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        const int hr = hr0 + 4 * s + grp;
+      for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+    }
+    const DnStage& S = stages[stage];
+    const int blk0 = tile * 4;
+    float s0f[4], s8f[4];
+    widen_scales(*reinterpret_cast<const uint2*>(&S.s[g][0]), s0f);
+    widen_scales(*reinterpret_cast<const uint2*>(&S.s[g + 8][0]), s8f);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int blk = cb + gl + 8 * t;
-          if (hr < H && blk < nb) {
-            q[s][t] = ldg_stream(dq + (size_t)hr * row_qs + (size_t)blk * 16);
-            sc[s][t] = f16_bits_to_f32(__ldcs(dsc + (size_t)hr * row_sc + blk));
-          }
+    for (int j = 0; j < 4; ++j) {
+      if (blk0 + j < nb) {
+        const uint4 X = pair_order(S.b[j][lane]);
+        float d[4];
+        q4_block_mma(S.a[j][g][q], S.a[j][g + 8][q], X, d);
+        acc[0] = __fmaf_rn(s0f[j], d[0], acc[0]); acc[1] = __fmaf_rn(s0f[j], d[1], acc[1]);
+        acc[2] = __fmaf_rn(s8f[j], d[2], acc[2]); acc[3] = __fmaf_rn(s8f[j], d[3], acc[3]);
+      }
+    }
+    __syncwarp();
+
+    if (tile == T - 1) {
+      const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : rt_info->rowmask[u - 1];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 2 * q + (e & 1);
+        const int row = rti * 16 + g + ((e & 2) ? 8 : 0);
+        if (c < R && ((rowmask >> c) & 1u)) {
+          const int slot = (u == 0) ? 0 : rt_info->slot[u - 1][c];
+          a.opart[((size_t)c * (1 + k) + slot) * H + row] = acc[e];
         }
       }
-#pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        const int hr = hr0 + 4 * s + grp;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int blk = cb + gl + 8 * t;
-          if (hr < H && blk < nb) {
-            const int sw = blk & 7;
-            float b[kMaxRows];
-#pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) b[r] = 0.0f;
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              float f[8];
-              widen8(word_of(q[s][t], m), f);
-#pragma unroll
-              for (int r = 0; r < kMaxRows; ++r)
-                if (rowmask & (1u << r)) b[r] = dot8(f, hs + r * I + blk * 32, m, sw, b[r]);
-            }
-#pragma unroll
-            for (int r = 0; r < kMaxRows; ++r)
-              if (rowmask & (1u << r))
-                acc[s][r] = __fmaf_rn(sc[s][t], __fsub_rn(b[r], cs[r * nb + blk]), acc[s][r]);
-          }
-        }
-      }
-    }
-
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      const int hr = hr0 + 4 * s + grp;
-#pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
-        if (rowmask & (1u << r)) {
-          float v = acc[s][r];
-          v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 4));
-          v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 2));
-          v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 1));
-          if (gl == 0 && hr < H) a.opart[((size_t)r * (1 + k) + slot[r]) * H + hr] = v;
-        }
-      }
-    }
-
-    // Tile arrival; the last expert unit of this tile combines it.
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      const unsigned prev = atomicAdd(&a.tile_count[tile], 1u);
-      s_last = (prev == (unsigned)(n_exp - 1));
-    }
-    __syncthreads();
-    if (s_last) {
       __threadfence();
-      for (int idx = tid; idx < R * kDownTileH; idx += blockDim.x) {
-        const int r = idx / kDownTileH;
-        const int hr = tile * kDownTileH + (idx - r * kDownTileH);
-        if (hr >= H) continue;
-        const float* orow = a.opart + (size_t)r * (1 + k) * H + hr;
-        float y = __ldcg(orow);
-        for (int j = 0; j < k; ++j)
-          y = __fmaf_rn(a.topk_w[r * k + j], __ldcg(orow + (size_t)(1 + j) * H), y);
-        a.y[(size_t)r * H + hr] = f32_to_bf16_rne(y);
+      __syncwarp();
+      unsigned prev = 0;
+      if (lane == 0) prev = atomicAdd(a.tile_count + rti, 1u);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev == (unsigned)(n_exp - 1)) {
+        __threadfence();
+        for (int idx = lane; idx < R * 16; idx += 32) {
+          const int r = idx >> 4, row = rti * 16 + (idx & 15);
+          const float* orow = a.opart + (size_t)r * (1 + k) * H + row;
+          float yv = __ldcg(orow);
+          for (int j = 0; j < k; ++j)
+            yv = __fmaf_rn(a.topk_w[r * k + j], __ldcg(orow + (size_t)(1 + j) * H), yv);
+          a.y[(size_t)r * H + row] = f32_to_bf16_rne(yv);
+        }
       }
     }
   }
+  cp_async_wait<0>();
 }
 
 template <typename K>
@@ -563,19 +718,56 @@ cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+template <typename... Exp, typename... Act>
+cudaError_t launch_pdl(void (*kernel)(Exp...), int grid, int block, size_t smem, cudaStream_t s,
+                       Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
+}
+
+size_t gate_up_smem(const MoeDims& d) {
+  const size_t xbytes = ((size_t)d.R * (d.H * 2 + 64) + 127) & ~(size_t)127;
+  return xbytes + sizeof(GuStage) * kMmaWarps * kStages + sizeof(int) * 2 * kStages * kMmaWarps;
+}
+
+size_t down_smem() {
+  return sizeof(DnStage) * kMmaWarps * kStages + sizeof(int) * 2 * kStages * kMmaWarps;
+}
+
 }  // namespace
+
+size_t gate_up_smem_bytes(const MoeDims& d) { return gate_up_smem(d); }
+
+int gate_up_kparts(int H) {
+  const int T = ((H >> 5) + 3) >> 2;
+  const int TP = (T + 3) >> 2;
+  return (T + TP - 1) / TP;
+}
 
 MoeLayout moe_layout(const MoeDims& d) {
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  const size_t U = 1 + (size_t)d.R * d.k;           // expert slots (shared + union bound)
+  const size_t RT = (size_t)d.I / 16;
   MoeLayout L{};
   size_t off = 0;
   L.header = off; off += 256;
-  L.tile_count = off; off += up(sizeof(uint32_t) * (size_t)((d.H + kDownTileH - 1) / kDownTileH));
+  L.tile_count = off; off += up(sizeof(uint32_t) * (size_t)(d.H / 16));
+  L.part_count = off; off += up(sizeof(uint32_t) * U * RT);
   L.zero_bytes = off;
   L.logits = off; off += up(sizeof(float) * (size_t)d.R * d.E);
   L.route = off; off += up(sizeof(RouteInfo));
   L.h = off; off += up(sizeof(uint16_t) * (size_t)d.R * (1 + d.k) * d.I);
   L.opart = off; off += up(sizeof(float) * (size_t)d.R * (1 + d.k) * d.H);
+  L.part = off; off += up(sizeof(float) * U * RT * (size_t)gate_up_kparts(d.H) * 256);
   L.total = off;
   return L;
 }
@@ -596,39 +788,22 @@ cudaError_t launch_router(const MoeDims& d, const uint16_t* x, const uint16_t* r
 cudaError_t launch_gate_up(const MoeDims& d, const uint16_t* x, Q4Ptr gate, Q4Ptr up,
                            Q4Ptr sh_gate, Q4Ptr sh_up, const MoeWorkspace& ws,
                            cudaStream_t s) {
-  const size_t smem = sizeof(float) * ((size_t)d.R * d.H + (size_t)d.R * (d.H / 32));
+  const size_t smem = gate_up_smem(d);
   cudaError_t err = set_smem(k3_gate_up, smem);
   if (err != cudaSuccess) return err;
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k3_gate_up, kGateUpThreads, smem);
-  if (err != cudaSuccess) return err;
-  if (per_sm < 1) per_sm = 1;
-  const int tiles = (d.I + 7) / 8;
-  const int max_units = (1 + d.R * d.k) * tiles;
-  int grid = device_sm_count() * per_sm;
-  if (grid > max_units) grid = max_units;
-  GateUpArgs a{x, d.R, d.H, d.I, d.k, gate, up, sh_gate, sh_up, ws.route, ws.h};
-  k3_gate_up<<<grid, kGateUpThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  GateUpArgs a{x, d.R, d.H, d.I, d.k, gate, up, sh_gate, sh_up, ws.route, ws.h, ws.part,
+               ws.part_count, ws.header + 2};
+  return launch_pdl(k3_gate_up, device_sm_count(), kMmaThreads, smem, s, a);
 }
 
 cudaError_t launch_down(const MoeDims& d, Q4Ptr down, Q4Ptr sh_down, const float* topk_w,
                         uint16_t* y, const MoeWorkspace& ws, cudaStream_t s) {
-  const size_t smem = sizeof(float) * ((size_t)d.R * d.I + (size_t)d.R * (d.I / 32));
+  const size_t smem = down_smem();
   cudaError_t err = set_smem(k4_down, smem);
   if (err != cudaSuccess) return err;
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k4_down, kDownThreads, smem);
-  if (err != cudaSuccess) return err;
-  if (per_sm < 1) per_sm = 1;
-  const int tiles = (d.H + kDownTileH - 1) / kDownTileH;
-  const int min_units = tiles;  // at least the shared expert
-  int grid = device_sm_count() * per_sm;
-  if (grid > min_units * 4) grid = min_units * 4 > 0 ? min_units * 4 : 1;
   DownArgs a{ws.h, d.R, d.H, d.I, d.k, down, sh_down, ws.route, topk_w, ws.opart,
-             ws.tile_count, y};
-  k4_down<<<grid, kDownThreads, smem, s>>>(a);
-  return cudaGetLastError();
+             ws.tile_count, ws.header + 3, y};
+  return launch_pdl(k4_down, device_sm_count(), kMmaThreads, smem, s, a);
 }
 
 }  // namespace dsmoe

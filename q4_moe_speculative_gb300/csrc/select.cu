@@ -6,22 +6,28 @@
 // score only the blocks their mask admits, compact the admitted index once per row and
 // select the top 512 with a bounded radix select.
 //
-// Order of the chain on the device: K6 (per-row admitted counts, exclusive offsets per
-// mask word, admitted index) -> K5 (scores, written at the compacted position) -> K7.
+// Chain on the device:
+//  K6  per (layer, row): the admitted index of the row (ascending, written once) and its
+//      count; per layer: the union of the rows' admitted blocks ("union list", ascending)
+//      with, for each entry, the rows that admit it.
+//  K5  scores every union entry for the rows that admit it; results are stored by union
+//      position [layer][row][entry]. Rows that do not admit an entry get a sentinel that
+//      sorts below every score.
+//  K7  per (layer, row): bounded radix top-k over the union entries.
 //
 // Two scoring modes give the same selection:
-//  * canonical: K5 computes every admitted block's score in the canonical fp32 order
-//    (fmaf over i ascending, then over heads ascending) on CUDA cores; K7 radix-selects.
-//  * tensor-core (default): K5 computes q_h . k for all rows and heads of a 128-block tile
-//    as one [128 x 128] x [128 x R*Hh] bf16 contraction on tcgen05 (TMA-staged operands,
-//    fp32 accumulators in TMEM) and writes, per admitted block, a certified interval
-//    [lo, hi] that contains the canonical score: |s_tc - s_canon| <= eps with
-//    eps = 2^-10 * ||k|| * sum_h |w_h| ||q_h||  (the two dot products differ by at most a
-//    few hundred fp32 roundings of terms bounded by |q_i k_i|, and the canonical sum of
-//    |q_i k_i| is at most ||q|| ||k||; 2^-10 leaves a margin of about 2^7 over that).
-//    K7 takes T = k-th largest lo; every block of the canonical top-k has hi >= T, so it
-//    re-scores only the candidates with hi >= T in the canonical order and selects among
-//    them exactly. The result is identical to the canonical mode by construction.
+//  * canonical: every score in the canonical fp32 order (fmaf over i ascending, then over
+//    heads ascending) on CUDA cores;
+//  * tensor-core (default): q_h . k for a tile of 128 union keys as one
+//    [128 x 128] x [128 x R*Hh] bf16 contraction on tcgen05 (keys gathered by cp.async into
+//    the 128-byte swizzled K-major layout, queries likewise, fp32 accumulators in TMEM),
+//    giving an interval [lo, hi] that contains the canonical score:
+//    |s_tc - s_canon| <= eps = 2^-10 * ||k|| * sum_h |w_h| ||q_h||. (Both dot products are
+//    sums of exact products whose magnitudes add up to at most ||q|| ||k||; a few hundred
+//    fp32 roundings of such sums stay below 2^-15 of that, so 2^-10 leaves a margin of 2^5.)
+//    K7 takes T = k-th largest lo; every block of the canonical top-k has hi >= T, so only
+//    the candidates with hi >= T are re-scored in the canonical order and selected among
+//    exactly. The result is identical to the canonical mode by construction.
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -30,13 +36,17 @@ namespace dsmoe {
 namespace {
 
 constexpr int kCompactThreads = 1024;
-constexpr int kScoreThreads = 128;   // one key per thread, one tile of keys per CTA
+constexpr int kScoreThreads = 128;   // canonical scorer: one key per thread
+constexpr int kTcThreads = 128;      // tensor-core scorer: 4 warps = 128 TMEM lanes
 constexpr int kScoreMaxHeads = 16;
 constexpr int kTopkThreads = 1024;
+constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kResidCap = 4096;      // residual radix bucket kept in shared memory
 constexpr int kCandCap = 4096;       // re-score candidates kept in shared memory
 constexpr uint32_t kWaitPolls = 1u << 17;   // bounded mbarrier polling (<= ~0.13 s)
 constexpr float kEpsRel = 0.0009765625f;    // 2^-10
+constexpr uint32_t kNoScoreKey = 0u;        // sorts below the key of every score
+constexpr uint32_t kMinusInfBits = 0xFF800000u;
 
 // Exclusive block-wide prefix sum of v over blockDim.x (<= 1024) threads; *total gets
 // the sum. Uses `scratch` (>= 33 ints of shared memory). All threads must call it.
@@ -116,46 +126,88 @@ __device__ __forceinline__ float canonical_score(const float* q, const uint16_t*
 }
 
 // ---------------------------------------------------------------------------------
-// K6: compaction once per (layer, row). One CTA per row: popcount + block scan of the
-// admitted words gives every word's exclusive offset (kept for K5) and the count; each
-// warp then scatters the admitted indices of 32 words with a ballot over per-lane
-// predicates (bit set and block below the causal limit).
+// K6: compaction. CTAs [0, L*R): one per (layer, row): popcount + block scan of the
+// admitted words, then each warp scatters the admitted indices of 32 words with a ballot
+// over per-lane predicates (bit set and block below the causal limit). CTAs [L*R, L*R+L):
+// one per layer: the same over the union of the rows' admitted words, recording for each
+// union entry the rows that admit it, plus each union word's exclusive offset.
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kCompactThreads)
-    k6_compact(int R, int N, const uint32_t* __restrict__ mask, const int32_t* __restrict__ limit,
-               int32_t* __restrict__ wordoff, int32_t* __restrict__ cidx,
-               int32_t* __restrict__ ccount) {
+struct CompactArgs {
+  int L, R, N;
+  const uint32_t* mask;
+  const int32_t* limit;
+  int32_t* cidx;
+  int32_t* ccount;
+  int32_t* uidx;       // [L][N]
+  int32_t* ucount;     // [L]
+  uint8_t* urows;      // [L][N]
+  int32_t* uwordoff;   // [L][W]
+};
+
+__global__ void __launch_bounds__(kCompactThreads) k6_compact(CompactArgs a) {
   __shared__ int scratch[33];
   __shared__ int s_off[kCompactThreads];
-  const int lr = blockIdx.x;
+  __shared__ int s_lim[8];
+  const int R = a.R, N = a.N;
   const int W = (N + 31) >> 5;
-  const uint32_t* m = mask + (size_t)lr * W;
-  int lim = limit[lr];
-  lim = lim < 0 ? 0 : (lim > N ? N : lim);
-  int32_t* wo = wordoff + (size_t)lr * W;
-  int32_t* ci = cidx + (size_t)lr * N;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool union_cta = (int)blockIdx.x >= a.L * R;
+  const int l = union_cta ? (int)blockIdx.x - a.L * R : (int)blockIdx.x / R;
+  const int lr = blockIdx.x;   // meaningful for row CTAs only
+  const uint32_t* mrow = a.mask + (size_t)(union_cta ? l * R : lr) * W;
+  if (tid < R) {
+    const int lim = a.limit[(size_t)l * R + tid];
+    s_lim[tid] = lim < 0 ? 0 : (lim > N ? N : lim);
+  }
+  __syncthreads();
+  const int lim_row = union_cta ? 0 : s_lim[lr - l * R];
 
   int base = 0;
   for (int c0 = 0; c0 < W; c0 += kCompactThreads) {
     const int wi = c0 + tid;
-    const uint32_t mw = (wi < W) ? admitted_word(m, wi, lim) : 0u;
+    uint32_t mw = 0;
+    if (wi < W) {
+      if (union_cta) {
+        for (int r = 0; r < R; ++r)
+          mw |= admitted_word(a.mask + ((size_t)l * R + r) * W, wi, s_lim[r]);
+      } else {
+        mw = admitted_word(mrow, wi, lim_row);
+      }
+    }
     int total;
     const int excl = base + block_excl_scan(__popc(mw), scratch, &total);
-    if (wi < W) wo[wi] = excl;
     s_off[tid] = excl;
+    if (union_cta && wi < W) a.uwordoff[(size_t)l * W + wi] = excl;
     __syncthreads();
-    for (int q = warp; q < kCompactThreads && c0 + q < W; q += kCompactThreads / 32) {
-      const int w = c0 + q;
+    for (int qd = warp; qd < kCompactThreads && c0 + qd < W; qd += kCompactThreads / 32) {
+      const int w = c0 + qd;
       const int b = w * 32 + lane;
-      const bool pred = (b < lim) && ((m[w] >> lane) & 1u);
-      const uint32_t bal = __ballot_sync(0xffffffffu, pred);
-      if (pred) ci[s_off[q] + __popc(bal & ((1u << lane) - 1u))] = b;
+      if (!union_cta) {
+        const bool pred = (b < lim_row) && ((mrow[w] >> lane) & 1u);
+        const uint32_t bal = __ballot_sync(0xffffffffu, pred);
+        if (pred) a.cidx[(size_t)lr * N + s_off[qd] + __popc(bal & ((1u << lane) - 1u))] = b;
+      } else {
+        uint32_t rows = 0;
+        for (int r = 0; r < R; ++r) {
+          const uint32_t m = a.mask[((size_t)l * R + r) * W + w];
+          if (b < s_lim[r] && ((m >> lane) & 1u)) rows |= 1u << r;
+        }
+        const bool pred = rows != 0;
+        const uint32_t bal = __ballot_sync(0xffffffffu, pred);
+        if (pred) {
+          const size_t pos = (size_t)l * N + s_off[qd] + __popc(bal & ((1u << lane) - 1u));
+          a.uidx[pos] = b;
+          a.urows[pos] = (uint8_t)rows;
+        }
+      }
     }
     base += total;
     __syncthreads();
   }
-  if (tid == 0) ccount[lr] = base;
+  if (tid == 0) {
+    if (union_cta) a.ucount[l] = base;
+    else a.ccount[lr] = base;
+  }
 }
 
 struct ScoreArgs {
@@ -166,34 +218,19 @@ struct ScoreArgs {
   const float* hw;
   const uint32_t* mask;
   const int32_t* limit;
-  const int32_t* wordoff;
-  uint32_t* sc0;      // canonical: fp32 scores; tensor-core: keys of the lower bounds
-  float* sc1;         // tensor-core: upper bounds
+  const int32_t* uidx;
+  const int32_t* ucount;
+  const uint8_t* urows;
+  const int32_t* uwordoff;
+  uint32_t* sc0;      // [L][R][N] by union entry: fp32 scores, or lower-bound keys
+  float* sc1;         // [L][R][N] by union entry: upper bounds (tensor-core mode)
   uint32_t* status;
 };
 
-// Rows (bit r) of the layer that admit block b.
-__device__ __forceinline__ uint32_t admitting_rows(const ScoreArgs& a, int l, int b, int W) {
-  uint32_t rows = 0;
-  if (b < a.N) {
-    for (int r = 0; r < a.R; ++r) {
-      const size_t lr = (size_t)l * a.R + r;
-      const int lim = a.limit[lr];
-      if (b < lim && ((a.mask[lr * W + (b >> 5)] >> (b & 31)) & 1u)) rows |= 1u << r;
-    }
-  }
-  return rows;
-}
-
-__device__ __forceinline__ int compact_pos(const ScoreArgs& a, size_t lr, int b, int W) {
-  const int wi = b >> 5;
-  const uint32_t mw = admitted_word(a.mask + lr * W, wi, a.limit[lr]);
-  return a.wordoff[lr * W + wi] + __popc(mw & ((1u << (b & 31)) - 1u));
-}
-
 // ---------------------------------------------------------------------------------
-// K5 (canonical mode): CUDA-core scoring of admitted blocks. CTA = (layer, 128 blocks);
-// a key is loaded only if some row admits it, once for all rows.
+// K5 (canonical mode): CUDA-core scoring. CTA = (layer, 128 consecutive blocks); a key
+// is loaded only if some row admits it, once for all rows; scores go to the key's union
+// position; rows that do not admit it get -inf there.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kScoreThreads) k5_score(ScoreArgs a) {
   extern __shared__ float smem[];
@@ -210,7 +247,15 @@ __global__ void __launch_bounds__(kScoreThreads) k5_score(ScoreArgs a) {
   const int b = tile * kScoreThreads + tid;
   const int W = (a.N + 31) >> 5;
 
-  const uint32_t rows = admitting_rows(a, l, b, W);
+  uint32_t rows = 0, uw = 0;
+  if (b < a.N) {
+    for (int r = 0; r < R; ++r) {
+      const size_t lr = (size_t)l * R + r;
+      const uint32_t m = admitted_word(a.mask + lr * W, b >> 5, a.limit[lr]);
+      uw |= m;
+      if ((m >> (b & 31)) & 1u) rows |= 1u << r;
+    }
+  }
   s_rows[tid] = rows;
   const int any = __syncthreads_or(rows != 0);
   if (!any) return;
@@ -230,9 +275,14 @@ __global__ void __launch_bounds__(kScoreThreads) k5_score(ScoreArgs a) {
   }
   __syncthreads();
   if (rows == 0u) return;
+  const int e = a.uwordoff[(size_t)l * W + (b >> 5)] + __popc(uw & ((1u << (b & 31)) - 1u));
 
   for (int r = 0; r < R; ++r) {
-    if (!(rows & (1u << r))) continue;
+    const size_t out = ((size_t)l * R + r) * a.N + e;
+    if (!(rows & (1u << r))) {
+      a.sc0[out] = kMinusInfBits;
+      continue;
+    }
     float d[kScoreMaxHeads];
 #pragma unroll
     for (int h = 0; h < kScoreMaxHeads; ++h) d[h] = 0.0f;
@@ -259,201 +309,327 @@ __global__ void __launch_bounds__(kScoreThreads) k5_score(ScoreArgs a) {
 #pragma unroll
     for (int h = 0; h < kScoreMaxHeads; ++h)
       if (h < Hh) s = __fmaf_rn(ws[r * Hh + h], d[h] > 0.0f ? d[h] : 0.0f, s);
-    const size_t lr = (size_t)l * R + r;
-    reinterpret_cast<float*>(a.sc0)[lr * (size_t)a.N + compact_pos(a, lr, b, W)] = s;
+    a.sc0[out] = __float_as_uint(s);
   }
 }
 
+// 16-byte async copy global -> shared; zero-fill (no global read) when !valid.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------------
-// K5 (tensor-core mode): CTA = (layer, 128 blocks), 4 warps. TMA brings the 128 keys
-// [128 x 128 bf16] and the layer's queries [R*Hh (padded to NCH*16) x 128 bf16] into
-// shared memory in the 128-byte swizzled K-major layout; one thread issues 8 tcgen05.mma
-// (M = 128 keys, N = R*Hh, K = 16 each) into a TMEM accumulator; each warp reads its 32
-// lanes (one key per thread) and forms the approximate score and its certified interval.
-// Every wait is bounded; on give-up the kernel flags a timeout, waits once more (bounded)
-// for its own copies / MMAs, frees TMEM and returns.
+// K5 (tensor-core mode): persistent CTAs of 4 warps; CTA c scores a contiguous range of
+// the layers' union tiles (128 union entries each). Keys and queries are gathered with
+// cp.async into a double-buffered 128-byte swizzled K-major layout (row r's 16-byte chunk
+// j of each 64-value half at r*128 + ((j ^ (r & 7)) * 16)), so tile i + 2 loads while tile i
+// is scored. Thread 0 issues the 8 tcgen05.mma (M = 128 keys, N = NPAD >= R*Hh, K = 16 each)
+// into the tile's TMEM accumulator and commits to an mbarrier; each warp then reads its 32
+// lanes (one key per thread) and writes the interval bounds for every row. Waits are
+// bounded; a give-up sets DS_ERR_TIMEOUT in the status word, waits once more (bounded) for
+// the MMAs already issued, frees TMEM and returns.
 // ---------------------------------------------------------------------------------
 template <int NCH>
-__global__ void __launch_bounds__(kScoreThreads)
-    k5_score_tc(const __grid_constant__ CUtensorMap tm_keys,
-                const __grid_constant__ CUtensorMap tm_q, ScoreArgs a) {
+__global__ void __launch_bounds__(kTcThreads) k5_score_tc(ScoreArgs a) {
   constexpr int NPAD = NCH * 16;
-  constexpr uint32_t kTmemCols = NPAD <= 32 ? 32 : (NPAD <= 64 ? 64 : 128);
-  constexpr uint32_t kKeyBytes = 128 * 128 * 2;
-  constexpr uint32_t kQChunk = NPAD * 128;          // one 64-column half of the queries
+  constexpr uint32_t kCols = NPAD <= 32 ? 32 : (NPAD <= 64 ? 64 : 128);   // per buffer
+  constexpr uint32_t kKeyBytes = 128 * 256;       // one tile of keys
+  constexpr uint32_t kQBytes = NPAD * 256;        // one layer's queries
+  constexpr uint32_t kStageBytes = kKeyBytes + kQBytes;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_tma, bar_mma;
+  __shared__ __align__(8) uint64_t bar_mma[2];
   __shared__ uint32_t s_tmem;
-  __shared__ uint32_t s_rows[kScoreThreads];
+  __shared__ float s_w[2][NPAD];
   __shared__ float s_qn[NPAD];
-  __shared__ float s_w[NPAD];
-  __shared__ float s_F[8];
+  __shared__ float s_F[2][8];
+  __shared__ int s_total;
 
-  const int R = a.R, Hh = a.Hh, RH = R * Hh;
-  const int tiles = (a.N + kScoreThreads - 1) / kScoreThreads;
-  const int l = blockIdx.x / tiles;
-  const int tile = blockIdx.x - l * tiles;
+  const int R = a.R, Hh = a.Hh, RH = R * Hh, L = a.L, N = a.N;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = tile * kScoreThreads + tid;
-  const int W = (a.N + 31) >> 5;
 
-  const uint32_t rows = admitting_rows(a, l, b, W);
-  s_rows[tid] = rows;
-  const int any = __syncthreads_or(rows != 0);
-  if (!any) return;
-
-  // 1024-byte aligned operand tiles inside the dynamic shared memory.
   const uint32_t raw = sm100::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* tile_keys = smem_raw + (base - raw);
-  uint8_t* tile_q = tile_keys + kKeyBytes;
+  uint8_t* const stage_ptr0 = smem_raw + (base - raw);
+  const uint32_t stage_addr0 = base;
+
+  // Tiles over all layers and this CTA's contiguous range.
+  if (tid == 0) {
+    int t = 0;
+    for (int l = 0; l < L; ++l) t += (a.ucount[l] + 127) >> 7;
+    s_total = t;
+  }
+  __syncthreads();
+  const int total = s_total;
+  const int t0 = (int)(((long long)blockIdx.x * total) / gridDim.x);
+  const int t1 = (int)(((long long)(blockIdx.x + 1) * total) / gridDim.x);
+  if (t0 >= t1) return;
 
   if (tid == 0) {
-    sm100::prefetch_tensormap(&tm_keys);
-    sm100::prefetch_tensormap(&tm_q);
-    sm100::mbar_init(&bar_tma, 1);
-    sm100::mbar_init(&bar_mma, 1);
+    sm100::mbar_init(&bar_mma[0], 1);
+    sm100::mbar_init(&bar_mma[1], 1);
     sm100::fence_mbar_init();
   }
   if (warp == 0) {
-    sm100::tmem_alloc(&s_tmem, kTmemCols);
+    sm100::tmem_alloc(&s_tmem, 2 * kCols);
     sm100::tmem_relinquish();
   }
-  if (tid < NPAD) s_w[tid] = tid < RH ? a.hw[(size_t)l * RH + tid] : 0.0f;
   sm100::tc_fence_before();
   __syncthreads();
   sm100::tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  if (tid == 0) {
-    sm100::mbar_arrive_expect_tx(&bar_tma, kKeyBytes + 2 * kQChunk);
-    sm100::tma_load_3d(tile_keys, &tm_keys, 0, tile * 128, l, &bar_tma);
-    sm100::tma_load_3d(tile_keys + kKeyBytes / 2, &tm_keys, 64, tile * 128, l, &bar_tma);
-    sm100::tma_load_2d(tile_q, &tm_q, 0, l * RH, &bar_tma);
-    sm100::tma_load_2d(tile_q + kQChunk, &tm_q, 64, l * RH, &bar_tma);
-  }
-  bool ok = sm100::mbar_wait(&bar_tma, 0, kWaitPolls);
-  if (!ok) {
-    if (tid == 0) flag_status(a.status, kStatusTimeout);
-    sm100::mbar_wait(&bar_tma, 0, kWaitPolls);    // let our own copies land before exit
-  }
-  if (ok && tid == 0) {
-    constexpr uint32_t idesc = sm100::idesc_bf16_f32(128, NPAD);
-    const uint32_t ka = sm100::smem_u32(tile_keys), qa = sm100::smem_u32(tile_q);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t half = (uint32_t)(kk >> 2), step = (uint32_t)(kk & 3) * 32u;
-      const uint64_t ad = sm100::desc_k_sw128(ka + half * (kKeyBytes / 2) + step);
-      const uint64_t bd = sm100::desc_k_sw128(qa + half * kQChunk + step);
-      sm100::mma_bf16(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+  // Tile t0 -> (layer, first entry): walk the layers once.
+  int cur_l = 0, cur_e0 = 0;
+  {
+    int t = 0;
+    for (; cur_l < L; ++cur_l) {
+      const int nt = (a.ucount[cur_l] + 127) >> 7;
+      if (t + nt > t0) { cur_e0 = (t0 - t) * 128; break; }
+      t += nt;
     }
-    sm100::mma_commit(&bar_mma);
   }
-  if (ok) {
-    ok = sm100::mbar_wait(&bar_mma, 0, kWaitPolls);
+  int is_l = cur_l, is_e0 = cur_e0;    // issue cursor
+  int stage_qlayer[2] = {-1, -1};       // layer whose queries each stage buffer holds
+  int norm_layer[2] = {-1, -1};         // layer whose norms / weights each stage has
+
+  auto advance = [&](int& lcur, int& ecur) {
+    ecur += 128;
+    if (ecur >= a.ucount[lcur]) {
+      ecur = 0;
+      ++lcur;
+      while (lcur < L && a.ucount[lcur] == 0) ++lcur;
+    }
+  };
+
+  auto issue = [&](int stage) {
+    const int l = is_l, e0 = is_e0;
+    const int ucnt = a.ucount[l];
+    const uint32_t sbase = stage_addr0 + (uint32_t)stage * kStageBytes;
+    const uint8_t* kbase8 = reinterpret_cast<const uint8_t*>(a.keys + (size_t)l * a.key_stride);
+    // keys: warp w copies rows w*32 .. w*32+31, two rows (512 contiguous bytes) per step
+#pragma unroll 4
+    for (int jj = 0; jj < 16; ++jj) {
+      const int r = warp * 32 + 2 * jj + (lane >> 4);
+      const int c = lane & 15;
+      const int e = e0 + r;
+      const bool v = e < ucnt;
+      const int b = v ? a.uidx[(size_t)l * N + e] : 0;
+      const uint32_t dst = sbase + (uint32_t)(c >> 3) * (kKeyBytes / 2) + (uint32_t)r * 128u +
+                           (uint32_t)(((c & 7) ^ (r & 7)) << 4);
+      cp_async16(dst, kbase8 + (size_t)b * 256 + c * 16, v);
+    }
+    // queries of layer l, when this stage buffer holds another layer's
+    if (stage_qlayer[stage] != l) {
+      const uint8_t* qbase8 = reinterpret_cast<const uint8_t*>(a.q + (size_t)l * RH * 128);
+      for (int i = tid; i < NPAD * 16; i += kTcThreads) {
+        const int r = i >> 4, c = i & 15;
+        const uint32_t dst = sbase + kKeyBytes + (uint32_t)(c >> 3) * (kQBytes / 2) +
+                             (uint32_t)r * 128u + (uint32_t)(((c & 7) ^ (r & 7)) << 4);
+        cp_async16(dst, qbase8 + (size_t)(r < RH ? r : 0) * 256 + c * 16, r < RH);
+      }
+      stage_qlayer[stage] = l;
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    advance(is_l, is_e0);
+  };
+
+  const int n = t1 - t0;
+  issue(0);
+  if (n > 1) issue(1);
+  else asm volatile("cp.async.commit_group;" ::: "memory");
+  uint32_t phase[2] = {0u, 0u};
+  bool ok = true;
+
+  for (int i = 0; i < n; ++i) {
+    const int stage = i & 1;
+    const int l = cur_l, e0 = cur_e0;
+    uint8_t* const sp = stage_ptr0 + stage * kStageBytes;
+    const uint32_t sa = stage_addr0 + (uint32_t)stage * kStageBytes;
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+
+    if (norm_layer[stage] != l) {   // per-layer query norms, weights and F_r
+      const uint8_t* qt = sp + kKeyBytes;
+      if (tid < NPAD) {
+        float ss = 0.0f;
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          const uint4* row = reinterpret_cast<const uint4*>(qt + hlf * (kQBytes / 2) + tid * 128);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const uint4 u = row[g];
+            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = bf16_lo(wv[e]), hi = bf16_hi(wv[e]);
+              ss = __fmaf_ru(lo, lo, ss);
+              ss = __fmaf_ru(hi, hi, ss);
+            }
+          }
+        }
+        s_qn[tid] = __fmul_ru(__fsqrt_ru(ss), 1.0000153f);   // (1 + 2^-16) margin
+        s_w[stage][tid] = tid < RH ? a.hw[(size_t)l * RH + tid] : 0.0f;
+      }
+      __syncthreads();
+      if (tid < R) {
+        float F = 0.0f;
+        for (int h = 0; h < Hh; ++h)
+          F = __fmaf_ru(fabsf(s_w[stage][tid * Hh + h]), s_qn[tid * Hh + h], F);
+        s_F[stage][tid] = F;
+      }
+      norm_layer[stage] = l;
+      __syncthreads();
+    }
+
+    const uint32_t tbuf = tmem + (uint32_t)stage * kCols;
+    if (tid == 0) {
+      sm100::tc_fence_after();
+      constexpr uint32_t idesc = sm100::idesc_bf16_f32(128, NPAD);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t half = (uint32_t)(kk >> 2), step = (uint32_t)(kk & 3) * 32u;
+        const uint64_t ad = sm100::desc_k_sw128(sa + half * (kKeyBytes / 2) + step);
+        const uint64_t bd = sm100::desc_k_sw128(sa + kKeyBytes + half * (kQBytes / 2) + step);
+        sm100::mma_bf16(tbuf, ad, bd, idesc, kk > 0 ? 1u : 0u);
+      }
+      sm100::mma_commit(&bar_mma[stage]);
+    }
+    bool done = sm100::mbar_wait(&bar_mma[stage], phase[stage], kWaitPolls);
+    if (!done) sm100::mbar_wait(&bar_mma[stage], phase[stage], kWaitPolls);  // own MMAs
+    ok = __syncthreads_and(done) != 0;
     if (!ok) {
       if (tid == 0) flag_status(a.status, kStatusTimeout);
-      sm100::mbar_wait(&bar_mma, 0, kWaitPolls);
+      break;
     }
-  }
-  sm100::tc_fence_after();
+    phase[stage] ^= 1u;
+    sm100::tc_fence_after();
 
-  if (ok) {
-    // Query norms (upper bounds) and the per-row factor F_r = sum_h |w_h| ||q_h||.
-    if (tid < NPAD) {
-      float ss = 0.0f;
-      const uint4* row0 = reinterpret_cast<const uint4*>(tile_q + tid * 128);
-      const uint4* row1 = reinterpret_cast<const uint4*>(tile_q + kQChunk + tid * 128);
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const uint4 u0 = row0[g], u1 = row1[g];
-        const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float lo = bf16_lo(wv[e]), hi = bf16_hi(wv[e]);
-          ss = __fmaf_ru(lo, lo, ss);
-          ss = __fmaf_ru(hi, hi, ss);
-        }
-      }
-      s_qn[tid] = __fmul_ru(__fsqrt_ru(ss), 1.0000153f);   // (1 + 2^-16) margin
-    }
-    __syncthreads();
-    if (tid < R) {
-      float F = 0.0f;
-      for (int h = 0; h < Hh; ++h) F = __fmaf_ru(fabsf(s_w[tid * Hh + h]), s_qn[tid * Hh + h], F);
-      s_F[tid] = F;
-    }
-    __syncthreads();
-
-    // This thread's key norm (order of the 16-byte granules does not matter).
-    float kss = 0.0f;
     {
-      const uint8_t* kr0 = tile_keys + tid * 128;
-      const uint8_t* kr1 = tile_keys + kKeyBytes / 2 + tid * 128;
+      const int e = e0 + tid;
+      const int ucnt = a.ucount[l];
+      // key norm of this thread's row (the order of the 16-byte granules does not matter)
+      float kss = 0.0f;
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const int gg = (g + tid) & 7;   // rotate to spread the banks
-        const uint4 u0 = *reinterpret_cast<const uint4*>(kr0 + gg * 16);
-        const uint4 u1 = *reinterpret_cast<const uint4*>(kr1 + gg * 16);
-        const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const uint8_t* kr = sp + hlf * (kKeyBytes / 2) + tid * 128;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float lo = bf16_lo(wv[e]), hi = bf16_hi(wv[e]);
-          kss = __fmaf_ru(lo, lo, kss);
-          kss = __fmaf_ru(hi, hi, kss);
+        for (int g = 0; g < 8; ++g) {
+          const uint4 u = *reinterpret_cast<const uint4*>(kr + (((g + tid) & 7) << 4));
+          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float lo = bf16_lo(wv[q]), hi = bf16_hi(wv[q]);
+            kss = __fmaf_ru(lo, lo, kss);
+            kss = __fmaf_ru(hi, hi, kss);
+          }
         }
       }
-    }
-    const float kn = __fmul_ru(__fsqrt_ru(kss), 1.0000153f);
-
-    float d[NPAD];
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+      const float kn = __fmul_ru(__fsqrt_ru(kss), 1.0000153f);
+      float d[NPAD];
+      const uint32_t lane_base = tbuf + ((uint32_t)(warp * 32) << 16);
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) sm100::tmem_ld16(lane_base + (uint32_t)(c * 16), d + c * 16);
-
-    if (rows != 0u) {
-      float s = 0.0f;
-      int r = 0, h = 0;
+      for (int c = 0; c < NCH; ++c) sm100::tmem_ld16(lane_base + (uint32_t)(c * 16), d + c * 16);
+      if (e < ucnt) {
+        const uint32_t rows = a.urows[(size_t)l * N + e];
+        float s = 0.0f;
+        int r = 0, h = 0;
 #pragma unroll
-      for (int p = 0; p < NPAD; ++p) {
-        if (p < RH) {
-          if (h == 0) s = 0.0f;
-          s = __fmaf_rn(s_w[p], d[p] > 0.0f ? d[p] : 0.0f, s);
-          if (h == Hh - 1) {
-            if (rows & (1u << r)) {
-              const size_t lr = (size_t)l * R + r;
-              const float eps = __fmul_ru(__fmul_ru(kEpsRel, kn), s_F[r]);
-              const int pos = compact_pos(a, lr, b, W);
-              a.sc0[lr * (size_t)a.N + pos] = score_key(__fsub_rd(s, eps));
-              a.sc1[lr * (size_t)a.N + pos] = __fadd_ru(s, eps);
+        for (int p = 0; p < NPAD; ++p) {
+          if (p < RH) {
+            if (h == 0) s = 0.0f;
+            s = __fmaf_rn(s_w[stage][p], d[p] > 0.0f ? d[p] : 0.0f, s);
+            if (h == Hh - 1) {
+              const size_t out = ((size_t)l * R + r) * N + e;
+              if (rows & (1u << r)) {
+                const float eps = __fmul_ru(__fmul_ru(kEpsRel, kn), s_F[stage][r]);
+                a.sc0[out] = score_key(__fsub_rd(s, eps));
+                a.sc1[out] = __fadd_ru(s, eps);
+              } else {
+                a.sc0[out] = kNoScoreKey;
+                a.sc1[out] = __uint_as_float(kMinusInfBits);
+              }
+              h = 0;
+              ++r;
+            } else {
+              ++h;
             }
-            h = 0;
-            ++r;
-          } else {
-            ++h;
           }
         }
       }
     }
+    sm100::tc_fence_before();
+    __syncthreads();   // stage buffers and TMEM accumulator of this tile are free again
+    advance(cur_l, cur_e0);
+    if (i + 2 < n) issue(stage);
+    else asm volatile("cp.async.commit_group;" ::: "memory");
   }
   (void)lane;
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   sm100::tc_fence_before();
   __syncthreads();
-  if (warp == 0) sm100::tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) sm100::tmem_dealloc(tmem, 2 * kCols);
 }
 
 // ---------------------------------------------------------------------------------
-// Radix threshold: the key of the need-th largest element among n keys, found MSB-first
-// 8 bits at a time. `key_at(i)` gives the key of element i. After the first two passes the
-// elements whose top 16 bits match are gathered into `r_key` (if at most kResidCap of
-// them) and the last two passes run there. On return *need_out = how many elements equal
-// to the threshold belong to the selection. All threads must call it.
+// K7 building blocks. Each warp owns a contiguous segment of the row's entries and walks
+// it 32 at a time (coalesced loads, several batches in flight); per-warp counts are
+// combined once where an ordered result is needed.
 // ---------------------------------------------------------------------------------
+__device__ __forceinline__ void warp_segment(int n, int* beg, int* end) {
+  const int warp = threadIdx.x >> 5;
+  const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
+  *beg = warp * seg;
+  *end = min(n, *beg + seg);
+}
+
+// One histogram pass of the radix select over digit (key >> shift) & 255 of the elements
+// whose higher digits equal `prefix` (all elements when `first`). One shared atomic per
+// distinct bucket per warp: scores cluster in a few top-byte buckets.
+template <typename KeyAt>
+__device__ __forceinline__ void hist_pass(int n, bool resid, const uint32_t* r_key, int rn,
+                                          int shift, uint32_t prefix, bool first,
+                                          KeyAt key_at, int* hist) {
+  const int lane = threadIdx.x & 31;
+  auto add = [&](uint32_t key, bool valid) {
+    const bool in = valid && (first || (key >> (shift + 8)) == prefix);
+    const uint32_t bucket = in ? ((key >> shift) & 255u) : 256u;
+    const unsigned peers = __match_any_sync(0xffffffffu, bucket);
+    if (in && lane == (__ffs(peers) - 1)) atomicAdd(&hist[bucket], __popc(peers));
+  };
+  if (resid) {
+    for (int i0 = 0; i0 < rn; i0 += blockDim.x) {
+      const int i = i0 + threadIdx.x;
+      add(i < rn ? r_key[i] : 0u, i < rn);
+    }
+  } else {
+    constexpr int U = 8;
+    int beg, end;
+    warp_segment(n, &beg, &end);
+    for (int i0 = beg; i0 < end; i0 += 32 * U) {
+      uint32_t k[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * 32 + lane;
+        k[u] = i < end ? key_at(i) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) add(k[u], i0 + u * 32 + lane < end);
+    }
+  }
+}
+
+// The key of the need-th largest element among n keys, MSB-first 8 bits at a time. After
+// the first two passes the elements whose top 16 bits match are gathered into r_key (if
+// at most kResidCap of them) and the last two passes run there. *need_out = how many
+// elements equal to the threshold belong to the selection. All threads must call it.
 template <typename KeyAt>
 __device__ uint32_t radix_threshold(int n, int need, KeyAt key_at, int* hist, int* scratch,
                                     uint32_t* r_key, int* s_misc, uint32_t* status,
                                     int* need_out) {
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   int& s_bucket = s_misc[0];
   int& s_need = s_misc[1];
   int& s_rn = s_misc[2];
@@ -467,18 +643,8 @@ __device__ uint32_t radix_threshold(int n, int need, KeyAt key_at, int* hist, in
       s_need = need;
     }
     __syncthreads();
-    if (resid) {
-      const int rn = s_rn < kResidCap ? s_rn : kResidCap;
-      for (int i = tid; i < rn; i += blockDim.x) {
-        const uint32_t key = r_key[i];
-        if ((key >> (shift + 8)) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
-      }
-    } else {
-      for (int i = tid; i < n; i += blockDim.x) {
-        const uint32_t key = key_at(i);
-        if (pass == 0 || (key >> (shift + 8)) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
-      }
-    }
+    hist_pass(n, resid, r_key, resid ? min(s_rn, kResidCap) : 0, shift, prefix,
+              pass == 0, key_at, hist);
     __syncthreads();
     {
       const int v = tid < 256 ? hist[255 - tid] : 0;
@@ -504,11 +670,23 @@ __device__ uint32_t radix_threshold(int n, int need, KeyAt key_at, int* hist, in
       if (cnt <= kResidCap) {
         if (tid == 0) s_rn = 0;
         __syncthreads();
-        for (int i = tid; i < n; i += blockDim.x) {
-          const uint32_t key = key_at(i);
-          if ((key >> 16) == prefix) {
-            const int p = atomicAdd(&s_rn, 1);
-            if (p < kResidCap) r_key[p] = key;
+        constexpr int U = 8;
+        int beg, end;
+        warp_segment(n, &beg, &end);
+        for (int i0 = beg; i0 < end; i0 += 32 * U) {
+          uint32_t k[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * 32 + lane;
+            k[u] = i < end ? key_at(i) : 0u;
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * 32 + lane;
+            if (i < end && (k[u] >> 16) == prefix) {
+              const int p = atomicAdd(&s_rn, 1);
+              if (p < kResidCap) r_key[p] = k[u];
+            }
           }
         }
         __syncthreads();
@@ -522,37 +700,54 @@ __device__ uint32_t radix_threshold(int n, int need, KeyAt key_at, int* hist, in
   return prefix;
 }
 
-// Writes, in array order, every element with key > T and the first `need` elements with
-// key == T: out[j] = idx_at(i). Returns the number written (<= K).
-template <typename KeyAt, typename IdxAt>
-__device__ int ordered_take(int n, int K, uint32_t T, int need, KeyAt key_at, IdxAt idx_at,
-                            int32_t* out, int* scratch) {
-  int taken = 0, eq_seen = 0;
-  for (int c0 = 0; c0 < n && taken < K; c0 += blockDim.x) {
-    const int i = c0 + threadIdx.x;
-    uint32_t key = 0;
-    if (i < n) key = key_at(i);
-    const int gt = (i < n) && key > T;
-    const int eq = (i < n) && key == T;
-    int eq_total;
-    const int eq_rank = eq_seen + block_excl_scan(eq, scratch, &eq_total);
-    const int take = gt || (eq && eq_rank < need);
-    int take_total;
-    const int pos = taken + block_excl_scan(take, scratch, &take_total);
-    if (take && pos < K) out[pos] = idx_at(i);
-    taken += take_total;
-    eq_seen += eq_total;
+// Ordered selection over n elements: every element classified 2 ("greater"), plus the
+// first `need` elements (in index order) classified 1 ("equal"); emit(pos, i) for each,
+// pos ascending from 0. Two passes over the warps' segments with the per-warp counts
+// combined in between. Returns how many were taken. All threads must call it.
+template <typename Cls, typename Emit>
+__device__ int ordered_take(int n, int need, Cls cls, Emit emit, int* s_eq, int* s_gt) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int beg, end;
+  warp_segment(n, &beg, &end);
+  int gt_w = 0, eq_w = 0;
+  for (int i0 = beg; i0 < end; i0 += 32) {
+    const int i = i0 + lane;
+    const int c = i < end ? cls(i) : 0;    // 2 = greater, 1 = equal, 0 = below
+    gt_w += __popc(__ballot_sync(0xffffffffu, c == 2));
+    eq_w += __popc(__ballot_sync(0xffffffffu, c == 1));
   }
-  return taken;
+  if (lane == 0) { s_eq[warp] = eq_w; s_gt[warp] = gt_w; }
+  __syncthreads();
+  int eq_acc = 0, out_acc = 0, my_eq = 0, my_out = 0;
+  for (int w = 0; w < kTopkWarps; ++w) {
+    if (w == warp) { my_eq = eq_acc; my_out = out_acc; }
+    out_acc += s_gt[w] + max(0, min(s_eq[w], need - eq_acc));
+    eq_acc += s_eq[w];
+  }
+  int pos = my_out, eq_seen = my_eq;
+  for (int i0 = beg; i0 < end; i0 += 32) {
+    const int i = i0 + lane;
+    const int c = i < end ? cls(i) : 0;
+    const uint32_t eqm = __ballot_sync(0xffffffffu, c == 1);
+    const int eq_rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
+    const bool take = (c == 2) || (c == 1 && eq_rank < need);
+    const uint32_t tm = __ballot_sync(0xffffffffu, take);
+    if (take) emit(pos + __popc(tm & ((1u << lane) - 1u)), i);
+    pos += __popc(tm);
+    eq_seen += __popc(eqm);
+  }
+  __syncthreads();
+  return out_acc;
 }
 
 // ---------------------------------------------------------------------------------
-// K7: bounded radix top-k per (layer, row), one CTA of 1024 threads.
+// K7: bounded radix top-k per (layer, row), one CTA of 1024 threads, over the layer's
+// union entries (entries the row does not admit carry the sentinel and never qualify).
 // Canonical mode: threshold and ordered take over the canonical scores.
 // Tensor-core mode: threshold T over the lower bounds; ordered gather of the candidates
 // with upper bound >= T (bounded by kCandCap); canonical re-score of the candidates;
 // threshold and ordered take among them. Above the bound: canonical re-score of every
-// admitted block of the row, then the canonical-mode path.
+// admitted entry of the row, then the canonical-mode path.
 // ---------------------------------------------------------------------------------
 struct TopkArgs {
   int R, Hh, N, K;
@@ -562,6 +757,8 @@ struct TopkArgs {
   const float* hw;
   const int32_t* cidx;
   const int32_t* ccount;
+  const int32_t* uidx;
+  const int32_t* ucount;
   uint32_t* sc0;
   const float* sc1;
   int32_t* sel;
@@ -574,9 +771,10 @@ __global__ void __launch_bounds__(kTopkThreads) k7_topk(TopkArgs a) {
   __shared__ int hist[256];
   __shared__ int scratch[33];
   __shared__ int s_misc[4];
+  __shared__ int s_eq[kTopkWarps], s_gt[kTopkWarps];
   __shared__ uint32_t r_key[kResidCap];
   extern __shared__ uint8_t dsm[];
-  int32_t* cand = reinterpret_cast<int32_t*>(dsm);               // [kCandCap] positions
+  int32_t* cand = reinterpret_cast<int32_t*>(dsm);               // [kCandCap] entries
   uint32_t* ckey = reinterpret_cast<uint32_t*>(cand + kCandCap);  // [kCandCap] keys
   float* qf = reinterpret_cast<float*>(ckey + kCandCap);          // [Hh][128]
   float* wf = qf + kScoreMaxHeads * 128;                          // [Hh]
@@ -584,19 +782,20 @@ __global__ void __launch_bounds__(kTopkThreads) k7_topk(TopkArgs a) {
   const int lr = blockIdx.x;
   const int l = lr / a.R;
   const int tid = threadIdx.x;
-  const int n = a.ccount[lr];
+  const int count = a.ccount[lr];
   const int K = a.K;
-  const int32_t* ci = a.cidx + (size_t)lr * a.N;
-  uint32_t* s0 = a.sc0 + (size_t)lr * a.N;
   int32_t* out = a.sel + (size_t)lr * K;
 
-  if (n <= K) {
-    for (int i = tid; i < K; i += blockDim.x) out[i] = i < n ? ci[i] : -1;
-    if (tid == 0) a.nsel[lr] = n;
+  if (count <= K) {
+    const int32_t* ci = a.cidx + (size_t)lr * a.N;
+    for (int i = tid; i < K; i += blockDim.x) out[i] = i < count ? ci[i] : -1;
+    if (tid == 0) a.nsel[lr] = count;
     return;
   }
 
-  auto idx_at = [&](int i) { return ci[i]; };
+  const int n = a.ucount[l];
+  const int32_t* ui = a.uidx + (size_t)l * a.N;
+  uint32_t* s0 = a.sc0 + (size_t)lr * a.N;
   const uint16_t* kbase = a.keys + (size_t)l * a.key_stride;
   bool canonical = !a.tc_mode;
 
@@ -605,24 +804,18 @@ __global__ void __launch_bounds__(kTopkThreads) k7_topk(TopkArgs a) {
     int need;
     const uint32_t T = radix_threshold(
         n, K, [&](int i) { return s0[i]; }, hist, scratch, r_key, s_misc, a.status, &need);
-    // Ordered gather of candidates (upper bound can reach T), bounded by kCandCap.
-    int m = 0;
-    for (int c0 = 0; c0 < n; c0 += blockDim.x) {
-      const int i = c0 + tid;
-      const int c = (i < n) && score_key(s1[i]) >= T;
-      int tot;
-      const int p = m + block_excl_scan(c, scratch, &tot);
-      if (c && p < kCandCap) cand[p] = i;
-      m += tot;
-    }
-    // Stage this row's queries and weights as fp32.
+    // Ordered gather of the candidates (upper bound reaches T), bounded by kCandCap.
+    const int m = ordered_take(
+        n, 0, [&](int i) { return score_key(s1[i]) >= T ? 2 : 0; },
+        [&](int p, int i) { if (p < kCandCap) cand[p] = i; }, s_eq, s_gt);
+    // This row's queries and weights as fp32.
     const uint16_t* qrow = a.q + (size_t)lr * a.Hh * 128;
     for (int i = tid; i < a.Hh * 128; i += blockDim.x) qf[i] = bf16_bits_to_f32(qrow[i]);
     for (int i = tid; i < a.Hh; i += blockDim.x) wf[i] = a.hw[(size_t)lr * a.Hh + i];
     __syncthreads();
     if (m <= kCandCap) {
       for (int j = tid; j < m; j += blockDim.x) {
-        const int b = ci[cand[j]];
+        const int b = ui[cand[j]];
         ckey[j] = score_key(canonical_score(qf, kbase + (size_t)b * 128, wf, a.Hh));
       }
       __syncthreads();
@@ -630,8 +823,9 @@ __global__ void __launch_bounds__(kTopkThreads) k7_topk(TopkArgs a) {
       const uint32_t T2 = radix_threshold(
           m, K, [&](int j) { return ckey[j]; }, hist, scratch, r_key, s_misc, a.status, &need2);
       const int taken = ordered_take(
-          m, K, T2, need2, [&](int j) { return ckey[j]; }, [&](int j) { return ci[cand[j]]; },
-          out, scratch);
+          m, need2,
+          [&](int j) { const uint32_t k = ckey[j]; return k > T2 ? 2 : (k == T2 ? 1 : 0); },
+          [&](int p, int j) { if (p < K) out[p] = ui[cand[j]]; }, s_eq, s_gt);
       if (tid == 0) {
         a.nsel[lr] = K;
         if (taken != K) flag_status(a.status, kStatusCheck);
@@ -639,17 +833,25 @@ __global__ void __launch_bounds__(kTopkThreads) k7_topk(TopkArgs a) {
       return;
     }
     // Too many candidates (e.g. heavy ties): canonical scores for the whole row.
-    for (int i = tid; i < n; i += blockDim.x)
-      s0[i] = __float_as_uint(canonical_score(qf, kbase + (size_t)ci[i] * 128, wf, a.Hh));
+    for (int i = tid; i < n; i += blockDim.x) {
+      const bool adm = __float_as_uint(s1[i]) != kMinusInfBits;
+      s0[i] = adm ? __float_as_uint(canonical_score(qf, kbase + (size_t)ui[i] * 128, wf, a.Hh))
+                  : kMinusInfBits;
+    }
     __syncthreads();
     canonical = true;
   }
 
   if (canonical) {
     int need;
-    auto key_at = [&](int i) { return score_key(__uint_as_float(s0[i])); };
+    auto key_at = [&](int i) {
+      const uint32_t b = s0[i];
+      return b == kMinusInfBits ? kNoScoreKey : score_key(__uint_as_float(b));
+    };
     const uint32_t T = radix_threshold(n, K, key_at, hist, scratch, r_key, s_misc, a.status, &need);
-    const int taken = ordered_take(n, K, T, need, key_at, idx_at, out, scratch);
+    const int taken = ordered_take(
+        n, need, [&](int i) { const uint32_t k = key_at(i); return k > T ? 2 : (k == T ? 1 : 0); },
+        [&](int p, int i) { if (p < K) out[p] = ui[i]; }, s_eq, s_gt);
     if (tid == 0) {
       a.nsel[lr] = K;
       if (taken != K) flag_status(a.status, kStatusCheck);
@@ -657,37 +859,21 @@ __global__ void __launch_bounds__(kTopkThreads) k7_topk(TopkArgs a) {
   }
 }
 
-// --------------------------------------------------------------- tensor maps --------
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                   CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
 template <int NCH>
-cudaError_t launch_tc(const SelDims& d, const CUtensorMap& tk, const CUtensorMap& tq,
-                      const ScoreArgs& a, cudaStream_t s) {
-  const size_t smem = 1024 + 128 * 128 * 2 + 2 * (size_t)NCH * 16 * 128;
+cudaError_t launch_tc(const SelDims& d, const ScoreArgs& a, cudaStream_t s) {
+  constexpr size_t stage = 128 * 256 + NCH * 16 * 256;
+  const size_t smem = 1024 + 2 * stage;
   if (smem > 48 * 1024) {
     cudaError_t err = cudaFuncSetAttribute(k5_score_tc<NCH>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
   }
-  const int tiles = (d.N + kScoreThreads - 1) / kScoreThreads;
-  k5_score_tc<NCH><<<d.L * tiles, kScoreThreads, smem, s>>>(tk, tq, a);
+  // Enough CTAs to keep every SM busy; each takes a contiguous range of tiles.
+  const long long tiles = (long long)((d.N + 127) / 128) * d.L;
+  int grid = device_sm_count() * 2;
+  if (tiles < grid) grid = (int)tiles;
+  if (grid < 1) grid = 1;
+  k5_score_tc<NCH><<<grid, kTcThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -700,13 +886,16 @@ SelLayout sel_layout(const SelDims& d, bool caller_cidx) {
   SelLayout L{};
   size_t off = 0;
   L.header = off; off += 256;
-  L.wordoff = off; off += up(sizeof(int32_t) * LR * W);
+  L.wordoff = off; off += up(sizeof(int32_t) * (size_t)d.L * W);
   if (!caller_cidx) {
     L.cidx = off; off += up(sizeof(int32_t) * LR * (size_t)d.N);
     L.ccount = off; off += up(sizeof(int32_t) * LR);
   } else {
     L.cidx = L.ccount = (size_t)-1;
   }
+  L.uidx = off; off += up(sizeof(int32_t) * (size_t)d.L * d.N);
+  L.ucount = off; off += up(sizeof(int32_t) * (size_t)d.L);
+  L.urows = off; off += up((size_t)d.L * d.N);
   L.cscore = off; off += up(sizeof(float) * LR * (size_t)d.N);
   L.chi = off; off += up(sizeof(float) * LR * (size_t)d.N);
   L.total = off;
@@ -715,23 +904,24 @@ SelLayout sel_layout(const SelDims& d, bool caller_cidx) {
 
 bool tc_scoring_supported(const SelDims& d, const uint16_t* keys, const uint16_t* q) {
   const int RH = d.R * d.Hh;
-  return encode_fn() != nullptr && RH <= 128 && d.D == 128 &&
-         (reinterpret_cast<uintptr_t>(keys) % 16) == 0 &&
-         (reinterpret_cast<uintptr_t>(q) % 16) == 0 && (d.key_stride % 8) == 0;
+  return RH <= 128 && d.D == 128 && (reinterpret_cast<uintptr_t>(keys) % 16) == 0 &&
+         (reinterpret_cast<uintptr_t>(q) % 16) == 0 && (d.key_stride % 8) == 0 && d.R <= 8;
 }
 
 cudaError_t launch_compact(const SelDims& d, const uint32_t* mask, const int32_t* limit,
                            const SelWorkspace& ws, cudaStream_t s) {
-  k6_compact<<<d.L * d.R, kCompactThreads, 0, s>>>(d.R, d.N, mask, limit, ws.wordoff, ws.cidx,
-                                                   ws.ccount);
+  CompactArgs a{d.L, d.R, d.N, mask, limit, ws.cidx, ws.ccount, ws.uidx, ws.ucount, ws.urows,
+                ws.wordoff};
+  k6_compact<<<d.L * d.R + d.L, kCompactThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_score(const SelDims& d, const uint16_t* keys, const uint16_t* q,
                          const float* head_w, const uint32_t* mask, const int32_t* limit,
                          const SelWorkspace& ws, bool tc, cudaStream_t s) {
-  ScoreArgs a{d.L, d.R, d.Hh, d.N, d.key_stride, keys, q, head_w, mask, limit, ws.wordoff,
-              reinterpret_cast<uint32_t*>(ws.cscore), ws.chi, ws.header};
+  ScoreArgs a{d.L, d.R, d.Hh, d.N, d.key_stride, keys, q, head_w, mask, limit, ws.uidx,
+              ws.ucount, ws.urows, ws.wordoff, reinterpret_cast<uint32_t*>(ws.cscore), ws.chi,
+              ws.header};
   if (!tc) {
     const int RH = d.R * d.Hh;
     const size_t smem = sizeof(float) * ((size_t)RH * 128 + ((RH + 3) & ~3)) +
@@ -745,40 +935,16 @@ cudaError_t launch_score(const SelDims& d, const uint16_t* keys, const uint16_t*
     k5_score<<<d.L * tiles, kScoreThreads, smem, s>>>(a);
     return cudaGetLastError();
   }
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
-  const int RH = d.R * d.Hh;
-  const int nch = (RH + 15) / 16;
-  CUtensorMap tk, tq;
-  {
-    const cuuint64_t dims[3] = {128, (cuuint64_t)d.N, (cuuint64_t)d.L};
-    const cuuint64_t strides[2] = {256, (cuuint64_t)d.key_stride * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(keys), dims, strides,
-            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[2] = {128, (cuuint64_t)d.L * RH};
-    const cuuint64_t strides[1] = {256};
-    const cuuint32_t box[2] = {64, (cuuint32_t)(nch * 16)};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(q), dims, strides,
-            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  const int nch = (d.R * d.Hh + 15) / 16;
   switch (nch) {
-    case 1: return launch_tc<1>(d, tk, tq, a, s);
-    case 2: return launch_tc<2>(d, tk, tq, a, s);
-    case 3: return launch_tc<3>(d, tk, tq, a, s);
-    case 4: return launch_tc<4>(d, tk, tq, a, s);
-    case 5: return launch_tc<5>(d, tk, tq, a, s);
-    case 6: return launch_tc<6>(d, tk, tq, a, s);
-    case 7: return launch_tc<7>(d, tk, tq, a, s);
-    case 8: return launch_tc<8>(d, tk, tq, a, s);
+    case 1: return launch_tc<1>(d, a, s);
+    case 2: return launch_tc<2>(d, a, s);
+    case 3: return launch_tc<3>(d, a, s);
+    case 4: return launch_tc<4>(d, a, s);
+    case 5: return launch_tc<5>(d, a, s);
+    case 6: return launch_tc<6>(d, a, s);
+    case 7: return launch_tc<7>(d, a, s);
+    case 8: return launch_tc<8>(d, a, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -787,9 +953,12 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
                         const float* head_w, int32_t* sel, int32_t* nsel,
                         const SelWorkspace& ws, bool tc, cudaStream_t s) {
   TopkArgs a{d.R, d.Hh, d.N, d.topk, d.key_stride, keys, q, head_w, ws.cidx, ws.ccount,
-             reinterpret_cast<uint32_t*>(ws.cscore), ws.chi, sel, nsel, ws.header, tc ? 1 : 0};
-  const size_t smem = sizeof(int32_t) * kCandCap * 2 + sizeof(float) * (kScoreMaxHeads * 128 + kScoreMaxHeads);
-  cudaError_t err = cudaFuncSetAttribute(k7_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+             ws.uidx, ws.ucount, reinterpret_cast<uint32_t*>(ws.cscore), ws.chi, sel, nsel,
+             ws.header, tc ? 1 : 0};
+  const size_t smem =
+      sizeof(int32_t) * kCandCap * 2 + sizeof(float) * (kScoreMaxHeads * 128 + kScoreMaxHeads);
+  cudaError_t err =
+      cudaFuncSetAttribute(k7_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   k7_topk<<<d.L * d.R, kTopkThreads, smem, s>>>(a);
   return cudaGetLastError();

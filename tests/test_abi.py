@@ -70,6 +70,8 @@ def test_moe_workspace_size_host_only(lib):
     (lambda s: None, 7, 1),
     (lambda s: setattr(s, "hidden", 4010), 6, 1),        # not a multiple of 32
     (lambda s: setattr(s, "inter", 1000), 6, 1),
+    (lambda s: setattr(s, "inter", 1056), 6, 1),         # multiple of 32, not of 64
+    (lambda s: setattr(s.up, "sc", FAKE + 2), 6, 1),     # scales not 4-byte aligned
     (lambda s: setattr(s, "top_k", 0), 6, 1),
     (lambda s: setattr(s, "top_k", 17), 6, 1),
     (lambda s: setattr(s, "n_experts", 4), 6, 1),        # E < k

@@ -245,6 +245,23 @@ def test_down_combine_from_own_h_reproduces_y():
                                           np.zeros_like(out["h"])) == 0)
 
 
+def test_band_checks_accept_exact_and_reject_perturbed():
+    from oracle import compare
+    shape = synth.TINY_MOE
+    d = layer_numpy(synth.moe_layer(shape, seed=8))
+    x = synth.to_numpy_bits(synth.activations(2, shape.H, seed=8))
+    out = oracle.moe_forward(d, x, shape.k, want_h=True)
+    assert compare.h_band_report(out["h"], out["aux"])["ok"]
+    bad = out["h"].copy()
+    bad.reshape(-1)[::97] ^= 0x0040          # flip a mantissa bit in ~1% of elements
+    assert not compare.h_band_report(bad, out["aux"])["ok"]
+    y, yaux = oracle.moe_down_combine(d, shape.k, out["idx"], out["w"], out["h"], want_aux=True)
+    assert compare.y_band_report(y, y, yaux)["ok"]
+    ybad = y.copy()
+    ybad.reshape(-1)[::50] ^= 0x0100          # perturb ~2% of the outputs by 2^-5 or more
+    assert not compare.y_band_report(ybad, y, yaux)["ok"]
+
+
 def test_layer_rows_independent():
     shape = synth.TINY_MOE
     d = layer_numpy(synth.moe_layer(shape, seed=5))
