@@ -29,7 +29,7 @@
 namespace dsmoe {
 namespace {
 
-constexpr int kRouterWarps = 4;
+constexpr int kRouterWarps = 8;
 constexpr int kMmaWarps = 16;
 constexpr int kMmaThreads = kMmaWarps * 32;
 constexpr int kStages = 4;
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     // has many in flight instead of one load -> store round trip at a time.
     const uint4* x8 = reinterpret_cast<const uint4*>(x);
     const int n8 = R * H / 8;
-#pragma unroll 4
+#pragma unroll 8
     for (int i = tid; i < n8; i += blockDim.x) {
       const uint4 v = __ldg(x8 + i);
       float4* d = reinterpret_cast<float4*>(smem_f + 8 * i);
@@ -162,15 +162,16 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.0f;
     const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)e * H);
     const int nc = H / 8;
-    for (int c0 = 0; c0 < nc; c0 += 4 * 32) {
-      uint4 wv[4];
+    // All of a warp's weight loads for up to 4096 values are issued before any use.
+    for (int c0 = 0; c0 < nc; c0 += 16 * 32) {
+      uint4 wv[16];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const int c = c0 + u * 32 + lane;
         wv[u] = c < nc ? __ldcs(wrow + c) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const int c = c0 + u * 32 + lane;
         if (c >= nc) continue;
         const float wf[8] = {bf16_lo(wv[u].x), bf16_hi(wv[u].x), bf16_lo(wv[u].y),
@@ -532,16 +533,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k3_gate_up(GateUpArgs a) {
 }
 
 // ---------------------------------------------------------------------------------
-// K4: down projection + combine. Unit of work = (expert slot u, 16 rows of H), all of K
-// = I. The warp streams the down rows and the expert's h (its rows' slots, in the same
-// ring) and accumulates D[16 rows][8 cols] with mma.sync; it writes fp32 partials per
-// (row, slot). The last unit to finish a 16-row tile (arrival count, no waiting) forms
-//   y = bf16_rne(o_shared + sum_j w_j o_j)   in rank order j.
+// K4: down projection + combine. Unit of work = (expert slot u, 32 rows of H), all of K
+// = I. The warp streams the down rows and the expert's h (its rows' slots) through a
+// 3-stage cp.async ring; each staged h fragment feeds the MMAs of both 16-row halves.
+// It writes fp32 partials per (row, slot); the last unit to finish a 32-row tile
+// (arrival count, no waiting) forms  y = bf16_rne(o_shared + sum_j w_j o_j)  in rank
+// order j.
 // ---------------------------------------------------------------------------------
+constexpr int kDownStages = 3;
+constexpr int kDownRows = 32;
+
 struct DnStage {
-  uint32_t a[4][16][4];      // [block j][row][word]
-  uint32_t s[16][2];         // [row][4 fp16 scales]
-  uint4 b[4][32];            // [block j][lane]: h values 8q..8q+7 of verify row g
+  uint32_t a[4][kDownRows][4];   // [block j][row][word]
+  uint32_t s[kDownRows][2];      // [row][4 fp16 scales]
+  uint4 b[4][32];                // [block j][lane]: h values 8q..8q+7 of verify row g
 };
 
 struct DownArgs {
@@ -551,7 +556,7 @@ struct DownArgs {
   const RouteInfo* route;
   const float* topk_w;
   float* opart;
-  uint32_t* tile_count;      // [H/16]
+  uint32_t* tile_count;      // [H/32]
   uint32_t* unit_counter;
   uint16_t* y;
 };
@@ -561,12 +566,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k4_down(DownArgs a) {
   const int R = a.R, H = a.H, I = a.I, k = a.k;
   const int nb = I >> 5;
   const int T = (nb + 3) >> 2;
-  const int RT = H >> 4;
+  const int RT = H / kDownRows;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
-  DnStage* stages = reinterpret_cast<DnStage*>(smem) + warp * kStages;
-  int* wdesc = reinterpret_cast<int*>(reinterpret_cast<DnStage*>(smem) + kMmaWarps * kStages) +
-               warp * (2 * kStages);
+  DnStage* stages = reinterpret_cast<DnStage*>(smem) + warp * kDownStages;
+  int* wdesc = reinterpret_cast<int*>(reinterpret_cast<DnStage*>(smem) + kMmaWarps * kDownStages) +
+               warp * (2 * kDownStages);
 
   pdl_wait();   // h and the route are complete from here on
   const RouteInfo* rt_info = a.route;
@@ -592,7 +597,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k4_down(DownArgs a) {
         iu = nu;
         it = 0;
         const int u = nu / RT, rti = nu - u * RT;
-        const size_t row0 = (size_t)rti * 16;
+        const size_t row0 = (size_t)rti * kDownRows;
         uint32_t rowmask;
         int slot_g = 0;
         if (u == 0) {
@@ -622,14 +627,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k4_down(DownArgs a) {
       const int blk0 = tile * 4;
       DnStage& S = stages[stage];
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int pp = lane + 32 * h2;
-        const int row = pp & 15, j = pp >> 4;
+      for (int h4 = 0; h4 < 4; ++h4) {
+        const int pp = lane + 32 * h4;
+        const int row = pp & (kDownRows - 1), j = pp >> 5;
         const bool v = blk0 + j < nb;
         cp_async16(&S.a[j][row][0], v ? idq + row * row_qs + (size_t)(blk0 + j) * 16 : idq, v);
       }
-      {
-        const int row = lane >> 1, hf = lane & 1;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int pp = lane + 32 * h2;
+        const int row = pp >> 1, hf = pp & 1;
         const bool v = blk0 + 2 * hf < nb;
         cp_async4(&S.s[row][hf], v ? ids + row * row_sc + blk0 + 2 * hf : ids, v);
       }
@@ -642,16 +649,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k4_down(DownArgs a) {
     cp_async_commit();
   };
 
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[2][4];
 #pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) issue(s);
+  for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[hh][i] = 0.f;
+#pragma unroll
+  for (int s = 0; s < kDownStages - 1; ++s) issue(s);
 
   int cu = -1, u = 0, rti = 0;
   for (int t = 0;; ++t) {
-    issue((t + kStages - 1) % kStages);
-    cp_async_wait<kStages - 1>();
+    issue((t + kDownStages - 1) % kDownStages);
+    cp_async_wait<kDownStages - 1>();
     __syncwarp();
-    const int stage = t % kStages;
+    const int stage = t % kDownStages;
     const int unit = wdesc[2 * stage], tile = wdesc[2 * stage + 1];
     if (unit < 0) break;
     if (unit != cu) {
@@ -661,21 +672,31 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k4_down(DownArgs a) {
     }
     if (tile == 0) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[hh][i] = 0.f;
     }
     const DnStage& S = stages[stage];
     const int blk0 = tile * 4;
-    float s0f[4], s8f[4];
-    widen_scales(*reinterpret_cast<const uint2*>(&S.s[g][0]), s0f);
-    widen_scales(*reinterpret_cast<const uint2*>(&S.s[g + 8][0]), s8f);
+    float sf[2][2][4];   // [half][row g / g+8][block]
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      widen_scales(*reinterpret_cast<const uint2*>(&S.s[hh * 16 + g][0]), sf[hh][0]);
+      widen_scales(*reinterpret_cast<const uint2*>(&S.s[hh * 16 + g + 8][0]), sf[hh][1]);
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (blk0 + j < nb) {
         const uint4 X = pair_order(S.b[j][lane]);
-        float d[4];
-        q4_block_mma(S.a[j][g][q], S.a[j][g + 8][q], X, d);
-        acc[0] = __fmaf_rn(s0f[j], d[0], acc[0]); acc[1] = __fmaf_rn(s0f[j], d[1], acc[1]);
-        acc[2] = __fmaf_rn(s8f[j], d[2], acc[2]); acc[3] = __fmaf_rn(s8f[j], d[3], acc[3]);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float d[4];
+          q4_block_mma(S.a[j][hh * 16 + g][q], S.a[j][hh * 16 + g + 8][q], X, d);
+          acc[hh][0] = __fmaf_rn(sf[hh][0][j], d[0], acc[hh][0]);
+          acc[hh][1] = __fmaf_rn(sf[hh][0][j], d[1], acc[hh][1]);
+          acc[hh][2] = __fmaf_rn(sf[hh][1][j], d[2], acc[hh][2]);
+          acc[hh][3] = __fmaf_rn(sf[hh][1][j], d[3], acc[hh][3]);
+        }
       }
     }
     __syncwarp();
@@ -683,12 +704,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k4_down(DownArgs a) {
     if (tile == T - 1) {
       const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : rt_info->rowmask[u - 1];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int c = 2 * q + (e & 1);
-        const int row = rti * 16 + g + ((e & 2) ? 8 : 0);
-        if (c < R && ((rowmask >> c) & 1u)) {
-          const int slot = (u == 0) ? 0 : rt_info->slot[u - 1][c];
-          a.opart[((size_t)c * (1 + k) + slot) * H + row] = acc[e];
+      for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 2 * q + (e & 1);
+          const int row = rti * kDownRows + hh * 16 + g + ((e & 2) ? 8 : 0);
+          if (c < R && ((rowmask >> c) & 1u)) {
+            const int slot = (u == 0) ? 0 : rt_info->slot[u - 1][c];
+            a.opart[((size_t)c * (1 + k) + slot) * H + row] = acc[hh][e];
+          }
         }
       }
       __threadfence();
@@ -698,8 +722,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k4_down(DownArgs a) {
       prev = __shfl_sync(0xffffffffu, prev, 0);
       if (prev == (unsigned)(n_exp - 1)) {
         __threadfence();
-        for (int idx = lane; idx < R * 16; idx += 32) {
-          const int r = idx >> 4, row = rti * 16 + (idx & 15);
+        for (int idx = lane; idx < R * kDownRows; idx += 32) {
+          const int r = idx / kDownRows, row = rti * kDownRows + (idx % kDownRows);
           const float* orow = a.opart + (size_t)r * (1 + k) * H + row;
           float yv = __ldcg(orow);
           for (int j = 0; j < k; ++j)
@@ -740,7 +764,7 @@ size_t gate_up_smem(const MoeDims& d) {
 }
 
 size_t down_smem() {
-  return sizeof(DnStage) * kMmaWarps * kStages + sizeof(int) * 2 * kStages * kMmaWarps;
+  return sizeof(DnStage) * kMmaWarps * kDownStages + sizeof(int) * 2 * kDownStages * kMmaWarps;
 }
 
 }  // namespace

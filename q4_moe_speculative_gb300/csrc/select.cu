@@ -179,25 +179,45 @@ __global__ void __launch_bounds__(kCompactThreads) k6_compact(CompactArgs a) {
     s_off[tid] = excl;
     if (union_cta && wi < W) a.uwordoff[(size_t)l * W + wi] = excl;
     __syncthreads();
-    for (int qd = warp; qd < kCompactThreads && c0 + qd < W; qd += kCompactThreads / 32) {
-      const int w = c0 + qd;
-      const int b = w * 32 + lane;
-      if (!union_cta) {
-        const bool pred = (b < lim_row) && ((mrow[w] >> lane) & 1u);
-        const uint32_t bal = __ballot_sync(0xffffffffu, pred);
-        if (pred) a.cidx[(size_t)lr * N + s_off[qd] + __popc(bal & ((1u << lane) - 1u))] = b;
-      } else {
+    // Warp `warp` scatters the words c0 + 32*warp .. c0 + 32*warp + 31 of this chunk: lane
+    // j first loads word j's admitted bits (per row for the union), then the words are
+    // taken one by one with the bits broadcast by shuffles (loads all in flight at once).
+    {
+      const int wbase = c0 + warp * 32;
+      const int wl = wbase + lane;
+      uint32_t mine[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) mine[r] = 0u;
+      if (wl < W) {
+        if (union_cta) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            if (r < R) mine[r] = admitted_word(a.mask + ((size_t)l * R + r) * W, wl, s_lim[r]);
+        } else {
+          mine[0] = admitted_word(mrow, wl, lim_row);
+        }
+      }
+      for (int jw = 0; jw < 32 && wbase + jw < W && warp * 32 + jw < kCompactThreads; ++jw) {
+        const int w = wbase + jw;
+        const int b = w * 32 + lane;
         uint32_t rows = 0;
-        for (int r = 0; r < R; ++r) {
-          const uint32_t m = a.mask[((size_t)l * R + r) * W + w];
-          if (b < s_lim[r] && ((m >> lane) & 1u)) rows |= 1u << r;
+        if (union_cta) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            if (r < R && ((__shfl_sync(0xffffffffu, mine[r], jw) >> lane) & 1u)) rows |= 1u << r;
+        } else {
+          rows = (__shfl_sync(0xffffffffu, mine[0], jw) >> lane) & 1u;
         }
         const bool pred = rows != 0;
         const uint32_t bal = __ballot_sync(0xffffffffu, pred);
         if (pred) {
-          const size_t pos = (size_t)l * N + s_off[qd] + __popc(bal & ((1u << lane) - 1u));
-          a.uidx[pos] = b;
-          a.urows[pos] = (uint8_t)rows;
+          const int off = s_off[warp * 32 + jw] + __popc(bal & ((1u << lane) - 1u));
+          if (union_cta) {
+            a.uidx[(size_t)l * N + off] = b;
+            a.urows[(size_t)l * N + off] = (uint8_t)rows;
+          } else {
+            a.cidx[(size_t)lr * N + off] = b;
+          }
         }
       }
     }
@@ -408,14 +428,17 @@ __global__ void __launch_bounds__(kTcThreads) k5_score_tc(ScoreArgs a) {
     const int ucnt = a.ucount[l];
     const uint32_t sbase = stage_addr0 + (uint32_t)stage * kStageBytes;
     const uint8_t* kbase8 = reinterpret_cast<const uint8_t*>(a.keys + (size_t)l * a.key_stride);
-    // keys: warp w copies rows w*32 .. w*32+31, two rows (512 contiguous bytes) per step
-#pragma unroll 4
+    // keys: warp w copies rows w*32 .. w*32+31, two rows (512 contiguous bytes) per step;
+    // the block ids of the warp's 32 rows come from one coalesced load, then shuffles.
+    const int my_e = e0 + warp * 32 + lane;
+    const int my_b = my_e < ucnt ? a.uidx[(size_t)l * N + my_e] : 0;
+#pragma unroll
     for (int jj = 0; jj < 16; ++jj) {
-      const int r = warp * 32 + 2 * jj + (lane >> 4);
+      const int rr = 2 * jj + (lane >> 4);
+      const int r = warp * 32 + rr;
       const int c = lane & 15;
-      const int e = e0 + r;
-      const bool v = e < ucnt;
-      const int b = v ? a.uidx[(size_t)l * N + e] : 0;
+      const bool v = e0 + r < ucnt;
+      const int b = __shfl_sync(0xffffffffu, my_b, rr);
       const uint32_t dst = sbase + (uint32_t)(c >> 3) * (kKeyBytes / 2) + (uint32_t)r * 128u +
                            (uint32_t)(((c & 7) ^ (r & 7)) << 4);
       cp_async16(dst, kbase8 + (size_t)b * 256 + c * 16, v);
@@ -709,12 +732,20 @@ __device__ int ordered_take(int n, int need, Cls cls, Emit emit, int* s_eq, int*
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int beg, end;
   warp_segment(n, &beg, &end);
+  constexpr int U = 8;
   int gt_w = 0, eq_w = 0;
-  for (int i0 = beg; i0 < end; i0 += 32) {
-    const int i = i0 + lane;
-    const int c = i < end ? cls(i) : 0;    // 2 = greater, 1 = equal, 0 = below
-    gt_w += __popc(__ballot_sync(0xffffffffu, c == 2));
-    eq_w += __popc(__ballot_sync(0xffffffffu, c == 1));
+  for (int i0 = beg; i0 < end; i0 += 32 * U) {
+    int c[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * 32 + lane;
+      c[u] = i < end ? cls(i) : 0;        // 2 = greater, 1 = equal, 0 = below
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      gt_w += __popc(__ballot_sync(0xffffffffu, c[u] == 2));
+      eq_w += __popc(__ballot_sync(0xffffffffu, c[u] == 1));
+    }
   }
   if (lane == 0) { s_eq[warp] = eq_w; s_gt[warp] = gt_w; }
   __syncthreads();
@@ -725,16 +756,24 @@ __device__ int ordered_take(int n, int need, Cls cls, Emit emit, int* s_eq, int*
     eq_acc += s_eq[w];
   }
   int pos = my_out, eq_seen = my_eq;
-  for (int i0 = beg; i0 < end; i0 += 32) {
-    const int i = i0 + lane;
-    const int c = i < end ? cls(i) : 0;
-    const uint32_t eqm = __ballot_sync(0xffffffffu, c == 1);
-    const int eq_rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
-    const bool take = (c == 2) || (c == 1 && eq_rank < need);
-    const uint32_t tm = __ballot_sync(0xffffffffu, take);
-    if (take) emit(pos + __popc(tm & ((1u << lane) - 1u)), i);
-    pos += __popc(tm);
-    eq_seen += __popc(eqm);
+  for (int i0 = beg; i0 < end; i0 += 32 * U) {
+    int c[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * 32 + lane;
+      c[u] = i < end ? cls(i) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * 32 + lane;
+      const uint32_t eqm = __ballot_sync(0xffffffffu, c[u] == 1);
+      const int eq_rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
+      const bool take = (c[u] == 2) || (c[u] == 1 && eq_rank < need);
+      const uint32_t tm = __ballot_sync(0xffffffffu, take);
+      if (take) emit(pos + __popc(tm & ((1u << lane) - 1u)), i);
+      pos += __popc(tm);
+      eq_seen += __popc(eqm);
+    }
   }
   __syncthreads();
   return out_acc;
