@@ -133,6 +133,34 @@ ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t
  * reused. Returns (size_t)-1 when the layer or R is invalid. */
 size_t ds_moe_workspace_h_offset(const ds_moe_layer* layer, int32_t R);
 
+/* Bytes of the scratch array that ds_moe_verify_forward_noalloc uses, one per device,
+ * reserved with the library's kernels (16 MiB: the verify layer of hidden 4096, 384
+ * experts, intermediate 1024, top-8 needs 13.2 MiB at R = 6). */
+#define DS_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* ds_moe_verify_forward without a workspace argument, for callers that cannot allocate
+ * device memory at call time: a plain C host loop that embeds one layer and owns no
+ * device allocator, or a server whose device memory is fully committed to a pre-reserved
+ * pool, where a cudaMalloc would fail or synchronise the device in mid-step. The paper
+ * has no counterpart to this call; it computes exactly what ds_moe_verify_forward
+ * computes, with the same kernels, and differs only in where its scratch lives.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library routine): it
+ * runs on a __device__ array of DS_NOALLOC_SCRATCH_BYTES inside the library, one per
+ * device. The first call with a given device current resolves that array's address
+ * (and, under lazy module loading, loads the library's kernels); make that first call
+ * before any stream capture. All calls on a device share the one array: calls whose work
+ * overlaps on the GPU (two streams, two host threads) race on it and give wrong results;
+ * serialise them on one stream. The call clears, on `stream`, every part of the array
+ * that must start at zero, so a previous call's leftovers do not matter.
+ * Arguments, layouts and results as ds_moe_verify_forward; every output buffer is the
+ * caller's. Errors: DS_ERR_WORKSPACE, decided on the host before any CUDA call, when
+ * ds_moe_workspace_size(layer, R) > DS_NOALLOC_SCRATCH_BYTES; DS_ERR_INVALID_ARG when
+ * that size is 0 (invalid layer or R); DS_ERR_CUDA when the array's address cannot be
+ * resolved; otherwise those of ds_moe_verify_forward. */
+ds_status ds_moe_verify_forward_noalloc(const ds_moe_layer* layer, const uint16_t* x,
+                                        int32_t R, uint16_t* y, int32_t* topk_idx,
+                                        float* topk_w, ds_stream_t stream);
+
 /* ------------------------------------------------------------------------------------
  * Block selection for compressed sparse attention (the pages' paragraph "Decode at
  * depth"), batched over L layers and R query rows. For layer l and row r, block b is

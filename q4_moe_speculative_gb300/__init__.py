@@ -141,6 +141,31 @@ def moe_verify_forward(layer: MoeLayer, x: torch.Tensor, *, y=None, topk_idx=Non
     return y, topk_idx, topk_w
 
 
+def moe_verify_forward_noalloc(layer: MoeLayer, x: torch.Tensor, y: torch.Tensor,
+                               topk_idx: torch.Tensor, topk_w: torch.Tensor, *, stream=None):
+    """moe_verify_forward on the library's own per-device scratch array: no workspace and
+    no allocation in the call (every output is the caller's). Calls that overlap on the
+    GPU share the scratch and race. Raises when the layer needs more scratch than
+    DS_NOALLOC_SCRATCH_BYTES."""
+    lib = N.load()
+    R, H = x.shape
+    k = layer.top_k
+    layer.validate()
+    _need(x, "x", torch.bfloat16, (R, layer.hidden))
+    _need(y, "y", torch.bfloat16, (R, H))
+    _need(topk_idx, "topk_idx", torch.int32, (R, k))
+    _need(topk_w, "topk_w", torch.float32, (R, k))
+    st = layer.struct()
+    status = lib.ds_moe_verify_forward_noalloc(st, _ptr(x), R, _ptr(y), _ptr(topk_idx),
+                                               _ptr(topk_w), _stream(stream))
+    if status == N.DS_ERR_WORKSPACE:
+        need = int(lib.ds_moe_workspace_size(st, R))
+        raise RuntimeError(f"ds_moe_verify_forward_noalloc: the layer needs {need} bytes of "
+                           f"scratch at R={R}; the library holds {N.DS_NOALLOC_SCRATCH_BYTES}")
+    _check(status, "ds_moe_verify_forward_noalloc")
+    return y, topk_idx, topk_w
+
+
 def _select_struct(keys, q, head_w, mask, limit, top_k, key_layer_stride=None,
                    canonical: bool = False) -> N.DsSelectArgs:
     L, Nb, D = keys.shape

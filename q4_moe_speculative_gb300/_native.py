@@ -10,6 +10,7 @@ from pathlib import Path
 LIB_PATH = Path(__file__).resolve().parent / "libdsmoe.so"
 
 DS_OK = 0
+DS_ERR_WORKSPACE = 3
 STATUS_NAMES = {
     0: "DS_OK", 1: "DS_ERR_INVALID_ARG", 2: "DS_ERR_UNSUPPORTED", 3: "DS_ERR_WORKSPACE",
     4: "DS_ERR_CUDA", 5: "DS_ERR_TIMEOUT", 6: "DS_ERR_DEVICE_CHECK",
@@ -20,9 +21,11 @@ EXPORTS = (
     "ds_moe_workspace_size", "ds_moe_verify_forward", "ds_select_workspace_size",
     "ds_select_blocks", "ds_workspace_status", "ds_status_string", "ds_version",
     "ds_moe_verify_forward_marked", "ds_select_blocks_marked", "ds_moe_workspace_h_offset",
+    "ds_moe_verify_forward_noalloc",
 )
 
 DS_SELECT_CANONICAL_SCORES = 1
+DS_NOALLOC_SCRATCH_BYTES = 16 << 20  # same value as the C header's macro
 
 
 class DsQ4(C.Structure):
@@ -77,6 +80,10 @@ def load() -> C.CDLL:
     lib.ds_moe_verify_forward_marked.restype = C.c_int
     lib.ds_moe_workspace_h_offset.argtypes = [C.POINTER(DsMoeLayer), C.c_int32]
     lib.ds_moe_workspace_h_offset.restype = C.c_size_t
+    lib.ds_moe_verify_forward_noalloc.argtypes = [
+        C.POINTER(DsMoeLayer), C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
+        C.c_void_p]
+    lib.ds_moe_verify_forward_noalloc.restype = C.c_int
     lib.ds_select_workspace_size.argtypes = [C.POINTER(DsSelectArgs)]
     lib.ds_select_workspace_size.restype = C.c_size_t
     lib.ds_select_blocks.argtypes = [

@@ -136,3 +136,25 @@ def test_select_rejects_half_compacted_outputs_and_small_workspace(lib):
 
 def test_status_query_rejects_null(lib):
     assert lib.ds_workspace_status(None, None) == 1
+
+
+def test_noalloc_scratch_limit_matches_header():
+    from q4_moe_speculative_gb300 import _native as N
+    text = (ROOT / "include" / "dsmoe.h").read_text()
+    m = re.search(r"#define DS_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m, "DS_NOALLOC_SCRATCH_BYTES not found"
+    assert int(m.group(1)) << int(m.group(2)) == N.DS_NOALLOC_SCRATCH_BYTES
+
+
+def test_noalloc_rejects_on_the_host(lib):
+    from q4_moe_speculative_gb300 import _native as N
+    # The verify layer fits the scratch at every R; a larger one is refused before any
+    # CUDA call (this machine may have no GPU at all).
+    for R in range(1, 7):
+        assert 0 < lib.ds_moe_workspace_size(fake_layer(), R) <= N.DS_NOALLOC_SCRATCH_BYTES
+    big = fake_layer(H=8192, I=2048)
+    assert lib.ds_moe_workspace_size(big, 6) > N.DS_NOALLOC_SCRATCH_BYTES
+    assert lib.ds_moe_verify_forward_noalloc(big, FAKE, 6, FAKE, FAKE, FAKE, None) == 3
+    assert lib.ds_moe_verify_forward_noalloc(fake_layer(), FAKE, 0, FAKE, FAKE, FAKE, None) == 1
+    assert lib.ds_moe_verify_forward_noalloc(fake_layer(), FAKE, 7, FAKE, FAKE, FAKE, None) == 1
+    assert lib.ds_moe_verify_forward_noalloc(None, FAKE, 1, FAKE, FAKE, FAKE, None) == 1
