@@ -18,8 +18,9 @@
  * Conventions shared by every call:
  *   - Every pointer argument is DEVICE memory owned by the caller (for instance the
  *     storage of a torch tensor), except the argument structs themselves, which live on
- *     the host and are only read during the call. The library allocates nothing and keeps
- *     no global state; its only state is the header of the caller's workspace.
+ *     the host and are only read during the call. The library allocates nothing; its
+ *     only state is the header of the caller's workspace, and, for
+ *     ds_moe_verify_forward_noalloc alone, one scratch array per device.
  *   - Calls are asynchronous on `stream` and never synchronise the host, except
  *     ds_workspace_status(), which does.
  *   - Arguments are validated on the host before anything is enqueued. A failed check
@@ -75,8 +76,8 @@ typedef struct {
  * down [H][I], and a bf16 router [E][H].
  * Limits of this build: H and I multiples of 64, 64 <= H <= 16384, 64 <= I <= 8192,
  * 1 <= top_k <= 16, top_k <= E <= 1024; the R verify rows are staged in shared memory,
- * R * (2H + 64) bytes, which must fit beside the weight ring (e.g. H <= 6976 at R = 6;
- * otherwise DS_ERR_UNSUPPORTED). */
+ * R * (2H + 64) bytes, which must fit beside the weight stages (e.g. H <= 10880 at
+ * R = 6; otherwise DS_ERR_UNSUPPORTED). */
 typedef struct {
   int32_t hidden;      /* H                                                   */
   int32_t n_experts;   /* E (routed)                                          */
@@ -134,9 +135,9 @@ ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t
 size_t ds_moe_workspace_h_offset(const ds_moe_layer* layer, int32_t R);
 
 /* Bytes of the scratch array that ds_moe_verify_forward_noalloc uses, one per device,
- * reserved with the library's kernels (16 MiB: the verify layer of hidden 4096, 384
- * experts, intermediate 1024, top-8 needs 13.2 MiB at R = 6). */
-#define DS_NOALLOC_SCRATCH_BYTES (16u << 20)
+ * reserved with the library's kernels (4 MiB: the verify layer of hidden 4096, 384
+ * experts, intermediate 1024, top-8 needs 1.0 MiB at R = 6). */
+#define DS_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 /* ds_moe_verify_forward without a workspace argument, for callers that cannot allocate
  * device memory at call time: a plain C host loop that embeds one layer and owns no

@@ -25,7 +25,7 @@ EXPORTS = (
 )
 
 DS_SELECT_CANONICAL_SCORES = 1
-DS_NOALLOC_SCRATCH_BYTES = 16 << 20  # same value as the C header's macro
+DS_NOALLOC_SCRATCH_BYTES = 4 << 20  # same value as the C header's macro
 
 
 class DsQ4(C.Structure):

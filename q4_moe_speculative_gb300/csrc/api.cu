@@ -119,19 +119,16 @@ ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t
   const MoeDims d = dims_of(layer, R);
   const MoeLayout L = moe_layout(d);
   if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return DS_ERR_WORKSPACE;
-  // The verify rows are staged in shared memory: R * (2H + 64) bytes beside the weight ring.
+  // The verify rows are staged in shared memory: R * (2H + 64) bytes beside the weight stages.
   if (gate_up_smem_bytes(d) > (size_t)device_max_smem_optin()) return DS_ERR_UNSUPPORTED;
 
   char* base = static_cast<char*>(workspace);
   MoeWorkspace ws{};
   ws.header = reinterpret_cast<uint32_t*>(base + L.header);
-  ws.tile_count = reinterpret_cast<uint32_t*>(base + L.tile_count);
-  ws.part_count = reinterpret_cast<uint32_t*>(base + L.part_count);
-  ws.logits = reinterpret_cast<float*>(base + L.logits);
+  ws.scores = reinterpret_cast<float*>(base + L.scores);
   ws.route = reinterpret_cast<RouteInfo*>(base + L.route);
   ws.h = reinterpret_cast<uint16_t*>(base + L.h);
   ws.opart = reinterpret_cast<float*>(base + L.opart);
-  ws.part = reinterpret_cast<float*>(base + L.part);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(base, 0, L.zero_bytes, s) != cudaSuccess) return DS_ERR_CUDA;

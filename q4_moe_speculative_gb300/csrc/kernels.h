@@ -30,22 +30,18 @@ struct MoeDims {
 };
 
 struct MoeWorkspace {
-  uint32_t* header;        // WsHeader; words 2 and 3 are the K3 / K4 work counters
-  uint32_t* tile_count;    // K4 arrivals per 16-row tile of H
-  uint32_t* part_count;    // K3 arrivals per (expert slot, 16-row tile of I)
-  float* logits;           // [R][E]
+  uint32_t* header;        // WsHeader: status word, router arrival count
+  float* scores;           // [R][E] sigmoid router scores
   RouteInfo* route;
   uint16_t* h;             // bf16 [R][1+k][I]
-  float* opart;            // [R][1+k][H]
-  float* part;             // K3 partial sums per K part
+  float* opart;            // [R][1+k][H] expert outputs before the combine
 };
 
 struct MoeLayout {
-  size_t header, tile_count, part_count, logits, route, h, opart, part, total, zero_bytes;
+  size_t header, scores, route, h, opart, total, zero_bytes;
 };
 MoeLayout moe_layout(const MoeDims& d);
-int gate_up_kparts(int H);
-// Dynamic shared memory of the gate/up kernel for these sizes (bytes).
+// Least dynamic shared memory the gate/up kernel needs for these sizes (bytes).
 size_t gate_up_smem_bytes(const MoeDims& d);
 
 cudaError_t launch_router(const MoeDims& d, const uint16_t* x, const uint16_t* router_w,

@@ -1,5 +1,5 @@
-// moe.cu — the speculative-verify Q4 MoE layer: router (K1), gate+up+SwiGLU (K3) and
-// down projection with the rank-ordered combine (K4).
+// moe.cu — the speculative-verify Q4 MoE layer: router (K1), gate+up+SwiGLU (K3), down
+// projection (K4) and the rank-ordered combine (K5).
 //
 // Page: "DeepSeek V4.1F Q4 on M3 Ultra with native DSpark MTP (40tps / 800tps)".
 //   paragraph "Decode": the 384-expert router is one dispatch; the shared expert's
@@ -18,21 +18,25 @@
 // block's fp16 scale is applied exactly to that block's two MMAs. Widening a 32-bit word
 // of 8 nibbles costs three shifts, four AND-ORs that put nibbles in the mantissa of the
 // bf16 number 128 + nibble, and four bf16x2 subtractions of 136 (exact q = nibble - 8).
-// Weight tiles stream through a per-warp cp.async ring in shared memory (4 stages), so no
-// register holds data in flight; units of work are taken from a counter (work stealing).
+// Weights reach shared memory as whole row segments of up to 1 KB by 1D bulk copies
+// (long contiguous runs are what HBM serves at full bandwidth), in a ring of CTA-wide
+// stages completed by mbarriers.
 #include <climits>
+#include <cstring>
+#include <mutex>
 #include <utility>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sm100.cuh"
 
 namespace dsmoe {
 namespace {
 
+using namespace sm100;
+
 constexpr int kRouterWarps = 8;
-constexpr int kMmaWarps = 16;
-constexpr int kMmaThreads = kMmaWarps * 32;
-constexpr int kStages = 4;
+constexpr uint32_t kWaitPolls = 1u << 20;   // bounded mbarrier waits (~1 s)
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -66,6 +70,15 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// The mbarrier receives one arrival once all of this thread's earlier cp.async copies have
+// landed; the arrival is counted in the barrier's initial count (noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(const uint8_t* p) {
+  return *reinterpret_cast<const uint32_t*>(p);
 }
 
 // bf16 pair (q_lo, q_hi) of the nibbles at bits 0-3 and 16-19 of w: (w & 0x000F000F) |
@@ -126,9 +139,9 @@ __device__ __forceinline__ void widen_scales(uint2 s, float (&f)[4]) {
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kRouterWarps * 32)
     k1_router(const uint16_t* __restrict__ x, int R, int H, const uint16_t* __restrict__ wr,
-              int E, int k, float* __restrict__ logits, int32_t* __restrict__ topk_idx,
+              int E, int k, float* __restrict__ scores, int32_t* __restrict__ topk_idx,
               float* __restrict__ topk_w, RouteInfo* __restrict__ route, WsHeader* hdr) {
-  extern __shared__ float smem_f[];  // x as fp32 [R][H]; then sigmoid scores [R][E]
+  extern __shared__ float smem_f[];  // x as fp32 [R][H]
   __shared__ int s_is_last;
   __shared__ int32_t sel_e[kMaxRows][kMaxTopK];
   __shared__ float sel_s[kMaxRows][kMaxTopK];
@@ -196,7 +209,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     for (int r = 0; r < kMaxRows; ++r) {
       if (r < R) {
         const float z = warp_sum(acc[r]);
-        if (lane == 0) logits[r * E + e] = z;
+        if (lane == 0) scores[r * E + e] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
       }
     }
   }
@@ -212,36 +225,44 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   if (!s_is_last) return;
   __threadfence();
 
-  float* s_sm = smem_f;  // [R][E] sigmoid scores
-  for (int i = tid; i < R * E; i += blockDim.x) {
-    const float z = __ldcg(logits + i);
-    s_sm[i] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
-  }
   if (tid < kMaxExperts / 32) ubits[tid] = 0u;
-  __syncthreads();
-
-  for (int r = warp; r < R; r += kRouterWarps) {
-    float* sr = s_sm + r * E;
+  // Warp r selects row r's top k. Its scores sit in registers, 32 experts per lane
+  // round; all loads of a row are issued before the first comparison.
+  if (warp < R) {
+    const int r = warp;
+    constexpr int kPer = kMaxExperts / 32;
+    float v[kPer];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e2 = i * 32 + lane;
+      const float sv = e2 < E ? __ldcg(scores + r * E + e2) : -1.0f;
+      // sigmoid scores lie in [0, 1]; a NaN (from NaN inputs) ranks below every score
+      bad |= (e2 < E) && !(sv >= 0.0f);
+      v[i] = (e2 >= E || sv >= 0.0f) ? sv : -0.5f;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(&hdr->status, kStatusCheck);
     for (int j = 0; j < k; ++j) {
       float best = -1.0f;
       int bi = INT_MAX;
-      for (int e2 = lane; e2 < E; e2 += 32) {
-        const float v = sr[e2];
-        if (v > best) { best = v; bi = e2; }
-      }
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        if (v[i] > best) { best = v[i]; bi = i * 32 + lane; }   // lower index wins ties
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, best, o);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
         if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
       }
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        if (i * 32 + lane == bi) v[i] = -1.0f;   // taken
       if (lane == 0) {
         sel_e[r][j] = bi;
         sel_s[r][j] = best;
-        sr[bi] = -1.0f;  // taken (scores are >= 0)
       }
-      __syncwarp();
     }
+    __syncwarp();
     if (lane == 0) {
       float sum = sel_s[r][0];
       for (int j = 1; j < k; ++j) sum = __fadd_rn(sum, sel_s[r][j]);
@@ -302,48 +323,138 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 }
 
 // ---------------------------------------------------------------------------------
-// K3: gate + up + SwiGLU. Unit of work = (expert slot u, 16 rows of I, one of KP parts of
-// K); expert slot 0 is the shared expert (all rows), slot u >= 1 the u-th expert of the
-// union (its rows). A warp streams its unit's gate and up rows in tiles of 4 Q4 blocks
-// through its cp.async ring and accumulates D[16 rows][8 cols] with mma.sync; the
-// activations sit in shared memory as bf16 in MMA pair order (staged once per CTA).
-// The last of the KP parts to arrive (atomic count) adds the parts in a fixed order and
-// writes h = bf16_rne(silu(g) * u) for the expert's rows.
+// Weight streaming for K3 and K4. A CTA has 16 consumer warps and one producer warp; a
+// ring of stages in shared memory is handed over with "full" and "empty" mbarriers, so
+// the copies of the next stages are always in flight while the consumers compute. HBM
+// serves long contiguous runs at full bandwidth and every copy operation has a fixed
+// cost, so a stage is a few large copies of whole row segments of consecutive rows:
+//  * boxed path (rows a multiple of 128 bytes, i.e. K a multiple of 256): the nibbles of
+//    the stage's rows arrive as ONE TMA box per matrix over the view [128-byte chunk][row]
+//    [128 bytes] with the 128-byte swizzle (granule j of row r stored at j ^ (r & 7), so
+//    the MMA fragment reads are free of bank conflicts), and the fp16 scales as one 2D
+//    TMA box per matrix;
+//  * row path (other sizes): one 1D bulk copy per row segment into a row padded by 16
+//    bytes, and the scales in 4-byte cp.async pieces.
+// Work is assigned statically, so the split depends only on the sizes.
 // ---------------------------------------------------------------------------------
-struct GuStage {
-  uint32_t a[2][4][16][4];   // [gate/up][block j][row][word]
-  uint32_t s[2][16][2];      // [gate/up][row][4 fp16 scales]
-};
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kMmaThreads = kConsumers + 32;            // + producer warp
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kChunkBlocks = 128;                       // Q4 blocks per row per stage (at most)
+constexpr int kMaxRing = 4;
+constexpr uint32_t kFullArrivals = 1 + 32;              // expect_tx + the producer's lanes
+constexpr int kConsumerBarrier = 1;                     // named barrier id of the consumers
 
-struct GateUpArgs {
-  const uint16_t* x;
-  int R, H, I, k;
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t a = smem_addr(p);
+  return p + (((a + 1023u) & ~1023u) - a);
+}
+
+__host__ __device__ constexpr size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// 1D bulk copy global -> shared of `bytes` (multiple of 16, both addresses 16-aligned).
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kConsumerBarrier), "n"(kConsumers) : "memory");
+}
+
+// Row path: `rows` rows of `cb` blocks (nibbles and scales; row strides `row_qs` bytes /
+// `nb` halves) into padded shared rows; called by all 32 producer lanes.
+__device__ __forceinline__ void copy_rows(uint8_t* qdst, int qpitch, const uint8_t* qsrc,
+                                          size_t row_qs, uint8_t* sdst, int spitch,
+                                          const uint16_t* ssrc, int nb, int rows, int cb,
+                                          uint64_t* bar, int lane) {
+  for (int r = lane; r < rows; r += 32)
+    bulk_copy(qdst + r * qpitch, qsrc + (size_t)r * row_qs, (uint32_t)cb * 16, bar);
+  const int per_row = cb >> 1;
+  for (int p = lane; p < rows * per_row; p += 32) {
+    const int r = p / per_row, pp = p - r * per_row;
+    cp_async4(sdst + r * spitch + pp * 4, ssrc + (size_t)r * nb + 2 * pp, true);
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// K3: gate + up + SwiGLU. A unit is (expert slot u, 16 rows of I): slot 0 is the shared
+// expert (all rows), slot u >= 1 the u-th expert of the union (its rows). CTA b takes
+// units b, b + G, b + 2G, ... (G = grid). A stage is one K chunk of a unit (the gate and
+// up rows' segments of up to 16 WB blocks); consumer warp w computes blocks WB w ..
+// WB w + WB - 1 of the chunk for both matrices and keeps its partial sums across the
+// unit's chunks. At the end of a unit the 16 warps' partials meet in shared memory and
+// are added in warp order; h = bf16_rne(silu(g) * u) is written for the expert's rows.
+// The activations sit in shared memory as bf16 in MMA pair order, staged once per CTA
+// while the router runs. The producer starts on the shared expert's units before the
+// router's results exist.
+// ---------------------------------------------------------------------------------
+// Stage geometry for WB blocks per warp (a chunk of 16 WB blocks per row): WB = 8 when
+// the stages fit beside the staged activations, else 4.
+template <int WB>
+struct GuGeom {
+  static constexpr int kCB = 16 * WB;                            // blocks per chunk
+  static constexpr int kQsPitch = kCB * 16 + 16;                 // row path: 2064 / 1040
+  static constexpr int kScPitch = kCB * 2 + 16;                  // row path: 272 / 144
+  static constexpr int kRowQs = 2 * 16 * kQsPitch;               // row path: nibble bytes
+  static constexpr int kBoxQs = 16 * kCB * 16;                   // boxed: one matrix
+  static constexpr int kBoxSc = 16 * kCB * 2;                    // boxed: one matrix
+  static constexpr int kStage = (int)round_up((size_t)kRowQs + 2 * 16 * kScPitch, 1024);
+};
+constexpr int kXPad = 64;                                  // staged activation row pad
+
+struct alignas(64) GateUpArgs {
+  CUtensorMap wq[4];   // boxed path: nibbles of gate, up, sh_gate, sh_up
+  CUtensorMap wsc[4];  // boxed path: their scales
   Q4Ptr gate, up, sh_gate, sh_up;
+  const uint16_t* x;
   const RouteInfo* route;
   uint16_t* h;
-  float* part;               // [(1+R*k) * (I/16) * KP][32 lanes][8]
-  uint32_t* part_count;      // [(1+R*k) * (I/16)]
-  uint32_t* unit_counter;
+  uint32_t* status;
+  int R, H, I, k, ring, boxed;
 };
 
+__host__ __device__ constexpr size_t gu_red_bytes(int R) {
+  return 2ull * kConsumerWarps * 2 * 16 * (size_t)R * 4;
+}
 
-__global__ void __launch_bounds__(kMmaThreads, 1) k3_gate_up(GateUpArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int R = a.R, H = a.H, I = a.I, k = a.k;
-  const int nb = H >> 5;                        // Q4 blocks per row
-  const int T = (nb + 3) >> 2;                  // tiles of 4 blocks
-  const int TP = (T + 3) >> 2;                  // tiles per K part
-  const int KP = (T + TP - 1) / TP;             // K parts (<= 4)
-  const int RT = I >> 4;                        // 16-row tiles
-  const int xstride = H * 2 + 64;               // bytes per staged activation row
+template <int WB>
+__global__ void __launch_bounds__(kMmaThreads, 1) k3_gate_up(const __grid_constant__ GateUpArgs a) {
+  using Geo = GuGeom<WB>;
+  constexpr int kCB = Geo::kCB, kStage = Geo::kStage;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int R = a.R, H = a.H, I = a.I, k = a.k, ring = a.ring;
+  const bool boxed = a.boxed != 0;
+  const int nb = H >> 5;                          // Q4 blocks per row
+  const int KC = (nb + kCB - 1) / kCB;
+  const int RT = I >> 4;
+  const int xstride = 2 * H + kXPad;
+  const size_t row_qs = (size_t)H / 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
 
-  uint8_t* xs = smem;
-  GuStage* stages = reinterpret_cast<GuStage*>(smem + ((R * xstride + 127) & ~127)) + warp * kStages;
-  int* wdesc = reinterpret_cast<int*>(reinterpret_cast<GuStage*>(smem + ((R * xstride + 127) & ~127)) +
-                                      kMmaWarps * kStages) + warp * (2 * kStages);
+  uint8_t* stages = smem;
+  float* red = reinterpret_cast<float*>(smem + (size_t)ring * kStage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)ring * kStage + gu_red_bytes(R));
+  uint64_t* empty = full + kMaxRing;
+  uint8_t* xs = smem + (size_t)ring * kStage + gu_red_bytes(R) + 64;
 
+  if (tid == 0) {
+    for (int s = 0; s < ring; ++s) {
+      mbar_init(&full[s], kFullArrivals);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+    if (boxed)
+      for (int i = 0; i < 4; ++i) { prefetch_tensormap(&a.wq[i]); prefetch_tensormap(&a.wsc[i]); }
+  }
   // Activations -> shared memory, bf16 in MMA pair order (independent of the router).
 #pragma unroll 4
   for (int i = tid; i < R * (H >> 3); i += blockDim.x) {
@@ -352,388 +463,397 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k3_gate_up(GateUpArgs a) {
     *reinterpret_cast<uint4*>(xs + r * xstride + (grp >> 2) * 64 + (grp & 3) * 16) = pair_order(v);
   }
   __syncthreads();
-  pdl_wait();   // the route produced by the router grid is visible from here on
 
-  const RouteInfo* rt_info = a.route;
-  const int n_union = rt_info->n_union;
-  const int n_units = (1 + n_union) * RT * KP;
-  const size_t row_qs = (size_t)H / 2, row_sc = (size_t)nb;
-
-  // Issue cursor (warp-uniform). A unit is decoded once, when the warp takes it; each
-  // further tile only advances the source pointers.
-  int iu = -1, it = 0, itiles = 0, iblk = 0;
-  bool exhausted = false;
-  const uint8_t *igq = nullptr, *iuq = nullptr;
-  const uint16_t *igs = nullptr, *ius = nullptr;
-
-  auto issue = [&](int stage) {
-    int unit = -1, tile = 0;
-    if (!exhausted && (iu < 0 || it >= itiles)) {
-      int nu = 0;
-      if (lane == 0) nu = (int)atomicAdd(a.unit_counter, 1u);
-      nu = __shfl_sync(0xffffffffu, nu, 0);
-      if (nu >= n_units) {
-        exhausted = true;
-      } else {
-        iu = nu;
-        it = 0;
-        const int u = nu / (RT * KP);
-        const int rem = nu - u * RT * KP;
-        const int rti = rem / KP, kp = rem - rti * KP;
-        itiles = min(TP, T - kp * TP);
-        iblk = kp * TP * 4;
-        const size_t row0 = (size_t)rti * 16;
-        if (u == 0) {
-          igq = a.sh_gate.qs + row0 * row_qs; iuq = a.sh_up.qs + row0 * row_qs;
-          igs = a.sh_gate.sc + row0 * row_sc; ius = a.sh_up.sc + row0 * row_sc;
-        } else {
-          const size_t e = (size_t)rt_info->expert[u - 1];
-          igq = a.gate.qs + (e * I + row0) * row_qs; iuq = a.up.qs + (e * I + row0) * row_qs;
-          igs = a.gate.sc + (e * I + row0) * row_sc; ius = a.up.sc + (e * I + row0) * row_sc;
-        }
-      }
-    }
-    if (!exhausted) {
-      unit = iu;
-      tile = it++;
-    }
-    if (lane == 0) {
-      wdesc[2 * stage] = unit;
-      wdesc[2 * stage + 1] = tile;
-    }
-    if (unit >= 0) {
-      const int blk0 = iblk + tile * 4;
-      GuStage& S = stages[stage];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int pp = lane + 32 * h2;
-        const int row = pp & 15, j = pp >> 4;
-        const bool v = blk0 + j < nb;
-        const size_t off = row * row_qs + (size_t)(blk0 + j) * 16;
-        cp_async16(&S.a[0][j][row][0], v ? igq + off : igq, v);
-        cp_async16(&S.a[1][j][row][0], v ? iuq + off : iuq, v);
-      }
-      {
-        const int row = lane >> 1, hf = lane & 1;
-        const bool v = blk0 + 2 * hf < nb;
-        const size_t off = row * row_sc + blk0 + 2 * hf;
-        cp_async4(&S.s[0][row][hf], v ? igs + off : igs, v);
-        cp_async4(&S.s[1][row][hf], v ? ius + off : ius, v);
-      }
-    }
-    cp_async_commit();
-  };
-
-  float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) issue(s);
-
-  // Compute cursor: the unit of the tile being computed, decoded once per unit.
-  int cu = -1, u = 0, rti = 0, kp = 0, tiles = 0;
-  uint32_t rowmask = 0;
-  bool member = false;
-  for (int t = 0;; ++t) {
-    issue((t + kStages - 1) % kStages);
-    cp_async_wait<kStages - 1>();
-    __syncwarp();
-    const int stage = t % kStages;
-    const int unit = wdesc[2 * stage], tile = wdesc[2 * stage + 1];
-    if (unit < 0) break;
-    if (unit != cu) {
-      cu = unit;
-      u = unit / (RT * KP);
-      const int rem = unit - u * RT * KP;
-      rti = rem / KP;
-      kp = rem - rti * KP;
-      tiles = min(TP, T - kp * TP);
-      rowmask = (u == 0) ? ((1u << R) - 1u) : rt_info->rowmask[u - 1];
-      member = (g < R) && ((rowmask >> g) & 1u);
-    }
-    if (tile == 0) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) { ag[i] = 0.f; au[i] = 0.f; }
-    }
-    const GuStage& S = stages[stage];
-    const int blk0 = (kp * TP + tile) * 4;
-    // fp16 scales of this lane's rows g and g+8 for the tile's 4 blocks, widened once
-    const uint2 sgv0 = *reinterpret_cast<const uint2*>(&S.s[0][g][0]);
-    const uint2 sgv8 = *reinterpret_cast<const uint2*>(&S.s[0][g + 8][0]);
-    const uint2 suv0 = *reinterpret_cast<const uint2*>(&S.s[1][g][0]);
-    const uint2 suv8 = *reinterpret_cast<const uint2*>(&S.s[1][g + 8][0]);
-    float sg0[4], sg8[4], su0[4], su8[4];
-    widen_scales(sgv0, sg0); widen_scales(sgv8, sg8);
-    widen_scales(suv0, su0); widen_scales(suv8, su8);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int blk = blk0 + j;
-      if (blk < nb) {
-        const uint4 X = member ? *reinterpret_cast<const uint4*>(xs + g * xstride + blk * 64 + q * 16)
-                               : make_uint4(0, 0, 0, 0);
-        float d[4];
-        q4_block_mma(S.a[0][j][g][q], S.a[0][j][g + 8][q], X, d);
-        ag[0] = __fmaf_rn(sg0[j], d[0], ag[0]); ag[1] = __fmaf_rn(sg0[j], d[1], ag[1]);
-        ag[2] = __fmaf_rn(sg8[j], d[2], ag[2]); ag[3] = __fmaf_rn(sg8[j], d[3], ag[3]);
-        q4_block_mma(S.a[1][j][g][q], S.a[1][j][g + 8][q], X, d);
-        au[0] = __fmaf_rn(su0[j], d[0], au[0]); au[1] = __fmaf_rn(su0[j], d[1], au[1]);
-        au[2] = __fmaf_rn(su8[j], d[2], au[2]); au[3] = __fmaf_rn(su8[j], d[3], au[3]);
-      }
-    }
-    __syncwarp();
-
-    if (tile == tiles - 1) {
-      // All K parts of (u, row tile) in a fixed order, then the SwiGLU epilogue.
-      float sg[4], su[4];
-      bool last = true;
-      const int ut = u * RT + rti;
-      if (KP > 1) {
-        float* mine = a.part + ((size_t)ut * KP + kp) * 256 + lane * 8;
-        *reinterpret_cast<float4*>(mine) = make_float4(ag[0], ag[1], ag[2], ag[3]);
-        *reinterpret_cast<float4*>(mine + 4) = make_float4(au[0], au[1], au[2], au[3]);
-        __threadfence();
-        __syncwarp();
-        unsigned prev = 0;
-        if (lane == 0) prev = atomicAdd(a.part_count + ut, 1u);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        last = (prev == (unsigned)(KP - 1));
-        if (last) {
-          __threadfence();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) { sg[i] = 0.f; su[i] = 0.f; }
-          for (int p = 0; p < KP; ++p) {
-            const float* src = a.part + ((size_t)ut * KP + p) * 256 + lane * 8;
-            const float4 g4 = __ldcg(reinterpret_cast<const float4*>(src));
-            const float4 u4 = __ldcg(reinterpret_cast<const float4*>(src + 4));
-            sg[0] = __fadd_rn(sg[0], g4.x); sg[1] = __fadd_rn(sg[1], g4.y);
-            sg[2] = __fadd_rn(sg[2], g4.z); sg[3] = __fadd_rn(sg[3], g4.w);
-            su[0] = __fadd_rn(su[0], u4.x); su[1] = __fadd_rn(su[1], u4.y);
-            su[2] = __fadd_rn(su[2], u4.z); su[3] = __fadd_rn(su[3], u4.w);
+  const int G = gridDim.x;
+  bool timed_out = false;
+  if (warp == kProducerWarp) {
+    bool routed = false;   // the router's results are known to be visible
+    // Units of the shared expert need nothing from the router; a unit of a routed expert
+    // waits for it (and so does the count of units, which needs the union size).
+    for (int f = 0;; ++f) {
+      const int n = (int)blockIdx.x + (f / KC) * G, c = f % KC;
+      const int u = n / RT, rti = n - u * RT;
+      if (u > 0 && !routed) { pdl_wait(); routed = true; }
+      if (routed && n >= (1 + a.route->n_union) * RT) break;
+      const int slot = f % ring;
+      if (f >= ring && !mbar_wait(&empty[slot], ((f / ring) - 1) & 1, kWaitPolls)) timed_out = true;
+      uint8_t* st = stages + (size_t)slot * kStage;
+      const int row0 = (u == 0 ? 0 : a.route->expert[u - 1] * I) + rti * 16;
+      if (boxed) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[slot], 2u * (Geo::kBoxQs + Geo::kBoxSc));
+          const int mi = u == 0 ? 2 : 0;
+          for (int m = 0; m < 2; ++m) {
+            tma_load_3d(st + m * Geo::kBoxQs, &a.wq[mi + m], 0, row0, c * (kCB / 8), &full[slot]);
+            tma_load_2d(st + 2 * Geo::kBoxQs + m * Geo::kBoxSc, &a.wsc[mi + m], c * kCB, row0,
+                        &full[slot]);
           }
         }
       } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) { sg[i] = ag[i]; su[i] = au[i]; }
+        const Q4Ptr mg = u == 0 ? a.sh_gate : a.gate, mu = u == 0 ? a.sh_up : a.up;
+        const int cb = min(kCB, nb - c * kCB);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * 16u * cb * 16u);
+        for (int m = 0; m < 2; ++m) {
+          const Q4Ptr mm = m ? mu : mg;
+          copy_rows(st + m * 16 * Geo::kQsPitch, Geo::kQsPitch,
+                    mm.qs + (size_t)row0 * row_qs + (size_t)c * kCB * 16, row_qs,
+                    st + Geo::kRowQs + m * 16 * Geo::kScPitch, Geo::kScPitch,
+                    mm.sc + (size_t)row0 * nb + c * kCB, nb, 16, cb, &full[slot], lane);
+        }
       }
-      if (last) {
+      cp_async_mbar_arrive(&full[slot]);
+    }
+    if (!routed) pdl_wait();
+  } else {
+    pdl_wait();      // the route produced by the router grid is visible from here on
+    const RouteInfo* rt = a.route;
+    const int n_units = (1 + rt->n_union) * RT;
+    const int n_mine = (int)blockIdx.x < n_units ? (n_units - (int)blockIdx.x + G - 1) / G : 0;
+    const int total = n_mine * KC;
+    const uint8_t* xrow = xs + min(g, R - 1) * xstride + q * 16;   // rows >= R: any finite row
+    // Byte offsets inside a stage (row g of the gate matrix; + m_q for up, + r8_q for row
+    // g + 8) of word q of this warp's block j, and of this warp's scales.
+    int woff[WB];
+    int m_q, r8_q, soff, m_s, r8_s;
+    if (boxed) {
+#pragma unroll
+      for (int j = 0; j < WB; ++j) {
+        const int b = WB * warp + j;
+        woff[j] = ((b >> 3) * 16 + g) * 128 + (((b & 7) ^ (g & 7)) << 4) + q * 4;
+      }
+      m_q = Geo::kBoxQs; r8_q = 8 * 128;
+      soff = 2 * Geo::kBoxQs + g * (kCB * 2) + warp * (2 * WB);
+      m_s = Geo::kBoxSc; r8_s = 8 * kCB * 2;
+    } else {
+#pragma unroll
+      for (int j = 0; j < WB; ++j) woff[j] = g * Geo::kQsPitch + (WB * warp + j) * 16 + q * 4;
+      m_q = 16 * Geo::kQsPitch; r8_q = 8 * Geo::kQsPitch;
+      soff = Geo::kRowQs + g * Geo::kScPitch + warp * (2 * WB);
+      m_s = 16 * Geo::kScPitch; r8_s = 8 * Geo::kScPitch;
+    }
+    float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
+    int buf = 0;
+    for (int f = 0; f < total; ++f) {
+      const int slot = f % ring;
+      if (!mbar_wait(&full[slot], (f / ring) & 1, kWaitPolls)) timed_out = true;
+      const uint8_t* st = stages + (size_t)slot * kStage;
+      const int c = f % KC;
+      const int cb = min(kCB, nb - c * kCB);
+      const int nv = max(0, min(WB, cb - WB * warp));   // this warp's blocks in the chunk
+      if (nv > 0) {
+        // fp16 scales of rows g, g + 8 (gate, up) for the warp's WB blocks
+        uint32_t sw[4][WB / 2];
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+          const uint8_t* p = st + soff + (m4 >> 1) * m_s + (m4 & 1) * r8_s;
+          if constexpr (WB == 8) {
+            const uint4 v = *reinterpret_cast<const uint4*>(p);
+            sw[m4][0] = v.x; sw[m4][1] = v.y; sw[m4][2] = v.z; sw[m4][3] = v.w;
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(p);
+            sw[m4][0] = v.x; sw[m4][1] = v.y;
+          }
+        }
+        const uint8_t* xb = xrow + (c * kCB + WB * warp) * 64;
+#pragma unroll
+        for (int jp = 0; jp < WB / 2; ++jp) {
+          const float2 sg0 = __half22float2(*reinterpret_cast<const __half2*>(&sw[0][jp]));
+          const float2 sg8 = __half22float2(*reinterpret_cast<const __half2*>(&sw[1][jp]));
+          const float2 su0 = __half22float2(*reinterpret_cast<const __half2*>(&sw[2][jp]));
+          const float2 su8 = __half22float2(*reinterpret_cast<const __half2*>(&sw[3][jp]));
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int j = 2 * jp + e2;
+            if (j < nv) {
+              const float g0 = e2 ? sg0.y : sg0.x, g8 = e2 ? sg8.y : sg8.x;
+              const float u0 = e2 ? su0.y : su0.x, u8 = e2 ? su8.y : su8.x;
+              const uint4 X = *reinterpret_cast<const uint4*>(xb + j * 64);
+              const uint8_t* w = st + woff[j];
+              float d[4];
+              q4_block_mma(lds32(w), lds32(w + r8_q), X, d);
+              ag[0] = __fmaf_rn(g0, d[0], ag[0]); ag[1] = __fmaf_rn(g0, d[1], ag[1]);
+              ag[2] = __fmaf_rn(g8, d[2], ag[2]); ag[3] = __fmaf_rn(g8, d[3], ag[3]);
+              q4_block_mma(lds32(w + m_q), lds32(w + m_q + r8_q), X, d);
+              au[0] = __fmaf_rn(u0, d[0], au[0]); au[1] = __fmaf_rn(u0, d[1], au[1]);
+              au[2] = __fmaf_rn(u8, d[2], au[2]); au[3] = __fmaf_rn(u8, d[3], au[3]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the slot
+      if (c == KC - 1) {
+        float* rb = red + (size_t)buf * kConsumerWarps * 2 * 16 * R;
+        // partials [warp][gate/up][row][col], cols < R only
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int c = 2 * q + (e & 1);
-          const int row = rti * 16 + g + ((e & 2) ? 8 : 0);
-          if (c < R && ((rowmask >> c) & 1u)) {
-            const int slot = (u == 0) ? 0 : rt_info->slot[u - 1][c];
-            const float gv = sg[e];
-            const float silu = __fdiv_rn(gv, __fadd_rn(1.0f, expf(-gv)));
-            a.h[((size_t)c * (1 + k) + slot) * I + row] = f32_to_bf16_rne(__fmul_rn(silu, su[e]));
+          const int col = 2 * q + (e & 1), row = g + ((e & 2) ? 8 : 0);
+          if (col < R) {
+            rb[((warp * 2 + 0) * 16 + row) * R + col] = ag[e];
+            rb[((warp * 2 + 1) * 16 + row) * R + col] = au[e];
+          }
+          ag[e] = 0.f;
+          au[e] = 0.f;
+        }
+        consumer_sync();
+        const int n = (int)blockIdx.x + (f / KC) * G;
+        const int u = n / RT, rti = n - u * RT;
+        if (tid < 16 * R) {
+          const int row = tid / R, col = tid - row * R;
+          const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : rt->rowmask[u - 1];
+          if ((rowmask >> col) & 1u) {
+            float gs = 0.f, us = 0.f;
+            for (int w = 0; w < kConsumerWarps; ++w) {
+              gs = __fadd_rn(gs, rb[((w * 2 + 0) * 16 + row) * R + col]);
+              us = __fadd_rn(us, rb[((w * 2 + 1) * 16 + row) * R + col]);
+            }
+            const int slot_c = (u == 0) ? 0 : rt->slot[u - 1][col];
+            const float silu = __fdiv_rn(gs, __fadd_rn(1.0f, expf(-gs)));
+            a.h[((size_t)col * (1 + k) + slot_c) * I + rti * 16 + row] =
+                f32_to_bf16_rne(__fmul_rn(silu, us));
           }
         }
+        buf ^= 1;
       }
     }
   }
-  cp_async_wait<0>();
-  pdl_trigger();
+  pdl_trigger();   // the down projection may be scheduled as CTAs of this grid retire
+  if (timed_out && lane == 0) flag_status(a.status, kStatusTimeout);
 }
 
 // ---------------------------------------------------------------------------------
-// K4: down projection + combine. Unit of work = (expert slot u, 32 rows of H), all of K
-// = I. The warp streams the down rows and the expert's h (its rows' slots) through a
-// 3-stage cp.async ring; each staged h fragment feeds the MMAs of both 16-row halves.
-// It writes fp32 partials per (row, slot); the last unit to finish a 32-row tile
-// (arrival count, no waiting) forms  y = bf16_rne(o_shared + sum_j w_j o_j)  in rank
-// order j.
+// K4: down projection. A unit is (expert slot u, a group of RS consecutive rows of H);
+// the 16 consumer warps split a stage (one K chunk of up to 4096 values of the group's
+// rows) into RS/16 row tiles x WK K slices of 8 blocks. CTA b takes a contiguous range of
+// units, so consecutive stages mostly belong to one expert and its h (the B operand, kept
+// in shared memory) is reloaded only when the expert or the chunk changes. The WK slice
+// partials of a row tile are added in slice order and written to o[row][slot] (fp32);
+// K5 combines. The weights do not depend on the gate/up kernel, so the producer starts
+// streaming them before that kernel has finished; only h waits for it.
 // ---------------------------------------------------------------------------------
-constexpr int kDownStages = 3;
-constexpr int kDownRows = 32;
-
-struct DnStage {
-  uint32_t a[4][kDownRows][4];   // [block j][row][word]
-  uint32_t s[kDownRows][2];      // [row][4 fp16 scales]
-  uint4 b[4][32];                // [block j][lane]: h values 8q..8q+7 of verify row g
+struct DownGeom {
+  int nb, KC, cbmax, WK, TPS, RS, NGR, qs_pitch, sc_pitch, h_pitch, stage_bytes, boxed;
 };
 
-struct DownArgs {
-  const uint16_t* h;
-  int R, H, I, k;
+__host__ __device__ inline DownGeom down_geom(int H, int I) {
+  DownGeom d{};
+  d.nb = I >> 5;
+  d.KC = (d.nb + kChunkBlocks - 1) / kChunkBlocks;
+  d.cbmax = d.nb < kChunkBlocks ? d.nb : kChunkBlocks;
+  const int slices = (d.cbmax + 7) / 8;
+  d.WK = slices <= 1 ? 1 : (slices <= 2 ? 2 : (slices <= 4 ? 4 : (slices <= 8 ? 8 : 16)));
+  d.TPS = kConsumerWarps / d.WK;
+  d.RS = 16 * d.TPS;
+  d.NGR = (H + d.RS - 1) / d.RS;
+  d.boxed = (d.nb % 8) == 0;            // rows of whole 128-byte chunks (and scale rows of 16 B)
+  d.qs_pitch = d.cbmax * 16 + 16;       // row path
+  d.sc_pitch = (int)round_up((size_t)d.cbmax * 2, 16) + 16;
+  d.h_pitch = d.cbmax * 64 + 64;
+  d.stage_bytes = (int)round_up((size_t)d.RS * (d.qs_pitch + d.sc_pitch), 1024);
+  return d;
+}
+
+struct alignas(64) DownArgs {
+  CUtensorMap wq[2];   // boxed path: nibbles of down, sh_down
+  CUtensorMap wsc[2];  // boxed path: their scales
   Q4Ptr down, sh_down;
+  const uint16_t* h;
   const RouteInfo* route;
-  const float* topk_w;
   float* opart;
-  uint32_t* tile_count;      // [H/32]
-  uint32_t* unit_counter;
-  uint16_t* y;
+  uint32_t* status;
+  int R, H, I, k, ring, boxed;
 };
 
-__global__ void __launch_bounds__(kMmaThreads, 1) k4_down(DownArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int R = a.R, H = a.H, I = a.I, k = a.k;
-  const int nb = I >> 5;
-  const int T = (nb + 3) >> 2;
-  const int RT = H / kDownRows;
+__host__ __device__ constexpr size_t dn_red_bytes(int R) {
+  return 2ull * kConsumerWarps * 16 * (size_t)R * 4;
+}
+
+__global__ void __launch_bounds__(kMmaThreads, 1) k4_down(const __grid_constant__ DownArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int R = a.R, H = a.H, I = a.I, k = a.k, ring = a.ring;
+  const DownGeom dg = down_geom(H, I);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
-  DnStage* stages = reinterpret_cast<DnStage*>(smem) + warp * kDownStages;
-  int* wdesc = reinterpret_cast<int*>(reinterpret_cast<DnStage*>(smem) + kMmaWarps * kDownStages) +
-               warp * (2 * kDownStages);
+  const size_t row_qs = (size_t)I / 2;
 
-  pdl_wait();   // h and the route are complete from here on
-  const RouteInfo* rt_info = a.route;
-  const int n_exp = 1 + rt_info->n_union;
-  const int n_units = n_exp * RT;
-  const size_t row_qs = (size_t)I / 2, row_sc = (size_t)nb;
+  uint8_t* stages = smem;
+  uint8_t* hs = smem + (size_t)ring * dg.stage_bytes;                      // [8][h_pitch]
+  float* red = reinterpret_cast<float*>(hs + (size_t)8 * dg.h_pitch);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + dn_red_bytes(R));
+  uint64_t* empty = full + kMaxRing;
 
-  int iu = -1, it = 0;
-  bool exhausted = false;
-  const uint8_t* idq = nullptr;
-  const uint16_t* ids = nullptr;
-  const uint16_t* ihrow = nullptr;
-  bool imember = false;
-  auto issue = [&](int stage) {
-    int unit = -1, tile = 0;
-    if (!exhausted && (iu < 0 || it >= T)) {
-      int nu = 0;
-      if (lane == 0) nu = (int)atomicAdd(a.unit_counter, 1u);
-      nu = __shfl_sync(0xffffffffu, nu, 0);
-      if (nu >= n_units) {
-        exhausted = true;
+  if (tid == 0) {
+    for (int s = 0; s < ring; ++s) {
+      mbar_init(&full[s], kFullArrivals);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_mbar_init();
+    if (a.boxed)
+      for (int i = 0; i < 2; ++i) { prefetch_tensormap(&a.wq[i]); prefetch_tensormap(&a.wsc[i]); }
+  }
+  __syncthreads();
+
+  // The route was complete before the gate/up kernel passed its own wait, which precedes
+  // the launch of this grid; h is waited for below.
+  const RouteInfo* rt = a.route;
+  const int n_units = (1 + rt->n_union) * dg.NGR;
+  const int G = gridDim.x;
+  const int u_begin = (int)(((long long)blockIdx.x * n_units) / G);
+  const int u_end = (int)(((long long)(blockIdx.x + 1) * n_units) / G);
+  const int total = (u_end - u_begin) * dg.KC;
+  const int box_qs = dg.RS * dg.cbmax * 16, box_sc = dg.RS * dg.cbmax * 2;
+  bool timed_out = false;
+
+  if (warp == kProducerWarp) {
+    for (int f = 0; f < total; ++f) {
+      const int slot = f % ring;
+      if (f >= ring && !mbar_wait(&empty[slot], ((f / ring) - 1) & 1, kWaitPolls)) timed_out = true;
+      uint8_t* st = stages + (size_t)slot * dg.stage_bytes;
+      const int n = u_begin + f / dg.KC, c = f % dg.KC;
+      const int u = n / dg.NGR, grp = n - u * dg.NGR;
+      const int r0 = grp * dg.RS;
+      const int row0 = (u == 0 ? 0 : rt->expert[u - 1] * H) + r0;
+      if (a.boxed) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[slot], (uint32_t)(box_qs + box_sc));
+          const int mi = u == 0 ? 1 : 0;
+          tma_load_3d(st, &a.wq[mi], 0, row0, c * (kChunkBlocks / 8), &full[slot]);
+          tma_load_2d(st + box_qs, &a.wsc[mi], c * kChunkBlocks, row0, &full[slot]);
+        }
       } else {
-        iu = nu;
-        it = 0;
-        const int u = nu / RT, rti = nu - u * RT;
-        const size_t row0 = (size_t)rti * kDownRows;
-        uint32_t rowmask;
-        int slot_g = 0;
-        if (u == 0) {
-          idq = a.sh_down.qs + row0 * row_qs;
-          ids = a.sh_down.sc + row0 * row_sc;
-          rowmask = (1u << R) - 1u;
-        } else {
-          const size_t e = (size_t)rt_info->expert[u - 1];
-          idq = a.down.qs + (e * H + row0) * row_qs;
-          ids = a.down.sc + (e * H + row0) * row_sc;
-          rowmask = rt_info->rowmask[u - 1];
-          slot_g = rt_info->slot[u - 1][g];
+        const Q4Ptr m = u == 0 ? a.sh_down : a.down;
+        const int nrows = min(dg.RS, H - r0);
+        const int cb = min(kChunkBlocks, dg.nb - c * kChunkBlocks);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)nrows * cb * 16u);
+        copy_rows(st, dg.qs_pitch, m.qs + (size_t)row0 * row_qs + (size_t)c * kChunkBlocks * 16,
+                  row_qs, st + dg.RS * dg.qs_pitch, dg.sc_pitch,
+                  m.sc + (size_t)row0 * dg.nb + c * kChunkBlocks, dg.nb, nrows, cb, &full[slot],
+                  lane);
+      }
+      cp_async_mbar_arrive(&full[slot]);
+    }
+    pdl_wait();
+  } else {
+    pdl_wait();      // h is complete from here on
+    const int rtl = warp / dg.WK, ks = warp - rtl * dg.WK;   // row tile, K slice
+    const int r = rtl * 16 + g;                              // this lane's first row
+    int woff[8];
+    int r8_q, soff, r8_s;
+    if (a.boxed) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) woff[j] = (ks * dg.RS + r) * 128 + ((j ^ (r & 7)) << 4) + q * 4;
+      r8_q = 8 * 128;
+      soff = box_qs + r * (dg.cbmax * 2) + ks * 16;
+      r8_s = 8 * dg.cbmax * 2;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) woff[j] = r * dg.qs_pitch + ks * 128 + j * 16 + q * 4;
+      r8_q = 8 * dg.qs_pitch;
+      soff = dg.RS * dg.qs_pitch + r * dg.sc_pitch + ks * 16;
+      r8_s = 8 * dg.sc_pitch;
+    }
+    int h_tag = -1;     // (expert slot, chunk) whose h is staged
+    int buf = 0;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int f = 0; f < total; ++f) {
+      const int slot = f % ring;
+      const int n = u_begin + f / dg.KC, c = f % dg.KC;
+      const int u = n / dg.NGR, grp = n - u * dg.NGR;
+      const int cb = min(kChunkBlocks, dg.nb - c * kChunkBlocks);
+      const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : rt->rowmask[u - 1];
+      const int tag = u * dg.KC + c;
+      if (tag != h_tag) {
+        // h of the expert's rows for this chunk: [verify row][values], 16-byte pieces. Rows
+        // that do not use the expert keep stale values; their MMA columns are never read.
+        consumer_sync();   // every consumer is done with the previous h
+        const int per_row = cb * 4;
+        for (int p = tid; p < R * per_row; p += kConsumers) {
+          const int rr = p / per_row, pp = p - rr * per_row;
+          if ((rowmask >> rr) & 1u) {
+            const int slot_r = (u == 0) ? 0 : rt->slot[u - 1][rr];
+            cp_async16(hs + rr * dg.h_pitch + pp * 16,
+                       a.h + ((size_t)rr * (1 + k) + slot_r) * I + c * (kChunkBlocks * 32) + pp * 8,
+                       true);
+          }
         }
-        imember = (g < R) && ((rowmask >> g) & 1u);
-        ihrow = a.h + ((size_t)g * (1 + k) + (imember ? slot_g : 0)) * I;
+        cp_async_commit();
+        cp_async_wait<0>();
+        consumer_sync();
+        h_tag = tag;
       }
-    }
-    if (!exhausted) {
-      unit = iu;
-      tile = it++;
-    }
-    if (lane == 0) {
-      wdesc[2 * stage] = unit;
-      wdesc[2 * stage + 1] = tile;
-    }
-    if (unit >= 0) {
-      const int blk0 = tile * 4;
-      DnStage& S = stages[stage];
+      if (!mbar_wait(&full[slot], (f / ring) & 1, kWaitPolls)) timed_out = true;
+      const uint8_t* st = stages + (size_t)slot * dg.stage_bytes;
+      const int row_t = grp * dg.RS + rtl * 16;         // first row of this warp's tile
+      const int nv = max(0, min(8, cb - 8 * ks));
+      if (nv > 0 && row_t < H) {
+        const uint4 s0v = *reinterpret_cast<const uint4*>(st + soff);
+        const uint4 s8v = *reinterpret_cast<const uint4*>(st + soff + r8_s);
+        float s0[2][4], s8[2][4];
+        widen_scales(make_uint2(s0v.x, s0v.y), s0[0]);
+        widen_scales(make_uint2(s0v.z, s0v.w), s0[1]);
+        widen_scales(make_uint2(s8v.x, s8v.y), s8[0]);
+        widen_scales(make_uint2(s8v.z, s8v.w), s8[1]);
+        const uint8_t* hb = hs + g * dg.h_pitch + ks * 512 + q * 16;
 #pragma unroll
-      for (int h4 = 0; h4 < 4; ++h4) {
-        const int pp = lane + 32 * h4;
-        const int row = pp & (kDownRows - 1), j = pp >> 5;
-        const bool v = blk0 + j < nb;
-        cp_async16(&S.a[j][row][0], v ? idq + row * row_qs + (size_t)(blk0 + j) * 16 : idq, v);
-      }
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int pp = lane + 32 * h2;
-        const int row = pp >> 1, hf = pp & 1;
-        const bool v = blk0 + 2 * hf < nb;
-        cp_async4(&S.s[row][hf], v ? ids + row * row_sc + blk0 + 2 * hf : ids, v);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const bool v = imember && (blk0 + j < nb);
-        cp_async16(&S.b[j][lane], v ? ihrow + (blk0 + j) * 32 + q * 8 : a.h, v);
-      }
-    }
-    cp_async_commit();
-  };
-
-  float acc[2][4];
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[hh][i] = 0.f;
-#pragma unroll
-  for (int s = 0; s < kDownStages - 1; ++s) issue(s);
-
-  int cu = -1, u = 0, rti = 0;
-  for (int t = 0;; ++t) {
-    issue((t + kDownStages - 1) % kDownStages);
-    cp_async_wait<kDownStages - 1>();
-    __syncwarp();
-    const int stage = t % kDownStages;
-    const int unit = wdesc[2 * stage], tile = wdesc[2 * stage + 1];
-    if (unit < 0) break;
-    if (unit != cu) {
-      cu = unit;
-      u = unit / RT;
-      rti = unit - u * RT;
-    }
-    if (tile == 0) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[hh][i] = 0.f;
-    }
-    const DnStage& S = stages[stage];
-    const int blk0 = tile * 4;
-    float sf[2][2][4];   // [half][row g / g+8][block]
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      widen_scales(*reinterpret_cast<const uint2*>(&S.s[hh * 16 + g][0]), sf[hh][0]);
-      widen_scales(*reinterpret_cast<const uint2*>(&S.s[hh * 16 + g + 8][0]), sf[hh][1]);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (blk0 + j < nb) {
-        const uint4 X = pair_order(S.b[j][lane]);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float d[4];
-          q4_block_mma(S.a[j][hh * 16 + g][q], S.a[j][hh * 16 + g + 8][q], X, d);
-          acc[hh][0] = __fmaf_rn(sf[hh][0][j], d[0], acc[hh][0]);
-          acc[hh][1] = __fmaf_rn(sf[hh][0][j], d[1], acc[hh][1]);
-          acc[hh][2] = __fmaf_rn(sf[hh][1][j], d[2], acc[hh][2]);
-          acc[hh][3] = __fmaf_rn(sf[hh][1][j], d[3], acc[hh][3]);
-        }
-      }
-    }
-    __syncwarp();
-
-    if (tile == T - 1) {
-      const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : rt_info->rowmask[u - 1];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 2 * q + (e & 1);
-          const int row = rti * kDownRows + hh * 16 + g + ((e & 2) ? 8 : 0);
-          if (c < R && ((rowmask >> c) & 1u)) {
-            const int slot = (u == 0) ? 0 : rt_info->slot[u - 1][c];
-            a.opart[((size_t)c * (1 + k) + slot) * H + row] = acc[hh][e];
+        for (int j = 0; j < 8; ++j) {
+          if (j < nv) {
+            const uint4 X = pair_order(*reinterpret_cast<const uint4*>(hb + j * 64));
+            const uint8_t* w = st + woff[j];
+            float d[4];
+            q4_block_mma(lds32(w), lds32(w + r8_q), X, d);
+            const float a0 = s0[j >> 2][j & 3], a8 = s8[j >> 2][j & 3];
+            acc[0] = __fmaf_rn(a0, d[0], acc[0]); acc[1] = __fmaf_rn(a0, d[1], acc[1]);
+            acc[2] = __fmaf_rn(a8, d[2], acc[2]); acc[3] = __fmaf_rn(a8, d[3], acc[3]);
           }
         }
       }
-      __threadfence();
       __syncwarp();
-      unsigned prev = 0;
-      if (lane == 0) prev = atomicAdd(a.tile_count + rti, 1u);
-      prev = __shfl_sync(0xffffffffu, prev, 0);
-      if (prev == (unsigned)(n_exp - 1)) {
-        __threadfence();
-        for (int idx = lane; idx < R * kDownRows; idx += 32) {
-          const int r = idx / kDownRows, row = rti * kDownRows + (idx % kDownRows);
-          const float* orow = a.opart + (size_t)r * (1 + k) * H + row;
-          float yv = __ldcg(orow);
-          for (int j = 0; j < k; ++j)
-            yv = __fmaf_rn(a.topk_w[r * k + j], __ldcg(orow + (size_t)(1 + j) * H), yv);
-          a.y[(size_t)r * H + row] = f32_to_bf16_rne(yv);
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      if (c == dg.KC - 1) {
+        float* rb = red + (size_t)buf * kConsumerWarps * 16 * R;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int col = 2 * q + (e & 1), row = g + ((e & 2) ? 8 : 0);
+          if (col < R) rb[(warp * 16 + row) * R + col] = acc[e];
+          acc[e] = 0.f;
         }
+        consumer_sync();
+        for (int t = tid; t < dg.RS * R; t += kConsumers) {
+          const int rl = t / R, col = t - rl * R;
+          const int row = grp * dg.RS + rl;
+          if (row < H && ((rowmask >> col) & 1u)) {
+            const int tile = rl >> 4, rr = rl & 15;
+            float o = 0.f;
+            for (int s = 0; s < dg.WK; ++s)
+              o = __fadd_rn(o, rb[((tile * dg.WK + s) * 16 + rr) * R + col]);
+            const int slot_c = (u == 0) ? 0 : rt->slot[u - 1][col];
+            a.opart[((size_t)col * (1 + k) + slot_c) * H + row] = o;
+          }
+        }
+        buf ^= 1;
       }
     }
   }
-  cp_async_wait<0>();
+  pdl_trigger();
+  if (timed_out && lane == 0) flag_status(a.status, kStatusTimeout);
+}
+
+// ---------------------------------------------------------------------------------
+// K5: combine. y[r] = bf16_rne(o_shared + sum_j w_j o_j), the sum taken in rank order j.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k5_combine(const float* __restrict__ opart,
+                                                  const float* __restrict__ topk_w,
+                                                  uint16_t* __restrict__ y, int R, int H,
+                                                  int k) {
+  pdl_wait();
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= R * H) return;
+  const int r = idx / H, col = idx - r * H;
+  const float* o = opart + (size_t)r * (1 + k) * H + col;
+  float yv = o[0];
+  for (int j = 0; j < k; ++j) yv = __fmaf_rn(topk_w[r * k + j], o[(size_t)(1 + j) * H], yv);
+  y[idx] = f32_to_bf16_rne(yv);
 }
 
 template <typename K>
@@ -758,40 +878,145 @@ cudaError_t launch_pdl(void (*kernel)(Exp...), int grid, int block, size_t smem,
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
 }
 
-size_t gate_up_smem(const MoeDims& d) {
-  const size_t xbytes = ((size_t)d.R * (d.H * 2 + 64) + 127) & ~(size_t)127;
-  return xbytes + sizeof(GuStage) * kMmaWarps * kStages + sizeof(int) * 2 * kStages * kMmaWarps;
+// ------------------------------------------------------------------ tensor maps ------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
 }
 
-size_t down_smem() {
-  return sizeof(DnStage) * kMmaWarps * kDownStages + sizeof(int) * 2 * kDownStages * kMmaWarps;
+// Encoded maps are kept in a small cache keyed by their parameters: a decode loop calls
+// the layer with the same weights every step.
+struct MapKey {
+  const void* base;
+  uint64_t d0, d1, d2;
+  uint32_t b0, b1, b2, kind;
+};
+
+bool same_key(const MapKey& a, const MapKey& b) {
+  return a.base == b.base && a.d0 == b.d0 && a.d1 == b.d1 && a.d2 == b.d2 && a.b0 == b.b0 &&
+         a.b1 == b.b1 && a.b2 == b.b2 && a.kind == b.kind;
+}
+
+cudaError_t cached_map(CUtensorMap* out, const MapKey& key) {
+  constexpr int kSlots = 64;
+  static std::mutex mu;
+  static MapKey keys[kSlots];
+  static CUtensorMap maps[kSlots];
+  static int used = 0, next = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (same_key(keys[i], key)) { *out = maps[i]; return cudaSuccess; }
+  }
+  const EncodeTiledFn f = encode_tiled();
+  if (!f) return cudaErrorNotSupported;
+  CUresult r;
+  if (key.kind == 0) {
+    // nibbles, viewed as [128-byte chunk][row][128 bytes]; 128-byte swizzle
+    const cuuint64_t dims[3] = {128, key.d1, key.d2};
+    const cuuint64_t strides[2] = {key.d0, 128};
+    const cuuint32_t box[3] = {128, key.b1, key.b2};
+    const cuuint32_t es[3] = {1, 1, 1};
+    r = f(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(key.base), dims, strides, box,
+          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    // fp16 scales [row][nb]
+    const cuuint64_t dims[2] = {key.d0, key.d1};
+    const cuuint64_t strides[1] = {key.d0 * 2};
+    const cuuint32_t box[2] = {key.b0, key.b1};
+    const cuuint32_t es[2] = {1, 1};
+    r = f(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(key.base), dims, strides, box,
+          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  std::lock_guard<std::mutex> lock(mu);
+  keys[next] = key;
+  maps[next] = *out;
+  next = (next + 1) % kSlots;
+  if (used < kSlots) ++used;
+  return cudaSuccess;
+}
+
+// Maps of one Q4 matrix of `rows` rows of K values (K a multiple of 256), in boxes of
+// `box_rows` rows by `box_blocks` Q4 blocks (a multiple of 8).
+cudaError_t q4_maps(CUtensorMap* wq, CUtensorMap* wsc, Q4Ptr m, uint64_t rows, int K,
+                    int box_rows, int box_blocks) {
+  MapKey kq{};
+  kq.base = m.qs; kq.d0 = (uint64_t)K / 2; kq.d1 = rows; kq.d2 = (uint64_t)K / 256;
+  kq.b1 = (uint32_t)box_rows; kq.b2 = (uint32_t)box_blocks / 8; kq.kind = 0;
+  cudaError_t err = cached_map(wq, kq);
+  if (err != cudaSuccess) return err;
+  MapKey ks{};
+  ks.base = m.sc; ks.d0 = (uint64_t)K / 32; ks.d1 = rows;
+  ks.b0 = (uint32_t)box_blocks; ks.b1 = (uint32_t)box_rows; ks.kind = 1;
+  return cached_map(wsc, ks);
+}
+
+template <int WB>
+size_t gate_up_smem(const MoeDims& d, int ring) {
+  return 1024 + (size_t)ring * GuGeom<WB>::kStage + gu_red_bytes(d.R) + 64 +
+         (size_t)d.R * (2 * d.H + kXPad);
+}
+
+size_t down_smem(const MoeDims& d, int ring) {
+  const DownGeom g = down_geom(d.H, d.I);
+  return 1024 + (size_t)ring * g.stage_bytes + (size_t)8 * g.h_pitch + dn_red_bytes(d.R) + 64;
+}
+
+// Deepest ring (4 .. 2 stages) whose shared memory fits; 0 if none does.
+template <typename F>
+int pick_ring(F smem_of) {
+  for (int ring = kMaxRing; ring >= 2; --ring)
+    if (smem_of(ring) <= (size_t)device_max_smem_optin()) return ring;
+  return 0;
+}
+
+template <int WB>
+cudaError_t launch_gate_up_wb(const MoeDims& d, GateUpArgs& a, int ring, cudaStream_t s) {
+  const size_t smem = gate_up_smem<WB>(d, ring);
+  cudaError_t err = set_smem(k3_gate_up<WB>, smem);
+  if (err != cudaSuccess) return err;
+  a.ring = ring;
+  if (a.boxed) {
+    const Q4Ptr mats[4] = {a.gate, a.up, a.sh_gate, a.sh_up};
+    for (int i = 0; i < 4; ++i) {
+      const uint64_t rows = (uint64_t)(i < 2 ? d.E : 1) * d.I;
+      if ((err = q4_maps(&a.wq[i], &a.wsc[i], mats[i], rows, d.H, 16, 16 * WB)) != cudaSuccess)
+        return err;
+    }
+  }
+  return launch_pdl(k3_gate_up<WB>, device_sm_count(), kMmaThreads, smem, s, a);
 }
 
 }  // namespace
 
-size_t gate_up_smem_bytes(const MoeDims& d) { return gate_up_smem(d); }
-
-int gate_up_kparts(int H) {
-  const int T = ((H >> 5) + 3) >> 2;
-  const int TP = (T + 3) >> 2;
-  return (T + TP - 1) / TP;
-}
+size_t gate_up_smem_bytes(const MoeDims& d) { return gate_up_smem<4>(d, 2); }
 
 MoeLayout moe_layout(const MoeDims& d) {
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
-  const size_t U = 1 + (size_t)d.R * d.k;           // expert slots (shared + union bound)
-  const size_t RT = (size_t)d.I / 16;
   MoeLayout L{};
   size_t off = 0;
   L.header = off; off += 256;
-  L.tile_count = off; off += up(sizeof(uint32_t) * (size_t)(d.H / 16));
-  L.part_count = off; off += up(sizeof(uint32_t) * U * RT);
   L.zero_bytes = off;
-  L.logits = off; off += up(sizeof(float) * (size_t)d.R * d.E);
+  L.scores = off; off += up(sizeof(float) * (size_t)d.R * d.E);
   L.route = off; off += up(sizeof(RouteInfo));
   L.h = off; off += up(sizeof(uint16_t) * (size_t)d.R * (1 + d.k) * d.I);
   L.opart = off; off += up(sizeof(float) * (size_t)d.R * (1 + d.k) * d.H);
-  L.part = off; off += up(sizeof(float) * U * RT * (size_t)gate_up_kparts(d.H) * 256);
   L.total = off;
   return L;
 }
@@ -799,12 +1024,12 @@ MoeLayout moe_layout(const MoeDims& d) {
 cudaError_t launch_router(const MoeDims& d, const uint16_t* x, const uint16_t* router_w,
                           int32_t* topk_idx, float* topk_w, const MoeWorkspace& ws,
                           cudaStream_t s) {
-  const size_t smem = sizeof(float) * (size_t)d.R * (size_t)(d.H > d.E ? d.H : d.E);
+  const size_t smem = sizeof(float) * (size_t)d.R * d.H;
   cudaError_t err = set_smem(k1_router, smem);
   if (err != cudaSuccess) return err;
   const int grid = (d.E + kRouterWarps - 1) / kRouterWarps;
   k1_router<<<grid, kRouterWarps * 32, smem, s>>>(
-      x, d.R, d.H, router_w, d.E, d.k, ws.logits, topk_idx, topk_w, ws.route,
+      x, d.R, d.H, router_w, d.E, d.k, ws.scores, topk_idx, topk_w, ws.route,
       reinterpret_cast<WsHeader*>(ws.header));
   return cudaGetLastError();
 }
@@ -812,22 +1037,45 @@ cudaError_t launch_router(const MoeDims& d, const uint16_t* x, const uint16_t* r
 cudaError_t launch_gate_up(const MoeDims& d, const uint16_t* x, Q4Ptr gate, Q4Ptr up,
                            Q4Ptr sh_gate, Q4Ptr sh_up, const MoeWorkspace& ws,
                            cudaStream_t s) {
-  const size_t smem = gate_up_smem(d);
-  cudaError_t err = set_smem(k3_gate_up, smem);
-  if (err != cudaSuccess) return err;
-  GateUpArgs a{x, d.R, d.H, d.I, d.k, gate, up, sh_gate, sh_up, ws.route, ws.h, ws.part,
-               ws.part_count, ws.header + 2};
-  return launch_pdl(k3_gate_up, device_sm_count(), kMmaThreads, smem, s, a);
+  // Whole 4096-value chunks when they fit with a ring of at least 2, else half chunks.
+  const int ring8 = pick_ring([&](int r) { return gate_up_smem<8>(d, r); });
+  const int ring4 = pick_ring([&](int r) { return gate_up_smem<4>(d, r); });
+  if (ring8 == 0 && ring4 == 0) return cudaErrorInvalidConfiguration;
+  GateUpArgs a{};
+  a.gate = gate; a.up = up; a.sh_gate = sh_gate; a.sh_up = sh_up;
+  a.x = x; a.route = ws.route; a.h = ws.h; a.status = ws.header;
+  a.R = d.R; a.H = d.H; a.I = d.I; a.k = d.k;
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  a.boxed = (d.H % 256) == 0 && a16(gate.sc) && a16(up.sc) && a16(sh_gate.sc) && a16(sh_up.sc)
+                ? 1 : 0;
+  return ring8 ? launch_gate_up_wb<8>(d, a, ring8, s) : launch_gate_up_wb<4>(d, a, ring4, s);
 }
 
 cudaError_t launch_down(const MoeDims& d, Q4Ptr down, Q4Ptr sh_down, const float* topk_w,
                         uint16_t* y, const MoeWorkspace& ws, cudaStream_t s) {
-  const size_t smem = down_smem();
+  const int ring = pick_ring([&](int r) { return down_smem(d, r); });
+  if (ring == 0) return cudaErrorInvalidConfiguration;
+  const size_t smem = down_smem(d, ring);
   cudaError_t err = set_smem(k4_down, smem);
   if (err != cudaSuccess) return err;
-  DownArgs a{ws.h, d.R, d.H, d.I, d.k, down, sh_down, ws.route, topk_w, ws.opart,
-             ws.tile_count, ws.header + 3, y};
-  return launch_pdl(k4_down, device_sm_count(), kMmaThreads, smem, s, a);
+  DownArgs a{};
+  a.down = down; a.sh_down = sh_down; a.h = ws.h; a.route = ws.route; a.opart = ws.opart;
+  a.status = ws.header;
+  a.R = d.R; a.H = d.H; a.I = d.I; a.k = d.k; a.ring = ring;
+  const DownGeom g = down_geom(d.H, d.I);
+  a.boxed = g.boxed && (reinterpret_cast<uintptr_t>(down.sc) & 15u) == 0 &&
+            (reinterpret_cast<uintptr_t>(sh_down.sc) & 15u) == 0;
+  if (a.boxed) {
+    if ((err = q4_maps(&a.wq[0], &a.wsc[0], down, (uint64_t)d.E * d.H, d.I, g.RS, g.cbmax)) !=
+            cudaSuccess ||
+        (err = q4_maps(&a.wq[1], &a.wsc[1], sh_down, (uint64_t)d.H, d.I, g.RS, g.cbmax)) !=
+            cudaSuccess)
+      return err;
+  }
+  err = launch_pdl(k4_down, device_sm_count(), kMmaThreads, smem, s, a);
+  if (err != cudaSuccess) return err;
+  const int n = d.R * d.H;
+  return launch_pdl(k5_combine, (n + 255) / 256, 256, 0, s, ws.opart, topk_w, y, d.R, d.H, d.k);
 }
 
 }  // namespace dsmoe

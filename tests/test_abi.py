@@ -152,7 +152,7 @@ def test_noalloc_rejects_on_the_host(lib):
     # CUDA call (this machine may have no GPU at all).
     for R in range(1, 7):
         assert 0 < lib.ds_moe_workspace_size(fake_layer(), R) <= N.DS_NOALLOC_SCRATCH_BYTES
-    big = fake_layer(H=8192, I=2048)
+    big = fake_layer(H=16384, E=64, I=1024, k=16)
     assert lib.ds_moe_workspace_size(big, 6) > N.DS_NOALLOC_SCRATCH_BYTES
     assert lib.ds_moe_verify_forward_noalloc(big, FAKE, 6, FAKE, FAKE, FAKE, None) == 3
     assert lib.ds_moe_verify_forward_noalloc(fake_layer(), FAKE, 0, FAKE, FAKE, FAKE, None) == 1

@@ -65,7 +65,7 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(dsm, shape):
 
 
 def test_oversized_layer_is_refused_with_the_limit(dsm):
-    shape = synth.MoeShape(H=8192, E=16, I=2048, k=8)
+    shape = synth.MoeShape(H=16384, E=16, I=64, k=16)
     d = synth.moe_layer(shape, seed=5, device="cuda")
     layer = dsm.MoeLayer.from_dict(d, shape.k)
     assert dsm.moe_workspace_size(layer, 6) > dsm._native.DS_NOALLOC_SCRATCH_BYTES
