@@ -132,16 +132,23 @@ __device__ __forceinline__ void widen_scales(uint2 s, float (&f)[4]) {
 }
 
 // ---------------------------------------------------------------------------------
-// K1: router. One warp per expert computes z = x . Wr[e] for all R rows (fp32, lane-
-// strided partial sums then a butterfly), the last CTA to finish (atomic arrival count,
-// no waiting) computes sigmoid scores, the top-k per row, the renormalised weights and
-// the union of the selected experts with each one's rows and rank slots.
+// K1: router. CTA c computes z = x . Wr[e] for the kRouterExperts experts e of its group
+// and all R rows: warp w takes the w-th eighth of the hidden dimension (x read straight
+// from global memory into registers, each lane 8 values at a time), the eight warps'
+// partial sums (lane-strided then a butterfly) are added in warp order, and the sigmoid
+// score is written. The last CTA to arrive (atomic count, nobody waits) selects each
+// row's top k (one warp per row, its scores in registers, a tree argmax per round with
+// ties to the lower index), renormalises the weights, and builds the union of the
+// selected experts with each one's rows and rank slots.
 // ---------------------------------------------------------------------------------
+constexpr int kRouterExperts = 4;
+
+template <int KPER>   // score registers per lane in the top-k: ceil(E / 32) <= KPER
 __global__ void __launch_bounds__(kRouterWarps * 32)
     k1_router(const uint16_t* __restrict__ x, int R, int H, const uint16_t* __restrict__ wr,
               int E, int k, float* __restrict__ scores, int32_t* __restrict__ topk_idx,
               float* __restrict__ topk_w, RouteInfo* __restrict__ route, WsHeader* hdr) {
-  extern __shared__ float smem_f[];  // x as fp32 [R][H]
+  __shared__ float part[kRouterWarps][kRouterExperts][kMaxRows];
   __shared__ int s_is_last;
   __shared__ int32_t sel_e[kMaxRows][kMaxTopK];
   __shared__ float sel_s[kMaxRows][kMaxTopK];
@@ -153,65 +160,63 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 
   pdl_trigger();   // the gate/up kernel may launch now; it waits for this grid's results
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int e0 = blockIdx.x * kRouterExperts;
+  const int ne = min(kRouterExperts, E - e0);
   {
-    // 8 values per 16-byte load; loads of an unrolled batch are independent, so the CTA
-    // has many in flight instead of one load -> store round trip at a time.
-    const uint4* x8 = reinterpret_cast<const uint4*>(x);
-    const int n8 = R * H / 8;
-#pragma unroll 8
-    for (int i = tid; i < n8; i += blockDim.x) {
-      const uint4 v = __ldg(x8 + i);
-      float4* d = reinterpret_cast<float4*>(smem_f + 8 * i);
-      d[0] = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
-      d[1] = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
-    }
-  }
-  __syncthreads();
-
-  const int e = blockIdx.x * kRouterWarps + warp;
-  if (e < E) {
-    float acc[kMaxRows];
+    float acc[kRouterExperts][kMaxRows];
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.0f;
-    const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)e * H);
-    const int nc = H / 8;
-    // All of a warp's weight loads for up to 4096 values are issued before any use.
-    for (int c0 = 0; c0 < nc; c0 += 16 * 32) {
-      uint4 wv[16];
+    for (int e = 0; e < kRouterExperts; ++e)
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int c = c0 + u * 32 + lane;
-        wv[u] = c < nc ? __ldcs(wrow + c) : make_uint4(0, 0, 0, 0);
-      }
+      for (int r = 0; r < kMaxRows; ++r) acc[e][r] = 0.0f;
+    const int slice = H / kRouterWarps;          // a multiple of 8
+    const int nch = slice / 8;
+#pragma unroll 2
+    for (int c = lane; c < nch; c += 32) {
+      const int col = warp * slice + c * 8;
+      uint4 wv[kRouterExperts], xv[kMaxRows];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int c = c0 + u * 32 + lane;
-        if (c >= nc) continue;
-        const float wf[8] = {bf16_lo(wv[u].x), bf16_hi(wv[u].x), bf16_lo(wv[u].y),
-                             bf16_hi(wv[u].y), bf16_lo(wv[u].z), bf16_hi(wv[u].z),
-                             bf16_lo(wv[u].w), bf16_hi(wv[u].w)};
+      for (int e = 0; e < kRouterExperts; ++e)
+        wv[e] = e < ne ? __ldcs(reinterpret_cast<const uint4*>(wr + (size_t)(e0 + e) * H + col))
+                       : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
-          if (r < R) {
-            const float4 a = *reinterpret_cast<const float4*>(smem_f + r * H + c * 8);
-            const float4 b = *reinterpret_cast<const float4*>(smem_f + r * H + c * 8 + 4);
-            float t = acc[r];
-            t = __fmaf_rn(wf[0], a.x, t); t = __fmaf_rn(wf[1], a.y, t);
-            t = __fmaf_rn(wf[2], a.z, t); t = __fmaf_rn(wf[3], a.w, t);
-            t = __fmaf_rn(wf[4], b.x, t); t = __fmaf_rn(wf[5], b.y, t);
-            t = __fmaf_rn(wf[6], b.z, t); t = __fmaf_rn(wf[7], b.w, t);
-            acc[r] = t;
+      for (int r = 0; r < kMaxRows; ++r)
+        xv[r] = r < R ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)r * H + col))
+                      : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) {
+        if (r < R) {
+          const float xf[8] = {bf16_lo(xv[r].x), bf16_hi(xv[r].x), bf16_lo(xv[r].y),
+                               bf16_hi(xv[r].y), bf16_lo(xv[r].z), bf16_hi(xv[r].z),
+                               bf16_lo(xv[r].w), bf16_hi(xv[r].w)};
+#pragma unroll
+          for (int e = 0; e < kRouterExperts; ++e) {
+            float t = acc[e][r];
+            t = __fmaf_rn(bf16_lo(wv[e].x), xf[0], t); t = __fmaf_rn(bf16_hi(wv[e].x), xf[1], t);
+            t = __fmaf_rn(bf16_lo(wv[e].y), xf[2], t); t = __fmaf_rn(bf16_hi(wv[e].y), xf[3], t);
+            t = __fmaf_rn(bf16_lo(wv[e].z), xf[4], t); t = __fmaf_rn(bf16_hi(wv[e].z), xf[5], t);
+            t = __fmaf_rn(bf16_lo(wv[e].w), xf[6], t); t = __fmaf_rn(bf16_hi(wv[e].w), xf[7], t);
+            acc[e][r] = t;
           }
         }
       }
     }
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
-      if (r < R) {
-        const float z = warp_sum(acc[r]);
-        if (lane == 0) scores[r * E + e] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
+    for (int e = 0; e < kRouterExperts; ++e)
+#pragma unroll
+      for (int r = 0; r < kMaxRows; ++r) {
+        if (r < R) {
+          const float v = warp_sum(acc[e][r]);
+          if (lane == 0) part[warp][e][r] = v;
+        }
       }
-    }
+  }
+  __syncthreads();
+  if (tid < ne * R) {
+    const int e = tid / R, r = tid - e * R;
+    float z = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kRouterWarps; ++w) z = __fadd_rn(z, part[w][e][r]);
+    scores[r * E + e0 + e] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
   }
 
   // Arrival count: the last CTA continues, the others are done. Nobody waits.
@@ -226,15 +231,12 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   __threadfence();
 
   if (tid < kMaxExperts / 32) ubits[tid] = 0u;
-  // Warp r selects row r's top k. Its scores sit in registers, 32 experts per lane
-  // round; all loads of a row are issued before the first comparison.
   if (warp < R) {
     const int r = warp;
-    constexpr int kPer = kMaxExperts / 32;
-    float v[kPer];
+    float v[KPER];
     bool bad = false;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
+    for (int i = 0; i < KPER; ++i) {
       const int e2 = i * 32 + lane;
       const float sv = e2 < E ? __ldcg(scores + r * E + e2) : -1.0f;
       // sigmoid scores lie in [0, 1]; a NaN (from NaN inputs) ranks below every score
@@ -243,22 +245,30 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(&hdr->status, kStatusCheck);
     for (int j = 0; j < k; ++j) {
-      float best = -1.0f;
-      int bi = INT_MAX;
+      // this lane's best (value, register index) by a tree; on equal values the lower
+      // index (the left operand) wins
+      float bv[KPER];
+      int bi[KPER];
 #pragma unroll
-      for (int i = 0; i < kPer; ++i)
-        if (v[i] > best) { best = v[i]; bi = i * 32 + lane; }   // lower index wins ties
+      for (int i = 0; i < KPER; ++i) { bv[i] = v[i]; bi[i] = i; }
+#pragma unroll
+      for (int w = 1; w < KPER; w <<= 1)
+#pragma unroll
+        for (int i = 0; i + w < KPER; i += 2 * w)
+          if (bv[i + w] > bv[i]) { bv[i] = bv[i + w]; bi[i] = bi[i + w]; }
+      float best = bv[0];
+      int bidx = bi[0] * 32 + lane;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+        const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+        if (ov > best || (ov == best && oi < bidx)) { best = ov; bidx = oi; }
       }
 #pragma unroll
-      for (int i = 0; i < kPer; ++i)
-        if (i * 32 + lane == bi) v[i] = -1.0f;   // taken
+      for (int i = 0; i < KPER; ++i)
+        if (i * 32 + lane == bidx) v[i] = -1.0f;   // taken
       if (lane == 0) {
-        sel_e[r][j] = bi;
+        sel_e[r][j] = bidx;
         sel_s[r][j] = best;
       }
     }
@@ -1024,13 +1034,14 @@ MoeLayout moe_layout(const MoeDims& d) {
 cudaError_t launch_router(const MoeDims& d, const uint16_t* x, const uint16_t* router_w,
                           int32_t* topk_idx, float* topk_w, const MoeWorkspace& ws,
                           cudaStream_t s) {
-  const size_t smem = sizeof(float) * (size_t)d.R * d.H;
-  cudaError_t err = set_smem(k1_router, smem);
-  if (err != cudaSuccess) return err;
-  const int grid = (d.E + kRouterWarps - 1) / kRouterWarps;
-  k1_router<<<grid, kRouterWarps * 32, smem, s>>>(
-      x, d.R, d.H, router_w, d.E, d.k, ws.scores, topk_idx, topk_w, ws.route,
-      reinterpret_cast<WsHeader*>(ws.header));
+  const int grid = (d.E + kRouterExperts - 1) / kRouterExperts;
+  auto* hdr = reinterpret_cast<WsHeader*>(ws.header);
+  if (d.E <= 12 * 32)
+    k1_router<12><<<grid, kRouterWarps * 32, 0, s>>>(x, d.R, d.H, router_w, d.E, d.k, ws.scores,
+                                                      topk_idx, topk_w, ws.route, hdr);
+  else
+    k1_router<kMaxExperts / 32><<<grid, kRouterWarps * 32, 0, s>>>(
+        x, d.R, d.H, router_w, d.E, d.k, ws.scores, topk_idx, topk_w, ws.route, hdr);
   return cudaGetLastError();
 }
 
