@@ -189,6 +189,10 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
   ws.urows = reinterpret_cast<uint8_t*>(base + L.urows);
   ws.cscore = reinterpret_cast<float*>(base + L.cscore);
   ws.chi = reinterpret_cast<float*>(base + L.chi);
+  ws.tau = reinterpret_cast<uint32_t*>(base + L.tau);
+  ws.ccnt = reinterpret_cast<int32_t*>(base + L.ccnt);
+  ws.clo = reinterpret_cast<int32_t*>(base + L.clo);
+  ws.creg = reinterpret_cast<int32_t*>(base + L.creg);
   const bool tc = !(a->flags & DS_SELECT_CANONICAL_SCORES) &&
                   tc_scoring_supported(d, a->keys, a->q);
 

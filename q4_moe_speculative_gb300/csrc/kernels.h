@@ -70,10 +70,19 @@ struct SelWorkspace {
   float* cscore;      // [L][R][N] by union entry: canonical scores, or (tensor-core
                       // scoring) order keys of the lower bounds of the scores
   float* chi;         // [L][R][N] by union entry: upper bounds (tensor-core scoring)
+  uint32_t* tau;      // [L][R] sampled collection threshold (top-k, tensor-core scoring)
+  int32_t* ccnt;      // [L][R][kTopkChunks] entries collected per row chunk
+  int32_t* clo;       // [L][R][kTopkChunks] entries with a lower bound >= tau per chunk
+  int32_t* creg;      // [3][L][R][kTopkChunks][kTopkChunkCap] collected entries in index
+                      // order: entry, lower bound key, upper bound key
 };
 
+constexpr int kTopkChunks = 8;        // collect CTAs per row
+constexpr int kTopkChunkCap = 512;    // collected entries kept per row chunk
+
 struct SelLayout {
-  size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, chi, total;
+  size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, chi, tau, ccnt, clo, creg,
+      total;
 };
 SelLayout sel_layout(const SelDims& d, bool caller_cidx);
 bool tc_scoring_supported(const SelDims& d, const uint16_t* keys, const uint16_t* q);

@@ -39,10 +39,11 @@ constexpr int kCompactThreads = 1024;
 constexpr int kScoreThreads = 128;   // canonical scorer: one key per thread
 constexpr int kTcThreads = 128;      // tensor-core scorer: 4 warps = 128 TMEM lanes
 constexpr int kScoreMaxHeads = 16;
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kResidCap = 4096;      // residual radix bucket kept in shared memory
 constexpr int kCandCap = 4096;       // re-score candidates kept in shared memory
+constexpr int kCollectCap = 4096;    // entries collected by the sampled-threshold pass
 constexpr uint32_t kWaitPolls = 1u << 17;   // bounded mbarrier polling (<= ~0.13 s)
 constexpr float kEpsRel = 0.0009765625f;    // 2^-10
 constexpr uint32_t kNoScoreKey = 0u;        // sorts below the key of every score
@@ -89,6 +90,18 @@ __device__ __forceinline__ uint32_t admitted_word(const uint32_t* m, int wi, int
   return w;
 }
 
+// d + q_lo k_lo, then + q_hi k_hi, for two packed bf16 pairs: each step is one fused
+// multiply-add of bf16 operands into fp32 (the product is exact, one rounding), the same
+// value as fmaf on the operands widened to fp32.
+__device__ __forceinline__ float fma2_bf16(uint32_t qw, uint32_t kw, float d) {
+  asm("{\n\t.reg .b16 ql, qh, kl, kh;\n\t"
+      "mov.b32 {ql, qh}, %1;\n\tmov.b32 {kl, kh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, ql, kl, %0;\n\tfma.rn.f32.bf16 %0, qh, kh, %0;\n\t}"
+      : "+f"(d)
+      : "r"(qw), "r"(kw));
+  return d;
+}
+
 // Order-preserving 32-bit key of an fp32 score: larger score -> larger key, -0 == +0.
 __device__ __forceinline__ uint32_t score_key(float s) {
   uint32_t u = __float_as_uint(s);
@@ -96,25 +109,33 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Canonical score of one block: q [Hh][128] fp32 (shared), key 128 bf16 (global), w [Hh].
+// Canonical score of one block: q fp32 (shared) in the layout [i][kScoreMaxHeads] (value i
+// of head h at i * kScoreMaxHeads + h), key 128 bf16 (global), w [Hh].
 __device__ __forceinline__ float canonical_score(const float* q, const uint16_t* key,
                                                  const float* w, int Hh) {
   float d[kScoreMaxHeads];
 #pragma unroll
   for (int h = 0; h < kScoreMaxHeads; ++h) d[h] = 0.0f;
   const uint4* k4 = reinterpret_cast<const uint4*>(key);
-  for (int c = 0; c < 16; ++c) {
-    const uint4 kv = __ldg(k4 + c);
-    const float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
-                         bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    uint4 kvs[8];
 #pragma unroll
-    for (int h = 0; h < kScoreMaxHeads; ++h) {
-      if (h < Hh) {
-        const float* qh = q + h * 128 + c * 8;
-        float t = d[h];
+    for (int c = 0; c < 8; ++c) kvs[c] = __ldg(k4 + half * 8 + c);
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      const uint4 kv = kvs[c];
+      const float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
+                           bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t = __fmaf_rn(qh[e], kf[e], t);
-        d[h] = t;
+      for (int h = 0; h < kScoreMaxHeads; ++h) {
+        if (h < Hh) {
+          const float* qh = q + ((half * 8 + c) * 8) * kScoreMaxHeads + h;
+          float t = d[h];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t = __fmaf_rn(qh[e * kScoreMaxHeads], kf[e], t);
+          d[h] = t;
+        }
       }
     }
   }
@@ -651,14 +672,14 @@ __device__ __forceinline__ void hist_pass(int n, bool resid, const uint32_t* r_k
 template <typename KeyAt>
 __device__ uint32_t radix_threshold(int n, int need, KeyAt key_at, int* hist, int* scratch,
                                     uint32_t* r_key, int* s_misc, uint32_t* status,
-                                    int* need_out) {
+                                    int* need_out, int passes = 4) {
   const int tid = threadIdx.x, lane = tid & 31;
   int& s_bucket = s_misc[0];
   int& s_need = s_misc[1];
   int& s_rn = s_misc[2];
   uint32_t prefix = 0;
   bool resid = false;
-  for (int pass = 0; pass < 4; ++pass) {
+  for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
     for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
     if (tid == 0) {
@@ -688,7 +709,7 @@ __device__ uint32_t radix_threshold(int n, int need, KeyAt key_at, int* hist, in
     }
     prefix = (prefix << 8) | (uint32_t)s_bucket;
     need = s_need;
-    if (pass == 1 && !resid) {
+    if (pass == 1 && !resid && passes > 2) {
       const int cnt = hist[s_bucket];
       if (cnt <= kResidCap) {
         if (tid == 0) s_rn = 0;
@@ -720,7 +741,7 @@ __device__ uint32_t radix_threshold(int n, int need, KeyAt key_at, int* hist, in
     __syncthreads();
   }
   *need_out = need;
-  return prefix;
+  return prefix << (32 - 8 * passes);   // with fewer passes: the bucket's lower bound
 }
 
 // Ordered selection over n elements: every element classified 2 ("greater"), plus the
@@ -804,9 +825,126 @@ struct TopkArgs {
   int32_t* nsel;
   uint32_t* status;
   int tc_mode;
+  uint32_t* tau;
+  int32_t* ccnt;
+  int32_t* clo;
+  int32_t* creg;
 };
 
-__global__ void __launch_bounds__(kTopkThreads) k7_topk(TopkArgs a) {
+constexpr uint32_t kTauDirect = 0xFFFFFFFFu;   // row with at most K admitted: no collection
+
+// ---------------------------------------------------------------------------------
+// K7a: per (layer, row), a collection threshold tau at or below the K-th largest lower
+// bound, from a sample of 2048 entries (64 chunks of 32, evenly spaced): the key of the
+// sample's rank-th largest lower bound, rank = K of the row scaled to the sample plus 16
+// (about 800 of the row's entries at 300k context, so that at least K lie above it with
+// a wide margin), to two digits (the bucket's lower bound). Rows that fit the collection
+// whole get tau = 0.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kTopkThreads) k7a_tau(TopkArgs a) {
+  __shared__ int hist[256];
+  __shared__ int scratch[33];
+  __shared__ int s_misc[4];
+  __shared__ uint32_t samp[2048];
+  const int lr = blockIdx.x, l = lr / a.R, tid = threadIdx.x;
+  const int K = a.K;
+  if (a.ccount[lr] <= K) {
+    if (tid == 0) a.tau[lr] = kTauDirect;
+    return;
+  }
+  const int n = a.ucount[l];
+  uint32_t tau = 0u;
+  if (n > kCollectCap) {
+    constexpr int kChunks = 64, kS = kChunks * 32;
+    const uint32_t* s0 = a.sc0 + (size_t)lr * a.N;
+    const int spacing = n / kChunks;
+    for (int j = tid; j < kS; j += blockDim.x) samp[j] = s0[(j >> 5) * spacing + (j & 31)];
+    __syncthreads();
+    const int rank = min(kS, (int)(((long long)K * kS + n - 1) / n) + 16);
+    int need;
+    tau = radix_threshold(kS, rank, [&](int j) { return samp[j]; }, hist, scratch, nullptr,
+                          s_misc, a.status, &need, 2);
+  }
+  if (tid == 0) a.tau[lr] = tau;
+}
+
+// ---------------------------------------------------------------------------------
+// K7b: per (layer, row, chunk of the row's union entries): the entries whose upper bound
+// reaches tau, with their lower and upper bound keys, in index order in the chunk's region
+// (each warp keeps its matches in shared memory, then the warps' lists are concatenated),
+// and how many entries have a lower bound >= tau. A chunk with more matches than its
+// region (or a warp with more than its buffer) reports a count above the capacity.
+// ---------------------------------------------------------------------------------
+constexpr int kCollectThreads = 256;
+constexpr int kCollectWarps = kCollectThreads / 32;
+constexpr int kWarpBuf = 128;
+
+__global__ void __launch_bounds__(kCollectThreads) k7b_collect(TopkArgs a) {
+  __shared__ int s_cnt[kCollectWarps], s_lo[kCollectWarps];
+  __shared__ uint32_t s_buf[kCollectWarps][3][kWarpBuf];
+  const int lr = blockIdx.x / kTopkChunks, chunk = blockIdx.x - lr * kTopkChunks;
+  const int l = lr / a.R, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t tau = a.tau[lr];
+  if (tau == kTauDirect) return;
+  const int n = a.ucount[l];
+  const int per = (n + kTopkChunks - 1) / kTopkChunks;
+  const int c0 = min(n, chunk * per), c1 = min(n, c0 + per);
+  const uint32_t* s0 = a.sc0 + (size_t)lr * a.N;
+  const float* s1 = a.sc1 + (size_t)lr * a.N;
+  // contiguous warp segments of the chunk, in multiples of 32
+  const int seg = ((c1 - c0 + kCollectWarps - 1) / kCollectWarps + 31) & ~31;
+  const int beg = min(c1, c0 + warp * seg), end = min(c1, beg + seg);
+  constexpr int U = 8;
+  int cnt = 0, nlo = 0;
+  for (int i0 = beg; i0 < end; i0 += 32 * U) {
+    uint32_t hk[U], lk[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * 32 + lane;
+      hk[u] = i < end ? score_key(s1[i]) : 0u;
+      lk[u] = i < end ? s0[i] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * 32 + lane;
+      const bool take = i < end && hk[u] >= tau;
+      const uint32_t tm = __ballot_sync(0xffffffffu, take);
+      nlo += __popc(__ballot_sync(0xffffffffu, i < end && lk[u] >= tau));
+      const int p = cnt + __popc(tm & ((1u << lane) - 1u));
+      if (take && p < kWarpBuf) {
+        s_buf[warp][0][p] = (uint32_t)i;
+        s_buf[warp][1][p] = lk[u];
+        s_buf[warp][2][p] = hk[u];
+      }
+      cnt += __popc(tm);
+    }
+  }
+  if (lane == 0) { s_cnt[warp] = cnt; s_lo[warp] = nlo; }
+  __syncthreads();
+  int off = 0, total = 0, lo_total = 0;
+  bool over = false;
+  for (int w = 0; w < kCollectWarps; ++w) {
+    if (w == warp) off = total;
+    total += s_cnt[w];
+    lo_total += s_lo[w];
+    over |= s_cnt[w] > kWarpBuf;
+  }
+  const size_t rc = (size_t)lr * kTopkChunks + chunk;
+  if (over || total > kTopkChunkCap) {
+    if (tid == 0) { a.ccnt[rc] = kTopkChunkCap + 1; a.clo[rc] = lo_total; }
+    return;
+  }
+  if (tid == 0) { a.ccnt[rc] = total; a.clo[rc] = lo_total; }
+  const size_t plane = (size_t)gridDim.x * kTopkChunkCap;   // (L R chunks) x capacity
+  int32_t* reg = a.creg + rc * kTopkChunkCap;
+  for (int p = lane; p < cnt; p += 32) {
+    reg[off + p] = (int32_t)s_buf[warp][0][p];
+    reg[plane + off + p] = (int32_t)s_buf[warp][1][p];
+    reg[2 * plane + off + p] = (int32_t)s_buf[warp][2][p];
+  }
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   __shared__ int hist[256];
   __shared__ int scratch[33];
   __shared__ int s_misc[4];
@@ -817,6 +955,10 @@ __global__ void __launch_bounds__(kTopkThreads) k7_topk(TopkArgs a) {
   uint32_t* ckey = reinterpret_cast<uint32_t*>(cand + kCandCap);  // [kCandCap] keys
   float* qf = reinterpret_cast<float*>(ckey + kCandCap);          // [Hh][128]
   float* wf = qf + kScoreMaxHeads * 128;                          // [Hh]
+  // the collected entries in index order, with their lower and upper bound keys
+  int32_t* col_i = reinterpret_cast<int32_t*>(wf + kScoreMaxHeads);
+  uint32_t* col_lo = reinterpret_cast<uint32_t*>(col_i + kCollectCap);
+  uint32_t* col_hi = col_lo + kCollectCap;
 
   const int lr = blockIdx.x;
   const int l = lr / a.R;
@@ -840,22 +982,135 @@ __global__ void __launch_bounds__(kTopkThreads) k7_topk(TopkArgs a) {
 
   if (a.tc_mode) {
     const float* s1 = a.sc1 + (size_t)lr * a.N;
-    int need;
-    const uint32_t T = radix_threshold(
-        n, K, [&](int i) { return s0[i]; }, hist, scratch, r_key, s_misc, a.status, &need);
-    // Ordered gather of the candidates (upper bound reaches T), bounded by kCandCap.
-    const int m = ordered_take(
-        n, 0, [&](int i) { return score_key(s1[i]) >= T ? 2 : 0; },
-        [&](int p, int i) { if (p < kCandCap) cand[p] = i; }, s_eq, s_gt);
+    // Fast path: the entries collected by K7b (every entry whose upper bound reaches tau,
+    // in index order). If at least K of the row's entries have a lower bound >= tau, the
+    // K-th largest lower bound T over the row is among them and every candidate (upper
+    // bound >= T) was collected, so the rest works on the collection alone; otherwise (or
+    // on overflow) the exact two-pass path below runs instead.
+    int m = -1;
+    {
+      __shared__ int s_off[kTopkChunks + 1], s_bad, s_lo_total;
+      if (tid == 0) {
+        int total = 0, lo = 0, bad = 0;
+        for (int c = 0; c < kTopkChunks; ++c) {
+          const int cc = a.ccnt[(size_t)lr * kTopkChunks + c];
+          s_off[c] = total;
+          bad |= cc > kTopkChunkCap;
+          total += cc;
+          lo += a.clo[(size_t)lr * kTopkChunks + c];
+        }
+        s_off[kTopkChunks] = total;
+        s_bad = bad || total > kCollectCap;
+        s_lo_total = lo;
+      }
+      __syncthreads();
+      if (!s_bad && s_lo_total >= K) {
+        const int total = s_off[kTopkChunks];
+        const size_t plane = (size_t)gridDim.x * kTopkChunks * kTopkChunkCap;
+        for (int c = 0; c < kTopkChunks; ++c) {
+          const int32_t* reg = a.creg + ((size_t)lr * kTopkChunks + c) * kTopkChunkCap;
+          const int cc = s_off[c + 1] - s_off[c];
+          for (int p = tid; p < cc; p += blockDim.x) {
+            col_i[s_off[c] + p] = reg[p];
+            col_lo[s_off[c] + p] = (uint32_t)reg[plane + p];
+            col_hi[s_off[c] + p] = (uint32_t)reg[2 * plane + p];
+          }
+        }
+        __syncthreads();
+        int need;
+        const uint32_t T = radix_threshold(total, K, [&](int j) { return col_lo[j]; }, hist,
+                                           scratch, r_key, s_misc, a.status, &need);
+        m = ordered_take(
+            total, 0, [&](int j) { return col_hi[j] >= T ? 2 : 0; },
+            [&](int p, int j) { if (p < kCandCap) cand[p] = col_i[j]; }, s_eq, s_gt);
+      }
+      __syncthreads();
+    }
+    if (m < 0) {
+      int need;
+      const uint32_t T = radix_threshold(
+          n, K, [&](int i) { return s0[i]; }, hist, scratch, r_key, s_misc, a.status, &need);
+      // Ordered gather of the candidates (upper bound reaches T), bounded by kCandCap.
+      m = ordered_take(
+          n, 0, [&](int i) { return score_key(s1[i]) >= T ? 2 : 0; },
+          [&](int p, int i) { if (p < kCandCap) cand[p] = i; }, s_eq, s_gt);
+    }
     // This row's queries and weights as fp32.
     const uint16_t* qrow = a.q + (size_t)lr * a.Hh * 128;
-    for (int i = tid; i < a.Hh * 128; i += blockDim.x) qf[i] = bf16_bits_to_f32(qrow[i]);
+    // [i][head] layout: the lanes of a candidate (one per head) read adjacent words
+    for (int i = tid; i < a.Hh * 128; i += blockDim.x)
+      qf[(i & 127) * kScoreMaxHeads + (i >> 7)] = bf16_bits_to_f32(qrow[i]);
     for (int i = tid; i < a.Hh; i += blockDim.x) wf[i] = a.hw[(size_t)lr * a.Hh + i];
     __syncthreads();
     if (m <= kCandCap) {
-      for (int j = tid; j < m; j += blockDim.x) {
-        const int b = ui[cand[j]];
-        ckey[j] = score_key(canonical_score(qf, kbase + (size_t)b * 128, wf, a.Hh));
+      // Canonical scores of the candidates: their keys are staged in shared memory 64 at a
+      // time (double-buffered cp.async, rows padded to 272 bytes, in the space of the
+      // finished collection); one lane per head runs that head's chain over i ascending,
+      // then the candidate's first lane adds the heads in order.
+      // candidate entries -> block ids, all in one round of loads
+      for (int j = tid; j < m; j += blockDim.x) cand[j] = ui[cand[j]];
+      __syncthreads();
+      {
+        const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+        const int HP = a.Hh <= 8 ? 8 : 16, per_warp = 32 / HP;
+        const int slot = lane / HP, h = lane - slot * HP;
+        constexpr int kStageCands = 64, kKeyPitch = 272;
+        uint8_t* kst = reinterpret_cast<uint8_t*>(col_i);
+        // this row's queries as bf16, head h at qb + 272 h (rows 4 banks apart)
+        uint8_t* qb = kst + 2 * kStageCands * kKeyPitch;
+        {
+          const uint16_t* qrow = a.q + (size_t)lr * a.Hh * 128;
+          for (int i = tid; i < a.Hh * 16; i += blockDim.x)
+            *reinterpret_cast<uint4*>(qb + (i >> 4) * kKeyPitch + (i & 15) * 16) =
+                __ldg(reinterpret_cast<const uint4*>(qrow) + i);
+        }
+        const uint32_t kst_addr = static_cast<uint32_t>(__cvta_generic_to_shared(kst));
+        const int nchunk = (m + kStageCands - 1) / kStageCands;
+        auto stage = [&](int ch) {
+          const uint32_t dst = kst_addr + (uint32_t)((ch & 1) * kStageCands * kKeyPitch);
+          const int base = ch * kStageCands;
+          for (int p = tid; p < kStageCands * 16; p += blockDim.x) {
+            const int cj = p >> 4, piece = p & 15;
+            const bool v = base + cj < m;
+            const uint16_t* src = v ? kbase + (size_t)cand[base + cj] * 128 + piece * 8 : kbase;
+            cp_async16(dst + (uint32_t)(cj * kKeyPitch + piece * 16), src, v);
+          }
+          asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        if (nchunk > 0) stage(0);
+        for (int ch = 0; ch < nchunk; ++ch) {
+          if (ch + 1 < nchunk) {
+            stage(ch + 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+          } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+          }
+          __syncthreads();
+          const uint8_t* buf = kst + (ch & 1) * kStageCands * kKeyPitch;
+          for (int c0 = warp * per_warp; c0 < kStageCands; c0 += nwarps * per_warp) {
+            const int cj = c0 + slot, j = ch * kStageCands + cj;
+            float d = 0.0f;
+            if (j < m && h < a.Hh) {
+              const uint4* kr = reinterpret_cast<const uint4*>(buf + cj * kKeyPitch);
+              const uint4* qr = reinterpret_cast<const uint4*>(qb + h * kKeyPitch);
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const uint4 kv = kr[c], qv = qr[c];
+                d = fma2_bf16(qv.x, kv.x, d);
+                d = fma2_bf16(qv.y, kv.y, d);
+                d = fma2_bf16(qv.z, kv.z, d);
+                d = fma2_bf16(qv.w, kv.w, d);
+              }
+            }
+            float sc = 0.0f;
+            for (int hh = 0; hh < a.Hh; ++hh) {
+              const float dh = __shfl_sync(0xffffffffu, d, slot * HP + hh);
+              sc = __fmaf_rn(wf[hh], dh > 0.0f ? dh : 0.0f, sc);
+            }
+            if (j < m && h == 0) ckey[j] = score_key(sc);
+          }
+          __syncthreads();   // this buffer may be refilled now
+        }
       }
       __syncthreads();
       int need2;
@@ -864,7 +1119,7 @@ __global__ void __launch_bounds__(kTopkThreads) k7_topk(TopkArgs a) {
       const int taken = ordered_take(
           m, need2,
           [&](int j) { const uint32_t k = ckey[j]; return k > T2 ? 2 : (k == T2 ? 1 : 0); },
-          [&](int p, int j) { if (p < K) out[p] = ui[cand[j]]; }, s_eq, s_gt);
+          [&](int p, int j) { if (p < K) out[p] = cand[j]; }, s_eq, s_gt);
       if (tid == 0) {
         a.nsel[lr] = K;
         if (taken != K) flag_status(a.status, kStatusCheck);
@@ -937,6 +1192,10 @@ SelLayout sel_layout(const SelDims& d, bool caller_cidx) {
   L.urows = off; off += up((size_t)d.L * d.N);
   L.cscore = off; off += up(sizeof(float) * LR * (size_t)d.N);
   L.chi = off; off += up(sizeof(float) * LR * (size_t)d.N);
+  L.tau = off; off += up(sizeof(uint32_t) * LR);
+  L.ccnt = off; off += up(sizeof(int32_t) * LR * kTopkChunks);
+  L.clo = off; off += up(sizeof(int32_t) * LR * kTopkChunks);
+  L.creg = off; off += up(sizeof(int32_t) * 3 * LR * kTopkChunks * kTopkChunkCap);
   L.total = off;
   return L;
 }
@@ -993,12 +1252,16 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
                         const SelWorkspace& ws, bool tc, cudaStream_t s) {
   TopkArgs a{d.R, d.Hh, d.N, d.topk, d.key_stride, keys, q, head_w, ws.cidx, ws.ccount,
              ws.uidx, ws.ucount, reinterpret_cast<uint32_t*>(ws.cscore), ws.chi, sel, nsel,
-             ws.header, tc ? 1 : 0};
-  const size_t smem =
-      sizeof(int32_t) * kCandCap * 2 + sizeof(float) * (kScoreMaxHeads * 128 + kScoreMaxHeads);
+             ws.header, tc ? 1 : 0, ws.tau, ws.ccnt, ws.clo, ws.creg};
+  const size_t smem = sizeof(int32_t) * (kCandCap * 2 + kCollectCap * 3) +
+                      sizeof(float) * (kScoreMaxHeads * 128 + kScoreMaxHeads);
   cudaError_t err =
       cudaFuncSetAttribute(k7_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
+  if (tc) {
+    k7a_tau<<<d.L * d.R, kTopkThreads, 0, s>>>(a);
+    k7b_collect<<<d.L * d.R * kTopkChunks, kCollectThreads, 0, s>>>(a);
+  }
   k7_topk<<<d.L * d.R, kTopkThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
