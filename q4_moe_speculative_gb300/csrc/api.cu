@@ -198,7 +198,7 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(base, 0, 256, s) != cudaSuccess) return DS_ERR_CUDA;
-  if (launch_compact(d, a->mask, a->limit, ws, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (launch_compact(d, a->mask, a->limit, ws, caller, s) != cudaSuccess) return DS_ERR_CUDA;
   if (!mark(marks, 0, s)) return DS_ERR_CUDA;
   if (launch_score(d, a->keys, a->q, a->head_w, a->mask, a->limit, ws, tc, s) != cudaSuccess)
     return DS_ERR_CUDA;

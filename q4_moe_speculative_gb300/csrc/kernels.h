@@ -88,7 +88,7 @@ SelLayout sel_layout(const SelDims& d, bool caller_cidx);
 bool tc_scoring_supported(const SelDims& d, const uint16_t* keys, const uint16_t* q);
 
 cudaError_t launch_compact(const SelDims& d, const uint32_t* mask, const int32_t* limit,
-                           const SelWorkspace& ws, cudaStream_t s);
+                           const SelWorkspace& ws, bool want_cidx, cudaStream_t s);
 cudaError_t launch_score(const SelDims& d, const uint16_t* keys, const uint16_t* q,
                          const float* head_w, const uint32_t* mask, const int32_t* limit,
                          const SelWorkspace& ws, bool tc, cudaStream_t s);

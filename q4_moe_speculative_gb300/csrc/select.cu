@@ -151,7 +151,9 @@ __device__ __forceinline__ float canonical_score(const float* q, const uint16_t*
 // admitted words, then each warp scatters the admitted indices of 32 words with a ballot
 // over per-lane predicates (bit set and block below the causal limit). CTAs [L*R, L*R+L):
 // one per layer: the same over the union of the rows' admitted words, recording for each
-// union entry the rows that admit it, plus each union word's exclusive offset.
+// union entry the rows that admit it, plus each union word's exclusive offset. A row CTA
+// counts first and scatters only when its compacted index is wanted: when the caller
+// asked for it, or when the row admits at most top_k blocks (the top-k then copies it).
 // ---------------------------------------------------------------------------------
 struct CompactArgs {
   int L, R, N;
@@ -163,6 +165,8 @@ struct CompactArgs {
   int32_t* ucount;     // [L]
   uint8_t* urows;      // [L][N]
   int32_t* uwordoff;   // [L][W]
+  int topk;
+  int want_cidx;       // the caller passed cidx / ccount
 };
 
 __global__ void __launch_bounds__(kCompactThreads) k6_compact(CompactArgs a) {
@@ -173,7 +177,11 @@ __global__ void __launch_bounds__(kCompactThreads) k6_compact(CompactArgs a) {
   const int W = (N + 31) >> 5;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool union_cta = (int)blockIdx.x >= a.L * R;
-  const int l = union_cta ? (int)blockIdx.x - a.L * R : (int)blockIdx.x / R;
+  // union CTAs: one per (layer, chunk of kCompactThreads words)
+  const int P = (W + kCompactThreads - 1) / kCompactThreads;
+  const int uc = (int)blockIdx.x - a.L * R;
+  const int l = union_cta ? uc / P : (int)blockIdx.x / R;
+  const int uchunk = union_cta ? uc - l * P : 0;
   const int lr = blockIdx.x;   // meaningful for row CTAs only
   const uint32_t* mrow = a.mask + (size_t)(union_cta ? l * R : lr) * W;
   if (tid < R) {
@@ -183,8 +191,32 @@ __global__ void __launch_bounds__(kCompactThreads) k6_compact(CompactArgs a) {
   __syncthreads();
   const int lim_row = union_cta ? 0 : s_lim[lr - l * R];
 
+  if (!union_cta && !a.want_cidx) {
+    int c = 0;
+    for (int wi = tid; wi < W; wi += kCompactThreads) c += __popc(admitted_word(mrow, wi, lim_row));
+    int total;
+    block_excl_scan(c, scratch, &total);
+    if (total > a.topk) {
+      if (tid == 0) a.ccount[lr] = total;
+      return;
+    }
+  }
+
   int base = 0;
-  for (int c0 = 0; c0 < W; c0 += kCompactThreads) {
+  int c_first = 0, c_last = W;
+  if (union_cta) {
+    // this CTA's chunk, and the union entries of the words before it
+    c_first = uchunk * kCompactThreads;
+    c_last = min(W, c_first + kCompactThreads);
+    int c = 0;
+    for (int wi = tid; wi < c_first; wi += kCompactThreads) {
+      uint32_t mw = 0;
+      for (int r = 0; r < R; ++r) mw |= admitted_word(a.mask + ((size_t)l * R + r) * W, wi, s_lim[r]);
+      c += __popc(mw);
+    }
+    block_excl_scan(c, scratch, &base);
+  }
+  for (int c0 = c_first; c0 < c_last; c0 += kCompactThreads) {
     const int wi = c0 + tid;
     uint32_t mw = 0;
     if (wi < W) {
@@ -246,8 +278,8 @@ __global__ void __launch_bounds__(kCompactThreads) k6_compact(CompactArgs a) {
     __syncthreads();
   }
   if (tid == 0) {
-    if (union_cta) a.ucount[l] = base;
-    else a.ccount[lr] = base;
+    if (!union_cta) a.ccount[lr] = base;
+    else if (c_last == W) a.ucount[l] = base;
   }
 }
 
@@ -1207,10 +1239,12 @@ bool tc_scoring_supported(const SelDims& d, const uint16_t* keys, const uint16_t
 }
 
 cudaError_t launch_compact(const SelDims& d, const uint32_t* mask, const int32_t* limit,
-                           const SelWorkspace& ws, cudaStream_t s) {
+                           const SelWorkspace& ws, bool want_cidx, cudaStream_t s) {
   CompactArgs a{d.L, d.R, d.N, mask, limit, ws.cidx, ws.ccount, ws.uidx, ws.ucount, ws.urows,
-                ws.wordoff};
-  k6_compact<<<d.L * d.R + d.L, kCompactThreads, 0, s>>>(a);
+                ws.wordoff, d.topk, want_cidx ? 1 : 0};
+  const int W = (d.N + 31) / 32;
+  const int P = (W + kCompactThreads - 1) / kCompactThreads;
+  k6_compact<<<d.L * d.R + d.L * P, kCompactThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
