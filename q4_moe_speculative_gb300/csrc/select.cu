@@ -586,23 +586,25 @@ __global__ void __launch_bounds__(kTcThreads) k5_score_tc(ScoreArgs a) {
     {
       const int e = e0 + tid;
       const int ucnt = a.ucount[l];
-      // key norm of this thread's row (the order of the 16-byte granules does not matter)
-      float kss = 0.0f;
+      // key norm of this thread's row (the order of the 16-byte granules does not matter):
+      // bf16 squares fused into four fp32 sums (exact products, round to nearest). 128
+      // roundings of nonnegative sums stay below 2^-17 relative, so scaling the sum up by
+      // 1 + 2^-16 and rounding the root up keeps kn an upper bound of the norm.
+      float ka[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int hlf = 0; hlf < 2; ++hlf) {
         const uint8_t* kr = sp + hlf * (kKeyBytes / 2) + tid * 128;
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const uint4 u = *reinterpret_cast<const uint4*>(kr + (((g + tid) & 7) << 4));
-          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float lo = bf16_lo(wv[q]), hi = bf16_hi(wv[q]);
-            kss = __fmaf_ru(lo, lo, kss);
-            kss = __fmaf_ru(hi, hi, kss);
-          }
+          ka[0] = fma2_bf16(u.x, u.x, ka[0]);
+          ka[1] = fma2_bf16(u.y, u.y, ka[1]);
+          ka[2] = fma2_bf16(u.z, u.z, ka[2]);
+          ka[3] = fma2_bf16(u.w, u.w, ka[3]);
         }
       }
+      const float kss = __fmul_ru(__fadd_ru(__fadd_ru(ka[0], ka[1]), __fadd_ru(ka[2], ka[3])),
+                                  1.0000153f);
       const float kn = __fmul_ru(__fsqrt_ru(kss), 1.0000153f);
       float d[NPAD];
       const uint32_t lane_base = tbuf + ((uint32_t)(warp * 32) << 16);
