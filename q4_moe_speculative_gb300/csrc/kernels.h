@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>   // CUtensorMap
 #include <cuda_runtime.h>
 
 namespace dsmoe {
@@ -95,6 +96,16 @@ cudaError_t launch_score(const SelDims& d, const uint16_t* keys, const uint16_t*
 cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* q,
                         const float* head_w, int32_t* sel, int32_t* nsel,
                         const SelWorkspace& ws, bool tc, cudaStream_t s);
+
+// TMA tensor maps (cached by their parameters). q4_maps: one Q4 matrix of `rows` rows of K
+// values (K a multiple of 256) in boxes of `box_rows` rows by `box_blocks` Q4 blocks (a
+// multiple of 8): nibbles as [128-byte chunk][row][128 B] with the 128-byte swizzle, scales
+// [row][K/32]. key_tile_map: bf16 block keys [L][N][128] (layer stride key_stride values, a
+// multiple of 8) in boxes of 64 values x box_rows blocks, 128-byte swizzle.
+cudaError_t q4_maps(CUtensorMap* wq, CUtensorMap* wsc, Q4Ptr m, uint64_t rows, int K,
+                    int box_rows, int box_blocks);
+cudaError_t key_tile_map(CUtensorMap* out, const uint16_t* keys, int N, int L,
+                         int64_t key_stride, int box_rows);
 
 // Cached device properties of the current device.
 int device_sm_count();

@@ -37,7 +37,6 @@ namespace {
 
 constexpr int kCompactThreads = 1024;
 constexpr int kScoreThreads = 128;   // canonical scorer: one key per thread
-constexpr int kTcThreads = 128;      // tensor-core scorer: 4 warps = 128 TMEM lanes
 constexpr int kScoreMaxHeads = 16;
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
@@ -298,6 +297,8 @@ struct ScoreArgs {
   uint32_t* sc0;      // [L][R][N] by union entry: fp32 scores, or lower-bound keys
   float* sc1;         // [L][R][N] by union entry: upper bounds (tensor-core mode)
   uint32_t* status;
+  int tma;            // kmap is valid: tiles of 128 consecutive blocks come by TMA
+  CUtensorMap kmap;   // keys [L][N][128] bf16, boxes of 64 values x 128 blocks, 128B swizzle
 };
 
 // ---------------------------------------------------------------------------------
@@ -394,58 +395,149 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
 }
 
 // ---------------------------------------------------------------------------------
-// K5 (tensor-core mode): persistent CTAs of 4 warps; CTA c scores a contiguous range of
-// the layers' union tiles (128 union entries each). Keys and queries are gathered with
-// cp.async into a double-buffered 128-byte swizzled K-major layout (row r's 16-byte chunk
-// j of each 64-value half at r*128 + ((j ^ (r & 7)) * 16)), so tile i + 2 loads while tile i
-// is scored. Thread 0 issues the 8 tcgen05.mma (M = 128 keys, N = NPAD >= R*Hh, K = 16 each)
-// into the tile's TMEM accumulator and commits to an mbarrier; each warp then reads its 32
-// lanes (one key per thread) and writes the interval bounds for every row. Waits are
-// bounded; a give-up sets DS_ERR_TIMEOUT in the status word, waits once more (bounded) for
-// the MMAs already issued, frees TMEM and returns.
+// K5 (tensor-core mode): one persistent CTA per SM scores a contiguous range of the
+// layers' union tiles (128 union entries each). Roles:
+//  * two producer warps fill a ring of kStages stage buffers with each tile's keys in the
+//    128-byte swizzled K-major layout (row r's 16-byte chunk j of each 64-value half at
+//    r*128 + ((j ^ (r & 7)) * 16)). A tile of 128 consecutive block ids (the common case:
+//    the union of the rows' admitted blocks is dense) is two TMA boxes of 64 values x 128
+//    blocks that the copy engine swizzles; any other tile is gathered with 16-byte
+//    cp.async, published on the stage's `full` barrier once the warp's copies have landed
+//    (cp.async.wait_group, then a proxy fence), kLag tiles behind the newest one. The
+//    block ids, entry count and row masks of the next tile are loaded while the current
+//    one is issued; the tile's layer, first entry, count and row masks go to shared
+//    memory beside the stage, so the epilogue reads nothing from global memory. Producer
+//    warp 0 also stages each layer's queries (one of two slots, by layer parity) with their
+//    norm bounds and head weights;
+//  * two epilogue groups of 4 warps take alternate tiles; each has its own TMEM
+//    accumulator. The group's first thread issues the 8 tcgen05.mma (M = 128 keys,
+//    N = NPAD >= R*Hh, K = 16 each) and commits to the group's mbarrier; each warp then
+//    reads its 32 lanes (one key per thread) and writes the interval bounds for every row,
+//    and releases the stage on its `empty` barrier.
+// Waits are bounded; a give-up sets DS_ERR_TIMEOUT in the status word and an abort flag
+// that every role checks before its next wait; the group that issued MMAs waits once more
+// (bounded) for them before TMEM is freed.
 // ---------------------------------------------------------------------------------
-template <int NCH>
-__global__ void __launch_bounds__(kTcThreads) k5_score_tc(ScoreArgs a) {
-  constexpr int NPAD = NCH * 16;
-  constexpr uint32_t kCols = NPAD <= 32 ? 32 : (NPAD <= 64 ? 64 : 128);   // per buffer
-  constexpr uint32_t kKeyBytes = 128 * 256;       // one tile of keys
-  constexpr uint32_t kQBytes = NPAD * 256;        // one layer's queries
-  constexpr uint32_t kStageBytes = kKeyBytes + kQBytes;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_mma[2];
-  __shared__ uint32_t s_tmem;
-  __shared__ float s_w[2][NPAD];
-  __shared__ float s_qn[NPAD];
-  __shared__ float s_F[2][8];
-  __shared__ int s_total;
+constexpr int kTcProducerWarps = 2;
+constexpr int kTcGroups = 2;
+constexpr int kTcThreads = 32 * (kTcProducerWarps + 4 * kTcGroups);
 
-  const int R = a.R, Hh = a.Hh, RH = R * Hh, L = a.L, N = a.N;
+template <int NCH>
+struct TcGeom {
+  static constexpr int NPAD = NCH * 16;
+  static constexpr uint32_t kCols = NPAD <= 32 ? 32 : (NPAD <= 64 ? 64 : 128);  // per group
+  static constexpr uint32_t kKeyBytes = 128 * 256;   // one tile of keys
+  static constexpr uint32_t kQBytes = NPAD * 256;    // one layer's queries
+  static constexpr int kFit = (int)((227u * 1024u - 4096u - 2u * kQBytes) / kKeyBytes);
+  static constexpr int kStages = kFit < 6 ? kFit : 6;
+  static constexpr int kLag = kStages - kTcGroups;   // tiles in flight behind the newest
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kKeyBytes + 2 * (size_t)kQBytes;
+  static_assert(kLag >= 1, "stage ring too small");
+};
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sm100::smem_u32(bar)) : "memory");
+}
+// Barrier `id` over `n` threads that also returns whether `pred` held in all of them.
+__device__ __forceinline__ bool bar_and(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// Tile t of the layers' union tiles (128 entries each, empty layers skipped): its layer and
+// first entry; *total gets the number of tiles. Warp-cooperative, every lane gets the result.
+__device__ __forceinline__ void tile_cursor(const int32_t* ucount, int L, int t, int* l_out,
+                                            int* e_out, int* total) {
+  const int lane = threadIdx.x & 31;
+  int carry = 0;
+  *l_out = L;
+  *e_out = 0;
+  bool found = false;
+  for (int l0 = 0; l0 < L; l0 += 32) {
+    const int l = l0 + lane;
+    const int nt = l < L ? (ucount[l] + 127) >> 7 : 0;
+    int incl = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, carry + incl > t);
+    if (!found && hit) {
+      const int src = __ffs(hit) - 1;
+      const int excl = __shfl_sync(0xffffffffu, incl - nt, src);
+      *l_out = l0 + src;
+      *e_out = (t - carry - excl) * 128;
+      found = true;
+    }
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  *total = carry;
+}
+
+template <int NCH, int HH>
+__global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_constant__ ScoreArgs a) {
+  using G = TcGeom<NCH>;
+  constexpr int NPAD = G::NPAD, S = G::kStages, D = G::kLag;
+  constexpr uint32_t kCols = G::kCols, kKeyBytes = G::kKeyBytes, kQBytes = G::kQBytes;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[S];
+  __shared__ __align__(8) uint64_t bar_empty[S];
+  __shared__ __align__(8) uint64_t bar_mma[kTcGroups];
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  __shared__ float s_w[2][NPAD];
+  __shared__ float s_F[2][8];
+  __shared__ float s_qn[NPAD];
+  __shared__ int s_tl[S], s_te[S], s_tn[S];     // per stage: layer, first entry, entry count
+  __shared__ uint8_t s_trows[S][128];           // per stage: row masks of the 128 entries
+
+  const int R = a.R, Hh = a.Hh, RH = R * Hh, N = a.N;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const uint32_t raw = sm100::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* const stage_ptr0 = smem_raw + (base - raw);
-  const uint32_t stage_addr0 = base;
+  uint8_t* const base_ptr = smem_raw + (base - raw);
+  const uint32_t qslot_addr = base + (uint32_t)S * kKeyBytes;
 
-  // Tiles over all layers and this CTA's contiguous range.
-  if (tid == 0) {
-    int t = 0;
-    for (int l = 0; l < L; ++l) t += (a.ucount[l] + 127) >> 7;
-    s_total = t;
-  }
-  __syncthreads();
-  const int total = s_total;
+  // This CTA's tile range [t0, t1) and the cursor of t0 (same in every warp).
+  int total = 0, cl = 0, ce = 0;
+  tile_cursor(a.ucount, a.L, 0, &cl, &ce, &total);
   const int t0 = (int)(((long long)blockIdx.x * total) / gridDim.x);
   const int t1 = (int)(((long long)(blockIdx.x + 1) * total) / gridDim.x);
   if (t0 >= t1) return;
+  if (t0 > 0) tile_cursor(a.ucount, a.L, t0, &cl, &ce, &total);
+  const int n = t1 - t0;
 
   if (tid == 0) {
-    sm100::mbar_init(&bar_mma[0], 1);
-    sm100::mbar_init(&bar_mma[1], 1);
+    for (int s = 0; s < S; ++s) {
+      sm100::mbar_init(&bar_full[s], kTcProducerWarps);
+      sm100::mbar_init(&bar_empty[s], 4);
+    }
+    for (int g = 0; g < kTcGroups; ++g) sm100::mbar_init(&bar_mma[g], 1);
+    s_abort = 0;
     sm100::fence_mbar_init();
   }
   if (warp == 0) {
-    sm100::tmem_alloc(&s_tmem, 2 * kCols);
+    sm100::tmem_alloc(&s_tmem, kTcGroups * kCols);
     sm100::tmem_relinquish();
   }
   sm100::tc_fence_before();
@@ -453,150 +545,239 @@ __global__ void __launch_bounds__(kTcThreads) k5_score_tc(ScoreArgs a) {
   sm100::tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  // Tile t0 -> (layer, first entry): walk the layers once.
-  int cur_l = 0, cur_e0 = 0;
-  {
-    int t = 0;
-    for (; cur_l < L; ++cur_l) {
-      const int nt = (a.ucount[cur_l] + 127) >> 7;
-      if (t + nt > t0) { cur_e0 = (t0 - t) * 128; break; }
-      t += nt;
-    }
-  }
-  int is_l = cur_l, is_e0 = cur_e0;    // issue cursor
-  int stage_qlayer[2] = {-1, -1};       // layer whose queries each stage buffer holds
-  int norm_layer[2] = {-1, -1};         // layer whose norms / weights each stage has
-
   auto advance = [&](int& lcur, int& ecur) {
     ecur += 128;
     if (ecur >= a.ucount[lcur]) {
       ecur = 0;
       ++lcur;
-      while (lcur < L && a.ucount[lcur] == 0) ++lcur;
+      while (lcur < a.L && a.ucount[lcur] == 0) ++lcur;
+    }
+  };
+  auto give_up = [&]() {
+    if (lane == 0) {
+      s_abort = 1;
+      flag_status(a.status, kStatusTimeout);
     }
   };
 
-  auto issue = [&](int stage) {
-    const int l = is_l, e0 = is_e0;
-    const int ucnt = a.ucount[l];
-    const uint32_t sbase = stage_addr0 + (uint32_t)stage * kStageBytes;
-    const uint8_t* kbase8 = reinterpret_cast<const uint8_t*>(a.keys + (size_t)l * a.key_stride);
-    // keys: warp w copies rows w*32 .. w*32+31, two rows (512 contiguous bytes) per step;
-    // the block ids of the warp's 32 rows come from one coalesced load, then shuffles.
-    const int my_e = e0 + warp * 32 + lane;
-    const int my_b = my_e < ucnt ? a.uidx[(size_t)l * N + my_e] : 0;
+  if (warp < kTcProducerWarps) {
+    // ------------------------------------------------------------- producers -----
+    const int pw = warp;
+    int l = cl, e0 = ce;
+    int qlayer[2] = {-1, -1};   // layer staged in each query slot
+    int qlast[2] = {-1, -1};    // last tile (local index) that reads each slot
+    int pub = 0;                // next tile to publish on its full barrier
+    uint32_t tma_bits = 0;      // bit (j & 31): tile j came by TMA (its arrivals are done)
+    auto publish = [&](int last) {   // gathered tiles pub..last, whose copies have landed
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0)
+        for (int j = pub; j <= last; ++j)
+          if (!((tma_bits >> (j & 31)) & 1u)) mbar_arrive1(&bar_full[j % S]);
+      pub = last + 1;
+    };
+    auto pwait = [&](uint64_t* bar, uint32_t parity) {   // warp-uniform bounded wait
+      return __all_sync(0xffffffffu, sm100::mbar_wait(bar, parity, kWaitPolls));
+    };
+    // What the tile at (ll, ee) needs from global memory, loaded one tile ahead: the
+    // entry count of its layer, the block ids of this warp's 64 rows, the first and last
+    // block ids (a tile of 128 consecutive blocks is one TMA box pair) and, in warp 0, the
+    // row masks of its 128 entries (byte k of rw: entry ee + lane + 32k).
+    struct Pref {
+      int ucnt, id0, id1, bf, bl;
+      uint32_t rw;
+    };
+    auto prefetch = [&](int ll, int ee, Pref& p) {
+      p.ucnt = a.ucount[ll];
+      const int32_t* u = a.uidx + (size_t)ll * N;
+      const int r0 = ee + pw * 64 + lane, r1 = r0 + 32;
+      p.id0 = r0 < p.ucnt ? u[r0] : 0;
+      p.id1 = r1 < p.ucnt ? u[r1] : 0;
+      p.bf = u[ee];
+      p.bl = ee + 127 < p.ucnt ? u[ee + 127] : -1;
+      p.rw = 0;
+      if (pw == 0) {
+        const uint8_t* ur = a.urows + (size_t)ll * N;
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) {
-      const int rr = 2 * jj + (lane >> 4);
-      const int r = warp * 32 + rr;
-      const int c = lane & 15;
-      const bool v = e0 + r < ucnt;
-      const int b = __shfl_sync(0xffffffffu, my_b, rr);
-      const uint32_t dst = sbase + (uint32_t)(c >> 3) * (kKeyBytes / 2) + (uint32_t)r * 128u +
-                           (uint32_t)(((c & 7) ^ (r & 7)) << 4);
-      cp_async16(dst, kbase8 + (size_t)b * 256 + c * 16, v);
-    }
-    // queries of layer l, when this stage buffer holds another layer's
-    if (stage_qlayer[stage] != l) {
-      const uint8_t* qbase8 = reinterpret_cast<const uint8_t*>(a.q + (size_t)l * RH * 128);
-      for (int i = tid; i < NPAD * 16; i += kTcThreads) {
-        const int r = i >> 4, c = i & 15;
-        const uint32_t dst = sbase + kKeyBytes + (uint32_t)(c >> 3) * (kQBytes / 2) +
-                             (uint32_t)r * 128u + (uint32_t)(((c & 7) ^ (r & 7)) << 4);
-        cp_async16(dst, qbase8 + (size_t)(r < RH ? r : 0) * 256 + c * 16, r < RH);
+        for (int k = 0; k < 4; ++k) {
+          const int e = ee + lane + 32 * k;
+          if (e < p.ucnt) p.rw |= (uint32_t)ur[e] << (8 * k);
+        }
       }
-      stage_qlayer[stage] = l;
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    advance(is_l, is_e0);
-  };
-
-  const int n = t1 - t0;
-  issue(0);
-  if (n > 1) issue(1);
-  else asm volatile("cp.async.commit_group;" ::: "memory");
-  uint32_t phase[2] = {0u, 0u};
-  bool ok = true;
-
-  for (int i = 0; i < n; ++i) {
-    const int stage = i & 1;
-    const int l = cur_l, e0 = cur_e0;
-    uint8_t* const sp = stage_ptr0 + stage * kStageBytes;
-    const uint32_t sa = stage_addr0 + (uint32_t)stage * kStageBytes;
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-
-    if (norm_layer[stage] != l) {   // per-layer query norms, weights and F_r
-      const uint8_t* qt = sp + kKeyBytes;
-      if (tid < NPAD) {
-        float ss = 0.0f;
-#pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          const uint4* row = reinterpret_cast<const uint4*>(qt + hlf * (kQBytes / 2) + tid * 128);
-#pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const uint4 u = row[g];
-            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float lo = bf16_lo(wv[e]), hi = bf16_hi(wv[e]);
-              ss = __fmaf_ru(lo, lo, ss);
-              ss = __fmaf_ru(hi, hi, ss);
+    };
+    // One tile: `cur` holds its prefetched indices, `nxt` receives the next tile's. The
+    // loop below alternates two of these so that no copy waits for a load in flight.
+    auto step = [&](int i, const Pref& cur, Pref& nxt) -> bool {
+        const int s = i % S;
+        {  // the next tile's indices, in flight while this one is issued
+          int ln = l, en = e0;
+          advance(ln, en);
+          if (i + 1 < n) prefetch(ln, en, nxt);
+        }
+        if (s_abort) return false;
+        if (i >= S && !pwait(&bar_empty[s], ((i / S) - 1) & 1)) {
+          give_up();
+          return false;
+        }
+        const int slot = l & 1;
+        if (qlayer[slot] != l) {
+          // every tile issued so far is published, then (warp 0) the slot's readers drain
+          if (pub < i) {
+            cp_async_wait<0>();
+            publish(i - 1);
+          }
+          if (pw == 0) {
+            for (int u = (i - S + 1 > 0 ? i - S + 1 : 0); u <= qlast[slot]; ++u)
+              if (!pwait(&bar_empty[u % S], (u / S) & 1)) {
+                give_up();
+                return false;
+              }
+            // queries of layer l (rows >= R*Hh are zero), their norm bounds, weights and F_r
+            const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(a.q + (size_t)l * RH * 128);
+            const uint32_t qa = qslot_addr + (uint32_t)slot * kQBytes;
+            for (int p0 = 0; p0 < NPAD; p0 += 2) {
+              const int p = p0 + (lane >> 4), c = lane & 15;
+              uint4 v = make_uint4(0u, 0u, 0u, 0u);
+              if (p < RH) v = *reinterpret_cast<const uint4*>(qsrc + (size_t)p * 256 + c * 16);
+              const uint32_t dst = qa + (uint32_t)(c >> 3) * (kQBytes / 2) + (uint32_t)p * 128u +
+                                   (uint32_t)(((c & 7) ^ (p & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x),
+                           "r"(v.y), "r"(v.z), "r"(v.w)
+                           : "memory");
+              // sum of squares rounded upward at every step: an upper bound of ||q_p||^2
+              const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+              float ss = 0.0f;
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float lo = bf16_lo(wv[e]), hi = bf16_hi(wv[e]);
+                ss = __fmaf_ru(lo, lo, ss);
+                ss = __fmaf_ru(hi, hi, ss);
+              }
+  #pragma unroll
+              for (int o = 8; o >= 1; o >>= 1)
+                ss = __fadd_ru(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+              if (c == 0) s_qn[p] = __fmul_ru(__fsqrt_ru(ss), 1.0000153f);   // (1 + 2^-16)
+            }
+            for (int p = lane; p < NPAD; p += 32)
+              s_w[slot][p] = p < RH ? a.hw[(size_t)l * RH + p] : 0.0f;
+            __syncwarp();
+            if (lane < R) {
+              float F = 0.0f;
+              for (int h = 0; h < Hh; ++h)
+                F = __fmaf_ru(fabsf(s_w[slot][lane * Hh + h]), s_qn[lane * Hh + h], F);
+              s_F[slot][lane] = F;
             }
           }
+          qlayer[slot] = l;
         }
-        s_qn[tid] = __fmul_ru(__fsqrt_ru(ss), 1.0000153f);   // (1 + 2^-16) margin
-        s_w[stage][tid] = tid < RH ? a.hw[(size_t)l * RH + tid] : 0.0f;
-      }
-      __syncthreads();
-      if (tid < R) {
-        float F = 0.0f;
-        for (int h = 0; h < Hh; ++h)
-          F = __fmaf_ru(fabsf(s_w[stage][tid * Hh + h]), s_qn[tid * Hh + h], F);
-        s_F[stage][tid] = F;
-      }
-      norm_layer[stage] = l;
-      __syncthreads();
+        qlast[slot] = i;
+        if (pw == 0) {   // the tile's layer, first entry, entry count and row masks
+          if (lane == 0) {
+            s_tl[s] = l;
+            s_te[s] = e0;
+            s_tn[s] = cur.ucnt;
+          }
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) s_trows[s][lane + 32 * k] = (uint8_t)(cur.rw >> (8 * k));
+        }
+        const bool boxed = a.tma != 0 && e0 + 128 <= cur.ucnt && cur.bl - cur.bf == 127;
+        uint8_t* const sp = base_ptr + (size_t)s * kKeyBytes;
+        if (boxed) {
+          // 128 consecutive blocks: two boxes of 64 values x 128 blocks, swizzled by the copy
+          tma_bits |= 1u << (i & 31);
+          cp_async_commit();      // an empty group: one group per tile in either mode
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            if (pw == 0) {
+              sm100::mbar_arrive_expect_tx(&bar_full[s], kKeyBytes);
+              sm100::tma_load_3d(sp, &a.kmap, 0, cur.bf, l, &bar_full[s]);
+              sm100::tma_load_3d(sp + kKeyBytes / 2, &a.kmap, 64, cur.bf, l, &bar_full[s]);
+            } else {
+              mbar_arrive1(&bar_full[s]);
+            }
+          }
+        } else {
+          // gather: this warp's 64 rows, two rows (512 contiguous bytes) per step
+          tma_bits &= ~(1u << (i & 31));
+          const uint8_t* kbase8 =
+              reinterpret_cast<const uint8_t*>(a.keys + (size_t)l * a.key_stride);
+          const uint32_t sa = base + (uint32_t)s * kKeyBytes;
+  #pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int rr = 2 * jj + (lane >> 4);
+            const int r = pw * 64 + rr;
+            const int c = lane & 15;
+            const int b = __shfl_sync(0xffffffffu, jj < 16 ? cur.id0 : cur.id1, rr & 31);
+            const uint32_t dst = sa + (uint32_t)(c >> 3) * (kKeyBytes / 2) + (uint32_t)r * 128u +
+                                 (uint32_t)(((c & 7) ^ (r & 7)) << 4);
+            cp_async16(dst, kbase8 + (size_t)b * 256 + c * 16, e0 + r < cur.ucnt);
+          }
+          cp_async_commit();
+        }
+        if (i - D >= pub) {
+          cp_async_wait<D>();
+          publish(i - D);
+        }
+        advance(l, e0);
+        return true;
+    };
+    Pref pa, pb;
+    prefetch(l, e0, pa);
+    bool ok = true;
+    for (int i = 0; i < n && ok; i += 2) {
+      ok = step(i, pa, pb);
+      if (ok && i + 1 < n) ok = step(i + 1, pb, pa);
     }
-
-    const uint32_t tbuf = tmem + (uint32_t)stage * kCols;
-    if (tid == 0) {
-      sm100::tc_fence_after();
-      constexpr uint32_t idesc = sm100::idesc_bf16_f32(128, NPAD);
+    cp_async_wait<0>();
+    if (ok && pub < n) publish(n - 1);
+  } else {
+    // ------------------------------------------------------------- epilogue ------
+    const int g = (warp - kTcProducerWarps) >> 2;
+    const int row = (warp & 3) * 32 + lane;          // TMEM lane = key row of the tile
+    const bool leader = warp == kTcProducerWarps + 4 * g && lane == 0;
+    const int bar_id = 1 + g;
+    const uint32_t tbuf = tmem + (uint32_t)g * kCols;
+    uint32_t mphase = 0;
+    bool issued = false;    // this group has MMAs whose commit it has not observed
+    for (int i = g; i < n; i += kTcGroups) {
+      const int s = i % S;
+      bool ok = !s_abort && sm100::mbar_wait(&bar_full[s], (i / S) & 1, kWaitPolls);
+      ok = bar_and(bar_id, 128, ok);
+      if (!ok) {
+        if (warp == kTcProducerWarps + 4 * g) give_up();
+        break;
+      }
+      const int l = s_tl[s], e0 = s_te[s], ucnt = s_tn[s];
+      const int slot = l & 1;
+      const uint32_t sa = base + (uint32_t)s * kKeyBytes;
+      if (leader) {
+        sm100::tc_fence_after();
+        fence_proxy_async();
+        constexpr uint32_t idesc = sm100::idesc_bf16_f32(128, NPAD);
+        const uint32_t qa = qslot_addr + (uint32_t)slot * kQBytes;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t half = (uint32_t)(kk >> 2), step = (uint32_t)(kk & 3) * 32u;
-        const uint64_t ad = sm100::desc_k_sw128(sa + half * (kKeyBytes / 2) + step);
-        const uint64_t bd = sm100::desc_k_sw128(sa + kKeyBytes + half * (kQBytes / 2) + step);
-        sm100::mma_bf16(tbuf, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t half = (uint32_t)(kk >> 2), step = (uint32_t)(kk & 3) * 32u;
+          const uint64_t ad = sm100::desc_k_sw128(sa + half * (kKeyBytes / 2) + step);
+          const uint64_t bd = sm100::desc_k_sw128(qa + half * (kQBytes / 2) + step);
+          sm100::mma_bf16(tbuf, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        sm100::mma_commit(&bar_mma[g]);
       }
-      sm100::mma_commit(&bar_mma[stage]);
-    }
-    bool done = sm100::mbar_wait(&bar_mma[stage], phase[stage], kWaitPolls);
-    if (!done) sm100::mbar_wait(&bar_mma[stage], phase[stage], kWaitPolls);  // own MMAs
-    ok = __syncthreads_and(done) != 0;
-    if (!ok) {
-      if (tid == 0) flag_status(a.status, kStatusTimeout);
-      break;
-    }
-    phase[stage] ^= 1u;
-    sm100::tc_fence_after();
-
-    {
-      const int e = e0 + tid;
-      const int ucnt = a.ucount[l];
-      // key norm of this thread's row (the order of the 16-byte granules does not matter):
-      // bf16 squares fused into four fp32 sums (exact products, round to nearest). 128
-      // roundings of nonnegative sums stay below 2^-17 relative, so scaling the sum up by
-      // 1 + 2^-16 and rounding the root up keeps kn an upper bound of the norm.
+      issued = true;
+      const uint32_t rows = s_trows[s][row];
+      // key norm of this thread's row while the MMAs run (the order of the 16-byte granules
+      // does not matter): bf16 squares fused into four fp32 sums (exact products, round to
+      // nearest). 128 roundings of nonnegative sums stay below 2^-17 relative, so scaling
+      // the sum up by 1 + 2^-16 and rounding the root up keeps kn an upper bound of the norm.
       float ka[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int hlf = 0; hlf < 2; ++hlf) {
-        const uint8_t* kr = sp + hlf * (kKeyBytes / 2) + tid * 128;
+        const uint8_t* kr = base_ptr + (size_t)s * kKeyBytes + hlf * (kKeyBytes / 2) + row * 128;
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const uint4 u = *reinterpret_cast<const uint4*>(kr + (((g + tid) & 7) << 4));
+        for (int gg = 0; gg < 8; ++gg) {
+          const uint4 u = *reinterpret_cast<const uint4*>(kr + (((gg + row) & 7) << 4));
           ka[0] = fma2_bf16(u.x, u.x, ka[0]);
           ka[1] = fma2_bf16(u.y, u.y, ka[1]);
           ka[2] = fma2_bf16(u.z, u.z, ka[2]);
@@ -606,49 +787,72 @@ __global__ void __launch_bounds__(kTcThreads) k5_score_tc(ScoreArgs a) {
       const float kss = __fmul_ru(__fadd_ru(__fadd_ru(ka[0], ka[1]), __fadd_ru(ka[2], ka[3])),
                                   1.0000153f);
       const float kn = __fmul_ru(__fsqrt_ru(kss), 1.0000153f);
+      ok = sm100::mbar_wait(&bar_mma[g], mphase, kWaitPolls);
+      ok = bar_and(bar_id, 128, ok);
+      if (!ok) {
+        if (warp == kTcProducerWarps + 4 * g) give_up();
+        break;
+      }
+      issued = false;
+      mphase ^= 1u;
+      sm100::tc_fence_after();
       float d[NPAD];
-      const uint32_t lane_base = tbuf + ((uint32_t)(warp * 32) << 16);
+      const uint32_t lane_base = tbuf + ((uint32_t)((warp & 3) * 32) << 16);
 #pragma unroll
       for (int c = 0; c < NCH; ++c) sm100::tmem_ld16(lane_base + (uint32_t)(c * 16), d + c * 16);
+      sm100::tc_fence_before();   // the group barrier of the next tile orders the next MMA
+      const int e = e0 + row;
       if (e < ucnt) {
-        const uint32_t rows = a.urows[(size_t)l * N + e];
-        float s = 0.0f;
-        int r = 0, h = 0;
+        // interval bounds of row r's score: [s - eps, s + eps] with
+        // eps = 2^-10 * ||k|| * sum_h |w_h| ||q_h||, both rounded outward
+        auto emit = [&](int r, float sc) {
+          const size_t out = ((size_t)l * R + r) * N + e;
+          if (rows & (1u << r)) {
+            const float eps = __fmul_ru(__fmul_ru(kEpsRel, kn), s_F[slot][r]);
+            a.sc0[out] = score_key(__fsub_rd(sc, eps));
+            a.sc1[out] = __fadd_ru(sc, eps);
+          } else {
+            a.sc0[out] = kNoScoreKey;
+            a.sc1[out] = __uint_as_float(kMinusInfBits);
+          }
+        };
+        if constexpr (HH > 0) {   // head count known at compile time: static indices
 #pragma unroll
-        for (int p = 0; p < NPAD; ++p) {
-          if (p < RH) {
-            if (h == 0) s = 0.0f;
-            s = __fmaf_rn(s_w[stage][p], d[p] > 0.0f ? d[p] : 0.0f, s);
-            if (h == Hh - 1) {
-              const size_t out = ((size_t)l * R + r) * N + e;
-              if (rows & (1u << r)) {
-                const float eps = __fmul_ru(__fmul_ru(kEpsRel, kn), s_F[stage][r]);
-                a.sc0[out] = score_key(__fsub_rd(s, eps));
-                a.sc1[out] = __fadd_ru(s, eps);
-              } else {
-                a.sc0[out] = kNoScoreKey;
-                a.sc1[out] = __uint_as_float(kMinusInfBits);
+          for (int r = 0; r < NPAD / HH; ++r) {
+            if (r < R) {
+              float sc = 0.0f;
+#pragma unroll
+              for (int h = 0; h < HH; ++h) {
+                const float v = d[r * HH + h];
+                sc = __fmaf_rn(s_w[slot][r * HH + h], v > 0.0f ? v : 0.0f, sc);
               }
-              h = 0;
-              ++r;
-            } else {
-              ++h;
+              emit(r, sc);
             }
+          }
+        } else {                  // any head count: each row picks its columns by predicate
+#pragma unroll 1
+          for (int r = 0; r < R; ++r) {
+            const int p0 = r * Hh, p1 = p0 + Hh;
+            float sc = 0.0f;
+#pragma unroll
+            for (int p = 0; p < NPAD; ++p) {
+              const float v = d[p];
+              const float t = __fmaf_rn(s_w[slot][p], v > 0.0f ? v : 0.0f, sc);
+              sc = (p >= p0 && p < p1) ? t : sc;
+            }
+            emit(r, sc);
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&bar_empty[s]);   // keys, queries and weights read
     }
-    sm100::tc_fence_before();
-    __syncthreads();   // stage buffers and TMEM accumulator of this tile are free again
-    advance(cur_l, cur_e0);
-    if (i + 2 < n) issue(stage);
-    else asm volatile("cp.async.commit_group;" ::: "memory");
+    // MMAs issued but never observed complete: wait (bounded) before TMEM is freed
+    if (issued) sm100::mbar_wait(&bar_mma[g], mphase, kWaitPolls);
   }
-  (void)lane;
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
   sm100::tc_fence_before();
   __syncthreads();
-  if (warp == 0) sm100::tmem_dealloc(tmem, 2 * kCols);
+  if (warp == 0) sm100::tmem_dealloc(tmem, kTcGroups * kCols);
 }
 
 // ---------------------------------------------------------------------------------
@@ -1187,21 +1391,20 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   }
 }
 
-template <int NCH>
+template <int NCH, int HH>
 cudaError_t launch_tc(const SelDims& d, const ScoreArgs& a, cudaStream_t s) {
-  constexpr size_t stage = 128 * 256 + NCH * 16 * 256;
-  const size_t smem = 1024 + 2 * stage;
-  if (smem > 48 * 1024) {
-    cudaError_t err = cudaFuncSetAttribute(k5_score_tc<NCH>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-  }
-  // Enough CTAs to keep every SM busy; each takes a contiguous range of tiles.
+  const size_t smem = TcGeom<NCH>::kSmem;
+  ScoreArgs ta = a;
+  ta.tma = key_tile_map(&ta.kmap, a.keys, d.N, d.L, d.key_stride, 128) == cudaSuccess ? 1 : 0;
+  cudaError_t err = cudaFuncSetAttribute(k5_score_tc<NCH, HH>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  // One persistent CTA per SM; each takes a contiguous range of the union tiles.
   const long long tiles = (long long)((d.N + 127) / 128) * d.L;
-  int grid = device_sm_count() * 2;
+  int grid = device_sm_count();
   if (tiles < grid) grid = (int)tiles;
   if (grid < 1) grid = 1;
-  k5_score_tc<NCH><<<grid, kTcThreads, smem, s>>>(a);
+  k5_score_tc<NCH, HH><<<grid, kTcThreads, smem, s>>>(ta);
   return cudaGetLastError();
 }
 
@@ -1270,15 +1473,23 @@ cudaError_t launch_score(const SelDims& d, const uint16_t* keys, const uint16_t*
     return cudaGetLastError();
   }
   const int nch = (d.R * d.Hh + 15) / 16;
+  if (d.Hh == 8) {   // the common index-head count gets a static epilogue
+    switch (nch) {
+      case 1: return launch_tc<1, 8>(d, a, s);
+      case 2: return launch_tc<2, 8>(d, a, s);
+      case 3: return launch_tc<3, 8>(d, a, s);
+      case 4: return launch_tc<4, 8>(d, a, s);
+    }
+  }
   switch (nch) {
-    case 1: return launch_tc<1>(d, a, s);
-    case 2: return launch_tc<2>(d, a, s);
-    case 3: return launch_tc<3>(d, a, s);
-    case 4: return launch_tc<4>(d, a, s);
-    case 5: return launch_tc<5>(d, a, s);
-    case 6: return launch_tc<6>(d, a, s);
-    case 7: return launch_tc<7>(d, a, s);
-    case 8: return launch_tc<8>(d, a, s);
+    case 1: return launch_tc<1, 0>(d, a, s);
+    case 2: return launch_tc<2, 0>(d, a, s);
+    case 3: return launch_tc<3, 0>(d, a, s);
+    case 4: return launch_tc<4, 0>(d, a, s);
+    case 5: return launch_tc<5, 0>(d, a, s);
+    case 6: return launch_tc<6, 0>(d, a, s);
+    case 7: return launch_tc<7, 0>(d, a, s);
+    case 8: return launch_tc<8, 0>(d, a, s);
   }
   return cudaErrorInvalidValue;
 }
