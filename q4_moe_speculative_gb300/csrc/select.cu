@@ -397,7 +397,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
 // ---------------------------------------------------------------------------------
 // K5 (tensor-core mode): one persistent CTA per SM scores a contiguous range of the
 // layers' union tiles (128 union entries each). Roles:
-//  * two producer warps fill a ring of kStages stage buffers with each tile's keys in the
+//  * four producer warps fill a ring of kStages stage buffers with each tile's keys in the
 //    128-byte swizzled K-major layout (row r's 16-byte chunk j of each 64-value half at
 //    r*128 + ((j ^ (r & 7)) * 16)). A tile of 128 consecutive block ids (the common case:
 //    the union of the rows' admitted blocks is dense) is two TMA boxes of 64 values x 128
@@ -418,7 +418,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
 // that every role checks before its next wait; the group that issued MMAs waits once more
 // (bounded) for them before TMEM is freed.
 // ---------------------------------------------------------------------------------
-constexpr int kTcProducerWarps = 2;
+constexpr int kTcProducerWarps = 4;
+constexpr int kTcRowsPerProducer = 128 / kTcProducerWarps;   // 32: one block id per lane
 constexpr int kTcGroups = 2;
 constexpr int kTcThreads = 32 * (kTcProducerWarps + 4 * kTcGroups);
 
@@ -545,14 +546,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
   sm100::tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  auto advance = [&](int& lcur, int& ecur) {
-    ecur += 128;
-    if (ecur >= a.ucount[lcur]) {
-      ecur = 0;
-      ++lcur;
-      while (lcur < a.L && a.ucount[lcur] == 0) ++lcur;
-    }
-  };
   auto give_up = [&]() {
     if (lane == 0) {
       s_abort = 1;
@@ -564,6 +557,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
     // ------------------------------------------------------------- producers -----
     const int pw = warp;
     int l = cl, e0 = ce;
+    int lcnt = a.ucount[cl];    // entry count of layer l
     int qlayer[2] = {-1, -1};   // layer staged in each query slot
     int qlast[2] = {-1, -1};    // last tile (local index) that reads each slot
     int pub = 0;                // next tile to publish on its full barrier
@@ -579,30 +573,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
     auto pwait = [&](uint64_t* bar, uint32_t parity) {   // warp-uniform bounded wait
       return __all_sync(0xffffffffu, sm100::mbar_wait(bar, parity, kWaitPolls));
     };
-    // What the tile at (ll, ee) needs from global memory, loaded one tile ahead: the
-    // entry count of its layer, the block ids of this warp's 64 rows, the first and last
-    // block ids (a tile of 128 consecutive blocks is one TMA box pair) and, in warp 0, the
-    // row masks of its 128 entries (byte k of rw: entry ee + lane + 32k).
-    struct Pref {
-      int ucnt, id0, id1, bf, bl;
-      uint32_t rw;
+    // Next tile after (lcur, ecur) of a layer with cnt entries; empty layers are skipped.
+    auto padvance = [&](int& lcur, int& ecur, int& cnt) {
+      ecur += 128;
+      if (ecur >= cnt) {
+        ecur = 0;
+        for (++lcur; lcur < a.L; ++lcur)
+          if ((cnt = a.ucount[lcur]) > 0) break;
+      }
     };
-    auto prefetch = [&](int ll, int ee, Pref& p) {
-      p.ucnt = a.ucount[ll];
+    // What the tile at (ll, ee) needs from global memory, loaded one tile ahead and not
+    // touched until that tile is issued: the block id of this warp's row `lane`, the first
+    // and last block ids (a tile of 128 consecutive blocks is one TMA box pair) and, in
+    // warp 0, the row masks of the tile's entries ee + lane + 32k.
+    struct Pref {
+      int ucnt, id, bf, bl;
+      uint32_t rw[4];
+    };
+    auto prefetch = [&](int ll, int ee, int cnt, Pref& p) {
+      p.ucnt = cnt;
       const int32_t* u = a.uidx + (size_t)ll * N;
-      const int r0 = ee + pw * 64 + lane, r1 = r0 + 32;
-      p.id0 = r0 < p.ucnt ? u[r0] : 0;
-      p.id1 = r1 < p.ucnt ? u[r1] : 0;
+      const int r0 = ee + pw * kTcRowsPerProducer + lane;
+      p.id = r0 < cnt ? u[r0] : 0;
       p.bf = u[ee];
-      p.bl = ee + 127 < p.ucnt ? u[ee + 127] : -1;
-      p.rw = 0;
-      if (pw == 0) {
-        const uint8_t* ur = a.urows + (size_t)ll * N;
+      p.bl = ee + 127 < cnt ? u[ee + 127] : -1;
+      const uint8_t* ur = a.urows + (size_t)ll * N;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int e = ee + lane + 32 * k;
-          if (e < p.ucnt) p.rw |= (uint32_t)ur[e] << (8 * k);
-        }
+      for (int k = 0; k < 4; ++k) {
+        const int e = ee + lane + 32 * k;
+        p.rw[k] = (pw == 0 && e < cnt) ? (uint32_t)ur[e] : 0u;
       }
     };
     // One tile: `cur` holds its prefetched indices, `nxt` receives the next tile's. The
@@ -610,9 +609,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
     auto step = [&](int i, const Pref& cur, Pref& nxt) -> bool {
         const int s = i % S;
         {  // the next tile's indices, in flight while this one is issued
-          int ln = l, en = e0;
-          advance(ln, en);
-          if (i + 1 < n) prefetch(ln, en, nxt);
+          int ln = l, en = e0, cn = lcnt;
+          padvance(ln, en, cn);
+          if (i + 1 < n) prefetch(ln, en, cn, nxt);
         }
         if (s_abort) return false;
         if (i >= S && !pwait(&bar_empty[s], ((i / S) - 1) & 1)) {
@@ -678,7 +677,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
             s_tn[s] = cur.ucnt;
           }
   #pragma unroll
-          for (int k = 0; k < 4; ++k) s_trows[s][lane + 32 * k] = (uint8_t)(cur.rw >> (8 * k));
+          for (int k = 0; k < 4; ++k) s_trows[s][lane + 32 * k] = (uint8_t)cur.rw[k];
         }
         const bool boxed = a.tma != 0 && e0 + 128 <= cur.ucnt && cur.bl - cur.bf == 127;
         uint8_t* const sp = base_ptr + (size_t)s * kKeyBytes;
@@ -698,19 +697,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
             }
           }
         } else {
-          // gather: this warp's 64 rows, two rows (512 contiguous bytes) per step
+          // gather: this warp's 32 rows, two rows (512 contiguous bytes) per step
           tma_bits &= ~(1u << (i & 31));
           const uint8_t* kbase8 =
               reinterpret_cast<const uint8_t*>(a.keys + (size_t)l * a.key_stride);
           const uint32_t sa = base + (uint32_t)s * kKeyBytes;
-  #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
+#pragma unroll
+          for (int jj = 0; jj < kTcRowsPerProducer / 2; ++jj) {
             const int rr = 2 * jj + (lane >> 4);
-            const int r = pw * 64 + rr;
+            const int r = pw * kTcRowsPerProducer + rr;
             const int c = lane & 15;
-            const int b = __shfl_sync(0xffffffffu, jj < 16 ? cur.id0 : cur.id1, rr & 31);
-            const uint32_t dst = sa + (uint32_t)(c >> 3) * (kKeyBytes / 2) + (uint32_t)r * 128u +
-                                 (uint32_t)(((c & 7) ^ (r & 7)) << 4);
+            const int b = __shfl_sync(0xffffffffu, cur.id, rr);
+            const uint32_t dst = sa + (uint32_t)(c >> 3) * (kKeyBytes / 2) +
+                                 (uint32_t)r * 128u + (uint32_t)(((c & 7) ^ (r & 7)) << 4);
             cp_async16(dst, kbase8 + (size_t)b * 256 + c * 16, e0 + r < cur.ucnt);
           }
           cp_async_commit();
@@ -719,11 +718,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
           cp_async_wait<D>();
           publish(i - D);
         }
-        advance(l, e0);
+        padvance(l, e0, lcnt);
         return true;
     };
     Pref pa, pb;
-    prefetch(l, e0, pa);
+    prefetch(l, e0, lcnt, pa);
     bool ok = true;
     for (int i = 0; i < n && ok; i += 2) {
       ok = step(i, pa, pb);
