@@ -631,31 +631,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
                 give_up();
                 return false;
               }
-            // queries of layer l (rows >= R*Hh are zero), their norm bounds, weights and F_r
+            // queries of layer l (rows >= R*Hh are zero) in the swizzled K-major layout, all
+            // copies in flight at once, then their norm bounds, the weights and F_r
             const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(a.q + (size_t)l * RH * 128);
             const uint32_t qa = qslot_addr + (uint32_t)slot * kQBytes;
-            for (int p0 = 0; p0 < NPAD; p0 += 2) {
-              const int p = p0 + (lane >> 4), c = lane & 15;
-              uint4 v = make_uint4(0u, 0u, 0u, 0u);
-              if (p < RH) v = *reinterpret_cast<const uint4*>(qsrc + (size_t)p * 256 + c * 16);
+            for (int idx = lane; idx < NPAD * 16; idx += 32) {
+              const int p = idx >> 4, c = idx & 15;
               const uint32_t dst = qa + (uint32_t)(c >> 3) * (kQBytes / 2) + (uint32_t)p * 128u +
                                    (uint32_t)(((c & 7) ^ (p & 7)) << 4);
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x),
-                           "r"(v.y), "r"(v.z), "r"(v.w)
-                           : "memory");
+              cp_async16(dst, qsrc + (size_t)(p < RH ? p : 0) * 256 + c * 16, p < RH);
+            }
+            cp_async_commit();
+            cp_async_wait<0>();     // no tile's copies are outstanding here
+            __syncwarp();
+            const uint8_t* qp = base_ptr + (size_t)S * kKeyBytes + (size_t)slot * kQBytes;
+            for (int p = lane; p < NPAD; p += 32) {
               // sum of squares rounded upward at every step: an upper bound of ||q_p||^2
-              const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
               float ss = 0.0f;
-  #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float lo = bf16_lo(wv[e]), hi = bf16_hi(wv[e]);
-                ss = __fmaf_ru(lo, lo, ss);
-                ss = __fmaf_ru(hi, hi, ss);
+#pragma unroll 4
+              for (int c = 0; c < 16; ++c) {
+                const uint4 v = *reinterpret_cast<const uint4*>(
+                    qp + (c >> 3) * (kQBytes / 2) + p * 128 + (((c & 7) ^ (p & 7)) << 4));
+                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float lo = bf16_lo(wv[e]), hi = bf16_hi(wv[e]);
+                  ss = __fmaf_ru(lo, lo, ss);
+                  ss = __fmaf_ru(hi, hi, ss);
+                }
               }
-  #pragma unroll
-              for (int o = 8; o >= 1; o >>= 1)
-                ss = __fadd_ru(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-              if (c == 0) s_qn[p] = __fmul_ru(__fsqrt_ru(ss), 1.0000153f);   // (1 + 2^-16)
+              s_qn[p] = __fmul_ru(__fsqrt_ru(ss), 1.0000153f);   // (1 + 2^-16) margin
             }
             for (int p = lane; p < NPAD; p += 32)
               s_w[slot][p] = p < RH ? a.hw[(size_t)l * RH + p] : 0.0f;

@@ -189,3 +189,26 @@ def test_status_word_clean(dsm):
     dsm.select_blocks(inp["keys"], inp["q"], inp["head_w"], inp["mask"], inp["limit"], 512,
                       workspace=ws)
     assert dsm.workspace_status(ws) == 0
+
+
+@pytest.mark.parametrize("canonical", [False, True])
+def test_mixed_density_and_empty_layers(dsm, canonical):
+    # layer 0: every block below 4000 admitted, 10% above; layer 1: limit 0 (nothing);
+    # layer 2: 20% everywhere; layer 3: every block, limits ending inside a 128-block tile
+    shape = synth.SelectShape(L=4, R=3, Hh=8, N=9000, topk=512)
+    inp = synth.select_inputs(shape, seed=8, shared_mask=False)
+    rng = np.random.default_rng(8)
+    N = shape.N
+    bits = np.zeros((4, 3, N), bool)
+    bits[0, :, :4000] = True
+    bits[0, :, 4000:] = rng.random((3, N - 4000)) < 0.1
+    bits[1] = rng.random((3, N)) < 0.7
+    bits[2] = rng.random((3, N)) < 0.2
+    bits[3] = True
+    limit = np.full((4, 3), N, dtype=np.int32)
+    limit[1] = 0
+    limit[3] = [N - 37, N - 100, 5000]
+    inp["mask"] = torch.from_numpy(synth.pack_bits(bits).view(np.int32).copy())
+    inp["limit"] = torch.from_numpy(limit)
+    dev, _ = check(dsm, inp, shape.topk, canonical=canonical)
+    assert np.all(dev[1][1] == 0)
