@@ -1,6 +1,7 @@
 // common.cuh — device helpers shared by the kernels of libdsmoe.so (sm_103a).
 #pragma once
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -22,6 +23,30 @@ struct WsHeader {
   uint32_t reserved[62];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// Programmatic dependent launch: a grid launched with launch_pdl may start while the grid
+// before it in the stream finishes; pdl_wait() returns once that grid has completed and its
+// memory operations are visible. pdl_trigger() lets the next grid start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Exp, typename... Act>
+cudaError_t launch_pdl(void (*kernel)(Exp...), int grid, int block, size_t smem, cudaStream_t s,
+                       Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
+}
 
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bit) {
   atomicOr(status, bit);

@@ -1088,6 +1088,7 @@ __global__ void __launch_bounds__(kTopkThreads) k7a_tau(TopkArgs a) {
   __shared__ int scratch[33];
   __shared__ int s_misc[4];
   __shared__ uint32_t samp[2048];
+  pdl_wait();   // the scores and the compaction are complete
   const int lr = blockIdx.x, l = lr / a.R, tid = threadIdx.x;
   const int K = a.K;
   if (a.ccount[lr] <= K) {
@@ -1108,6 +1109,7 @@ __global__ void __launch_bounds__(kTopkThreads) k7a_tau(TopkArgs a) {
                           s_misc, a.status, &need, 2);
   }
   if (tid == 0) a.tau[lr] = tau;
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------------
@@ -1126,6 +1128,7 @@ __global__ void __launch_bounds__(kCollectThreads) k7b_collect(TopkArgs a) {
   __shared__ uint32_t s_buf[kCollectWarps][3][kWarpBuf];
   const int lr = blockIdx.x / kTopkChunks, chunk = blockIdx.x - lr * kTopkChunks;
   const int l = lr / a.R, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();   // tau of every row is complete
   const uint32_t tau = a.tau[lr];
   if (tau == kTauDirect) return;
   const int n = a.ucount[l];
@@ -1177,6 +1180,7 @@ __global__ void __launch_bounds__(kCollectThreads) k7b_collect(TopkArgs a) {
     return;
   }
   if (tid == 0) { a.ccnt[rc] = total; a.clo[rc] = lo_total; }
+  pdl_trigger();
   const size_t plane = (size_t)gridDim.x * kTopkChunkCap;   // (L R chunks) x capacity
   int32_t* reg = a.creg + rc * kTopkChunkCap;
   for (int p = lane; p < cnt; p += 32) {
@@ -1202,6 +1206,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   uint32_t* col_lo = reinterpret_cast<uint32_t*>(col_i + kCollectCap);
   uint32_t* col_hi = col_lo + kCollectCap;
 
+  pdl_wait();   // the collection (or, in canonical mode, the scores) is complete
   const int lr = blockIdx.x;
   const int l = lr / a.R;
   const int tid = threadIdx.x;
@@ -1277,11 +1282,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
           n, 0, [&](int i) { return score_key(s1[i]) >= T ? 2 : 0; },
           [&](int p, int i) { if (p < kCandCap) cand[p] = i; }, s_eq, s_gt);
     }
-    // This row's queries and weights as fp32.
-    const uint16_t* qrow = a.q + (size_t)lr * a.Hh * 128;
-    // [i][head] layout: the lanes of a candidate (one per head) read adjacent words
-    for (int i = tid; i < a.Hh * 128; i += blockDim.x)
-      qf[(i & 127) * kScoreMaxHeads + (i >> 7)] = bf16_bits_to_f32(qrow[i]);
+    // This row's head weights (fp32).
     for (int i = tid; i < a.Hh; i += blockDim.x) wf[i] = a.hw[(size_t)lr * a.Hh + i];
     __syncthreads();
     if (m <= kCandCap) {
@@ -1368,7 +1369,14 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       }
       return;
     }
-    // Too many candidates (e.g. heavy ties): canonical scores for the whole row.
+    // Too many candidates (e.g. heavy ties): canonical scores for the whole row, with the
+    // row's queries as fp32 in the [i][head] layout (the lanes of a block read adjacent words).
+    {
+      const uint16_t* qrow = a.q + (size_t)lr * a.Hh * 128;
+      for (int i = tid; i < a.Hh * 128; i += blockDim.x)
+        qf[(i & 127) * kScoreMaxHeads + (i >> 7)] = bf16_bits_to_f32(qrow[i]);
+      __syncthreads();
+    }
     for (int i = tid; i < n; i += blockDim.x) {
       const bool adm = __float_as_uint(s1[i]) != kMinusInfBits;
       s0[i] = adm ? __float_as_uint(canonical_score(qf, kbase + (size_t)ui[i] * 128, wf, a.Hh))
@@ -1510,11 +1518,11 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
       cudaFuncSetAttribute(k7_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   if (tc) {
-    k7a_tau<<<d.L * d.R, kTopkThreads, 0, s>>>(a);
-    k7b_collect<<<d.L * d.R * kTopkChunks, kCollectThreads, 0, s>>>(a);
+    if ((err = launch_pdl(k7a_tau, d.L * d.R, kTopkThreads, 0, s, a)) != cudaSuccess) return err;
+    err = launch_pdl(k7b_collect, d.L * d.R * kTopkChunks, kCollectThreads, 0, s, a);
+    if (err != cudaSuccess) return err;
   }
-  k7_topk<<<d.L * d.R, kTopkThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k7_topk, d.L * d.R, kTopkThreads, smem, s, a);
 }
 
 }  // namespace dsmoe
