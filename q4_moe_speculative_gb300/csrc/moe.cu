@@ -18,9 +18,11 @@
 // block's fp16 scale is applied exactly to that block's two MMAs. Widening a 32-bit word
 // of 8 nibbles costs three shifts, four AND-ORs that put nibbles in the mantissa of the
 // bf16 number 128 + nibble, and four bf16x2 subtractions of 136 (exact q = nibble - 8).
-// Weights reach shared memory as whole row segments of up to 1 KB by 1D bulk copies
-// (long contiguous runs are what HBM serves at full bandwidth), in a ring of CTA-wide
-// stages completed by mbarriers.
+// A producer warp streams the weights into a ring of CTA-wide stages completed by
+// mbarriers: as TMA boxes (a 3D view of the nibbles, [128-byte chunk][row][128 bytes],
+// with the 128-byte swizzle, and a 2D box of the scales) when the rows are whole 128-byte
+// chunks and the scales 16-byte aligned, else as per-row 1D bulk copies of up to 1 KB and
+// 4-byte scale copies.
 #include <climits>
 #include <utility>
 
