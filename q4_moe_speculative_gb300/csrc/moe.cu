@@ -630,7 +630,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k3_gate_up(const __grid_consta
 // ---------------------------------------------------------------------------------
 // K4: down projection. A unit is (expert slot u, a group of RS consecutive rows of H);
 // the 16 consumer warps split a stage (one K chunk of up to 4096 values of the group's
-// rows) into RS/16 row tiles x WK K slices of 8 blocks. CTA b takes a contiguous range of
+// rows) into RS/16 row tiles x WK K slices of BPS blocks (16 where two stages fit, else 8;
+// the larger slice halves the per-stage overhead per weight byte). CTA b takes a contiguous range of
 // units, so consecutive stages mostly belong to one expert and its h (the B operand, kept
 // in shared memory) is reloaded only when the expert or the chunk changes. The WK slice
 // partials of a row tile are added in slice order and written to o[row][slot] (fp32);
@@ -641,12 +642,12 @@ struct DownGeom {
   int nb, KC, cbmax, WK, TPS, RS, NGR, qs_pitch, sc_pitch, h_pitch, stage_bytes, boxed;
 };
 
-__host__ __device__ inline DownGeom down_geom(int H, int I) {
+__host__ __device__ inline DownGeom down_geom(int H, int I, int bps) {
   DownGeom d{};
   d.nb = I >> 5;
   d.KC = (d.nb + kChunkBlocks - 1) / kChunkBlocks;
   d.cbmax = d.nb < kChunkBlocks ? d.nb : kChunkBlocks;
-  const int slices = (d.cbmax + 7) / 8;
+  const int slices = (d.cbmax + bps - 1) / bps;
   d.WK = slices <= 1 ? 1 : (slices <= 2 ? 2 : (slices <= 4 ? 4 : (slices <= 8 ? 8 : 16)));
   d.TPS = kConsumerWarps / d.WK;
   d.RS = 16 * d.TPS;
@@ -674,11 +675,14 @@ __host__ __device__ constexpr size_t dn_red_bytes(int R) {
   return 2ull * kConsumerWarps * 16 * (size_t)R * 4;
 }
 
+template <int BPS>
 __global__ void __launch_bounds__(kMmaThreads, 1) k4_down(const __grid_constant__ DownArgs a) {
   extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t s_rowmask[kMaxUnion];
+  __shared__ __align__(8) int8_t s_slot[kMaxUnion][8];
   uint8_t* smem = align1024(smem_raw);
   const int R = a.R, H = a.H, I = a.I, k = a.k, ring = a.ring;
-  const DownGeom dg = down_geom(H, I);
+  const DownGeom dg = down_geom(H, I, BPS);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
   const size_t row_qs = (size_t)I / 2;
@@ -742,23 +746,25 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k4_down(const __grid_constant_
     pdl_wait();
   } else {
     pdl_wait();      // h is complete from here on
+    // the union's row masks and rank slots, read every stage, kept in shared memory
+    for (int i = tid; i < rt->n_union; i += kConsumers) {
+      s_rowmask[i] = rt->rowmask[i];
+      *reinterpret_cast<uint2*>(s_slot[i]) = *reinterpret_cast<const uint2*>(rt->slot[i]);
+    }
+    consumer_sync();
     const int rtl = warp / dg.WK, ks = warp - rtl * dg.WK;   // row tile, K slice
     const int r = rtl * 16 + g;                              // this lane's first row
-    int woff[8];
-    int r8_q, soff, r8_s;
-    if (a.boxed) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) woff[j] = (ks * dg.RS + r) * 128 + ((j ^ (r & 7)) << 4) + q * 4;
-      r8_q = 8 * 128;
-      soff = box_qs + r * (dg.cbmax * 2) + ks * 16;
-      r8_s = 8 * dg.cbmax * 2;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) woff[j] = r * dg.qs_pitch + ks * 128 + j * 16 + q * 4;
-      r8_q = 8 * dg.qs_pitch;
-      soff = dg.RS * dg.qs_pitch + r * dg.sc_pitch + ks * 16;
-      r8_s = 8 * dg.sc_pitch;
-    }
+    // byte offset in a stage of word q of block j of this warp's slice (row r; + r8_q for
+    // row r + 8), and of the slice's scales of row r (+ r8_s for row r + 8)
+    auto woff = [&](int j) {
+      const int b = ks * BPS + j;
+      return a.boxed ? ((b >> 3) * dg.RS + r) * 128 + (((b & 7) ^ (r & 7)) << 4) + q * 4
+                     : r * dg.qs_pitch + b * 16 + q * 4;
+    };
+    const int r8_q = a.boxed ? 8 * 128 : 8 * dg.qs_pitch;
+    const int soff = a.boxed ? box_qs + r * (dg.cbmax * 2) + ks * (2 * BPS)
+                             : dg.RS * dg.qs_pitch + r * dg.sc_pitch + ks * (2 * BPS);
+    const int r8_s = a.boxed ? 8 * dg.cbmax * 2 : 8 * dg.sc_pitch;
     int h_tag = -1;     // (expert slot, chunk) whose h is staged
     int buf = 0;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -767,17 +773,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k4_down(const __grid_constant_
       const int n = u_begin + f / dg.KC, c = f % dg.KC;
       const int u = n / dg.NGR, grp = n - u * dg.NGR;
       const int cb = min(kChunkBlocks, dg.nb - c * kChunkBlocks);
-      const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : rt->rowmask[u - 1];
+      const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : s_rowmask[u - 1];
       const int tag = u * dg.KC + c;
       if (tag != h_tag) {
-        // h of the expert's rows for this chunk: [verify row][values], 16-byte pieces. Rows
-        // that do not use the expert keep stale values; their MMA columns are never read.
+        // h of the expert's rows for this chunk: [verify row][values], 16-byte pieces, then
+        // each piece put in MMA pair order in place. Rows that do not use the expert keep
+        // stale values; their MMA columns are never read.
         consumer_sync();   // every consumer is done with the previous h
         const int per_row = cb * 4;
         for (int p = tid; p < R * per_row; p += kConsumers) {
           const int rr = p / per_row, pp = p - rr * per_row;
           if ((rowmask >> rr) & 1u) {
-            const int slot_r = (u == 0) ? 0 : rt->slot[u - 1][rr];
+            const int slot_r = (u == 0) ? 0 : s_slot[u - 1][rr];
             cp_async16(hs + rr * dg.h_pitch + pp * 16,
                        a.h + ((size_t)rr * (1 + k) + slot_r) * I + c * (kChunkBlocks * 32) + pp * 8,
                        true);
@@ -785,56 +792,86 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k4_down(const __grid_constant_
         }
         cp_async_commit();
         cp_async_wait<0>();
+        for (int p = tid; p < R * per_row; p += kConsumers) {
+          const int rr = p / per_row, pp = p - rr * per_row;
+          if ((rowmask >> rr) & 1u) {
+            uint4* hp = reinterpret_cast<uint4*>(hs + rr * dg.h_pitch + pp * 16);
+            *hp = pair_order(*hp);
+          }
+        }
         consumer_sync();
         h_tag = tag;
       }
       if (!mbar_wait(&full[slot], (f / ring) & 1, kWaitPolls)) timed_out = true;
       const uint8_t* st = stages + (size_t)slot * dg.stage_bytes;
       const int row_t = grp * dg.RS + rtl * 16;         // first row of this warp's tile
-      const int nv = max(0, min(8, cb - 8 * ks));
+      const int nv = max(0, min(BPS, cb - BPS * ks));
       if (nv > 0 && row_t < H) {
-        const uint4 s0v = *reinterpret_cast<const uint4*>(st + soff);
-        const uint4 s8v = *reinterpret_cast<const uint4*>(st + soff + r8_s);
-        float s0[2][4], s8[2][4];
-        widen_scales(make_uint2(s0v.x, s0v.y), s0[0]);
-        widen_scales(make_uint2(s0v.z, s0v.w), s0[1]);
-        widen_scales(make_uint2(s8v.x, s8v.y), s8[0]);
-        widen_scales(make_uint2(s8v.z, s8v.w), s8[1]);
-        const uint8_t* hb = hs + g * dg.h_pitch + ks * 512 + q * 16;
+        const uint8_t* hb = hs + g * dg.h_pitch + ks * (BPS * 64) + q * 16;
+        // four blocks at a time: scales, activations and weights loaded before the MMAs
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (j < nv) {
-            const uint4 X = pair_order(*reinterpret_cast<const uint4*>(hb + j * 64));
-            const uint8_t* w = st + woff[j];
-            float d[4];
-            q4_block_mma(lds32(w), lds32(w + r8_q), X, d);
-            const float a0 = s0[j >> 2][j & 3], a8 = s8[j >> 2][j & 3];
-            acc[0] = __fmaf_rn(a0, d[0], acc[0]); acc[1] = __fmaf_rn(a0, d[1], acc[1]);
-            acc[2] = __fmaf_rn(a8, d[2], acc[2]); acc[3] = __fmaf_rn(a8, d[3], acc[3]);
+        for (int j0 = 0; j0 < BPS; j0 += 4) {
+          if (j0 < nv) {
+            float s0[4], s8[4];
+            widen_scales(*reinterpret_cast<const uint2*>(st + soff + 2 * j0), s0);
+            widen_scales(*reinterpret_cast<const uint2*>(st + soff + r8_s + 2 * j0), s8);
+            uint4 X[4];
+            uint32_t wl[4], wh[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              X[jj] = *reinterpret_cast<const uint4*>(hb + (j0 + jj) * 64);
+              const uint8_t* w = st + woff(j0 + jj);
+              wl[jj] = lds32(w);
+              wh[jj] = lds32(w + r8_q);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              if (j0 + jj < nv) {
+                float d[4];
+                q4_block_mma(wl[jj], wh[jj], X[jj], d);
+                acc[0] = __fmaf_rn(s0[jj], d[0], acc[0]); acc[1] = __fmaf_rn(s0[jj], d[1], acc[1]);
+                acc[2] = __fmaf_rn(s8[jj], d[2], acc[2]); acc[3] = __fmaf_rn(s8[jj], d[3], acc[3]);
+              }
+            }
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
       if (c == dg.KC - 1) {
-        float* rb = red + (size_t)buf * kConsumerWarps * 16 * R;
+        // The WK slice warps of this row tile add their partials in slice order (a named
+        // barrier per row tile, so the tiles do not wait for one another); with one slice
+        // the warp writes its rows directly.
+        if (dg.WK == 1) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int col = 2 * q + (e & 1), row = g + ((e & 2) ? 8 : 0);
-          if (col < R) rb[(warp * 16 + row) * R + col] = acc[e];
-          acc[e] = 0.f;
-        }
-        consumer_sync();
-        for (int t = tid; t < dg.RS * R; t += kConsumers) {
-          const int rl = t / R, col = t - rl * R;
-          const int row = grp * dg.RS + rl;
-          if (row < H && ((rowmask >> col) & 1u)) {
-            const int tile = rl >> 4, rr = rl & 15;
-            float o = 0.f;
-            for (int s = 0; s < dg.WK; ++s)
-              o = __fadd_rn(o, rb[((tile * dg.WK + s) * 16 + rr) * R + col]);
-            const int slot_c = (u == 0) ? 0 : rt->slot[u - 1][col];
-            a.opart[((size_t)col * (1 + k) + slot_c) * H + row] = o;
+          for (int e = 0; e < 4; ++e) {
+            const int col = 2 * q + (e & 1), row = row_t + g + ((e & 2) ? 8 : 0);
+            if (col < R && row < H && ((rowmask >> col) & 1u)) {
+              const int slot_c = (u == 0) ? 0 : s_slot[u - 1][col];
+              a.opart[((size_t)col * (1 + k) + slot_c) * H + row] = __fadd_rn(0.f, acc[e]);
+            }
+            acc[e] = 0.f;
+          }
+        } else {
+          float* rb = red + (size_t)buf * kConsumerWarps * 16 * R;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int col = 2 * q + (e & 1), row = g + ((e & 2) ? 8 : 0);
+            if (col < R) rb[(warp * 16 + row) * R + col] = acc[e];
+            acc[e] = 0.f;
+          }
+          const int gthreads = dg.WK * 32, gt = tid - rtl * gthreads;
+          asm volatile("bar.sync %0, %1;" ::"r"(2 + rtl), "r"(gthreads) : "memory");
+          for (int t = gt; t < 16 * R; t += gthreads) {
+            const int rr = t / R, col = t - rr * R;
+            const int row = row_t + rr;
+            if (row < H && ((rowmask >> col) & 1u)) {
+              float o = 0.f;
+              for (int s = 0; s < dg.WK; ++s)
+                o = __fadd_rn(o, rb[((rtl * dg.WK + s) * 16 + rr) * R + col]);
+              const int slot_c = (u == 0) ? 0 : s_slot[u - 1][col];
+              a.opart[((size_t)col * (1 + k) + slot_c) * H + row] = o;
+            }
           }
         }
         buf ^= 1;
@@ -875,8 +912,8 @@ size_t gate_up_smem(const MoeDims& d, int ring) {
          (size_t)d.R * (2 * d.H + kXPad);
 }
 
-size_t down_smem(const MoeDims& d, int ring) {
-  const DownGeom g = down_geom(d.H, d.I);
+size_t down_smem(const MoeDims& d, int ring, int bps) {
+  const DownGeom g = down_geom(d.H, d.I, bps);
   return 1024 + (size_t)ring * g.stage_bytes + (size_t)8 * g.h_pitch + dn_red_bytes(d.R) + 64;
 }
 
@@ -956,16 +993,23 @@ cudaError_t launch_gate_up(const MoeDims& d, const uint16_t* x, Q4Ptr gate, Q4Pt
 
 cudaError_t launch_down(const MoeDims& d, Q4Ptr down, Q4Ptr sh_down, const float* topk_w,
                         uint16_t* y, const MoeWorkspace& ws, cudaStream_t s) {
-  const int ring = pick_ring([&](int r) { return down_smem(d, r); });
+  // 16 blocks per K slice where two stages fit (fewer stage overheads per byte), else 8
+  int bps = 16;
+  int ring = pick_ring([&](int r) { return down_smem(d, r, 16); });
+  if (ring == 0) {
+    bps = 8;
+    ring = pick_ring([&](int r) { return down_smem(d, r, 8); });
+  }
   if (ring == 0) return cudaErrorInvalidConfiguration;
-  const size_t smem = down_smem(d, ring);
-  cudaError_t err = set_smem(k4_down, smem);
+  const size_t smem = down_smem(d, ring, bps);
+  auto kern = bps == 16 ? k4_down<16> : k4_down<8>;
+  cudaError_t err = set_smem(kern, smem);
   if (err != cudaSuccess) return err;
   DownArgs a{};
   a.down = down; a.sh_down = sh_down; a.h = ws.h; a.route = ws.route; a.opart = ws.opart;
   a.status = ws.header;
   a.R = d.R; a.H = d.H; a.I = d.I; a.k = d.k; a.ring = ring;
-  const DownGeom g = down_geom(d.H, d.I);
+  const DownGeom g = down_geom(d.H, d.I, bps);
   a.boxed = g.boxed && (reinterpret_cast<uintptr_t>(down.sc) & 15u) == 0 &&
             (reinterpret_cast<uintptr_t>(sh_down.sc) & 15u) == 0;
   if (a.boxed) {
@@ -975,7 +1019,7 @@ cudaError_t launch_down(const MoeDims& d, Q4Ptr down, Q4Ptr sh_down, const float
             cudaSuccess)
       return err;
   }
-  err = launch_pdl(k4_down, device_sm_count(), kMmaThreads, smem, s, a);
+  err = launch_pdl(kern, device_sm_count(), kMmaThreads, smem, s, a);
   if (err != cudaSuccess) return err;
   const int n = d.R * d.H;
   return launch_pdl(k5_combine, (n + 255) / 256, 256, 0, s, ws.opart, topk_w, y, d.R, d.H, d.k);
