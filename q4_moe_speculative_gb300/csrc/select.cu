@@ -108,6 +108,19 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The fp32 score of an order-preserving key (inverse of score_key; -0 comes back as +0).
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+constexpr uint32_t kCertainKey = 0xFFFFFFFFu;   // above the key of every finite score
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
 // Canonical score of one block: q fp32 (shared) in the layout [i][kScoreMaxHeads] (value i
 // of head h at i * kScoreMaxHeads + h), key 128 bf16 (global), w [Hh].
 __device__ __forceinline__ float canonical_score(const float* q, const uint16_t* key,
@@ -1267,9 +1280,34 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
         int need;
         const uint32_t T = radix_threshold(total, K, [&](int j) { return col_lo[j]; }, hist,
                                            scratch, r_key, s_misc, a.status, &need);
+        // H = T + max over the candidates of (upper - lower), rounded upward, is at least
+        // the (K+1)-th largest upper bound of the row (the K+1 largest upper bounds each
+        // exceed their lower bound by at most that much, and at most K lower bounds reach
+        // past T). A candidate whose lower bound exceeds H is beaten by fewer than K others
+        // whatever the exact scores: it is selected without being re-scored, and takes the
+        // key kCertainKey so that the exact select below keeps it.
+        __shared__ unsigned s_dmax;
+        if (tid == 0) s_dmax = 0u;
+        __syncthreads();
+        {
+          float dm = 0.0f;
+          for (int j = tid; j < total; j += blockDim.x)
+            if (col_hi[j] >= T)
+              dm = fmaxf(dm, __fsub_ru(key_score(col_hi[j]), key_score(col_lo[j])));
+          dm = warp_max(dm);
+          if ((tid & 31) == 0) atomicMax(&s_dmax, __float_as_uint(dm));   // dm >= 0
+        }
+        __syncthreads();
+        const uint32_t Hk = score_key(__fadd_ru(key_score(T), __uint_as_float(s_dmax)));
         m = ordered_take(
             total, 0, [&](int j) { return col_hi[j] >= T ? 2 : 0; },
-            [&](int p, int j) { if (p < kCandCap) cand[p] = col_i[j]; }, s_eq, s_gt);
+            [&](int p, int j) {
+              if (p < kCandCap) {
+                cand[p] = col_i[j];
+                ckey[p] = col_lo[j] > Hk ? kCertainKey : 0u;
+              }
+            },
+            s_eq, s_gt);
       }
       __syncthreads();
     }
@@ -1280,19 +1318,39 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       // Ordered gather of the candidates (upper bound reaches T), bounded by kCandCap.
       m = ordered_take(
           n, 0, [&](int i) { return score_key(s1[i]) >= T ? 2 : 0; },
-          [&](int p, int i) { if (p < kCandCap) cand[p] = i; }, s_eq, s_gt);
+          [&](int p, int i) {
+            if (p < kCandCap) {
+              cand[p] = i;
+              ckey[p] = 0u;
+            }
+          },
+          s_eq, s_gt);
     }
     // This row's head weights (fp32).
     for (int i = tid; i < a.Hh; i += blockDim.x) wf[i] = a.hw[(size_t)lr * a.Hh + i];
     __syncthreads();
     if (m <= kCandCap) {
-      // Canonical scores of the candidates: their keys are staged in shared memory 64 at a
-      // time (double-buffered cp.async, rows padded to 272 bytes, in the space of the
+      // Canonical scores of the candidates that are not certain: their keys are staged in
+      // shared memory 64 at a time (double-buffered cp.async, rows padded to 272 bytes, in the space of the
       // finished collection); one lane per head runs that head's chain over i ascending,
       // then the candidate's first lane adds the heads in order.
       // candidate entries -> block ids, all in one round of loads
       for (int j = tid; j < m; j += blockDim.x) cand[j] = ui[cand[j]];
+      // the candidates to re-score (not certain), listed in r_key
+      __shared__ int s_mu;
+      if (tid == 0) s_mu = 0;
       __syncthreads();
+      for (int j0 = 0; j0 < m; j0 += blockDim.x) {
+        const int j = j0 + tid;
+        const bool u = j < m && ckey[j] != kCertainKey;
+        const unsigned bal = __ballot_sync(0xffffffffu, u);
+        int wbase = 0;
+        if ((tid & 31) == 0 && bal) wbase = atomicAdd(&s_mu, __popc(bal));
+        wbase = __shfl_sync(0xffffffffu, wbase, 0);
+        if (u) r_key[wbase + __popc(bal & ((1u << (tid & 31)) - 1u))] = (uint32_t)j;
+      }
+      __syncthreads();
+      const int mu = s_mu;
       {
         const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
         const int HP = a.Hh <= 8 ? 8 : 16, per_warp = 32 / HP;
@@ -1308,14 +1366,15 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
                 __ldg(reinterpret_cast<const uint4*>(qrow) + i);
         }
         const uint32_t kst_addr = static_cast<uint32_t>(__cvta_generic_to_shared(kst));
-        const int nchunk = (m + kStageCands - 1) / kStageCands;
+        const int nchunk = (mu + kStageCands - 1) / kStageCands;
         auto stage = [&](int ch) {
           const uint32_t dst = kst_addr + (uint32_t)((ch & 1) * kStageCands * kKeyPitch);
           const int base = ch * kStageCands;
           for (int p = tid; p < kStageCands * 16; p += blockDim.x) {
             const int cj = p >> 4, piece = p & 15;
-            const bool v = base + cj < m;
-            const uint16_t* src = v ? kbase + (size_t)cand[base + cj] * 128 + piece * 8 : kbase;
+            const bool v = base + cj < mu;
+            const uint16_t* src =
+                v ? kbase + (size_t)cand[r_key[base + cj]] * 128 + piece * 8 : kbase;
             cp_async16(dst + (uint32_t)(cj * kKeyPitch + piece * 16), src, v);
           }
           asm volatile("cp.async.commit_group;" ::: "memory");
@@ -1333,7 +1392,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
           for (int c0 = warp * per_warp; c0 < kStageCands; c0 += nwarps * per_warp) {
             const int cj = c0 + slot, j = ch * kStageCands + cj;
             float d = 0.0f;
-            if (j < m && h < a.Hh) {
+            if (j < mu && h < a.Hh) {
               const uint4* kr = reinterpret_cast<const uint4*>(buf + cj * kKeyPitch);
               const uint4* qr = reinterpret_cast<const uint4*>(qb + h * kKeyPitch);
 #pragma unroll
@@ -1350,7 +1409,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
               const float dh = __shfl_sync(0xffffffffu, d, slot * HP + hh);
               sc = __fmaf_rn(wf[hh], dh > 0.0f ? dh : 0.0f, sc);
             }
-            if (j < m && h == 0) ckey[j] = score_key(sc);
+            if (j < mu && h == 0) ckey[r_key[j]] = score_key(sc);
           }
           __syncthreads();   // this buffer may be refilled now
         }
