@@ -350,6 +350,8 @@ constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kChunkBlocks = 128;                       // Q4 blocks per row per stage (at most)
 constexpr int kMaxRing = 4;
 constexpr uint32_t kFullArrivals = 1 + 32;              // expect_tx + the producer's lanes
+constexpr int kReducerWarps = 3;                         // gate/up: 16 rows x R <= 96 outputs
+constexpr int kGuThreads = kMmaThreads + 32 * kReducerWarps;
 constexpr int kConsumerBarrier = 1;                     // named barrier id of the consumers
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -431,8 +433,11 @@ __host__ __device__ constexpr size_t gu_red_bytes(int R) {
 }
 
 template <int WB>
-__global__ void __launch_bounds__(kMmaThreads, 1) k3_gate_up(const __grid_constant__ GateUpArgs a) {
+__global__ void __launch_bounds__(kGuThreads, 1) k3_gate_up(const __grid_constant__ GateUpArgs a) {
   using Geo = GuGeom<WB>;
+  // partial-sum buffers: written by the 16 consumer warps (pfull), read by the reducer
+  // warps (pempty); two buffers, so consumers wait only when two units are unreduced
+  __shared__ __align__(8) uint64_t s_pfull[2], s_pempty[2];
   constexpr int kCB = Geo::kCB, kStage = Geo::kStage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -456,6 +461,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k3_gate_up(const __grid_consta
     for (int s = 0; s < ring; ++s) {
       mbar_init(&full[s], kFullArrivals);
       mbar_init(&empty[s], kConsumerWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_pfull[b], kConsumerWarps);
+      mbar_init(&s_pempty[b], kReducerWarps);
     }
     fence_mbar_init();
     if (boxed)
@@ -510,7 +519,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k3_gate_up(const __grid_consta
       cp_async_mbar_arrive(&full[slot]);
     }
     if (!routed) pdl_wait();
-  } else {
+  } else if (warp < kProducerWarp) {
     pdl_wait();      // the route produced by the router grid is visible from here on
     const RouteInfo* rt = a.route;
     const int n_units = (1 + rt->n_union) * RT;
@@ -589,8 +598,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k3_gate_up(const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the slot
       if (c == KC - 1) {
+        // partials [warp][gate/up][row][col] (cols < R only) into buffer unit & 1, once
+        // the reducers are done with the unit that used it before
+        const int unit = f / KC;
+        if (unit >= 2 && !mbar_wait(&s_pempty[buf], ((unit >> 1) - 1) & 1, kWaitPolls))
+          timed_out = true;
         float* rb = red + (size_t)buf * kConsumerWarps * 2 * 16 * R;
-        // partials [warp][gate/up][row][col], cols < R only
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int col = 2 * q + (e & 1), row = g + ((e & 2) ? 8 : 0);
@@ -601,26 +614,44 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k3_gate_up(const __grid_consta
           ag[e] = 0.f;
           au[e] = 0.f;
         }
-        consumer_sync();
-        const int n = (int)blockIdx.x + (f / KC) * G;
-        const int u = n / RT, rti = n - u * RT;
-        if (tid < 16 * R) {
-          const int row = tid / R, col = tid - row * R;
-          const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : rt->rowmask[u - 1];
-          if ((rowmask >> col) & 1u) {
-            float gs = 0.f, us = 0.f;
-            for (int w = 0; w < kConsumerWarps; ++w) {
-              gs = __fadd_rn(gs, rb[((w * 2 + 0) * 16 + row) * R + col]);
-              us = __fadd_rn(us, rb[((w * 2 + 1) * 16 + row) * R + col]);
-            }
-            const int slot_c = (u == 0) ? 0 : rt->slot[u - 1][col];
-            const float silu = __fdiv_rn(gs, __fadd_rn(1.0f, expf(-gs)));
-            a.h[((size_t)col * (1 + k) + slot_c) * I + rti * 16 + row] =
-                f32_to_bf16_rne(__fmul_rn(silu, us));
-          }
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_pfull[buf]);
         buf ^= 1;
       }
+    }
+  } else {
+    // Reducers: for each unit of this CTA, in order, the 16 warps' partials are added in
+    // warp order and h = bf16_rne(silu(g) * u) is written for the expert's rows.
+    pdl_wait();
+    const RouteInfo* rt = a.route;
+    const int n_units = (1 + rt->n_union) * RT;
+    const int rtid = tid - (kProducerWarp + 1) * 32;
+    int unit = 0;
+    for (int n = (int)blockIdx.x; n < n_units; n += G, ++unit) {
+      const int b = unit & 1;
+      if (!mbar_wait(&s_pfull[b], (unit >> 1) & 1, kWaitPolls)) {
+        timed_out = true;
+        break;
+      }
+      const float* rb = red + (size_t)b * kConsumerWarps * 2 * 16 * R;
+      const int u = n / RT, rti = n - u * RT;
+      if (rtid < 16 * R) {
+        const int row = rtid / R, col = rtid - row * R;
+        const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : rt->rowmask[u - 1];
+        if ((rowmask >> col) & 1u) {
+          float gs = 0.f, us = 0.f;
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            gs = __fadd_rn(gs, rb[((w * 2 + 0) * 16 + row) * R + col]);
+            us = __fadd_rn(us, rb[((w * 2 + 1) * 16 + row) * R + col]);
+          }
+          const int slot_c = (u == 0) ? 0 : rt->slot[u - 1][col];
+          const float silu = __fdiv_rn(gs, __fadd_rn(1.0f, expf(-gs)));
+          a.h[((size_t)col * (1 + k) + slot_c) * I + rti * 16 + row] =
+              f32_to_bf16_rne(__fmul_rn(silu, us));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_pempty[b]);
     }
   }
   pdl_trigger();   // the down projection may be scheduled as CTAs of this grid retire
@@ -939,7 +970,7 @@ cudaError_t launch_gate_up_wb(const MoeDims& d, GateUpArgs& a, int ring, cudaStr
         return err;
     }
   }
-  return launch_pdl(k3_gate_up<WB>, device_sm_count(), kMmaThreads, smem, s, a);
+  return launch_pdl(k3_gate_up<WB>, device_sm_count(), kGuThreads, smem, s, a);
 }
 
 }  // namespace
