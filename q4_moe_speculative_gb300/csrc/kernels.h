@@ -78,8 +78,8 @@ struct SelWorkspace {
                       // order: entry, lower bound key, upper bound key
 };
 
-constexpr int kTopkChunks = 8;        // collect CTAs per row
-constexpr int kTopkChunkCap = 512;    // collected entries kept per row chunk
+constexpr int kTopkChunks = 4;        // collect CTAs per row
+constexpr int kTopkChunkCap = 1024;   // collected entries kept per row chunk
 
 struct SelLayout {
   size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, chi, tau, ccnt, clo, creg,

@@ -1134,7 +1134,7 @@ __global__ void __launch_bounds__(kTopkThreads) k7a_tau(TopkArgs a) {
 // ---------------------------------------------------------------------------------
 constexpr int kCollectThreads = 256;
 constexpr int kCollectWarps = kCollectThreads / 32;
-constexpr int kWarpBuf = 128;
+constexpr int kWarpBuf = 256;
 
 __global__ void __launch_bounds__(kCollectThreads) k7b_collect(TopkArgs a) {
   __shared__ int s_cnt[kCollectWarps], s_lo[kCollectWarps];
@@ -1152,7 +1152,7 @@ __global__ void __launch_bounds__(kCollectThreads) k7b_collect(TopkArgs a) {
   // contiguous warp segments of the chunk, in multiples of 32
   const int seg = ((c1 - c0 + kCollectWarps - 1) / kCollectWarps + 31) & ~31;
   const int beg = min(c1, c0 + warp * seg), end = min(c1, beg + seg);
-  constexpr int U = 8;
+  constexpr int U = 16;   // 32 loads in flight per lane
   int cnt = 0, nlo = 0;
   for (int i0 = beg; i0 < end; i0 += 32 * U) {
     uint32_t hk[U], lk[U];
