@@ -1330,10 +1330,12 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
     for (int i = tid; i < a.Hh; i += blockDim.x) wf[i] = a.hw[(size_t)lr * a.Hh + i];
     __syncthreads();
     if (m <= kCandCap) {
-      // Canonical scores of the candidates that are not certain: their keys are staged in
-      // shared memory 64 at a time (double-buffered cp.async, rows padded to 272 bytes, in the space of the
-      // finished collection); one lane per head runs that head's chain over i ascending,
-      // then the candidate's first lane adds the heads in order.
+      // Canonical scores of the candidates that are not certain. Each warp takes groups of
+      // per_warp candidates (group g of warp w is pass g's slot w) and stages their keys
+      // itself, three groups deep (cp.async into the warp's own buffers in the space of the
+      // finished collection, 16-byte chunks XOR-swizzled by the row), so the warps overlap
+      // their loads with no block-wide barrier. One lane per head runs that head's chain over
+      // i ascending, then the candidate's first lane adds the heads in order.
       // candidate entries -> block ids, all in one round of loads
       for (int j = tid; j < m; j += blockDim.x) cand[j] = ui[cand[j]];
       // the candidates to re-score (not certain), listed in r_key
@@ -1355,64 +1357,68 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
         const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
         const int HP = a.Hh <= 8 ? 8 : 16, per_warp = 32 / HP;
         const int slot = lane / HP, h = lane - slot * HP;
-        constexpr int kStageCands = 64, kKeyPitch = 272;
-        uint8_t* kst = reinterpret_cast<uint8_t*>(col_i);
-        // this row's queries as bf16, head h at qb + 272 h (rows 4 banks apart)
-        uint8_t* qb = kst + 2 * kStageCands * kKeyPitch;
+        constexpr int kDepth = 3, kQPitch = 272;
+        static_assert(kTopkWarps * kDepth * 4 * 256 <= 3 * kCollectCap * (int)sizeof(int32_t),
+                      "key staging exceeds the collection space");
+        // this warp's kDepth buffers of up to 4 keys (256 bytes each)
+        uint8_t* wst = reinterpret_cast<uint8_t*>(col_i) + (size_t)warp * kDepth * 4 * 256;
+        const uint32_t wst_addr = static_cast<uint32_t>(__cvta_generic_to_shared(wst));
+        // this row's queries as bf16, head h at qb + 272 h (rows 4 banks apart), in the
+        // space of the fp32 queries (used only by the whole-row fallback)
+        uint8_t* qb = reinterpret_cast<uint8_t*>(qf);
         {
           const uint16_t* qrow = a.q + (size_t)lr * a.Hh * 128;
           for (int i = tid; i < a.Hh * 16; i += blockDim.x)
-            *reinterpret_cast<uint4*>(qb + (i >> 4) * kKeyPitch + (i & 15) * 16) =
+            *reinterpret_cast<uint4*>(qb + (i >> 4) * kQPitch + (i & 15) * 16) =
                 __ldg(reinterpret_cast<const uint4*>(qrow) + i);
         }
-        const uint32_t kst_addr = static_cast<uint32_t>(__cvta_generic_to_shared(kst));
-        const int nchunk = (mu + kStageCands - 1) / kStageCands;
-        auto stage = [&](int ch) {
-          const uint32_t dst = kst_addr + (uint32_t)((ch & 1) * kStageCands * kKeyPitch);
-          const int base = ch * kStageCands;
-          for (int p = tid; p < kStageCands * 16; p += blockDim.x) {
-            const int cj = p >> 4, piece = p & 15;
-            const bool v = base + cj < mu;
-            const uint16_t* src =
-                v ? kbase + (size_t)cand[r_key[base + cj]] * 128 + piece * 8 : kbase;
-            cp_async16(dst + (uint32_t)(cj * kKeyPitch + piece * 16), src, v);
+        __syncthreads();
+        const int per_pass = nwarps * per_warp;
+        const int npass = (mu + per_pass - 1) / per_pass;
+        auto stage = [&](int ps) {   // one commit group per pass (empty past the end)
+          if (ps < npass) {
+            const uint32_t dst = wst_addr + (uint32_t)((ps % kDepth) * 4 * 256);
+            const int base = ps * per_pass + warp * per_warp;
+            for (int p = lane; p < per_warp * 16; p += 32) {
+              const int cj = p >> 4, piece = p & 15;
+              const bool v = base + cj < mu;
+              const uint16_t* src =
+                  v ? kbase + (size_t)cand[r_key[base + cj]] * 128 + piece * 8 : kbase;
+              cp_async16(dst + (uint32_t)(cj * 256 + ((piece ^ cj) & 15) * 16), src, v);
+            }
           }
           asm volatile("cp.async.commit_group;" ::: "memory");
         };
-        if (nchunk > 0) stage(0);
-        for (int ch = 0; ch < nchunk; ++ch) {
-          if (ch + 1 < nchunk) {
-            stage(ch + 1);
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-          } else {
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
-          }
-          __syncthreads();
-          const uint8_t* buf = kst + (ch & 1) * kStageCands * kKeyPitch;
-          for (int c0 = warp * per_warp; c0 < kStageCands; c0 += nwarps * per_warp) {
-            const int cj = c0 + slot, j = ch * kStageCands + cj;
-            float d = 0.0f;
-            if (j < mu && h < a.Hh) {
-              const uint4* kr = reinterpret_cast<const uint4*>(buf + cj * kKeyPitch);
-              const uint4* qr = reinterpret_cast<const uint4*>(qb + h * kKeyPitch);
+        for (int ps = 0; ps < kDepth - 1; ++ps) stage(ps);
+        for (int ps = 0; ps < npass; ++ps) {
+          stage(ps + kDepth - 1);   // into the buffer the previous pass used
+          asm volatile("cp.async.wait_group %0;" ::"n"(kDepth - 1) : "memory");
+          __syncwarp();
+          const uint8_t* buf = wst + (ps % kDepth) * 4 * 256;
+          const int j = ps * per_pass + warp * per_warp + slot;
+          float d = 0.0f;
+          if (j < mu && h < a.Hh) {
+            const uint8_t* kr = buf + slot * 256;
+            const uint4* qr = reinterpret_cast<const uint4*>(qb + h * kQPitch);
 #pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const uint4 kv = kr[c], qv = qr[c];
-                d = fma2_bf16(qv.x, kv.x, d);
-                d = fma2_bf16(qv.y, kv.y, d);
-                d = fma2_bf16(qv.z, kv.z, d);
-                d = fma2_bf16(qv.w, kv.w, d);
-              }
+            for (int c = 0; c < 16; ++c) {
+              const uint4 kv = *reinterpret_cast<const uint4*>(kr + ((c ^ slot) & 15) * 16);
+              const uint4 qv = qr[c];
+              d = fma2_bf16(qv.x, kv.x, d);
+              d = fma2_bf16(qv.y, kv.y, d);
+              d = fma2_bf16(qv.z, kv.z, d);
+              d = fma2_bf16(qv.w, kv.w, d);
             }
-            float sc = 0.0f;
-            for (int hh = 0; hh < a.Hh; ++hh) {
-              const float dh = __shfl_sync(0xffffffffu, d, slot * HP + hh);
-              sc = __fmaf_rn(wf[hh], dh > 0.0f ? dh : 0.0f, sc);
-            }
-            if (j < mu && h == 0) ckey[r_key[j]] = score_key(sc);
           }
-          __syncthreads();   // this buffer may be refilled now
+          float sc = 0.0f;
+          for (int hh = 0; hh < a.Hh; ++hh) {
+            const float dh = __shfl_sync(0xffffffffu, d, slot * HP + hh);
+            sc = __fmaf_rn(wf[hh], dh > 0.0f ? dh : 0.0f, sc);
+          }
+          if (j < mu && h == 0) ckey[r_key[j]] = score_key(sc);
+          __syncwarp();   // the warp is done with this buffer
         }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
       }
       __syncthreads();
       int need2;
