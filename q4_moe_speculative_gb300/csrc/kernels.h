@@ -75,11 +75,11 @@ struct SelWorkspace {
   int32_t* ccnt;      // [L][R][kTopkChunks] entries collected per row chunk
   int32_t* clo;       // [L][R][kTopkChunks] entries with a lower bound >= tau per chunk
   int32_t* creg;      // [3][L][R][kTopkChunks][kTopkChunkCap] collected entries in index
-                      // order: entry, lower bound key, upper bound key
+                      // order: block id, lower bound key, upper bound key
 };
 
-constexpr int kTopkChunks = 4;        // collect CTAs per row
-constexpr int kTopkChunkCap = 1024;   // collected entries kept per row chunk
+constexpr int kTopkChunks = 3;        // collect CTAs per row
+constexpr int kTopkChunkCap = 1408;   // collected entries kept per row chunk (x3 >= 4096)
 
 struct SelLayout {
   size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, chi, tau, ccnt, clo, creg,

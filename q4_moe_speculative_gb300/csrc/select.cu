@@ -1127,7 +1127,8 @@ __global__ void __launch_bounds__(kTopkThreads) k7a_tau(TopkArgs a) {
 
 // ---------------------------------------------------------------------------------
 // K7b: per (layer, row, chunk of the row's union entries): the entries whose upper bound
-// reaches tau, with their lower and upper bound keys, in index order in the chunk's region
+// reaches tau, as block ids with their lower and upper bound keys, in index order in the
+// chunk's region
 // (each warp keeps its matches in shared memory, then the warps' lists are concatenated),
 // and how many entries have a lower bound >= tau. A chunk with more matches than its
 // region (or a warp with more than its buffer) reports a count above the capacity.
@@ -1196,8 +1197,9 @@ __global__ void __launch_bounds__(kCollectThreads) k7b_collect(TopkArgs a) {
   pdl_trigger();
   const size_t plane = (size_t)gridDim.x * kTopkChunkCap;   // (L R chunks) x capacity
   int32_t* reg = a.creg + rc * kTopkChunkCap;
+  const int32_t* ui = a.uidx + (size_t)l * a.N;
   for (int p = lane; p < cnt; p += 32) {
-    reg[off + p] = (int32_t)s_buf[warp][0][p];
+    reg[off + p] = ui[s_buf[warp][0][p]];   // the entry's block id
     reg[plane + off + p] = (int32_t)s_buf[warp][1][p];
     reg[2 * plane + off + p] = (int32_t)s_buf[warp][2][p];
   }
@@ -1214,7 +1216,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   uint32_t* ckey = reinterpret_cast<uint32_t*>(cand + kCandCap);  // [kCandCap] keys
   float* qf = reinterpret_cast<float*>(ckey + kCandCap);          // [Hh][128]
   float* wf = qf + kScoreMaxHeads * 128;                          // [Hh]
-  // the collected entries in index order, with their lower and upper bound keys
+  // the collected entries in index order (block ids), with their lower and upper bound keys
   int32_t* col_i = reinterpret_cast<int32_t*>(wf + kScoreMaxHeads);
   uint32_t* col_lo = reinterpret_cast<uint32_t*>(col_i + kCollectCap);
   uint32_t* col_hi = col_lo + kCollectCap;
@@ -1311,7 +1313,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       }
       __syncthreads();
     }
+    bool cand_entries = false;   // cand holds union entries (else block ids)
     if (m < 0) {
+      cand_entries = true;
       int need;
       const uint32_t T = radix_threshold(
           n, K, [&](int i) { return s0[i]; }, hist, scratch, r_key, s_misc, a.status, &need);
@@ -1336,8 +1340,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       // finished collection, 16-byte chunks XOR-swizzled by the row), so the warps overlap
       // their loads with no block-wide barrier. One lane per head runs that head's chain over
       // i ascending, then the candidate's first lane adds the heads in order.
-      // candidate entries -> block ids, all in one round of loads
-      for (int j = tid; j < m; j += blockDim.x) cand[j] = ui[cand[j]];
+      // candidates taken from the whole row are union entries: -> block ids, one round of loads
+      if (cand_entries)
+        for (int j = tid; j < m; j += blockDim.x) cand[j] = ui[cand[j]];
       // the candidates to re-score (not certain), listed in r_key
       __shared__ int s_mu;
       if (tid == 0) s_mu = 0;
