@@ -166,32 +166,44 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
       for (int r = 0; r < kMaxRows; ++r) acc[e][r] = 0.0f;
     const int slice = H / kRouterWarps;          // a multiple of 8
     const int nch = slice / 8;
-#pragma unroll 2
-    for (int c = lane; c < nch; c += 32) {
-      const int col = warp * slice + c * 8;
-      uint4 wv[kRouterExperts], xv[kMaxRows];
+    // the weights of two chunks per lane are requested before either is used
+    for (int c0 = lane; c0 < nch; c0 += 64) {
+      uint4 wv2[2][kRouterExperts];
 #pragma unroll
-      for (int e = 0; e < kRouterExperts; ++e)
-        wv[e] = e < ne ? __ldcs(reinterpret_cast<const uint4*>(wr + (size_t)(e0 + e) * H + col))
-                       : make_uint4(0, 0, 0, 0);
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = c0 + 32 * cc, col = warp * slice + c * 8;
 #pragma unroll
-      for (int r = 0; r < kMaxRows; ++r)
-        xv[r] = r < R ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)r * H + col))
-                      : make_uint4(0, 0, 0, 0);
+        for (int e = 0; e < kRouterExperts; ++e)
+          wv2[cc][e] = (c < nch && e < ne)
+                           ? __ldcs(reinterpret_cast<const uint4*>(wr + (size_t)(e0 + e) * H + col))
+                           : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
-        if (r < R) {
-          const float xf[8] = {bf16_lo(xv[r].x), bf16_hi(xv[r].x), bf16_lo(xv[r].y),
-                               bf16_hi(xv[r].y), bf16_lo(xv[r].z), bf16_hi(xv[r].z),
-                               bf16_lo(xv[r].w), bf16_hi(xv[r].w)};
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = c0 + 32 * cc;
+        if (c >= nch) break;
+        const int col = warp * slice + c * 8;
+        const uint4* wv = wv2[cc];
+        uint4 xv[kMaxRows];
 #pragma unroll
-          for (int e = 0; e < kRouterExperts; ++e) {
-            float t = acc[e][r];
-            t = __fmaf_rn(bf16_lo(wv[e].x), xf[0], t); t = __fmaf_rn(bf16_hi(wv[e].x), xf[1], t);
-            t = __fmaf_rn(bf16_lo(wv[e].y), xf[2], t); t = __fmaf_rn(bf16_hi(wv[e].y), xf[3], t);
-            t = __fmaf_rn(bf16_lo(wv[e].z), xf[4], t); t = __fmaf_rn(bf16_hi(wv[e].z), xf[5], t);
-            t = __fmaf_rn(bf16_lo(wv[e].w), xf[6], t); t = __fmaf_rn(bf16_hi(wv[e].w), xf[7], t);
-            acc[e][r] = t;
+        for (int r = 0; r < kMaxRows; ++r)
+          xv[r] = r < R ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)r * H + col))
+                        : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) {
+          if (r < R) {
+            const float xf[8] = {bf16_lo(xv[r].x), bf16_hi(xv[r].x), bf16_lo(xv[r].y),
+                                 bf16_hi(xv[r].y), bf16_lo(xv[r].z), bf16_hi(xv[r].z),
+                                 bf16_lo(xv[r].w), bf16_hi(xv[r].w)};
+#pragma unroll
+            for (int e = 0; e < kRouterExperts; ++e) {
+              float t = acc[e][r];
+              t = __fmaf_rn(bf16_lo(wv[e].x), xf[0], t); t = __fmaf_rn(bf16_hi(wv[e].x), xf[1], t);
+              t = __fmaf_rn(bf16_lo(wv[e].y), xf[2], t); t = __fmaf_rn(bf16_hi(wv[e].y), xf[3], t);
+              t = __fmaf_rn(bf16_lo(wv[e].z), xf[4], t); t = __fmaf_rn(bf16_hi(wv[e].z), xf[5], t);
+              t = __fmaf_rn(bf16_lo(wv[e].w), xf[6], t); t = __fmaf_rn(bf16_hi(wv[e].w), xf[7], t);
+              acc[e][r] = t;
+            }
           }
         }
       }
@@ -215,10 +227,12 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     scores[r * E + e0 + e] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
   }
 
-  // Arrival count: the last CTA continues, the others are done. Nobody waits.
-  __threadfence();
+  // Arrival count: the last CTA continues, the others are done. Nobody waits. (The CTA
+  // barrier orders the scores before thread 0's fence, which makes them visible device-wide
+  // before the count.)
   __syncthreads();
   if (tid == 0) {
+    __threadfence();
     const unsigned prev = atomicAdd(&hdr->router_arrivals, 1u);
     s_is_last = (prev == gridDim.x - 1);
   }
