@@ -78,8 +78,8 @@ struct SelWorkspace {
                       // order: block id, lower bound key, upper bound key
 };
 
-constexpr int kTopkChunks = 3;        // collect CTAs per row
-constexpr int kTopkChunkCap = 1408;   // collected entries kept per row chunk (x3 >= 4096)
+constexpr int kTopkChunks = 2;        // collect CTAs per row (516 at 43 x 6 rows: one wave)
+constexpr int kTopkChunkCap = 2048;   // collected entries kept per row chunk (x2 = 4096)
 
 struct SelLayout {
   size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, chi, tau, ccnt, clo, creg,
