@@ -76,14 +76,20 @@ struct SelWorkspace {
   int32_t* clo;       // [L][R][kTopkChunks] entries with a lower bound >= tau per chunk
   int32_t* creg;      // [3][L][R][kTopkChunks][kTopkChunkCap] collected entries in index
                       // order: block id, lower bound key, upper bound key
+  int32_t* rcand;     // [L][R][kTopkCandCap] re-score candidates in index order (block ids)
+  uint32_t* rkey;     // [L][R][kTopkCandCap] their keys (certain, or the canonical score's)
+  int32_t* rlist;     // [L][R][kTopkCandCap][2] uncertain candidates: position, block id
+  int32_t* rcount;    // [L][R][2] candidates (-1: the row is complete), uncertain ones
+  int32_t* rtask;     // [L][R * kTopkCandCap / 32][2] re-score tasks: row * 128 + part, count
 };
 
 constexpr int kTopkChunks = 2;        // collect CTAs per row (516 at 43 x 6 rows: one wave)
 constexpr int kTopkChunkCap = 2048;   // collected entries kept per row chunk (x2 = 4096)
+constexpr int kTopkCandCap = 4096;    // re-score candidates per row
 
 struct SelLayout {
   size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, chi, tau, ccnt, clo, creg,
-      total;
+      rcand, rkey, rlist, rcount, rtask, total;
 };
 SelLayout sel_layout(const SelDims& d, bool caller_cidx);
 bool tc_scoring_supported(const SelDims& d, const uint16_t* keys, const uint16_t* q);

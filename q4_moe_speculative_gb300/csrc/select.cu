@@ -41,7 +41,7 @@ constexpr int kScoreMaxHeads = 16;
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kResidCap = 4096;      // residual radix bucket kept in shared memory
-constexpr int kCandCap = 4096;       // re-score candidates kept in shared memory
+constexpr int kCandCap = kTopkCandCap;   // re-score candidates kept in shared memory
 constexpr int kCollectCap = 4096;    // entries collected by the sampled-threshold pass
 constexpr uint32_t kWaitPolls = 1u << 17;   // bounded mbarrier polling (<= ~0.13 s)
 constexpr float kEpsRel = 0.0009765625f;    // 2^-10
@@ -1056,13 +1056,14 @@ __device__ int ordered_take(int n, int need, Cls cls, Emit emit, int* s_eq, int*
 }
 
 // ---------------------------------------------------------------------------------
-// K7: bounded radix top-k per (layer, row), one CTA of 1024 threads, over the layer's
+// K7: bounded radix top-k per (layer, row), one CTA of 512 threads, over the layer's
 // union entries (entries the row does not admit carry the sentinel and never qualify).
 // Canonical mode: threshold and ordered take over the canonical scores.
 // Tensor-core mode: threshold T over the lower bounds; ordered gather of the candidates
-// with upper bound >= T (bounded by kCandCap); canonical re-score of the candidates;
-// threshold and ordered take among them. Above the bound: canonical re-score of every
-// admitted entry of the row, then the canonical-mode path.
+// with upper bound >= T (bounded by kCandCap), the certain ones marked; the canonical
+// re-score of the others (K7r, over the whole GPU) and the threshold and ordered take
+// among the candidates (K7c) follow. Above the bound: canonical re-score of every
+// admitted entry of the row, then the canonical-mode path, here.
 // ---------------------------------------------------------------------------------
 struct TopkArgs {
   int R, Hh, N, K;
@@ -1084,9 +1085,18 @@ struct TopkArgs {
   int32_t* ccnt;
   int32_t* clo;
   int32_t* creg;
+  int32_t* rcand;
+  uint32_t* rkey;
+  int32_t* rlist;
+  int32_t* rcount;
+  int32_t* rtask;
 };
 
 constexpr uint32_t kTauDirect = 0xFFFFFFFFu;   // row with at most K admitted: no collection
+// Words of the workspace header (word 0 is the status word; the header is zeroed per call):
+// the number of re-score tasks listed by K7 and the next task K7r hands out.
+constexpr int kRescoreTasks = 1;
+constexpr int kRescoreNext = 2;
 
 // ---------------------------------------------------------------------------------
 // K7a: per (layer, row), a collection threshold tau at or below the K-th largest lower
@@ -1222,6 +1232,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   uint32_t* col_hi = col_lo + kCollectCap;
 
   pdl_wait();   // the collection (or, in canonical mode, the scores) is complete
+  pdl_trigger();
   const int lr = blockIdx.x;
   const int l = lr / a.R;
   const int tid = threadIdx.x;
@@ -1229,6 +1240,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   const int K = a.K;
   int32_t* out = a.sel + (size_t)lr * K;
 
+  if (a.tc_mode && tid == 0) a.rcount[2 * lr] = -1;   // complete here unless deferred below
   if (count <= K) {
     const int32_t* ci = a.cidx + (size_t)lr * a.N;
     for (int i = tid; i < K; i += blockDim.x) out[i] = i < count ? ci[i] : -1;
@@ -1334,109 +1346,45 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
     for (int i = tid; i < a.Hh; i += blockDim.x) wf[i] = a.hw[(size_t)lr * a.Hh + i];
     __syncthreads();
     if (m <= kCandCap) {
-      // Canonical scores of the candidates that are not certain. Each warp takes groups of
-      // per_warp candidates (group g of warp w is pass g's slot w) and stages their keys
-      // itself, three groups deep (cp.async into the warp's own buffers in the space of the
-      // finished collection, 16-byte chunks XOR-swizzled by the row), so the warps overlap
-      // their loads with no block-wide barrier. One lane per head runs that head's chain over
-      // i ascending, then the candidate's first lane adds the heads in order.
-      // candidates taken from the whole row are union entries: -> block ids, one round of loads
+      // Deferred to K7r / K7c: the candidates (block ids, in index order) with their keys
+      // (kCertainKey, or 0 until K7r writes the canonical score's key) and the positions of
+      // the uncertain ones, compacted by warp ballot.
       if (cand_entries)
         for (int j = tid; j < m; j += blockDim.x) cand[j] = ui[cand[j]];
-      // the candidates to re-score (not certain), listed in r_key
       __shared__ int s_mu;
       if (tid == 0) s_mu = 0;
       __syncthreads();
+      int32_t* rcand = a.rcand + (size_t)lr * kCandCap;
+      uint32_t* rkey = a.rkey + (size_t)lr * kCandCap;
+      int32_t* rlist = a.rlist + (size_t)lr * kCandCap * 2;
       for (int j0 = 0; j0 < m; j0 += blockDim.x) {
         const int j = j0 + tid;
-        const bool u = j < m && ckey[j] != kCertainKey;
+        const uint32_t k = j < m ? ckey[j] : kCertainKey;
+        if (j < m) {
+          rcand[j] = cand[j];
+          rkey[j] = k;
+        }
+        const bool u = k != kCertainKey;
         const unsigned bal = __ballot_sync(0xffffffffu, u);
         int wbase = 0;
         if ((tid & 31) == 0 && bal) wbase = atomicAdd(&s_mu, __popc(bal));
         wbase = __shfl_sync(0xffffffffu, wbase, 0);
-        if (u) r_key[wbase + __popc(bal & ((1u << (tid & 31)) - 1u))] = (uint32_t)j;
+        if (u) {
+          const int p = wbase + __popc(bal & ((1u << (tid & 31)) - 1u));
+          reinterpret_cast<int2*>(rlist)[p] = make_int2(j, cand[j]);
+        }
       }
       __syncthreads();
-      const int mu = s_mu;
-      {
-        const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-        const int HP = a.Hh <= 8 ? 8 : 16, per_warp = 32 / HP;
-        const int slot = lane / HP, h = lane - slot * HP;
-        constexpr int kDepth = 3, kQPitch = 272;
-        static_assert(kTopkWarps * kDepth * 4 * 256 <= 3 * kCollectCap * (int)sizeof(int32_t),
-                      "key staging exceeds the collection space");
-        // this warp's kDepth buffers of up to 4 keys (256 bytes each)
-        uint8_t* wst = reinterpret_cast<uint8_t*>(col_i) + (size_t)warp * kDepth * 4 * 256;
-        const uint32_t wst_addr = static_cast<uint32_t>(__cvta_generic_to_shared(wst));
-        // this row's queries as bf16, head h at qb + 272 h (rows 4 banks apart), in the
-        // space of the fp32 queries (used only by the whole-row fallback)
-        uint8_t* qb = reinterpret_cast<uint8_t*>(qf);
-        {
-          const uint16_t* qrow = a.q + (size_t)lr * a.Hh * 128;
-          for (int i = tid; i < a.Hh * 16; i += blockDim.x)
-            *reinterpret_cast<uint4*>(qb + (i >> 4) * kQPitch + (i & 15) * 16) =
-                __ldg(reinterpret_cast<const uint4*>(qrow) + i);
-        }
-        __syncthreads();
-        const int per_pass = nwarps * per_warp;
-        const int npass = (mu + per_pass - 1) / per_pass;
-        auto stage = [&](int ps) {   // one commit group per pass (empty past the end)
-          if (ps < npass) {
-            const uint32_t dst = wst_addr + (uint32_t)((ps % kDepth) * 4 * 256);
-            const int base = ps * per_pass + warp * per_warp;
-            for (int p = lane; p < per_warp * 16; p += 32) {
-              const int cj = p >> 4, piece = p & 15;
-              const bool v = base + cj < mu;
-              const uint16_t* src =
-                  v ? kbase + (size_t)cand[r_key[base + cj]] * 128 + piece * 8 : kbase;
-              cp_async16(dst + (uint32_t)(cj * 256 + ((piece ^ cj) & 15) * 16), src, v);
-            }
-          }
-          asm volatile("cp.async.commit_group;" ::: "memory");
-        };
-        for (int ps = 0; ps < kDepth - 1; ++ps) stage(ps);
-        for (int ps = 0; ps < npass; ++ps) {
-          stage(ps + kDepth - 1);   // into the buffer the previous pass used
-          asm volatile("cp.async.wait_group %0;" ::"n"(kDepth - 1) : "memory");
-          __syncwarp();
-          const uint8_t* buf = wst + (ps % kDepth) * 4 * 256;
-          const int j = ps * per_pass + warp * per_warp + slot;
-          float d = 0.0f;
-          if (j < mu && h < a.Hh) {
-            const uint8_t* kr = buf + slot * 256;
-            const uint4* qr = reinterpret_cast<const uint4*>(qb + h * kQPitch);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const uint4 kv = *reinterpret_cast<const uint4*>(kr + ((c ^ slot) & 15) * 16);
-              const uint4 qv = qr[c];
-              d = fma2_bf16(qv.x, kv.x, d);
-              d = fma2_bf16(qv.y, kv.y, d);
-              d = fma2_bf16(qv.z, kv.z, d);
-              d = fma2_bf16(qv.w, kv.w, d);
-            }
-          }
-          float sc = 0.0f;
-          for (int hh = 0; hh < a.Hh; ++hh) {
-            const float dh = __shfl_sync(0xffffffffu, d, slot * HP + hh);
-            sc = __fmaf_rn(wf[hh], dh > 0.0f ? dh : 0.0f, sc);
-          }
-          if (j < mu && h == 0) ckey[r_key[j]] = score_key(sc);
-          __syncwarp();   // the warp is done with this buffer
-        }
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-      }
-      __syncthreads();
-      int need2;
-      const uint32_t T2 = radix_threshold(
-          m, K, [&](int j) { return ckey[j]; }, hist, scratch, r_key, s_misc, a.status, &need2);
-      const int taken = ordered_take(
-          m, need2,
-          [&](int j) { const uint32_t k = ckey[j]; return k > T2 ? 2 : (k == T2 ? 1 : 0); },
-          [&](int p, int j) { if (p < K) out[p] = cand[j]; }, s_eq, s_gt);
+      // this row's re-score tasks (32 uncertain candidates each), appended to the task list
+      const int mu = s_mu, nt = (mu + 31) / 32;
       if (tid == 0) {
-        a.nsel[lr] = K;
-        if (taken != K) flag_status(a.status, kStatusCheck);
+        a.rcount[2 * lr] = m;
+        a.rcount[2 * lr + 1] = mu;
+        s_misc[0] = nt > 0 ? (int)atomicAdd(&a.status[kRescoreTasks], (uint32_t)nt) : 0;
       }
+      __syncthreads();
+      for (int i = tid; i < nt; i += blockDim.x)
+        reinterpret_cast<int2*>(a.rtask)[s_misc[0] + i] = make_int2(lr * (kCandCap / 32) + i, mu);
       return;
     }
     // Too many candidates (e.g. heavy ties): canonical scores for the whole row, with the
@@ -1470,6 +1418,161 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       a.nsel[lr] = K;
       if (taken != K) flag_status(a.status, kStatusCheck);
     }
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// K7r (tensor-core scoring): canonical scores of the uncertain candidates of every row,
+// spread over the whole GPU. K7 lists the tasks (32 uncertain candidates of one row each);
+// each warp takes the next task from a counter, one lane per candidate, and fetches the task
+// after it before computing this one. The warp copies its 32 keys into shared memory
+// (coalesced 16-byte copies, 272-byte rows so that the lanes' reads of one 16-byte chunk
+// spread over all banks) and the row's queries widened to fp32; each lane then runs the Hh
+// head chains over i ascending (a fused multiply-add of the widened bf16 operands per step)
+// and sums the heads' ReLU terms in head order.
+// ---------------------------------------------------------------------------------
+constexpr int kRescoreThreads = 256;
+constexpr int kRescoreWarps = kRescoreThreads / 32;
+constexpr int kRescorePitch = 272;   // bytes per staged key row
+
+__host__ __device__ constexpr size_t rescore_smem(int hh) {
+  return (size_t)kRescoreWarps * (32 * kRescorePitch + (size_t)hh * 128 * sizeof(float));
+}
+
+template <int HH>   // 0: any head count up to kScoreMaxHeads
+__global__ void __launch_bounds__(kRescoreThreads, 2) k7r_rescore(TopkArgs a) {
+  extern __shared__ __align__(16) uint8_t rsm[];
+  constexpr int kH = HH > 0 ? HH : kScoreMaxHeads;
+  const int Hh = HH > 0 ? HH : a.Hh;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint8_t* sk = rsm + (size_t)warp * (32 * kRescorePitch + (size_t)kH * 128 * sizeof(float));
+  float* sq = reinterpret_cast<float*>(sk + 32 * kRescorePitch);   // [Hh][128]
+  const uint32_t sk_addr = static_cast<uint32_t>(__cvta_generic_to_shared(sk));
+  pdl_wait();   // every row's candidate lists and the task list are complete
+  pdl_trigger();
+  const int total = (int)a.status[kRescoreTasks];
+  const int2* tasks = reinterpret_cast<const int2*>(a.rtask);
+  auto grab = [&]() {
+    int t = 0;
+    if (lane == 0) t = (int)atomicAdd(&a.status[kRescoreNext], 1u);
+    return __shfl_sync(0xffffffffu, t, 0);
+  };
+  // a task: its row, part and uncertain count, and this lane's (position, block id)
+  struct Task { int lr, part, mu; int2 pb; };
+  auto fetch = [&](int t) {
+    Task k{-1, 0, 0, make_int2(-1, 0)};
+    if (t < total) {
+      const int2 tk = tasks[t];
+      k.lr = tk.x / (kCandCap / 32);
+      k.part = tk.x - k.lr * (kCandCap / 32);
+      k.mu = tk.y;
+      const int jl = k.part * 32 + lane;
+      if (jl < k.mu)
+        k.pb = reinterpret_cast<const int2*>(a.rlist + (size_t)k.lr * kCandCap * 2)[jl];
+    }
+    return k;
+  };
+  int cur = -1;   // the row whose queries are staged
+  Task tk = fetch(grab());
+  while (tk.lr >= 0) {
+    const int lr = tk.lr, l = lr / a.R;
+    const bool valid = tk.pb.x >= 0;
+    const uint8_t* kb = reinterpret_cast<const uint8_t*>(a.keys + (size_t)l * a.key_stride);
+    __syncwarp();   // the previous task's reads of the staging are done
+    // keys: half a warp per key row, 2 rows per copy instruction
+#pragma unroll 4
+    for (int r0 = 0; r0 < 32; r0 += 2) {
+      const int r = r0 + (lane >> 4), c = lane & 15;
+      const int rb = __shfl_sync(0xffffffffu, tk.pb.y, r);
+      const bool v = tk.part * 32 + r < tk.mu;
+      cp_async16(sk_addr + (uint32_t)(r * kRescorePitch + c * 16),
+                 v ? kb + (size_t)rb * 256 + c * 16 : kb, v);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const Task next = fetch(grab());   // its loads overlap this task's
+    if (lr != cur) {
+      const uint16_t* qrow = a.q + (size_t)lr * Hh * 128;
+      for (int i = lane; i < Hh * 64; i += 32) {
+        const uint32_t w2 = __ldg(reinterpret_cast<const uint32_t*>(qrow) + i);
+        sq[2 * i] = bf16_lo(w2);
+        sq[2 * i + 1] = bf16_hi(w2);
+      }
+      cur = lr;
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+    float d[kH];
+#pragma unroll
+    for (int h = 0; h < kH; ++h) d[h] = 0.0f;
+    const uint8_t* kr = sk + lane * kRescorePitch;
+#pragma unroll 2
+    for (int c = 0; c < 16; ++c) {
+      const uint4 kv = *reinterpret_cast<const uint4*>(kr + c * 16);
+      const float k0 = bf16_lo(kv.x), k1 = bf16_hi(kv.x), k2 = bf16_lo(kv.y), k3 = bf16_hi(kv.y);
+      const float k4 = bf16_lo(kv.z), k5 = bf16_hi(kv.z), k6 = bf16_lo(kv.w), k7 = bf16_hi(kv.w);
+#pragma unroll
+      for (int h = 0; h < kH; ++h) {
+        if (HH == 0 && h >= Hh) break;
+        const float4 q0 = *reinterpret_cast<const float4*>(sq + h * 128 + c * 8);
+        const float4 q1 = *reinterpret_cast<const float4*>(sq + h * 128 + c * 8 + 4);
+        float x = d[h];
+        x = __fmaf_rn(q0.x, k0, x);
+        x = __fmaf_rn(q0.y, k1, x);
+        x = __fmaf_rn(q0.z, k2, x);
+        x = __fmaf_rn(q0.w, k3, x);
+        x = __fmaf_rn(q1.x, k4, x);
+        x = __fmaf_rn(q1.y, k5, x);
+        x = __fmaf_rn(q1.z, k6, x);
+        x = __fmaf_rn(q1.w, k7, x);
+        d[h] = x;
+      }
+    }
+    const float* w = a.hw + (size_t)lr * Hh;
+    float sc = 0.0f;
+#pragma unroll
+    for (int h = 0; h < kH; ++h) {
+      if (HH == 0 && h >= Hh) break;
+      sc = __fmaf_rn(__ldg(w + h), d[h] > 0.0f ? d[h] : 0.0f, sc);
+    }
+    if (valid) a.rkey[(size_t)lr * kCandCap + tk.pb.x] = score_key(sc);
+    tk = next;
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// K7c (tensor-core scoring): per (layer, row) deferred by K7, the exact selection among its
+// candidates: threshold over their keys (certain candidates carry the largest key) and the
+// ordered take, ties to the lowest index.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kTopkThreads) k7c_final(TopkArgs a) {
+  __shared__ int hist[256];
+  __shared__ int scratch[33];
+  __shared__ int s_misc[4];
+  __shared__ int s_eq[kTopkWarps], s_gt[kTopkWarps];
+  __shared__ uint32_t r_key[kResidCap];
+  extern __shared__ uint8_t dsm[];
+  int32_t* cand = reinterpret_cast<int32_t*>(dsm);               // [kCandCap] block ids
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(cand + kCandCap);  // [kCandCap] keys
+  pdl_wait();   // the canonical keys of the uncertain candidates are complete
+  const int lr = blockIdx.x, tid = threadIdx.x, K = a.K;
+  const int m = a.rcount[2 * lr];
+  if (m < 0) return;
+  for (int j = tid; j < m; j += blockDim.x) {
+    cand[j] = a.rcand[(size_t)lr * kCandCap + j];
+    ckey[j] = a.rkey[(size_t)lr * kCandCap + j];
+  }
+  __syncthreads();
+  int32_t* out = a.sel + (size_t)lr * K;
+  int need;
+  const uint32_t T = radix_threshold(
+      m, K, [&](int j) { return ckey[j]; }, hist, scratch, r_key, s_misc, a.status, &need);
+  const int taken = ordered_take(
+      m, need,
+      [&](int j) { const uint32_t k = ckey[j]; return k > T ? 2 : (k == T ? 1 : 0); },
+      [&](int p, int j) { if (p < K) out[p] = cand[j]; }, s_eq, s_gt);
+  if (tid == 0) {
+    a.nsel[lr] = K;
+    if (taken != K) flag_status(a.status, kStatusCheck);
   }
 }
 
@@ -1515,6 +1618,11 @@ SelLayout sel_layout(const SelDims& d, bool caller_cidx) {
   L.ccnt = off; off += up(sizeof(int32_t) * LR * kTopkChunks);
   L.clo = off; off += up(sizeof(int32_t) * LR * kTopkChunks);
   L.creg = off; off += up(sizeof(int32_t) * 3 * LR * kTopkChunks * kTopkChunkCap);
+  L.rcand = off; off += up(sizeof(int32_t) * LR * kTopkCandCap);
+  L.rkey = off; off += up(sizeof(uint32_t) * LR * kTopkCandCap);
+  L.rlist = off; off += up(sizeof(int32_t) * 2 * LR * kTopkCandCap);
+  L.rcount = off; off += up(sizeof(int32_t) * 2 * LR);
+  L.rtask = off; off += up(sizeof(int32_t) * 2 * LR * (kTopkCandCap / 32));
   L.total = off;
   return L;
 }
@@ -1581,7 +1689,8 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
                         const SelWorkspace& ws, bool tc, cudaStream_t s) {
   TopkArgs a{d.R, d.Hh, d.N, d.topk, d.key_stride, keys, q, head_w, ws.cidx, ws.ccount,
              ws.uidx, ws.ucount, reinterpret_cast<uint32_t*>(ws.cscore), ws.chi, sel, nsel,
-             ws.header, tc ? 1 : 0, ws.tau, ws.ccnt, ws.clo, ws.creg};
+             ws.header, tc ? 1 : 0, ws.tau, ws.ccnt, ws.clo, ws.creg, ws.rcand, ws.rkey,
+             ws.rlist, ws.rcount, ws.rtask};
   const size_t smem = sizeof(int32_t) * (kCandCap * 2 + kCollectCap * 3) +
                       sizeof(float) * (kScoreMaxHeads * 128 + kScoreMaxHeads);
   cudaError_t err =
@@ -1592,7 +1701,25 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
     err = launch_pdl(k7b_collect, d.L * d.R * kTopkChunks, kCollectThreads, 0, s, a);
     if (err != cudaSuccess) return err;
   }
-  return launch_pdl(k7_topk, d.L * d.R, kTopkThreads, smem, s, a);
+  err = launch_pdl(k7_topk, d.L * d.R, kTopkThreads, smem, s, a);
+  if (err != cudaSuccess || !tc) return err;
+  const int LR = d.L * d.R;
+  const size_t rsmem = rescore_smem(d.Hh == 8 ? 8 : kScoreMaxHeads);
+  const int grid = 2 * device_sm_count();
+  if (d.Hh == 8) {
+    err = cudaFuncSetAttribute(k7r_rescore<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)rsmem);
+    if (err == cudaSuccess) err = launch_pdl(k7r_rescore<8>, grid, kRescoreThreads, rsmem, s, a);
+  } else {
+    err = cudaFuncSetAttribute(k7r_rescore<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)rsmem);
+    if (err == cudaSuccess) err = launch_pdl(k7r_rescore<0>, grid, kRescoreThreads, rsmem, s, a);
+  }
+  if (err != cudaSuccess) return err;
+  const size_t csmem = sizeof(int32_t) * 2 * kCandCap;
+  err = cudaFuncSetAttribute(k7c_final, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(k7c_final, LR, kTopkThreads, csmem, s, a);
 }
 
 }  // namespace dsmoe
