@@ -188,7 +188,8 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
   ws.ucount = reinterpret_cast<int32_t*>(base + L.ucount);
   ws.urows = reinterpret_cast<uint8_t*>(base + L.urows);
   ws.cscore = reinterpret_cast<float*>(base + L.cscore);
-  ws.chi = reinterpret_cast<float*>(base + L.chi);
+  ws.knorm = reinterpret_cast<float*>(base + L.knorm);
+  ws.qnorm = reinterpret_cast<float*>(base + L.qnorm);
   ws.tau = reinterpret_cast<uint32_t*>(base + L.tau);
   ws.ccnt = reinterpret_cast<int32_t*>(base + L.ccnt);
   ws.clo = reinterpret_cast<int32_t*>(base + L.clo);

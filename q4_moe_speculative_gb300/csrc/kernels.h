@@ -68,9 +68,10 @@ struct SelWorkspace {
   int32_t* uidx;      // [L][N] union of the rows' admitted blocks, ascending
   int32_t* ucount;    // [L]
   uint8_t* urows;     // [L][N] bit r: row r admits the union entry
-  float* cscore;      // [L][R][N] by union entry: canonical scores, or (tensor-core
-                      // scoring) order keys of the lower bounds of the scores
-  float* chi;         // [L][R][N] by union entry: upper bounds (tensor-core scoring)
+  float* cscore;      // [L][R][NS] by union entry: canonical or tensor-core scores
+                      // (-inf where the row does not admit the entry)
+  float* knorm;       // [L][NS] by union entry: key norm bound (tensor-core scoring)
+  float* qnorm;       // [L][R] sum_h |w_h| ||q_h|| bound (tensor-core scoring)
   uint32_t* tau;      // [L][R] sampled collection threshold (top-k, tensor-core scoring)
   int32_t* ccnt;      // [L][R][kTopkChunks] entries collected per row chunk
   int32_t* clo;       // [L][R][kTopkChunks] entries with a lower bound >= tau per chunk
@@ -83,12 +84,17 @@ struct SelWorkspace {
   int32_t* rtask;     // [L][R * kTopkCandCap / 32][2] re-score tasks: row * 128 + part, count
 };
 
-constexpr int kTopkChunks = 2;        // collect CTAs per row (516 at 43 x 6 rows: one wave)
-constexpr int kTopkChunkCap = 2048;   // collected entries kept per row chunk (x2 = 4096)
+constexpr int kTopkChunks = 8;        // collect CTAs (2 warps) per row: 2064 at 43 x 6 rows,
+                                      // 13 or 14 per SM in one wave
+constexpr int kTopkChunkCap = 1024;   // collected entries kept per row chunk (x8 = 8192)
 constexpr int kTopkCandCap = 4096;    // re-score candidates per row
+// Row stride of the score arrays (cscore, knorm): N rounded up to a multiple of 4, so that
+// every row starts 16-byte aligned.
+inline int score_stride(int N) { return (N + 3) & ~3; }
 
 struct SelLayout {
-  size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, chi, tau, ccnt, clo, creg,
+  size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, knorm, qnorm, tau, ccnt, clo,
+      creg,
       rcand, rkey, rlist, rcount, rtask, total;
 };
 SelLayout sel_layout(const SelDims& d, bool caller_cidx);

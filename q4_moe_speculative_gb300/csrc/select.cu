@@ -115,6 +115,20 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 
 constexpr uint32_t kCertainKey = 0xFFFFFFFFu;   // above the key of every finite score
 
+// Interval [lo, hi] (order keys) around a tensor-core score s (fp32 bits) that contains the
+// canonical score: eps = kn * G rounded upward (kn the key norm bound, G the row's
+// 2^-10 * sum_h |w_h| ||q_h|| rounded upward), lo = s - eps rounded downward, hi = s + eps
+// rounded upward. An entry the row does not admit (s = -inf) gets lo = kNoScoreKey and
+// hi = the key of -inf.
+__device__ __forceinline__ uint32_t tc_lo(uint32_t sbits, float kn, float G) {
+  if (sbits == kMinusInfBits) return kNoScoreKey;
+  return score_key(__fsub_rd(__uint_as_float(sbits), __fmul_ru(kn, G)));
+}
+__device__ __forceinline__ uint32_t tc_hi(uint32_t sbits, float kn, float G) {
+  if (sbits == kMinusInfBits) return score_key(__uint_as_float(kMinusInfBits));
+  return score_key(__fadd_ru(__uint_as_float(sbits), __fmul_ru(kn, G)));
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -307,11 +321,13 @@ struct ScoreArgs {
   const int32_t* ucount;
   const uint8_t* urows;
   const int32_t* uwordoff;
-  uint32_t* sc0;      // [L][R][N] by union entry: fp32 scores, or lower-bound keys
-  float* sc1;         // [L][R][N] by union entry: upper bounds (tensor-core mode)
+  uint32_t* sc0;      // [L][R][N] by union entry: fp32 scores (-inf: not admitted)
+  float* knorm;       // [L][N] by union entry: key norm bound (tensor-core mode)
+  float* qnorm;       // [L][R] 2^-10 sum_h |w_h| ||q_h|| bound (tensor-core mode)
   uint32_t* status;
   int tma;            // kmap is valid: tiles of 128 consecutive blocks come by TMA
   CUtensorMap kmap;   // keys [L][N][128] bf16, boxes of 64 values x 128 blocks, 128B swizzle
+  int NS;             // row stride of sc0 / knorm (N rounded up to a multiple of 4)
 };
 
 // ---------------------------------------------------------------------------------
@@ -365,7 +381,7 @@ __global__ void __launch_bounds__(kScoreThreads) k5_score(ScoreArgs a) {
   const int e = a.uwordoff[(size_t)l * W + (b >> 5)] + __popc(uw & ((1u << (b & 31)) - 1u));
 
   for (int r = 0; r < R; ++r) {
-    const size_t out = ((size_t)l * R + r) * a.N + e;
+    const size_t out = ((size_t)l * R + r) * a.NS + e;
     if (!(rows & (1u << r))) {
       a.sc0[out] = kMinusInfBits;
       continue;
@@ -683,6 +699,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
               for (int h = 0; h < Hh; ++h)
                 F = __fmaf_ru(fabsf(s_w[slot][lane * Hh + h]), s_qn[lane * Hh + h], F);
               s_F[slot][lane] = F;
+              a.qnorm[(size_t)l * R + lane] = __fmul_ru(kEpsRel, F);   // same from every CTA
             }
           }
           qlayer[slot] = l;
@@ -820,18 +837,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
       sm100::tc_fence_before();   // the group barrier of the next tile orders the next MMA
       const int e = e0 + row;
       if (e < ucnt) {
-        // interval bounds of row r's score: [s - eps, s + eps] with
-        // eps = 2^-10 * ||k|| * sum_h |w_h| ||q_h||, both rounded outward
+        // row r's tensor-core score; its interval comes from kn and the row's norm bound
+        // (tc_interval) wherever it is used
+        a.knorm[(size_t)l * a.NS + e] = kn;
         auto emit = [&](int r, float sc) {
-          const size_t out = ((size_t)l * R + r) * N + e;
-          if (rows & (1u << r)) {
-            const float eps = __fmul_ru(__fmul_ru(kEpsRel, kn), s_F[slot][r]);
-            a.sc0[out] = score_key(__fsub_rd(sc, eps));
-            a.sc1[out] = __fadd_ru(sc, eps);
-          } else {
-            a.sc0[out] = kNoScoreKey;
-            a.sc1[out] = __uint_as_float(kMinusInfBits);
-          }
+          const size_t out = ((size_t)l * R + r) * a.NS + e;
+          a.sc0[out] = (rows & (1u << r)) ? __float_as_uint(sc) : kMinusInfBits;
         };
         if constexpr (HH > 0) {   // head count known at compile time: static indices
 #pragma unroll
@@ -982,9 +993,14 @@ __device__ uint32_t radix_threshold(int n, int need, KeyAt key_at, int* hist, in
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             const int i = i0 + u * 32 + lane;
-            if (i < end && (k[u] >> 16) == prefix) {
-              const int p = atomicAdd(&s_rn, 1);
-              if (p < kResidCap) r_key[p] = k[u];
+            const bool in = i < end && (k[u] >> 16) == prefix;
+            const unsigned bal = __ballot_sync(0xffffffffu, in);
+            if (bal) {   // one shared atomic per warp and batch
+              int base = 0;
+              if (lane == 0) base = atomicAdd(&s_rn, __popc(bal));
+              base = __shfl_sync(0xffffffffu, base, 0);
+              const int p = base + __popc(bal & ((1u << lane) - 1u));
+              if (in && p < kResidCap) r_key[p] = k[u];
             }
           }
         }
@@ -1076,7 +1092,8 @@ struct TopkArgs {
   const int32_t* uidx;
   const int32_t* ucount;
   uint32_t* sc0;
-  const float* sc1;
+  const float* knorm;
+  const float* qnorm;
   int32_t* sel;
   int32_t* nsel;
   uint32_t* status;
@@ -1090,6 +1107,7 @@ struct TopkArgs {
   int32_t* rlist;
   int32_t* rcount;
   int32_t* rtask;
+  int NS;             // row stride of sc0 / knorm (N rounded up to a multiple of 4)
 };
 
 constexpr uint32_t kTauDirect = 0xFFFFFFFFu;   // row with at most K admitted: no collection
@@ -1122,9 +1140,14 @@ __global__ void __launch_bounds__(kTopkThreads) k7a_tau(TopkArgs a) {
   uint32_t tau = 0u;
   if (n > kCollectCap) {
     constexpr int kChunks = 64, kS = kChunks * 32;
-    const uint32_t* s0 = a.sc0 + (size_t)lr * a.N;
+    const uint32_t* s0 = a.sc0 + (size_t)lr * a.NS;
+    const float* kn = a.knorm + (size_t)l * a.NS;
+    const float G = a.qnorm[lr];   // eps per unit key norm
     const int spacing = n / kChunks;
-    for (int j = tid; j < kS; j += blockDim.x) samp[j] = s0[(j >> 5) * spacing + (j & 31)];
+    for (int j = tid; j < kS; j += blockDim.x) {
+      const int i = (j >> 5) * spacing + (j & 31);
+      samp[j] = tc_lo(s0[i], kn[i], G);
+    }
     __syncthreads();
     const int rank = min(kS, (int)(((long long)K * kS + n - 1) / n) + 16);
     int need;
@@ -1143,7 +1166,7 @@ __global__ void __launch_bounds__(kTopkThreads) k7a_tau(TopkArgs a) {
 // and how many entries have a lower bound >= tau. A chunk with more matches than its
 // region (or a warp with more than its buffer) reports a count above the capacity.
 // ---------------------------------------------------------------------------------
-constexpr int kCollectThreads = 256;
+constexpr int kCollectThreads = 64;
 constexpr int kCollectWarps = kCollectThreads / 32;
 constexpr int kWarpBuf = 256;
 
@@ -1156,38 +1179,81 @@ __global__ void __launch_bounds__(kCollectThreads) k7b_collect(TopkArgs a) {
   const uint32_t tau = a.tau[lr];
   if (tau == kTauDirect) return;
   const int n = a.ucount[l];
-  const int per = (n + kTopkChunks - 1) / kTopkChunks;
+  // chunks and warp segments start at multiples of 4 entries: 16-byte aligned in the rows
+  const int per = ((n + kTopkChunks - 1) / kTopkChunks + 127) & ~127;
   const int c0 = min(n, chunk * per), c1 = min(n, c0 + per);
-  const uint32_t* s0 = a.sc0 + (size_t)lr * a.N;
-  const float* s1 = a.sc1 + (size_t)lr * a.N;
-  // contiguous warp segments of the chunk, in multiples of 32
-  const int seg = ((c1 - c0 + kCollectWarps - 1) / kCollectWarps + 31) & ~31;
+  const uint32_t* s0 = a.sc0 + (size_t)lr * a.NS;
+  const float* kn = a.knorm + (size_t)l * a.NS;
+  const float G = a.qnorm[lr];   // eps per unit key norm
+  const int seg = ((c1 - c0 + kCollectWarps - 1) / kCollectWarps + 127) & ~127;
   const int beg = min(c1, c0 + warp * seg), end = min(c1, beg + seg);
-  constexpr int U = 16;   // 32 loads in flight per lane
+  // Each lane takes 4 consecutive entries of a group of 128 (16-byte loads; entries past
+  // `end` in the last group lie inside the row's padded stride and are masked). U groups
+  // per batch; the next batch's loads are in flight while this one is classified. The
+  // taken entries keep index order: a lane's place is the prefix over the lanes of their
+  // counts (bit-sliced ballots).
+  constexpr int U = 2;
   int cnt = 0, nlo = 0;
-  for (int i0 = beg; i0 < end; i0 += 32 * U) {
-    uint32_t hk[U], lk[U];
+  uint4 sv[U];
+  float4 kv[U];
+  const uint4 kNone = make_uint4(kMinusInfBits, kMinusInfBits, kMinusInfBits, kMinusInfBits);
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int i = beg + u * 128 + 4 * lane;
+    sv[u] = i < end ? *reinterpret_cast<const uint4*>(s0 + i) : kNone;
+    kv[u] = i < end ? *reinterpret_cast<const float4*>(kn + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  for (int g0 = beg; g0 < end; g0 += 128 * U) {
+    uint4 sn[U];
+    float4 kx[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int i = i0 + u * 32 + lane;
-      hk[u] = i < end ? score_key(s1[i]) : 0u;
-      lk[u] = i < end ? s0[i] : 0u;
+      const int i = g0 + 128 * U + u * 128 + 4 * lane;
+      sn[u] = i < end ? *reinterpret_cast<const uint4*>(s0 + i) : kNone;
+      kx[u] = i < end ? *reinterpret_cast<const float4*>(kn + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int i = i0 + u * 32 + lane;
-      const bool take = i < end && hk[u] >= tau;
-      const uint32_t tm = __ballot_sync(0xffffffffu, take);
-      nlo += __popc(__ballot_sync(0xffffffffu, i < end && lk[u] >= tau));
-      const int p = cnt + __popc(tm & ((1u << lane) - 1u));
-      if (take && p < kWarpBuf) {
-        s_buf[warp][0][p] = (uint32_t)i;
-        s_buf[warp][1][p] = lk[u];
-        s_buf[warp][2][p] = hk[u];
+      const int i = g0 + u * 128 + 4 * lane;
+      const uint32_t sb[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+      const float k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+      uint32_t hk[4];
+      unsigned tm = 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hk[e] = tc_hi(sb[e], k4[e], G);
+        tm |= (i + e < end && hk[e] >= tau) ? 1u << e : 0u;
       }
-      cnt += __popc(tm);
+      if (__ballot_sync(0xffffffffu, tm != 0u)) {   // lo <= hi: only taken entries count
+        const int c = __popc(tm);
+        const unsigned b0 = __ballot_sync(0xffffffffu, c & 1);
+        const unsigned b1 = __ballot_sync(0xffffffffu, c & 2);
+        const unsigned b2 = __ballot_sync(0xffffffffu, c & 4);
+        int p = cnt + __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (tm & (1u << e)) {
+            const uint32_t lk = tc_lo(sb[e], k4[e], G);
+            nlo += lk >= tau ? 1 : 0;
+            if (p < kWarpBuf) {
+              s_buf[warp][0][p] = (uint32_t)(i + e);
+              s_buf[warp][1][p] = lk;
+              s_buf[warp][2][p] = hk[e];
+            }
+            ++p;
+          }
+        }
+        cnt += __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      sv[u] = sn[u];
+      kv[u] = kx[u];
     }
   }
+  nlo = __reduce_add_sync(0xffffffffu, nlo);
   if (lane == 0) { s_cnt[warp] = cnt; s_lo[warp] = nlo; }
   __syncthreads();
   int off = 0, total = 0, lo_total = 0;
@@ -1250,12 +1316,13 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
 
   const int n = a.ucount[l];
   const int32_t* ui = a.uidx + (size_t)l * a.N;
-  uint32_t* s0 = a.sc0 + (size_t)lr * a.N;
+  uint32_t* s0 = a.sc0 + (size_t)lr * a.NS;
   const uint16_t* kbase = a.keys + (size_t)l * a.key_stride;
   bool canonical = !a.tc_mode;
 
   if (a.tc_mode) {
-    const float* s1 = a.sc1 + (size_t)lr * a.N;
+    const float* kn = a.knorm + (size_t)l * a.NS;
+    const float G = a.qnorm[lr];   // eps per unit key norm
     // Fast path: the entries collected by K7b (every entry whose upper bound reaches tau,
     // in index order). If at least K of the row's entries have a lower bound >= tau, the
     // K-th largest lower bound T over the row is among them and every candidate (upper
@@ -1330,10 +1397,11 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       cand_entries = true;
       int need;
       const uint32_t T = radix_threshold(
-          n, K, [&](int i) { return s0[i]; }, hist, scratch, r_key, s_misc, a.status, &need);
+          n, K, [&](int i) { return tc_lo(s0[i], kn[i], G); }, hist, scratch, r_key, s_misc,
+          a.status, &need);
       // Ordered gather of the candidates (upper bound reaches T), bounded by kCandCap.
       m = ordered_take(
-          n, 0, [&](int i) { return score_key(s1[i]) >= T ? 2 : 0; },
+          n, 0, [&](int i) { return tc_hi(s0[i], kn[i], G) >= T ? 2 : 0; },
           [&](int p, int i) {
             if (p < kCandCap) {
               cand[p] = i;
@@ -1396,7 +1464,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       __syncthreads();
     }
     for (int i = tid; i < n; i += blockDim.x) {
-      const bool adm = __float_as_uint(s1[i]) != kMinusInfBits;
+      const bool adm = s0[i] != kMinusInfBits;
       s0[i] = adm ? __float_as_uint(canonical_score(qf, kbase + (size_t)ui[i] * 128, wf, a.Hh))
                   : kMinusInfBits;
     }
@@ -1612,8 +1680,9 @@ SelLayout sel_layout(const SelDims& d, bool caller_cidx) {
   L.uidx = off; off += up(sizeof(int32_t) * (size_t)d.L * d.N);
   L.ucount = off; off += up(sizeof(int32_t) * (size_t)d.L);
   L.urows = off; off += up((size_t)d.L * d.N);
-  L.cscore = off; off += up(sizeof(float) * LR * (size_t)d.N);
-  L.chi = off; off += up(sizeof(float) * LR * (size_t)d.N);
+  L.cscore = off; off += up(sizeof(float) * LR * (size_t)score_stride(d.N));
+  L.knorm = off; off += up(sizeof(float) * (size_t)d.L * score_stride(d.N));
+  L.qnorm = off; off += up(sizeof(float) * LR);
   L.tau = off; off += up(sizeof(uint32_t) * LR);
   L.ccnt = off; off += up(sizeof(int32_t) * LR * kTopkChunks);
   L.clo = off; off += up(sizeof(int32_t) * LR * kTopkChunks);
@@ -1647,8 +1716,9 @@ cudaError_t launch_score(const SelDims& d, const uint16_t* keys, const uint16_t*
                          const float* head_w, const uint32_t* mask, const int32_t* limit,
                          const SelWorkspace& ws, bool tc, cudaStream_t s) {
   ScoreArgs a{d.L, d.R, d.Hh, d.N, d.key_stride, keys, q, head_w, mask, limit, ws.uidx,
-              ws.ucount, ws.urows, ws.wordoff, reinterpret_cast<uint32_t*>(ws.cscore), ws.chi,
-              ws.header};
+              ws.ucount, ws.urows, ws.wordoff, reinterpret_cast<uint32_t*>(ws.cscore), ws.knorm,
+              ws.qnorm, ws.header};
+  a.NS = score_stride(d.N);
   if (!tc) {
     const int RH = d.R * d.Hh;
     const size_t smem = sizeof(float) * ((size_t)RH * 128 + ((RH + 3) & ~3)) +
@@ -1688,9 +1758,11 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
                         const float* head_w, int32_t* sel, int32_t* nsel,
                         const SelWorkspace& ws, bool tc, cudaStream_t s) {
   TopkArgs a{d.R, d.Hh, d.N, d.topk, d.key_stride, keys, q, head_w, ws.cidx, ws.ccount,
-             ws.uidx, ws.ucount, reinterpret_cast<uint32_t*>(ws.cscore), ws.chi, sel, nsel,
+             ws.uidx, ws.ucount, reinterpret_cast<uint32_t*>(ws.cscore), ws.knorm, ws.qnorm, sel,
+             nsel,
              ws.header, tc ? 1 : 0, ws.tau, ws.ccnt, ws.clo, ws.creg, ws.rcand, ws.rkey,
              ws.rlist, ws.rcount, ws.rtask};
+  a.NS = score_stride(d.N);
   const size_t smem = sizeof(int32_t) * (kCandCap * 2 + kCollectCap * 3) +
                       sizeof(float) * (kScoreMaxHeads * 128 + kScoreMaxHeads);
   cudaError_t err =
