@@ -35,7 +35,7 @@
 namespace dsmoe {
 namespace {
 
-constexpr int kCompactThreads = 1024;
+constexpr int kCompactThreads = 512;   // 3 CTAs per SM
 constexpr int kScoreThreads = 128;   // canonical scorer: one key per thread
 constexpr int kScoreMaxHeads = 16;
 constexpr int kTopkThreads = 512;
@@ -195,20 +195,21 @@ struct CompactArgs {
   int want_cidx;       // the caller passed cidx / ccount
 };
 
-__global__ void __launch_bounds__(kCompactThreads) k6_compact(CompactArgs a) {
+__global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) {
   __shared__ int scratch[33];
   __shared__ int s_off[kCompactThreads];
   __shared__ int s_lim[8];
   const int R = a.R, N = a.N;
   const int W = (N + 31) >> 5;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool union_cta = (int)blockIdx.x >= a.L * R;
-  // union CTAs: one per (layer, chunk of kCompactThreads words)
+  // union CTAs (the longer ones, first): one per (layer, chunk of kCompactThreads words);
+  // then one row CTA per (layer, row)
   const int P = (W + kCompactThreads - 1) / kCompactThreads;
-  const int uc = (int)blockIdx.x - a.L * R;
-  const int l = union_cta ? uc / P : (int)blockIdx.x / R;
+  const bool union_cta = (int)blockIdx.x < a.L * P;
+  const int uc = blockIdx.x;
+  const int lr = (int)blockIdx.x - a.L * P;   // meaningful for row CTAs only
+  const int l = union_cta ? uc / P : lr / R;
   const int uchunk = union_cta ? uc - l * P : 0;
-  const int lr = blockIdx.x;   // meaningful for row CTAs only
   const uint32_t* mrow = a.mask + (size_t)(union_cta ? l * R : lr) * W;
   if (tid < R) {
     const int lim = a.limit[(size_t)l * R + tid];
@@ -321,8 +322,8 @@ struct ScoreArgs {
   const int32_t* ucount;
   const uint8_t* urows;
   const int32_t* uwordoff;
-  uint32_t* sc0;      // [L][R][N] by union entry: fp32 scores (-inf: not admitted)
-  float* knorm;       // [L][N] by union entry: key norm bound (tensor-core mode)
+  uint32_t* sc0;      // [L][R][NS] by union entry: fp32 scores (-inf: not admitted)
+  float* knorm;       // [L][NS] by union entry: key norm bound (tensor-core mode)
   float* qnorm;       // [L][R] 2^-10 sum_h |w_h| ||q_h|| bound (tensor-core mode)
   uint32_t* status;
   int tma;            // kmap is valid: tiles of 128 consecutive blocks come by TMA
