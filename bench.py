@@ -35,6 +35,10 @@ if str(ROOT) not in sys.path:
 
 import synth  # noqa: E402
 
+# Kernels one step launches: the MoE verify call (router, gate/up, down, combine) and the
+# tensor-core select (compact, score, tau, collect, top-k, re-score, final select).
+MOE_KERNELS = 4
+SELECT_KERNELS = 7
 METRIC = "Q4 MoE verify weight GB/s (% of HBM peak) at R=1/6; top-512 select µs @300k ctx"
 UNIT = "GB/s"
 Q4_BYTES_PER_WEIGHT = 0.5625          # 4 bits + one fp16 scale per 32 values
@@ -463,7 +467,7 @@ def run_ours(args, world, rank, local):
                 "d2h_bytes_per_step": int(d2h),
                 "select_300k_us_median": round(1e3 * statistics.median(e2e_sel), 2),
                 "api": "ds_moe_verify_forward + ds_select_blocks, pinned host buffers"},
-        "gpu_launches": 7 * K,
+        "gpu_launches": (MOE_KERNELS + SELECT_KERNELS) * K,
         "sha256": {"y_last_step": y0_sha},
     }
     out["config"]["select_layers"] = args.select_layers
