@@ -934,53 +934,79 @@ __device__ __forceinline__ void hist_pass(int n, bool resid, const uint32_t* r_k
 
 // The key of the need-th largest element among n keys, MSB-first 8 bits at a time. After
 // the first two passes the elements whose top 16 bits match are gathered into r_key (if
-// at most kResidCap of them) and the last two passes run there. *need_out = how many
-// elements equal to the threshold belong to the selection. All threads must call it.
+// at most kResidCap of them) and the last two passes run there. Two block barriers per
+// pass: one after the histogram (hist holds two 256-bin buffers, the next pass's cleared
+// while this one fills), one after warp 0 has found the bucket (8 bins per lane, a warp
+// scan). *need_out = how many elements equal to the threshold belong to the selection.
+// All threads must call it.
 template <typename KeyAt>
 __device__ uint32_t radix_threshold(int n, int need, KeyAt key_at, int* hist, int* scratch,
                                     uint32_t* r_key, int* s_misc, uint32_t* status,
                                     int* need_out, int passes = 4) {
-  const int tid = threadIdx.x, lane = tid & 31;
+  (void)scratch;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int& s_bucket = s_misc[0];
   int& s_need = s_misc[1];
   int& s_rn = s_misc[2];
+  int& s_cnt = s_misc[3];   // elements in the chosen bucket
   uint32_t prefix = 0;
   bool resid = false;
+  for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
   for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-    if (tid == 0) {
-      s_bucket = -1;
-      s_need = need;
-    }
-    __syncthreads();
+    int* h = hist + (pass & 1) * 256;
+    if (tid == 0 && pass == 1) s_rn = 0;
     hist_pass(n, resid, r_key, resid ? min(s_rn, kResidCap) : 0, shift, prefix,
-              pass == 0, key_at, hist);
+              pass == 0, key_at, h);
+    for (int i = tid; i < 256; i += blockDim.x) hist[((pass + 1) & 1) * 256 + i] = 0;
     __syncthreads();
-    {
-      const int v = tid < 256 ? hist[255 - tid] : 0;
-      int total;
-      const int excl = block_excl_scan(v, scratch, &total);
-      if (tid < 256 && excl < need && need <= excl + v) {
-        s_bucket = 255 - tid;
-        s_need = need - excl;
+    if (warp == 0) {
+      // lane l holds bins 255 - 8l down to 248 - 8l (descending keys)
+      int v[8], sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        v[q] = h[255 - 8 * lane - q];
+        sum += v[q];
       }
-    }
-    __syncthreads();
-    if (s_bucket < 0) {  // histogram inconsistent with `need`: report, keep indices valid
-      if (tid == 0) {
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      int acc = incl - sum, bucket = -1, nneed = need, bcnt = 0;
+      if (acc < need && need <= incl) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (bucket < 0 && acc < need && need <= acc + v[q]) {
+            bucket = 255 - 8 * lane - q;
+            nneed = need - acc;
+            bcnt = v[q];
+          }
+          acc += v[q];
+        }
+      }
+      const unsigned found = __ballot_sync(0xffffffffu, bucket >= 0);
+      if (bucket >= 0) {
+        s_bucket = bucket;
+        s_need = nneed;
+        s_cnt = bcnt;
+      }
+      if (!found && lane == 0) {   // histogram inconsistent with `need`: report
         flag_status(status, kStatusCheck);
         s_bucket = 0;
+        s_need = need;
+        s_cnt = h[255];
       }
-      __syncthreads();
     }
-    prefix = (prefix << 8) | (uint32_t)s_bucket;
+    __syncthreads();
+    const int b = s_bucket;
+    const int cnt = s_cnt;   // (h may be cleared by a thread already in the next pass)
+    prefix = (prefix << 8) | (uint32_t)b;
     need = s_need;
     if (pass == 1 && !resid && passes > 2) {
-      const int cnt = hist[s_bucket];
       if (cnt <= kResidCap) {
-        if (tid == 0) s_rn = 0;
-        __syncthreads();
         constexpr int U = 8;
         int beg, end;
         warp_segment(n, &beg, &end);
@@ -994,14 +1020,9 @@ __device__ uint32_t radix_threshold(int n, int need, KeyAt key_at, int* hist, in
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             const int i = i0 + u * 32 + lane;
-            const bool in = i < end && (k[u] >> 16) == prefix;
-            const unsigned bal = __ballot_sync(0xffffffffu, in);
-            if (bal) {   // one shared atomic per warp and batch
-              int base = 0;
-              if (lane == 0) base = atomicAdd(&s_rn, __popc(bal));
-              base = __shfl_sync(0xffffffffu, base, 0);
-              const int p = base + __popc(bal & ((1u << lane) - 1u));
-              if (in && p < kResidCap) r_key[p] = k[u];
+            if (i < end && (k[u] >> 16) == prefix) {
+              const int p = atomicAdd(&s_rn, 1);
+              if (p < kResidCap) r_key[p] = k[u];
             }
           }
         }
@@ -1010,8 +1031,8 @@ __device__ uint32_t radix_threshold(int n, int need, KeyAt key_at, int* hist, in
         if (s_rn != cnt && tid == 0) flag_status(status, kStatusCheck);
       }
     }
-    __syncthreads();
   }
+  __syncthreads();   // s_misc and hist are free for the caller
   *need_out = need;
   return prefix << (32 - 8 * passes);   // with fewer passes: the bucket's lower bound
 }
@@ -1126,7 +1147,7 @@ constexpr int kRescoreNext = 2;
 // whole get tau = 0.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kTopkThreads) k7a_tau(TopkArgs a) {
-  __shared__ int hist[256];
+  __shared__ int hist[512];   // two radix histogram buffers
   __shared__ int scratch[33];
   __shared__ int s_misc[4];
   __shared__ uint32_t samp[2048];
@@ -1283,7 +1304,7 @@ __global__ void __launch_bounds__(kCollectThreads) k7b_collect(TopkArgs a) {
 }
 
 __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
-  __shared__ int hist[256];
+  __shared__ int hist[512];   // two radix histogram buffers
   __shared__ int scratch[33];
   __shared__ int s_misc[4];
   __shared__ int s_eq[kTopkWarps], s_gt[kTopkWarps];
@@ -1614,7 +1635,7 @@ __global__ void __launch_bounds__(kRescoreThreads, 2) k7r_rescore(TopkArgs a) {
 // ordered take, ties to the lowest index.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kTopkThreads) k7c_final(TopkArgs a) {
-  __shared__ int hist[256];
+  __shared__ int hist[512];   // two radix histogram buffers
   __shared__ int scratch[33];
   __shared__ int s_misc[4];
   __shared__ int s_eq[kTopkWarps], s_gt[kTopkWarps];
