@@ -1514,8 +1514,8 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
 // ---------------------------------------------------------------------------------
 // K7r (tensor-core scoring): canonical scores of the uncertain candidates of every row,
 // spread over the whole GPU. K7 lists the tasks (32 uncertain candidates of one row each);
-// each warp takes the next task from a counter, one lane per candidate, and fetches the task
-// after it before computing this one. The warp copies its 32 keys into shared memory
+// warp w starts with task w and then takes the next task from a counter, one lane per
+// candidate, fetching the task after it before computing this one. The warp copies its 32 keys into shared memory
 // (coalesced 16-byte copies, 272-byte rows so that the lanes' reads of one 16-byte chunk
 // spread over all banks) and the row's queries widened to fp32; each lane then runs the Hh
 // head chains over i ascending (a fused multiply-add of the widened bf16 operands per step)
@@ -1542,9 +1542,11 @@ __global__ void __launch_bounds__(kRescoreThreads, 2) k7r_rescore(TopkArgs a) {
   pdl_trigger();
   const int total = (int)a.status[kRescoreTasks];
   const int2* tasks = reinterpret_cast<const int2*>(a.rtask);
+  // the first task of warp w is task w; later ones come from the counter, past the grid
+  const int W = (int)gridDim.x * kRescoreWarps;
   auto grab = [&]() {
     int t = 0;
-    if (lane == 0) t = (int)atomicAdd(&a.status[kRescoreNext], 1u);
+    if (lane == 0) t = W + (int)atomicAdd(&a.status[kRescoreNext], 1u);
     return __shfl_sync(0xffffffffu, t, 0);
   };
   // a task: its row, part and uncertain count, and this lane's (position, block id)
@@ -1563,7 +1565,7 @@ __global__ void __launch_bounds__(kRescoreThreads, 2) k7r_rescore(TopkArgs a) {
     return k;
   };
   int cur = -1;   // the row whose queries are staged
-  Task tk = fetch(grab());
+  Task tk = fetch((int)blockIdx.x * kRescoreWarps + warp);
   while (tk.lr >= 0) {
     const int lr = tk.lr, l = lr / a.R;
     const bool valid = tk.pb.x >= 0;
