@@ -1370,14 +1370,16 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       if (!s_bad && s_lo_total >= K) {
         const int total = s_off[kTopkChunks];
         const size_t plane = (size_t)gridDim.x * kTopkChunks * kTopkChunkCap;
-        for (int c = 0; c < kTopkChunks; ++c) {
+        // one pass over the concatenation (each entry finds its chunk), loads all independent
+        for (int q = tid; q < total; q += blockDim.x) {
+          int c = 0;
+#pragma unroll
+          for (int cc = 1; cc < kTopkChunks; ++cc) c += q >= s_off[cc] ? 1 : 0;
           const int32_t* reg = a.creg + ((size_t)lr * kTopkChunks + c) * kTopkChunkCap;
-          const int cc = s_off[c + 1] - s_off[c];
-          for (int p = tid; p < cc; p += blockDim.x) {
-            col_i[s_off[c] + p] = reg[p];
-            col_lo[s_off[c] + p] = (uint32_t)reg[plane + p];
-            col_hi[s_off[c] + p] = (uint32_t)reg[2 * plane + p];
-          }
+          const int p = q - s_off[c];
+          col_i[q] = reg[p];
+          col_lo[q] = (uint32_t)reg[plane + p];
+          col_hi[q] = (uint32_t)reg[2 * plane + p];
         }
         __syncthreads();
         int need;
@@ -1432,8 +1434,6 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
           },
           s_eq, s_gt);
     }
-    // This row's head weights (fp32).
-    for (int i = tid; i < a.Hh; i += blockDim.x) wf[i] = a.hw[(size_t)lr * a.Hh + i];
     __syncthreads();
     if (m <= kCandCap) {
       // Deferred to K7r / K7c: the candidates (block ids, in index order) with their keys
@@ -1478,8 +1478,10 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       return;
     }
     // Too many candidates (e.g. heavy ties): canonical scores for the whole row, with the
-    // row's queries as fp32 in the [i][head] layout (the lanes of a block read adjacent words).
+    // row's queries as fp32 in the [i][head] layout (the lanes of a block read adjacent words)
+    // and its head weights.
     {
+      for (int i = tid; i < a.Hh; i += blockDim.x) wf[i] = a.hw[(size_t)lr * a.Hh + i];
       const uint16_t* qrow = a.q + (size_t)lr * a.Hh * 128;
       for (int i = tid; i < a.Hh * 128; i += blockDim.x)
         qf[(i & 127) * kScoreMaxHeads + (i >> 7)] = bf16_bits_to_f32(qrow[i]);
