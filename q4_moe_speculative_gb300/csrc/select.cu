@@ -13,7 +13,9 @@
 //  K5  scores every union entry for the rows that admit it; results are stored by union
 //      position [layer][row][entry]. Rows that do not admit an entry get a sentinel that
 //      sorts below every score.
-//  K7  per (layer, row): bounded radix top-k over the union entries.
+//  K7  per (layer, row): bounded radix top-k over the union entries (tensor-core mode: K7a
+//      sampled threshold, K7b collection, K7 candidates, K7r re-score over the whole GPU,
+//      K7c final select).
 //
 // Two scoring modes give the same selection:
 //  * canonical: every score in the canonical fp32 order (fmaf over i ascending, then over
@@ -25,9 +27,11 @@
 //    |s_tc - s_canon| <= eps = 2^-10 * ||k|| * sum_h |w_h| ||q_h||. (Both dot products are
 //    sums of exact products whose magnitudes add up to at most ||q|| ||k||; a few hundred
 //    fp32 roundings of such sums stay below 2^-15 of that, so 2^-10 leaves a margin of 2^5.)
-//    K7 takes T = k-th largest lo; every block of the canonical top-k has hi >= T, so only
-//    the candidates with hi >= T are re-scored in the canonical order and selected among
-//    exactly. The result is identical to the canonical mode by construction.
+//    K5 stores s_tc per admitting row and ||k|| per entry; every consumer derives [lo, hi]
+//    with the same function (tc_lo / tc_hi), so the bounds agree bit for bit. K7 takes
+//    T = k-th largest lo; every block of the canonical top-k has hi >= T, so only the
+//    candidates with hi >= T are re-scored in the canonical order (K7r) and selected among
+//    exactly (K7c). The result is identical to the canonical mode by construction.
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -442,8 +446,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
 //  * two epilogue groups of 4 warps take alternate tiles; each has its own TMEM
 //    accumulator. The group's first thread issues the 8 tcgen05.mma (M = 128 keys,
 //    N = NPAD >= R*Hh, K = 16 each) and commits to the group's mbarrier; each warp then
-//    reads its 32 lanes (one key per thread) and writes the interval bounds for every row,
-//    and releases the stage on its `empty` barrier.
+//    reads its 32 lanes (one key per thread), writes the score for every admitting row and
+//    the key's norm bound, and releases the stage on its `empty` barrier.
 // Waits are bounded; a give-up sets DS_ERR_TIMEOUT in the status word and an abort flag
 // that every role checks before its next wait; the group that issued MMAs waits once more
 // (bounded) for them before TMEM is freed.
@@ -838,8 +842,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
       sm100::tc_fence_before();   // the group barrier of the next tile orders the next MMA
       const int e = e0 + row;
       if (e < ucnt) {
-        // row r's tensor-core score; its interval comes from kn and the row's norm bound
-        // (tc_interval) wherever it is used
+        // row r's tensor-core score; its interval comes from kn and the row's scale
+        // (tc_lo / tc_hi) wherever it is used
         a.knorm[(size_t)l * a.NS + e] = kn;
         auto emit = [&](int r, float sc) {
           const size_t out = ((size_t)l * R + r) * a.NS + e;
