@@ -212,3 +212,12 @@ def test_mixed_density_and_empty_layers(dsm, canonical):
     inp["limit"] = torch.from_numpy(limit)
     dev, _ = check(dsm, inp, shape.topk, canonical=canonical)
     assert np.all(dev[1][1] == 0)
+
+
+@pytest.mark.parametrize("canonical", [False, True])
+def test_twelve_heads_odd_block_count(dsm, canonical):
+    # Hh = 12 (the generic scoring and re-score paths), 3 rows, an odd block count (score
+    # rows padded to a multiple of 4, the last collection group ragged) and K = 300
+    shape = synth.SelectShape(L=2, R=3, Hh=12, N=12345, topk=300)
+    inp = synth.select_inputs(shape, seed=21)
+    check(dsm, inp, shape.topk, canonical=canonical)
