@@ -58,6 +58,10 @@ def lib() -> C.CDLL:
         L.orc_select.argtypes = [C.c_int32] * 6 + [P, C.c_int64, P, P, P, P, C.c_int32,
                                                    C.c_int32, P, P, P, P, P]
         L.orc_select.restype = None
+        L.orc_verify_greedy.argtypes = [P, C.c_int32, C.c_int32, P, P]
+        L.orc_verify_greedy.restype = C.c_int32
+        L.orc_verify_sample.argtypes = [P, C.c_int32, C.c_int32, C.c_double, P, P, P, P, P]
+        L.orc_verify_sample.restype = C.c_int32
         L.orc_committed_tokens.argtypes = [P, C.c_int32]
         L.orc_committed_tokens.restype = C.c_int32
         _lib = L
@@ -230,3 +234,33 @@ def select(keys: np.ndarray, q: np.ndarray, hw: np.ndarray, mask: np.ndarray, li
 def committed_tokens(accepted: np.ndarray, R: int) -> int:
     a = np.ascontiguousarray(accepted, dtype=np.uint8)
     return int(lib().orc_committed_tokens(_p(a), R))
+
+
+def verify_greedy(logits: np.ndarray, draft: np.ndarray) -> np.ndarray:
+    """Tokens emitted by one greedy verify step: logits fp32 [R][V], draft int32 [R-1]."""
+    z = np.ascontiguousarray(logits, dtype=np.float32)
+    R, V = z.shape
+    d = np.ascontiguousarray(draft, dtype=np.int32).reshape(-1)
+    assert d.size == R - 1
+    out = np.zeros(R, dtype=np.int32)
+    n = lib().orc_verify_greedy(_p(z), R, V, _p(d) if d.size else None, _p(out))
+    return out[:n]
+
+
+def verify_sample(logits: np.ndarray, T: float, qd: np.ndarray, draft: np.ndarray,
+                  u_acc: np.ndarray, u_res: np.ndarray) -> np.ndarray:
+    """Tokens emitted by one verify step with exact speculative sampling at temperature T:
+    logits fp32 [R][V], qd fp64 [R-1][V] (the drafter's distributions), draft int32 [R-1],
+    u_acc fp64 [R-1], u_res fp64 [R] (uniforms in [0, 1))."""
+    z = np.ascontiguousarray(logits, dtype=np.float32)
+    R, V = z.shape
+    q = np.ascontiguousarray(qd, dtype=np.float64).reshape(max(R - 1, 0), V)
+    d = np.ascontiguousarray(draft, dtype=np.int32).reshape(-1)
+    ua = np.ascontiguousarray(u_acc, dtype=np.float64).reshape(-1)
+    ur = np.ascontiguousarray(u_res, dtype=np.float64).reshape(-1)
+    assert d.size == R - 1 and ua.size == R - 1 and ur.size == R
+    out = np.zeros(R, dtype=np.int32)
+    n = lib().orc_verify_sample(_p(z), R, V, float(T), _p(q) if q.size else None,
+                                _p(d) if d.size else None, _p(ua) if ua.size else None,
+                                _p(ur), _p(out))
+    return out[:n]

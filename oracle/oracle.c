@@ -18,6 +18,10 @@
  *   orc_select        paragraph "Decode at depth": score admitted blocks only,
  *                     compact the admitted index per row, take the top 512 by
  *                     (score desc, index asc); canonical fp32 score order.
+ *   orc_verify_greedy / orc_verify_sample
+ *                     paragraph "DSpark" (a 6-row verify per decode step; identical
+ *                     output under greedy decode; exact speculative sampling at
+ *                     temperature > 0): accepted drafts, then one target token.
  * Readings where the pages are silent are stated beside the code that takes them.
  */
 #include <math.h>
@@ -384,4 +388,99 @@ int32_t orc_committed_tokens(const uint8_t* accepted, int32_t R) {
     ++c;
   }
   return c;
+}
+
+/* ------------------------------------------------------------ verify acceptance ---- */
+
+/* Paragraph "DSpark": a decode step verifies R rows (the last committed token and R - 1
+ * drafted tokens) in one pass; under greedy decode the output is the same as without
+ * drafts, and at temperature > 0 the drafts are accepted by exact speculative sampling.
+ * Readings: row r's target logits (fp32 [R][V]) predict the token after row r's input;
+ * draft token j (draft[j], j = 0..R-2) is the input of row j + 1, so it is checked against
+ * row j's prediction. Both functions write the emitted tokens to out (at most R) and
+ * return how many: the accepted drafts, then one token from the target (the correction at
+ * the first rejection, or the bonus token after the last row). */
+
+/* Greedy: a draft is accepted iff it equals the argmax of its row (ties to the lower id). */
+int32_t orc_verify_greedy(const float* logits, int32_t R, int32_t V, const int32_t* draft,
+                          int32_t* out) {
+  int32_t n = 0;
+  for (int32_t r = 0; r < R; ++r) {
+    const float* z = logits + (int64_t)r * V;
+    int32_t best = 0;
+    for (int32_t v = 1; v < V; ++v)
+      if (z[v] > z[best]) best = v;
+    out[n++] = best;
+    if (r == R - 1 || draft[r] != best) break;
+  }
+  return n;
+}
+
+/* The smallest x with u * sum(w) < w[0] + ... + w[x] (sums in index order, fp64); when
+ * rounding leaves none, the last x with w[x] > 0. u in [0, 1). */
+static int32_t sample_weights(const double* w, int32_t V, double u) {
+  double total = 0.0;
+  int32_t last = 0;
+  for (int32_t v = 0; v < V; ++v) {
+    total += w[v];
+    if (w[v] > 0.0) last = v;
+  }
+  const double target = u * total;
+  double acc = 0.0;
+  for (int32_t v = 0; v < V; ++v) {
+    acc += w[v];
+    if (target < acc) return v;
+  }
+  return last;
+}
+
+/* p = softmax(z / T) in fp64: exp(z / T - max z / T) over the row, divided by their sum in
+ * index order. */
+static void softmax_t(const float* z, int32_t V, double T, double* p) {
+  double m = (double)z[0] / T;
+  for (int32_t v = 1; v < V; ++v)
+    if ((double)z[v] / T > m) m = (double)z[v] / T;
+  double s = 0.0;
+  for (int32_t v = 0; v < V; ++v) {
+    p[v] = exp((double)z[v] / T - m);
+    s += p[v];
+  }
+  for (int32_t v = 0; v < V; ++v) p[v] /= s;
+}
+
+/* Exact speculative sampling at temperature T > 0. The drafter's proposal distributions
+ * qd (fp64 [R-1][V], rows summing to 1) and the uniforms in [0, 1) are inputs. Row r's
+ * draft d = draft[r] is accepted iff u_acc[r] * qd_r[d] < p_r[d] (probability
+ * min(1, p_r[d] / qd_r[d])); at the first rejection the correction is drawn from the
+ * residual max(p_r - qd_r, 0) with u_res[r] (from p_r if rounding leaves the residual
+ * empty); after R - 1 acceptances the bonus token is drawn from p_{R-1} with u_res[R-1]. */
+int32_t orc_verify_sample(const float* logits, int32_t R, int32_t V, double T, const double* qd,
+                          const int32_t* draft, const double* u_acc, const double* u_res,
+                          int32_t* out) {
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  double* res = (double*)malloc(sizeof(double) * (size_t)V);
+  int32_t n = 0;
+  for (int32_t r = 0; r < R; ++r) {
+    softmax_t(logits + (int64_t)r * V, V, T, p);
+    if (r == R - 1) {
+      out[n++] = sample_weights(p, V, u_res[r]);
+      break;
+    }
+    const double* q = qd + (int64_t)r * V;
+    const int32_t d = draft[r];
+    if (u_acc[r] * q[d] < p[d]) {
+      out[n++] = d;
+      continue;
+    }
+    double rs = 0.0;
+    for (int32_t v = 0; v < V; ++v) {
+      res[v] = p[v] > q[v] ? p[v] - q[v] : 0.0;
+      rs += res[v];
+    }
+    out[n++] = sample_weights(rs > 0.0 ? res : p, V, u_res[r]);
+    break;
+  }
+  free(p);
+  free(res);
+  return n;
 }

@@ -4,7 +4,10 @@ Each pin would fail under a plausible mistake in the oracle: a wrong nibble orde
 offset (Q4 golden blocks, one-hot columns), a double rounding or wrong tie rule (bf16
 golden cases, torch's converter), a transposed operand or dropped term (dequantise-then-
 numpy-matmul layer check), a wrong selection order or tie-break (full sorts, all-equal
-scores), a wrong summation order in the block score (hand-worked fp32 cases).
+scores), a wrong summation order in the block score (hand-worked fp32 cases), a wrong
+acceptance rule or residual in the verify step (the acceptance probability min(1, p/q) and
+the first emitted token's distribution equal to the target's, both in closed form over a
+stratified grid of the uniforms; the inverse CDF against scipy's softmax; the greedy limit).
 """
 import json
 import math
@@ -426,3 +429,91 @@ def test_committed_tokens_bernoulli_mean_closed_form(a, R):
     acc = synth.draft_acceptance(20000, R, a, seed=0)
     mean = np.mean([oracle.committed_tokens(acc[t], R) for t in range(acc.shape[0])])
     assert mean == pytest.approx((1 - a ** R) / (1 - a), rel=0.01)
+
+
+# --------------------------------------------------------------- verify acceptance --
+
+
+def test_verify_greedy_hand_cases():
+    z = np.array([[0.0, 3.0, 1.0], [5.0, 0.0, 0.0], [0.0, 0.0, 9.0]], np.float32)
+    # every draft equals its row's argmax: both accepted, then the bonus token of row 2
+    assert oracle.verify_greedy(z, np.array([1, 0])).tolist() == [1, 0, 2]
+    # the first draft is wrong: nothing accepted, the correction is row 0's argmax
+    assert oracle.verify_greedy(z, np.array([2, 0])).tolist() == [1]
+    # the second draft is wrong: one accepted, then row 1's argmax
+    assert oracle.verify_greedy(z, np.array([1, 2])).tolist() == [1, 0]
+    # a single row (no drafts): its argmax
+    assert oracle.verify_greedy(z[:1], np.zeros(0, np.int32)).tolist() == [1]
+
+
+def test_verify_greedy_tie_goes_to_lower_id():
+    z = np.array([[1.0, 7.0, 7.0, 2.0], [0.0, 0.0, 0.0, 4.0]], np.float32)
+    assert oracle.verify_greedy(z, np.array([1])).tolist() == [1, 3]
+    assert oracle.verify_greedy(z, np.array([2])).tolist() == [1]
+
+
+def _grid(G):
+    return (np.arange(G) + 0.5) / G   # stratified midpoints of [0, 1)
+
+
+def _softmax64(z, T):
+    from scipy.special import softmax
+    return softmax(np.asarray(z, np.float64) / T)
+
+
+def test_verify_sample_acceptance_probability_closed_form():
+    # one draft d: the fraction of u_acc values that accept it is min(1, p[d] / q[d])
+    z = np.array([[0.3, -1.0, 2.0, 0.5, 0.0], [0.0, 0.0, 0.0, 0.0, 0.0]], np.float32)
+    T = 0.8
+    p = _softmax64(z[0], T)
+    q = np.array([0.05, 0.4, 0.2, 0.3, 0.05])
+    G = 2000
+    for d in range(5):
+        acc = sum(int(oracle.verify_sample(z, T, q[None], np.array([d]), np.array([u]),
+                                           np.array([0.5, 0.5])).size == 2)
+                  for u in _grid(G))
+        assert acc / G == pytest.approx(min(1.0, p[d] / q[d]), abs=1.0 / G)
+
+
+def test_verify_sample_first_token_follows_target_exactly():
+    # exact speculative sampling: with the draft drawn from q, the first emitted token is
+    # distributed as p whatever q is (accepted draft, or the residual's correction)
+    z = np.array([[0.3, -1.0, 2.0, 0.5, 0.0], [1.0, 0.0, 0.0, 0.0, 0.0]], np.float32)
+    T = 0.8
+    p = _softmax64(z[0], T)
+    q = np.array([0.05, 0.4, 0.2, 0.3, 0.05])
+    G = 300
+    dist = np.zeros(5)
+    for d in range(5):
+        for ua in _grid(G):
+            for ur in _grid(G):
+                tok = oracle.verify_sample(z, T, q[None], np.array([d]), np.array([ua]),
+                                           np.array([ur, 0.5]))[0]
+                dist[tok] += q[d] / (G * G)
+    assert np.allclose(dist, p, atol=4.0 / G)
+
+
+@pytest.mark.parametrize("u", [0.0, 0.1, 0.37, 0.5, 0.81, 0.999])
+def test_verify_sample_bonus_token_is_the_softmax_inverse_cdf(u):
+    # a single row: the token drawn with u is the first whose cumulative softmax exceeds u
+    z = np.array([[0.2, 1.5, -0.3, 0.9, 0.0, 2.2]], np.float32)
+    T = 1.3
+    cdf = np.cumsum(_softmax64(z[0], T))
+    want = int(np.searchsorted(cdf, u, side="right"))
+    got = oracle.verify_sample(z, T, np.zeros((0, 6)), np.zeros(0, np.int32), np.zeros(0),
+                               np.array([u]))
+    assert got.tolist() == [want]
+
+
+def test_verify_sample_low_temperature_is_greedy():
+    # as T -> 0 the target rows become one-hot at their argmax; with one-hot drafter
+    # distributions on the drafted tokens the sampled step equals the greedy one
+    rng = np.random.default_rng(3)
+    R, V = 6, 50
+    z = rng.normal(size=(R, V)).astype(np.float32) * 4
+    best = np.argmax(z, axis=1)
+    for draft in (best[:-1].copy(), np.array([best[0], best[1], (best[2] + 1) % V, 0, 0])):
+        q = np.zeros((R - 1, V))
+        q[np.arange(R - 1), draft] = 1.0
+        got = oracle.verify_sample(z, 1e-3, q, draft, np.full(R - 1, 0.5), np.full(R, 0.5))
+        assert got.tolist() == oracle.verify_greedy(z, draft).tolist()
