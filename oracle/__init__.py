@@ -58,6 +58,10 @@ def lib() -> C.CDLL:
         L.orc_select.argtypes = [C.c_int32] * 6 + [P, C.c_int64, P, P, P, P, C.c_int32,
                                                    C.c_int32, P, P, P, P, P]
         L.orc_select.restype = None
+        L.orc_q8_value.argtypes = [P, P, C.c_int64, C.c_int64, C.c_int64]
+        L.orc_q8_value.restype = C.c_double
+        L.orc_q8_project.argtypes = [P, P, C.c_int64, C.c_int64, P, C.c_int32, P, P]
+        L.orc_q8_project.restype = None
         L.orc_verify_greedy.argtypes = [P, C.c_int32, C.c_int32, P, P]
         L.orc_verify_greedy.restype = C.c_int32
         L.orc_verify_sample.argtypes = [P, C.c_int32, C.c_int32, C.c_double, P, P, P, P, P]
@@ -264,3 +268,23 @@ def verify_sample(logits: np.ndarray, T: float, qd: np.ndarray, draft: np.ndarra
                                 _p(d) if d.size else None, _p(ua) if ua.size else None,
                                 _p(ur), _p(out))
     return out[:n]
+
+
+def q8_value(qs: np.ndarray, sc: np.ndarray, K: int, row: int, k: int) -> float:
+    q = np.ascontiguousarray(qs, dtype=np.int8)
+    s = _u16(sc)
+    return float(lib().orc_q8_value(_p(q), _p(s), K, row, k))
+
+
+def q8_project(qs: np.ndarray, sc: np.ndarray, x: np.ndarray):
+    """R rows through one Q8 matrix: qs int8 [rows][K], sc fp16 bits [rows][K/32], x bf16
+    bits [R][K] -> (y fp64 [R][rows], y rounded to bf16 bits [R][rows])."""
+    q = np.ascontiguousarray(qs, dtype=np.int8)
+    s = _u16(sc)
+    xb = _u16(x)
+    rows, K = q.shape
+    R = xb.shape[0]
+    y = np.zeros((R, rows), np.float64)
+    yb = np.zeros((R, rows), np.uint16)
+    lib().orc_q8_project(_p(q), _p(s), rows, K, _p(xb), R, _p(y), _p(yb))
+    return y, yb

@@ -18,6 +18,8 @@
  *   orc_select        paragraph "Decode at depth": score admitted blocks only,
  *                     compact the admitted index per row, take the top 512 by
  *                     (score desc, index asc); canonical fp32 score order.
+ *   orc_q8_project    paragraph "DSpark" (paired Q8 projections shared by the verify
+ *                     rows): dequantise, then fp64 products; one bf16 rounding.
  *   orc_verify_greedy / orc_verify_sample
  *                     paragraph "DSpark" (a 6-row verify per decode step; identical
  *                     output under greedy decode; exact speculative sampling at
@@ -86,6 +88,35 @@ double orc_q4_value(const uint8_t* qs, const uint16_t* sc, int64_t K, int64_t ro
   int q = nib - 8;
   double s = orc_f16_to_f64(sc[row * (K / 32) + k / 32]);
   return s * (double)q;
+}
+
+/* ------------------------------------------------------------------- Q8 weights ----- */
+
+/* Paragraph "DSpark": the verify rows share one weight stream through paired Q8
+ * projections. Reading: blocks of 32 signed 8-bit values (two's complement) along K with
+ * one fp16 scale per block, value = scale * q; planar, qs int8 [rows][K] and sc fp16
+ * [rows][K/32]. Returns value k of row `row` in fp64. */
+double orc_q8_value(const int8_t* qs, const uint16_t* sc, int64_t K, int64_t row, int64_t k) {
+  double s = orc_f16_to_f64(sc[row * (K / 32) + k / 32]);
+  return s * (double)qs[row * K + k];
+}
+
+/* The R verify rows through one Q8 projection: y[r][i] = sum_k W[i][k] * x[r][k] in fp64
+ * (x bf16 [R][K], W the dequantised [rows][K]), and, when ybf is non-NULL, y rounded once
+ * to bf16 (round to nearest, ties to even). */
+void orc_q8_project(const int8_t* qs, const uint16_t* sc, int64_t rows, int64_t K,
+                    const uint16_t* x, int32_t R, double* y, uint16_t* ybf) {
+  double* xr = (double*)malloc(sizeof(double) * (size_t)K);
+  for (int32_t r = 0; r < R; ++r) {
+    for (int64_t k = 0; k < K; ++k) xr[k] = orc_bf16_to_f64(x[(int64_t)r * K + k]);
+    for (int64_t i = 0; i < rows; ++i) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k) acc += orc_q8_value(qs, sc, K, i, k) * xr[k];
+      y[(int64_t)r * rows + i] = acc;
+      if (ybf) ybf[(int64_t)r * rows + i] = orc_bf16_rne(acc);
+    }
+  }
+  free(xr);
 }
 
 /* y[i] = sum_k W[i][k] * x[k] for the dequantised Q4 matrix W [rows][K], fp64.

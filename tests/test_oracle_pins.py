@@ -5,6 +5,7 @@ offset (Q4 golden blocks, one-hot columns), a double rounding or wrong tie rule 
 golden cases, torch's converter), a transposed operand or dropped term (dequantise-then-
 numpy-matmul layer check), a wrong selection order or tie-break (full sorts, all-equal
 scores), a wrong summation order in the block score (hand-worked fp32 cases), a wrong
+byte order or sign in Q8 values (hand-worked blocks, one-hot columns), a wrong
 acceptance rule or residual in the verify step (the acceptance probability min(1, p/q) and
 the first emitted token's distribution equal to the target's, both in closed form over a
 stratified grid of the uniforms; the inverse CDF against scipy's softmax; the greedy limit).
@@ -96,6 +97,58 @@ def test_q4_golden_blocks(golden_dir):
             assert oracle.q4_value(qs, sc, 32, 0, k) == blk["scale"] * blk["q"][k]
         # the numpy helper used by the other pins agrees with the hand-worked values too
         assert np.array_equal(np_dequant(qs, sc)[0], blk["scale"] * np.array(blk["q"]))
+
+
+# ---------------------------------------------------------------------- Q8 weights ----
+
+
+def np_dequant_q8(qs: np.ndarray, sc: np.ndarray) -> np.ndarray:
+    """Independent numpy dequantisation of a Q8 matrix: int8 [rows, K] and fp16-bit scales
+    [rows, K/32] -> fp64 [rows, K]."""
+    s = sc.view(np.float16).astype(np.float64)
+    return qs.astype(np.float64) * np.repeat(s, 32, axis=-1)
+
+
+def test_q8_golden_blocks(golden_dir):
+    d = json.loads((golden_dir / "q8_block.json").read_text())
+    for blk in d["blocks"]:
+        qs = np.frombuffer(bytes.fromhex(blk["bytes_hex"]), dtype=np.int8).reshape(1, 32)
+        sc = np.array([[int(blk["scale_f16_hex"], 16)]], dtype=np.uint16)
+        for k in range(32):
+            assert oracle.q8_value(qs, sc, 32, 0, k) == blk["scale"] * blk["q"][k]
+        assert np.array_equal(np_dequant_q8(qs, sc)[0], blk["scale"] * np.array(blk["q"]))
+
+
+def _q8_case(rows, K, R, seed):
+    rng = np.random.default_rng(seed)
+    qs = rng.integers(-128, 128, size=(rows, K), dtype=np.int64).astype(np.int8)
+    sc = (rng.uniform(0.5, 2.0, size=(rows, K // 32)) * 2.0 ** -7).astype(np.float16).view(np.uint16)
+    x = torch.randn(R, K).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return qs, sc, x
+
+
+def test_q8_project_onehot_gives_the_column():
+    qs, sc, _ = _q8_case(40, 96, 1, seed=5)
+    W = np_dequant_q8(qs, sc)
+    for k in (0, 31, 32, 95):
+        x = np.zeros((1, 96), np.uint16)
+        x[0, k] = 0x3F80   # bf16 1.0
+        y, _ = oracle.q8_project(qs, sc, x)
+        assert np.array_equal(y[0], W[:, k])
+
+
+def test_q8_project_against_numpy_and_row_pairing():
+    qs, sc, x = _q8_case(72, 256, 6, seed=6)
+    y, yb = oracle.q8_project(qs, sc, x)
+    ref = bf16_to_np(x) @ np_dequant_q8(qs, sc).T
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+    # one bf16 rounding of the fp64 value (torch's converter rounds to nearest even)
+    want = torch.from_numpy(y).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(yb, want)
+    # the rows share the weights but not their results: each row alone gives the same
+    for r in range(6):
+        y1, yb1 = oracle.q8_project(qs, sc, x[r:r + 1])
+        assert np.array_equal(y1[0], y[r]) and np.array_equal(yb1[0], yb[r])
 
 
 # ------------------------------------------------------------------------- router ----
