@@ -74,10 +74,11 @@ typedef struct {
 
 /* One MoE layer: E routed experts + 1 shared expert, each with gate and up [I][H] and
  * down [H][I], and a bf16 router [E][H].
- * Limits of this build: H and I multiples of 64, 64 <= H <= 16384, 64 <= I <= 8192,
- * 1 <= top_k <= 16, top_k <= E <= 1024; the R verify rows are staged in shared memory,
- * R * (2H + 64) bytes, which must fit beside the weight stages (e.g. H <= 10880 at
- * R = 6; otherwise DS_ERR_UNSUPPORTED). */
+ * Limits: H and I multiples of 32, 64 <= H <= 16384, 64 <= I <= 8192, 1 <= top_k <= 16,
+ * top_k <= E <= 1024 (else DS_ERR_INVALID_ARG). This build's kernels also need H and I
+ * to be multiples of 64, and stage the R verify rows in shared memory, R * (2H + 64)
+ * bytes beside the weight stages (e.g. H <= 10880 at R = 6); other valid layers get
+ * DS_ERR_UNSUPPORTED. */
 typedef struct {
   int32_t hidden;      /* H                                                   */
   int32_t n_experts;   /* E (routed)                                          */
@@ -89,7 +90,9 @@ typedef struct {
 } ds_moe_layer;
 
 /* Bytes of workspace ds_moe_verify_forward needs for this layer and R rows, or 0 when
- * the layer or R is invalid. The workspace must be 256-byte aligned. */
+ * the call would refuse the layer's sizes or R (DS_ERR_INVALID_ARG or
+ * DS_ERR_UNSUPPORTED). Host-only: pointers and the device's shared-memory capacity are
+ * not examined. The workspace must be 256-byte aligned. */
 size_t ds_moe_workspace_size(const ds_moe_layer* layer, int32_t R);
 
 /* One speculative-verify step of one MoE layer for R = 1..6 rows (the pages' 6-row
@@ -111,8 +114,8 @@ size_t ds_moe_workspace_size(const ds_moe_layer* layer, int32_t R);
  *   workspace: >= ds_moe_workspace_size bytes, 256-byte aligned; its contents on entry
  *              are ignored and it must not be used by another call in flight.
  * Errors: DS_ERR_INVALID_ARG (null pointer, R outside 1..6, sizes outside the limits,
- * misaligned qs/sc/x/y), DS_ERR_WORKSPACE, DS_ERR_UNSUPPORTED (R * H too large for the
- * shared-memory staging), DS_ERR_CUDA. */
+ * misaligned qs/sc/x/y), DS_ERR_WORKSPACE, DS_ERR_UNSUPPORTED (H or I not a multiple of
+ * 64, or R * H too large for the shared-memory staging), DS_ERR_CUDA. */
 ds_status ds_moe_verify_forward(const ds_moe_layer* layer, const uint16_t* x, int32_t R,
                                 uint16_t* y, int32_t* topk_idx, float* topk_w,
                                 void* workspace, size_t ws_bytes, ds_stream_t stream);
@@ -155,12 +158,22 @@ size_t ds_moe_workspace_h_offset(const ds_moe_layer* layer, int32_t R);
  * that must start at zero, so a previous call's leftovers do not matter.
  * Arguments, layouts and results as ds_moe_verify_forward; every output buffer is the
  * caller's. Errors: DS_ERR_WORKSPACE, decided on the host before any CUDA call, when
- * ds_moe_workspace_size(layer, R) > DS_NOALLOC_SCRATCH_BYTES; DS_ERR_INVALID_ARG when
- * that size is 0 (invalid layer or R); DS_ERR_CUDA when the array's address cannot be
- * resolved; otherwise those of ds_moe_verify_forward. */
+ * ds_moe_workspace_size(layer, R) > DS_NOALLOC_SCRATCH_BYTES; when that size is 0, the
+ * status ds_moe_verify_forward gives the layer (DS_ERR_INVALID_ARG or DS_ERR_UNSUPPORTED); DS_ERR_CUDA when the array's address cannot be
+ * resolved; otherwise those of ds_moe_verify_forward. The device-side outcomes
+ * (DS_ERR_TIMEOUT, DS_ERR_DEVICE_CHECK) are read with ds_noalloc_status().
+ * The array's address is resolved once per device and kept for the life of the process;
+ * a cudaDeviceReset() invalidates it, so the call must not be used after a reset. */
 ds_status ds_moe_verify_forward_noalloc(const ds_moe_layer* layer, const uint16_t* x,
                                         int32_t R, uint16_t* y, int32_t* topk_idx,
                                         float* topk_w, ds_stream_t stream);
+
+/* Synchronises `stream`, then reads the status word that the kernels of the last
+ * ds_moe_verify_forward_noalloc call on the current device left at the start of its
+ * scratch array: DS_OK, DS_ERR_TIMEOUT or DS_ERR_DEVICE_CHECK, as ds_workspace_status()
+ * reports them for a caller workspace. DS_ERR_CUDA when the synchronise, the copy or the
+ * address lookup fails. Allocates nothing. */
+ds_status ds_noalloc_status(ds_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * Block selection for compressed sparse attention (the pages' paragraph "Decode at

@@ -256,6 +256,8 @@ def verify_sample(logits: np.ndarray, T: float, qd: np.ndarray, draft: np.ndarra
     """Tokens emitted by one verify step with exact speculative sampling at temperature T:
     logits fp32 [R][V], qd fp64 [R-1][V] (the drafter's distributions), draft int32 [R-1],
     u_acc fp64 [R-1], u_res fp64 [R] (uniforms in [0, 1))."""
+    if not (np.isfinite(T) and T > 0):
+        raise ValueError(f"temperature must be finite and > 0 (got {T})")
     z = np.ascontiguousarray(logits, dtype=np.float32)
     R, V = z.shape
     q = np.ascontiguousarray(qd, dtype=np.float64).reshape(max(R - 1, 0), V)
@@ -267,6 +269,8 @@ def verify_sample(logits: np.ndarray, T: float, qd: np.ndarray, draft: np.ndarra
     n = lib().orc_verify_sample(_p(z), R, V, float(T), _p(q) if q.size else None,
                                 _p(d) if d.size else None, _p(ua) if ua.size else None,
                                 _p(ur), _p(out))
+    if n < 0:
+        raise ValueError(f"orc_verify_sample refused temperature {T}")
     return out[:n]
 
 

@@ -484,10 +484,12 @@ static void softmax_t(const float* z, int32_t V, double T, double* p) {
  * draft d = draft[r] is accepted iff u_acc[r] * qd_r[d] < p_r[d] (probability
  * min(1, p_r[d] / qd_r[d])); at the first rejection the correction is drawn from the
  * residual max(p_r - qd_r, 0) with u_res[r] (from p_r if rounding leaves the residual
- * empty); after R - 1 acceptances the bonus token is drawn from p_{R-1} with u_res[R-1]. */
+ * empty); after R - 1 acceptances the bonus token is drawn from p_{R-1} with u_res[R-1].
+ * Returns -1 (nothing written) when T is not a finite positive number. */
 int32_t orc_verify_sample(const float* logits, int32_t R, int32_t V, double T, const double* qd,
                           const int32_t* draft, const double* u_acc, const double* u_res,
                           int32_t* out) {
+  if (!(T > 0.0) || !isfinite(T)) return -1;   /* softmax(z / T) needs a finite T > 0 */
   double* p = (double*)malloc(sizeof(double) * (size_t)V);
   double* res = (double*)malloc(sizeof(double) * (size_t)V);
   int32_t n = 0;

@@ -221,6 +221,12 @@ def moe_workspace_h(layer: MoeLayer, R: int, workspace: torch.Tensor) -> torch.T
     return workspace[off: off + 2 * n].view(torch.bfloat16).view(R, 1 + layer.top_k, layer.inter)
 
 
+def noalloc_status(stream=None) -> int:
+    """Synchronises the stream and returns the device status code that the last
+    moe_verify_forward_noalloc call on the current device left in the library's scratch."""
+    return int(N.load().ds_noalloc_status(_stream(stream)))
+
+
 def workspace_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronises the stream and returns the device status code left in the workspace."""
     return int(N.load().ds_workspace_status(_ptr(workspace), _stream(stream)))

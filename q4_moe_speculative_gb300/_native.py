@@ -21,7 +21,7 @@ EXPORTS = (
     "ds_moe_workspace_size", "ds_moe_verify_forward", "ds_select_workspace_size",
     "ds_select_blocks", "ds_workspace_status", "ds_status_string", "ds_version",
     "ds_moe_verify_forward_marked", "ds_select_blocks_marked", "ds_moe_workspace_h_offset",
-    "ds_moe_verify_forward_noalloc",
+    "ds_moe_verify_forward_noalloc", "ds_noalloc_status",
 )
 
 DS_SELECT_CANONICAL_SCORES = 1
@@ -84,6 +84,8 @@ def load() -> C.CDLL:
         C.POINTER(DsMoeLayer), C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
         C.c_void_p]
     lib.ds_moe_verify_forward_noalloc.restype = C.c_int
+    lib.ds_noalloc_status.argtypes = [C.c_void_p]
+    lib.ds_noalloc_status.restype = C.c_int
     lib.ds_select_workspace_size.argtypes = [C.POINTER(DsSelectArgs)]
     lib.ds_select_workspace_size.restype = C.c_size_t
     lib.ds_select_blocks.argtypes = [

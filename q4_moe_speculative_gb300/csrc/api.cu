@@ -44,13 +44,23 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 bool q4_ok(const ds_q4& w) { return w.qs && w.sc && aligned(w.qs, 16) && aligned(w.sc, 4); }
 
-ds_status check_layer(const ds_moe_layer* L, int32_t R) {
+// Sizes only (no pointers): DS_ERR_INVALID_ARG outside the format's limits (H and I
+// multiples of 32, ranges, k, E, R), DS_ERR_UNSUPPORTED for valid sizes this build's
+// kernels do not run (H or I not a multiple of 64).
+ds_status check_layer_sizes(const ds_moe_layer* L, int32_t R) {
   if (!L) return DS_ERR_INVALID_ARG;
   if (R < 1 || R > kMaxRows) return DS_ERR_INVALID_ARG;
-  if (L->hidden < 64 || L->hidden > 16384 || L->hidden % 64) return DS_ERR_INVALID_ARG;
-  if (L->inter < 64 || L->inter > 8192 || L->inter % 64) return DS_ERR_INVALID_ARG;
+  if (L->hidden < 64 || L->hidden > 16384 || L->hidden % 32) return DS_ERR_INVALID_ARG;
+  if (L->inter < 64 || L->inter > 8192 || L->inter % 32) return DS_ERR_INVALID_ARG;
   if (L->top_k < 1 || L->top_k > kMaxTopK) return DS_ERR_INVALID_ARG;
   if (L->n_experts < L->top_k || L->n_experts > kMaxExperts) return DS_ERR_INVALID_ARG;
+  if (L->hidden % 64 || L->inter % 64) return DS_ERR_UNSUPPORTED;
+  return DS_OK;
+}
+
+ds_status check_layer(const ds_moe_layer* L, int32_t R) {
+  const ds_status st = check_layer_sizes(L, R);
+  if (st != DS_OK) return st;
   if (!L->router_w || !aligned(L->router_w, 16)) return DS_ERR_INVALID_ARG;
   if (!q4_ok(L->gate) || !q4_ok(L->up) || !q4_ok(L->down) || !q4_ok(L->sh_gate) ||
       !q4_ok(L->sh_up) || !q4_ok(L->sh_down))
@@ -93,10 +103,7 @@ SelDims sdims_of(const ds_select_args* a) {
 extern "C" {
 
 size_t ds_moe_workspace_size(const ds_moe_layer* layer, int32_t R) {
-  if (!layer || R < 1 || R > kMaxRows || layer->hidden < 64 || layer->inter < 64 ||
-      layer->top_k < 1 || layer->top_k > kMaxTopK || layer->n_experts < layer->top_k ||
-      layer->n_experts > kMaxExperts)
-    return 0;
+  if (check_layer_sizes(layer, R) != DS_OK) return 0;
   return moe_layout(dims_of(layer, R)).total;
 }
 

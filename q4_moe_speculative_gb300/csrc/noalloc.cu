@@ -14,7 +14,11 @@
 // Every call on a device shares the one array: calls whose work overlaps on the GPU (two
 // streams, or two host threads) race on it and give wrong results. The launch sequence
 // clears, on the call's stream, every word of the scratch that must start at zero, so what
-// an earlier call left there does not matter.
+// an earlier call left there does not matter. The kernels report a bounded wait that gave
+// up, or a failed device check, in a status word at the start of the array;
+// ds_noalloc_status() reads it. The resolved address is kept for the life of the process:
+// a cudaDeviceReset() destroys the context that owns the array, after which this call must
+// not be used again in the process.
 #include <atomic>
 #include <mutex>
 
@@ -59,11 +63,19 @@ extern "C" ds_status ds_moe_verify_forward_noalloc(const ds_moe_layer* layer,
   // Host-only size check first: a layer that needs more scratch than the array holds is
   // refused before any CUDA call.
   const size_t need = ds_moe_workspace_size(layer, R);
-  if (need == 0) return DS_ERR_INVALID_ARG;
+  if (need == 0)   // sizes the call refuses: its own host check gives the status, no CUDA call
+    return ds_moe_verify_forward(layer, x, R, y, topk_idx, topk_w, nullptr, 0, stream);
   if (need > (size_t)DS_NOALLOC_SCRATCH_BYTES) return DS_ERR_WORKSPACE;
   void* scratch = nullptr;
   const ds_status st = scratch_of_current_device(&scratch);
   if (st != DS_OK) return st;
   return ds_moe_verify_forward(layer, x, R, y, topk_idx, topk_w, scratch,
                                (size_t)DS_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" ds_status ds_noalloc_status(ds_stream_t stream) {
+  void* scratch = nullptr;
+  const ds_status st = scratch_of_current_device(&scratch);
+  if (st != DS_OK) return st;
+  return ds_workspace_status(scratch, stream);
 }

@@ -63,6 +63,9 @@ def test_moe_workspace_size_host_only(lib):
     assert s6 >= 6 * 9 * 1024 * 2 + 6 * 9 * 4096 * 4
     assert lib.ds_moe_workspace_size(st, 0) == 0
     assert lib.ds_moe_workspace_size(st, 7) == 0
+    # sizes the call refuses (invalid, or valid but not run by this build) get no size
+    assert lib.ds_moe_workspace_size(fake_layer(I=1056), 6) == 0
+    assert lib.ds_moe_workspace_size(fake_layer(H=4010), 6) == 0
 
 
 @pytest.mark.parametrize("mutate,R,expect", [
@@ -70,7 +73,8 @@ def test_moe_workspace_size_host_only(lib):
     (lambda s: None, 7, 1),
     (lambda s: setattr(s, "hidden", 4010), 6, 1),        # not a multiple of 32
     (lambda s: setattr(s, "inter", 1000), 6, 1),
-    (lambda s: setattr(s, "inter", 1056), 6, 1),         # multiple of 32, not of 64
+    (lambda s: setattr(s, "inter", 1056), 6, 2),         # multiple of 32, not of 64
+    (lambda s: setattr(s, "hidden", 4064), 6, 2),
     (lambda s: setattr(s.up, "sc", FAKE + 2), 6, 1),     # scales not 4-byte aligned
     (lambda s: setattr(s, "top_k", 0), 6, 1),
     (lambda s: setattr(s, "top_k", 17), 6, 1),
@@ -157,4 +161,13 @@ def test_noalloc_rejects_on_the_host(lib):
     assert lib.ds_moe_verify_forward_noalloc(big, FAKE, 6, FAKE, FAKE, FAKE, None) == 3
     assert lib.ds_moe_verify_forward_noalloc(fake_layer(), FAKE, 0, FAKE, FAKE, FAKE, None) == 1
     assert lib.ds_moe_verify_forward_noalloc(fake_layer(), FAKE, 7, FAKE, FAKE, FAKE, None) == 1
+    assert lib.ds_moe_verify_forward_noalloc(fake_layer(I=1056), FAKE, 6, FAKE, FAKE, FAKE,
+                                             None) == 2
+
+
+def test_noalloc_status_without_a_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; the GPU tests cover the status query")
+    assert lib.ds_noalloc_status(None) == 4   # DS_ERR_CUDA: no device to query
     assert lib.ds_moe_verify_forward_noalloc(None, FAKE, 1, FAKE, FAKE, FAKE, None) == 1

@@ -307,15 +307,69 @@ def test_band_checks_accept_exact_and_reject_perturbed():
     d = layer_numpy(synth.moe_layer(shape, seed=8))
     x = synth.to_numpy_bits(synth.activations(2, shape.H, seed=8))
     out = oracle.moe_forward(d, x, shape.k, want_h=True)
-    assert compare.h_band_report(out["h"], out["aux"])["ok"]
+    rel_gu, rel_y = compare.kernel_bands(shape.H, shape.I, shape.k)
+    assert compare.h_band_report(out["h"], out["aux"], rel_gu)["ok"]
     bad = out["h"].copy()
     bad.reshape(-1)[::97] ^= 0x0040          # flip a mantissa bit in ~1% of elements
-    assert not compare.h_band_report(bad, out["aux"])["ok"]
+    assert not compare.h_band_report(bad, out["aux"], rel_gu)["ok"]
     y, yaux = oracle.moe_down_combine(d, shape.k, out["idx"], out["w"], out["h"], want_aux=True)
-    assert compare.y_band_report(y, y, yaux)["ok"]
+    assert compare.y_band_report(y, y, yaux, rel_y)["ok"]
     ybad = y.copy()
     ybad.reshape(-1)[::50] ^= 0x0100          # perturb ~2% of the outputs by 2^-5 or more
-    assert not compare.y_band_report(ybad, y, yaux)["ok"]
+    assert not compare.y_band_report(ybad, y, yaux, rel_y)["ok"]
+
+
+def _moe_numpy_case(seed=9, R=3):
+    shape = synth.TINY_MOE
+    d = layer_numpy(synth.moe_layer(shape, seed=seed))
+    x = synth.to_numpy_bits(synth.activations(R, shape.H, seed=seed))
+    out = oracle.moe_forward(d, x, shape.k, want_h=True)
+    return shape, d, x, out
+
+
+def test_moe_check_accepts_the_oracle_itself():
+    from oracle import compare
+    shape, d, x, out = _moe_numpy_case()
+    rep = compare.moe_check(d, x, shape.k, out["y"], out["idx"], out["w"].astype(np.float32),
+                            out["h"])
+    assert rep["ok"], rep
+    assert rep["y_vs_oracle"]["exact"] == rep["y_vs_oracle"]["n"]
+
+
+def test_moe_check_rejects_planted_mistakes():
+    # Mistakes planted in copies of the oracle's own results (on the CPU): each must be
+    # caught by the check that covers it.
+    from oracle import compare
+    shape, d, x, out = _moe_numpy_case()
+    w32 = out["w"].astype(np.float32)
+    # an h value moved far outside its band
+    h_bad = out["h"].copy()
+    h_bad[1, 0, 5] ^= 0x0200
+    rep = compare.moe_check(d, x, shape.k, out["y"], out["idx"], w32, h_bad)
+    assert not rep["h_band"]["ok"] and not rep["ok"]
+    # a y value off by a quarter of its magnitude: outside the tolerance, not explained
+    y_bad = out["y"].copy()
+    y_bad[2, 7] ^= 0x0020
+    rep = compare.moe_check(d, x, shape.k, y_bad, out["idx"], w32, out["h"])
+    assert rep["y_vs_oracle"]["fail"] >= 1 and not rep["ok"]
+    # swapped expert order in one row (not a near-tie)
+    idx_bad = out["idx"].copy()
+    idx_bad[0, [0, 1]] = idx_bad[0, [1, 0]]
+    rep = compare.moe_check(d, x, shape.k, out["y"], idx_bad, w32, out["h"])
+    assert rep["routing"]["rows_bad"] == [0] and not rep["ok"]
+    # routing weights off by 1e-4
+    rep = compare.moe_check(d, x, shape.k, out["y"], out["idx"], w32 + np.float32(1e-4), out["h"])
+    assert not rep["weights_ok"] and not rep["ok"]
+
+
+def test_accumulation_band_matches_its_derivation():
+    from oracle import compare
+    # 2 MMAs x 17 truncating steps of 2^-23, plus one rounding per chained block and per
+    # added partial, each 2^-24
+    assert compare.accumulation_band(0, 0) == 34 * 2.0 ** -23
+    assert compare.accumulation_band(8, 16) == (68 + 24) * 2.0 ** -24
+    rel_gu, rel_y = compare.kernel_bands(4096, 1024, 8)
+    assert 2.0 ** -18 < rel_gu < 2.0 ** -17 and 2.0 ** -18 < rel_y < 2.0 ** -17
 
 
 def test_layer_rows_independent():
@@ -570,3 +624,19 @@ def test_verify_sample_low_temperature_is_greedy():
         q[np.arange(R - 1), draft] = 1.0
         got = oracle.verify_sample(z, 1e-3, q, draft, np.full(R - 1, 0.5), np.full(R, 0.5))
         assert got.tolist() == oracle.verify_greedy(z, draft).tolist()
+
+
+@pytest.mark.parametrize("T", [0.0, -1.0, float("inf"), float("nan")])
+def test_verify_sample_rejects_a_temperature_without_a_softmax(T):
+    z = np.zeros((1, 4), np.float32)
+    with pytest.raises(ValueError):
+        oracle.verify_sample(z, T, np.zeros((0, 4)), np.zeros(0, np.int32), np.zeros(0),
+                             np.array([0.5]))
+    # and the C function itself refuses it before writing anything
+    import ctypes as C
+    out = np.full(1, -7, np.int32)
+    zz = np.ascontiguousarray(z)
+    ur = np.array([0.5])
+    n = oracle.lib().orc_verify_sample(zz.ctypes.data, 1, 4, T, None, None, None,
+                                       ur.ctypes.data, out.ctypes.data)
+    assert n == -1 and out[0] == -7
