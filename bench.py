@@ -476,16 +476,17 @@ def run_ours(args, world, rank, local):
         for k_ in ("moe_r1_gbs", "moe_r1_us_median", "moe_r1_pct_of_hbm_peak"):
             out["components"][k_] = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(layers[0], xs6[0], sel_host, shape, sshape)
+        # the oracle reads the planar form: regenerate layer 0's (same seed) for the host
+        planar = synth.moe_layer(shape, seed=args.seed, device=dev)
+        host = {k: synth.to_numpy_bits(v) for k, v in planar.items()}
+        del planar
+        out["cpu_baseline"] = cpu_baseline(host, xs6[0], sel_host, shape, sshape)
     return out
 
 
-def cpu_baseline(layer, x, sel_host, shape, sshape) -> dict:
+def cpu_baseline(host, x, sel_host, shape, sshape) -> dict:
     """The oracle, as it stands, on a bounded sample of the same workload, host cores."""
     import oracle
-    host = {k: synth.to_numpy_bits(getattr(layer, k)) for k in (
-        "router_w gate_qs gate_sc up_qs up_sc down_qs down_sc sh_gate_qs sh_gate_sc "
-        "sh_up_qs sh_up_sc sh_down_qs sh_down_sc").split()}
     xb = synth.to_numpy_bits(x)
     t = time.perf_counter()
     ref = oracle.moe_forward(host, xb, shape.k)

@@ -60,20 +60,59 @@ typedef enum {
  * a logical [rows][K] matrix in blocks of 32 consecutive values along K. Each value is
  * an int4 q in [-8, 7]; each block has one fp16 scale; the dequantised value is
  * scale * q (no offset, no minimum).
+ *
+ * Planar form (the interchange format, input of ds_q4_tile):
  *   qs : uint8 [rows][K/2]. Block b of a row occupies bytes 16b .. 16b+15. Byte j of a
  *        block holds value 2j in its low nibble and value 2j+1 in its high nibble, each
  *        stored as q + 8 (0..15).
  *   sc : fp16 bits [rows][K/32].
- * For a stack of E experts the arrays are [E][rows][...], expert-major.
- * qs must be 16-byte aligned; sc must be 4-byte aligned.
+ *
+ * Tile-major form (what the MoE kernels stream; written once, at load time, by
+ * ds_q4_tile): the same values and scales, 0.5625 bytes per weight as above, in tiles of
+ * 16 rows x 64 values (two blocks) of 576 bytes. Tile (t, u) covers rows 16t .. 16t+15
+ * and values 64u .. 64u+63. Inside a tile, bytes 16L .. 16L+15 (L = 0..31, g = L / 4,
+ * w = L % 4) hold the 4-byte word w (values 8w .. 8w+7 of a block, planar byte order) of:
+ * row g of block 0, row g+8 of block 0, row g of block 1, row g+8 of block 1; bytes
+ * 512 + 8g .. 512 + 8g+7 hold the fp16 scales of row g / block 0, row g+8 / block 0,
+ * row g / block 1, row g+8 / block 1. Tile rows are ordered in groups of G consecutive tile
+ * rows (the last group of a matrix may be shorter, n rows); inside a group, by K tile
+ * first, then by tile row: tile (t, u) of a matrix with T = K/64 sits at tile index
+ *   (t - t % G) * T + u * n + t % G,   n = min(G, rows/16 - (t - t % G)),
+ * i.e. byte 576 * that index. G = 1 gives plain row-major tiles. The MoE layer's gate and
+ * up matrices use G = 1, its down matrices G = DS_Q4_DOWN_GROUP.
+ * For a stack of E experts both forms are [E][rows][...], expert-major; each expert's
+ * matrix is tiled on its own.
  * ---------------------------------------------------------------------------------- */
 typedef struct {
   const uint8_t* qs;
   const uint16_t* sc;
 } ds_q4;
 
-/* One MoE layer: E routed experts + 1 shared expert, each with gate and up [I][H] and
- * down [H][I], and a bf16 router [E][H].
+/* A Q4 matrix (or expert stack) in the tile-major form; 16-byte aligned. */
+typedef struct {
+  const void* tiles;
+} ds_q4_tiled;
+
+/* Bytes of the tile-major form of a [rows][K] Q4 matrix (rows * K * 9 / 16), or 0 when
+ * rows is not a positive multiple of 16 or K not a positive multiple of 64. */
+size_t ds_q4_tiled_bytes(int64_t rows, int32_t K);
+
+/* Tile rows per group of the down-projection matrices in the tile-major form. */
+#define DS_Q4_DOWN_GROUP 16
+
+/* Writes the tile-major form, with groups of `group` tile rows (1 ..  65536), of n_mats
+ * planar matrices [rows][K] stored one after another in `src` (an expert stack:
+ * n_mats = E) to `dst` (device memory, >= ds_q4_tiled_bytes(n_mats * rows, K), 16-byte
+ * aligned), asynchronously on `stream`. A pure rearrangement of bytes: every nibble and
+ * every scale is copied unchanged. src.qs must be 4-byte aligned and src.sc 2-byte
+ * aligned. Errors: DS_ERR_INVALID_ARG (null or misaligned pointer, sizes, group),
+ * DS_ERR_WORKSPACE (dst_bytes too small), DS_ERR_CUDA. */
+ds_status ds_q4_tile(const ds_q4* src, int32_t n_mats, int64_t rows, int32_t K, int32_t group,
+                     void* dst, size_t dst_bytes, ds_stream_t stream);
+
+/* One MoE layer: E routed experts + 1 shared expert, each with gate and up [I][H] (tile-
+ * major, groups of 1) and down [H][I] (tile-major, groups of DS_Q4_DOWN_GROUP), and a bf16
+ * router [E][H].
  * Limits: H and I multiples of 32, 64 <= H <= 16384, 64 <= I <= 8192, 1 <= top_k <= 16,
  * top_k <= E <= 1024 (else DS_ERR_INVALID_ARG). This build's kernels also need H and I
  * to be multiples of 64, and stage the R verify rows in shared memory, R * (2H + 64)
@@ -84,9 +123,9 @@ typedef struct {
   int32_t n_experts;   /* E (routed)                                          */
   int32_t inter;       /* I (expert intermediate size)                        */
   int32_t top_k;       /* k                                                   */
-  const uint16_t* router_w;     /* bf16 [E][H]                                */
-  ds_q4 gate, up, down;         /* routed: gate, up [E][I][H]; down [E][H][I] */
-  ds_q4 sh_gate, sh_up, sh_down;/* shared: gate, up [I][H]; down [H][I]      */
+  const uint16_t* router_w;              /* bf16 [E][H]                       */
+  ds_q4_tiled gate, up, down;            /* routed: gate, up [E][I][H]; down [E][H][I] */
+  ds_q4_tiled sh_gate, sh_up, sh_down;   /* shared: gate, up [I][H]; down [H][I]      */
 } ds_moe_layer;
 
 /* Bytes of workspace ds_moe_verify_forward needs for this layer and R rows, or 0 when
@@ -114,7 +153,7 @@ size_t ds_moe_workspace_size(const ds_moe_layer* layer, int32_t R);
  *   workspace: >= ds_moe_workspace_size bytes, 256-byte aligned; its contents on entry
  *              are ignored and it must not be used by another call in flight.
  * Errors: DS_ERR_INVALID_ARG (null pointer, R outside 1..6, sizes outside the limits,
- * misaligned qs/sc/x/y), DS_ERR_WORKSPACE, DS_ERR_UNSUPPORTED (H or I not a multiple of
+ * tiles not 16-byte aligned, misaligned x/y), DS_ERR_WORKSPACE, DS_ERR_UNSUPPORTED (H or I not a multiple of
  * 64, or R * H too large for the shared-memory staging), DS_ERR_CUDA. */
 ds_status ds_moe_verify_forward(const ds_moe_layer* layer, const uint16_t* x, int32_t R,
                                 uint16_t* y, int32_t* topk_idx, float* topk_w,
@@ -122,7 +161,8 @@ ds_status ds_moe_verify_forward(const ds_moe_layer* layer, const uint16_t* x, in
 
 /* Same as ds_moe_verify_forward, and in addition records caller-created events on
  * `stream` right after each kernel of the call, for per-kernel timing:
- *   marks[0] after the router, marks[1] after gate+up+SwiGLU, marks[2] after down+combine.
+ *   marks[0] after the router (and the prologue that zeroes the workspace header),
+ *   marks[1] after gate+up+SwiGLU, marks[2] after the down projection and combine.
  * `marks` may be NULL and any entry may be NULL (skipped). The events must belong to the
  * stream's device. Errors as ds_moe_verify_forward; DS_ERR_CUDA if recording fails. */
 ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t* x,

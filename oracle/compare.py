@@ -193,15 +193,15 @@ def y_full_report(y_dev_bits: np.ndarray, y_ref_bits: np.ndarray, yraw_dev: np.n
 def kernel_bands(H: int, I: int, k: int) -> tuple[float, float]:
     """Accumulation bands of the library's Q4 kernels for a layer of hidden H,
     intermediate I and top-k (relative to sum|terms|): (g and u, y).
-    Gate/up: a lane's chain covers up to 8 blocks of each K chunk of 128 blocks (4 of each
-    chunk of 64 when the larger stages do not fit), and the 16 consumer warps' chains are
-    added in warp order. Down: a chain covers up to 16 blocks of each chunk of 128 blocks,
-    up to 16 K-slice chains are added in slice order, and the combine adds the k weighted
-    expert outputs to the shared one by k fmas in rank order."""
-    nb_h, nb_i = H // 32, I // 32
-    chain_gu = min(nb_h, max(8 * -(-nb_h // 128), 4 * -(-nb_h // 64)))
-    chain_dn = min(nb_i, 16 * -(-nb_i // 128))
-    return accumulation_band(chain_gu, 16), accumulation_band(chain_dn, 16) + 2.0 ** -24 * k
+    Gate/up: K = H is cut into chunks of 32 tiles (2 per consumer warp) or, when the larger
+    stages do not fit, of 16 tiles (1 per warp), tiles of two blocks; a lane's chain holds
+    its blocks of every chunk, and the 16 consumer warps' chains are added in warp order.
+    Down: one warp owns a 16-row tile row for all of K = I, so a lane's chain holds every
+    block of the row and no partial sums follow; the combine adds the k weighted expert
+    outputs to the shared one by k fmas in rank order."""
+    T_h, nb_i = H // 64, I // 32
+    chain_gu = min(2 * T_h, max(4 * -(-T_h // 32), 2 * -(-T_h // 16)))
+    return accumulation_band(chain_gu, 16), accumulation_band(nb_i, 0) + 2.0 ** -24 * k
 
 
 def moe_check(host: dict, x_bits: np.ndarray, k: int, y_dev: np.ndarray, idx_dev: np.ndarray,

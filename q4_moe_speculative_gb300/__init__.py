@@ -13,7 +13,7 @@ import torch
 from . import _native as N
 
 __all__ = [
-    "MoeLayer", "moe_workspace_size", "moe_verify_forward", "select_workspace_size",
+    "MoeLayer", "q4_tile", "moe_workspace_size", "moe_verify_forward", "select_workspace_size",
     "select_blocks", "workspace_status", "version", "DsmoeError",
 ]
 
@@ -48,24 +48,43 @@ def _check(status: int, what: str):
         raise N.DsmoeError(status, what)
 
 
+def q4_tile(qs: torch.Tensor, sc: torch.Tensor, group: int = 1, stream=None) -> torch.Tensor:
+    """Tile-major form (include/dsmoe.h) of a planar Q4 matrix or expert stack, with tile
+    rows in groups of `group`: qs uint8 [..., rows, K/2], sc fp16 [..., rows, K/32] ->
+    uint8 [..., rows/16, K/64, 576] (the tile order inside each matrix is the grouped one),
+    written on the device by ds_q4_tile (a rearrangement of bytes, done once at load)."""
+    lib = N.load()
+    _need(qs, "qs", torch.uint8)
+    _need(sc, "sc", torch.float16)
+    lead, rows, K = tuple(qs.shape[:-2]), qs.shape[-2], qs.shape[-1] * 2
+    if tuple(sc.shape) != lead + (rows, K // 32):
+        raise ValueError(f"sc must have shape {lead + (rows, K // 32)} (got {tuple(sc.shape)})")
+    n_mats = 1
+    for n in lead:
+        n_mats *= n
+    if rows % 16 or K % 64:
+        raise ValueError(f"tile-major Q4 needs rows % 16 == 0 and K % 64 == 0 (got {rows}, {K})")
+    out = torch.empty(lead + (rows // 16, K // 64, N.Q4_TILE_BYTES), dtype=torch.uint8,
+                      device=qs.device)
+    src = N.DsQ4(_ptr(qs), _ptr(sc))
+    _check(lib.ds_q4_tile(src, n_mats, rows, K, group, _ptr(out), out.numel(), _stream(stream)),
+           "ds_q4_tile")
+    return out
+
+
 @dataclass
 class MoeLayer:
-    """One MoE layer on the device (layout of include/dsmoe.h):
-    router_w bf16 [E,H]; routed gate/up qs uint8 [E,I,H/2], sc fp16 [E,I,H/32];
-    routed down qs [E,H,I/2], sc [E,H,I/32]; shared expert the same without the E axis."""
+    """One MoE layer on the device (include/dsmoe.h): router_w bf16 [E,H]; routed gate/up
+    uint8 tiles [E, I/16, H/64, 576] (groups of 1), routed down [E, H/16, I/64, 576] (groups of
+    16 tile rows); the shared expert the same without the E axis. Built from planar weights
+    with `from_dict`."""
     router_w: torch.Tensor
-    gate_qs: torch.Tensor
-    gate_sc: torch.Tensor
-    up_qs: torch.Tensor
-    up_sc: torch.Tensor
-    down_qs: torch.Tensor
-    down_sc: torch.Tensor
-    sh_gate_qs: torch.Tensor
-    sh_gate_sc: torch.Tensor
-    sh_up_qs: torch.Tensor
-    sh_up_sc: torch.Tensor
-    sh_down_qs: torch.Tensor
-    sh_down_sc: torch.Tensor
+    gate: torch.Tensor
+    up: torch.Tensor
+    down: torch.Tensor
+    sh_gate: torch.Tensor
+    sh_up: torch.Tensor
+    sh_down: torch.Tensor
     top_k: int
 
     @property
@@ -78,31 +97,33 @@ class MoeLayer:
 
     @property
     def inter(self) -> int:
-        return self.gate_qs.shape[1]
+        return self.gate.shape[1] * 16
 
     def validate(self):
         E, H, I = self.n_experts, self.hidden, self.inter
+        T = N.Q4_TILE_BYTES
         _need(self.router_w, "router_w", torch.bfloat16, (E, H))
         for nm, rows, K, stack in (("gate", I, H, True), ("up", I, H, True), ("down", H, I, True),
                                    ("sh_gate", I, H, False), ("sh_up", I, H, False),
                                    ("sh_down", H, I, False)):
             lead = (E,) if stack else ()
-            _need(getattr(self, nm + "_qs"), nm + "_qs", torch.uint8, lead + (rows, K // 2))
-            _need(getattr(self, nm + "_sc"), nm + "_sc", torch.float16, lead + (rows, K // 32))
+            _need(getattr(self, nm), nm, torch.uint8, lead + (rows // 16, K // 64, T))
 
     def struct(self) -> N.DsMoeLayer:
-        q4 = lambda a, b: N.DsQ4(_ptr(a), _ptr(b))  # noqa: E731
+        t = lambda a: N.DsQ4Tiled(_ptr(a))  # noqa: E731
         return N.DsMoeLayer(
             self.hidden, self.n_experts, self.inter, self.top_k, _ptr(self.router_w),
-            q4(self.gate_qs, self.gate_sc), q4(self.up_qs, self.up_sc),
-            q4(self.down_qs, self.down_sc), q4(self.sh_gate_qs, self.sh_gate_sc),
-            q4(self.sh_up_qs, self.sh_up_sc), q4(self.sh_down_qs, self.sh_down_sc))
+            t(self.gate), t(self.up), t(self.down), t(self.sh_gate), t(self.sh_up),
+            t(self.sh_down))
 
     @staticmethod
     def from_dict(d: dict, top_k: int) -> "MoeLayer":
-        keys = ("router_w gate_qs gate_sc up_qs up_sc down_qs down_sc sh_gate_qs sh_gate_sc "
-                "sh_up_qs sh_up_sc sh_down_qs sh_down_sc").split()
-        return MoeLayer(**{k: d[k] for k in keys}, top_k=top_k)
+        """From planar device tensors (router_w, and qs/sc of gate, up, down, sh_gate, sh_up,
+        sh_down): the Q4 matrices are converted to the tile-major form on the device."""
+        mats = {nm: q4_tile(d[nm + "_qs"], d[nm + "_sc"],
+                            N.Q4_DOWN_GROUP if nm.endswith("down") else 1)
+                for nm in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down")}
+        return MoeLayer(router_w=d["router_w"], **mats, top_k=top_k)
 
 
 def version() -> str:

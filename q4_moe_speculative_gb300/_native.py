@@ -21,7 +21,7 @@ EXPORTS = (
     "ds_moe_workspace_size", "ds_moe_verify_forward", "ds_select_workspace_size",
     "ds_select_blocks", "ds_workspace_status", "ds_status_string", "ds_version",
     "ds_moe_verify_forward_marked", "ds_select_blocks_marked", "ds_moe_workspace_h_offset",
-    "ds_moe_verify_forward_noalloc", "ds_noalloc_status",
+    "ds_moe_verify_forward_noalloc", "ds_noalloc_status", "ds_q4_tiled_bytes", "ds_q4_tile",
 )
 
 DS_SELECT_CANONICAL_SCORES = 1
@@ -32,12 +32,20 @@ class DsQ4(C.Structure):
     _fields_ = [("qs", C.c_void_p), ("sc", C.c_void_p)]
 
 
+class DsQ4Tiled(C.Structure):
+    _fields_ = [("tiles", C.c_void_p)]
+
+
+Q4_TILE_BYTES = 576   # 16 rows x 64 values: 512 bytes of nibbles + 64 bytes of scales
+Q4_DOWN_GROUP = 16    # tile rows per group of the down matrices (same value as the header)
+
+
 class DsMoeLayer(C.Structure):
     _fields_ = [
         ("hidden", C.c_int32), ("n_experts", C.c_int32), ("inter", C.c_int32),
         ("top_k", C.c_int32), ("router_w", C.c_void_p),
-        ("gate", DsQ4), ("up", DsQ4), ("down", DsQ4),
-        ("sh_gate", DsQ4), ("sh_up", DsQ4), ("sh_down", DsQ4),
+        ("gate", DsQ4Tiled), ("up", DsQ4Tiled), ("down", DsQ4Tiled),
+        ("sh_gate", DsQ4Tiled), ("sh_up", DsQ4Tiled), ("sh_down", DsQ4Tiled),
     ]
 
 
@@ -70,6 +78,11 @@ def load() -> C.CDLL:
             f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
             f"g.build()\"` (nvcc, sm_103a). There is no CPU fallback.")
     lib = C.CDLL(str(LIB_PATH))
+    lib.ds_q4_tiled_bytes.argtypes = [C.c_int64, C.c_int32]
+    lib.ds_q4_tiled_bytes.restype = C.c_size_t
+    lib.ds_q4_tile.argtypes = [C.POINTER(DsQ4), C.c_int32, C.c_int64, C.c_int32, C.c_int32,
+                               C.c_void_p, C.c_size_t, C.c_void_p]
+    lib.ds_q4_tile.restype = C.c_int
     lib.ds_moe_workspace_size.argtypes = [C.POINTER(DsMoeLayer), C.c_int32]
     lib.ds_moe_workspace_size.restype = C.c_size_t
     lib.ds_moe_verify_forward.argtypes = [

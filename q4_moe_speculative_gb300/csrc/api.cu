@@ -42,7 +42,7 @@ namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-bool q4_ok(const ds_q4& w) { return w.qs && w.sc && aligned(w.qs, 16) && aligned(w.sc, 4); }
+bool tiles_ok(const ds_q4_tiled& w) { return w.tiles && aligned(w.tiles, 16); }
 
 // Sizes only (no pointers): DS_ERR_INVALID_ARG outside the format's limits (H and I
 // multiples of 32, ranges, k, E, R), DS_ERR_UNSUPPORTED for valid sizes this build's
@@ -62,8 +62,8 @@ ds_status check_layer(const ds_moe_layer* L, int32_t R) {
   const ds_status st = check_layer_sizes(L, R);
   if (st != DS_OK) return st;
   if (!L->router_w || !aligned(L->router_w, 16)) return DS_ERR_INVALID_ARG;
-  if (!q4_ok(L->gate) || !q4_ok(L->up) || !q4_ok(L->down) || !q4_ok(L->sh_gate) ||
-      !q4_ok(L->sh_up) || !q4_ok(L->sh_down))
+  if (!tiles_ok(L->gate) || !tiles_ok(L->up) || !tiles_ok(L->down) || !tiles_ok(L->sh_gate) ||
+      !tiles_ok(L->sh_up) || !tiles_ok(L->sh_down))
     return DS_ERR_INVALID_ARG;
   return DS_OK;
 }
@@ -102,6 +102,26 @@ SelDims sdims_of(const ds_select_args* a) {
 
 extern "C" {
 
+size_t ds_q4_tiled_bytes(int64_t rows, int32_t K) {
+  if (rows <= 0 || rows % 16 || K <= 0 || K % 64) return 0;
+  return (size_t)rows / 16 * (size_t)(K / 64) * kQ4TileBytes;
+}
+
+ds_status ds_q4_tile(const ds_q4* src, int32_t n_mats, int64_t rows, int32_t K, int32_t group,
+                     void* dst, size_t dst_bytes, ds_stream_t stream) {
+  if (!src || !src->qs || !src->sc || !dst || !aligned(src->qs, 4) || !aligned(src->sc, 2) ||
+      !aligned(dst, 16))
+    return DS_ERR_INVALID_ARG;
+  if (n_mats < 1 || group < 1 || group > 65536 || rows > ((int64_t)1 << 40)) return DS_ERR_INVALID_ARG;
+  const size_t need = ds_q4_tiled_bytes(rows, K);
+  if (need == 0) return DS_ERR_INVALID_ARG;
+  if (dst_bytes / (size_t)n_mats < need) return DS_ERR_WORKSPACE;
+  return launch_tile(src->qs, src->sc, n_mats, rows, K, group, static_cast<uint8_t*>(dst),
+                     reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DS_OK
+             : DS_ERR_CUDA;
+}
+
 size_t ds_moe_workspace_size(const ds_moe_layer* layer, int32_t R) {
   if (check_layer_sizes(layer, R) != DS_OK) return 0;
   return moe_layout(dims_of(layer, R)).total;
@@ -132,23 +152,24 @@ ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t
   char* base = static_cast<char*>(workspace);
   MoeWorkspace ws{};
   ws.header = reinterpret_cast<uint32_t*>(base + L.header);
+  ws.counts = reinterpret_cast<uint32_t*>(base + L.counts);
+  ws.zero_bytes = L.zero_bytes;
   ws.scores = reinterpret_cast<float*>(base + L.scores);
   ws.route = reinterpret_cast<RouteInfo*>(base + L.route);
   ws.h = reinterpret_cast<uint16_t*>(base + L.h);
   ws.opart = reinterpret_cast<float*>(base + L.opart);
 
+  auto t = [](const ds_q4_tiled& m) { return static_cast<const uint8_t*>(m.tiles); };
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(base, 0, L.zero_bytes, s) != cudaSuccess) return DS_ERR_CUDA;
   if (launch_router(d, x, layer->router_w, topk_idx, topk_w, ws, s) != cudaSuccess)
     return DS_ERR_CUDA;
   if (!mark(marks, 0, s)) return DS_ERR_CUDA;
-  const Q4Ptr gate{layer->gate.qs, layer->gate.sc}, up{layer->up.qs, layer->up.sc};
-  const Q4Ptr down{layer->down.qs, layer->down.sc};
-  const Q4Ptr sg{layer->sh_gate.qs, layer->sh_gate.sc}, su{layer->sh_up.qs, layer->sh_up.sc};
-  const Q4Ptr sd{layer->sh_down.qs, layer->sh_down.sc};
-  if (launch_gate_up(d, x, gate, up, sg, su, ws, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (launch_gate_up(d, x, t(layer->gate), t(layer->up), t(layer->sh_gate), t(layer->sh_up), ws,
+                     s) != cudaSuccess)
+    return DS_ERR_CUDA;
   if (!mark(marks, 1, s)) return DS_ERR_CUDA;
-  if (launch_down(d, down, sd, topk_w, y, ws, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (launch_down(d, t(layer->down), t(layer->sh_down), topk_w, y, ws, s) != cudaSuccess)
+    return DS_ERR_CUDA;
   if (!mark(marks, 2, s)) return DS_ERR_CUDA;
   return DS_OK;
 }

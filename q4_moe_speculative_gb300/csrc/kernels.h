@@ -5,6 +5,8 @@
 #include <cuda.h>   // CUtensorMap
 #include <cuda_runtime.h>
 
+#include "dsmoe.h"
+
 namespace dsmoe {
 
 constexpr int kMaxRows = 6;        // verify rows per MoE call
@@ -21,17 +23,18 @@ struct RouteInfo {
   int8_t slot[kMaxUnion][8];        // rank + 1 of the expert in row r (slot 0 = shared)
 };
 
-struct Q4Ptr {
-  const uint8_t* qs;
-  const uint16_t* sc;
-};
-
 struct MoeDims {
   int R, H, E, I, k;
 };
 
+// Bytes of one tile of the tile-major Q4 layout: 16 rows x 64 values, 512 bytes of nibbles
+// in tensor-core fragment order followed by 64 bytes of fp16 scales.
+constexpr int kQ4TileBytes = 576;
+
 struct MoeWorkspace {
   uint32_t* header;        // WsHeader: status word, router arrival count
+  uint32_t* counts;        // [ceil(H/256)] down-projection units completed per row group
+  size_t zero_bytes;       // bytes from header on that every call zeroes first
   float* scores;           // [R][E] sigmoid router scores
   RouteInfo* route;
   uint16_t* h;             // bf16 [R][1+k][I]
@@ -39,20 +42,28 @@ struct MoeWorkspace {
 };
 
 struct MoeLayout {
-  size_t header, scores, route, h, opart, total, zero_bytes;
+  size_t header, counts, scores, route, h, opart, total, zero_bytes;
 };
 MoeLayout moe_layout(const MoeDims& d);
 // Least dynamic shared memory the gate/up kernel needs for these sizes (bytes).
 size_t gate_up_smem_bytes(const MoeDims& d);
 
+// n_mats planar Q4 matrices (qs [rows][K/2], sc [rows][K/32] each) -> tile-major with
+// tile rows in groups of `group` (rows % 16 == 0, K % 64 == 0).
+cudaError_t launch_tile(const uint8_t* qs, const uint16_t* sc, int n_mats, int64_t rows,
+                        int K, int group, uint8_t* dst, cudaStream_t s);
+// Tile rows per group of the down-projection matrices (gate and up use groups of 1).
+constexpr int kDownGroup = DS_Q4_DOWN_GROUP;
+// Prologue (zeroes the workspace's first zero_bytes) + router.
 cudaError_t launch_router(const MoeDims& d, const uint16_t* x, const uint16_t* router_w,
                           int32_t* topk_idx, float* topk_w, const MoeWorkspace& ws,
                           cudaStream_t s);
-cudaError_t launch_gate_up(const MoeDims& d, const uint16_t* x, Q4Ptr gate, Q4Ptr up,
-                           Q4Ptr sh_gate, Q4Ptr sh_up, const MoeWorkspace& ws,
-                           cudaStream_t s);
-cudaError_t launch_down(const MoeDims& d, Q4Ptr down, Q4Ptr sh_down, const float* topk_w,
-                        uint16_t* y, const MoeWorkspace& ws, cudaStream_t s);
+cudaError_t launch_gate_up(const MoeDims& d, const uint16_t* x, const uint8_t* gate,
+                           const uint8_t* up, const uint8_t* sh_gate, const uint8_t* sh_up,
+                           const MoeWorkspace& ws, cudaStream_t s);
+cudaError_t launch_down(const MoeDims& d, const uint8_t* down, const uint8_t* sh_down,
+                        const float* topk_w, uint16_t* y, const MoeWorkspace& ws,
+                        cudaStream_t s);
 
 // ------------------------------------------------------------------ block select ----
 struct SelDims {
@@ -109,13 +120,9 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
                         const float* head_w, int32_t* sel, int32_t* nsel,
                         const SelWorkspace& ws, bool tc, cudaStream_t s);
 
-// TMA tensor maps (cached by their parameters). q4_maps: one Q4 matrix of `rows` rows of K
-// values (K a multiple of 256) in boxes of `box_rows` rows by `box_blocks` Q4 blocks (a
-// multiple of 8): nibbles as [128-byte chunk][row][128 B] with the 128-byte swizzle, scales
-// [row][K/32]. key_tile_map: bf16 block keys [L][N][128] (layer stride key_stride values, a
-// multiple of 8) in boxes of 64 values x box_rows blocks, 128-byte swizzle.
-cudaError_t q4_maps(CUtensorMap* wq, CUtensorMap* wsc, Q4Ptr m, uint64_t rows, int K,
-                    int box_rows, int box_blocks);
+// TMA tensor map (cached by its parameters) of bf16 block keys [L][N][128] (layer stride
+// key_stride values, a multiple of 8) in boxes of 64 values x box_rows blocks, 128-byte
+// swizzle.
 cudaError_t key_tile_map(CUtensorMap* out, const uint16_t* keys, int N, int L,
                          int64_t key_stride, int box_rows);
 

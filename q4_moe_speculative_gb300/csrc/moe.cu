@@ -1,5 +1,6 @@
-// moe.cu — the speculative-verify Q4 MoE layer: router (K1), gate+up+SwiGLU (K3), down
-// projection (K4) and the rank-ordered combine (K5).
+// moe.cu — the speculative-verify Q4 MoE layer: router (K1), gate+up+SwiGLU (K3) and the
+// down projection with the rank-ordered combine in its epilogue (K4); the conversion of Q4
+// weights to the tile-major layout the kernels stream (K0).
 //
 // Page: "DeepSeek V4.1F Q4 on M3 Ultra with native DSpark MTP (40tps / 800tps)".
 //   paragraph "Decode": the 384-expert router is one dispatch; the shared expert's
@@ -12,17 +13,22 @@
 // fixed order that does not depend on R or on the other rows, so an R-row call writes the
 // same bytes as R one-row calls.
 //
-// Q4 dot products (K3, K4) run on the tensor cores as mma.sync m16n8k16 (bf16 in, fp32
-// accumulate) with the weights dequantised in registers: the M dimension is 16 weight rows,
-// N = 8 is the (up to 6) verify rows, K = 16 values of one 32-value Q4 block, so each
-// block's fp16 scale is applied exactly to that block's two MMAs. Widening a 32-bit word
-// of 8 nibbles costs three shifts, four AND-ORs that put nibbles in the mantissa of the
-// bf16 number 128 + nibble, and four bf16x2 subtractions of 136 (exact q = nibble - 8).
-// A producer warp streams the weights into a ring of CTA-wide stages completed by
-// mbarriers: as TMA boxes (a 3D view of the nibbles, [128-byte chunk][row][128 bytes],
-// with the 128-byte swizzle, and a 2D box of the scales) when the rows are whole 128-byte
-// chunks and the scales 16-byte aligned, else as per-row 1D bulk copies of up to 1 KB and
-// 4-byte scale copies.
+// Weights are streamed in the tile-major layout (written once by K0 from the planar Q4
+// format): a tile is 16 rows x 64 values (two Q4 blocks) in 576 bytes, the 512 bytes of
+// nibbles in the order the tensor-core fragments want them (lane L = 4g + q holds word q of
+// rows g and g + 8 of both blocks in its 16 bytes) followed by the 64 bytes of fp16 scales
+// (8 bytes per row pair g, g + 8). Tiles run along K within a 16-row tile row, tile rows
+// follow one another (in groups of 16 tile rows, K tile first within a group, for the
+// down matrices). A pipeline stage is therefore one or two long contiguous runs,
+// moved by 1D bulk copies at the full HBM rate, and every fragment read from shared memory
+// is one conflict-free 16-byte load.
+//
+// Q4 dot products run on the tensor cores as mma.sync m16n8k16 (bf16 in, fp32 accumulate)
+// with the weights dequantised in registers: the M dimension is 16 weight rows, N = 8 is the
+// (up to 6) verify rows, K = 16 values of one 32-value Q4 block, so each block's fp16 scale
+// is applied exactly to that block's two MMAs. Widening a 32-bit word of 8 nibbles costs
+// three shifts, four AND-ORs that put nibbles in the mantissa of the bf16 number
+// 128 + nibble, and four bf16x2 subtractions of 136 (exact q = nibble - 8).
 #include <climits>
 #include <utility>
 
@@ -35,8 +41,22 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kRouterWarps = 8;
-constexpr uint32_t kWaitPolls = 1u << 20;   // bounded mbarrier waits (~1 s)
+// Pipeline waits sleep in polls of at most kWaitSleepNs and give up after kWaitPolls polls
+// (about 1 s in all).
+#ifndef DSMOE_WAIT_SLEEP_NS
+#define DSMOE_WAIT_SLEEP_NS 2000
+#endif
+constexpr uint32_t kWaitSleepNs = DSMOE_WAIT_SLEEP_NS;
+constexpr uint32_t kWaitPolls = kWaitSleepNs > 0 ? (1u << 30) / kWaitSleepNs : (1u << 20);
+
+__device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity) {
+  if constexpr (kWaitSleepNs > 0)
+    return mbar_wait_sleep(bar, parity, kWaitPolls, kWaitSleepNs);
+  else
+    return mbar_wait(bar, parity, kWaitPolls);
+}
+constexpr int kTile = kQ4TileBytes;         // 576: 16 rows x 64 values
+constexpr int kTileNib = 512;               // nibble bytes of a tile; the scales follow
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -49,15 +69,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-// 16-byte async copy global -> shared; zero-fill (no global read) when !valid.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(dst)), "l"(src),
-               "r"(valid ? 4 : 0)
+// 16-byte async copy global -> shared.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
@@ -67,14 +81,17 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// The mbarrier receives one arrival once all of this thread's earlier cp.async copies have
-// landed; the arrival is counted in the barrier's initial count (noinc).
-__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
+// 1D bulk copy global -> shared of `bytes` (multiple of 16, both addresses 16-aligned),
+// completing `bytes` of the transaction count of `bar`.
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
 }
-__device__ __forceinline__ uint32_t lds32(const uint8_t* p) {
-  return *reinterpret_cast<const uint32_t*>(p);
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 // bf16 pair (q_lo, q_hi) of the nibbles at bits 0-3 and 16-19 of w: (w & 0x000F000F) |
@@ -114,37 +131,113 @@ __device__ __forceinline__ void q4_block_mma(uint32_t w_lo, uint32_t w_hi, const
   mma16816(d, p2, r2, p3, r3, X.z, X.w, d);
 }
 
+// acc (rows g, g+8 of this lane) += scale * the raw block dot products d.
+__device__ __forceinline__ void scale_add(float (&acc)[4], float s_g, float s_g8,
+                                          const float (&d)[4]) {
+  acc[0] = __fmaf_rn(s_g, d[0], acc[0]);
+  acc[1] = __fmaf_rn(s_g, d[1], acc[1]);
+  acc[2] = __fmaf_rn(s_g8, d[2], acc[2]);
+  acc[3] = __fmaf_rn(s_g8, d[3], acc[3]);
+}
+
+// Both blocks of one tile for this lane: W = the lane's 16 nibble bytes, S = the 8 bytes of
+// scales of its row pair, X0 / X1 the activations of the tile's two blocks.
+__device__ __forceinline__ void q4_tile_mma(const uint4& W, const uint2& S, const uint4& X0,
+                                            const uint4& X1, float (&acc)[4]) {
+  const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&S.x));   // block 0
+  const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&S.y));   // block 1
+  float d[4];
+  q4_block_mma(W.x, W.y, X0, d);
+  scale_add(acc, s0.x, s0.y, d);
+  q4_block_mma(W.z, W.w, X1, d);
+  scale_add(acc, s1.x, s1.y, d);
+}
+
 // Natural-order bf16 values v0..v7 (as 4 packed words) -> MMA pair order.
 __device__ __forceinline__ uint4 pair_order(const uint4& v) {
   return make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
                     __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
 }
 
-// Four packed fp16 scales (blocks j = 0..3) -> fp32.
-__device__ __forceinline__ void widen_scales(uint2 s, float (&f)[4]) {
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&s.x));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&s.y));
-  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+__device__ __forceinline__ uint2 lds64(const uint8_t* p) {
+  return *reinterpret_cast<const uint2*>(p);
 }
 
 // ---------------------------------------------------------------------------------
-// K1: router. CTA c computes z = x . Wr[e] for the kRouterExperts experts e of its group
-// and all R rows: warp w takes the w-th eighth of the hidden dimension (x read straight
-// from global memory into registers, each lane 8 values at a time), the eight warps'
-// partial sums (lane-strided then a butterfly) are added in warp order, and the sigmoid
-// score is written. The last CTA to arrive (atomic count, nobody waits) selects each
-// row's top k (one warp per row, its scores in registers, a tree argmax per round with
-// ties to the lower index), renormalises the weights, and builds the union of the
-// selected experts with each one's rows and rank slots.
+// K0: planar Q4 -> tile-major. One thread per (tile, lane): the lane's 16 bytes of nibble
+// words (word q of rows g and g + 8, blocks 2u and 2u + 1 of the tile's K range), and for
+// lanes 0..7 the 8 bytes of scales of row pair (lane, lane + 8). Tile rows are ordered in
+// groups of G: within a group (the last one of a matrix may be shorter), by K tile first,
+// then by tile row, so that G tile rows x a few K tiles are one contiguous run.
 // ---------------------------------------------------------------------------------
-constexpr int kRouterExperts = 4;
+__global__ void __launch_bounds__(256) k0_q4_tile(const uint8_t* __restrict__ qs,
+                                                  const uint16_t* __restrict__ sc,
+                                                  int64_t tiles, int TR, int T, int K, int G,
+                                                  uint8_t* __restrict__ dst) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t tile = i >> 5;
+  if (tile >= tiles) return;
+  const int lane = (int)(i & 31), g = lane >> 2, q = lane & 3;
+  const int64_t trg = tile / T;                   // tile row over all matrices
+  const int u = (int)(tile - trg * T);
+  const int64_t mat = trg / TR;
+  const int t = (int)(trg - mat * TR);            // tile row within the matrix
+  const int g0 = t / G * G, rig = min(G, TR - g0);
+  const int64_t out = (mat * TR + g0) * T + (int64_t)u * rig + (t - g0);
+  const size_t row_qs = (size_t)K / 2, row_sc = (size_t)K / 32;
+  const uint8_t* p0 = qs + (size_t)(trg * 16 + g) * row_qs + (size_t)u * 32 + q * 4;
+  const uint8_t* p1 = p0 + 8 * row_qs;
+  uint4 v;
+  v.x = *reinterpret_cast<const uint32_t*>(p0);        // row g,     block 2u
+  v.y = *reinterpret_cast<const uint32_t*>(p1);        // row g + 8, block 2u
+  v.z = *reinterpret_cast<const uint32_t*>(p0 + 16);   // row g,     block 2u + 1
+  v.w = *reinterpret_cast<const uint32_t*>(p1 + 16);   // row g + 8, block 2u + 1
+  uint8_t* tp = dst + (size_t)out * kTile;
+  *reinterpret_cast<uint4*>(tp + lane * 16) = v;
+  if (lane < 8) {
+    const uint16_t* s0 = sc + (size_t)(trg * 16 + lane) * row_sc + 2 * u;
+    const uint16_t* s1 = s0 + 8 * row_sc;
+    uint2 sv;
+    sv.x = (uint32_t)s0[0] | ((uint32_t)s1[0] << 16);
+    sv.y = (uint32_t)s0[1] | ((uint32_t)s1[1] << 16);
+    *reinterpret_cast<uint2*>(tp + kTileNib + lane * 8) = sv;
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Prologue: zeroes the words of the workspace that must start at zero (status word,
+// router arrival count, combine arrival counts) and lets the router start at once; the
+// router waits for this grid only before its arrival count.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k0_clear(uint32_t* __restrict__ p, int nwords) {
+  pdl_trigger();
+  for (int i = threadIdx.x; i < nwords; i += blockDim.x) p[i] = 0u;
+}
+
+// ---------------------------------------------------------------------------------
+// K1: router. CTA c computes z = x . Wr[e] for two experts e and all R rows: warps 0-3
+// take expert 2c, warps 4-7 expert 2c + 1, warp w the (w % 4)-th quarter of the hidden
+// dimension (each lane up to 4 chunks of 8 values, all requested before the first is
+// used, x read straight from global memory). A lane adds its chunks in order, the warp's
+// lanes are added by a butterfly, the four warps' sums in warp order, and the sigmoid
+// score is written. The last CTA to arrive (atomic count, nobody waits) selects each row's
+// top k (one warp per row, its scores in registers, a tree argmax per round with ties to
+// the lower index), renormalises the weights, and builds the union of the selected
+// experts with each one's rows and rank slots.
+// ---------------------------------------------------------------------------------
+constexpr int kRouterWarps = 8;
+constexpr int kRouterExperts = 2;
+constexpr int kRouterChunks = 4;   // chunks of 8 values per lane in flight
 
 template <int KPER>   // score registers per lane in the top-k: ceil(E / 32) <= KPER
 __global__ void __launch_bounds__(kRouterWarps * 32)
     k1_router(const uint16_t* __restrict__ x, int R, int H, const uint16_t* __restrict__ wr,
               int E, int k, float* __restrict__ scores, int32_t* __restrict__ topk_idx,
               float* __restrict__ topk_w, RouteInfo* __restrict__ route, WsHeader* hdr) {
-  __shared__ float part[kRouterWarps][kRouterExperts][kMaxRows];
+  __shared__ float part[kRouterWarps][kMaxRows];
   __shared__ int s_is_last;
   __shared__ int32_t sel_e[kMaxRows][kMaxTopK];
   __shared__ float sel_s[kMaxRows][kMaxTopK];
@@ -156,89 +249,81 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 
   pdl_trigger();   // the gate/up kernel may launch now; it waits for this grid's results
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int e0 = blockIdx.x * kRouterExperts;
-  const int ne = min(kRouterExperts, E - e0);
+  const int e = blockIdx.x * kRouterExperts + (warp >> 2);
   {
-    float acc[kRouterExperts][kMaxRows];
+    float acc[kMaxRows];
 #pragma unroll
-    for (int e = 0; e < kRouterExperts; ++e)
+    for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.0f;
+    const int quarter = H / 4;            // a multiple of 16
+    const int nch = quarter / 8;
+    const int col0 = (warp & 3) * quarter;
+    if (e < E) {
+      const uint16_t* wrow = wr + (size_t)e * H + col0;
+      for (int c0 = lane; c0 < nch; c0 += 32 * kRouterChunks) {
+        // every load of the batch (weights, then the rows' activations) is issued before
+        // the first multiply, so the batch costs one memory round trip
+        uint4 wv[kRouterChunks], xv[kRouterChunks][kMaxRows];
 #pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) acc[e][r] = 0.0f;
-    const int slice = H / kRouterWarps;          // a multiple of 8
-    const int nch = slice / 8;
-    // the weights of two chunks per lane are requested before either is used
-    for (int c0 = lane; c0 < nch; c0 += 64) {
-      uint4 wv2[2][kRouterExperts];
+        for (int j = 0; j < kRouterChunks; ++j) {
+          const int c = min(c0 + 32 * j, nch - 1);
+          wv[j] = __ldcs(reinterpret_cast<const uint4*>(wrow + c * 8));
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = c0 + 32 * cc, col = warp * slice + c * 8;
+          for (int r = 0; r < kMaxRows; ++r)
+            xv[j][r] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)min(r, R - 1) * H + col0 + c * 8));
+        }
 #pragma unroll
-        for (int e = 0; e < kRouterExperts; ++e)
-          wv2[cc][e] = (c < nch && e < ne)
-                           ? __ldcs(reinterpret_cast<const uint4*>(wr + (size_t)(e0 + e) * H + col))
-                           : make_uint4(0, 0, 0, 0);
-      }
+        for (int j = 0; j < kRouterChunks; ++j) {
+          if (c0 + 32 * j >= nch) break;
+          const float wf[8] = {bf16_lo(wv[j].x), bf16_hi(wv[j].x), bf16_lo(wv[j].y),
+                               bf16_hi(wv[j].y), bf16_lo(wv[j].z), bf16_hi(wv[j].z),
+                               bf16_lo(wv[j].w), bf16_hi(wv[j].w)};
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = c0 + 32 * cc;
-        if (c >= nch) break;
-        const int col = warp * slice + c * 8;
-        const uint4* wv = wv2[cc];
-        uint4 xv[kMaxRows];
-#pragma unroll
-        for (int r = 0; r < kMaxRows; ++r)
-          xv[r] = r < R ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)r * H + col))
-                        : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
-          if (r < R) {
-            const float xf[8] = {bf16_lo(xv[r].x), bf16_hi(xv[r].x), bf16_lo(xv[r].y),
-                                 bf16_hi(xv[r].y), bf16_lo(xv[r].z), bf16_hi(xv[r].z),
-                                 bf16_lo(xv[r].w), bf16_hi(xv[r].w)};
-#pragma unroll
-            for (int e = 0; e < kRouterExperts; ++e) {
-              float t = acc[e][r];
-              t = __fmaf_rn(bf16_lo(wv[e].x), xf[0], t); t = __fmaf_rn(bf16_hi(wv[e].x), xf[1], t);
-              t = __fmaf_rn(bf16_lo(wv[e].y), xf[2], t); t = __fmaf_rn(bf16_hi(wv[e].y), xf[3], t);
-              t = __fmaf_rn(bf16_lo(wv[e].z), xf[4], t); t = __fmaf_rn(bf16_hi(wv[e].z), xf[5], t);
-              t = __fmaf_rn(bf16_lo(wv[e].w), xf[6], t); t = __fmaf_rn(bf16_hi(wv[e].w), xf[7], t);
-              acc[e][r] = t;
-            }
+          for (int r = 0; r < kMaxRows; ++r) {
+            const uint4 xr = xv[j][r];
+            float t = acc[r];
+            t = __fmaf_rn(wf[0], bf16_lo(xr.x), t); t = __fmaf_rn(wf[1], bf16_hi(xr.x), t);
+            t = __fmaf_rn(wf[2], bf16_lo(xr.y), t); t = __fmaf_rn(wf[3], bf16_hi(xr.y), t);
+            t = __fmaf_rn(wf[4], bf16_lo(xr.z), t); t = __fmaf_rn(wf[5], bf16_hi(xr.z), t);
+            t = __fmaf_rn(wf[6], bf16_lo(xr.w), t); t = __fmaf_rn(wf[7], bf16_hi(xr.w), t);
+            acc[r] = t;   // rows >= R accumulate a copy of row R - 1, never read
           }
         }
       }
     }
 #pragma unroll
-    for (int e = 0; e < kRouterExperts; ++e)
-#pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
-        if (r < R) {
-          const float v = warp_sum(acc[e][r]);
-          if (lane == 0) part[warp][e][r] = v;
-        }
+    for (int r = 0; r < kMaxRows; ++r) {
+      if (r < R) {
+        const float v = warp_sum(acc[r]);
+        if (lane == 0) part[warp][r] = v;
       }
+    }
   }
   __syncthreads();
-  if (tid < ne * R) {
-    const int e = tid / R, r = tid - e * R;
-    float z = 0.0f;
+  if (tid < kRouterExperts * R) {
+    const int ee = tid / R, r = tid - ee * R;
+    const int e2 = blockIdx.x * kRouterExperts + ee;
+    if (e2 < E) {
+      float z = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kRouterWarps; ++w) z = __fadd_rn(z, part[w][e][r]);
-    scores[r * E + e0 + e] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
+      for (int w = 0; w < 4; ++w) z = __fadd_rn(z, part[ee * 4 + w][r]);
+      scores[r * E + e2] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
+    }
   }
 
   // Arrival count: the last CTA continues, the others are done. Nobody waits. (The CTA
   // barrier orders the scores before thread 0's fence, which makes them visible device-wide
-  // before the count.)
+  // before the count.) The count was zeroed by the prologue grid, which thread 0 waits for.
   __syncthreads();
   if (tid == 0) {
+    pdl_wait();
     __threadfence();
     const unsigned prev = atomicAdd(&hdr->router_arrivals, 1u);
     s_is_last = (prev == gridDim.x - 1);
+    if (s_is_last) __threadfence();   // the other CTAs' scores are visible to this CTA after
+                                      // the barrier below (the fence is cumulative)
   }
   __syncthreads();
   if (!s_is_last) return;
-  __threadfence();
 
   if (tid < kMaxExperts / 32) ubits[tid] = 0u;
   if (warp < R) {
@@ -283,13 +368,16 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
       }
     }
     __syncwarp();
+    // renormalise: the sum in rank order (one lane), then one division per lane
+    float sum = 0.0f;
     if (lane == 0) {
-      float sum = sel_s[r][0];
+      sum = sel_s[r][0];
       for (int j = 1; j < k; ++j) sum = __fadd_rn(sum, sel_s[r][j]);
-      for (int j = 0; j < k; ++j) {
-        topk_idx[r * k + j] = sel_e[r][j];
-        topk_w[r * k + j] = __fdiv_rn(sel_s[r][j], sum);
-      }
+    }
+    sum = __shfl_sync(0xffffffffu, sum, 0);
+    if (lane < k) {
+      topk_idx[r * k + lane] = sel_e[r][lane];
+      topk_w[r * k + lane] = __fdiv_rn(sel_s[r][lane], sum);
     }
   }
   __syncthreads();
@@ -336,144 +424,91 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 #pragma unroll
     for (int r = 0; r < 8; ++r) route->slot[i][r] = u_slot[i][r];
   }
-  if (tid == 0) {
-    route->n_union = nu;
-    hdr->router_arrivals = 0u;
-  }
+  if (tid == 0) route->n_union = nu;
 }
 
 // ---------------------------------------------------------------------------------
 // Weight streaming for K3 and K4. A CTA has 16 consumer warps and one producer warp; a
-// ring of stages in shared memory is handed over with "full" and "empty" mbarriers, so
-// the copies of the next stages are always in flight while the consumers compute. HBM
-// serves long contiguous runs at full bandwidth and every copy operation has a fixed
-// cost, so a stage is a few large copies of whole row segments of consecutive rows:
-//  * boxed path (rows a multiple of 128 bytes, i.e. K a multiple of 256): the nibbles of
-//    the stage's rows arrive as ONE TMA box per matrix over the view [128-byte chunk][row]
-//    [128 bytes] with the 128-byte swizzle (granule j of row r stored at j ^ (r & 7), so
-//    the MMA fragment reads are free of bank conflicts), and the fp16 scales as one 2D
-//    TMA box per matrix;
-//  * row path (other sizes): one 1D bulk copy per row segment into a row padded by 16
-//    bytes, and the scales in 4-byte cp.async pieces.
-// Work is assigned statically, so the split depends only on the sizes.
+// ring of stages in shared memory is handed over with "full" and "empty" mbarriers, so the
+// copies of the next stages are always in flight while the consumers compute. A stage is a
+// few long runs of consecutive tiles, each one 1D bulk copy. Work is assigned statically,
+// so the split depends only on the sizes.
 // ---------------------------------------------------------------------------------
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kMmaThreads = kConsumers + 32;            // + producer warp
 constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kChunkBlocks = 128;                       // Q4 blocks per row per stage (at most)
-constexpr int kMaxRing = 4;
-constexpr uint32_t kFullArrivals = 1 + 32;              // expect_tx + the producer's lanes
+constexpr int kMaxRing = 8;
 constexpr int kReducerWarps = 3;                         // gate/up: 16 rows x R <= 96 outputs
 constexpr int kGuThreads = kMmaThreads + 32 * kReducerWarps;
 constexpr int kConsumerBarrier = 1;                     // named barrier id of the consumers
+constexpr int kXPad = 64;                                // staged activation row pad (bytes)
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   const uint32_t a = smem_addr(p);
   return p + (((a + 1023u) & ~1023u) - a);
 }
 
-__host__ __device__ constexpr size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-// 1D bulk copy global -> shared of `bytes` (multiple of 16, both addresses 16-aligned).
-__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync %0, %1;" ::"n"(kConsumerBarrier), "n"(kConsumers) : "memory");
 }
 
-// Row path: `rows` rows of `cb` blocks (nibbles and scales; row strides `row_qs` bytes /
-// `nb` halves) into padded shared rows; called by all 32 producer lanes.
-__device__ __forceinline__ void copy_rows(uint8_t* qdst, int qpitch, const uint8_t* qsrc,
-                                          size_t row_qs, uint8_t* sdst, int spitch,
-                                          const uint16_t* ssrc, int nb, int rows, int cb,
-                                          uint64_t* bar, int lane) {
-  for (int r = lane; r < rows; r += 32)
-    bulk_copy(qdst + r * qpitch, qsrc + (size_t)r * row_qs, (uint32_t)cb * 16, bar);
-  const int per_row = cb >> 1;
-  for (int p = lane; p < rows * per_row; p += 32) {
-    const int r = p / per_row, pp = p - r * per_row;
-    cp_async4(sdst + r * spitch + pp * 4, ssrc + (size_t)r * nb + 2 * pp, true);
-  }
-}
-
 // ---------------------------------------------------------------------------------
-// K3: gate + up + SwiGLU. A unit is (expert slot u, 16 rows of I): slot 0 is the shared
-// expert (all rows), slot u >= 1 the u-th expert of the union (its rows). CTA b takes
-// units b, b + G, b + 2G, ... (G = grid). A stage is one K chunk of a unit (the gate and
-// up rows' segments of up to 16 WB blocks); consumer warp w computes blocks WB w ..
-// WB w + WB - 1 of the chunk for both matrices and keeps its partial sums across the
-// unit's chunks. At the end of a unit the 16 warps' partials meet in shared memory and
-// are added in warp order; h = bf16_rne(silu(g) * u) is written for the expert's rows.
-// The activations sit in shared memory as bf16 in MMA pair order, staged once per CTA
-// while the router runs. The producer starts on the shared expert's units before the
-// router's results exist.
+// K3: gate + up + SwiGLU. A unit is (expert slot u, tile row of I = 16 rows): slot 0 is the
+// shared expert (all rows), slot u >= 1 the u-th expert of the union (its rows). CTA b
+// takes units b, b + G, b + 2G, ... (G = grid). A stage is one K chunk of a unit: CT
+// consecutive tiles of the gate tile row and the same of the up tile row, two bulk copies.
+// Consumer warp w takes tiles CT/16 w .. CT/16 w + CT/16 - 1 of the chunk for both matrices
+// and keeps its partial sums across the unit's chunks. At the end of a unit the 16 warps'
+// partials meet in shared memory and are added in warp order by the reducer warps, which
+// write h = bf16_rne(silu(g) * u) for the expert's rows. The activations sit in shared
+// memory as bf16 in MMA pair order, staged once per CTA while the router runs; the
+// producer starts on the shared expert's units before the router's results exist.
 // ---------------------------------------------------------------------------------
-// Stage geometry for WB blocks per warp (a chunk of 16 WB blocks per row): WB = 8 when
-// the stages fit beside the staged activations, else 4.
-template <int WB>
-struct GuGeom {
-  static constexpr int kCB = 16 * WB;                            // blocks per chunk
-  static constexpr int kQsPitch = kCB * 16 + 16;                 // row path: 2064 / 1040
-  static constexpr int kScPitch = kCB * 2 + 16;                  // row path: 272 / 144
-  static constexpr int kRowQs = 2 * 16 * kQsPitch;               // row path: nibble bytes
-  static constexpr int kBoxQs = 16 * kCB * 16;                   // boxed: one matrix
-  static constexpr int kBoxSc = 16 * kCB * 2;                    // boxed: one matrix
-  static constexpr int kStage = (int)round_up((size_t)kRowQs + 2 * 16 * kScPitch, 1024);
-};
-constexpr int kXPad = 64;                                  // staged activation row pad
-
-struct alignas(64) GateUpArgs {
-  CUtensorMap wq[4];   // boxed path: nibbles of gate, up, sh_gate, sh_up
-  CUtensorMap wsc[4];  // boxed path: their scales
-  Q4Ptr gate, up, sh_gate, sh_up;
+struct GateUpArgs {
+  const uint8_t* gate;     // tiles [E][I/16][H/64]
+  const uint8_t* up;
+  const uint8_t* sh_gate;  // tiles [I/16][H/64]
+  const uint8_t* sh_up;
   const uint16_t* x;
   const RouteInfo* route;
   uint16_t* h;
   uint32_t* status;
-  int R, H, I, k, ring, boxed;
+  int R, H, I, k, ring;
 };
 
 __host__ __device__ constexpr size_t gu_red_bytes(int R) {
   return 2ull * kConsumerWarps * 2 * 16 * (size_t)R * 4;
 }
+template <int CT>
+__host__ __device__ constexpr size_t gu_stage_bytes() { return 2ull * CT * kTile; }
 
-template <int WB>
-__global__ void __launch_bounds__(kGuThreads, 1) k3_gate_up(const __grid_constant__ GateUpArgs a) {
-  using Geo = GuGeom<WB>;
+template <int CT>   // tiles per matrix per stage: 32 or 16
+__global__ void __launch_bounds__(kGuThreads, 1) k3_gate_up(const GateUpArgs a) {
+  constexpr int TPW = CT / kConsumerWarps;   // tiles per warp per matrix per stage
+  constexpr int kStage = (int)gu_stage_bytes<CT>();
+  __shared__ __align__(8) uint64_t full[kMaxRing], empty[kMaxRing];
   // partial-sum buffers: written by the 16 consumer warps (pfull), read by the reducer
   // warps (pempty); two buffers, so consumers wait only when two units are unreduced
   __shared__ __align__(8) uint64_t s_pfull[2], s_pempty[2];
-  constexpr int kCB = Geo::kCB, kStage = Geo::kStage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int R = a.R, H = a.H, I = a.I, k = a.k, ring = a.ring;
-  const bool boxed = a.boxed != 0;
-  const int nb = H >> 5;                          // Q4 blocks per row
-  const int KC = (nb + kCB - 1) / kCB;
-  const int RT = I >> 4;
+  const int T = H >> 6;                           // tiles per tile row (K = H)
+  const int KC = (T + CT - 1) / CT;               // chunks per unit
+  const int RT = I >> 4;                          // tile rows (units) per expert
+  const size_t expert_bytes = (size_t)RT * T * kTile;
   const int xstride = 2 * H + kXPad;
-  const size_t row_qs = (size_t)H / 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
 
   uint8_t* stages = smem;
   float* red = reinterpret_cast<float*>(smem + (size_t)ring * kStage);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)ring * kStage + gu_red_bytes(R));
-  uint64_t* empty = full + kMaxRing;
-  uint8_t* xs = smem + (size_t)ring * kStage + gu_red_bytes(R) + 64;
+  uint8_t* xs = smem + (size_t)ring * kStage + gu_red_bytes(R);
 
   if (tid == 0) {
     for (int s = 0; s < ring; ++s) {
-      mbar_init(&full[s], kFullArrivals);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
     for (int b = 0; b < 2; ++b) {
@@ -481,8 +516,6 @@ __global__ void __launch_bounds__(kGuThreads, 1) k3_gate_up(const __grid_constan
       mbar_init(&s_pempty[b], kReducerWarps);
     }
     fence_mbar_init();
-    if (boxed)
-      for (int i = 0; i < 4; ++i) { prefetch_tensormap(&a.wq[i]); prefetch_tensormap(&a.wsc[i]); }
   }
   // Activations -> shared memory, bf16 in MMA pair order (independent of the router).
 #pragma unroll 4
@@ -499,38 +532,28 @@ __global__ void __launch_bounds__(kGuThreads, 1) k3_gate_up(const __grid_constan
     bool routed = false;   // the router's results are known to be visible
     // Units of the shared expert need nothing from the router; a unit of a routed expert
     // waits for it (and so does the count of units, which needs the union size).
-    for (int f = 0;; ++f) {
-      const int n = (int)blockIdx.x + (f / KC) * G, c = f % KC;
-      const int u = n / RT, rti = n - u * RT;
+    int slot = 0, f = 0;
+    uint32_t phase = 0;    // ring cursor: stage f sits in `slot`, pass parity `phase`
+    for (int n = (int)blockIdx.x;; n += G) {
+      const int u = n / RT, rt = n - u * RT;
       if (u > 0 && !routed) { pdl_wait(); routed = true; }
       if (routed && n >= (1 + a.route->n_union) * RT) break;
-      const int slot = f % ring;
-      if (f >= ring && !mbar_wait(&empty[slot], ((f / ring) - 1) & 1, kWaitPolls)) timed_out = true;
-      uint8_t* st = stages + (size_t)slot * kStage;
-      const int row0 = (u == 0 ? 0 : a.route->expert[u - 1] * I) + rti * 16;
-      if (boxed) {
+      const uint8_t* gbase = (u == 0 ? a.sh_gate : a.gate + (size_t)a.route->expert[u - 1] * expert_bytes) +
+                             (size_t)rt * T * kTile;
+      const uint8_t* ubase = (u == 0 ? a.sh_up : a.up + (size_t)a.route->expert[u - 1] * expert_bytes) +
+                             (size_t)rt * T * kTile;
+      for (int c = 0; c < KC; ++c, ++f) {
+        if (f >= ring && !pipe_wait(&empty[slot], phase ^ 1u)) timed_out = true;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[slot], 2u * (Geo::kBoxQs + Geo::kBoxSc));
-          const int mi = u == 0 ? 2 : 0;
-          for (int m = 0; m < 2; ++m) {
-            tma_load_3d(st + m * Geo::kBoxQs, &a.wq[mi + m], 0, row0, c * (kCB / 8), &full[slot]);
-            tma_load_2d(st + 2 * Geo::kBoxQs + m * Geo::kBoxSc, &a.wsc[mi + m], c * kCB, row0,
-                        &full[slot]);
-          }
+          uint8_t* st = stages + (size_t)slot * kStage;
+          const uint32_t bytes = (uint32_t)min(CT, T - c * CT) * kTile;
+          mbar_arrive_expect_tx(&full[slot], 2u * bytes);
+          bulk_copy(st, gbase + (size_t)c * CT * kTile, bytes, &full[slot]);
+          bulk_copy(st + CT * kTile, ubase + (size_t)c * CT * kTile, bytes, &full[slot]);
         }
-      } else {
-        const Q4Ptr mg = u == 0 ? a.sh_gate : a.gate, mu = u == 0 ? a.sh_up : a.up;
-        const int cb = min(kCB, nb - c * kCB);
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * 16u * cb * 16u);
-        for (int m = 0; m < 2; ++m) {
-          const Q4Ptr mm = m ? mu : mg;
-          copy_rows(st + m * 16 * Geo::kQsPitch, Geo::kQsPitch,
-                    mm.qs + (size_t)row0 * row_qs + (size_t)c * kCB * 16, row_qs,
-                    st + Geo::kRowQs + m * 16 * Geo::kScPitch, Geo::kScPitch,
-                    mm.sc + (size_t)row0 * nb + c * kCB, nb, 16, cb, &full[slot], lane);
-        }
+        __syncwarp();
+        if (++slot == ring) { slot = 0; phase ^= 1u; }
       }
-      cp_async_mbar_arrive(&full[slot]);
     }
     if (!routed) pdl_wait();
   } else if (warp < kProducerWarp) {
@@ -538,100 +561,51 @@ __global__ void __launch_bounds__(kGuThreads, 1) k3_gate_up(const __grid_constan
     const RouteInfo* rt = a.route;
     const int n_units = (1 + rt->n_union) * RT;
     const int n_mine = (int)blockIdx.x < n_units ? (n_units - (int)blockIdx.x + G - 1) / G : 0;
-    const int total = n_mine * KC;
     const uint8_t* xrow = xs + min(g, R - 1) * xstride + q * 16;   // rows >= R: any finite row
-    // Byte offsets inside a stage (row g of the gate matrix; + m_q for up, + r8_q for row
-    // g + 8) of word q of this warp's block j, and of this warp's scales.
-    int woff[WB];
-    int m_q, r8_q, soff, m_s, r8_s;
-    if (boxed) {
-#pragma unroll
-      for (int j = 0; j < WB; ++j) {
-        const int b = WB * warp + j;
-        woff[j] = ((b >> 3) * 16 + g) * 128 + (((b & 7) ^ (g & 7)) << 4) + q * 4;
-      }
-      m_q = Geo::kBoxQs; r8_q = 8 * 128;
-      soff = 2 * Geo::kBoxQs + g * (kCB * 2) + warp * (2 * WB);
-      m_s = Geo::kBoxSc; r8_s = 8 * kCB * 2;
-    } else {
-#pragma unroll
-      for (int j = 0; j < WB; ++j) woff[j] = g * Geo::kQsPitch + (WB * warp + j) * 16 + q * 4;
-      m_q = 16 * Geo::kQsPitch; r8_q = 8 * Geo::kQsPitch;
-      soff = Geo::kRowQs + g * Geo::kScPitch + warp * (2 * WB);
-      m_s = 16 * Geo::kScPitch; r8_s = 8 * Geo::kScPitch;
-    }
     float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
-    int buf = 0;
-    for (int f = 0; f < total; ++f) {
-      const int slot = f % ring;
-      if (!mbar_wait(&full[slot], (f / ring) & 1, kWaitPolls)) timed_out = true;
-      const uint8_t* st = stages + (size_t)slot * kStage;
-      const int c = f % KC;
-      const int cb = min(kCB, nb - c * kCB);
-      const int nv = max(0, min(WB, cb - WB * warp));   // this warp's blocks in the chunk
-      if (nv > 0) {
-        // fp16 scales of rows g, g + 8 (gate, up) for the warp's WB blocks
-        uint32_t sw[4][WB / 2];
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int unit = 0; unit < n_mine; ++unit) {
+      for (int c = 0; c < KC; ++c) {
+        if (!pipe_wait(&full[slot], phase)) timed_out = true;
+        const uint8_t* st = stages + (size_t)slot * kStage;
+        const int ct = min(CT, T - c * CT);
+        const uint8_t* xc = xrow + (size_t)c * CT * 128;
 #pragma unroll
-        for (int m4 = 0; m4 < 4; ++m4) {
-          const uint8_t* p = st + soff + (m4 >> 1) * m_s + (m4 & 1) * r8_s;
-          if constexpr (WB == 8) {
-            const uint4 v = *reinterpret_cast<const uint4*>(p);
-            sw[m4][0] = v.x; sw[m4][1] = v.y; sw[m4][2] = v.z; sw[m4][3] = v.w;
-          } else {
-            const uint2 v = *reinterpret_cast<const uint2*>(p);
-            sw[m4][0] = v.x; sw[m4][1] = v.y;
+        for (int tt = 0; tt < TPW; ++tt) {
+          const int t = warp * TPW + tt;
+          if (t < ct) {
+            const uint8_t* xb = xc + t * 128;   // blocks 2t, 2t + 1 of the chunk
+            const uint4 X0 = lds128(xb), X1 = lds128(xb + 64);
+            const uint8_t* tg = st + t * kTile;
+            const uint8_t* tu = st + (CT + t) * kTile;
+            const uint4 Wg = lds128(tg + lane * 16), Wu = lds128(tu + lane * 16);
+            const uint2 Sg = lds64(tg + kTileNib + g * 8), Su = lds64(tu + kTileNib + g * 8);
+            q4_tile_mma(Wg, Sg, X0, X1, ag);
+            q4_tile_mma(Wu, Su, X0, X1, au);
           }
-        }
-        const uint8_t* xb = xrow + (c * kCB + WB * warp) * 64;
-#pragma unroll
-        for (int jp = 0; jp < WB / 2; ++jp) {
-          const float2 sg0 = __half22float2(*reinterpret_cast<const __half2*>(&sw[0][jp]));
-          const float2 sg8 = __half22float2(*reinterpret_cast<const __half2*>(&sw[1][jp]));
-          const float2 su0 = __half22float2(*reinterpret_cast<const __half2*>(&sw[2][jp]));
-          const float2 su8 = __half22float2(*reinterpret_cast<const __half2*>(&sw[3][jp]));
-#pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            const int j = 2 * jp + e2;
-            if (j < nv) {
-              const float g0 = e2 ? sg0.y : sg0.x, g8 = e2 ? sg8.y : sg8.x;
-              const float u0 = e2 ? su0.y : su0.x, u8 = e2 ? su8.y : su8.x;
-              const uint4 X = *reinterpret_cast<const uint4*>(xb + j * 64);
-              const uint8_t* w = st + woff[j];
-              float d[4];
-              q4_block_mma(lds32(w), lds32(w + r8_q), X, d);
-              ag[0] = __fmaf_rn(g0, d[0], ag[0]); ag[1] = __fmaf_rn(g0, d[1], ag[1]);
-              ag[2] = __fmaf_rn(g8, d[2], ag[2]); ag[3] = __fmaf_rn(g8, d[3], ag[3]);
-              q4_block_mma(lds32(w + m_q), lds32(w + m_q + r8_q), X, d);
-              au[0] = __fmaf_rn(u0, d[0], au[0]); au[1] = __fmaf_rn(u0, d[1], au[1]);
-              au[2] = __fmaf_rn(u8, d[2], au[2]); au[3] = __fmaf_rn(u8, d[3], au[3]);
-            }
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the slot
-      if (c == KC - 1) {
-        // partials [warp][gate/up][row][col] (cols < R only) into buffer unit & 1, once
-        // the reducers are done with the unit that used it before
-        const int unit = f / KC;
-        if (unit >= 2 && !mbar_wait(&s_pempty[buf], ((unit >> 1) - 1) & 1, kWaitPolls))
-          timed_out = true;
-        float* rb = red + (size_t)buf * kConsumerWarps * 2 * 16 * R;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int col = 2 * q + (e & 1), row = g + ((e & 2) ? 8 : 0);
-          if (col < R) {
-            rb[((warp * 2 + 0) * 16 + row) * R + col] = ag[e];
-            rb[((warp * 2 + 1) * 16 + row) * R + col] = au[e];
-          }
-          ag[e] = 0.f;
-          au[e] = 0.f;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_pfull[buf]);
-        buf ^= 1;
+        if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the slot
+        if (++slot == ring) { slot = 0; phase ^= 1u; }
       }
+      // partials [warp][gate/up][row][col] (cols < R only) into buffer unit & 1, once the
+      // reducers are done with the unit that used it before
+      const int buf = unit & 1;
+      if (unit >= 2 && !pipe_wait(&s_pempty[buf], ((unit >> 1) - 1) & 1)) timed_out = true;
+      float* rb = red + (size_t)buf * kConsumerWarps * 2 * 16 * R;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int col = 2 * q + (e & 1), row = g + ((e & 2) ? 8 : 0);
+        if (col < R) {
+          rb[((warp * 2 + 0) * 16 + row) * R + col] = ag[e];
+          rb[((warp * 2 + 1) * 16 + row) * R + col] = au[e];
+        }
+        ag[e] = 0.f;
+        au[e] = 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_pfull[buf]);
     }
   } else {
     // Reducers: for each unit of this CTA, in order, the 16 warps' partials are added in
@@ -643,7 +617,7 @@ __global__ void __launch_bounds__(kGuThreads, 1) k3_gate_up(const __grid_constan
     int unit = 0;
     for (int n = (int)blockIdx.x; n < n_units; n += G, ++unit) {
       const int b = unit & 1;
-      if (!mbar_wait(&s_pfull[b], (unit >> 1) & 1, kWaitPolls)) {
+      if (!pipe_wait(&s_pfull[b], (unit >> 1) & 1)) {
         timed_out = true;
         break;
       }
@@ -673,166 +647,167 @@ __global__ void __launch_bounds__(kGuThreads, 1) k3_gate_up(const __grid_constan
 }
 
 // ---------------------------------------------------------------------------------
-// K4: down projection. A unit is (expert slot u, a group of RS consecutive rows of H);
-// the 16 consumer warps split a stage (one K chunk of up to 4096 values of the group's
-// rows) into RS/16 row tiles x WK K slices of BPS blocks (16 where two stages fit, else 8;
-// the larger slice halves the per-stage overhead per weight byte). CTA b takes a contiguous range of
-// units, so consecutive stages mostly belong to one expert and its h (the B operand, kept
-// in shared memory) is reloaded only when the expert or the chunk changes. The WK slice
-// partials of a row tile are added in slice order and written to o[row][slot] (fp32);
-// K5 combines. The weights do not depend on the gate/up kernel, so the producer starts
-// streaming them before that kernel has finished; only h waits for it.
+// K4: down projection and combine. A unit is (expert slot u, row group of 16 tile rows =
+// 256 rows of H); consumer warp w owns tile row w of the group for the whole unit, so its
+// fp32 sums need no reduction with other warps. A stage is one K chunk of KT tiles of the
+// group's 16 tile rows, one contiguous run (the down matrices keep their tile rows in
+// groups of 16, K tile first within a group): one bulk copy. CTA b takes a contiguous
+// range of units, so consecutive stages mostly belong to one expert and its h (the B
+// operand, kept in shared memory in MMA pair order) is reloaded only when the expert
+// changes. At the end of a unit each warp writes o[row][slot] (fp32) for the rows that use
+// the expert; a counting warp then counts the unit against its row group (fence, atomic
+// add) while the consumers go on, and after its last unit the CTA that completed a row
+// group (every slot's unit done; nobody waits) writes y = bf16_rne(o_shared +
+// sum_j w_j o_j) for the group's rows, j in rank order.
+// The weights do not depend on the gate/up kernel, so the producer starts streaming them
+// before that kernel has finished; only h waits for it.
 // ---------------------------------------------------------------------------------
-struct DownGeom {
-  int nb, KC, cbmax, WK, TPS, RS, NGR, qs_pitch, sc_pitch, h_pitch, stage_bytes, boxed;
-};
+#ifndef DSMOE_DOWN_KT
+#define DSMOE_DOWN_KT 4
+#endif
+constexpr int kDownKT = DSMOE_DOWN_KT;   // tiles per tile row per stage
+constexpr int kGroupRows = kDownGroup;   // tile rows per unit (one per consumer warp)
+constexpr int kDownStage = kGroupRows * kDownKT * kTile;   // 36,864 bytes
 
-__host__ __device__ inline DownGeom down_geom(int H, int I, int bps) {
-  DownGeom d{};
-  d.nb = I >> 5;
-  d.KC = (d.nb + kChunkBlocks - 1) / kChunkBlocks;
-  d.cbmax = d.nb < kChunkBlocks ? d.nb : kChunkBlocks;
-  const int slices = (d.cbmax + bps - 1) / bps;
-  d.WK = slices <= 1 ? 1 : (slices <= 2 ? 2 : (slices <= 4 ? 4 : (slices <= 8 ? 8 : 16)));
-  d.TPS = kConsumerWarps / d.WK;
-  d.RS = 16 * d.TPS;
-  d.NGR = (H + d.RS - 1) / d.RS;
-  d.boxed = (d.nb % 8) == 0;            // rows of whole 128-byte chunks (and scale rows of 16 B)
-  d.qs_pitch = d.cbmax * 16 + 16;       // row path
-  d.sc_pitch = (int)round_up((size_t)d.cbmax * 2, 16) + 16;
-  d.h_pitch = d.cbmax * 64 + 64;
-  d.stage_bytes = (int)round_up((size_t)d.RS * (d.qs_pitch + d.sc_pitch), 1024);
-  return d;
-}
-
-struct alignas(64) DownArgs {
-  CUtensorMap wq[2];   // boxed path: nibbles of down, sh_down
-  CUtensorMap wsc[2];  // boxed path: their scales
-  Q4Ptr down, sh_down;
+struct DownArgs {
+  const uint8_t* down;      // tiles [E][H/16][I/64]
+  const uint8_t* sh_down;   // tiles [H/16][I/64]
   const uint16_t* h;
   const RouteInfo* route;
-  float* opart;
+  const float* topk_w;
+  float* opart;             // [R][1+k][H] expert outputs
+  uint32_t* counts;         // [ceil(H/256)] units completed per row group (zeroed per call)
+  uint16_t* y;
   uint32_t* status;
-  int R, H, I, k, ring, boxed;
+  int R, H, I, k, ring;
 };
 
-__host__ __device__ constexpr size_t dn_red_bytes(int R) {
-  return 2ull * kConsumerWarps * 16 * (size_t)R * 4;
-}
+__host__ __device__ constexpr int down_hpitch(int I) { return 2 * I + kXPad; }
 
-template <int BPS>
-__global__ void __launch_bounds__(kMmaThreads, 1) k4_down(const __grid_constant__ DownArgs a) {
-  extern __shared__ uint8_t smem_raw[];
+constexpr int kCountWarp = kProducerWarp + 1;
+constexpr int kDownThreads = kMmaThreads + 32;   // + the counting warp
+constexpr int kMaxGroupsPerCta = 64;             // row groups a CTA can complete (H <= 16384)
+
+__global__ void __launch_bounds__(kDownThreads, 1) k4_down(const DownArgs a) {
+  __shared__ __align__(8) uint64_t full[kMaxRing], empty[kMaxRing];
+  // a unit's outputs written (16 consumer warps) / taken over by the counting warp (1)
+  __shared__ __align__(8) uint64_t s_udone[2], s_ufree[2];
   __shared__ uint32_t s_rowmask[kMaxUnion];
   __shared__ __align__(8) int8_t s_slot[kMaxUnion][8];
+  __shared__ int s_done[kMaxGroupsPerCta];   // row groups this CTA completed
+  __shared__ int s_ndone;
+  extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int R = a.R, H = a.H, I = a.I, k = a.k, ring = a.ring;
-  const DownGeom dg = down_geom(H, I, BPS);
+  const int T = I >> 6;                              // tiles per tile row (K = I)
+  const int KC = (T + kDownKT - 1) / kDownKT;        // chunks per unit
+  const int RTt = H >> 4;                            // tile rows per expert
+  const int NGR = (RTt + kGroupRows - 1) / kGroupRows;
+  const size_t expert_bytes = (size_t)RTt * T * kTile;
+  const int hpitch = down_hpitch(I);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
-  const size_t row_qs = (size_t)I / 2;
 
   uint8_t* stages = smem;
-  uint8_t* hs = smem + (size_t)ring * dg.stage_bytes;                      // [8][h_pitch]
-  float* red = reinterpret_cast<float*>(hs + (size_t)8 * dg.h_pitch);
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + dn_red_bytes(R));
-  uint64_t* empty = full + kMaxRing;
+  uint8_t* hs = smem + (size_t)ring * kDownStage;   // [8][hpitch]
 
   if (tid == 0) {
     for (int s = 0; s < ring; ++s) {
-      mbar_init(&full[s], kFullArrivals);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_udone[b], kConsumerWarps);
+      mbar_init(&s_ufree[b], 1);
+    }
+    s_ndone = 0;
     fence_mbar_init();
-    if (a.boxed)
-      for (int i = 0; i < 2; ++i) { prefetch_tensormap(&a.wq[i]); prefetch_tensormap(&a.wsc[i]); }
   }
   __syncthreads();
 
   // The route was complete before the gate/up kernel passed its own wait, which precedes
   // the launch of this grid; h is waited for below.
   const RouteInfo* rt = a.route;
-  const int n_units = (1 + rt->n_union) * dg.NGR;
+  const int n_union = rt->n_union;
+  const int n_units = (1 + n_union) * NGR;
   const int G = gridDim.x;
   const int u_begin = (int)(((long long)blockIdx.x * n_units) / G);
   const int u_end = (int)(((long long)(blockIdx.x + 1) * n_units) / G);
-  const int total = (u_end - u_begin) * dg.KC;
-  const int box_qs = dg.RS * dg.cbmax * 16, box_sc = dg.RS * dg.cbmax * 2;
   bool timed_out = false;
 
   if (warp == kProducerWarp) {
-    for (int f = 0; f < total; ++f) {
-      const int slot = f % ring;
-      if (f >= ring && !mbar_wait(&empty[slot], ((f / ring) - 1) & 1, kWaitPolls)) timed_out = true;
-      uint8_t* st = stages + (size_t)slot * dg.stage_bytes;
-      const int n = u_begin + f / dg.KC, c = f % dg.KC;
-      const int u = n / dg.NGR, grp = n - u * dg.NGR;
-      const int r0 = grp * dg.RS;
-      const int row0 = (u == 0 ? 0 : rt->expert[u - 1] * H) + r0;
-      if (a.boxed) {
+    int slot = 0, f = 0;
+    uint32_t phase = 0;    // ring cursor
+    for (int n = u_begin; n < u_end; ++n) {
+      const int u = n / NGR, rg = n - u * NGR;
+      const int rig = min(kGroupRows, RTt - rg * kGroupRows);   // tile rows in the group
+      const uint8_t* gbase = (u == 0 ? a.sh_down : a.down + (size_t)rt->expert[u - 1] * expert_bytes) +
+                             (size_t)rg * kGroupRows * T * kTile;
+      for (int c = 0; c < KC; ++c, ++f) {
+        if (f >= ring && !pipe_wait(&empty[slot], phase ^ 1u)) timed_out = true;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[slot], (uint32_t)(box_qs + box_sc));
-          const int mi = u == 0 ? 1 : 0;
-          tma_load_3d(st, &a.wq[mi], 0, row0, c * (kChunkBlocks / 8), &full[slot]);
-          tma_load_2d(st + box_qs, &a.wsc[mi], c * kChunkBlocks, row0, &full[slot]);
+          // the group's tiles of K tiles c KT .. c KT + kt - 1: one contiguous run
+          const uint32_t bytes = (uint32_t)(min(kDownKT, T - c * kDownKT) * rig * kTile);
+          mbar_arrive_expect_tx(&full[slot], bytes);
+          bulk_copy(stages + (size_t)slot * kDownStage,
+                    gbase + (size_t)c * kDownKT * rig * kTile, bytes, &full[slot]);
         }
-      } else {
-        const Q4Ptr m = u == 0 ? a.sh_down : a.down;
-        const int nrows = min(dg.RS, H - r0);
-        const int cb = min(kChunkBlocks, dg.nb - c * kChunkBlocks);
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)nrows * cb * 16u);
-        copy_rows(st, dg.qs_pitch, m.qs + (size_t)row0 * row_qs + (size_t)c * kChunkBlocks * 16,
-                  row_qs, st + dg.RS * dg.qs_pitch, dg.sc_pitch,
-                  m.sc + (size_t)row0 * dg.nb + c * kChunkBlocks, dg.nb, nrows, cb, &full[slot],
-                  lane);
+        __syncwarp();
+        if (++slot == ring) { slot = 0; phase ^= 1u; }
       }
-      cp_async_mbar_arrive(&full[slot]);
     }
     pdl_wait();
+  } else if (warp == kCountWarp) {
+    // Counts each finished unit against its row group: once the consumers' outputs of the
+    // unit are written (mbarrier, CTA scope), a fence makes them visible device-wide, then
+    // the atomic count; the unit that completes a group (1 + n_union units, nobody waits)
+    // records it for the combine below.
+    pdl_wait();
+    int j = 0;
+    for (int n = u_begin; n < u_end; ++n, ++j) {
+      const int b = j & 1;
+      if (!pipe_wait(&s_udone[b], (j >> 1) & 1)) timed_out = true;
+      if (lane == 0) {
+        const int rg = n % NGR;
+        __threadfence();
+        const unsigned prev = atomicAdd(&a.counts[rg], 1u);
+        if (prev == (unsigned)n_union) {
+          __threadfence();
+          if (s_ndone < kMaxGroupsPerCta) s_done[s_ndone++] = rg;
+          else flag_status(a.status, kStatusCheck);
+        }
+        mbar_arrive(&s_ufree[b]);
+      }
+      __syncwarp();
+    }
   } else {
     pdl_wait();      // h is complete from here on
-    // the union's row masks and rank slots, read every stage, kept in shared memory
-    for (int i = tid; i < rt->n_union; i += kConsumers) {
+    // the union's row masks and rank slots, read every unit, kept in shared memory
+    for (int i = tid; i < n_union; i += kConsumers) {
       s_rowmask[i] = rt->rowmask[i];
       *reinterpret_cast<uint2*>(s_slot[i]) = *reinterpret_cast<const uint2*>(rt->slot[i]);
     }
     consumer_sync();
-    const int rtl = warp / dg.WK, ks = warp - rtl * dg.WK;   // row tile, K slice
-    const int r = rtl * 16 + g;                              // this lane's first row
-    // byte offset in a stage of word q of block j of this warp's slice (row r; + r8_q for
-    // row r + 8), and of the slice's scales of row r (+ r8_s for row r + 8)
-    auto woff = [&](int j) {
-      const int b = ks * BPS + j;
-      return a.boxed ? ((b >> 3) * dg.RS + r) * 128 + (((b & 7) ^ (r & 7)) << 4) + q * 4
-                     : r * dg.qs_pitch + b * 16 + q * 4;
-    };
-    const int r8_q = a.boxed ? 8 * 128 : 8 * dg.qs_pitch;
-    const int soff = a.boxed ? box_qs + r * (dg.cbmax * 2) + ks * (2 * BPS)
-                             : dg.RS * dg.qs_pitch + r * dg.sc_pitch + ks * (2 * BPS);
-    const int r8_s = a.boxed ? 8 * dg.cbmax * 2 : 8 * dg.sc_pitch;
-    int h_tag = -1;     // (expert slot, chunk) whose h is staged
-    int buf = 0;
+    const uint8_t* hrow = hs + g * hpitch + q * 16;   // rows >= R or unused: never read out
+    int h_u = -1;       // expert slot whose h is staged
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int f = 0; f < total; ++f) {
-      const int slot = f % ring;
-      const int n = u_begin + f / dg.KC, c = f % dg.KC;
-      const int u = n / dg.NGR, grp = n - u * dg.NGR;
-      const int cb = min(kChunkBlocks, dg.nb - c * kChunkBlocks);
+    int slot = 0, j = 0;
+    uint32_t phase = 0;
+    for (int n = u_begin; n < u_end; ++n, ++j) {
+      const int u = n / NGR, rg = n - u * NGR;
+      const int rig = min(kGroupRows, RTt - rg * kGroupRows);
       const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : s_rowmask[u - 1];
-      const int tag = u * dg.KC + c;
-      if (tag != h_tag) {
-        // h of the expert's rows for this chunk: [verify row][values], 16-byte pieces, then
-        // each piece put in MMA pair order in place. Rows that do not use the expert keep
-        // stale values; their MMA columns are never read.
+      if (u != h_u) {
+        // h of the expert's rows: [verify row][values], 16-byte pieces, then each piece
+        // put in MMA pair order in place. Rows that do not use the expert keep stale
+        // values; their MMA columns are never read.
         consumer_sync();   // every consumer is done with the previous h
-        const int per_row = cb * 4;
+        const int per_row = I / 8;
         for (int p = tid; p < R * per_row; p += kConsumers) {
           const int rr = p / per_row, pp = p - rr * per_row;
           if ((rowmask >> rr) & 1u) {
             const int slot_r = (u == 0) ? 0 : s_slot[u - 1][rr];
-            cp_async16(hs + rr * dg.h_pitch + pp * 16,
-                       a.h + ((size_t)rr * (1 + k) + slot_r) * I + c * (kChunkBlocks * 32) + pp * 8,
-                       true);
+            cp_async16(hs + rr * hpitch + pp * 16, a.h + ((size_t)rr * (1 + k) + slot_r) * I + pp * 8);
           }
         }
         cp_async_commit();
@@ -840,108 +815,73 @@ __global__ void __launch_bounds__(kMmaThreads, 1) k4_down(const __grid_constant_
         for (int p = tid; p < R * per_row; p += kConsumers) {
           const int rr = p / per_row, pp = p - rr * per_row;
           if ((rowmask >> rr) & 1u) {
-            uint4* hp = reinterpret_cast<uint4*>(hs + rr * dg.h_pitch + pp * 16);
+            uint4* hp = reinterpret_cast<uint4*>(hs + rr * hpitch + pp * 16);
             *hp = pair_order(*hp);
           }
         }
         consumer_sync();
-        h_tag = tag;
+        h_u = u;
       }
-      if (!mbar_wait(&full[slot], (f / ring) & 1, kWaitPolls)) timed_out = true;
-      const uint8_t* st = stages + (size_t)slot * dg.stage_bytes;
-      const int row_t = grp * dg.RS + rtl * 16;         // first row of this warp's tile
-      const int nv = max(0, min(BPS, cb - BPS * ks));
-      if (nv > 0 && row_t < H) {
-        const uint8_t* hb = hs + g * dg.h_pitch + ks * (BPS * 64) + q * 16;
-        // four blocks at a time: scales, activations and weights loaded before the MMAs
+      const int tr = rg * kGroupRows + warp;              // this warp's tile row
+      for (int c = 0; c < KC; ++c) {
+        if (!pipe_wait(&full[slot], phase)) timed_out = true;
+        const uint8_t* st = stages + (size_t)slot * kDownStage;
+        const int kt = min(kDownKT, T - c * kDownKT);
+        if (warp < rig) {
+          const uint8_t* xc = hrow + (size_t)c * kDownKT * 128;
 #pragma unroll
-        for (int j0 = 0; j0 < BPS; j0 += 4) {
-          if (j0 < nv) {
-            float s0[4], s8[4];
-            widen_scales(*reinterpret_cast<const uint2*>(st + soff + 2 * j0), s0);
-            widen_scales(*reinterpret_cast<const uint2*>(st + soff + r8_s + 2 * j0), s8);
-            uint4 X[4];
-            uint32_t wl[4], wh[4];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              X[jj] = *reinterpret_cast<const uint4*>(hb + (j0 + jj) * 64);
-              const uint8_t* w = st + woff(j0 + jj);
-              wl[jj] = lds32(w);
-              wh[jj] = lds32(w + r8_q);
-            }
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              if (j0 + jj < nv) {
-                float d[4];
-                q4_block_mma(wl[jj], wh[jj], X[jj], d);
-                acc[0] = __fmaf_rn(s0[jj], d[0], acc[0]); acc[1] = __fmaf_rn(s0[jj], d[1], acc[1]);
-                acc[2] = __fmaf_rn(s8[jj], d[2], acc[2]); acc[3] = __fmaf_rn(s8[jj], d[3], acc[3]);
-              }
+          for (int jj = 0; jj < kDownKT; ++jj) {
+            if (jj < kt) {
+              const uint8_t* tp = st + (jj * rig + warp) * kTile;
+              const uint4 W = lds128(tp + lane * 16);
+              const uint2 S = lds64(tp + kTileNib + g * 8);
+              const uint8_t* xb = xc + jj * 128;   // blocks 2t, 2t + 1
+              q4_tile_mma(W, S, lds128(xb), lds128(xb + 64), acc);
             }
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (++slot == ring) { slot = 0; phase ^= 1u; }
       }
+      // the unit is done: this warp's rows, once the counting warp has taken over the unit
+      // two before (its outputs are counted before new ones are announced)
+      const int b = j & 1;
+      if (j >= 2 && !pipe_wait(&s_ufree[b], ((j >> 1) - 1) & 1)) timed_out = true;
+      if (warp < rig) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int col = 2 * q + (e & 1), row = tr * 16 + g + ((e & 2) ? 8 : 0);
+          if (col < R && ((rowmask >> col) & 1u)) {
+            const int slot_c = (u == 0) ? 0 : s_slot[u - 1][col];
+            a.opart[((size_t)col * (1 + k) + slot_c) * H + row] = acc[e];
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] = 0.f;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
-      if (c == dg.KC - 1) {
-        // The WK slice warps of this row tile add their partials in slice order (a named
-        // barrier per row tile, so the tiles do not wait for one another); with one slice
-        // the warp writes its rows directly.
-        if (dg.WK == 1) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int col = 2 * q + (e & 1), row = row_t + g + ((e & 2) ? 8 : 0);
-            if (col < R && row < H && ((rowmask >> col) & 1u)) {
-              const int slot_c = (u == 0) ? 0 : s_slot[u - 1][col];
-              a.opart[((size_t)col * (1 + k) + slot_c) * H + row] = __fadd_rn(0.f, acc[e]);
-            }
-            acc[e] = 0.f;
-          }
-        } else {
-          float* rb = red + (size_t)buf * kConsumerWarps * 16 * R;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int col = 2 * q + (e & 1), row = g + ((e & 2) ? 8 : 0);
-            if (col < R) rb[(warp * 16 + row) * R + col] = acc[e];
-            acc[e] = 0.f;
-          }
-          const int gthreads = dg.WK * 32, gt = tid - rtl * gthreads;
-          asm volatile("bar.sync %0, %1;" ::"r"(2 + rtl), "r"(gthreads) : "memory");
-          for (int t = gt; t < 16 * R; t += gthreads) {
-            const int rr = t / R, col = t - rr * R;
-            const int row = row_t + rr;
-            if (row < H && ((rowmask >> col) & 1u)) {
-              float o = 0.f;
-              for (int s = 0; s < dg.WK; ++s)
-                o = __fadd_rn(o, rb[((rtl * dg.WK + s) * 16 + rr) * R + col]);
-              const int slot_c = (u == 0) ? 0 : s_slot[u - 1][col];
-              a.opart[((size_t)col * (1 + k) + slot_c) * H + row] = o;
-            }
-          }
-        }
-        buf ^= 1;
-      }
+      if (lane == 0) mbar_arrive(&s_udone[b]);
+    }
+  }
+  // The row groups whose last unit this CTA counted: every slot's rows are written, so
+  // combine them, rank order (all warps of the CTA).
+  __syncthreads();
+  for (int d = 0; d < s_ndone; ++d) {
+    const int rg = s_done[d];
+    const int r0 = rg * kGroupRows * 16;
+    const int nrows = min(kGroupRows * 16, H - r0);
+    for (int i = tid; i < R * nrows; i += kDownThreads) {
+      const int r = i / nrows, row = r0 + (i - r * nrows);
+      const float* o = a.opart + (size_t)r * (1 + k) * H + row;
+      float yv = __ldcg(o);
+      for (int jj = 0; jj < k; ++jj)
+        yv = __fmaf_rn(__ldcg(a.topk_w + r * k + jj), __ldcg(o + (size_t)(1 + jj) * H), yv);
+      a.y[(size_t)r * H + row] = f32_to_bf16_rne(yv);
     }
   }
   pdl_trigger();
   if (timed_out && lane == 0) flag_status(a.status, kStatusTimeout);
-}
-
-// ---------------------------------------------------------------------------------
-// K5: combine. y[r] = bf16_rne(o_shared + sum_j w_j o_j), the sum taken in rank order j.
-// ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k5_combine(const float* __restrict__ opart,
-                                                  const float* __restrict__ topk_w,
-                                                  uint16_t* __restrict__ y, int R, int H,
-                                                  int k) {
-  pdl_wait();
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= R * H) return;
-  const int r = idx / H, col = idx - r * H;
-  const float* o = opart + (size_t)r * (1 + k) * H + col;
-  float yv = o[0];
-  for (int j = 0; j < k; ++j) yv = __fmaf_rn(topk_w[r * k + j], o[(size_t)(1 + j) * H], yv);
-  y[idx] = f32_to_bf16_rne(yv);
 }
 
 template <typename K>
@@ -950,52 +890,47 @@ cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-
-template <int WB>
+template <int CT>
 size_t gate_up_smem(const MoeDims& d, int ring) {
-  return 1024 + (size_t)ring * GuGeom<WB>::kStage + gu_red_bytes(d.R) + 64 +
+  return 1024 + (size_t)ring * gu_stage_bytes<CT>() + gu_red_bytes(d.R) +
          (size_t)d.R * (2 * d.H + kXPad);
 }
 
-size_t down_smem(const MoeDims& d, int ring, int bps) {
-  const DownGeom g = down_geom(d.H, d.I, bps);
-  return 1024 + (size_t)ring * g.stage_bytes + (size_t)8 * g.h_pitch + dn_red_bytes(d.R) + 64;
+size_t down_smem(const MoeDims& d, int ring) {
+  return 1024 + (size_t)ring * kDownStage + (size_t)8 * down_hpitch(d.I);
 }
 
-// Deepest ring (4 .. 2 stages) whose shared memory fits; 0 if none does.
+// Deepest ring (kMaxRing .. lo stages) whose shared memory fits; 0 if none does.
+#ifndef DSMOE_RING_MAX
+#define DSMOE_RING_MAX kMaxRing
+#endif
 template <typename F>
-int pick_ring(F smem_of) {
-  for (int ring = kMaxRing; ring >= 2; --ring)
+int pick_ring(F smem_of, int lo = 2, int hi = DSMOE_RING_MAX) {
+  for (int ring = hi; ring >= lo; --ring)
     if (smem_of(ring) <= (size_t)device_max_smem_optin()) return ring;
   return 0;
 }
 
-template <int WB>
-cudaError_t launch_gate_up_wb(const MoeDims& d, GateUpArgs& a, int ring, cudaStream_t s) {
-  const size_t smem = gate_up_smem<WB>(d, ring);
-  cudaError_t err = set_smem(k3_gate_up<WB>, smem);
+template <int CT>
+cudaError_t launch_gate_up_ct(const MoeDims& d, GateUpArgs& a, int ring, cudaStream_t s) {
+  const size_t smem = gate_up_smem<CT>(d, ring);
+  cudaError_t err = set_smem(k3_gate_up<CT>, smem);
   if (err != cudaSuccess) return err;
   a.ring = ring;
-  if (a.boxed) {
-    const Q4Ptr mats[4] = {a.gate, a.up, a.sh_gate, a.sh_up};
-    for (int i = 0; i < 4; ++i) {
-      const uint64_t rows = (uint64_t)(i < 2 ? d.E : 1) * d.I;
-      if ((err = q4_maps(&a.wq[i], &a.wsc[i], mats[i], rows, d.H, 16, 16 * WB)) != cudaSuccess)
-        return err;
-    }
-  }
-  return launch_pdl(k3_gate_up<WB>, device_sm_count(), kGuThreads, smem, s, a);
+  return launch_pdl(k3_gate_up<CT>, device_sm_count(), kGuThreads, smem, s, a);
 }
 
 }  // namespace
 
-size_t gate_up_smem_bytes(const MoeDims& d) { return gate_up_smem<4>(d, 2); }
+size_t gate_up_smem_bytes(const MoeDims& d) { return gate_up_smem<16>(d, 2); }
 
 MoeLayout moe_layout(const MoeDims& d) {
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
   MoeLayout L{};
   size_t off = 0;
   L.header = off; off += 256;
+  const int ngr = ((d.H >> 4) + kGroupRows - 1) / kGroupRows;
+  L.counts = off; off += up(sizeof(uint32_t) * (size_t)ngr);
   L.zero_bytes = off;
   L.scores = off; off += up(sizeof(float) * (size_t)d.R * d.E);
   L.route = off; off += up(sizeof(RouteInfo));
@@ -1005,69 +940,67 @@ MoeLayout moe_layout(const MoeDims& d) {
   return L;
 }
 
-cudaError_t launch_router(const MoeDims& d, const uint16_t* x, const uint16_t* router_w,
-                          int32_t* topk_idx, float* topk_w, const MoeWorkspace& ws,
-                          cudaStream_t s) {
-  const int grid = (d.E + kRouterExperts - 1) / kRouterExperts;
-  auto* hdr = reinterpret_cast<WsHeader*>(ws.header);
-  if (d.E <= 12 * 32)
-    k1_router<12><<<grid, kRouterWarps * 32, 0, s>>>(x, d.R, d.H, router_w, d.E, d.k, ws.scores,
-                                                      topk_idx, topk_w, ws.route, hdr);
-  else
-    k1_router<kMaxExperts / 32><<<grid, kRouterWarps * 32, 0, s>>>(
-        x, d.R, d.H, router_w, d.E, d.k, ws.scores, topk_idx, topk_w, ws.route, hdr);
+cudaError_t launch_tile(const uint8_t* qs, const uint16_t* sc, int n_mats, int64_t rows,
+                        int K, int group, uint8_t* dst, cudaStream_t s) {
+  const int T = K / 64;
+  const int64_t TR = rows / 16;
+  const int64_t tiles = (int64_t)n_mats * TR * T;
+  const int64_t threads = tiles * 32;
+  const int64_t grid = (threads + 255) / 256;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > INT_MAX || TR > INT_MAX) return cudaErrorInvalidValue;
+  k0_q4_tile<<<(unsigned)grid, 256, 0, s>>>(qs, sc, tiles, (int)TR, T, K, group, dst);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gate_up(const MoeDims& d, const uint16_t* x, Q4Ptr gate, Q4Ptr up,
-                           Q4Ptr sh_gate, Q4Ptr sh_up, const MoeWorkspace& ws,
-                           cudaStream_t s) {
-  // Whole 4096-value chunks when they fit with a ring of at least 2, else half chunks.
-  const int ring8 = pick_ring([&](int r) { return gate_up_smem<8>(d, r); });
-  const int ring4 = pick_ring([&](int r) { return gate_up_smem<4>(d, r); });
-  if (ring8 == 0 && ring4 == 0) return cudaErrorInvalidConfiguration;
+cudaError_t launch_router(const MoeDims& d, const uint16_t* x, const uint16_t* router_w,
+                          int32_t* topk_idx, float* topk_w, const MoeWorkspace& ws,
+                          cudaStream_t s) {
+  // zero the header and the combine counts (a plain launch: it follows the stream's earlier
+  // work), then the router, which overlaps it
+  k0_clear<<<1, 256, 0, s>>>(ws.header, (int)(ws.zero_bytes / 4));
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const int grid = (d.E + kRouterExperts - 1) / kRouterExperts;
+  auto* hdr = reinterpret_cast<WsHeader*>(ws.header);
+  if (d.E <= 12 * 32)
+    return launch_pdl(k1_router<12>, grid, kRouterWarps * 32, 0, s, x, d.R, d.H, router_w, d.E,
+                      d.k, ws.scores, topk_idx, topk_w, ws.route, hdr);
+  return launch_pdl(k1_router<kMaxExperts / 32>, grid, kRouterWarps * 32, 0, s, x, d.R, d.H,
+                    router_w, d.E, d.k, ws.scores, topk_idx, topk_w, ws.route, hdr);
+}
+
+cudaError_t launch_gate_up(const MoeDims& d, const uint16_t* x, const uint8_t* gate,
+                           const uint8_t* up, const uint8_t* sh_gate, const uint8_t* sh_up,
+                           const MoeWorkspace& ws, cudaStream_t s) {
   GateUpArgs a{};
   a.gate = gate; a.up = up; a.sh_gate = sh_gate; a.sh_up = sh_up;
   a.x = x; a.route = ws.route; a.h = ws.h; a.status = ws.header;
   a.R = d.R; a.H = d.H; a.I = d.I; a.k = d.k;
-  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  a.boxed = (d.H % 256) == 0 && a16(gate.sc) && a16(up.sc) && a16(sh_gate.sc) && a16(sh_up.sc)
-                ? 1 : 0;
-  return ring8 ? launch_gate_up_wb<8>(d, a, ring8, s) : launch_gate_up_wb<4>(d, a, ring4, s);
+  // Chunks of 32 tiles when a ring of at least 3 of them fits, else chunks of 16.
+#ifndef DSMOE_GU_CT
+#define DSMOE_GU_CT 32
+#endif
+  const int ring32 = DSMOE_GU_CT == 32 ? pick_ring([&](int r) { return gate_up_smem<32>(d, r); }, 3) : 0;
+  if (ring32) return launch_gate_up_ct<32>(d, a, ring32, s);
+  const int ring16 = pick_ring([&](int r) { return gate_up_smem<16>(d, r); });
+  if (ring16) return launch_gate_up_ct<16>(d, a, ring16, s);
+  return cudaErrorInvalidConfiguration;
 }
 
-cudaError_t launch_down(const MoeDims& d, Q4Ptr down, Q4Ptr sh_down, const float* topk_w,
-                        uint16_t* y, const MoeWorkspace& ws, cudaStream_t s) {
-  // 16 blocks per K slice where two stages fit (fewer stage overheads per byte), else 8
-  int bps = 16;
-  int ring = pick_ring([&](int r) { return down_smem(d, r, 16); });
-  if (ring == 0) {
-    bps = 8;
-    ring = pick_ring([&](int r) { return down_smem(d, r, 8); });
-  }
+cudaError_t launch_down(const MoeDims& d, const uint8_t* down, const uint8_t* sh_down,
+                        const float* topk_w, uint16_t* y, const MoeWorkspace& ws,
+                        cudaStream_t s) {
+  const int ring = pick_ring([&](int r) { return down_smem(d, r); });
   if (ring == 0) return cudaErrorInvalidConfiguration;
-  const size_t smem = down_smem(d, ring, bps);
-  auto kern = bps == 16 ? k4_down<16> : k4_down<8>;
-  cudaError_t err = set_smem(kern, smem);
+  const size_t smem = down_smem(d, ring);
+  cudaError_t err = set_smem(k4_down, smem);
   if (err != cudaSuccess) return err;
   DownArgs a{};
-  a.down = down; a.sh_down = sh_down; a.h = ws.h; a.route = ws.route; a.opart = ws.opart;
-  a.status = ws.header;
+  a.down = down; a.sh_down = sh_down; a.h = ws.h; a.route = ws.route; a.topk_w = topk_w;
+  a.opart = ws.opart; a.counts = ws.counts; a.y = y; a.status = ws.header;
   a.R = d.R; a.H = d.H; a.I = d.I; a.k = d.k; a.ring = ring;
-  const DownGeom g = down_geom(d.H, d.I, bps);
-  a.boxed = g.boxed && (reinterpret_cast<uintptr_t>(down.sc) & 15u) == 0 &&
-            (reinterpret_cast<uintptr_t>(sh_down.sc) & 15u) == 0;
-  if (a.boxed) {
-    if ((err = q4_maps(&a.wq[0], &a.wsc[0], down, (uint64_t)d.E * d.H, d.I, g.RS, g.cbmax)) !=
-            cudaSuccess ||
-        (err = q4_maps(&a.wq[1], &a.wsc[1], sh_down, (uint64_t)d.H, d.I, g.RS, g.cbmax)) !=
-            cudaSuccess)
-      return err;
-  }
-  err = launch_pdl(kern, device_sm_count(), kMmaThreads, smem, s, a);
-  if (err != cudaSuccess) return err;
-  const int n = d.R * d.H;
-  return launch_pdl(k5_combine, (n + 255) / 256, 256, 0, s, ws.opart, topk_w, y, d.R, d.H, d.k);
+  return launch_pdl(k4_down, device_sm_count(), kDownThreads, smem, s, a);
 }
 
 }  // namespace dsmoe

@@ -50,6 +50,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// One poll that may suspend the thread for up to `hint_ns` nanoseconds; the thread resumes
+// as soon as the phase completes. True when the phase with parity `parity` is done.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait whose polls sleep instead of spinning (a waiting warp takes no issue slots
+// from the warps that compute): at most `polls` polls of at most `hint_ns` each.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t polls,
+                                                uint32_t hint_ns) {
+  for (uint32_t i = 0; i < polls; ++i)
+    if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
+  return false;
+}
+
 // --------------------------------------------------------------------- TMA ---------
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {

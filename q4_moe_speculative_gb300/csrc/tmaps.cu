@@ -52,16 +52,7 @@ cudaError_t cached_map(CUtensorMap* out, const MapKey& key) {
   const EncodeTiledFn f = encode_tiled();
   if (!f) return cudaErrorNotSupported;
   CUresult r;
-  if (key.kind == 0) {
-    // nibbles, viewed as [128-byte chunk][row][128 bytes]; 128-byte swizzle
-    const cuuint64_t dims[3] = {128, key.d1, key.d2};
-    const cuuint64_t strides[2] = {key.d0, 128};
-    const cuuint32_t box[3] = {128, key.b1, key.b2};
-    const cuuint32_t es[3] = {1, 1, 1};
-    r = f(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(key.base), dims, strides, box,
-          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  } else if (key.kind == 2) {
+  if (key.kind == 2) {
     // bf16 block keys [layer][block][128 values]: boxes of 64 values x b1 blocks x 1 layer,
     // 128-byte swizzle (the K-major operand layout of the tensor-core scorer)
     const cuuint64_t dims[3] = {128, key.d1, key.d2};
@@ -72,14 +63,7 @@ cudaError_t cached_map(CUtensorMap* out, const MapKey& key) {
           es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
-    // fp16 scales [row][nb]
-    const cuuint64_t dims[2] = {key.d0, key.d1};
-    const cuuint64_t strides[1] = {key.d0 * 2};
-    const cuuint32_t box[2] = {key.b0, key.b1};
-    const cuuint32_t es[2] = {1, 1};
-    r = f(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(key.base), dims, strides, box,
-          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return cudaErrorInvalidValue;
   }
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   std::lock_guard<std::mutex> lock(mu);
@@ -91,21 +75,6 @@ cudaError_t cached_map(CUtensorMap* out, const MapKey& key) {
 }
 
 }  // namespace
-
-// Maps of one Q4 matrix of `rows` rows of K values (K a multiple of 256), in boxes of
-// `box_rows` rows by `box_blocks` Q4 blocks (a multiple of 8).
-cudaError_t q4_maps(CUtensorMap* wq, CUtensorMap* wsc, Q4Ptr m, uint64_t rows, int K,
-                    int box_rows, int box_blocks) {
-  MapKey kq{};
-  kq.base = m.qs; kq.d0 = (uint64_t)K / 2; kq.d1 = rows; kq.d2 = (uint64_t)K / 256;
-  kq.b1 = (uint32_t)box_rows; kq.b2 = (uint32_t)box_blocks / 8; kq.kind = 0;
-  cudaError_t err = cached_map(wq, kq);
-  if (err != cudaSuccess) return err;
-  MapKey ks{};
-  ks.base = m.sc; ks.d0 = (uint64_t)K / 32; ks.d1 = rows;
-  ks.b0 = (uint32_t)box_blocks; ks.b1 = (uint32_t)box_rows; ks.kind = 1;
-  return cached_map(wsc, ks);
-}
 
 cudaError_t key_tile_map(CUtensorMap* out, const uint16_t* keys, int N, int L,
                          int64_t key_stride, int box_rows) {

@@ -20,7 +20,7 @@ def lib():
 def declared_functions():
     text = (ROOT / "include" / "dsmoe.h").read_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ds_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(ds_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_api():
@@ -50,7 +50,7 @@ FAKE = 1 << 20  # a 256-aligned address that is never dereferenced: validation f
 
 def fake_layer(H=4096, E=384, I=1024, k=8):
     from q4_moe_speculative_gb300 import _native as N
-    q = N.DsQ4(FAKE, FAKE)
+    q = N.DsQ4Tiled(FAKE)
     return N.DsMoeLayer(H, E, I, k, FAKE, q, q, q, q, q, q)
 
 
@@ -75,13 +75,13 @@ def test_moe_workspace_size_host_only(lib):
     (lambda s: setattr(s, "inter", 1000), 6, 1),
     (lambda s: setattr(s, "inter", 1056), 6, 2),         # multiple of 32, not of 64
     (lambda s: setattr(s, "hidden", 4064), 6, 2),
-    (lambda s: setattr(s.up, "sc", FAKE + 2), 6, 1),     # scales not 4-byte aligned
+    (lambda s: setattr(s.up, "tiles", FAKE + 8), 6, 1),  # tiles not 16-byte aligned
     (lambda s: setattr(s, "top_k", 0), 6, 1),
     (lambda s: setattr(s, "top_k", 17), 6, 1),
     (lambda s: setattr(s, "n_experts", 4), 6, 1),        # E < k
     (lambda s: setattr(s, "router_w", None), 6, 1),
-    (lambda s: setattr(s.gate, "qs", FAKE + 8), 6, 1),   # qs not 16-byte aligned
-    (lambda s: setattr(s.sh_down, "sc", None), 6, 1),
+    (lambda s: setattr(s.gate, "tiles", FAKE + 4), 6, 1),
+    (lambda s: setattr(s.sh_down, "tiles", None), 6, 1),
 ])
 def test_moe_forward_rejects_bad_arguments(lib, mutate, R, expect):
     st = fake_layer()
@@ -171,3 +171,29 @@ def test_noalloc_status_without_a_device(lib):
         pytest.skip("a GPU is present; the GPU tests cover the status query")
     assert lib.ds_noalloc_status(None) == 4   # DS_ERR_CUDA: no device to query
     assert lib.ds_moe_verify_forward_noalloc(None, FAKE, 1, FAKE, FAKE, FAKE, None) == 1
+
+
+def test_q4_tiled_bytes_and_tile_argument_checks(lib):
+    from q4_moe_speculative_gb300 import _native as N
+    assert lib.ds_q4_tiled_bytes(1024, 4096) == 1024 * 4096 * 9 // 16
+    assert lib.ds_q4_tiled_bytes(384 * 1024, 4096) == 384 * 1024 * 4096 * 9 // 16
+    for rows, K in ((1000, 4096), (1024, 4064), (0, 64), (16, 0), (-16, 64)):
+        assert lib.ds_q4_tiled_bytes(rows, K) == 0
+    src = N.DsQ4(FAKE, FAKE)
+    need = lib.ds_q4_tiled_bytes(64, 256)
+    assert lib.ds_q4_tile(src, 1, 64, 256, 1, FAKE, need - 1, None) == 3
+    assert lib.ds_q4_tile(src, 2, 64, 256, 16, FAKE, 2 * need - 1, None) == 3
+    assert lib.ds_q4_tile(src, 1, 60, 256, 1, FAKE, 1 << 30, None) == 1
+    assert lib.ds_q4_tile(src, 1, 64, 256, 1, FAKE + 8, need, None) == 1      # dst not 16-aligned
+    assert lib.ds_q4_tile(N.DsQ4(FAKE + 2, FAKE), 1, 64, 256, 1, FAKE, need, None) == 1
+    assert lib.ds_q4_tile(N.DsQ4(FAKE, None), 1, 64, 256, 1, FAKE, need, None) == 1
+    assert lib.ds_q4_tile(None, 1, 64, 256, 1, FAKE, need, None) == 1
+    assert lib.ds_q4_tile(src, 0, 64, 256, 1, FAKE, need, None) == 1          # no matrices
+    assert lib.ds_q4_tile(src, 1, 64, 256, 0, FAKE, need, None) == 1          # group 0
+
+
+def test_header_group_constant_matches_binding():
+    from q4_moe_speculative_gb300 import _native as N
+    text = (ROOT / "include" / "dsmoe.h").read_text()
+    m = re.search(r"#define DS_Q4_DOWN_GROUP (\d+)", text)
+    assert m and int(m.group(1)) == N.Q4_DOWN_GROUP
