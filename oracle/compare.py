@@ -196,12 +196,13 @@ def kernel_bands(H: int, I: int, k: int) -> tuple[float, float]:
     Gate/up: K = H is cut into chunks of 32 tiles (2 per consumer warp) or, when the larger
     stages do not fit, of 16 tiles (1 per warp), tiles of two blocks; a lane's chain holds
     its blocks of every chunk, and the 16 consumer warps' chains are added in warp order.
-    Down: one warp owns a 16-row tile row for all of K = I, so a lane's chain holds every
-    block of the row and no partial sums follow; the combine adds the k weighted expert
-    outputs to the shared one by k fmas in rank order."""
-    T_h, nb_i = H // 64, I // 32
+    Down: one warp owns a 16-row tile row for all of K = I in two chains (even and odd
+    tiles, two blocks each), added once; the combine adds the k weighted expert outputs to
+    the shared one by k fmas in rank order."""
+    T_h, T_i = H // 64, I // 64
     chain_gu = min(2 * T_h, max(4 * -(-T_h // 32), 2 * -(-T_h // 16)))
-    return accumulation_band(chain_gu, 16), accumulation_band(nb_i, 0) + 2.0 ** -24 * k
+    chain_dn = 2 * -(-T_i // 2)
+    return accumulation_band(chain_gu, 16), accumulation_band(chain_dn, 2) + 2.0 ** -24 * k
 
 
 def moe_check(host: dict, x_bits: np.ndarray, k: int, y_dev: np.ndarray, idx_dev: np.ndarray,

@@ -327,44 +327,41 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 
   if (tid < kMaxExperts / 32) ubits[tid] = 0u;
   if (warp < R) {
+    // Row r's top k by (score desc, expert asc): each round takes the warp-wide largest
+    // key (one reduction), then the smallest expert index holding it (a second one).
+    // Keys: score bits + 2 for a score (sigmoid scores lie in [0, 1], so the bits order
+    // like the values), 1 for NaN (from NaN inputs; ranks below every score), 0 for none.
     const int r = warp;
-    float v[KPER];
+    uint32_t key[KPER];
     bool bad = false;
 #pragma unroll
     for (int i = 0; i < KPER; ++i) {
       const int e2 = i * 32 + lane;
-      const float sv = e2 < E ? __ldcg(scores + r * E + e2) : -1.0f;
-      // sigmoid scores lie in [0, 1]; a NaN (from NaN inputs) ranks below every score
+      const float sv = e2 < E ? __ldcg(scores + r * E + e2) : 0.0f;
       bad |= (e2 < E) && !(sv >= 0.0f);
-      v[i] = (e2 >= E || sv >= 0.0f) ? sv : -0.5f;
+      key[i] = e2 >= E ? 0u : (sv >= 0.0f ? __float_as_uint(sv) + 2u : 1u);
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(&hdr->status, kStatusCheck);
     for (int j = 0; j < k; ++j) {
-      // this lane's best (value, register index) by a tree; on equal values the lower
-      // index (the left operand) wins
-      float bv[KPER];
+      // this lane's largest key and its lowest register index (a tree; ties keep the left)
+      uint32_t bk[KPER];
       int bi[KPER];
 #pragma unroll
-      for (int i = 0; i < KPER; ++i) { bv[i] = v[i]; bi[i] = i; }
+      for (int i = 0; i < KPER; ++i) { bk[i] = key[i]; bi[i] = i; }
 #pragma unroll
       for (int w = 1; w < KPER; w <<= 1)
 #pragma unroll
         for (int i = 0; i + w < KPER; i += 2 * w)
-          if (bv[i + w] > bv[i]) { bv[i] = bv[i + w]; bi[i] = bi[i + w]; }
-      float best = bv[0];
-      int bidx = bi[0] * 32 + lane;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-        if (ov > best || (ov == best && oi < bidx)) { best = ov; bidx = oi; }
-      }
+          if (bk[i + w] > bk[i]) { bk[i] = bk[i + w]; bi[i] = bi[i + w]; }
+      const uint32_t mk = __reduce_max_sync(0xffffffffu, bk[0]);
+      const uint32_t widx = __reduce_min_sync(
+          0xffffffffu, bk[0] == mk ? (uint32_t)(bi[0] * 32 + lane) : 0xFFFFFFFFu);
 #pragma unroll
       for (int i = 0; i < KPER; ++i)
-        if (i * 32 + lane == bidx) v[i] = -1.0f;   // taken
+        if ((uint32_t)(i * 32 + lane) == widx) key[i] = 0u;   // taken
       if (lane == 0) {
-        sel_e[r][j] = bidx;
-        sel_s[r][j] = best;
+        sel_e[r][j] = (int32_t)widx;
+        sel_s[r][j] = mk >= 2u ? __uint_as_float(mk - 2u) : -1.0f;
       }
     }
     __syncwarp();
@@ -781,16 +778,18 @@ __global__ void __launch_bounds__(kDownThreads, 1) k4_down(const DownArgs a) {
       __syncwarp();
     }
   } else {
-    pdl_wait();      // h is complete from here on
-    // the union's row masks and rank slots, read every unit, kept in shared memory
+    // the union's row masks and rank slots, read every unit, kept in shared memory (the
+    // route is visible already, see above)
     for (int i = tid; i < n_union; i += kConsumers) {
       s_rowmask[i] = rt->rowmask[i];
       *reinterpret_cast<uint2*>(s_slot[i]) = *reinterpret_cast<const uint2*>(rt->slot[i]);
     }
+    pdl_wait();      // h is complete from here on
     consumer_sync();
     const uint8_t* hrow = hs + g * hpitch + q * 16;   // rows >= R or unused: never read out
     int h_u = -1;       // expert slot whose h is staged
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // two chains: even (acc) and odd (acc2) tiles of the row, added once at the unit end
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
     int slot = 0, j = 0;
     uint32_t phase = 0;
     for (int n = u_begin; n < u_end; ++n, ++j) {
@@ -829,6 +828,7 @@ __global__ void __launch_bounds__(kDownThreads, 1) k4_down(const DownArgs a) {
         const int kt = min(kDownKT, T - c * kDownKT);
         if (warp < rig) {
           const uint8_t* xc = hrow + (size_t)c * kDownKT * 128;
+          static_assert(kDownKT % 2 == 0, "tiles alternate between the two chains");
 #pragma unroll
           for (int jj = 0; jj < kDownKT; ++jj) {
             if (jj < kt) {
@@ -836,7 +836,10 @@ __global__ void __launch_bounds__(kDownThreads, 1) k4_down(const DownArgs a) {
               const uint4 W = lds128(tp + lane * 16);
               const uint2 S = lds64(tp + kTileNib + g * 8);
               const uint8_t* xb = xc + jj * 128;   // blocks 2t, 2t + 1
-              q4_tile_mma(W, S, lds128(xb), lds128(xb + 64), acc);
+              if (jj & 1)
+                q4_tile_mma(W, S, lds128(xb), lds128(xb + 64), acc2);
+              else
+                q4_tile_mma(W, S, lds128(xb), lds128(xb + 64), acc);
             }
           }
         }
@@ -854,12 +857,12 @@ __global__ void __launch_bounds__(kDownThreads, 1) k4_down(const DownArgs a) {
           const int col = 2 * q + (e & 1), row = tr * 16 + g + ((e & 2) ? 8 : 0);
           if (col < R && ((rowmask >> col) & 1u)) {
             const int slot_c = (u == 0) ? 0 : s_slot[u - 1][col];
-            a.opart[((size_t)col * (1 + k) + slot_c) * H + row] = acc[e];
+            a.opart[((size_t)col * (1 + k) + slot_c) * H + row] = __fadd_rn(acc[e], acc2[e]);
           }
         }
       }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc[e] = acc2[e] = 0.f;
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_udone[b]);
     }
@@ -867,18 +870,25 @@ __global__ void __launch_bounds__(kDownThreads, 1) k4_down(const DownArgs a) {
   // The row groups whose last unit this CTA counted: every slot's rows are written, so
   // combine them, rank order (all warps of the CTA).
   __syncthreads();
-  for (int d = 0; d < s_ndone; ++d) {
+  const int per_group = R * kGroupRows * 16;   // outputs of a full group
+  for (int i = tid; i < s_ndone * per_group; i += kDownThreads) {
+    const int d = i / per_group, rem = i - d * per_group;
     const int rg = s_done[d];
     const int r0 = rg * kGroupRows * 16;
-    const int nrows = min(kGroupRows * 16, H - r0);
-    for (int i = tid; i < R * nrows; i += kDownThreads) {
-      const int r = i / nrows, row = r0 + (i - r * nrows);
-      const float* o = a.opart + (size_t)r * (1 + k) * H + row;
-      float yv = __ldcg(o);
-      for (int jj = 0; jj < k; ++jj)
-        yv = __fmaf_rn(__ldcg(a.topk_w + r * k + jj), __ldcg(o + (size_t)(1 + jj) * H), yv);
-      a.y[(size_t)r * H + row] = f32_to_bf16_rne(yv);
-    }
+    const int r = rem / (kGroupRows * 16), row = r0 + (rem - r * (kGroupRows * 16));
+    if (row >= H) continue;   // a short last group
+    const float* o = a.opart + (size_t)r * (1 + k) * H + row;
+    // every load first (one round trip), then the fma chain in rank order
+    float ov[kMaxTopK + 1], wv[kMaxTopK];
+#pragma unroll
+    for (int jj = 0; jj <= kMaxTopK; ++jj) ov[jj] = jj <= k ? __ldcg(o + (size_t)jj * H) : 0.0f;
+#pragma unroll
+    for (int jj = 0; jj < kMaxTopK; ++jj) wv[jj] = jj < k ? __ldcg(a.topk_w + r * k + jj) : 0.0f;
+    float yv = ov[0];
+#pragma unroll
+    for (int jj = 0; jj < kMaxTopK; ++jj)
+      if (jj < k) yv = __fmaf_rn(wv[jj], ov[1 + jj], yv);
+    a.y[(size_t)r * H + row] = f32_to_bf16_rne(yv);
   }
   pdl_trigger();
   if (timed_out && lane == 0) flag_status(a.status, kStatusTimeout);
