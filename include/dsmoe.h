@@ -115,9 +115,7 @@ ds_status ds_q4_tile(const ds_q4* src, int32_t n_mats, int64_t rows, int32_t K, 
  * router [E][H].
  * Limits: H and I multiples of 32, 64 <= H <= 16384, 64 <= I <= 8192, 1 <= top_k <= 16,
  * top_k <= E <= 1024 (else DS_ERR_INVALID_ARG). This build's kernels also need H and I
- * to be multiples of 64, and stage the R verify rows in shared memory, R * (2H + 64)
- * bytes beside the weight stages (e.g. H <= 10880 at R = 6); other valid layers get
- * DS_ERR_UNSUPPORTED. */
+ * to be multiples of 64 (else DS_ERR_UNSUPPORTED). */
 typedef struct {
   int32_t hidden;      /* H                                                   */
   int32_t n_experts;   /* E (routed)                                          */
@@ -153,16 +151,18 @@ size_t ds_moe_workspace_size(const ds_moe_layer* layer, int32_t R);
  *   workspace: >= ds_moe_workspace_size bytes, 256-byte aligned; its contents on entry
  *              are ignored and it must not be used by another call in flight.
  * Errors: DS_ERR_INVALID_ARG (null pointer, R outside 1..6, sizes outside the limits,
- * tiles not 16-byte aligned, misaligned x/y), DS_ERR_WORKSPACE, DS_ERR_UNSUPPORTED (H or I not a multiple of
- * 64, or R * H too large for the shared-memory staging), DS_ERR_CUDA. */
+ * tiles not 16-byte aligned, misaligned x/y), DS_ERR_WORKSPACE, DS_ERR_UNSUPPORTED (H or
+ * I not a multiple of 64, or the device's shared memory too small for the kernel's
+ * stages), DS_ERR_CUDA. */
 ds_status ds_moe_verify_forward(const ds_moe_layer* layer, const uint16_t* x, int32_t R,
                                 uint16_t* y, int32_t* topk_idx, float* topk_w,
                                 void* workspace, size_t ws_bytes, ds_stream_t stream);
 
 /* Same as ds_moe_verify_forward, and in addition records caller-created events on
  * `stream` right after each kernel of the call, for per-kernel timing:
- *   marks[0] after the router (and the prologue that zeroes the workspace header),
- *   marks[1] after gate+up+SwiGLU, marks[2] after the down projection and combine.
+ *   marks[0] after the prologue that zeroes the workspace header; marks[1] and marks[2]
+ *   after the layer's kernel (router, gate+up+SwiGLU, down projection and combine run as
+ *   one kernel, so there is nothing to record between them).
  * `marks` may be NULL and any entry may be NULL (skipped). The events must belong to the
  * stream's device. Errors as ds_moe_verify_forward; DS_ERR_CUDA if recording fails. */
 ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t* x,
@@ -199,8 +199,8 @@ size_t ds_moe_workspace_h_offset(const ds_moe_layer* layer, int32_t R);
  * Arguments, layouts and results as ds_moe_verify_forward; every output buffer is the
  * caller's. Errors: DS_ERR_WORKSPACE, decided on the host before any CUDA call, when
  * ds_moe_workspace_size(layer, R) > DS_NOALLOC_SCRATCH_BYTES; when that size is 0, the
- * status ds_moe_verify_forward gives the layer (DS_ERR_INVALID_ARG or DS_ERR_UNSUPPORTED); DS_ERR_CUDA when the array's address cannot be
- * resolved; otherwise those of ds_moe_verify_forward. The device-side outcomes
+ * status ds_moe_verify_forward gives the layer (DS_ERR_INVALID_ARG or
+ * DS_ERR_UNSUPPORTED); DS_ERR_CUDA when the array's address cannot be resolved; otherwise those of ds_moe_verify_forward. The device-side outcomes
  * (DS_ERR_TIMEOUT, DS_ERR_DEVICE_CHECK) are read with ds_noalloc_status().
  * The array's address is resolved once per device and kept for the life of the process;
  * a cudaDeviceReset() invalidates it, so the call must not be used after a reset. */

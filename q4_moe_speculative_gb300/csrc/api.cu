@@ -147,12 +147,11 @@ ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t
   const MoeLayout L = moe_layout(d);
   if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return DS_ERR_WORKSPACE;
   // The verify rows are staged in shared memory: R * (2H + 64) bytes beside the weight stages.
-  if (gate_up_smem_bytes(d) > (size_t)device_max_smem_optin()) return DS_ERR_UNSUPPORTED;
+  if (!moe_fits(d)) return DS_ERR_UNSUPPORTED;
 
   char* base = static_cast<char*>(workspace);
   MoeWorkspace ws{};
   ws.header = reinterpret_cast<uint32_t*>(base + L.header);
-  ws.counts = reinterpret_cast<uint32_t*>(base + L.counts);
   ws.zero_bytes = L.zero_bytes;
   ws.scores = reinterpret_cast<float*>(base + L.scores);
   ws.route = reinterpret_cast<RouteInfo*>(base + L.route);
@@ -161,16 +160,12 @@ ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t
 
   auto t = [](const ds_q4_tiled& m) { return static_cast<const uint8_t*>(m.tiles); };
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_router(d, x, layer->router_w, topk_idx, topk_w, ws, s) != cudaSuccess)
+  cudaEvent_t m0 = (marks && marks[0]) ? reinterpret_cast<cudaEvent_t>(marks[0]) : nullptr;
+  if (launch_moe(d, x, layer->router_w, t(layer->gate), t(layer->up), t(layer->down),
+                 t(layer->sh_gate), t(layer->sh_up), t(layer->sh_down), topk_idx, topk_w, y, ws,
+                 s, m0) != cudaSuccess)
     return DS_ERR_CUDA;
-  if (!mark(marks, 0, s)) return DS_ERR_CUDA;
-  if (launch_gate_up(d, x, t(layer->gate), t(layer->up), t(layer->sh_gate), t(layer->sh_up), ws,
-                     s) != cudaSuccess)
-    return DS_ERR_CUDA;
-  if (!mark(marks, 1, s)) return DS_ERR_CUDA;
-  if (launch_down(d, t(layer->down), t(layer->sh_down), topk_w, y, ws, s) != cudaSuccess)
-    return DS_ERR_CUDA;
-  if (!mark(marks, 2, s)) return DS_ERR_CUDA;
+  if (!mark(marks, 1, s) || !mark(marks, 2, s)) return DS_ERR_CUDA;
   return DS_OK;
 }
 

@@ -32,8 +32,7 @@ struct MoeDims {
 constexpr int kQ4TileBytes = 576;
 
 struct MoeWorkspace {
-  uint32_t* header;        // WsHeader: status word, router arrival count
-  uint32_t* counts;        // [ceil(H/256)] down-projection units completed per row group
+  uint32_t* header;        // status word, arrival counts and flags (zeroed per call)
   size_t zero_bytes;       // bytes from header on that every call zeroes first
   float* scores;           // [R][E] sigmoid router scores
   RouteInfo* route;
@@ -42,11 +41,11 @@ struct MoeWorkspace {
 };
 
 struct MoeLayout {
-  size_t header, counts, scores, route, h, opart, total, zero_bytes;
+  size_t header, scores, route, h, opart, total, zero_bytes;
 };
 MoeLayout moe_layout(const MoeDims& d);
-// Least dynamic shared memory the gate/up kernel needs for these sizes (bytes).
-size_t gate_up_smem_bytes(const MoeDims& d);
+// The layer's kernel fits this device's shared memory (the R verify rows are staged there).
+bool moe_fits(const MoeDims& d);
 
 // n_mats planar Q4 matrices (qs [rows][K/2], sc [rows][K/32] each) -> tile-major with
 // tile rows in groups of `group` (rows % 16 == 0, K % 64 == 0).
@@ -54,16 +53,14 @@ cudaError_t launch_tile(const uint8_t* qs, const uint16_t* sc, int n_mats, int64
                         int K, int group, uint8_t* dst, cudaStream_t s);
 // Tile rows per group of the down-projection matrices (gate and up use groups of 1).
 constexpr int kDownGroup = DS_Q4_DOWN_GROUP;
-// Prologue (zeroes the workspace's first zero_bytes) + router.
-cudaError_t launch_router(const MoeDims& d, const uint16_t* x, const uint16_t* router_w,
-                          int32_t* topk_idx, float* topk_w, const MoeWorkspace& ws,
-                          cudaStream_t s);
-cudaError_t launch_gate_up(const MoeDims& d, const uint16_t* x, const uint8_t* gate,
-                           const uint8_t* up, const uint8_t* sh_gate, const uint8_t* sh_up,
-                           const MoeWorkspace& ws, cudaStream_t s);
-cudaError_t launch_down(const MoeDims& d, const uint8_t* down, const uint8_t* sh_down,
-                        const float* topk_w, uint16_t* y, const MoeWorkspace& ws,
-                        cudaStream_t s);
+// The whole verify step of one layer: a prologue that zeroes the workspace header (then
+// `after_prologue` is recorded when not null), and one cooperative kernel (router,
+// gate/up/SwiGLU, down projection, combine).
+cudaError_t launch_moe(const MoeDims& d, const uint16_t* x, const uint16_t* router_w,
+                       const uint8_t* gate, const uint8_t* up, const uint8_t* down,
+                       const uint8_t* sh_gate, const uint8_t* sh_up, const uint8_t* sh_down,
+                       int32_t* topk_idx, float* topk_w, uint16_t* y, const MoeWorkspace& ws,
+                       cudaStream_t s, cudaEvent_t after_prologue);
 
 // ------------------------------------------------------------------ block select ----
 struct SelDims {

@@ -29,6 +29,7 @@
 // is applied exactly to that block's two MMAs. Widening a 32-bit word of 8 nibbles costs
 // three shifts, four AND-ORs that put nibbles in the mantissa of the bf16 number
 // 128 + nibble, and four bf16x2 subtractions of 136 (exact q = nibble - 8).
+#include <algorithm>
 #include <climits>
 #include <utility>
 
@@ -218,228 +219,79 @@ __global__ void __launch_bounds__(256) k0_clear(uint32_t* __restrict__ p, int nw
 }
 
 // ---------------------------------------------------------------------------------
-// K1: router. CTA c computes z = x . Wr[e] for two experts e and all R rows: warps 0-3
-// take expert 2c, warps 4-7 expert 2c + 1, warp w the (w % 4)-th quarter of the hidden
-// dimension (each lane up to 4 chunks of 8 values, all requested before the first is
-// used, x read straight from global memory). A lane adds its chunks in order, the warp's
-// lanes are added by a butterfly, the four warps' sums in warp order, and the sigmoid
-// score is written. The last CTA to arrive (atomic count, nobody waits) selects each row's
-// top k (one warp per row, its scores in registers, a tree argmax per round with ties to
-// the lower index), renormalises the weights, and builds the union of the selected
-// experts with each one's rows and rank slots.
-// ---------------------------------------------------------------------------------
-constexpr int kRouterWarps = 8;
-constexpr int kRouterExperts = 2;
-constexpr int kRouterChunks = 4;   // chunks of 8 values per lane in flight
-
-template <int KPER>   // score registers per lane in the top-k: ceil(E / 32) <= KPER
-__global__ void __launch_bounds__(kRouterWarps * 32)
-    k1_router(const uint16_t* __restrict__ x, int R, int H, const uint16_t* __restrict__ wr,
-              int E, int k, float* __restrict__ scores, int32_t* __restrict__ topk_idx,
-              float* __restrict__ topk_w, RouteInfo* __restrict__ route, WsHeader* hdr) {
-  __shared__ float part[kRouterWarps][kMaxRows];
-  __shared__ int s_is_last;
-  __shared__ int32_t sel_e[kMaxRows][kMaxTopK];
-  __shared__ float sel_s[kMaxRows][kMaxTopK];
-  __shared__ uint32_t ubits[kMaxExperts / 32];
-  __shared__ int16_t upos[kMaxExperts];
-  __shared__ uint32_t u_rowmask[kMaxUnion];
-  __shared__ int8_t u_slot[kMaxUnion][8];
-  __shared__ int s_nunion;
-
-  pdl_trigger();   // the gate/up kernel may launch now; it waits for this grid's results
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int e = blockIdx.x * kRouterExperts + (warp >> 2);
-  {
-    float acc[kMaxRows];
-#pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.0f;
-    const int quarter = H / 4;            // a multiple of 16
-    const int nch = quarter / 8;
-    const int col0 = (warp & 3) * quarter;
-    if (e < E) {
-      const uint16_t* wrow = wr + (size_t)e * H + col0;
-      for (int c0 = lane; c0 < nch; c0 += 32 * kRouterChunks) {
-        // every load of the batch (weights, then the rows' activations) is issued before
-        // the first multiply, so the batch costs one memory round trip
-        uint4 wv[kRouterChunks], xv[kRouterChunks][kMaxRows];
-#pragma unroll
-        for (int j = 0; j < kRouterChunks; ++j) {
-          const int c = min(c0 + 32 * j, nch - 1);
-          wv[j] = __ldcs(reinterpret_cast<const uint4*>(wrow + c * 8));
-#pragma unroll
-          for (int r = 0; r < kMaxRows; ++r)
-            xv[j][r] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)min(r, R - 1) * H + col0 + c * 8));
-        }
-#pragma unroll
-        for (int j = 0; j < kRouterChunks; ++j) {
-          if (c0 + 32 * j >= nch) break;
-          const float wf[8] = {bf16_lo(wv[j].x), bf16_hi(wv[j].x), bf16_lo(wv[j].y),
-                               bf16_hi(wv[j].y), bf16_lo(wv[j].z), bf16_hi(wv[j].z),
-                               bf16_lo(wv[j].w), bf16_hi(wv[j].w)};
-#pragma unroll
-          for (int r = 0; r < kMaxRows; ++r) {
-            const uint4 xr = xv[j][r];
-            float t = acc[r];
-            t = __fmaf_rn(wf[0], bf16_lo(xr.x), t); t = __fmaf_rn(wf[1], bf16_hi(xr.x), t);
-            t = __fmaf_rn(wf[2], bf16_lo(xr.y), t); t = __fmaf_rn(wf[3], bf16_hi(xr.y), t);
-            t = __fmaf_rn(wf[4], bf16_lo(xr.z), t); t = __fmaf_rn(wf[5], bf16_hi(xr.z), t);
-            t = __fmaf_rn(wf[6], bf16_lo(xr.w), t); t = __fmaf_rn(wf[7], bf16_hi(xr.w), t);
-            acc[r] = t;   // rows >= R accumulate a copy of row R - 1, never read
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
-      if (r < R) {
-        const float v = warp_sum(acc[r]);
-        if (lane == 0) part[warp][r] = v;
-      }
-    }
-  }
-  __syncthreads();
-  if (tid < kRouterExperts * R) {
-    const int ee = tid / R, r = tid - ee * R;
-    const int e2 = blockIdx.x * kRouterExperts + ee;
-    if (e2 < E) {
-      float z = 0.0f;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) z = __fadd_rn(z, part[ee * 4 + w][r]);
-      scores[r * E + e2] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
-    }
-  }
-
-  // Arrival count: the last CTA continues, the others are done. Nobody waits. (The CTA
-  // barrier orders the scores before thread 0's fence, which makes them visible device-wide
-  // before the count.) The count was zeroed by the prologue grid, which thread 0 waits for.
-  __syncthreads();
-  if (tid == 0) {
-    pdl_wait();
-    __threadfence();
-    const unsigned prev = atomicAdd(&hdr->router_arrivals, 1u);
-    s_is_last = (prev == gridDim.x - 1);
-    if (s_is_last) __threadfence();   // the other CTAs' scores are visible to this CTA after
-                                      // the barrier below (the fence is cumulative)
-  }
-  __syncthreads();
-  if (!s_is_last) return;
-
-  if (tid < kMaxExperts / 32) ubits[tid] = 0u;
-  if (warp < R) {
-    // Row r's top k by (score desc, expert asc): each round takes the warp-wide largest
-    // key (one reduction), then the smallest expert index holding it (a second one).
-    // Keys: score bits + 2 for a score (sigmoid scores lie in [0, 1], so the bits order
-    // like the values), 1 for NaN (from NaN inputs; ranks below every score), 0 for none.
-    const int r = warp;
-    uint32_t key[KPER];
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < KPER; ++i) {
-      const int e2 = i * 32 + lane;
-      const float sv = e2 < E ? __ldcg(scores + r * E + e2) : 0.0f;
-      bad |= (e2 < E) && !(sv >= 0.0f);
-      key[i] = e2 >= E ? 0u : (sv >= 0.0f ? __float_as_uint(sv) + 2u : 1u);
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) flag_status(&hdr->status, kStatusCheck);
-    for (int j = 0; j < k; ++j) {
-      // this lane's largest key and its lowest register index (a tree; ties keep the left)
-      uint32_t bk[KPER];
-      int bi[KPER];
-#pragma unroll
-      for (int i = 0; i < KPER; ++i) { bk[i] = key[i]; bi[i] = i; }
-#pragma unroll
-      for (int w = 1; w < KPER; w <<= 1)
-#pragma unroll
-        for (int i = 0; i + w < KPER; i += 2 * w)
-          if (bk[i + w] > bk[i]) { bk[i] = bk[i + w]; bi[i] = bi[i + w]; }
-      const uint32_t mk = __reduce_max_sync(0xffffffffu, bk[0]);
-      const uint32_t widx = __reduce_min_sync(
-          0xffffffffu, bk[0] == mk ? (uint32_t)(bi[0] * 32 + lane) : 0xFFFFFFFFu);
-#pragma unroll
-      for (int i = 0; i < KPER; ++i)
-        if ((uint32_t)(i * 32 + lane) == widx) key[i] = 0u;   // taken
-      if (lane == 0) {
-        sel_e[r][j] = (int32_t)widx;
-        sel_s[r][j] = mk >= 2u ? __uint_as_float(mk - 2u) : -1.0f;
-      }
-    }
-    __syncwarp();
-    // renormalise: the sum in rank order (one lane), then one division per lane
-    float sum = 0.0f;
-    if (lane == 0) {
-      sum = sel_s[r][0];
-      for (int j = 1; j < k; ++j) sum = __fadd_rn(sum, sel_s[r][j]);
-    }
-    sum = __shfl_sync(0xffffffffu, sum, 0);
-    if (lane < k) {
-      topk_idx[r * k + lane] = sel_e[r][lane];
-      topk_w[r * k + lane] = __fdiv_rn(sel_s[r][lane], sum);
-    }
-  }
-  __syncthreads();
-
-  for (int i = tid; i < R * k; i += blockDim.x) {
-    const int e2 = sel_e[i / k][i % k];
-    atomicOr(&ubits[e2 >> 5], 1u << (e2 & 31));
-  }
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t b = ubits[lane];
-    const int c = __popc(b);
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
-    }
-    int pos = incl - c;
-    while (b) {
-      const int bit = __ffs(b) - 1;
-      b &= b - 1;
-      const int e2 = lane * 32 + bit;
-      upos[e2] = (int16_t)pos;
-      route->expert[pos] = e2;
-      u_rowmask[pos] = 0u;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) u_slot[pos][r] = -1;
-      ++pos;
-    }
-    if (lane == 31) s_nunion = incl;
-  }
-  __syncthreads();
-  for (int i = tid; i < R * k; i += blockDim.x) {
-    const int r = i / k, j = i % k;
-    const int p = upos[sel_e[r][j]];
-    atomicOr(&u_rowmask[p], 1u << r);
-    u_slot[p][r] = (int8_t)(j + 1);
-  }
-  __syncthreads();
-  const int nu = s_nunion;
-  for (int i = tid; i < nu; i += blockDim.x) {
-    route->rowmask[i] = u_rowmask[i];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) route->slot[i][r] = u_slot[i][r];
-  }
-  if (tid == 0) route->n_union = nu;
-}
-
-// ---------------------------------------------------------------------------------
-// Weight streaming for K3 and K4. A CTA has 16 consumer warps and one producer warp; a
-// ring of stages in shared memory is handed over with "full" and "empty" mbarriers, so the
-// copies of the next stages are always in flight while the consumers compute. A stage is a
-// few long runs of consecutive tiles, each one 1D bulk copy. Work is assigned statically,
-// so the split depends only on the sizes.
+// The layer as one persistent kernel, one CTA per SM, launched cooperatively so that every
+// CTA is resident at once (the phases below wait on one another's results; every such
+// wait is bounded and a give-up sets DS_ERR_TIMEOUT). Roles: 16 consumer warps, one
+// producer warp, three reducer warps. Both weight phases stream through one ring of
+// 36,864-byte stages in shared memory, handed over with "full" / "empty" mbarriers, so
+// the producer moves on from the last gate/up stage to the first down stage at once.
+//
+//  1. Router. The consumers compute the sigmoid scores of experts b, b + G, ... (b = this
+//     CTA, G = grid): thread t adds the products of chunks t, t + 512, ... of 8 values in
+//     order, the lanes of a warp by a butterfly, the 16 warps in warp order. Once every
+//     CTA has written its scores (an arrival count), every CTA reads them all and builds
+//     the route itself: each row's top k (the largest key by a warp reduction per round,
+//     ties to the lower expert), the renormalised weights, and the union of the selected
+//     experts with each one's rows and rank slots, in shared memory. Meanwhile the
+//     producer already streams the shared expert.
+//  2. Gate + up + SwiGLU. A unit is (expert slot u, tile row of I = 16 rows): slot 0 is
+//     the shared expert (all rows), slot u >= 1 the u-th expert of the union (its rows);
+//     CTA b takes units b, b + G, ... A stage is one K chunk of a unit: 32 tiles of the
+//     gate tile row and 32 of the up tile row, two bulk copies. Consumer warp w takes
+//     tiles 2w, 2w + 1 of each chunk for both matrices and keeps its partial sums across
+//     the unit's chunks; its activation fragments for those tiles sit in tensor memory
+//     (written once, read back with tcgen05.ld), which leaves shared memory to the ring.
+//     At the end of a unit the 16 warps' partials meet in shared memory; the reducer warps
+//     add them in warp order, write h = bf16_rne(silu(g) * u) and count the unit against
+//     its expert slot.
+//  3. Down projection. A unit is (expert slot u, row group of 16 tile rows = 256 rows of
+//     H); consumer warp w owns tile row w of the group for all of K (two accumulation
+//     chains, even and odd tiles), so no reduction with other warps follows. A stage is 4
+//     K tiles of the group's 16 tile rows, one contiguous bulk copy (the down matrices keep
+//     their tile rows in groups of 16). CTA b takes a contiguous range of units, so its h
+//     (the B operand, in shared memory) is reloaded only when the expert changes, once
+//     every gate/up unit of that expert is counted. Each warp writes o[row][slot] (fp32).
+//  4. Combine. Once every CTA's down units are done (a count), CTA b writes y =
+//     bf16_rne(o_shared + sum_j w_j o_j), j in rank order, for its share of H.
 // ---------------------------------------------------------------------------------
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kMmaThreads = kConsumers + 32;            // + producer warp
 constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kReducerWarps = 3;                         // 16 rows x R <= 96 outputs
+constexpr int kReducer0 = (kProducerWarp + 1) * 32;      // first reducer thread
+constexpr int kMoeThreads = kReducer0 + 32 * kReducerWarps;
 constexpr int kMaxRing = 8;
-constexpr int kReducerWarps = 3;                         // gate/up: 16 rows x R <= 96 outputs
-constexpr int kGuThreads = kMmaThreads + 32 * kReducerWarps;
-constexpr int kConsumerBarrier = 1;                     // named barrier id of the consumers
-constexpr int kXPad = 64;                                // staged activation row pad (bytes)
+constexpr int kConsumerBarrier = 1;                      // named barrier: consumer warps
+constexpr int kReducerBarrier = 2;                       // named barrier: reducer warps
+constexpr int kXPad = 64;                                // staged h row pad (bytes)
+constexpr int kGuCT = 32;                                // gate/up tiles per matrix per stage
+constexpr int kDownKT = 4;                               // down tiles per tile row per stage
+constexpr int kGroupRows = kDownGroup;                   // down tile rows per unit
+constexpr int kStage = 2 * kGuCT * kTile;                // 36,864 bytes
+static_assert(kGroupRows * kDownKT * kTile == kStage, "both phases share the stage size");
+static_assert(kDownKT % 2 == 0, "down tiles alternate between two chains");
+constexpr int kRouterBatch = 4;                          // experts per CTA per router batch
+
+// Words of the workspace's zeroed area (the prologue clears it before every call): the
+// status word, the router arrival count, the count of CTAs whose down outputs are written,
+// and from word kHdrUnits on, per expert slot, the gate/up units whose h is written.
+enum : int { kHdrStatus = 0, kHdrArrivals = 1, kHdrDDone = 2, kHdrUnits = 64 };
+constexpr int kMoeZeroBytes = 4 * (kHdrUnits + 128);
+static_assert(kMaxUnion + 1 <= 128, "unit counts fit the zeroed area");
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Bounded wait (about 1 s) until *p >= target; false on give-up.
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t target) {
+  for (uint32_t i = 0; i < (1u << 23); ++i) {
+    if (ld_acquire(p) >= target) return true;
+    __nanosleep(128);
+  }
+  return false;
+}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   const uint32_t a = smem_addr(p);
@@ -449,133 +301,367 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync %0, %1;" ::"n"(kConsumerBarrier), "n"(kConsumers) : "memory");
 }
+__device__ __forceinline__ void reducer_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kReducerBarrier), "n"(32 * kReducerWarps) : "memory");
+}
 
-// ---------------------------------------------------------------------------------
-// K3: gate + up + SwiGLU. A unit is (expert slot u, tile row of I = 16 rows): slot 0 is the
-// shared expert (all rows), slot u >= 1 the u-th expert of the union (its rows). CTA b
-// takes units b, b + G, b + 2G, ... (G = grid). A stage is one K chunk of a unit: CT
-// consecutive tiles of the gate tile row and the same of the up tile row, two bulk copies.
-// Consumer warp w takes tiles CT/16 w .. CT/16 w + CT/16 - 1 of the chunk for both matrices
-// and keeps its partial sums across the unit's chunks. At the end of a unit the 16 warps'
-// partials meet in shared memory and are added in warp order by the reducer warps, which
-// write h = bf16_rne(silu(g) * u) for the expert's rows. The activations sit in shared
-// memory as bf16 in MMA pair order, staged once per CTA while the router runs; the
-// producer starts on the shared expert's units before the router's results exist.
-// ---------------------------------------------------------------------------------
-struct GateUpArgs {
-  const uint8_t* gate;     // tiles [E][I/16][H/64]
+struct MoeArgs {
+  const uint16_t* x;          // bf16 [R][H]
+  const uint16_t* router_w;   // bf16 [E][H]
+  const uint8_t* gate;        // tiles [E][I/16][H/64], groups of 1
   const uint8_t* up;
-  const uint8_t* sh_gate;  // tiles [I/16][H/64]
+  const uint8_t* down;        // tiles [E][H/16][I/64], groups of 16
+  const uint8_t* sh_gate;
   const uint8_t* sh_up;
-  const uint16_t* x;
-  const RouteInfo* route;
-  uint16_t* h;
-  uint32_t* status;
-  int R, H, I, k, ring;
+  const uint8_t* sh_down;
+  float* scores;              // [R][E]
+  RouteInfo* route;           // written by CTA 0 for inspection
+  uint16_t* h;                // bf16 [R][1+k][I]
+  float* opart;               // [R][1+k][H]
+  int32_t* topk_idx;          // [R][k]
+  float* topk_w;              // [R][k]
+  uint16_t* y;                // bf16 [R][H]
+  uint32_t* hdr;              // zeroed words (status, counts)
+  int R, H, E, I, k, ring;
 };
 
-__host__ __device__ constexpr size_t gu_red_bytes(int R) {
-  return 2ull * kConsumerWarps * 2 * 16 * (size_t)R * 4;
+__host__ __device__ constexpr size_t moe_red_bytes(int R) {
+  return (size_t)kConsumerWarps * 2 * 16 * R * 4;
 }
-template <int CT>
-__host__ __device__ constexpr size_t gu_stage_bytes() { return 2ull * CT * kTile; }
+__host__ __device__ constexpr size_t moe_h_bytes(int I) { return (size_t)8 * (2 * I + kXPad); }
+// TMEM columns of the activation fragments: 16 per K chunk per warp, 4 warps per lane quarter.
+__host__ __device__ constexpr uint32_t moe_tmem_cols(int H) {
+  const int kc = (H / 64 + kGuCT - 1) / kGuCT;
+  const uint32_t need = 64u * kc;
+  uint32_t c = 32;
+  while (c < need) c <<= 1;
+  return c;
+}
 
-template <int CT>   // tiles per matrix per stage: 32 or 16
-__global__ void __launch_bounds__(kGuThreads, 1) k3_gate_up(const GateUpArgs a) {
-  constexpr int TPW = CT / kConsumerWarps;   // tiles per warp per matrix per stage
-  constexpr int kStage = (int)gu_stage_bytes<CT>();
+template <int KPER>   // score registers per lane in the top-k: ceil(E / 32) <= KPER
+__global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
   __shared__ __align__(8) uint64_t full[kMaxRing], empty[kMaxRing];
-  // partial-sum buffers: written by the 16 consumer warps (pfull), read by the reducer
-  // warps (pempty); two buffers, so consumers wait only when two units are unreduced
-  __shared__ __align__(8) uint64_t s_pfull[2], s_pempty[2];
+  // the partial sums of one gate/up unit: written by the 16 consumer warps (pfull), read by
+  // the reducer warps (pempty); the route is built (s_route)
+  __shared__ __align__(8) uint64_t s_pfull, s_pempty, s_route;
+  __shared__ uint32_t s_tmem;
+  __shared__ float s_part[kRouterBatch][kConsumerWarps][kMaxRows];
+  __shared__ int32_t sel_e[kMaxRows][kMaxTopK];
+  __shared__ float sel_s[kMaxRows][kMaxTopK];
+  __shared__ uint32_t ubits[kMaxExperts / 32];
+  __shared__ int16_t upos[kMaxExperts];
+  __shared__ int32_t u_expert[kMaxUnion];
+  __shared__ uint32_t u_rowmask[kMaxUnion];
+  __shared__ __align__(8) int8_t u_slot[kMaxUnion][8];
+  __shared__ int s_nunion;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  const int R = a.R, H = a.H, I = a.I, k = a.k, ring = a.ring;
-  const int T = H >> 6;                           // tiles per tile row (K = H)
-  const int KC = (T + CT - 1) / CT;               // chunks per unit
-  const int RT = I >> 4;                          // tile rows (units) per expert
-  const size_t expert_bytes = (size_t)RT * T * kTile;
-  const int xstride = 2 * H + kXPad;
+  const int R = a.R, H = a.H, E = a.E, I = a.I, k = a.k, ring = a.ring;
+  const int G = gridDim.x, b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
+  uint32_t* status = a.hdr + kHdrStatus;
+  uint32_t* ucount = a.hdr + kHdrUnits;
 
   uint8_t* stages = smem;
-  float* red = reinterpret_cast<float*>(smem + (size_t)ring * kStage);
-  uint8_t* xs = smem + (size_t)ring * kStage + gu_red_bytes(R);
+  uint8_t* region = smem + (size_t)ring * kStage;   // gate/up: red; down: hs
+  float* red = reinterpret_cast<float*>(region);
+  uint8_t* hs = region;
+
+  // gate/up geometry (K = H)
+  const int Tg = H >> 6, KCg = (Tg + kGuCT - 1) / kGuCT, RTg = I >> 4;
+  const size_t gu_expert = (size_t)RTg * Tg * kTile;
+  // down geometry (K = I)
+  const int Td = I >> 6, KCd = (Td + kDownKT - 1) / kDownKT, RTd = H >> 4;
+  const int NGR = (RTd + kGroupRows - 1) / kGroupRows;
+  const size_t dn_expert = (size_t)RTd * Td * kTile;
+  const int hpitch = 2 * I + kXPad;
+  const uint32_t tcols = moe_tmem_cols(H);
 
   if (tid == 0) {
     for (int s = 0; s < ring; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_pfull[b], kConsumerWarps);
-      mbar_init(&s_pempty[b], kReducerWarps);
-    }
+    mbar_init(&s_pfull, kConsumerWarps);
+    mbar_init(&s_pempty, kReducerWarps);
+    mbar_init(&s_route, 1);
     fence_mbar_init();
   }
-  // Activations -> shared memory, bf16 in MMA pair order (independent of the router).
-#pragma unroll 4
-  for (int i = tid; i < R * (H >> 3); i += blockDim.x) {
-    const int r = i / (H >> 3), grp = i - r * (H >> 3);
-    const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)r * H + grp * 8);
-    *reinterpret_cast<uint4*>(xs + r * xstride + (grp >> 2) * 64 + (grp & 3) * 16) = pair_order(v);
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, tcols);
+    tmem_relinquish();
   }
+  tc_fence_before();
   __syncthreads();
-
-  const int G = gridDim.x;
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
   bool timed_out = false;
+
   if (warp == kProducerWarp) {
-    bool routed = false;   // the router's results are known to be visible
-    // Units of the shared expert need nothing from the router; a unit of a routed expert
-    // waits for it (and so does the count of units, which needs the union size).
+    // ------------------------------------------------------------- producer ----------
     int slot = 0, f = 0;
     uint32_t phase = 0;    // ring cursor: stage f sits in `slot`, pass parity `phase`
-    for (int n = (int)blockIdx.x;; n += G) {
-      const int u = n / RT, rt = n - u * RT;
-      if (u > 0 && !routed) { pdl_wait(); routed = true; }
-      if (routed && n >= (1 + a.route->n_union) * RT) break;
-      const uint8_t* gbase = (u == 0 ? a.sh_gate : a.gate + (size_t)a.route->expert[u - 1] * expert_bytes) +
-                             (size_t)rt * T * kTile;
-      const uint8_t* ubase = (u == 0 ? a.sh_up : a.up + (size_t)a.route->expert[u - 1] * expert_bytes) +
-                             (size_t)rt * T * kTile;
-      for (int c = 0; c < KC; ++c, ++f) {
-        if (f >= ring && !pipe_wait(&empty[slot], phase ^ 1u)) timed_out = true;
+    int n_union = -1;      // known once this CTA has built the route
+    auto routed = [&]() {
+      if (n_union < 0) {
+        if (!pipe_wait(&s_route, 0)) timed_out = true;
+        n_union = s_nunion;
+      }
+    };
+    auto next_slot = [&]() -> uint8_t* {
+      if (f >= ring && !pipe_wait(&empty[slot], phase ^ 1u)) timed_out = true;
+      return stages + (size_t)slot * kStage;
+    };
+    auto advance = [&]() {
+      ++f;
+      if (++slot == ring) { slot = 0; phase ^= 1u; }
+    };
+    // gate/up units b, b + G, ...: the shared expert's need nothing from the router
+    for (int n = b;; n += G) {
+      const int u = n / RTg, rt = n - u * RTg;
+      if (u > 0) routed();
+      if (n_union >= 0 && n >= (1 + n_union) * RTg) break;
+      const size_t e = u > 0 ? (size_t)u_expert[u - 1] : 0;
+      const uint8_t* gb = u > 0 ? a.gate + e * gu_expert : a.sh_gate;
+      const uint8_t* ub = u > 0 ? a.up + e * gu_expert : a.sh_up;
+      for (int c = 0; c < KCg; ++c) {
+        uint8_t* st = next_slot();
         if (lane == 0) {
-          uint8_t* st = stages + (size_t)slot * kStage;
-          const uint32_t bytes = (uint32_t)min(CT, T - c * CT) * kTile;
+          const size_t off = ((size_t)rt * Tg + (size_t)c * kGuCT) * kTile;
+          const uint32_t bytes = (uint32_t)min(kGuCT, Tg - c * kGuCT) * kTile;
           mbar_arrive_expect_tx(&full[slot], 2u * bytes);
-          bulk_copy(st, gbase + (size_t)c * CT * kTile, bytes, &full[slot]);
-          bulk_copy(st + CT * kTile, ubase + (size_t)c * CT * kTile, bytes, &full[slot]);
+          bulk_copy(st, gb + off, bytes, &full[slot]);
+          bulk_copy(st + kGuCT * kTile, ub + off, bytes, &full[slot]);
         }
         __syncwarp();
-        if (++slot == ring) { slot = 0; phase ^= 1u; }
+        advance();
       }
     }
-    if (!routed) pdl_wait();
+    routed();
+    // down units: a contiguous range
+    const int nd = (1 + n_union) * NGR;
+    const int d0 = (int)(((long long)b * nd) / G), d1 = (int)(((long long)(b + 1) * nd) / G);
+    for (int n = d0; n < d1; ++n) {
+      const int u = n / NGR, rg = n - u * NGR;
+      const int rig = min(kGroupRows, RTd - rg * kGroupRows);   // tile rows in the group
+      const uint8_t* gbase = (u > 0 ? a.down + (size_t)u_expert[u - 1] * dn_expert : a.sh_down) +
+                             (size_t)rg * kGroupRows * Td * kTile;
+      for (int c = 0; c < KCd; ++c) {
+        uint8_t* st = next_slot();
+        if (lane == 0) {
+          const uint32_t bytes = (uint32_t)(min(kDownKT, Td - c * kDownKT) * rig * kTile);
+          mbar_arrive_expect_tx(&full[slot], bytes);
+          bulk_copy(st, gbase + (size_t)c * kDownKT * rig * kTile, bytes, &full[slot]);
+        }
+        __syncwarp();
+        advance();
+      }
+    }
   } else if (warp < kProducerWarp) {
-    pdl_wait();      // the route produced by the router grid is visible from here on
-    const RouteInfo* rt = a.route;
-    const int n_units = (1 + rt->n_union) * RT;
-    const int n_mine = (int)blockIdx.x < n_units ? (n_units - (int)blockIdx.x + G - 1) / G : 0;
-    const uint8_t* xrow = xs + min(g, R - 1) * xstride + q * 16;   // rows >= R: any finite row
+    // ------------------------------------------------------------- consumers ---------
+    // (1) router scores of experts b + j G
+    for (int j0 = 0; b + j0 * G < E; j0 += kRouterBatch) {
+      int ne = 0;
+      while (ne < kRouterBatch && b + (j0 + ne) * G < E) ++ne;
+      float acc[kRouterBatch][kMaxRows];
+#pragma unroll
+      for (int j = 0; j < kRouterBatch; ++j)
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) acc[j][r] = 0.0f;
+      for (int ci = tid; ci < (H >> 3); ci += kConsumers) {
+        uint4 wv[kRouterBatch], xv[kMaxRows];
+#pragma unroll
+        for (int j = 0; j < kRouterBatch; ++j)
+          wv[j] = j < ne ? __ldcs(reinterpret_cast<const uint4*>(
+                               a.router_w + (size_t)(b + (j0 + j) * G) * H + ci * 8))
+                         : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r)
+          xv[r] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)min(r, R - 1) * H + ci * 8));
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r) {
+          const uint32_t xw[4] = {xv[r].x, xv[r].y, xv[r].z, xv[r].w};
+#pragma unroll
+          for (int j = 0; j < kRouterBatch; ++j) {
+            const uint32_t ww[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+            float t = acc[j][r];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              t = __fmaf_rn(bf16_lo(ww[m]), bf16_lo(xw[m]), t);
+              t = __fmaf_rn(bf16_hi(ww[m]), bf16_hi(xw[m]), t);
+            }
+            acc[j][r] = t;   // rows >= R accumulate a copy of row R - 1, never read
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kRouterBatch; ++j)
+#pragma unroll
+        for (int r = 0; r < kMaxRows; ++r)
+          if (j < ne && r < R) {
+            const float v = warp_sum(acc[j][r]);
+            if (lane == 0) s_part[j][warp][r] = v;
+          }
+      consumer_sync();
+      if (tid < ne * R) {
+        const int j = tid / R, r = tid - j * R;
+        float z = 0.0f;
+        for (int w = 0; w < kConsumerWarps; ++w) z = __fadd_rn(z, s_part[j][w][r]);
+        a.scores[r * E + b + (j0 + j) * G] = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
+      }
+      consumer_sync();
+    }
+    // (2) every CTA's scores are written: count this one (the barrier orders its scores
+    // before the fence), wait for all, then each CTA builds the route from all scores
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(a.hdr + kHdrArrivals, 1u);
+    }
+    // While the other CTAs finish their scores: this warp's activation fragments -> tensor
+    // memory. For each K chunk, tiles 2w and 2w + 1, each two blocks of 4 words in MMA pair
+    // order (verify row g; rows >= R take a copy of row R - 1, any finite row): 16 columns
+    // of this lane.
+    const uint32_t tw = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(warp >> 2) * 16u * KCg;
+    {
+      const uint16_t* xg = a.x + (size_t)min(g, R - 1) * H + q * 8;
+      for (int c = 0; c < KCg; ++c) {
+        uint32_t v[16];
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+          const int t = c * kGuCT + warp * 2 + tt;
+#pragma unroll
+          for (int blk = 0; blk < 2; ++blk) {
+            uint4 w4 = make_uint4(0, 0, 0, 0);
+            if (t < Tg) w4 = pair_order(__ldg(reinterpret_cast<const uint4*>(xg + (size_t)(2 * t + blk) * 32)));
+            v[(tt * 2 + blk) * 4 + 0] = w4.x; v[(tt * 2 + blk) * 4 + 1] = w4.y;
+            v[(tt * 2 + blk) * 4 + 2] = w4.z; v[(tt * 2 + blk) * 4 + 3] = w4.w;
+          }
+        }
+        tmem_st16(tw + (uint32_t)c * 16u, v);
+      }
+    }
+    if (tid == 0 && !wait_count(a.hdr + kHdrArrivals, (uint32_t)G)) timed_out = true;
+    if (tid < kMaxExperts / 32) ubits[tid] = 0u;
+    consumer_sync();
+    if (warp < R) {
+      // row r's top k by (score desc, expert asc): the warp-wide largest key, then the
+      // smallest expert index holding it. Keys: score bits + 2 (sigmoid scores lie in
+      // [0, 1]), 1 for NaN (from NaN inputs; below every score), 0 for none / taken.
+      const int r = warp;
+      uint32_t key[KPER];
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < KPER; ++i) {
+        const int e2 = i * 32 + lane;
+        const float sv = e2 < E ? __ldcg(a.scores + r * E + e2) : 0.0f;
+        bad |= (e2 < E) && !(sv >= 0.0f);
+        key[i] = e2 >= E ? 0u : (sv >= 0.0f ? __float_as_uint(sv) + 2u : 1u);
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0 && b == 0) flag_status(status, kStatusCheck);
+      for (int j = 0; j < k; ++j) {
+        uint32_t bk[KPER];
+        int bi[KPER];
+#pragma unroll
+        for (int i = 0; i < KPER; ++i) { bk[i] = key[i]; bi[i] = i; }
+#pragma unroll
+        for (int w = 1; w < KPER; w <<= 1)
+#pragma unroll
+          for (int i = 0; i + w < KPER; i += 2 * w)
+            if (bk[i + w] > bk[i]) { bk[i] = bk[i + w]; bi[i] = bi[i + w]; }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk[0]);
+        const uint32_t widx = __reduce_min_sync(
+            0xffffffffu, bk[0] == mk ? (uint32_t)(bi[0] * 32 + lane) : 0xFFFFFFFFu);
+#pragma unroll
+        for (int i = 0; i < KPER; ++i)
+          if ((uint32_t)(i * 32 + lane) == widx) key[i] = 0u;   // taken
+        if (lane == 0) {
+          sel_e[r][j] = (int32_t)widx;
+          sel_s[r][j] = mk >= 2u ? __uint_as_float(mk - 2u) : -1.0f;
+        }
+      }
+      __syncwarp();
+      if (b == 0) {
+        // renormalise: the sum in rank order (one lane), then one division per lane
+        float sum = 0.0f;
+        if (lane == 0) {
+          sum = sel_s[r][0];
+          for (int j = 1; j < k; ++j) sum = __fadd_rn(sum, sel_s[r][j]);
+        }
+        sum = __shfl_sync(0xffffffffu, sum, 0);
+        if (lane < k) {
+          a.topk_idx[r * k + lane] = sel_e[r][lane];
+          a.topk_w[r * k + lane] = __fdiv_rn(sel_s[r][lane], sum);
+        }
+      }
+    }
+    consumer_sync();
+    for (int i = tid; i < R * k; i += kConsumers) {
+      const int e2 = sel_e[i / k][i % k];
+      atomicOr(&ubits[e2 >> 5], 1u << (e2 & 31));
+    }
+    consumer_sync();
+    if (warp == 0) {
+      uint32_t bits = ubits[lane];
+      const int c = __popc(bits);
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int nn = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += nn;
+      }
+      int pos = incl - c;
+      while (bits) {
+        const int bit = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const int e2 = lane * 32 + bit;
+        upos[e2] = (int16_t)pos;
+        u_expert[pos] = e2;
+        u_rowmask[pos] = 0u;
+        *reinterpret_cast<uint2*>(u_slot[pos]) = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
+        ++pos;
+      }
+      if (lane == 31) s_nunion = incl;
+    }
+    consumer_sync();
+    for (int i = tid; i < R * k; i += kConsumers) {
+      const int r = i / k, j = i % k;
+      const int p = upos[sel_e[r][j]];
+      atomicOr(&u_rowmask[p], 1u << r);
+      u_slot[p][r] = (int8_t)(j + 1);
+    }
+    consumer_sync();
+    const int n_union = s_nunion;
+    if (tid == 0) mbar_arrive(&s_route);   // the producer and the reducers may read it now
+    if (b == 0) {   // a copy of the route for inspection
+      for (int i = tid; i < n_union; i += kConsumers) {
+        a.route->expert[i] = u_expert[i];
+        a.route->rowmask[i] = u_rowmask[i];
+        *reinterpret_cast<uint2*>(a.route->slot[i]) = *reinterpret_cast<const uint2*>(u_slot[i]);
+      }
+      if (tid == 0) a.route->n_union = n_union;
+    }
+    // (3) gate/up units
+    const int n_units = (1 + n_union) * RTg;
+    const int n_mine = b < n_units ? (n_units - b + G - 1) / G : 0;
     float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
     int slot = 0;
     uint32_t phase = 0;
     for (int unit = 0; unit < n_mine; ++unit) {
-      for (int c = 0; c < KC; ++c) {
+      for (int c = 0; c < KCg; ++c) {
         if (!pipe_wait(&full[slot], phase)) timed_out = true;
         const uint8_t* st = stages + (size_t)slot * kStage;
-        const int ct = min(CT, T - c * CT);
-        const uint8_t* xc = xrow + (size_t)c * CT * 128;
+        const int ct = min(kGuCT, Tg - c * kGuCT);
 #pragma unroll
-        for (int tt = 0; tt < TPW; ++tt) {
-          const int t = warp * TPW + tt;
+        for (int tt = 0; tt < 2; ++tt) {
+          const int t = warp * 2 + tt;
           if (t < ct) {
-            const uint8_t* xb = xc + t * 128;   // blocks 2t, 2t + 1 of the chunk
-            const uint4 X0 = lds128(xb), X1 = lds128(xb + 64);
+            uint32_t xw[8];   // blocks 2t, 2t + 1 of the chunk
+            tmem_ld8(tw + (uint32_t)(c * 16 + tt * 8), xw);
+            const uint4 X0 = make_uint4(xw[0], xw[1], xw[2], xw[3]);
+            const uint4 X1 = make_uint4(xw[4], xw[5], xw[6], xw[7]);
             const uint8_t* tg = st + t * kTile;
-            const uint8_t* tu = st + (CT + t) * kTile;
+            const uint8_t* tu = st + (kGuCT + t) * kTile;
             const uint4 Wg = lds128(tg + lane * 16), Wu = lds128(tu + lane * 16);
             const uint2 Sg = lds64(tg + kTileNib + g * 8), Su = lds64(tu + kTileNib + g * 8);
             q4_tile_mma(Wg, Sg, X0, X1, ag);
@@ -586,226 +672,48 @@ __global__ void __launch_bounds__(kGuThreads, 1) k3_gate_up(const GateUpArgs a) 
         if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the slot
         if (++slot == ring) { slot = 0; phase ^= 1u; }
       }
-      // partials [warp][gate/up][row][col] (cols < R only) into buffer unit & 1, once the
-      // reducers are done with the unit that used it before
-      const int buf = unit & 1;
-      if (unit >= 2 && !pipe_wait(&s_pempty[buf], ((unit >> 1) - 1) & 1)) timed_out = true;
-      float* rb = red + (size_t)buf * kConsumerWarps * 2 * 16 * R;
+      // partials [warp][gate/up][row][col] (cols < R only), once the reducers are done
+      // with the unit before
+      if (unit >= 1 && !pipe_wait(&s_pempty, (unit - 1) & 1)) timed_out = true;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int col = 2 * q + (e & 1), row = g + ((e & 2) ? 8 : 0);
         if (col < R) {
-          rb[((warp * 2 + 0) * 16 + row) * R + col] = ag[e];
-          rb[((warp * 2 + 1) * 16 + row) * R + col] = au[e];
+          red[((warp * 2 + 0) * 16 + row) * R + col] = ag[e];
+          red[((warp * 2 + 1) * 16 + row) * R + col] = au[e];
         }
         ag[e] = 0.f;
         au[e] = 0.f;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_pfull[buf]);
+      if (lane == 0) mbar_arrive(&s_pfull);
     }
-  } else {
-    // Reducers: for each unit of this CTA, in order, the 16 warps' partials are added in
-    // warp order and h = bf16_rne(silu(g) * u) is written for the expert's rows.
-    pdl_wait();
-    const RouteInfo* rt = a.route;
-    const int n_units = (1 + rt->n_union) * RT;
-    const int rtid = tid - (kProducerWarp + 1) * 32;
-    int unit = 0;
-    for (int n = (int)blockIdx.x; n < n_units; n += G, ++unit) {
-      const int b = unit & 1;
-      if (!pipe_wait(&s_pfull[b], (unit >> 1) & 1)) {
-        timed_out = true;
-        break;
-      }
-      const float* rb = red + (size_t)b * kConsumerWarps * 2 * 16 * R;
-      const int u = n / RT, rti = n - u * RT;
-      if (rtid < 16 * R) {
-        const int row = rtid / R, col = rtid - row * R;
-        const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : rt->rowmask[u - 1];
-        if ((rowmask >> col) & 1u) {
-          float gs = 0.f, us = 0.f;
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            gs = __fadd_rn(gs, rb[((w * 2 + 0) * 16 + row) * R + col]);
-            us = __fadd_rn(us, rb[((w * 2 + 1) * 16 + row) * R + col]);
-          }
-          const int slot_c = (u == 0) ? 0 : rt->slot[u - 1][col];
-          const float silu = __fdiv_rn(gs, __fadd_rn(1.0f, expf(-gs)));
-          a.h[((size_t)col * (1 + k) + slot_c) * I + rti * 16 + row] =
-              f32_to_bf16_rne(__fmul_rn(silu, us));
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_pempty[b]);
-    }
-  }
-  pdl_trigger();   // the down projection may be scheduled as CTAs of this grid retire
-  if (timed_out && lane == 0) flag_status(a.status, kStatusTimeout);
-}
-
-// ---------------------------------------------------------------------------------
-// K4: down projection and combine. A unit is (expert slot u, row group of 16 tile rows =
-// 256 rows of H); consumer warp w owns tile row w of the group for the whole unit, so its
-// fp32 sums need no reduction with other warps. A stage is one K chunk of KT tiles of the
-// group's 16 tile rows, one contiguous run (the down matrices keep their tile rows in
-// groups of 16, K tile first within a group): one bulk copy. CTA b takes a contiguous
-// range of units, so consecutive stages mostly belong to one expert and its h (the B
-// operand, kept in shared memory in MMA pair order) is reloaded only when the expert
-// changes. At the end of a unit each warp writes o[row][slot] (fp32) for the rows that use
-// the expert; a counting warp then counts the unit against its row group (fence, atomic
-// add) while the consumers go on, and after its last unit the CTA that completed a row
-// group (every slot's unit done; nobody waits) writes y = bf16_rne(o_shared +
-// sum_j w_j o_j) for the group's rows, j in rank order.
-// The weights do not depend on the gate/up kernel, so the producer starts streaming them
-// before that kernel has finished; only h waits for it.
-// ---------------------------------------------------------------------------------
-#ifndef DSMOE_DOWN_KT
-#define DSMOE_DOWN_KT 4
-#endif
-constexpr int kDownKT = DSMOE_DOWN_KT;   // tiles per tile row per stage
-constexpr int kGroupRows = kDownGroup;   // tile rows per unit (one per consumer warp)
-constexpr int kDownStage = kGroupRows * kDownKT * kTile;   // 36,864 bytes
-
-struct DownArgs {
-  const uint8_t* down;      // tiles [E][H/16][I/64]
-  const uint8_t* sh_down;   // tiles [H/16][I/64]
-  const uint16_t* h;
-  const RouteInfo* route;
-  const float* topk_w;
-  float* opart;             // [R][1+k][H] expert outputs
-  uint32_t* counts;         // [ceil(H/256)] units completed per row group (zeroed per call)
-  uint16_t* y;
-  uint32_t* status;
-  int R, H, I, k, ring;
-};
-
-__host__ __device__ constexpr int down_hpitch(int I) { return 2 * I + kXPad; }
-
-constexpr int kCountWarp = kProducerWarp + 1;
-constexpr int kDownThreads = kMmaThreads + 32;   // + the counting warp
-constexpr int kMaxGroupsPerCta = 64;             // row groups a CTA can complete (H <= 16384)
-
-__global__ void __launch_bounds__(kDownThreads, 1) k4_down(const DownArgs a) {
-  __shared__ __align__(8) uint64_t full[kMaxRing], empty[kMaxRing];
-  // a unit's outputs written (16 consumer warps) / taken over by the counting warp (1)
-  __shared__ __align__(8) uint64_t s_udone[2], s_ufree[2];
-  __shared__ uint32_t s_rowmask[kMaxUnion];
-  __shared__ __align__(8) int8_t s_slot[kMaxUnion][8];
-  __shared__ int s_done[kMaxGroupsPerCta];   // row groups this CTA completed
-  __shared__ int s_ndone;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  const int R = a.R, H = a.H, I = a.I, k = a.k, ring = a.ring;
-  const int T = I >> 6;                              // tiles per tile row (K = I)
-  const int KC = (T + kDownKT - 1) / kDownKT;        // chunks per unit
-  const int RTt = H >> 4;                            // tile rows per expert
-  const int NGR = (RTt + kGroupRows - 1) / kGroupRows;
-  const size_t expert_bytes = (size_t)RTt * T * kTile;
-  const int hpitch = down_hpitch(I);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, q = lane & 3;
-
-  uint8_t* stages = smem;
-  uint8_t* hs = smem + (size_t)ring * kDownStage;   // [8][hpitch]
-
-  if (tid == 0) {
-    for (int s = 0; s < ring; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_udone[b], kConsumerWarps);
-      mbar_init(&s_ufree[b], 1);
-    }
-    s_ndone = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  // The route was complete before the gate/up kernel passed its own wait, which precedes
-  // the launch of this grid; h is waited for below.
-  const RouteInfo* rt = a.route;
-  const int n_union = rt->n_union;
-  const int n_units = (1 + n_union) * NGR;
-  const int G = gridDim.x;
-  const int u_begin = (int)(((long long)blockIdx.x * n_units) / G);
-  const int u_end = (int)(((long long)(blockIdx.x + 1) * n_units) / G);
-  bool timed_out = false;
-
-  if (warp == kProducerWarp) {
-    int slot = 0, f = 0;
-    uint32_t phase = 0;    // ring cursor
-    for (int n = u_begin; n < u_end; ++n) {
-      const int u = n / NGR, rg = n - u * NGR;
-      const int rig = min(kGroupRows, RTt - rg * kGroupRows);   // tile rows in the group
-      const uint8_t* gbase = (u == 0 ? a.sh_down : a.down + (size_t)rt->expert[u - 1] * expert_bytes) +
-                             (size_t)rg * kGroupRows * T * kTile;
-      for (int c = 0; c < KC; ++c, ++f) {
-        if (f >= ring && !pipe_wait(&empty[slot], phase ^ 1u)) timed_out = true;
-        if (lane == 0) {
-          // the group's tiles of K tiles c KT .. c KT + kt - 1: one contiguous run
-          const uint32_t bytes = (uint32_t)(min(kDownKT, T - c * kDownKT) * rig * kTile);
-          mbar_arrive_expect_tx(&full[slot], bytes);
-          bulk_copy(stages + (size_t)slot * kDownStage,
-                    gbase + (size_t)c * kDownKT * rig * kTile, bytes, &full[slot]);
-        }
-        __syncwarp();
-        if (++slot == ring) { slot = 0; phase ^= 1u; }
-      }
-    }
-    pdl_wait();
-  } else if (warp == kCountWarp) {
-    // Counts each finished unit against its row group: once the consumers' outputs of the
-    // unit are written (mbarrier, CTA scope), a fence makes them visible device-wide, then
-    // the atomic count; the unit that completes a group (1 + n_union units, nobody waits)
-    // records it for the combine below.
-    pdl_wait();
-    int j = 0;
-    for (int n = u_begin; n < u_end; ++n, ++j) {
-      const int b = j & 1;
-      if (!pipe_wait(&s_udone[b], (j >> 1) & 1)) timed_out = true;
-      if (lane == 0) {
-        const int rg = n % NGR;
-        __threadfence();
-        const unsigned prev = atomicAdd(&a.counts[rg], 1u);
-        if (prev == (unsigned)n_union) {
-          __threadfence();
-          if (s_ndone < kMaxGroupsPerCta) s_done[s_ndone++] = rg;
-          else flag_status(a.status, kStatusCheck);
-        }
-        mbar_arrive(&s_ufree[b]);
-      }
-      __syncwarp();
-    }
-  } else {
-    // the union's row masks and rank slots, read every unit, kept in shared memory (the
-    // route is visible already, see above)
-    for (int i = tid; i < n_union; i += kConsumers) {
-      s_rowmask[i] = rt->rowmask[i];
-      *reinterpret_cast<uint2*>(s_slot[i]) = *reinterpret_cast<const uint2*>(rt->slot[i]);
-    }
-    pdl_wait();      // h is complete from here on
-    consumer_sync();
+    tc_fence_before();   // this warp's tensor-memory reads are done
+    // (4) down units. The partial buffer shares shared memory with h: the reducers must be
+    // done with it first.
+    if (n_mine > 0 && !pipe_wait(&s_pempty, (n_mine - 1) & 1)) timed_out = true;
+    const int nd = (1 + n_union) * NGR;
+    const int d0 = (int)(((long long)b * nd) / G), d1 = (int)(((long long)(b + 1) * nd) / G);
     const uint8_t* hrow = hs + g * hpitch + q * 16;   // rows >= R or unused: never read out
     int h_u = -1;       // expert slot whose h is staged
     // two chains: even (acc) and odd (acc2) tiles of the row, added once at the unit end
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-    int slot = 0, j = 0;
-    uint32_t phase = 0;
-    for (int n = u_begin; n < u_end; ++n, ++j) {
+    for (int n = d0; n < d1; ++n) {
       const int u = n / NGR, rg = n - u * NGR;
-      const int rig = min(kGroupRows, RTt - rg * kGroupRows);
-      const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : s_rowmask[u - 1];
+      const int rig = min(kGroupRows, RTd - rg * kGroupRows);
+      const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : u_rowmask[u - 1];
       if (u != h_u) {
-        // h of the expert's rows: [verify row][values], 16-byte pieces, then each piece
-        // put in MMA pair order in place. Rows that do not use the expert keep stale
-        // values; their MMA columns are never read.
+        // h of the expert's rows, once every gate/up unit of the expert is counted:
+        // [verify row][values], 16-byte pieces, then each piece put in MMA pair order in
+        // place. Rows that do not use the expert keep stale values; their MMA columns are
+        // never read.
+        if (tid == 0 && !wait_count(ucount + u, (uint32_t)RTg)) timed_out = true;
         consumer_sync();   // every consumer is done with the previous h
         const int per_row = I / 8;
         for (int p = tid; p < R * per_row; p += kConsumers) {
           const int rr = p / per_row, pp = p - rr * per_row;
           if ((rowmask >> rr) & 1u) {
-            const int slot_r = (u == 0) ? 0 : s_slot[u - 1][rr];
+            const int slot_r = (u == 0) ? 0 : u_slot[u - 1][rr];
             cp_async16(hs + rr * hpitch + pp * 16, a.h + ((size_t)rr * (1 + k) + slot_r) * I + pp * 8);
           }
         }
@@ -822,13 +730,12 @@ __global__ void __launch_bounds__(kDownThreads, 1) k4_down(const DownArgs a) {
         h_u = u;
       }
       const int tr = rg * kGroupRows + warp;              // this warp's tile row
-      for (int c = 0; c < KC; ++c) {
+      for (int c = 0; c < KCd; ++c) {
         if (!pipe_wait(&full[slot], phase)) timed_out = true;
-        const uint8_t* st = stages + (size_t)slot * kDownStage;
-        const int kt = min(kDownKT, T - c * kDownKT);
+        const uint8_t* st = stages + (size_t)slot * kStage;
+        const int kt = min(kDownKT, Td - c * kDownKT);
         if (warp < rig) {
           const uint8_t* xc = hrow + (size_t)c * kDownKT * 128;
-          static_assert(kDownKT % 2 == 0, "tiles alternate between the two chains");
 #pragma unroll
           for (int jj = 0; jj < kDownKT; ++jj) {
             if (jj < kt) {
@@ -847,36 +754,76 @@ __global__ void __launch_bounds__(kDownThreads, 1) k4_down(const DownArgs a) {
         if (lane == 0) mbar_arrive(&empty[slot]);
         if (++slot == ring) { slot = 0; phase ^= 1u; }
       }
-      // the unit is done: this warp's rows, once the counting warp has taken over the unit
-      // two before (its outputs are counted before new ones are announced)
-      const int b = j & 1;
-      if (j >= 2 && !pipe_wait(&s_ufree[b], ((j >> 1) - 1) & 1)) timed_out = true;
       if (warp < rig) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int col = 2 * q + (e & 1), row = tr * 16 + g + ((e & 2) ? 8 : 0);
           if (col < R && ((rowmask >> col) & 1u)) {
-            const int slot_c = (u == 0) ? 0 : s_slot[u - 1][col];
+            const int slot_c = (u == 0) ? 0 : u_slot[u - 1][col];
             a.opart[((size_t)col * (1 + k) + slot_c) * H + row] = __fadd_rn(acc[e], acc2[e]);
           }
         }
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[e] = acc2[e] = 0.f;
+    }
+    // this CTA's outputs are written: count it (the barrier orders them before the fence)
+    consumer_sync();
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(a.hdr + kHdrDDone, 1u);
+    }
+  } else {
+    // ------------------------------------------------------------- reducers ----------
+    // For each gate/up unit of this CTA, in order, the 16 warps' partials are added in warp
+    // order, h = bf16_rne(silu(g) * u) is written for the expert's rows, and the unit is
+    // counted against its expert slot.
+    const int rtid = tid - kReducer0;
+    if (!pipe_wait(&s_route, 0)) timed_out = true;
+    const int n_union = s_nunion;
+    const int n_units = (1 + n_union) * RTg;
+    int unit = 0;
+    for (int n = b; n < n_units; n += G, ++unit) {
+      if (!pipe_wait(&s_pfull, unit & 1)) timed_out = true;
+      const int u = n / RTg, rti = n - u * RTg;
+      if (rtid < 16 * R) {
+        const int row = rtid / R, col = rtid - row * R;
+        const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : u_rowmask[u - 1];
+        if ((rowmask >> col) & 1u) {
+          float gs = 0.f, us = 0.f;
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            gs = __fadd_rn(gs, red[((w * 2 + 0) * 16 + row) * R + col]);
+            us = __fadd_rn(us, red[((w * 2 + 1) * 16 + row) * R + col]);
+          }
+          const int slot_c = (u == 0) ? 0 : u_slot[u - 1][col];
+          const float silu = __fdiv_rn(gs, __fadd_rn(1.0f, expf(-gs)));
+          a.h[((size_t)col * (1 + k) + slot_c) * I + rti * 16 + row] =
+              f32_to_bf16_rne(__fmul_rn(silu, us));
+        }
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_udone[b]);
+      if (lane == 0) mbar_arrive(&s_pempty);
+      // the unit's h is written by all three warps: count it (the barrier orders the
+      // writes before the fence)
+      reducer_sync();
+      if (rtid == 0) {
+        __threadfence();
+        atomicAdd(ucount + u, 1u);
+      }
     }
   }
-  // The row groups whose last unit this CTA counted: every slot's rows are written, so
-  // combine them, rank order (all warps of the CTA).
+
+  // (5) combine, once every CTA's down outputs are written: rows [H b / G, H (b+1) / G)
+  if (tid == 0 && !wait_count(a.hdr + kHdrDDone, (uint32_t)G)) timed_out = true;
   __syncthreads();
-  const int per_group = R * kGroupRows * 16;   // outputs of a full group
-  for (int i = tid; i < s_ndone * per_group; i += kDownThreads) {
-    const int d = i / per_group, rem = i - d * per_group;
-    const int rg = s_done[d];
-    const int r0 = rg * kGroupRows * 16;
-    const int r = rem / (kGroupRows * 16), row = r0 + (rem - r * (kGroupRows * 16));
-    if (row >= H) continue;   // a short last group
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tcols);
+  }
+  const int r0 = (int)(((long long)b * H) / G), r1 = (int)(((long long)(b + 1) * H) / G);
+  const int nrows = r1 - r0;
+  for (int i = tid; i < R * nrows; i += kMoeThreads) {
+    const int r = i / nrows, row = r0 + (i - r * nrows);
     const float* o = a.opart + (size_t)r * (1 + k) * H + row;
     // every load first (one round trip), then the fma chain in rank order
     float ov[kMaxTopK + 1], wv[kMaxTopK];
@@ -890,57 +837,54 @@ __global__ void __launch_bounds__(kDownThreads, 1) k4_down(const DownArgs a) {
       if (jj < k) yv = __fmaf_rn(wv[jj], ov[1 + jj], yv);
     a.y[(size_t)r * H + row] = f32_to_bf16_rne(yv);
   }
-  pdl_trigger();
-  if (timed_out && lane == 0) flag_status(a.status, kStatusTimeout);
+  if (timed_out && lane == 0) flag_status(status, kStatusTimeout);
 }
 
-template <typename K>
-cudaError_t set_smem(K kernel, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+size_t moe_smem(const MoeDims& d, int ring) {
+  const size_t region = std::max(moe_red_bytes(d.R), moe_h_bytes(d.I));
+  return 1024 + (size_t)ring * kStage + region;
 }
 
-template <int CT>
-size_t gate_up_smem(const MoeDims& d, int ring) {
-  return 1024 + (size_t)ring * gu_stage_bytes<CT>() + gu_red_bytes(d.R) +
-         (size_t)d.R * (2 * d.H + kXPad);
-}
-
-size_t down_smem(const MoeDims& d, int ring) {
-  return 1024 + (size_t)ring * kDownStage + (size_t)8 * down_hpitch(d.I);
-}
-
-// Deepest ring (kMaxRing .. lo stages) whose shared memory fits; 0 if none does.
-#ifndef DSMOE_RING_MAX
-#define DSMOE_RING_MAX kMaxRing
-#endif
-template <typename F>
-int pick_ring(F smem_of, int lo = 2, int hi = DSMOE_RING_MAX) {
-  for (int ring = hi; ring >= lo; --ring)
-    if (smem_of(ring) <= (size_t)device_max_smem_optin()) return ring;
+// Deepest ring (kMaxRing .. 2 stages) whose shared memory fits beside the kernel's static
+// shared memory (under 8 KB); 0 if none does.
+int moe_ring(const MoeDims& d) {
+  for (int ring = kMaxRing; ring >= 2; --ring)
+    if (moe_smem(d, ring) + 8 * 1024 <= (size_t)device_max_smem_optin()) return ring;
   return 0;
 }
 
-template <int CT>
-cudaError_t launch_gate_up_ct(const MoeDims& d, GateUpArgs& a, int ring, cudaStream_t s) {
-  const size_t smem = gate_up_smem<CT>(d, ring);
-  cudaError_t err = set_smem(k3_gate_up<CT>, smem);
+template <int KPER>
+cudaError_t launch_moe_k(const MoeArgs& a, size_t smem, cudaStream_t s) {
+  cudaError_t err = cudaFuncSetAttribute(k_moe<KPER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
   if (err != cudaSuccess) return err;
-  a.ring = ring;
-  return launch_pdl(k3_gate_up<CT>, device_sm_count(), kGuThreads, smem, s, a);
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_moe<KPER>, kMoeThreads, smem);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // one CTA per SM, all resident at once (cooperative launch)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(device_sm_count());
+  cfg.blockDim = dim3(kMoeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_moe<KPER>, a);
 }
 
 }  // namespace
 
-size_t gate_up_smem_bytes(const MoeDims& d) { return gate_up_smem<16>(d, 2); }
+bool moe_fits(const MoeDims& d) { return moe_ring(d) != 0; }
 
 MoeLayout moe_layout(const MoeDims& d) {
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
   MoeLayout L{};
   size_t off = 0;
-  L.header = off; off += 256;
-  const int ngr = ((d.H >> 4) + kGroupRows - 1) / kGroupRows;
-  L.counts = off; off += up(sizeof(uint32_t) * (size_t)ngr);
+  L.header = off; off += kMoeZeroBytes;
   L.zero_bytes = off;
   L.scores = off; off += up(sizeof(float) * (size_t)d.R * d.E);
   L.route = off; off += up(sizeof(RouteInfo));
@@ -963,54 +907,28 @@ cudaError_t launch_tile(const uint8_t* qs, const uint16_t* sc, int n_mats, int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_router(const MoeDims& d, const uint16_t* x, const uint16_t* router_w,
-                          int32_t* topk_idx, float* topk_w, const MoeWorkspace& ws,
-                          cudaStream_t s) {
-  // zero the header and the combine counts (a plain launch: it follows the stream's earlier
-  // work), then the router, which overlaps it
+cudaError_t launch_moe(const MoeDims& d, const uint16_t* x, const uint16_t* router_w,
+                       const uint8_t* gate, const uint8_t* up, const uint8_t* down,
+                       const uint8_t* sh_gate, const uint8_t* sh_up, const uint8_t* sh_down,
+                       int32_t* topk_idx, float* topk_w, uint16_t* y, const MoeWorkspace& ws,
+                       cudaStream_t s, cudaEvent_t after_prologue) {
+  // zero the header (status, arrival counts, flags): a plain launch, after the stream's
+  // earlier work
   k0_clear<<<1, 256, 0, s>>>(ws.header, (int)(ws.zero_bytes / 4));
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const int grid = (d.E + kRouterExperts - 1) / kRouterExperts;
-  auto* hdr = reinterpret_cast<WsHeader*>(ws.header);
-  if (d.E <= 12 * 32)
-    return launch_pdl(k1_router<12>, grid, kRouterWarps * 32, 0, s, x, d.R, d.H, router_w, d.E,
-                      d.k, ws.scores, topk_idx, topk_w, ws.route, hdr);
-  return launch_pdl(k1_router<kMaxExperts / 32>, grid, kRouterWarps * 32, 0, s, x, d.R, d.H,
-                    router_w, d.E, d.k, ws.scores, topk_idx, topk_w, ws.route, hdr);
-}
-
-cudaError_t launch_gate_up(const MoeDims& d, const uint16_t* x, const uint8_t* gate,
-                           const uint8_t* up, const uint8_t* sh_gate, const uint8_t* sh_up,
-                           const MoeWorkspace& ws, cudaStream_t s) {
-  GateUpArgs a{};
-  a.gate = gate; a.up = up; a.sh_gate = sh_gate; a.sh_up = sh_up;
-  a.x = x; a.route = ws.route; a.h = ws.h; a.status = ws.header;
-  a.R = d.R; a.H = d.H; a.I = d.I; a.k = d.k;
-  // Chunks of 32 tiles when a ring of at least 3 of them fits, else chunks of 16.
-#ifndef DSMOE_GU_CT
-#define DSMOE_GU_CT 32
-#endif
-  const int ring32 = DSMOE_GU_CT == 32 ? pick_ring([&](int r) { return gate_up_smem<32>(d, r); }, 3) : 0;
-  if (ring32) return launch_gate_up_ct<32>(d, a, ring32, s);
-  const int ring16 = pick_ring([&](int r) { return gate_up_smem<16>(d, r); });
-  if (ring16) return launch_gate_up_ct<16>(d, a, ring16, s);
-  return cudaErrorInvalidConfiguration;
-}
-
-cudaError_t launch_down(const MoeDims& d, const uint8_t* down, const uint8_t* sh_down,
-                        const float* topk_w, uint16_t* y, const MoeWorkspace& ws,
-                        cudaStream_t s) {
-  const int ring = pick_ring([&](int r) { return down_smem(d, r); });
+  if (after_prologue && (err = cudaEventRecord(after_prologue, s)) != cudaSuccess) return err;
+  const int ring = moe_ring(d);
   if (ring == 0) return cudaErrorInvalidConfiguration;
-  const size_t smem = down_smem(d, ring);
-  cudaError_t err = set_smem(k4_down, smem);
-  if (err != cudaSuccess) return err;
-  DownArgs a{};
-  a.down = down; a.sh_down = sh_down; a.h = ws.h; a.route = ws.route; a.topk_w = topk_w;
-  a.opart = ws.opart; a.counts = ws.counts; a.y = y; a.status = ws.header;
-  a.R = d.R; a.H = d.H; a.I = d.I; a.k = d.k; a.ring = ring;
-  return launch_pdl(k4_down, device_sm_count(), kDownThreads, smem, s, a);
+  MoeArgs a{};
+  a.x = x; a.router_w = router_w;
+  a.gate = gate; a.up = up; a.down = down; a.sh_gate = sh_gate; a.sh_up = sh_up; a.sh_down = sh_down;
+  a.scores = ws.scores; a.route = ws.route; a.h = ws.h; a.opart = ws.opart;
+  a.topk_idx = topk_idx; a.topk_w = topk_w; a.y = y; a.hdr = ws.header;
+  a.R = d.R; a.H = d.H; a.E = d.E; a.I = d.I; a.k = d.k; a.ring = ring;
+  const size_t smem = moe_smem(d, ring);
+  if (d.E <= 12 * 32) return launch_moe_k<12>(a, smem, s);
+  return launch_moe_k<kMaxExperts / 32>(a, smem, s);
 }
 
 }  // namespace dsmoe

@@ -133,17 +133,12 @@ def test_run_to_run_and_dirty_workspace(dsm, verify_case):
     assert dsm.workspace_status(ws) == 0
 
 
-def test_staging_limit_is_reported(dsm):
-    # R * (2H + 64) bytes of verify rows must fit in shared memory beside the weight ring
-    shape = synth.MoeShape(H=16384, E=2, I=64, k=1)
+def test_largest_hidden_size(dsm):
+    # hidden 16384 at R = 6: the verify rows' tensor-core fragments live in tensor memory
+    # (16 K chunks' worth fill its 512 columns), so shared memory holds only the ring
+    shape = synth.MoeShape(H=16384, E=4, I=64, k=2)
     d, x = make(shape, 6, 3)
-    layer = dsm.MoeLayer.from_dict(d, shape.k)
-    with pytest.raises(dsm.DsmoeError) as ei:
-        dsm.moe_verify_forward(layer, x)
-    assert ei.value.status == 2    # DS_ERR_UNSUPPORTED
-    y, _, _ = dsm.moe_verify_forward(layer, x[:2].contiguous())   # R = 2 fits
-    torch.cuda.synchronize()
-    assert torch.isfinite(y.float()).all()
+    check_case(dsm, d, host_layer(d), x, shape.k)
 
 
 def test_gpu_validation_errors(dsm):
