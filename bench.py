@@ -35,9 +35,10 @@ if str(ROOT) not in sys.path:
 
 import synth  # noqa: E402
 
-# Kernels one step launches: the MoE verify call (router, gate/up, down, combine) and the
+# Kernels one step launches: the MoE verify call (a prologue that zeroes the workspace
+# header, then one kernel: router, gate/up/SwiGLU, down projection, combine) and the
 # tensor-core select (compact, score, tau, collect, top-k, re-score, final select).
-MOE_KERNELS = 4
+MOE_KERNELS = 2
 SELECT_KERNELS = 7
 METRIC = "Q4 MoE verify weight GB/s (% of HBM peak) at R=1/6; top-512 select µs @300k ctx"
 UNIT = "GB/s"
@@ -324,7 +325,8 @@ def run_ours(args, world, rank, local):
     for i in range(K):
         step(i, "marked")
     torch.cuda.synchronize()
-    names = ["router", "gate_up", "down", "compact", "score", "topk"]
+    # marks: moe prologue, moe kernel (recorded twice), compact, score, top-k
+    names = ["moe_prologue", "moe", "moe_end", "compact", "score", "topk"]
     per = {n: [] for n in names}
     marked_ms = []
     for e in evs:
@@ -333,6 +335,8 @@ def run_ours(args, world, rank, local):
         for n, a, b in zip(names, prev, t):
             per[n].append(b - a)
         marked_ms.append(t[5])
+    del per["moe_end"]
+    names = [n for n in names if n != "moe_end"]
     idx_np = idx_all.cpu().numpy()
     unions = [union_size(idx_np[i]) for i in range(K)]
     moe_bytes = [moe_weight_bytes(shape, u) for u in unions]
@@ -414,9 +418,8 @@ def run_ours(args, world, rank, local):
 
     peak, peak_src = measured_peaks()
     kbytes = {
-        "router": [2.0 * shape.E * shape.H] * K,
-        "gate_up": [(1 + u) * 2.0 * shape.H * shape.I * Q4_BYTES_PER_WEIGHT for u in unions],
-        "down": [(1 + u) * 1.0 * shape.H * shape.I * Q4_BYTES_PER_WEIGHT for u in unions],
+        "moe_prologue": [0.0] * K,
+        "moe": moe_bytes,
         "compact": [sbytes["compact"]] * K, "score": [sbytes["score"]] * K,
         "topk": [sbytes["topk"]] * K,
     }
@@ -428,8 +431,8 @@ def run_ours(args, world, rank, local):
                       "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                       "share": round(float(np.sum(per[n]) / np.sum(marked_ms)), 4)}
     dom = max(kernels, key=lambda n: kernels[n]["share"])
-    src_of = {"router": "moe", "gate_up": "moe", "down": "moe", "compact": "select",
-              "score": "select", "topk": "select"}
+    src_of = {"moe_prologue": "moe", "moe": "moe", "compact": "select", "score": "select",
+              "topk": "select"}
     traffic, tnote = traffic_for(dom)
     roofline = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak,
                 "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": traffic,
@@ -450,11 +453,13 @@ def run_ours(args, world, rank, local):
         "pct_of_hbm_peak": round(100.0 * value / peak, 1),
         "components": {
             "moe_r6_gbs": round(value, 1), "moe_r6_us_median": round(1e3 * statistics.median(moe_ms), 2),
+            "moe_r6_us_p90": round(1e3 * float(np.percentile(moe_ms, 90)), 2),
             "moe_r6_union_mean": round(float(np.mean(unions)), 2),
             "moe_r6_weight_bytes_mean": float(np.mean(moe_bytes)),
             "moe_r1_gbs": round(r1_gbs, 1), "moe_r1_us_median": round(1e3 * statistics.median(r1_ms), 2),
             "moe_r1_pct_of_hbm_peak": round(100.0 * r1_gbs / peak, 1),
             "select_300k_us_median": round(1e3 * statistics.median(sel_ms), 2),
+            "select_300k_us_p90": round(1e3 * float(np.percentile(sel_ms, 90)), 2),
             "select_300k_bytes": sbytes["total"],
             "select_300k_gbs": round(sbytes["total"] / (statistics.median(sel_ms) / 1e3) / 1e9, 1),
             "select_300k_pct_of_hbm_peak": round(
@@ -480,28 +485,200 @@ def run_ours(args, world, rank, local):
         planar = synth.moe_layer(shape, seed=args.seed, device=dev)
         host = {k: synth.to_numpy_bits(v) for k, v in planar.items()}
         del planar
-        out["cpu_baseline"] = cpu_baseline(host, xs6[0], sel_host, shape, sshape)
+        out["cpu_baseline"] = cpu_baseline(host, xs6, sel_host, shape, sshape)
+    if not args.no_sweep and not args.skip_extras:
+        del layers, structs
+        torch.cuda.empty_cache()
+        out["sweep"] = decode_step_sweep(args, lib, dsm, dev, stream)
     return out
 
 
-def cpu_baseline(host, x, sel_host, shape, sshape) -> dict:
-    """The oracle, as it stands, on a bounded sample of the same workload, host cores."""
+def _timed(fn) -> float:
+    t = time.perf_counter()
+    fn()
+    return time.perf_counter() - t
+
+
+def cpu_baseline(host, xs, sel_host, shape, sshape) -> dict:
+    """The oracle, as it stands, on a bounded sample of the same workload, on the host cores:
+    one thread, and one thread per core over independent units (the oracle's C calls drop
+    Python's lock, so threads run in parallel): rows of verify calls for the MoE, layers of
+    the select."""
     import oracle
-    xb = synth.to_numpy_bits(x)
-    t = time.perf_counter()
-    ref = oracle.moe_forward(host, xb, shape.k)
-    dt = time.perf_counter() - t
-    gbs = moe_weight_bytes(shape, union_size(ref["idx"])) / dt / 1e9
-    keys = synth.to_numpy_bits(sel_host["keys"][:1])
-    q = synth.to_numpy_bits(sel_host["q"][:1])
-    t = time.perf_counter()
-    oracle.select(keys, q, sel_host["head_w"][:1].numpy(), sel_host["mask"][:1].numpy().view(np.uint32),
-                  sel_host["limit"][:1].numpy(), sshape.topk)
-    ds = time.perf_counter() - t
-    return {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"MoE: one R=6 verify call of one layer ({dt:.1f} s); select: 1 of 43 "
-                      f"layers at 300k ({ds:.1f} s), scaled x43",
-            "select_300k_us": round(ds * 43 * 1e6, 0)}
+    from concurrent.futures import ThreadPoolExecutor
+    nproc = os.cpu_count() or 1
+    x6 = [synth.to_numpy_bits(x) for x in xs]
+    ref = oracle.moe_forward(host, x6[0], shape.k)            # warm-up, and the union size
+    call_bytes = moe_weight_bytes(shape, union_size(ref["idx"]))
+    t1 = _timed(lambda: oracle.moe_forward(host, x6[0], shape.k))
+    gbs1 = call_bytes / t1 / 1e9
+    # all cores: nproc one-row jobs (rows of several verify calls), credited 1/R of a call
+    jobs = [x6[(j // R_VERIFY) % len(x6)][j % R_VERIFY:j % R_VERIFY + 1] for j in range(nproc)]
+    with ThreadPoolExecutor(nproc) as ex:
+        tp = _timed(lambda: list(ex.map(lambda xr: oracle.moe_forward(host, xr, shape.k), jobs)))
+    gbsp = call_bytes * (nproc / R_VERIFY) / tp / 1e9
+    keys = synth.to_numpy_bits(sel_host["keys"])
+    q = synth.to_numpy_bits(sel_host["q"])
+    hw = sel_host["head_w"].numpy()
+    mask = sel_host["mask"].numpy().view(np.uint32)
+    lim = sel_host["limit"].numpy()
+
+    def sel_layer(l):
+        oracle.select(keys[l:l + 1], q[l:l + 1], hw[l:l + 1], mask[l:l + 1], lim[l:l + 1], sshape.topk)
+
+    ds1 = _timed(lambda: sel_layer(0))
+    nl = min(nproc, sshape.L)
+    with ThreadPoolExecutor(nproc) as ex:
+        dsp = _timed(lambda: list(ex.map(sel_layer, range(nl))))
+    return {"value": round(gbs1, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"MoE: one R=6 verify call of one layer ({t1:.1f} s); select: 1 of 43 "
+                      f"layers at 300k ({ds1:.1f} s), scaled x43",
+            "select_300k_us": round(ds1 * sshape.L * 1e6, 0),
+            "all_cores": {"value": round(gbsp, 4), "unit": UNIT, "cores": nproc,
+                          "sample": f"MoE: {nproc} one-row verify calls in parallel threads "
+                                    f"({tp:.1f} s), credited 1/6 of an R=6 call each; select: "
+                                    f"{nl} layers in parallel ({dsp:.1f} s), scaled to 43",
+                          "select_300k_us": round(dsp * (sshape.L / nl) * 1e6, 0)},
+            "nproc": nproc}
+
+
+def decode_step_sweep(args, lib, dsm, dev, stream) -> dict:
+    """The full decode step: 43 distinct MoE layers resident in HBM (the verify layer's
+    shape, ~2.7 GB each) called back to back at R = 1, 2, 4, 6, the block select over 43
+    layers at 8k / 64k / 300k context, and weight bytes per committed token at draft
+    acceptance rates 0.5 / 0.7 / 0.9 (seeded Bernoulli draws). The 43-layer step is timed
+    both as stream launches and as one captured CUDA graph."""
+    shape = synth.VERIFY_MOE
+    per_layer = 2.0 * shape.E * shape.H + (shape.E + 1) * expert_bytes(shape)
+    free = torch.cuda.mem_get_info()[0]
+    L = int(min(43, max(1, (free - 24e9) // per_layer)))
+    sptr = stream.cuda_stream
+    t0 = time.perf_counter()
+    layers = []
+    for i in range(L):
+        d = synth.moe_layer(shape, seed=args.seed + 1000 + i, device=dev)
+        layers.append(dsm.MoeLayer.from_dict(d, shape.k))
+        del d
+    torch.cuda.synchronize()
+    structs = [l.struct() for l in layers]
+    gen_s = time.perf_counter() - t0
+    out = {"moe_layers": L, "layer_bytes": per_layer, "setup_s": round(gen_s, 1), "moe": {},
+           "select": {}}
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    reps, warm = 5, 2
+    for R in (1, 2, 4, 6):
+        xs = [synth.activations(R, shape.H, seed=args.seed + 3000 + 10 * R + i, device=dev)
+              for i in range(L)]
+        ws = torch.empty(lib.ds_moe_workspace_size(structs[0], R), dtype=torch.uint8, device=dev)
+        ys = [torch.empty((R, shape.H), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+        idx = torch.empty((L, R, shape.k), dtype=torch.int32, device=dev)
+        w = torch.empty((L, R, shape.k), dtype=torch.float32, device=dev)
+
+        def step():
+            for l in range(L):
+                st = lib.ds_moe_verify_forward(structs[l], xs[l].data_ptr(), R, ys[l].data_ptr(),
+                                               idx[l].data_ptr(), w[l].data_ptr(), ws.data_ptr(),
+                                               ws.numel(), sptr)
+                if st:
+                    raise RuntimeError(f"ds_moe_verify_forward: status {st}")
+
+        ts = []
+        for i in range(warm + reps):
+            a, b = ev(), ev()
+            a.record(stream)
+            step()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= warm:
+                ts.append(a.elapsed_time(b))
+        idx_np = idx.cpu().numpy()
+        step_bytes = sum(moe_weight_bytes(shape, union_size(idx_np[l])) for l in range(L))
+        us = 1e3 * statistics.median(ts)
+        entry = {"us_per_step": round(us, 1), "gbs": round(step_bytes / (us * 1e-6) / 1e9, 1),
+                 "weight_bytes_per_step": step_bytes, "per_layer_us": round(us / L, 2)}
+        # the same step captured as one CUDA graph
+        try:
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                sptr_c = cap.cuda_stream
+                with torch.cuda.graph(g, stream=cap):
+                    for l in range(L):
+                        lib.ds_moe_verify_forward(structs[l], xs[l].data_ptr(), R, ys[l].data_ptr(),
+                                                  idx[l].data_ptr(), w[l].data_ptr(), ws.data_ptr(),
+                                                  ws.numel(), sptr_c)
+            stream.wait_stream(cap)
+            tg = []
+            for i in range(warm + reps):
+                a, b = ev(), ev()
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                torch.cuda.synchronize()
+                if i >= warm:
+                    tg.append(a.elapsed_time(b))
+            gus = 1e3 * statistics.median(tg)
+            entry["graph_us_per_step"] = round(gus, 1)
+            entry["graph_gbs"] = round(step_bytes / (gus * 1e-6) / 1e9, 1)
+            del g
+        except Exception as e:  # capture not available: say so
+            entry["graph_us_per_step"] = None
+            entry["graph_error"] = str(e)[:120]
+        # weight bytes per committed token: 1 + leading accepted drafts among R - 1
+        for a_ in (0.5, 0.7, 0.9):
+            acc = synth.draft_acceptance(20000, R, a_, seed=args.seed)
+            lead = np.cumprod(acc, axis=1).sum(axis=1) if R > 1 else np.zeros(len(acc))
+            mean_c = float(np.mean(1 + lead))
+            closed = (1 - a_ ** R) / (1 - a_)
+            entry[f"a{a_}"] = {"committed_mean": round(mean_c, 4), "closed_form": round(closed, 4),
+                               "weight_bytes_per_committed_token": round(step_bytes / mean_c, 0)}
+        out["moe"][f"R{R}"] = entry
+        del xs, ys, ws
+    for name, N in (("8k", 2048), ("64k", 16000), ("300k", 75000)):
+        sh = synth.SelectShape(L=43, R=6, Hh=8, N=N, topk=512)
+        inp = synth.select_inputs(sh, seed=args.seed + 77, device=dev)
+        sa = dsm._select_struct(inp["keys"], inp["q"], inp["head_w"], inp["mask"], inp["limit"], 512)
+        ws = torch.empty(lib.ds_select_workspace_size(sa), dtype=torch.uint8, device=dev)
+        sel = torch.empty((43, 6, 512), dtype=torch.int32, device=dev)
+        nsel = torch.empty((43, 6), dtype=torch.int32, device=dev)
+        ts = []
+        for i in range(warm + 3 * reps):
+            a, b = ev(), ev()
+            a.record(stream)
+            st = lib.ds_select_blocks(sa, sel.data_ptr(), nsel.data_ptr(), None, None, ws.data_ptr(),
+                                      ws.numel(), sptr)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if st:
+                raise RuntimeError(f"ds_select_blocks: status {st}")
+            if i >= warm:
+                ts.append(a.elapsed_time(b))
+        out["select"][name] = {"blocks": N, "layers": 43, "us": round(1e3 * statistics.median(ts), 1)}
+        del inp, ws
+    # the single-layer 8k case
+    sh = synth.SELECT_8K
+    inp = synth.select_inputs(sh, seed=args.seed + 78, device=dev)
+    sa = dsm._select_struct(inp["keys"], inp["q"], inp["head_w"], inp["mask"], inp["limit"], 512)
+    ws = torch.empty(lib.ds_select_workspace_size(sa), dtype=torch.uint8, device=dev)
+    sel = torch.empty((1, 6, 512), dtype=torch.int32, device=dev)
+    nsel = torch.empty((1, 6), dtype=torch.int32, device=dev)
+    ts = []
+    for i in range(warm + 20):
+        a, b = ev(), ev()
+        a.record(stream)
+        lib.ds_select_blocks(sa, sel.data_ptr(), nsel.data_ptr(), None, None, ws.data_ptr(), ws.numel(), sptr)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= warm:
+            ts.append(a.elapsed_time(b))
+    out["select"]["8k_one_layer"] = {"blocks": 2048, "layers": 1, "us": round(1e3 * statistics.median(ts), 1)}
+    del layers, structs
+    torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------------- reference arm ----
@@ -559,6 +736,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--select-layers", type=int, default=43, help="layers of the 300k select")
     ap.add_argument("--skip-extras", action="store_true", help="no R=1 and end-to-end loops")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the 43-layer decode-step sweep (R=1/2/4/6, select 8k/64k/300k)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

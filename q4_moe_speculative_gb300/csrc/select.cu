@@ -1219,6 +1219,16 @@ __global__ void __launch_bounds__(kCollectThreads) k7b_collect(TopkArgs a) {
   // taken entries keep index order: a lane's place is the prefix over the lanes of their
   // counts (bit-sliced ballots).
   constexpr int U = 2;
+  // First test, in round-to-nearest arithmetic: x = fmaf(kn, G, s) must reach t*, the
+  // smallest score whose key reaches tau, less a margin. If the exact test passes (the
+  // upper bound RU(s + RU(kn G)) >= t*), then s + kn G >= t* - 2^-23 (|s + RU(kn G)| +
+  // kn G) less a subnormal quantum, and x lies within 2^-24 |x| of s + kn G, so
+  // t* - x <= 2^-22 (|x| + kn G) + 2^-126: the margin 2^-21 (|x| + kn G) + 2^-126 keeps
+  // every entry the exact test takes (and an entry the row does not admit, s = -inf,
+  // never passes). tau at or below the key of -inf takes every entry: no first test.
+  const bool take_all = tau <= 0x007FFFFFu;
+  const float tstar = key_score(tau);
+  const float crow = __fmaf_rn(0.000000476837158203125f, fabsf(tstar), 1.17549435e-38f);  // 2^-21 |t*| + 2^-126
   int cnt = 0, nlo = 0;
   uint4 sv[U];
   float4 kv[U];
@@ -1244,12 +1254,26 @@ __global__ void __launch_bounds__(kCollectThreads) k7b_collect(TopkArgs a) {
       const int i = g0 + u * 128 + 4 * lane;
       const uint32_t sb[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
       const float k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-      uint32_t hk[4];
+      unsigned pm = 0u;   // entries that pass the first test
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float sf = __uint_as_float(sb[e]);
+        const float ke = __fmul_rn(k4[e], G);
+        const float x = __fmaf_rn(k4[e], G, sf);
+        const bool pass =
+            take_all || __fsub_rn(tstar, x) <= __fmaf_rn(0.000000476837158203125f,
+                                                       __fadd_rn(fabsf(x), ke), crow);
+        pm |= (i + e < end && pass) ? 1u << e : 0u;
+      }
+      if (!__ballot_sync(0xffffffffu, pm != 0u)) continue;
+      uint32_t hk[4] = {0u, 0u, 0u, 0u};
       unsigned tm = 0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        hk[e] = tc_hi(sb[e], k4[e], G);
-        tm |= (i + e < end && hk[e] >= tau) ? 1u << e : 0u;
+        if (pm & (1u << e)) {
+          hk[e] = tc_hi(sb[e], k4[e], G);
+          tm |= hk[e] >= tau ? 1u << e : 0u;
+        }
       }
       if (__ballot_sync(0xffffffffu, tm != 0u)) {   // lo <= hi: only taken entries count
         const int c = __popc(tm);
