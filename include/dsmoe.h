@@ -275,6 +275,32 @@ ds_status ds_select_blocks_marked(const ds_select_args* args, int32_t* sel, int3
                                   size_t ws_bytes, ds_stream_t stream,
                                   const ds_event_t marks[3]);
 
+/* Parts of a select workspace that a completed tensor-core-mode call (flags 0) leaves for
+ * inspection, at the byte offsets ds_select_workspace_offset returns (NS = N rounded up
+ * to a multiple of 4):
+ *   DS_SELECT_WS_UNION       int32 [L][N]: per layer, the blocks some row admits, ascending
+ *                            (the first count entries are valid);
+ *   DS_SELECT_WS_UNION_COUNT int32 [L]: that count;
+ *   DS_SELECT_WS_SCORES      fp32 [L][R][NS]: the tensor-core score s of union entry e for
+ *                            row r (-inf where the row does not admit it). A row whose
+ *                            candidates overflow the bounded re-score holds canonical
+ *                            scores here instead;
+ *   DS_SELECT_WS_KEY_NORMS   fp32 [L][NS]: an upper bound kn of the union entry's key norm;
+ *   DS_SELECT_WS_ROW_SCALES  fp32 [L][R]: G, an upper bound of 2^-10 * sum_h |w_h| ||q_h||.
+ * The selection treats the canonical score as lying within kn * G of s (rounded outward).
+ * Valid once the call has completed and until the workspace is reused. */
+#define DS_SELECT_WS_UNION 0
+#define DS_SELECT_WS_UNION_COUNT 1
+#define DS_SELECT_WS_SCORES 2
+#define DS_SELECT_WS_KEY_NORMS 3
+#define DS_SELECT_WS_ROW_SCALES 4
+
+/* Byte offset of workspace part `part` for a call with these arguments that passes
+ * (with_compacted != 0) or does not pass its own cidx / ccount; (size_t)-1 when the
+ * arguments or the part are invalid. Host-only. */
+size_t ds_select_workspace_offset(const ds_select_args* args, int32_t with_compacted,
+                                  int32_t part);
+
 /* Synchronises `stream`, then reads the status word that the kernels of the last call on
  * this workspace left in its header: DS_OK, DS_ERR_TIMEOUT (a bounded device wait gave
  * up) or DS_ERR_DEVICE_CHECK (a device consistency check failed, e.g. an index out of

@@ -234,6 +234,30 @@ def select_blocks(keys, q, head_w, mask, limit, top_k: int = 512, *, sel=None, n
     return sel, nsel, cidx, ccount
 
 
+def select_workspace_views(keys, q, head_w, mask, limit, top_k: int, workspace: torch.Tensor,
+                           with_compacted: bool = False) -> dict:
+    """Views of what a completed tensor-core-mode select call left in `workspace`
+    (include/dsmoe.h): union [L,N] int32 and union_count [L]; scores [L,R,NS] fp32 by union
+    entry (-inf where the row does not admit it); key_norms [L,NS]; row_scales [L,R]."""
+    lib = N.load()
+    L, Nb, _ = keys.shape
+    R = q.shape[1]
+    NS = (Nb + 3) & ~3
+    args = _select_struct(keys, q, head_w, mask, limit, top_k)
+    shapes = {"union": ((L, Nb), torch.int32), "union_count": ((L,), torch.int32),
+              "scores": ((L, R, NS), torch.float32), "key_norms": ((L, NS), torch.float32),
+              "row_scales": ((L, R), torch.float32)}
+    out = {}
+    for name, (shape, dt) in shapes.items():
+        off = int(lib.ds_select_workspace_offset(args, 1 if with_compacted else 0,
+                                                 N.SELECT_WS_PARTS[name]))
+        n = 1
+        for d in shape:
+            n *= d
+        out[name] = workspace[off:off + 4 * n].view(dt).view(shape)
+    return out
+
+
 def moe_workspace_h(layer: MoeLayer, R: int, workspace: torch.Tensor) -> torch.Tensor:
     """View of the bf16 SwiGLU activations h [R, 1+k, I] that the last call left in
     `workspace` (slot 0 = shared expert, slot j+1 = the row's rank-j expert)."""

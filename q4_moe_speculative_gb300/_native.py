@@ -22,7 +22,9 @@ EXPORTS = (
     "ds_select_blocks", "ds_workspace_status", "ds_status_string", "ds_version",
     "ds_moe_verify_forward_marked", "ds_select_blocks_marked", "ds_moe_workspace_h_offset",
     "ds_moe_verify_forward_noalloc", "ds_noalloc_status", "ds_q4_tiled_bytes", "ds_q4_tile",
+    "ds_select_workspace_offset",
 )
+SELECT_WS_PARTS = {"union": 0, "union_count": 1, "scores": 2, "key_norms": 3, "row_scales": 4}
 
 DS_SELECT_CANONICAL_SCORES = 1
 DS_NOALLOC_SCRATCH_BYTES = 4 << 20  # same value as the C header's macro
@@ -101,6 +103,8 @@ def load() -> C.CDLL:
     lib.ds_noalloc_status.restype = C.c_int
     lib.ds_select_workspace_size.argtypes = [C.POINTER(DsSelectArgs)]
     lib.ds_select_workspace_size.restype = C.c_size_t
+    lib.ds_select_workspace_offset.argtypes = [C.POINTER(DsSelectArgs), C.c_int32, C.c_int32]
+    lib.ds_select_workspace_offset.restype = C.c_size_t
     lib.ds_select_blocks.argtypes = [
         C.POINTER(DsSelectArgs), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
         C.c_size_t, C.c_void_p]

@@ -180,6 +180,20 @@ size_t ds_select_workspace_size(const ds_select_args* args) {
   return sel_layout(sdims_of(args), false).total;
 }
 
+size_t ds_select_workspace_offset(const ds_select_args* args, int32_t with_compacted,
+                                  int32_t part) {
+  if (check_select(args) != DS_OK) return (size_t)-1;
+  const SelLayout L = sel_layout(sdims_of(args), with_compacted != 0);
+  switch (part) {
+    case DS_SELECT_WS_UNION: return L.uidx;
+    case DS_SELECT_WS_UNION_COUNT: return L.ucount;
+    case DS_SELECT_WS_SCORES: return L.cscore;
+    case DS_SELECT_WS_KEY_NORMS: return L.knorm;
+    case DS_SELECT_WS_ROW_SCALES: return L.qnorm;
+  }
+  return (size_t)-1;
+}
+
 ds_status ds_select_blocks(const ds_select_args* a, int32_t* sel, int32_t* nsel, int32_t* cidx,
                            int32_t* ccount, void* workspace, size_t ws_bytes,
                            ds_stream_t stream) {
