@@ -286,7 +286,7 @@ ds_status ds_select_blocks_marked(const ds_select_args* args, int32_t* sel, int3
  *                            candidates overflow the bounded re-score holds canonical
  *                            scores here instead;
  *   DS_SELECT_WS_KEY_NORMS   fp32 [L][NS]: an upper bound kn of the union entry's key norm;
- *   DS_SELECT_WS_ROW_SCALES  fp32 [L][R]: G, an upper bound of 2^-10 * sum_h |w_h| ||q_h||.
+ *   DS_SELECT_WS_ROW_SCALES  fp32 [L][R]: G, an upper bound of 2^-13 * sum_h |w_h| ||q_h||.
  * The selection treats the canonical score as lying within kn * G of s (rounded outward).
  * Valid once the call has completed and until the workspace is reused. */
 #define DS_SELECT_WS_UNION 0

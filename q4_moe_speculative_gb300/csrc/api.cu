@@ -227,15 +227,6 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
   ws.cscore = reinterpret_cast<float*>(base + L.cscore);
   ws.knorm = reinterpret_cast<float*>(base + L.knorm);
   ws.qnorm = reinterpret_cast<float*>(base + L.qnorm);
-  ws.tau = reinterpret_cast<uint32_t*>(base + L.tau);
-  ws.ccnt = reinterpret_cast<int32_t*>(base + L.ccnt);
-  ws.clo = reinterpret_cast<int32_t*>(base + L.clo);
-  ws.creg = reinterpret_cast<int32_t*>(base + L.creg);
-  ws.rcand = reinterpret_cast<int32_t*>(base + L.rcand);
-  ws.rkey = reinterpret_cast<uint32_t*>(base + L.rkey);
-  ws.rlist = reinterpret_cast<int32_t*>(base + L.rlist);
-  ws.rcount = reinterpret_cast<int32_t*>(base + L.rcount);
-  ws.rtask = reinterpret_cast<int32_t*>(base + L.rtask);
   const bool tc = !(a->flags & DS_SELECT_CANONICAL_SCORES) &&
                   tc_scoring_supported(d, a->keys, a->q);
 

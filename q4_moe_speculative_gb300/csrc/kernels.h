@@ -80,30 +80,14 @@ struct SelWorkspace {
                       // (-inf where the row does not admit the entry)
   float* knorm;       // [L][NS] by union entry: key norm bound (tensor-core scoring)
   float* qnorm;       // [L][R] sum_h |w_h| ||q_h|| bound (tensor-core scoring)
-  uint32_t* tau;      // [L][R] sampled collection threshold (top-k, tensor-core scoring)
-  int32_t* ccnt;      // [L][R][kTopkChunks] entries collected per row chunk
-  int32_t* clo;       // [L][R][kTopkChunks] entries with a lower bound >= tau per chunk
-  int32_t* creg;      // [3][L][R][kTopkChunks][kTopkChunkCap] collected entries in index
-                      // order: block id, lower bound key, upper bound key
-  int32_t* rcand;     // [L][R][kTopkCandCap] re-score candidates in index order (block ids)
-  uint32_t* rkey;     // [L][R][kTopkCandCap] their keys (certain, or the canonical score's)
-  int32_t* rlist;     // [L][R][kTopkCandCap][2] uncertain candidates: position, block id
-  int32_t* rcount;    // [L][R][2] candidates (-1: the row is complete), uncertain ones
-  int32_t* rtask;     // [L][R * kTopkCandCap / 32][2] re-score tasks: row * 128 + part, count
 };
 
-constexpr int kTopkChunks = 8;        // collect CTAs (2 warps) per row: 2064 at 43 x 6 rows,
-                                      // 13 or 14 per SM in one wave
-constexpr int kTopkChunkCap = 1024;   // collected entries kept per row chunk (x8 = 8192)
-constexpr int kTopkCandCap = 4096;    // re-score candidates per row
 // Row stride of the score arrays (cscore, knorm): N rounded up to a multiple of 4, so that
 // every row starts 16-byte aligned.
 inline int score_stride(int N) { return (N + 3) & ~3; }
 
 struct SelLayout {
-  size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, knorm, qnorm, tau, ccnt, clo,
-      creg,
-      rcand, rkey, rlist, rcount, rtask, total;
+  size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, knorm, qnorm, total;
 };
 SelLayout sel_layout(const SelDims& d, bool caller_cidx);
 bool tc_scoring_supported(const SelDims& d, const uint16_t* keys, const uint16_t* q);

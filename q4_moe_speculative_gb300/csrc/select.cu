@@ -13,9 +13,9 @@
 //  K5  scores every union entry for the rows that admit it; results are stored by union
 //      position [layer][row][entry]. Rows that do not admit an entry get a sentinel that
 //      sorts below every score.
-//  K7  per (layer, row): bounded radix top-k over the union entries (tensor-core mode: K7a
-//      sampled threshold, K7b collection, K7 candidates, K7r re-score over the whole GPU,
-//      K7c final select).
+//  K7  per (layer, row): bounded radix top-k over the union entries, in one CTA (tensor-core
+//      mode: sampled threshold, collection, candidates, canonical re-score of the uncertain
+//      ones, final select).
 //
 // Two scoring modes give the same selection:
 //  * canonical: every score in the canonical fp32 order (fmaf over i ascending, then over
@@ -24,14 +24,18 @@
 //    [128 x 128] x [128 x R*Hh] bf16 contraction on tcgen05 (keys gathered by cp.async into
 //    the 128-byte swizzled K-major layout, queries likewise, fp32 accumulators in TMEM),
 //    giving an interval [lo, hi] that contains the canonical score:
-//    |s_tc - s_canon| <= eps = 2^-10 * ||k|| * sum_h |w_h| ||q_h||. (Both dot products are
-//    sums of exact products whose magnitudes add up to at most ||q|| ||k||; a few hundred
-//    fp32 roundings of such sums stay below 2^-15 of that, so 2^-10 leaves a margin of 2^5.)
+//    |s_tc - s_canon| <= eps = 2^-13 * ||k|| * sum_h |w_h| ||q_h||. Both dot products are
+//    sums of 128 exact products whose magnitudes add up to at most ||q_h|| ||k||: the
+//    canonical chain rounds 128 times (at most 2^-17 of that sum); the tensor core adds 8
+//    groups of 16 products to an fp32 accumulator, and even 16 units in the last place of
+//    that sum per group (far more than the hardware loses) stay below 2^-16 of it. The
+//    two sums over the heads add 2 x 8 roundings of terms below |w_h| ||q_h|| ||k|| (2^-20).
+//    In all at most 2^-15.2 of ||k|| sum_h |w_h| ||q_h||, so 2^-13 leaves a margin above 4.
 //    K5 stores s_tc per admitting row and ||k|| per entry; every consumer derives [lo, hi]
 //    with the same function (tc_lo / tc_hi), so the bounds agree bit for bit. K7 takes
 //    T = k-th largest lo; every block of the canonical top-k has hi >= T, so only the
-//    candidates with hi >= T are re-scored in the canonical order (K7r) and selected among
-//    exactly (K7c). The result is identical to the canonical mode by construction.
+//    candidates with hi >= T are re-scored in the canonical order and selected among
+//    exactly. The result is identical to the canonical mode by construction.
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -45,10 +49,10 @@ constexpr int kScoreMaxHeads = 16;
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kResidCap = 4096;      // residual radix bucket kept in shared memory
-constexpr int kCandCap = kTopkCandCap;   // re-score candidates kept in shared memory
+constexpr int kCandCap = 4096;       // re-score candidates kept in shared memory
 constexpr int kCollectCap = 4096;    // entries collected by the sampled-threshold pass
 constexpr uint32_t kWaitPolls = 1u << 17;   // bounded mbarrier polling (<= ~0.13 s)
-constexpr float kEpsRel = 0.0009765625f;    // 2^-10
+constexpr float kEpsRel = 0.0001220703125f;  // 2^-13
 constexpr uint32_t kNoScoreKey = 0u;        // sorts below the key of every score
 constexpr uint32_t kMinusInfBits = 0xFF800000u;
 
@@ -121,7 +125,7 @@ constexpr uint32_t kCertainKey = 0xFFFFFFFFu;   // above the key of every finite
 
 // Interval [lo, hi] (order keys) around a tensor-core score s (fp32 bits) that contains the
 // canonical score: eps = kn * G rounded upward (kn the key norm bound, G the row's
-// 2^-10 * sum_h |w_h| ||q_h|| rounded upward), lo = s - eps rounded downward, hi = s + eps
+// 2^-13 * sum_h |w_h| ||q_h|| rounded upward), lo = s - eps rounded downward, hi = s + eps
 // rounded upward. An entry the row does not admit (s = -inf) gets lo = kNoScoreKey and
 // hi = the key of -inf.
 __device__ __forceinline__ uint32_t tc_lo(uint32_t sbits, float kn, float G) {
@@ -139,8 +143,13 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Place of head h among the kScoreMaxHeads query values of one element in the fp32 query
+// layout of the top-k: heads h = 4j + t at t * 4 + j, so that thread t of a candidate's four
+// reads the values of its heads t, t + 4, t + 8, t + 12 as one 16-byte word.
+__host__ __device__ constexpr int qslot(int h) { return (h & 3) * 4 + (h >> 2); }
+
 // Canonical score of one block: q fp32 (shared) in the layout [i][kScoreMaxHeads] (value i
-// of head h at i * kScoreMaxHeads + h), key 128 bf16 (global), w [Hh].
+// of head h at i * kScoreMaxHeads + qslot(h)), key 128 bf16 (global), w [Hh].
 __device__ __forceinline__ float canonical_score(const float* q, const uint16_t* key,
                                                  const float* w, int Hh) {
   float d[kScoreMaxHeads];
@@ -160,7 +169,7 @@ __device__ __forceinline__ float canonical_score(const float* q, const uint16_t*
 #pragma unroll
       for (int h = 0; h < kScoreMaxHeads; ++h) {
         if (h < Hh) {
-          const float* qh = q + ((half * 8 + c) * 8) * kScoreMaxHeads + h;
+          const float* qh = q + ((half * 8 + c) * 8) * kScoreMaxHeads + qslot(h);
           float t = d[h];
 #pragma unroll
           for (int e = 0; e < 8; ++e) t = __fmaf_rn(qh[e * kScoreMaxHeads], kf[e], t);
@@ -328,7 +337,7 @@ struct ScoreArgs {
   const int32_t* uwordoff;
   uint32_t* sc0;      // [L][R][NS] by union entry: fp32 scores (-inf: not admitted)
   float* knorm;       // [L][NS] by union entry: key norm bound (tensor-core mode)
-  float* qnorm;       // [L][R] 2^-10 sum_h |w_h| ||q_h|| bound (tensor-core mode)
+  float* qnorm;       // [L][R] 2^-13 sum_h |w_h| ||q_h|| bound (tensor-core mode)
   uint32_t* status;
   int tma;            // kmap is valid: tiles of 128 consecutive blocks come by TMA
   CUtensorMap kmap;   // keys [L][N][128] bf16, boxes of 64 values x 128 blocks, 128B swizzle
@@ -428,6 +437,20 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
                : "memory");
 }
 
+// The same with an L2 eviction-priority hint: streamed data (read once) goes first, so that
+// the scores written meanwhile stay in L2 for the top-k that reads them next.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, bool valid,
+                                                uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint.L2::256B [%0], [%1], 16, %2, %3;" ::"r"(dst),
+               "l"(src), "r"(valid ? 16 : 0), "l"(policy)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------------
 // K5 (tensor-core mode): one persistent CTA per SM scores a contiguous range of the
 // layers' union tiles (128 union entries each). Roles:
@@ -468,6 +491,10 @@ struct TcGeom {
   static constexpr int kLag = kStages - kTcGroups;   // tiles in flight behind the newest
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kKeyBytes + 2 * (size_t)kQBytes;
   static_assert(kLag >= 1, "stage ring too small");
+  // tcgen05.alloc takes a power of two of at least 32 columns
+  static constexpr uint32_t kTmemCols = kTcGroups * kCols;
+  static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
+                "TMEM allocation must be a power of two");
 };
 
 __device__ __forceinline__ void cp_async_commit() {
@@ -540,6 +567,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ float s_w[2][NPAD];
+  __shared__ float s_wg[kTcGroups][NPAD];       // each epilogue group's copy of its layer's w
   __shared__ float s_F[2][8];
   __shared__ float s_qn[NPAD];
   __shared__ int s_tl[S], s_te[S], s_tn[S];     // per stage: layer, first entry, entry count
@@ -572,7 +600,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
     sm100::fence_mbar_init();
   }
   if (warp == 0) {
-    sm100::tmem_alloc(&s_tmem, kTcGroups * kCols);
+    sm100::tmem_alloc(&s_tmem, G::kTmemCols);
     sm100::tmem_relinquish();
   }
   sm100::tc_fence_before();
@@ -590,6 +618,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
   if (warp < kTcProducerWarps) {
     // ------------------------------------------------------------- producers -----
     const int pw = warp;
+    const uint64_t kpol = l2_evict_first_policy();   // keys are read once
     int l = cl, e0 = ce;
     int lcnt = a.ucount[cl];    // entry count of layer l
     int qlayer[2] = {-1, -1};   // layer staged in each query slot
@@ -750,7 +779,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
             const int b = __shfl_sync(0xffffffffu, cur.id, rr);
             const uint32_t dst = sa + (uint32_t)(c >> 3) * (kKeyBytes / 2) +
                                  (uint32_t)r * 128u + (uint32_t)(((c & 7) ^ (r & 7)) << 4);
-            cp_async16(dst, kbase8 + (size_t)b * 256 + c * 16, e0 + r < cur.ucnt);
+            cp_async16_hint(dst, kbase8 + (size_t)b * 256 + c * 16, e0 + r < cur.ucnt, kpol);
           }
           cp_async_commit();
         }
@@ -779,6 +808,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
     const uint32_t tbuf = tmem + (uint32_t)g * kCols;
     uint32_t mphase = 0;
     bool issued = false;    // this group has MMAs whose commit it has not observed
+    int wlayer = -1;        // layer whose head weights s_wg[g] holds
     for (int i = g; i < n; i += kTcGroups) {
       const int s = i % S;
       bool ok = !s_abort && sm100::mbar_wait(&bar_full[s], (i / S) & 1, kWaitPolls);
@@ -790,6 +820,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
       const int l = s_tl[s], e0 = s_te[s], ucnt = s_tn[s];
       const int slot = l & 1;
       const uint32_t sa = base + (uint32_t)s * kKeyBytes;
+      if (l != wlayer) {
+        // the group's own copy of the head weights: the stage (and with it the query slot)
+        // is released before the scores are formed, and the producer may then refill it
+        const int t = (warp & 3) * 32 + lane;
+        if (t < NPAD) s_wg[g][t] = s_w[slot][t];
+        asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(128) : "memory");
+        wlayer = l;
+      }
       if (leader) {
         sm100::tc_fence_after();
         fence_proxy_async();
@@ -834,6 +872,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
       }
       issued = false;
       mphase ^= 1u;
+      // keys, queries and weights of the stage are read (the MMAs are complete and this
+      // thread's key norm is formed): release it before the scores are formed
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&bar_empty[s]);
       sm100::tc_fence_after();
       float d[NPAD];
       const uint32_t lane_base = tbuf + ((uint32_t)((warp & 3) * 32) << 16);
@@ -857,7 +899,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
 #pragma unroll
               for (int h = 0; h < HH; ++h) {
                 const float v = d[r * HH + h];
-                sc = __fmaf_rn(s_w[slot][r * HH + h], v > 0.0f ? v : 0.0f, sc);
+                sc = __fmaf_rn(s_wg[g][r * HH + h], v > 0.0f ? v : 0.0f, sc);
               }
               emit(r, sc);
             }
@@ -870,22 +912,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
 #pragma unroll
             for (int p = 0; p < NPAD; ++p) {
               const float v = d[p];
-              const float t = __fmaf_rn(s_w[slot][p], v > 0.0f ? v : 0.0f, sc);
+              const float t = __fmaf_rn(s_wg[g][p], v > 0.0f ? v : 0.0f, sc);
               sc = (p >= p0 && p < p1) ? t : sc;
             }
             emit(r, sc);
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive1(&bar_empty[s]);   // keys, queries and weights read
     }
     // MMAs issued but never observed complete: wait (bounded) before TMEM is freed
     if (issued) sm100::mbar_wait(&bar_mma[g], mphase, kWaitPolls);
   }
   sm100::tc_fence_before();
   __syncthreads();
-  if (warp == 0) sm100::tmem_dealloc(tmem, kTcGroups * kCols);
+  if (warp == 0) sm100::tmem_dealloc(tmem, G::kTmemCols);
 }
 
 // ---------------------------------------------------------------------------------
@@ -1098,14 +1138,27 @@ __device__ int ordered_take(int n, int need, Cls cls, Emit emit, int* s_eq, int*
 }
 
 // ---------------------------------------------------------------------------------
-// K7: bounded radix top-k per (layer, row), one CTA of 512 threads, over the layer's
-// union entries (entries the row does not admit carry the sentinel and never qualify).
+// K7: bounded radix top-k, one CTA of 512 threads per (layer, row), over the layer's union
+// entries (entries the row does not admit carry the sentinel and never qualify).
 // Canonical mode: threshold and ordered take over the canonical scores.
-// Tensor-core mode: threshold T over the lower bounds; ordered gather of the candidates
-// with upper bound >= T (bounded by kCandCap), the certain ones marked; the canonical
-// re-score of the others (K7r, over the whole GPU) and the threshold and ordered take
-// among the candidates (K7c) follow. Above the bound: canonical re-score of every
-// admitted entry of the row, then the canonical-mode path, here.
+// Tensor-core mode, all inside the CTA:
+//  1. tau, a collection threshold at or below the K-th largest lower bound: from a sample
+//     of 2048 entries (64 chunks of 32, evenly spaced), the key of the sample's rank-th
+//     largest lower bound, rank = K scaled to the sample plus 16 (about 800 of the row's
+//     entries lie above it at 300k context), to two digits (the bucket's lower bound).
+//     Rows that fit the collection whole take tau = 0.
+//  2. collection: the entries whose upper bound reaches tau, in index order, with their
+//     bounds, and how many of them have a lower bound >= tau. Each warp walks a contiguous
+//     segment and keeps its matches in shared memory; the warps' lists are concatenated.
+//  3. If at least K lower bounds reach tau, the K-th largest lower bound T of the row is
+//     among the collected entries and so is every candidate (upper bound >= T). Otherwise
+//     (or on overflow) T and the candidates come from two passes over the whole row.
+//  4. Candidates whose lower bound exceeds H (below) are selected whatever the exact scores;
+//     the others are re-scored in the canonical order.
+//  5. The exact select among the candidates: threshold over their keys (the certain ones
+//     carry the largest key) and the ordered take, ties to the lowest index.
+// With more candidates than the CTA keeps: canonical re-score of every admitted entry of
+// the row, then the canonical-mode path.
 // ---------------------------------------------------------------------------------
 struct TopkArgs {
   int R, Hh, N, K;
@@ -1124,239 +1177,53 @@ struct TopkArgs {
   int32_t* nsel;
   uint32_t* status;
   int tc_mode;
-  uint32_t* tau;
-  int32_t* ccnt;
-  int32_t* clo;
-  int32_t* creg;
-  int32_t* rcand;
-  uint32_t* rkey;
-  int32_t* rlist;
-  int32_t* rcount;
-  int32_t* rtask;
   int NS;             // row stride of sc0 / knorm (N rounded up to a multiple of 4)
 };
 
-constexpr uint32_t kTauDirect = 0xFFFFFFFFu;   // row with at most K admitted: no collection
-// Words of the workspace header (word 0 is the status word; the header is zeroed per call):
-// the number of re-score tasks listed by K7 and the next task K7r hands out.
-constexpr int kRescoreTasks = 1;
-constexpr int kRescoreNext = 2;
-
-// ---------------------------------------------------------------------------------
-// K7a: per (layer, row), a collection threshold tau at or below the K-th largest lower
-// bound, from a sample of 2048 entries (64 chunks of 32, evenly spaced): the key of the
-// sample's rank-th largest lower bound, rank = K of the row scaled to the sample plus 16
-// (about 800 of the row's entries at 300k context, so that at least K lie above it with
-// a wide margin), to two digits (the bucket's lower bound). Rows that fit the collection
-// whole get tau = 0.
-// ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kTopkThreads) k7a_tau(TopkArgs a) {
-  __shared__ int hist[512];   // two radix histogram buffers
-  __shared__ int scratch[33];
-  __shared__ int s_misc[4];
-  __shared__ uint32_t samp[2048];
-  pdl_wait();   // the scores and the compaction are complete
-  const int lr = blockIdx.x, l = lr / a.R, tid = threadIdx.x;
-  const int K = a.K;
-  if (a.ccount[lr] <= K) {
-    if (tid == 0) a.tau[lr] = kTauDirect;
-    return;
-  }
-  const int n = a.ucount[l];
-  uint32_t tau = 0u;
-  if (n > kCollectCap) {
-    constexpr int kChunks = 64, kS = kChunks * 32;
-    const uint32_t* s0 = a.sc0 + (size_t)lr * a.NS;
-    const float* kn = a.knorm + (size_t)l * a.NS;
-    const float G = a.qnorm[lr];   // eps per unit key norm
-    const int spacing = n / kChunks;
-    for (int j = tid; j < kS; j += blockDim.x) {
-      const int i = (j >> 5) * spacing + (j & 31);
-      samp[j] = tc_lo(s0[i], kn[i], G);
-    }
-    __syncthreads();
-    const int rank = min(kS, (int)(((long long)K * kS + n - 1) / n) + 16);
-    int need;
-    tau = radix_threshold(kS, rank, [&](int j) { return samp[j]; }, hist, scratch, nullptr,
-                          s_misc, a.status, &need, 2);
-  }
-  if (tid == 0) a.tau[lr] = tau;
-  pdl_trigger();
-}
-
-// ---------------------------------------------------------------------------------
-// K7b: per (layer, row, chunk of the row's union entries): the entries whose upper bound
-// reaches tau, as block ids with their lower and upper bound keys, in index order in the
-// chunk's region
-// (each warp keeps its matches in shared memory, then the warps' lists are concatenated),
-// and how many entries have a lower bound >= tau. A chunk with more matches than its
-// region (or a warp with more than its buffer) reports a count above the capacity.
-// ---------------------------------------------------------------------------------
-constexpr int kCollectThreads = 64;
-constexpr int kCollectWarps = kCollectThreads / 32;
-constexpr int kWarpBuf = 256;
-
-__global__ void __launch_bounds__(kCollectThreads) k7b_collect(TopkArgs a) {
-  __shared__ int s_cnt[kCollectWarps], s_lo[kCollectWarps];
-  __shared__ uint32_t s_buf[kCollectWarps][3][kWarpBuf];
-  const int lr = blockIdx.x / kTopkChunks, chunk = blockIdx.x - lr * kTopkChunks;
-  const int l = lr / a.R, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait();   // tau of every row is complete
-  const uint32_t tau = a.tau[lr];
-  if (tau == kTauDirect) return;
-  const int n = a.ucount[l];
-  // chunks and warp segments start at multiples of 4 entries: 16-byte aligned in the rows
-  const int per = ((n + kTopkChunks - 1) / kTopkChunks + 127) & ~127;
-  const int c0 = min(n, chunk * per), c1 = min(n, c0 + per);
-  const uint32_t* s0 = a.sc0 + (size_t)lr * a.NS;
-  const float* kn = a.knorm + (size_t)l * a.NS;
-  const float G = a.qnorm[lr];   // eps per unit key norm
-  const int seg = ((c1 - c0 + kCollectWarps - 1) / kCollectWarps + 127) & ~127;
-  const int beg = min(c1, c0 + warp * seg), end = min(c1, beg + seg);
-  // Each lane takes 4 consecutive entries of a group of 128 (16-byte loads; entries past
-  // `end` in the last group lie inside the row's padded stride and are masked). U groups
-  // per batch; the next batch's loads are in flight while this one is classified. The
-  // taken entries keep index order: a lane's place is the prefix over the lanes of their
-  // counts (bit-sliced ballots).
-  constexpr int U = 2;
-  // First test, in round-to-nearest arithmetic: x = fmaf(kn, G, s) must reach t*, the
-  // smallest score whose key reaches tau, less a margin. If the exact test passes (the
-  // upper bound RU(s + RU(kn G)) >= t*), then s + kn G >= t* - 2^-23 (|s + RU(kn G)| +
-  // kn G) less a subnormal quantum, and x lies within 2^-24 |x| of s + kn G, so
-  // t* - x <= 2^-22 (|x| + kn G) + 2^-126: the margin 2^-21 (|x| + kn G) + 2^-126 keeps
-  // every entry the exact test takes (and an entry the row does not admit, s = -inf,
-  // never passes). tau at or below the key of -inf takes every entry: no first test.
-  const bool take_all = tau <= 0x007FFFFFu;
-  const float tstar = key_score(tau);
-  const float crow = __fmaf_rn(0.000000476837158203125f, fabsf(tstar), 1.17549435e-38f);  // 2^-21 |t*| + 2^-126
-  int cnt = 0, nlo = 0;
-  uint4 sv[U];
-  float4 kv[U];
-  const uint4 kNone = make_uint4(kMinusInfBits, kMinusInfBits, kMinusInfBits, kMinusInfBits);
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int i = beg + u * 128 + 4 * lane;
-    sv[u] = i < end ? *reinterpret_cast<const uint4*>(s0 + i) : kNone;
-    kv[u] = i < end ? *reinterpret_cast<const float4*>(kn + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  const unsigned lt = (1u << lane) - 1u;
-  for (int g0 = beg; g0 < end; g0 += 128 * U) {
-    uint4 sn[U];
-    float4 kx[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = g0 + 128 * U + u * 128 + 4 * lane;
-      sn[u] = i < end ? *reinterpret_cast<const uint4*>(s0 + i) : kNone;
-      kx[u] = i < end ? *reinterpret_cast<const float4*>(kn + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = g0 + u * 128 + 4 * lane;
-      const uint32_t sb[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
-      const float k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-      unsigned pm = 0u;   // entries that pass the first test
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float sf = __uint_as_float(sb[e]);
-        const float ke = __fmul_rn(k4[e], G);
-        const float x = __fmaf_rn(k4[e], G, sf);
-        const bool pass =
-            take_all || __fsub_rn(tstar, x) <= __fmaf_rn(0.000000476837158203125f,
-                                                       __fadd_rn(fabsf(x), ke), crow);
-        pm |= (i + e < end && pass) ? 1u << e : 0u;
-      }
-      if (!__ballot_sync(0xffffffffu, pm != 0u)) continue;
-      uint32_t hk[4] = {0u, 0u, 0u, 0u};
-      unsigned tm = 0u;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (pm & (1u << e)) {
-          hk[e] = tc_hi(sb[e], k4[e], G);
-          tm |= hk[e] >= tau ? 1u << e : 0u;
-        }
-      }
-      if (__ballot_sync(0xffffffffu, tm != 0u)) {   // lo <= hi: only taken entries count
-        const int c = __popc(tm);
-        const unsigned b0 = __ballot_sync(0xffffffffu, c & 1);
-        const unsigned b1 = __ballot_sync(0xffffffffu, c & 2);
-        const unsigned b2 = __ballot_sync(0xffffffffu, c & 4);
-        int p = cnt + __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (tm & (1u << e)) {
-            const uint32_t lk = tc_lo(sb[e], k4[e], G);
-            nlo += lk >= tau ? 1 : 0;
-            if (p < kWarpBuf) {
-              s_buf[warp][0][p] = (uint32_t)(i + e);
-              s_buf[warp][1][p] = lk;
-              s_buf[warp][2][p] = hk[e];
-            }
-            ++p;
-          }
-        }
-        cnt += __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      sv[u] = sn[u];
-      kv[u] = kx[u];
-    }
-  }
-  nlo = __reduce_add_sync(0xffffffffu, nlo);
-  if (lane == 0) { s_cnt[warp] = cnt; s_lo[warp] = nlo; }
-  __syncthreads();
-  int off = 0, total = 0, lo_total = 0;
-  bool over = false;
-  for (int w = 0; w < kCollectWarps; ++w) {
-    if (w == warp) off = total;
-    total += s_cnt[w];
-    lo_total += s_lo[w];
-    over |= s_cnt[w] > kWarpBuf;
-  }
-  const size_t rc = (size_t)lr * kTopkChunks + chunk;
-  if (over || total > kTopkChunkCap) {
-    if (tid == 0) { a.ccnt[rc] = kTopkChunkCap + 1; a.clo[rc] = lo_total; }
-    return;
-  }
-  if (tid == 0) { a.ccnt[rc] = total; a.clo[rc] = lo_total; }
-  pdl_trigger();
-  const size_t plane = (size_t)gridDim.x * kTopkChunkCap;   // (L R chunks) x capacity
-  int32_t* reg = a.creg + rc * kTopkChunkCap;
-  const int32_t* ui = a.uidx + (size_t)l * a.N;
-  for (int p = lane; p < cnt; p += 32) {
-    reg[off + p] = ui[s_buf[warp][0][p]];   // the entry's block id
-    reg[plane + off + p] = (int32_t)s_buf[warp][1][p];
-    reg[2 * plane + off + p] = (int32_t)s_buf[warp][2][p];
-  }
-}
+constexpr int kWarpBuf = 256;   // collected entries a warp keeps before the lists merge
+constexpr int kRescoreRound = kTopkThreads / 4;   // uncertain candidates re-scored per round
+constexpr int kRescorePitch = 272;   // bytes per staged key row (16-byte reads spread over banks)
+// dynamic shared memory of K7: residual keys, candidates and their keys, the row's queries
+// (fp32, [i][head]) and head weights, the collection (block id, lower and upper bound key)
+constexpr size_t kTopkSmem = sizeof(uint32_t) * kResidCap + sizeof(int32_t) * 2 * kCandCap +
+                             sizeof(float) * (kScoreMaxHeads * 128 + kScoreMaxHeads) +
+                             sizeof(int32_t) * 3 * kCollectCap;
+// the warps' collection lists live over the residual keys and the candidates
+static_assert((size_t)3 * kTopkWarps * kWarpBuf <= (size_t)kResidCap + 2 * kCandCap,
+              "collection lists overlap the queries");
+static_assert(kCollectCap >= 2048, "the tau sample lives over the collection");
+static_assert((size_t)kRescoreRound * kRescorePitch <= sizeof(int32_t) * 3 * kCollectCap,
+              "key staging overlaps past the collection");
+static_assert(kScoreMaxHeads == 16, "four threads of four heads each per candidate");
 
 __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   __shared__ int hist[512];   // two radix histogram buffers
   __shared__ int scratch[33];
   __shared__ int s_misc[4];
   __shared__ int s_eq[kTopkWarps], s_gt[kTopkWarps];
-  __shared__ uint32_t r_key[kResidCap];
-  extern __shared__ uint8_t dsm[];
-  int32_t* cand = reinterpret_cast<int32_t*>(dsm);               // [kCandCap] entries
-  uint32_t* ckey = reinterpret_cast<uint32_t*>(cand + kCandCap);  // [kCandCap] keys
-  float* qf = reinterpret_cast<float*>(ckey + kCandCap);          // [Hh][128]
-  float* wf = qf + kScoreMaxHeads * 128;                          // [Hh]
-  // the collected entries in index order (block ids), with their lower and upper bound keys
+  __shared__ int s_cnt[kTopkWarps], s_lo[kTopkWarps];
+  __shared__ unsigned s_dmax;
+  extern __shared__ __align__(16) uint8_t dsm[];
+  uint32_t* r_key = reinterpret_cast<uint32_t*>(dsm);              // [kResidCap]
+  int32_t* cand = reinterpret_cast<int32_t*>(r_key + kResidCap);   // [kCandCap]
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(cand + kCandCap);   // [kCandCap]
+  float* qf = reinterpret_cast<float*>(ckey + kCandCap);           // [128][kScoreMaxHeads]
+  float* wf = qf + kScoreMaxHeads * 128;                           // [Hh]
   int32_t* col_i = reinterpret_cast<int32_t*>(wf + kScoreMaxHeads);
   uint32_t* col_lo = reinterpret_cast<uint32_t*>(col_i + kCollectCap);
   uint32_t* col_hi = col_lo + kCollectCap;
+  uint32_t* const wbuf = r_key;                                    // [warp][3][kWarpBuf]
+  uint32_t* const samp = reinterpret_cast<uint32_t*>(col_i);       // [2048]
 
-  pdl_wait();   // the collection (or, in canonical mode, the scores) is complete
+  pdl_wait();   // the scores and the compaction are complete
   pdl_trigger();
   const int lr = blockIdx.x;
   const int l = lr / a.R;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int count = a.ccount[lr];
   const int K = a.K;
   int32_t* out = a.sel + (size_t)lr * K;
 
-  if (a.tc_mode && tid == 0) a.rcount[2 * lr] = -1;   // complete here unless deferred below
   if (count <= K) {
     const int32_t* ci = a.cidx + (size_t)lr * a.N;
     for (int i = tid; i < K; i += blockDim.x) out[i] = i < count ? ci[i] : -1;
@@ -1369,47 +1236,155 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   uint32_t* s0 = a.sc0 + (size_t)lr * a.NS;
   const uint16_t* kbase = a.keys + (size_t)l * a.key_stride;
   bool canonical = !a.tc_mode;
+  // the row's queries as fp32 in the [i][head] layout (heads at qslot(h), heads past Hh
+  // zero) and its head weights
+  auto stage_queries = [&]() {
+    for (int i = tid; i < a.Hh; i += blockDim.x) wf[i] = a.hw[(size_t)lr * a.Hh + i];
+    for (int i = a.Hh * 128 + tid; i < kScoreMaxHeads * 128; i += blockDim.x)
+      qf[(i & 127) * kScoreMaxHeads + qslot(i >> 7)] = 0.0f;
+    const uint16_t* qrow = a.q + (size_t)lr * a.Hh * 128;
+    for (int i = tid; i < a.Hh * 128; i += blockDim.x)
+      qf[(i & 127) * kScoreMaxHeads + qslot(i >> 7)] = bf16_bits_to_f32(qrow[i]);
+  };
 
   if (a.tc_mode) {
     const float* kn = a.knorm + (size_t)l * a.NS;
     const float G = a.qnorm[lr];   // eps per unit key norm
-    // Fast path: the entries collected by K7b (every entry whose upper bound reaches tau,
-    // in index order). If at least K of the row's entries have a lower bound >= tau, the
-    // K-th largest lower bound T over the row is among them and every candidate (upper
-    // bound >= T) was collected, so the rest works on the collection alone; otherwise (or
-    // on overflow) the exact two-pass path below runs instead.
-    int m = -1;
-    {
-      __shared__ int s_off[kTopkChunks + 1], s_bad, s_lo_total;
-      if (tid == 0) {
-        int total = 0, lo = 0, bad = 0;
-        for (int c = 0; c < kTopkChunks; ++c) {
-          const int cc = a.ccnt[(size_t)lr * kTopkChunks + c];
-          s_off[c] = total;
-          bad |= cc > kTopkChunkCap;
-          total += cc;
-          lo += a.clo[(size_t)lr * kTopkChunks + c];
-        }
-        s_off[kTopkChunks] = total;
-        s_bad = bad || total > kCollectCap;
-        s_lo_total = lo;
+    // ---- 1. tau
+    uint32_t tau = 0u;
+    if (n > kCollectCap) {
+      constexpr int kChunks = 64, kS = kChunks * 32;
+      const int spacing = n / kChunks;
+      for (int j = tid; j < kS; j += blockDim.x) {
+        const int i = (j >> 5) * spacing + (j & 31);
+        samp[j] = tc_lo(s0[i], kn[i], G);
       }
       __syncthreads();
-      if (!s_bad && s_lo_total >= K) {
-        const int total = s_off[kTopkChunks];
-        const size_t plane = (size_t)gridDim.x * kTopkChunks * kTopkChunkCap;
-        // one pass over the concatenation (each entry finds its chunk), loads all independent
-        for (int q = tid; q < total; q += blockDim.x) {
-          int c = 0;
+      const int rank = min(kS, (int)(((long long)K * kS + n - 1) / n) + 16);
+      int need;
+      tau = radix_threshold(kS, rank, [&](int j) { return samp[j]; }, hist, scratch, nullptr,
+                            s_misc, a.status, &need, 2);
+    }
+    // ---- 2. collection. Each lane takes 4 consecutive entries of a group of 128 (16-byte
+    // loads; warp segments start at multiples of 128 entries, and entries past `end` in the
+    // last group lie inside the row's padded stride and are masked). U groups per batch;
+    // the next batch's loads are in flight while this one is classified. The taken entries
+    // keep index order: a lane's place is the prefix over the lanes of their counts
+    // (bit-sliced ballots).
+    //   First test, in round-to-nearest arithmetic: x = fmaf(kn, G, s) must reach t*, the
+    // smallest score whose key reaches tau, less a margin. If the exact test passes (the
+    // upper bound RU(s + RU(kn G)) >= t*), then s + kn G >= t* - 2^-23 (|s + RU(kn G)| +
+    // kn G) less a subnormal quantum, and x lies within 2^-24 |x| of s + kn G, so
+    // t* - x <= 2^-22 (|x| + kn G) + 2^-126: the margin 2^-21 (|x| + kn G) + 2^-126 keeps
+    // every entry the exact test takes (and an entry the row does not admit, s = -inf,
+    // never passes). tau at or below the key of -inf takes every entry: no first test.
+    int m = -1;
+    {
+      const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 127) & ~127;
+      const int beg = min(n, warp * seg), end = min(n, beg + seg);
+      uint32_t* const b_i = wbuf + (size_t)warp * 3 * kWarpBuf;
+      uint32_t* const b_lo = b_i + kWarpBuf;
+      uint32_t* const b_hi = b_lo + kWarpBuf;
+      constexpr int U = 2;
+      const bool take_all = tau <= 0x007FFFFFu;
+      const float tstar = key_score(tau);
+      const float crow = __fmaf_rn(0.000000476837158203125f, fabsf(tstar), 1.17549435e-38f);
+      int cnt = 0, nlo = 0;
+      uint4 sv[U];
+      float4 kv[U];
+      const uint4 kNone = make_uint4(kMinusInfBits, kMinusInfBits, kMinusInfBits, kMinusInfBits);
+      const float4 kZero = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int cc = 1; cc < kTopkChunks; ++cc) c += q >= s_off[cc] ? 1 : 0;
-          const int32_t* reg = a.creg + ((size_t)lr * kTopkChunks + c) * kTopkChunkCap;
-          const int p = q - s_off[c];
-          col_i[q] = reg[p];
-          col_lo[q] = (uint32_t)reg[plane + p];
-          col_hi[q] = (uint32_t)reg[2 * plane + p];
+      for (int u = 0; u < U; ++u) {
+        const int i = beg + u * 128 + 4 * lane;
+        sv[u] = i < end ? *reinterpret_cast<const uint4*>(s0 + i) : kNone;
+        kv[u] = i < end ? *reinterpret_cast<const float4*>(kn + i) : kZero;
+      }
+      const unsigned lt = (1u << lane) - 1u;
+      for (int g0 = beg; g0 < end; g0 += 128 * U) {
+        uint4 sn[U];
+        float4 kx[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = g0 + 128 * U + u * 128 + 4 * lane;
+          sn[u] = i < end ? *reinterpret_cast<const uint4*>(s0 + i) : kNone;
+          kx[u] = i < end ? *reinterpret_cast<const float4*>(kn + i) : kZero;
         }
-        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = g0 + u * 128 + 4 * lane;
+          const uint32_t sb[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+          const float k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+          unsigned pm = 0u;   // entries that pass the first test
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float sf = __uint_as_float(sb[e]);
+            const float ke = __fmul_rn(k4[e], G);
+            const float x = __fmaf_rn(k4[e], G, sf);
+            const bool pass =
+                take_all || __fsub_rn(tstar, x) <= __fmaf_rn(0.000000476837158203125f,
+                                                           __fadd_rn(fabsf(x), ke), crow);
+            pm |= (i + e < end && pass) ? 1u << e : 0u;
+          }
+          if (!__ballot_sync(0xffffffffu, pm != 0u)) continue;
+          uint32_t hk[4] = {0u, 0u, 0u, 0u};
+          unsigned tm = 0u;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (pm & (1u << e)) {
+              hk[e] = tc_hi(sb[e], k4[e], G);
+              tm |= hk[e] >= tau ? 1u << e : 0u;
+            }
+          }
+          if (__ballot_sync(0xffffffffu, tm != 0u)) {   // lo <= hi: only taken entries count
+            const int c = __popc(tm);
+            const unsigned c0 = __ballot_sync(0xffffffffu, c & 1);
+            const unsigned c1 = __ballot_sync(0xffffffffu, c & 2);
+            const unsigned c2 = __ballot_sync(0xffffffffu, c & 4);
+            int p = cnt + __popc(c0 & lt) + 2 * __popc(c1 & lt) + 4 * __popc(c2 & lt);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (tm & (1u << e)) {
+                const uint32_t lk = tc_lo(sb[e], k4[e], G);
+                nlo += lk >= tau ? 1 : 0;
+                if (p < kWarpBuf) {
+                  b_i[p] = (uint32_t)(i + e);
+                  b_lo[p] = lk;
+                  b_hi[p] = hk[e];
+                }
+                ++p;
+              }
+            }
+            cnt += __popc(c0) + 2 * __popc(c1) + 4 * __popc(c2);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          sv[u] = sn[u];
+          kv[u] = kx[u];
+        }
+      }
+      nlo = __reduce_add_sync(0xffffffffu, nlo);
+      if (lane == 0) { s_cnt[warp] = cnt; s_lo[warp] = nlo; }
+      __syncthreads();
+      int off = 0, total = 0, lo_total = 0;
+      bool over = false;
+      for (int w = 0; w < kTopkWarps; ++w) {
+        if (w == warp) off = total;
+        total += s_cnt[w];
+        lo_total += s_lo[w];
+        over |= s_cnt[w] > kWarpBuf;
+      }
+      const bool fast = !over && total <= kCollectCap && lo_total >= K;
+      if (fast)
+        for (int p = lane; p < cnt; p += 32) {
+          col_i[off + p] = ui[b_i[p]];   // the entry's block id
+          col_lo[off + p] = b_lo[p];
+          col_hi[off + p] = b_hi[p];
+        }
+      __syncthreads();
+      // ---- 3./4. over the collection: T, the candidates and the certain ones
+      if (fast) {
         int need;
         const uint32_t T = radix_threshold(total, K, [&](int j) { return col_lo[j]; }, hist,
                                            scratch, r_key, s_misc, a.status, &need);
@@ -1419,7 +1394,6 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
         // past T). A candidate whose lower bound exceeds H is beaten by fewer than K others
         // whatever the exact scores: it is selected without being re-scored, and takes the
         // key kCertainKey so that the exact select below keeps it.
-        __shared__ unsigned s_dmax;
         if (tid == 0) s_dmax = 0u;
         __syncthreads();
         {
@@ -1428,7 +1402,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
             if (col_hi[j] >= T)
               dm = fmaxf(dm, __fsub_ru(key_score(col_hi[j]), key_score(col_lo[j])));
           dm = warp_max(dm);
-          if ((tid & 31) == 0) atomicMax(&s_dmax, __float_as_uint(dm));   // dm >= 0
+          if (lane == 0) atomicMax(&s_dmax, __float_as_uint(dm));   // dm >= 0
         }
         __syncthreads();
         const uint32_t Hk = score_key(__fadd_ru(key_score(T), __uint_as_float(s_dmax)));
@@ -1442,16 +1416,16 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
             },
             s_eq, s_gt);
       }
-      __syncthreads();
     }
     bool cand_entries = false;   // cand holds union entries (else block ids)
     if (m < 0) {
+      // exact T over the whole row, then the ordered gather of the candidates (upper bound
+      // reaches T), bounded by kCandCap; none is taken as certain
       cand_entries = true;
       int need;
       const uint32_t T = radix_threshold(
           n, K, [&](int i) { return tc_lo(s0[i], kn[i], G); }, hist, scratch, r_key, s_misc,
           a.status, &need);
-      // Ordered gather of the candidates (upper bound reaches T), bounded by kCandCap.
       m = ordered_take(
           n, 0, [&](int i) { return tc_hi(s0[i], kn[i], G) >= T ? 2 : 0; },
           [&](int p, int i) {
@@ -1463,58 +1437,96 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
           s_eq, s_gt);
     }
     __syncthreads();
+    stage_queries();
     if (m <= kCandCap) {
-      // Deferred to K7r / K7c: the candidates (block ids, in index order) with their keys
-      // (kCertainKey, or 0 until K7r writes the canonical score's key) and the positions of
-      // the uncertain ones, compacted by warp ballot.
       if (cand_entries)
         for (int j = tid; j < m; j += blockDim.x) cand[j] = ui[cand[j]];
-      __shared__ int s_mu;
-      if (tid == 0) s_mu = 0;
       __syncthreads();
-      int32_t* rcand = a.rcand + (size_t)lr * kCandCap;
-      uint32_t* rkey = a.rkey + (size_t)lr * kCandCap;
-      int32_t* rlist = a.rlist + (size_t)lr * kCandCap * 2;
-      for (int j0 = 0; j0 < m; j0 += blockDim.x) {
-        const int j = j0 + tid;
-        const uint32_t k = j < m ? ckey[j] : kCertainKey;
-        if (j < m) {
-          rcand[j] = cand[j];
-          rkey[j] = k;
+      // ---- 4. canonical scores of the uncertain candidates. Their positions are listed
+      // (over the residual keys); rounds of 128 stage their keys in shared memory (rows of
+      // 272 bytes, over the collection), and four threads take a candidate: thread t runs
+      // the chains of heads t, t + 4, t + 8, t + 12 over i ascending (a fused multiply-add
+      // per step), and the first of the four sums the heads' ReLU terms in head order.
+      {
+        int32_t* const ulist = reinterpret_cast<int32_t*>(r_key);
+        if (tid == 0) s_misc[0] = 0;
+        __syncthreads();
+        for (int j0 = 0; j0 < m; j0 += blockDim.x) {
+          const int j = j0 + tid;
+          const bool u = j < m && ckey[j] != kCertainKey;
+          const unsigned bal = __ballot_sync(0xffffffffu, u);
+          int wb = 0;
+          if (lane == 0 && bal) wb = atomicAdd(&s_misc[0], __popc(bal));
+          wb = __shfl_sync(0xffffffffu, wb, 0);
+          if (u) ulist[wb + __popc(bal & ((1u << lane) - 1u))] = j;
         }
-        const bool u = k != kCertainKey;
-        const unsigned bal = __ballot_sync(0xffffffffu, u);
-        int wbase = 0;
-        if ((tid & 31) == 0 && bal) wbase = atomicAdd(&s_mu, __popc(bal));
-        wbase = __shfl_sync(0xffffffffu, wbase, 0);
-        if (u) {
-          const int p = wbase + __popc(bal & ((1u << (tid & 31)) - 1u));
-          reinterpret_cast<int2*>(rlist)[p] = make_int2(j, cand[j]);
+        __syncthreads();
+        const int mu = s_misc[0];
+        uint8_t* const stg = reinterpret_cast<uint8_t*>(col_i);
+        const uint32_t stg_addr = static_cast<uint32_t>(__cvta_generic_to_shared(stg));
+        const uint8_t* kb8 = reinterpret_cast<const uint8_t*>(kbase);
+        const int sub = tid & 3, slot = tid >> 2;
+        for (int u0 = 0; u0 < mu; u0 += kRescoreRound) {
+          const int nr = min(kRescoreRound, mu - u0);
+          for (int t = tid; t < nr * 16; t += blockDim.x) {
+            const int r = t >> 4, c = t & 15;
+            cp_async16(stg_addr + (uint32_t)(r * kRescorePitch + c * 16),
+                       kb8 + (size_t)cand[ulist[u0 + r]] * 256 + c * 16, true);
+          }
+          cp_async_commit();
+          cp_async_wait<0>();
+          __syncthreads();
+          float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          if (slot < nr) {
+            const uint8_t* kr = stg + slot * kRescorePitch;
+#pragma unroll 2
+            for (int c = 0; c < 16; ++c) {
+              const uint4 kv = *reinterpret_cast<const uint4*>(kr + c * 16);
+              const float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
+                                   bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float4 qv =
+                    *reinterpret_cast<const float4*>(qf + (c * 8 + e) * kScoreMaxHeads + sub * 4);
+                d[0] = __fmaf_rn(qv.x, kf[e], d[0]);
+                d[1] = __fmaf_rn(qv.y, kf[e], d[1]);
+                d[2] = __fmaf_rn(qv.z, kf[e], d[2]);
+                d[3] = __fmaf_rn(qv.w, kf[e], d[3]);
+              }
+            }
+          }
+          float dh[kScoreMaxHeads];   // head h = 4j + t: d[j] of thread t
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dh[4 * j + t] = __shfl_sync(0xffffffffu, d[j], (lane & ~3) + t);
+          if (sub == 0 && slot < nr) {
+            float sc = 0.0f;
+#pragma unroll
+            for (int h = 0; h < kScoreMaxHeads; ++h)
+              if (h < a.Hh) sc = __fmaf_rn(wf[h], dh[h] > 0.0f ? dh[h] : 0.0f, sc);
+            ckey[ulist[u0 + slot]] = score_key(sc);
+          }
+          __syncthreads();   // the staging is free for the next round
         }
       }
-      __syncthreads();
-      // this row's re-score tasks (32 uncertain candidates each), appended to the task list
-      const int mu = s_mu, nt = (mu + 31) / 32;
+      // ---- 5. the exact select among the candidates
+      int need;
+      const uint32_t T = radix_threshold(
+          m, K, [&](int j) { return ckey[j]; }, hist, scratch, r_key, s_misc, a.status, &need);
+      const int taken = ordered_take(
+          m, need,
+          [&](int j) { const uint32_t k = ckey[j]; return k > T ? 2 : (k == T ? 1 : 0); },
+          [&](int p, int j) { if (p < K) out[p] = cand[j]; }, s_eq, s_gt);
       if (tid == 0) {
-        a.rcount[2 * lr] = m;
-        a.rcount[2 * lr + 1] = mu;
-        s_misc[0] = nt > 0 ? (int)atomicAdd(&a.status[kRescoreTasks], (uint32_t)nt) : 0;
+        a.nsel[lr] = K;
+        if (taken != K) flag_status(a.status, kStatusCheck);
       }
-      __syncthreads();
-      for (int i = tid; i < nt; i += blockDim.x)
-        reinterpret_cast<int2*>(a.rtask)[s_misc[0] + i] = make_int2(lr * (kCandCap / 32) + i, mu);
       return;
     }
-    // Too many candidates (e.g. heavy ties): canonical scores for the whole row, with the
-    // row's queries as fp32 in the [i][head] layout (the lanes of a block read adjacent words)
-    // and its head weights.
-    {
-      for (int i = tid; i < a.Hh; i += blockDim.x) wf[i] = a.hw[(size_t)lr * a.Hh + i];
-      const uint16_t* qrow = a.q + (size_t)lr * a.Hh * 128;
-      for (int i = tid; i < a.Hh * 128; i += blockDim.x)
-        qf[(i & 127) * kScoreMaxHeads + (i >> 7)] = bf16_bits_to_f32(qrow[i]);
-      __syncthreads();
-    }
+    // Too many candidates (e.g. heavy ties): canonical scores for the whole row.
+    __syncthreads();
     for (int i = tid; i < n; i += blockDim.x) {
       const bool adm = s0[i] != kMinusInfBits;
       s0[i] = adm ? __float_as_uint(canonical_score(qf, kbase + (size_t)ui[i] * 128, wf, a.Hh))
@@ -1538,163 +1550,6 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       a.nsel[lr] = K;
       if (taken != K) flag_status(a.status, kStatusCheck);
     }
-  }
-}
-
-// ---------------------------------------------------------------------------------
-// K7r (tensor-core scoring): canonical scores of the uncertain candidates of every row,
-// spread over the whole GPU. K7 lists the tasks (32 uncertain candidates of one row each);
-// warp w starts with task w and then takes the next task from a counter, one lane per
-// candidate, fetching the task after it before computing this one. The warp copies its 32 keys into shared memory
-// (coalesced 16-byte copies, 272-byte rows so that the lanes' reads of one 16-byte chunk
-// spread over all banks) and the row's queries widened to fp32; each lane then runs the Hh
-// head chains over i ascending (a fused multiply-add of the widened bf16 operands per step)
-// and sums the heads' ReLU terms in head order.
-// ---------------------------------------------------------------------------------
-constexpr int kRescoreThreads = 256;
-constexpr int kRescoreWarps = kRescoreThreads / 32;
-constexpr int kRescorePitch = 272;   // bytes per staged key row
-
-__host__ __device__ constexpr size_t rescore_smem(int hh) {
-  return (size_t)kRescoreWarps * (32 * kRescorePitch + (size_t)hh * 128 * sizeof(float));
-}
-
-template <int HH>   // 0: any head count up to kScoreMaxHeads
-__global__ void __launch_bounds__(kRescoreThreads, 2) k7r_rescore(TopkArgs a) {
-  extern __shared__ __align__(16) uint8_t rsm[];
-  constexpr int kH = HH > 0 ? HH : kScoreMaxHeads;
-  const int Hh = HH > 0 ? HH : a.Hh;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint8_t* sk = rsm + (size_t)warp * (32 * kRescorePitch + (size_t)kH * 128 * sizeof(float));
-  float* sq = reinterpret_cast<float*>(sk + 32 * kRescorePitch);   // [Hh][128]
-  const uint32_t sk_addr = static_cast<uint32_t>(__cvta_generic_to_shared(sk));
-  pdl_wait();   // every row's candidate lists and the task list are complete
-  pdl_trigger();
-  const int total = (int)a.status[kRescoreTasks];
-  const int2* tasks = reinterpret_cast<const int2*>(a.rtask);
-  // the first task of warp w is task w; later ones come from the counter, past the grid
-  const int W = (int)gridDim.x * kRescoreWarps;
-  auto grab = [&]() {
-    int t = 0;
-    if (lane == 0) t = W + (int)atomicAdd(&a.status[kRescoreNext], 1u);
-    return __shfl_sync(0xffffffffu, t, 0);
-  };
-  // a task: its row, part and uncertain count, and this lane's (position, block id)
-  struct Task { int lr, part, mu; int2 pb; };
-  auto fetch = [&](int t) {
-    Task k{-1, 0, 0, make_int2(-1, 0)};
-    if (t < total) {
-      const int2 tk = tasks[t];
-      k.lr = tk.x / (kCandCap / 32);
-      k.part = tk.x - k.lr * (kCandCap / 32);
-      k.mu = tk.y;
-      const int jl = k.part * 32 + lane;
-      if (jl < k.mu)
-        k.pb = reinterpret_cast<const int2*>(a.rlist + (size_t)k.lr * kCandCap * 2)[jl];
-    }
-    return k;
-  };
-  int cur = -1;   // the row whose queries are staged
-  Task tk = fetch((int)blockIdx.x * kRescoreWarps + warp);
-  while (tk.lr >= 0) {
-    const int lr = tk.lr, l = lr / a.R;
-    const bool valid = tk.pb.x >= 0;
-    const uint8_t* kb = reinterpret_cast<const uint8_t*>(a.keys + (size_t)l * a.key_stride);
-    __syncwarp();   // the previous task's reads of the staging are done
-    // keys: half a warp per key row, 2 rows per copy instruction
-#pragma unroll 4
-    for (int r0 = 0; r0 < 32; r0 += 2) {
-      const int r = r0 + (lane >> 4), c = lane & 15;
-      const int rb = __shfl_sync(0xffffffffu, tk.pb.y, r);
-      const bool v = tk.part * 32 + r < tk.mu;
-      cp_async16(sk_addr + (uint32_t)(r * kRescorePitch + c * 16),
-                 v ? kb + (size_t)rb * 256 + c * 16 : kb, v);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    const Task next = fetch(grab());   // its loads overlap this task's
-    if (lr != cur) {
-      const uint16_t* qrow = a.q + (size_t)lr * Hh * 128;
-      for (int i = lane; i < Hh * 64; i += 32) {
-        const uint32_t w2 = __ldg(reinterpret_cast<const uint32_t*>(qrow) + i);
-        sq[2 * i] = bf16_lo(w2);
-        sq[2 * i + 1] = bf16_hi(w2);
-      }
-      cur = lr;
-    }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncwarp();
-    float d[kH];
-#pragma unroll
-    for (int h = 0; h < kH; ++h) d[h] = 0.0f;
-    const uint8_t* kr = sk + lane * kRescorePitch;
-#pragma unroll 2
-    for (int c = 0; c < 16; ++c) {
-      const uint4 kv = *reinterpret_cast<const uint4*>(kr + c * 16);
-      const float k0 = bf16_lo(kv.x), k1 = bf16_hi(kv.x), k2 = bf16_lo(kv.y), k3 = bf16_hi(kv.y);
-      const float k4 = bf16_lo(kv.z), k5 = bf16_hi(kv.z), k6 = bf16_lo(kv.w), k7 = bf16_hi(kv.w);
-#pragma unroll
-      for (int h = 0; h < kH; ++h) {
-        if (HH == 0 && h >= Hh) break;
-        const float4 q0 = *reinterpret_cast<const float4*>(sq + h * 128 + c * 8);
-        const float4 q1 = *reinterpret_cast<const float4*>(sq + h * 128 + c * 8 + 4);
-        float x = d[h];
-        x = __fmaf_rn(q0.x, k0, x);
-        x = __fmaf_rn(q0.y, k1, x);
-        x = __fmaf_rn(q0.z, k2, x);
-        x = __fmaf_rn(q0.w, k3, x);
-        x = __fmaf_rn(q1.x, k4, x);
-        x = __fmaf_rn(q1.y, k5, x);
-        x = __fmaf_rn(q1.z, k6, x);
-        x = __fmaf_rn(q1.w, k7, x);
-        d[h] = x;
-      }
-    }
-    const float* w = a.hw + (size_t)lr * Hh;
-    float sc = 0.0f;
-#pragma unroll
-    for (int h = 0; h < kH; ++h) {
-      if (HH == 0 && h >= Hh) break;
-      sc = __fmaf_rn(__ldg(w + h), d[h] > 0.0f ? d[h] : 0.0f, sc);
-    }
-    if (valid) a.rkey[(size_t)lr * kCandCap + tk.pb.x] = score_key(sc);
-    tk = next;
-  }
-}
-
-// ---------------------------------------------------------------------------------
-// K7c (tensor-core scoring): per (layer, row) deferred by K7, the exact selection among its
-// candidates: threshold over their keys (certain candidates carry the largest key) and the
-// ordered take, ties to the lowest index.
-// ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kTopkThreads) k7c_final(TopkArgs a) {
-  __shared__ int hist[512];   // two radix histogram buffers
-  __shared__ int scratch[33];
-  __shared__ int s_misc[4];
-  __shared__ int s_eq[kTopkWarps], s_gt[kTopkWarps];
-  __shared__ uint32_t r_key[kResidCap];
-  extern __shared__ uint8_t dsm[];
-  int32_t* cand = reinterpret_cast<int32_t*>(dsm);               // [kCandCap] block ids
-  uint32_t* ckey = reinterpret_cast<uint32_t*>(cand + kCandCap);  // [kCandCap] keys
-  pdl_wait();   // the canonical keys of the uncertain candidates are complete
-  const int lr = blockIdx.x, tid = threadIdx.x, K = a.K;
-  const int m = a.rcount[2 * lr];
-  if (m < 0) return;
-  for (int j = tid; j < m; j += blockDim.x) {
-    cand[j] = a.rcand[(size_t)lr * kCandCap + j];
-    ckey[j] = a.rkey[(size_t)lr * kCandCap + j];
-  }
-  __syncthreads();
-  int32_t* out = a.sel + (size_t)lr * K;
-  int need;
-  const uint32_t T = radix_threshold(
-      m, K, [&](int j) { return ckey[j]; }, hist, scratch, r_key, s_misc, a.status, &need);
-  const int taken = ordered_take(
-      m, need,
-      [&](int j) { const uint32_t k = ckey[j]; return k > T ? 2 : (k == T ? 1 : 0); },
-      [&](int p, int j) { if (p < K) out[p] = cand[j]; }, s_eq, s_gt);
-  if (tid == 0) {
-    a.nsel[lr] = K;
-    if (taken != K) flag_status(a.status, kStatusCheck);
   }
 }
 
@@ -1737,15 +1592,6 @@ SelLayout sel_layout(const SelDims& d, bool caller_cidx) {
   L.cscore = off; off += up(sizeof(float) * LR * (size_t)score_stride(d.N));
   L.knorm = off; off += up(sizeof(float) * (size_t)d.L * score_stride(d.N));
   L.qnorm = off; off += up(sizeof(float) * LR);
-  L.tau = off; off += up(sizeof(uint32_t) * LR);
-  L.ccnt = off; off += up(sizeof(int32_t) * LR * kTopkChunks);
-  L.clo = off; off += up(sizeof(int32_t) * LR * kTopkChunks);
-  L.creg = off; off += up(sizeof(int32_t) * 3 * LR * kTopkChunks * kTopkChunkCap);
-  L.rcand = off; off += up(sizeof(int32_t) * LR * kTopkCandCap);
-  L.rkey = off; off += up(sizeof(uint32_t) * LR * kTopkCandCap);
-  L.rlist = off; off += up(sizeof(int32_t) * 2 * LR * kTopkCandCap);
-  L.rcount = off; off += up(sizeof(int32_t) * 2 * LR);
-  L.rtask = off; off += up(sizeof(int32_t) * 2 * LR * (kTopkCandCap / 32));
   L.total = off;
   return L;
 }
@@ -1813,39 +1659,12 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
                         const SelWorkspace& ws, bool tc, cudaStream_t s) {
   TopkArgs a{d.R, d.Hh, d.N, d.topk, d.key_stride, keys, q, head_w, ws.cidx, ws.ccount,
              ws.uidx, ws.ucount, reinterpret_cast<uint32_t*>(ws.cscore), ws.knorm, ws.qnorm, sel,
-             nsel,
-             ws.header, tc ? 1 : 0, ws.tau, ws.ccnt, ws.clo, ws.creg, ws.rcand, ws.rkey,
-             ws.rlist, ws.rcount, ws.rtask};
+             nsel, ws.header, tc ? 1 : 0};
   a.NS = score_stride(d.N);
-  const size_t smem = sizeof(int32_t) * (kCandCap * 2 + kCollectCap * 3) +
-                      sizeof(float) * (kScoreMaxHeads * 128 + kScoreMaxHeads);
   cudaError_t err =
-      cudaFuncSetAttribute(k7_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaFuncSetAttribute(k7_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
   if (err != cudaSuccess) return err;
-  if (tc) {
-    if ((err = launch_pdl(k7a_tau, d.L * d.R, kTopkThreads, 0, s, a)) != cudaSuccess) return err;
-    err = launch_pdl(k7b_collect, d.L * d.R * kTopkChunks, kCollectThreads, 0, s, a);
-    if (err != cudaSuccess) return err;
-  }
-  err = launch_pdl(k7_topk, d.L * d.R, kTopkThreads, smem, s, a);
-  if (err != cudaSuccess || !tc) return err;
-  const int LR = d.L * d.R;
-  const size_t rsmem = rescore_smem(d.Hh == 8 ? 8 : kScoreMaxHeads);
-  const int grid = 2 * device_sm_count();
-  if (d.Hh == 8) {
-    err = cudaFuncSetAttribute(k7r_rescore<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)rsmem);
-    if (err == cudaSuccess) err = launch_pdl(k7r_rescore<8>, grid, kRescoreThreads, rsmem, s, a);
-  } else {
-    err = cudaFuncSetAttribute(k7r_rescore<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)rsmem);
-    if (err == cudaSuccess) err = launch_pdl(k7r_rescore<0>, grid, kRescoreThreads, rsmem, s, a);
-  }
-  if (err != cudaSuccess) return err;
-  const size_t csmem = sizeof(int32_t) * 2 * kCandCap;
-  err = cudaFuncSetAttribute(k7c_final, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
-  if (err != cudaSuccess) return err;
-  return launch_pdl(k7c_final, LR, kTopkThreads, csmem, s, a);
+  return launch_pdl(k7_topk, d.L * d.R, kTopkThreads, kTopkSmem, s, a);
 }
 
 }  // namespace dsmoe

@@ -2,7 +2,7 @@
 
 The selection is exact because every admitted block's canonical score lies within
 kn * G of its tensor-core score s (kn: the key-norm bound, G: the row's bound of
-2^-10 * sum_h |w_h| ||q_h||, both read back from the workspace). These tests check that
+2^-13 * sum_h |w_h| ||q_h||, both read back from the workspace). These tests check that
 bound entry by entry against the oracle's canonical score on inputs built to strain it:
 key and query entries spread over 2^-12 .. 2^12, keys made nearly orthogonal to a head's
 query (heavy cancellation, dot products at the ReLU boundary), head weights of both
