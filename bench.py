@@ -676,6 +676,43 @@ def decode_step_sweep(args, lib, dsm, dev, stream) -> dict:
         if i >= warm:
             ts.append(a.elapsed_time(b))
     out["select"]["8k_one_layer"] = {"blocks": 2048, "layers": 1, "us": round(1e3 * statistics.median(ts), 1)}
+    # the acceptance step after the verify: R = 6 rows over the vocabulary, one step and a
+    # batch of 64 independent steps, greedy and exact speculative sampling at T = 1
+    out["accept"] = {}
+    for B in (1, 64):
+        d = synth.verify_inputs(B, 6, synth.VOCAB, seed=args.seed + 90 + B)
+        t = {k: torch.from_numpy(np.ascontiguousarray(d[k])).to(dev)
+             for k in ("logits", "qd", "draft", "u_acc", "u_res")}
+        ws = torch.empty(lib.ds_verify_workspace_size(B, 6, synth.VOCAB), dtype=torch.uint8,
+                         device=dev)
+        o = torch.empty((B, 6), dtype=torch.int32, device=dev)
+        n = torch.empty((B,), dtype=torch.int32, device=dev)
+        for mode in ("greedy", "sample"):
+            ts = []
+            for i in range(warm + 20):
+                a, b = ev(), ev()
+                a.record(stream)
+                if mode == "greedy":
+                    st = lib.ds_verify_greedy(t["logits"].data_ptr(), B, 6, synth.VOCAB,
+                                              t["draft"].data_ptr(), o.data_ptr(), n.data_ptr(),
+                                              ws.data_ptr(), ws.numel(), sptr)
+                else:
+                    st = lib.ds_verify_sample(t["logits"].data_ptr(), B, 6, synth.VOCAB, 1.0,
+                                              t["qd"].data_ptr(), t["draft"].data_ptr(),
+                                              t["u_acc"].data_ptr(), t["u_res"].data_ptr(),
+                                              o.data_ptr(), n.data_ptr(), ws.data_ptr(),
+                                              ws.numel(), sptr)
+                b.record(stream)
+                torch.cuda.synchronize()
+                if st:
+                    raise RuntimeError(f"ds_verify_{mode}: status {st}")
+                if i >= warm:
+                    ts.append(a.elapsed_time(b))
+            us = 1e3 * statistics.median(ts)
+            read = B * 6 * synth.VOCAB * 4 + (B * 5 * synth.VOCAB * 8 if mode == "sample" else 0)
+            out["accept"][f"{mode}_B{B}"] = {"us": round(us, 1), "vocab": synth.VOCAB, "rows": 6,
+                                             "input_mb": round(read / 1e6, 1)}
+        del t, ws, o, n
     del layers, structs
     torch.cuda.empty_cache()
     return out

@@ -301,6 +301,48 @@ ds_status ds_select_blocks_marked(const ds_select_args* args, int32_t* sel, int3
 size_t ds_select_workspace_offset(const ds_select_args* args, int32_t with_compacted,
                                   int32_t part);
 
+/* ------------------------------------------------------------------------------------
+ * Verify acceptance (page "DeepSeek V4.1F Q4 on M3 Ultra with native DSpark MTP
+ * (40tps / 800tps)", paragraph "DSpark": a decode step verifies the last committed token
+ * and R - 1 drafts in one pass; greedy decode gives the same output as without the
+ * drafter, and at temperature > 0 the step does exact speculative sampling).
+ *
+ * B independent steps of R rows (1 <= R <= 16) over a vocabulary of V tokens
+ * (1 <= V <= 2^24), 1 <= B <= 4096. Row r's logits predict the token after row r's
+ * input, so draft r (r < R - 1) is checked against row r.
+ *   logits  fp32 [B][R][V], finite.
+ *   draft   int32 [B][R-1], tokens in [0, V) (NULL when R == 1). A draft outside the
+ *           vocabulary is rejected and reported as DS_ERR_DEVICE_CHECK by
+ *           ds_workspace_status.
+ *   out     int32 [B][R]: the emitted tokens of each step (the kept drafts, then the one
+ *           token the target adds), -1 after them.
+ *   n_out   int32 [B]: how many tokens each step emitted (1 .. R).
+ * Greedy: every row's argmax, ties to the lowest token id; drafts are kept while they
+ * equal their row's argmax; the first mismatching row, or the last row, adds its argmax.
+ * Sampling at temperature T (finite, > 0; else DS_ERR_INVALID_ARG), every decision in
+ * fp64: p_r = softmax(logits_r / T); draft d of row r is kept iff u_acc * qd_r[d] < p_r[d];
+ * at the first rejection the added token is drawn from max(p_r - qd_r, 0) (from p_r if
+ * that is zero everywhere), after R - 1 kept drafts from p_{R-1}; a draw with u takes the
+ * smallest token whose cumulative weight (token order) exceeds u times the total weight,
+ * else the last token with a positive weight.
+ *   qd      fp64 [B][R-1][V]: the drafter's proposal distributions (NULL when R == 1).
+ *   u_acc   fp64 [B][R-1] in [0, 1): the acceptance uniforms (NULL when R == 1).
+ *   u_res   fp64 [B][R] in [0, 1): the uniforms of the added token (only the one of the
+ *           row it is drawn from is read).
+ * Sums over the vocabulary are taken in a fixed parallel order, so a draw whose target
+ * lies within rounding (about 1e-15 of the total) of a cumulative boundary may differ
+ * from a sequential fp64 evaluation.
+ * The workspace (ds_verify_workspace_size, 256-byte aligned) holds per-chunk partials
+ * and the status word. */
+size_t ds_verify_workspace_size(int32_t B, int32_t R, int32_t V);
+ds_status ds_verify_greedy(const float* logits, int32_t B, int32_t R, int32_t V,
+                           const int32_t* draft, int32_t* out, int32_t* n_out, void* workspace,
+                           size_t ws_bytes, ds_stream_t stream);
+ds_status ds_verify_sample(const float* logits, int32_t B, int32_t R, int32_t V, double T,
+                           const double* qd, const int32_t* draft, const double* u_acc,
+                           const double* u_res, int32_t* out, int32_t* n_out, void* workspace,
+                           size_t ws_bytes, ds_stream_t stream);
+
 /* Synchronises `stream`, then reads the status word that the kernels of the last call on
  * this workspace left in its header: DS_OK, DS_ERR_TIMEOUT (a bounded device wait gave
  * up) or DS_ERR_DEVICE_CHECK (a device consistency check failed, e.g. an index out of

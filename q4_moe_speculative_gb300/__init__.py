@@ -14,7 +14,8 @@ from . import _native as N
 
 __all__ = [
     "MoeLayer", "q4_tile", "moe_workspace_size", "moe_verify_forward", "select_workspace_size",
-    "select_blocks", "workspace_status", "version", "DsmoeError",
+    "select_blocks", "workspace_status", "version", "DsmoeError", "verify_greedy",
+    "verify_sample",
 ]
 
 DsmoeError = N.DsmoeError
@@ -264,6 +265,58 @@ def moe_workspace_h(layer: MoeLayer, R: int, workspace: torch.Tensor) -> torch.T
     off = int(N.load().ds_moe_workspace_h_offset(layer.struct(), R))
     n = R * (1 + layer.top_k) * layer.inter
     return workspace[off: off + 2 * n].view(torch.bfloat16).view(R, 1 + layer.top_k, layer.inter)
+
+
+def _verify_common(logits, draft, out, n_out, workspace):
+    if logits.dim() != 3:
+        raise ValueError("logits must be [B][R][V]")
+    _need(logits, "logits", torch.float32)
+    B, R, V = logits.shape
+    if R > 1:
+        _need(draft, "draft", torch.int32, (B, R - 1))
+    dev = logits.device
+    out = torch.empty((B, R), dtype=torch.int32, device=dev) if out is None else out
+    n_out = torch.empty((B,), dtype=torch.int32, device=dev) if n_out is None else n_out
+    _need(out, "out", torch.int32, (B, R))
+    _need(n_out, "n_out", torch.int32, (B,))
+    need = N.load().ds_verify_workspace_size(B, R, V)
+    if need == 0:
+        raise ValueError(f"unsupported verify sizes B={B} R={R} V={V}")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    return B, R, V, out, n_out, workspace
+
+
+def verify_greedy(logits: torch.Tensor, draft: torch.Tensor | None, *, out=None, n_out=None,
+                  workspace=None, stream=None):
+    """Greedy acceptance of B verify steps: logits fp32 [B][R][V], draft int32 [B][R-1].
+    Returns (out int32 [B][R], -1 padded; n_out int32 [B])."""
+    B, R, V, out, n_out, workspace = _verify_common(logits, draft, out, n_out, workspace)
+    st = N.load().ds_verify_greedy(logits.data_ptr(), B, R, V, _ptr(draft) if R > 1 else None,
+                                   out.data_ptr(), n_out.data_ptr(), workspace.data_ptr(),
+                                   workspace.numel(), _stream(stream))
+    _check(st, "ds_verify_greedy")
+    return out, n_out
+
+
+def verify_sample(logits: torch.Tensor, T: float, qd: torch.Tensor | None,
+                  draft: torch.Tensor | None, u_acc: torch.Tensor | None, u_res: torch.Tensor,
+                  *, out=None, n_out=None, workspace=None, stream=None):
+    """Exact speculative sampling for B verify steps at temperature T: logits fp32 [B][R][V],
+    qd fp64 [B][R-1][V], draft int32 [B][R-1], u_acc fp64 [B][R-1], u_res fp64 [B][R].
+    Returns (out int32 [B][R], -1 padded; n_out int32 [B])."""
+    B, R, V, out, n_out, workspace = _verify_common(logits, draft, out, n_out, workspace)
+    if R > 1:
+        _need(qd, "qd", torch.float64, (B, R - 1, V))
+        _need(u_acc, "u_acc", torch.float64, (B, R - 1))
+    _need(u_res, "u_res", torch.float64, (B, R))
+    st = N.load().ds_verify_sample(
+        logits.data_ptr(), B, R, V, float(T), _ptr(qd) if R > 1 else None,
+        _ptr(draft) if R > 1 else None, _ptr(u_acc) if R > 1 else None, u_res.data_ptr(),
+        out.data_ptr(), n_out.data_ptr(), workspace.data_ptr(), workspace.numel(),
+        _stream(stream))
+    _check(st, "ds_verify_sample")
+    return out, n_out
 
 
 def noalloc_status(stream=None) -> int:

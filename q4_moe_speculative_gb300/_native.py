@@ -22,7 +22,8 @@ EXPORTS = (
     "ds_select_blocks", "ds_workspace_status", "ds_status_string", "ds_version",
     "ds_moe_verify_forward_marked", "ds_select_blocks_marked", "ds_moe_workspace_h_offset",
     "ds_moe_verify_forward_noalloc", "ds_noalloc_status", "ds_q4_tiled_bytes", "ds_q4_tile",
-    "ds_select_workspace_offset",
+    "ds_select_workspace_offset", "ds_verify_workspace_size", "ds_verify_greedy",
+    "ds_verify_sample",
 )
 SELECT_WS_PARTS = {"union": 0, "union_count": 1, "scores": 2, "key_norms": 3, "row_scales": 4}
 
@@ -111,6 +112,15 @@ def load() -> C.CDLL:
     lib.ds_select_blocks.restype = C.c_int
     lib.ds_select_blocks_marked.argtypes = lib.ds_select_blocks.argtypes + [C.c_void_p]
     lib.ds_select_blocks_marked.restype = C.c_int
+    lib.ds_verify_workspace_size.argtypes = [C.c_int32, C.c_int32, C.c_int32]
+    lib.ds_verify_workspace_size.restype = C.c_size_t
+    lib.ds_verify_greedy.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
+                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]
+    lib.ds_verify_greedy.restype = C.c_int
+    lib.ds_verify_sample.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_double,
+                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                     C.c_void_p, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]
+    lib.ds_verify_sample.restype = C.c_int
     lib.ds_workspace_status.argtypes = [C.c_void_p, C.c_void_p]
     lib.ds_workspace_status.restype = C.c_int
     lib.ds_status_string.argtypes = [C.c_int]

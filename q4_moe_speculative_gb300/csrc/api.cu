@@ -1,6 +1,7 @@
 // api.cu — the C ABI of libdsmoe.so: host-side validation, workspace carving and the
 // launch sequence of each call. Nothing here allocates memory or synchronises, except
 // ds_workspace_status(), which synchronises the stream to read the device status word.
+#include <cmath>
 #include <cstring>
 
 #include "common.cuh"
@@ -241,6 +242,50 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
     return DS_ERR_CUDA;
   if (!mark(marks, 2, s)) return DS_ERR_CUDA;
   return DS_OK;
+}
+
+namespace {
+
+bool verify_sizes_ok(int32_t B, int32_t R, int32_t V) {
+  return B >= 1 && B <= 4096 && R >= 1 && R <= kAcceptMaxRows && V >= 1 && V <= (1 << 24);
+}
+
+ds_status verify_call(AcceptProblem& pr, void* workspace, size_t ws_bytes, ds_stream_t stream) {
+  if (!pr.logits || !pr.out || !pr.n_out) return DS_ERR_INVALID_ARG;
+  if (pr.R > 1 && !pr.draft) return DS_ERR_INVALID_ARG;
+  const AcceptLayout L = accept_layout(pr.B, pr.R, pr.V);
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return DS_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(base, 0, 256, s) != cudaSuccess) return DS_ERR_CUDA;
+  return launch_accept(pr, base, s) == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t ds_verify_workspace_size(int32_t B, int32_t R, int32_t V) {
+  if (!verify_sizes_ok(B, R, V)) return 0;
+  return accept_layout(B, R, V).total;
+}
+
+ds_status ds_verify_greedy(const float* logits, int32_t B, int32_t R, int32_t V,
+                           const int32_t* draft, int32_t* out, int32_t* n_out,
+                           void* workspace, size_t ws_bytes, ds_stream_t stream) {
+  if (!verify_sizes_ok(B, R, V)) return DS_ERR_INVALID_ARG;
+  AcceptProblem pr{logits, B, R, V, true, 1.0, nullptr, draft, nullptr, nullptr, out, n_out};
+  return verify_call(pr, workspace, ws_bytes, stream);
+}
+
+ds_status ds_verify_sample(const float* logits, int32_t B, int32_t R, int32_t V,
+                           double T, const double* qd, const int32_t* draft,
+                           const double* u_acc, const double* u_res, int32_t* out,
+                           int32_t* n_out, void* workspace, size_t ws_bytes,
+                           ds_stream_t stream) {
+  if (!verify_sizes_ok(B, R, V)) return DS_ERR_INVALID_ARG;
+  if (!(T > 0.0) || !(T < HUGE_VAL)) return DS_ERR_INVALID_ARG;   // finite and positive
+  if (!u_res || (R > 1 && (!qd || !u_acc))) return DS_ERR_INVALID_ARG;
+  AcceptProblem pr{logits, B, R, V, false, T, qd, draft, u_acc, u_res, out, n_out};
+  return verify_call(pr, workspace, ws_bytes, stream);
 }
 
 ds_status ds_workspace_status(const void* workspace, ds_stream_t stream) {

@@ -33,10 +33,10 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 
 template <typename... Exp, typename... Act>
-cudaError_t launch_pdl(void (*kernel)(Exp...), int grid, int block, size_t smem, cudaStream_t s,
+cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, int block, size_t smem, cudaStream_t s,
                        Act&&... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;

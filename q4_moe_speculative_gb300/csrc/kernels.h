@@ -107,6 +107,40 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
 cudaError_t key_tile_map(CUtensorMap* out, const uint16_t* keys, int N, int L,
                          int64_t key_stride, int box_rows);
 
+// ---- verify acceptance (accept.cu)
+constexpr int kAcceptChunk = 4096;    // tokens of a row per CTA
+constexpr int kAcceptMaxRows = 16;
+struct AcceptChunk {      // per (step, row, chunk)
+  float m;                // greedy / sampling: the chunk's largest logit
+  int32_t id;             // greedy: its lowest token id
+  double s;               // sampling: sum of exp(z / T - m / T) over the chunk
+};
+struct AcceptDecision {   // per step (sampling)
+  int32_t row, mode;      // the row the added token is drawn from; residual or target
+  double M, s;            // that row's max logit / T and softmax normaliser
+};
+struct AcceptPart {       // per (step, chunk) (sampling)
+  double res, p;          // residual and target weight sums of the chunk
+  int32_t last_res, last_p;   // the chunk's last token with a positive weight (-1: none)
+};
+struct AcceptLayout {
+  size_t header, cstat, dec, spart, total;
+};
+struct AcceptProblem {
+  const float* logits;
+  int B, R, V;
+  bool greedy;
+  double T;
+  const double* qd;
+  const int32_t* draft;
+  const double* u_acc;
+  const double* u_res;
+  int32_t* out;
+  int32_t* n_out;
+};
+AcceptLayout accept_layout(int B, int R, int V);
+cudaError_t launch_accept(const AcceptProblem& p, uint8_t* ws, cudaStream_t s);
+
 // Cached device properties of the current device.
 int device_sm_count();
 int device_max_smem_optin();

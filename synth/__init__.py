@@ -14,7 +14,11 @@ distributions of the workload definitions):
     admitted, the rest Bernoulli(0.7), drawn per (layer, block) and shared by the rows
     (default) or drawn per (layer, row, block). Mask bits at or above the limit are random
     too, so a consumer must honour the limit.
-  - Speculative acceptance: Bernoulli(a) per draft, seeded.
+  - Speculative acceptance: Bernoulli(a) per draft, seeded (the sweep); and, for the
+    acceptance step itself, target logits N(0, 1.5^2) per token with one planted strong
+    token per row (its logit raised by `peak` x U(0.5, 1.5)), a drafter distribution that
+    is the mixture alpha x (one-hot at the planted token) + (1 - alpha) x uniform, drafts
+    drawn from that mixture, and uniforms in [0, 1). Vocabulary 129,280 tokens.
 """
 from __future__ import annotations
 
@@ -165,3 +169,54 @@ def to_numpy_bits(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.int32:
         return t.numpy()
     return t.numpy()
+
+
+VOCAB = 129280   # tokens in the vocabulary of the acceptance workload
+
+
+def verify_inputs(B: int, R: int, V: int, seed: int = 0, peak: float = 6.0,
+                  alpha: float = 0.7) -> dict:
+    """One batch of B verify steps of R rows: logits fp32 [B][R][V], the planted strong
+    token of each row, the drafter's distributions qd fp64 [B][R-1][V] (alpha on the
+    planted token plus (1 - alpha) / V everywhere), drafts int32 [B][R-1] drawn from qd,
+    and the uniforms u_acc fp64 [B][R-1], u_res fp64 [B][R]."""
+    rng = np.random.default_rng(seed)
+    z = (rng.standard_normal((B, R, V)) * 1.5).astype(np.float32)
+    strong = rng.integers(0, V, size=(B, R))
+    lift = (peak * rng.uniform(0.5, 1.5, size=(B, R))).astype(np.float32)
+    bi, ri = np.meshgrid(np.arange(B), np.arange(R), indexing="ij")
+    z[bi, ri, strong] += lift
+    n = max(R - 1, 0)
+    qd = np.full((B, n, V), (1.0 - alpha) / V, dtype=np.float64)
+    if n:
+        qd[bi[:, :n], ri[:, :n], strong[:, :n]] += alpha
+    # a draw from the mixture: the planted token with probability alpha, else uniform
+    pick = rng.random((B, n)) < alpha
+    draft = np.where(pick, strong[:, :n], rng.integers(0, V, size=(B, n))).astype(np.int32)
+    return {"logits": z, "strong": strong.astype(np.int32), "qd": qd, "draft": draft,
+            "u_acc": rng.random((B, n)), "u_res": rng.random((B, R))}
+
+
+def greedy_inputs(B: int, R: int, V: int, seed: int = 0) -> dict:
+    """Greedy verify steps with known row maxima: logits N(0, 1) with the row's top token
+    planted at `top` (value 10); step b plants a tie for odd b (the same value at a second
+    token `twin`, below `top` in id for b % 4 == 1, above it for b % 4 == 3); the drafts
+    repeat `top` for the first b % R rows, then one different token, then random ones."""
+    rng = np.random.default_rng(seed)
+    z = rng.standard_normal((B, R, V)).astype(np.float32)
+    top = rng.integers(1, V - 1, size=(B, R)) if V > 2 else np.zeros((B, R), np.int64)
+    twin = np.where((np.arange(B) % 4 == 1)[:, None], rng.integers(0, np.maximum(top, 1)),
+                    top + 1 + rng.integers(0, np.maximum(V - 1 - top, 1)))
+    twin = np.minimum(twin, V - 1)
+    bi, ri = np.meshgrid(np.arange(B), np.arange(R), indexing="ij")
+    z[bi, ri, top] = 10.0
+    odd = (np.arange(B) % 2 == 1)[:, None] & (twin != top)
+    z[bi[odd], ri[odd], twin[odd]] = 10.0
+    n = max(R - 1, 0)
+    draft = rng.integers(0, V, size=(B, n)).astype(np.int32)
+    for b in range(B):
+        k = b % R
+        draft[b, :min(k, n)] = top[b, :min(k, n)]
+        if k < n:
+            draft[b, k] = (top[b, k] + 1) % V
+    return {"logits": z, "draft": draft}

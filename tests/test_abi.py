@@ -197,3 +197,40 @@ def test_header_group_constant_matches_binding():
     text = (ROOT / "include" / "dsmoe.h").read_text()
     m = re.search(r"#define DS_Q4_DOWN_GROUP (\d+)", text)
     assert m and int(m.group(1)) == N.Q4_DOWN_GROUP
+
+
+def test_verify_workspace_size_host_only(lib):
+    s = lib.ds_verify_workspace_size(8, 6, 129280)
+    assert s > 0 and s % 256 == 0
+    assert lib.ds_verify_workspace_size(16, 6, 129280) > s
+    for B, R, V in ((0, 6, 100), (4097, 6, 100), (1, 0, 100), (1, 17, 100), (1, 6, 0),
+                    (1, 6, (1 << 24) + 1)):
+        assert lib.ds_verify_workspace_size(B, R, V) == 0
+
+
+@pytest.mark.parametrize("T", [0.0, -0.5, float("inf"), float("nan")])
+def test_verify_sample_rejects_temperature(lib, T):
+    ws = lib.ds_verify_workspace_size(1, 2, 100)
+    st = lib.ds_verify_sample(FAKE, 1, 2, 100, T, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws,
+                              None)
+    assert st == 1
+
+
+def test_verify_rejects_bad_arguments_on_the_host(lib):
+    ws = lib.ds_verify_workspace_size(2, 6, 1000)
+    g = lib.ds_verify_greedy
+    assert g(None, 2, 6, 1000, FAKE, FAKE, FAKE, FAKE, ws, None) == 1      # logits
+    assert g(FAKE, 2, 6, 1000, None, FAKE, FAKE, FAKE, ws, None) == 1      # drafts, R > 1
+    assert g(FAKE, 2, 6, 1000, FAKE, None, FAKE, FAKE, ws, None) == 1      # out
+    assert g(FAKE, 2, 6, 1000, FAKE, FAKE, None, FAKE, ws, None) == 1      # n_out
+    assert g(FAKE, 0, 6, 1000, FAKE, FAKE, FAKE, FAKE, ws, None) == 1      # B
+    assert g(FAKE, 2, 17, 1000, FAKE, FAKE, FAKE, FAKE, ws, None) == 1     # R
+    assert g(FAKE, 2, 6, 1000, FAKE, FAKE, FAKE, FAKE, ws - 1, None) == 3  # workspace size
+    assert g(FAKE, 2, 6, 1000, FAKE, FAKE, FAKE, FAKE + 8, ws, None) == 3  # alignment
+    assert g(FAKE, 2, 6, 1000, FAKE, FAKE, FAKE, None, ws, None) == 3
+    s = lib.ds_verify_sample
+    assert s(FAKE, 2, 6, 1000, 1.0, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, None) == 1
+    assert s(FAKE, 2, 6, 1000, 1.0, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, ws, None) == 1
+    assert s(FAKE, 2, 6, 1000, 1.0, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, ws, None) == 1
+    assert s(FAKE, 2, 6, 1000, 1.0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws - 1,
+             None) == 3
