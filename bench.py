@@ -548,6 +548,7 @@ def decode_step_sweep(args, lib, dsm, dev, stream) -> dict:
     layers at 8k / 64k / 300k context, and weight bytes per committed token at draft
     acceptance rates 0.5 / 0.7 / 0.9 (seeded Bernoulli draws). The 43-layer step is timed
     both as stream launches and as one captured CUDA graph."""
+    from q4_moe_speculative_gb300 import _native as NB
     shape = synth.VERIFY_MOE
     per_layer = 2.0 * shape.E * shape.H + (shape.E + 1) * expert_bytes(shape)
     free = torch.cuda.mem_get_info()[0]
@@ -676,6 +677,72 @@ def decode_step_sweep(args, lib, dsm, dev, stream) -> dict:
         if i >= warm:
             ts.append(a.elapsed_time(b))
     out["select"]["8k_one_layer"] = {"blocks": 2048, "layers": 1, "us": round(1e3 * statistics.median(ts), 1)}
+    # paired Q8 projections: 43 distinct 4096 x 4096 matrices (one per layer, 17.8 MB each,
+    # 765 MB in all: past L2) for R = 1 and 6, back to back as one captured CUDA graph (the
+    # per-call host cost of a small projection exceeds its GPU time, so single calls would
+    # time the host), and one 65536 x 4096 matrix (285 MB) by itself
+    out["q8"] = {}
+    q8_list = []
+    for l in range(43):
+        qs, sc = synth.q8_matrix(4096, 4096, seed=args.seed + 500 + l, device=dev)
+        q8_list.append(dsm.q8_tile(qs, sc))
+        del qs, sc
+    q8_ws = torch.empty(lib.ds_q8_workspace_size(), dtype=torch.uint8, device=dev)
+    q8_structs = [NB.DsQ8Tiled(t.data_ptr()) for t in q8_list]
+    for R in (1, 6):
+        xq = synth.activations(R, 4096, seed=args.seed + 600 + R, device=dev)
+        yq = [torch.empty((R, 4096), dtype=torch.bfloat16, device=dev) for _ in range(43)]
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for l in range(43):
+                    lib.ds_q8_project(q8_structs[l], 4096, 4096, xq.data_ptr(), R,
+                                      yq[l].data_ptr(), q8_ws.data_ptr(), q8_ws.numel(),
+                                      cap.cuda_stream)
+        stream.wait_stream(cap)
+        tg = []
+        for i in range(warm + reps):
+            a, b = ev(), ev()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= warm:
+                tg.append(a.elapsed_time(b))
+        us = 1e3 * statistics.median(tg)
+        by = 43 * 4096 * 4096 * 1.0625
+        out["q8"][f"43x4096x4096_R{R}_graph"] = {
+            "us": round(us, 1), "us_per_matrix": round(us / 43, 2),
+            "gbs": round(by / (us * 1e-6) / 1e9, 1)}
+        del g, yq
+    st_ = lib.ds_q8_workspace_size()
+    del q8_list, q8_structs
+    qs, sc = synth.q8_matrix(65536, 4096, seed=args.seed + 700, device=dev)
+    big = [dsm.q8_tile(qs, sc) for _ in range(2)]
+    del qs, sc
+    for R in (1, 6):
+        xq = synth.activations(R, 4096, seed=args.seed + 800 + R, device=dev)
+        yq = torch.empty((R, 65536), dtype=torch.bfloat16, device=dev)
+        ts = []
+        for i in range(warm + 20):
+            a, b = ev(), ev()
+            a.record(stream)
+            st = lib.ds_q8_project(NB.DsQ8Tiled(big[i % 2].data_ptr()), 65536, 4096,
+                                   xq.data_ptr(), R, yq.data_ptr(), q8_ws.data_ptr(),
+                                   q8_ws.numel(), sptr)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if st:
+                raise RuntimeError(f"ds_q8_project: status {st}")
+            if i >= warm:
+                ts.append(a.elapsed_time(b))
+        us = 1e3 * statistics.median(ts)
+        out["q8"][f"65536x4096_R{R}"] = {"us": round(us, 1),
+                                         "gbs": round(65536 * 4096 * 1.0625 / (us * 1e-6) / 1e9, 1)}
+    del big
+    assert dsm.workspace_status(q8_ws) == 0 and st_ == 256
     # the acceptance step after the verify: R = 6 rows over the vocabulary, one step and a
     # batch of 64 independent steps, greedy and exact speculative sampling at T = 1
     out["accept"] = {}

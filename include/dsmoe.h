@@ -302,6 +302,50 @@ size_t ds_select_workspace_offset(const ds_select_args* args, int32_t with_compa
                                   int32_t part);
 
 /* ------------------------------------------------------------------------------------
+ * Paired Q8 projections (page "DeepSeek V4.1F Q4 on M3 Ultra with native DSpark MTP
+ * (40tps / 800tps)", paragraph "DSpark": the 6 verify rows share one weight stream
+ * through paired Q8 projections). Format as defined for this workload: a logical
+ * [rows][K] matrix in blocks of 32 consecutive int8 values (two's complement) along K,
+ * one fp16 scale per block, value = scale * q.
+ *   Planar interchange form: qs int8 [rows][K], sc fp16 bits [rows][K/32].
+ *   Tile-major form (what ds_q8_project streams; written by ds_q8_tile): tiles of 16 rows
+ *   x 64 values, 1088 bytes each, ordered by 16-row unit, then K tile. Within a tile,
+ *   block j (0, 1) occupies bytes 512 j .. 512 j + 511: lane L = 4g + q (g, q < 8, 4) holds
+ *   at 512 j + 16 L the int8 values k = 4q .. 4q+3 of rows g and g + 8 of the block's first
+ *   16 values, then the same of its last 16 values (4 bytes each, k ascending). Bytes
+ *   1024 + 8 g hold the fp16 scales (row g block 0, row g+8 block 0, row g block 1,
+ *   row g+8 block 1). A pure rearrangement (1.0625 bytes per weight in both forms). */
+typedef struct {
+  const int8_t* qs;
+  const uint16_t* sc;
+} ds_q8;
+typedef struct {
+  const void* tiles;   /* 16-byte aligned */
+} ds_q8_tiled;
+
+/* Bytes of the tile-major form of a [rows][K] Q8 matrix (0 when rows is not a positive
+ * multiple of 16 or K not a positive multiple of 64). */
+size_t ds_q8_tiled_bytes(int64_t rows, int32_t K);
+/* Planar -> tile-major on the device (qs, sc and dst 16-byte aligned device memory,
+ * dst_bytes >= ds_q8_tiled_bytes). DS_ERR_INVALID_ARG for nulls, misalignment, or sizes
+ * outside rows % 16 == 0, K % 64 == 0, rows <= 2^24, K <= 65536; DS_ERR_WORKSPACE when dst is
+ * too small. */
+ds_status ds_q8_tile(const ds_q8* src, int64_t rows, int32_t K, void* dst, size_t dst_bytes,
+                     ds_stream_t stream);
+/* Workspace of ds_q8_project: the 256-byte status header. */
+size_t ds_q8_workspace_size(void);
+/* y[r][i] = bf16_RNE(sum_k W[i][k] * x[r][k]) for r < R: x bf16 [R][K], y bf16 [R][rows]
+ * (device, 16-byte aligned), 1 <= R <= 8. Every weight byte is read from HBM once for all
+ * R rows; products are exact and summed in fp32 in an order that does not depend on R,
+ * so an R-row call writes the same bytes as R one-row calls. DS_ERR_INVALID_ARG outside
+ * the format (rows % 16, K % 32, ranges as for ds_q8_tile, R); DS_ERR_UNSUPPORTED for a
+ * valid K this kernel does not run (K not a multiple of 1024, or R x K activations beyond
+ * its shared memory: R x K x 2 bytes must leave room for its ring). */
+ds_status ds_q8_project(const ds_q8_tiled* w, int64_t rows, int32_t K, const uint16_t* x,
+                        int32_t R, uint16_t* y, void* workspace, size_t ws_bytes,
+                        ds_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * Verify acceptance (page "DeepSeek V4.1F Q4 on M3 Ultra with native DSpark MTP
  * (40tps / 800tps)", paragraph "DSpark": a decode step verifies the last committed token
  * and R - 1 drafts in one pass; greedy decode gives the same output as without the

@@ -15,7 +15,7 @@ from . import _native as N
 __all__ = [
     "MoeLayer", "q4_tile", "moe_workspace_size", "moe_verify_forward", "select_workspace_size",
     "select_blocks", "workspace_status", "version", "DsmoeError", "verify_greedy",
-    "verify_sample",
+    "verify_sample", "q8_tile", "q8_project",
 ]
 
 DsmoeError = N.DsmoeError
@@ -71,6 +71,40 @@ def q4_tile(qs: torch.Tensor, sc: torch.Tensor, group: int = 1, stream=None) -> 
     _check(lib.ds_q4_tile(src, n_mats, rows, K, group, _ptr(out), out.numel(), _stream(stream)),
            "ds_q4_tile")
     return out
+
+
+def q8_tile(qs: torch.Tensor, sc: torch.Tensor, stream=None) -> torch.Tensor:
+    """Tile-major form (include/dsmoe.h) of a planar Q8 matrix: qs int8 [rows, K], sc fp16
+    [rows, K/32] -> uint8 [rows/16, K/64, 1088], written on the device by ds_q8_tile."""
+    lib = N.load()
+    _need(qs, "qs", torch.int8)
+    rows, K = qs.shape
+    _need(sc, "sc", torch.float16, (rows, K // 32))
+    out = torch.empty((rows // 16, K // 64, N.Q8_TILE_BYTES), dtype=torch.uint8,
+                      device=qs.device)
+    src = N.DsQ8(_ptr(qs), _ptr(sc))
+    _check(lib.ds_q8_tile(src, rows, K, _ptr(out), out.numel(), _stream(stream)), "ds_q8_tile")
+    return out
+
+
+def q8_project(tiles: torch.Tensor, x: torch.Tensor, *, y=None, workspace=None, stream=None):
+    """R verify rows through one tile-major Q8 matrix: tiles uint8 [rows/16, K/64, 1088],
+    x bf16 [R, K] -> y bf16 [R, rows] (ds_q8_project)."""
+    lib = N.load()
+    _need(tiles, "tiles", torch.uint8)
+    _need(x, "x", torch.bfloat16)
+    rows, K = tiles.shape[0] * 16, tiles.shape[1] * 64
+    R = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError(f"x must be [R, {K}] (got {tuple(x.shape)})")
+    y = torch.empty((R, rows), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _need(y, "y", torch.bfloat16, (R, rows))
+    if workspace is None:
+        workspace = torch.empty(lib.ds_q8_workspace_size(), dtype=torch.uint8, device=x.device)
+    w = N.DsQ8Tiled(_ptr(tiles))
+    _check(lib.ds_q8_project(w, rows, K, _ptr(x), R, _ptr(y), _ptr(workspace),
+                             workspace.numel(), _stream(stream)), "ds_q8_project")
+    return y
 
 
 @dataclass

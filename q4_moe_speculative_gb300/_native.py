@@ -23,7 +23,8 @@ EXPORTS = (
     "ds_moe_verify_forward_marked", "ds_select_blocks_marked", "ds_moe_workspace_h_offset",
     "ds_moe_verify_forward_noalloc", "ds_noalloc_status", "ds_q4_tiled_bytes", "ds_q4_tile",
     "ds_select_workspace_offset", "ds_verify_workspace_size", "ds_verify_greedy",
-    "ds_verify_sample",
+    "ds_verify_sample", "ds_q8_tiled_bytes", "ds_q8_tile", "ds_q8_workspace_size",
+    "ds_q8_project",
 )
 SELECT_WS_PARTS = {"union": 0, "union_count": 1, "scores": 2, "key_norms": 3, "row_scales": 4}
 
@@ -41,6 +42,17 @@ class DsQ4Tiled(C.Structure):
 
 Q4_TILE_BYTES = 576   # 16 rows x 64 values: 512 bytes of nibbles + 64 bytes of scales
 Q4_DOWN_GROUP = 16    # tile rows per group of the down matrices (same value as the header)
+
+
+class DsQ8(C.Structure):
+    _fields_ = [("qs", C.c_void_p), ("sc", C.c_void_p)]
+
+
+class DsQ8Tiled(C.Structure):
+    _fields_ = [("tiles", C.c_void_p)]
+
+
+Q8_TILE_BYTES = 1088  # 16 rows x 64 int8 values + 32 fp16 scales
 
 
 class DsMoeLayer(C.Structure):
@@ -112,6 +124,16 @@ def load() -> C.CDLL:
     lib.ds_select_blocks.restype = C.c_int
     lib.ds_select_blocks_marked.argtypes = lib.ds_select_blocks.argtypes + [C.c_void_p]
     lib.ds_select_blocks_marked.restype = C.c_int
+    lib.ds_q8_tiled_bytes.argtypes = [C.c_int64, C.c_int32]
+    lib.ds_q8_tiled_bytes.restype = C.c_size_t
+    lib.ds_q8_tile.argtypes = [C.POINTER(DsQ8), C.c_int64, C.c_int32, C.c_void_p, C.c_size_t,
+                               C.c_void_p]
+    lib.ds_q8_tile.restype = C.c_int
+    lib.ds_q8_workspace_size.argtypes = []
+    lib.ds_q8_workspace_size.restype = C.c_size_t
+    lib.ds_q8_project.argtypes = [C.POINTER(DsQ8Tiled), C.c_int64, C.c_int32, C.c_void_p,
+                                  C.c_int32, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]
+    lib.ds_q8_project.restype = C.c_int
     lib.ds_verify_workspace_size.argtypes = [C.c_int32, C.c_int32, C.c_int32]
     lib.ds_verify_workspace_size.restype = C.c_size_t
     lib.ds_verify_greedy.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,

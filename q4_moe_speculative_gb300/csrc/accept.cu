@@ -19,8 +19,8 @@
 //    u_res[R-1]. Drawing with u from weights w takes the smallest x whose cumulative
 //    weight (token order) exceeds u * sum(w), else the last x with w[x] > 0.
 //
-// Every decision is taken in fp64. The rows are split into chunks of kChunk tokens over
-// the whole GPU:
+// Every decision is taken in fp64 (on GB300 the fp64 exponentials of the softmax are the
+// cost of sampling). The rows are split into chunks of kAcceptChunk tokens over the GPU:
 //   K_stats   per (chunk, row): greedy: the chunk's (max, lowest id); sampling: the
 //             chunk's max m_c and sum_v exp(z_v / T - m_c / T).
 //   K_decide  per step: each row's max M and normaliser s = sum_c s_c exp(m_c/T - M)

@@ -246,6 +246,54 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
 
 namespace {
 
+bool q8_sizes_ok(int64_t rows, int32_t K) {
+  return rows >= 16 && rows <= (1 << 24) && rows % 16 == 0 && K >= 32 && K <= 65536 &&
+         K % 32 == 0;
+}
+
+}  // namespace
+
+size_t ds_q8_tiled_bytes(int64_t rows, int32_t K) {
+  if (!q8_sizes_ok(rows, K) || K % 64) return 0;
+  return q8_tiled_bytes(rows, K);
+}
+
+ds_status ds_q8_tile(const ds_q8* src, int64_t rows, int32_t K, void* dst, size_t dst_bytes,
+                     ds_stream_t stream) {
+  if (!src || !src->qs || !src->sc || !dst) return DS_ERR_INVALID_ARG;
+  if (!q8_sizes_ok(rows, K) || K % 64) return DS_ERR_INVALID_ARG;
+  if (!aligned(src->qs, 16) || !aligned(src->sc, 16) || !aligned(dst, 16))
+    return DS_ERR_INVALID_ARG;
+  if (dst_bytes < q8_tiled_bytes(rows, K)) return DS_ERR_WORKSPACE;
+  return launch_q8_tile(src->qs, src->sc, (int)rows, K, dst,
+                        reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DS_OK
+             : DS_ERR_CUDA;
+}
+
+size_t ds_q8_workspace_size(void) { return 256; }
+
+ds_status ds_q8_project(const ds_q8_tiled* w, int64_t rows, int32_t K, const uint16_t* x,
+                        int32_t R, uint16_t* y, void* workspace, size_t ws_bytes,
+                        ds_stream_t stream) {
+  if (!w || !w->tiles || !x || !y) return DS_ERR_INVALID_ARG;
+  if (!q8_sizes_ok(rows, K) || R < 1 || R > 8) return DS_ERR_INVALID_ARG;
+  if (!aligned(w->tiles, 16) || !aligned(x, 16) || !aligned(y, 16)) return DS_ERR_INVALID_ARG;
+  if (K % 1024) return DS_ERR_UNSUPPORTED;
+  int S = 0, P = 0;
+  size_t smem = 0;
+  if (!q8_plan(R, K, &S, &P, &smem)) return DS_ERR_UNSUPPORTED;
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < 256) return DS_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, 256, s) != cudaSuccess) return DS_ERR_CUDA;
+  return launch_q8_project(w->tiles, (int)rows, K, x, R, y, static_cast<uint32_t*>(workspace), s) ==
+                 cudaSuccess
+             ? DS_OK
+             : DS_ERR_CUDA;
+}
+
+namespace {
+
 bool verify_sizes_ok(int32_t B, int32_t R, int32_t V) {
   return B >= 1 && B <= 4096 && R >= 1 && R <= kAcceptMaxRows && V >= 1 && V <= (1 << 24);
 }

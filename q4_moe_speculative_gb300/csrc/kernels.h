@@ -107,6 +107,17 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
 cudaError_t key_tile_map(CUtensorMap* out, const uint16_t* keys, int N, int L,
                          int64_t key_stride, int box_rows);
 
+// ---- paired Q8 projections (q8.cu)
+constexpr int kQ8TileBytes = 1088;   // 16 rows x 64 int8 values + 32 fp16 scales
+constexpr int kQ8MaxStages = 16;
+constexpr int kQ8MaxSlots = 40;
+size_t q8_tiled_bytes(long long rows, int K);
+cudaError_t launch_q8_tile(const int8_t* qs, const uint16_t* sc, int rows, int K, void* dst,
+                           cudaStream_t s);
+bool q8_plan(int R, int K, int* stages, int* slots, size_t* smem);
+cudaError_t launch_q8_project(const void* tiles, int rows, int K, const uint16_t* x, int R,
+                              uint16_t* y, uint32_t* status, cudaStream_t s);
+
 // ---- verify acceptance (accept.cu)
 constexpr int kAcceptChunk = 4096;    // tokens of a row per CTA
 constexpr int kAcceptMaxRows = 16;

@@ -14,6 +14,9 @@ distributions of the workload definitions):
     admitted, the rest Bernoulli(0.7), drawn per (layer, block) and shared by the rows
     (default) or drawn per (layer, row, block). Mask bits at or above the limit are random
     too, so a consumer must honour the limit.
+  - Paired Q8 projections: int8 values uniform in [-128, 127], fp16 scales
+    uniform(0.5, 2) x 2^-7 (so |W| is about 0.5 at most, comparable to a trained layer's
+    weights), verify rows bf16 N(0, 1).
   - Speculative acceptance: Bernoulli(a) per draft, seeded (the sweep); and, for the
     acceptance step itself, target logits N(0, 1.5^2) per token with one planted strong
     token per row (its logit raised by `peak` x U(0.5, 1.5)), a drafter distribution that
@@ -220,3 +223,12 @@ def greedy_inputs(B: int, R: int, V: int, seed: int = 0) -> dict:
         if k < n:
             draft[b, k] = (top[b, k] + 1) % V
     return {"logits": z, "draft": draft}
+
+
+def q8_matrix(rows: int, K: int, seed: int = 0, device="cpu"):
+    """Random Q8 matrix: qs int8 [rows, K] uniform in [-128, 127], sc fp16 [rows, K/32]
+    uniform(0.5, 2) x 2^-7."""
+    g = _gen(seed, device)
+    qs = torch.randint(-128, 128, (rows, K), dtype=torch.int8, generator=g, device=device)
+    sc = torch.rand((rows, K // 32), generator=g, device=device).mul_(1.5).add_(0.5)
+    return qs, sc.mul_(2.0 ** -7).to(torch.float16)

@@ -234,3 +234,27 @@ def test_verify_rejects_bad_arguments_on_the_host(lib):
     assert s(FAKE, 2, 6, 1000, 1.0, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, ws, None) == 1
     assert s(FAKE, 2, 6, 1000, 1.0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws - 1,
              None) == 3
+
+
+def test_q8_sizes_and_argument_checks(lib):
+    from q4_moe_speculative_gb300 import _native as N
+    assert lib.ds_q8_tiled_bytes(4096, 4096) == 256 * 64 * 1088
+    for rows, K in ((0, 64), (15, 64), (16, 32), (16, 0), (16, 96), ((1 << 24) + 16, 64)):
+        assert lib.ds_q8_tiled_bytes(rows, K) == 0
+    assert lib.ds_q8_workspace_size() == 256
+    src = N.DsQ8(FAKE, FAKE)
+    n = lib.ds_q8_tiled_bytes(64, 512)
+    assert lib.ds_q8_tile(None, 64, 512, FAKE, n, None) == 1
+    assert lib.ds_q8_tile(src, 60, 512, FAKE, n, None) == 1
+    assert lib.ds_q8_tile(src, 64, 480, FAKE, n, None) == 1      # K % 64
+    assert lib.ds_q8_tile(src, 64, 512, FAKE + 4, n, None) == 1  # alignment
+    assert lib.ds_q8_tile(src, 64, 512, FAKE, n - 1, None) == 3
+    w = N.DsQ8Tiled(FAKE)
+    p = lib.ds_q8_project
+    assert p(None, 64, 512, FAKE, 6, FAKE, FAKE, 256, None) == 1
+    assert p(w, 64, 512, None, 6, FAKE, FAKE, 256, None) == 1
+    assert p(w, 64, 512, FAKE, 0, FAKE, FAKE, 256, None) == 1
+    assert p(w, 64, 512, FAKE, 9, FAKE, FAKE, 256, None) == 1
+    assert p(w, 48, 512, FAKE, 6, FAKE + 8, FAKE, 256, None) == 1   # x alignment
+    assert p(w, 64, 544, FAKE, 6, FAKE, FAKE, 256, None) == 2       # K % 512: unsupported
+    assert p(w, 64, 1056, FAKE, 6, FAKE, FAKE, 256, None) == 2
