@@ -68,6 +68,9 @@ def lib() -> C.CDLL:
         L.orc_verify_sample.restype = C.c_int32
         L.orc_committed_tokens.argtypes = [P, C.c_int32]
         L.orc_committed_tokens.restype = C.c_int32
+        L.orc_sparse_attention.argtypes = [P, P, P, C.c_int64, C.c_int32, C.c_int32, C.c_int32,
+                                           P, C.c_int32, C.c_int32, P, P]
+        L.orc_sparse_attention.restype = C.c_int32
         _lib = L
     return _lib
 
@@ -292,3 +295,23 @@ def q8_project(qs: np.ndarray, sc: np.ndarray, x: np.ndarray):
     yb = np.zeros((R, rows), np.uint16)
     lib().orc_q8_project(_p(q), _p(s), rows, K, _p(xb), R, _p(y), _p(yb))
     return y, yb
+
+
+def sparse_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, sel: np.ndarray,
+                     block: int = 4):
+    """One layer: q bf16 bits [R][Hq][D], k and v bf16 bits [T][D], sel int32 [R][K]
+    (selected block ids, -1 padded) -> (o fp64 [R][Hq][D], o bf16 bits [R][Hq][D])."""
+    qb = _u16(q)
+    kb = _u16(k)
+    vb = _u16(v)
+    s = np.ascontiguousarray(sel, dtype=np.int32)
+    R, Hq, D = qb.shape
+    T = kb.shape[0]
+    assert kb.shape == (T, D) and vb.shape == (T, D) and s.shape[0] == R
+    o = np.zeros((R, Hq, D), np.float64)
+    ob = np.zeros((R, Hq, D), np.uint16)
+    st = lib().orc_sparse_attention(_p(qb), _p(kb), _p(vb), T, D, R, Hq, _p(s), s.shape[1],
+                                    block, _p(o), _p(ob))
+    if st < 0:
+        raise ValueError("a selected block lies outside the key range")
+    return o, ob

@@ -24,6 +24,10 @@
  *                     paragraph "DSpark" (a 6-row verify per decode step; identical
  *                     output under greedy decode; exact speculative sampling at
  *                     temperature > 0): accepted drafts, then one target token.
+ *   orc_sparse_attention
+ *                     paragraph "Decode at depth" (attention reads the 512 blocks the
+ *                     selection picks): softmax attention of each query head over the
+ *                     tokens of the row's selected blocks, fp64, one bf16 rounding.
  * Readings where the pages are silent are stated beside the code that takes them.
  */
 #include <math.h>
@@ -516,4 +520,73 @@ int32_t orc_verify_sample(const float* logits, int32_t R, int32_t V, double T, c
   free(p);
   free(res);
   return n;
+}
+
+/* ---------------------------------------------------------- sparse attention ---- */
+
+/* Attention of R query rows over the tokens of their selected blocks (one layer).
+ * Reading (the pages stop at the selection): blocks of `bs` consecutive tokens; row r reads
+ * the tokens bs*b .. bs*b + bs - 1 of every selected block b (sel[r][j] >= 0, j < K); all
+ * Hq query heads of a row share one key and one value per token (D values each). For
+ * row r and head h, with the tokens t in ascending order:
+ *   s_t = (q_{r,h} . k_t) / sqrt(D),  p = softmax(s),  o_{r,h} = sum_t p_t v_t,
+ * in fp64 from the bf16 inputs, then o rounded once to bf16 (round to nearest even). A row
+ * with no selected block gets o = 0. q bf16 [R][Hq][D], k and v bf16 [T][D], sel int32
+ * [R][K] (ascending, -1 padded), o64 fp64 [R][Hq][D] and obf bf16 [R][Hq][D] (either may
+ * be NULL). Returns -1 when a selected block lies outside [0, T / bs), else 0. */
+int32_t orc_sparse_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                             int64_t T, int32_t D, int32_t R, int32_t Hq, const int32_t* sel,
+                             int32_t K, int32_t bs, double* o64, uint16_t* obf) {
+  const int64_t nblk = T / bs;
+  for (int32_t r = 0; r < R; ++r)
+    for (int32_t j = 0; j < K; ++j) {
+      const int32_t b = sel[(int64_t)r * K + j];
+      if (b >= nblk) return -1;
+    }
+  double* s = (double*)malloc(sizeof(double) * (size_t)K * (size_t)bs + 1);
+  double* acc = (double*)malloc(sizeof(double) * (size_t)D);
+  const double scale = 1.0 / sqrt((double)D);
+  for (int32_t r = 0; r < R; ++r) {
+    const int32_t* sr = sel + (int64_t)r * K;
+    for (int32_t h = 0; h < Hq; ++h) {
+      const uint16_t* qh = q + ((int64_t)r * Hq + h) * D;
+      /* scores of the selected tokens in token order, and their maximum */
+      int64_t n = 0;
+      double m = -INFINITY;
+      for (int32_t j = 0; j < K; ++j) {
+        const int32_t b = sr[j];
+        if (b < 0) continue;
+        for (int32_t e = 0; e < bs; ++e) {
+          const uint16_t* kt = k + ((int64_t)b * bs + e) * D;
+          double dot = 0.0;
+          for (int32_t i = 0; i < D; ++i) dot += orc_bf16_to_f64(qh[i]) * orc_bf16_to_f64(kt[i]);
+          s[n] = dot * scale;
+          if (s[n] > m) m = s[n];
+          ++n;
+        }
+      }
+      for (int32_t i = 0; i < D; ++i) acc[i] = 0.0;
+      double den = 0.0;
+      n = 0;
+      for (int32_t j = 0; j < K; ++j) {
+        const int32_t b = sr[j];
+        if (b < 0) continue;
+        for (int32_t e = 0; e < bs; ++e) {
+          const double w = exp(s[n++] - m);
+          const uint16_t* vt = v + ((int64_t)b * bs + e) * D;
+          den += w;
+          for (int32_t i = 0; i < D; ++i) acc[i] += w * orc_bf16_to_f64(vt[i]);
+        }
+      }
+      for (int32_t i = 0; i < D; ++i) {
+        const double o = n > 0 ? acc[i] / den : 0.0;
+        const int64_t at = ((int64_t)r * Hq + h) * D + i;
+        if (o64) o64[at] = o;
+        if (obf) obf[at] = orc_bf16_rne(o);
+      }
+    }
+  }
+  free(s);
+  free(acc);
+  return 0;
 }

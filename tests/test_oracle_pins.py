@@ -640,3 +640,87 @@ def test_verify_sample_rejects_a_temperature_without_a_softmax(T):
     n = oracle.lib().orc_verify_sample(zz.ctypes.data, 1, 4, T, None, None, None,
                                        ur.ctypes.data, out.ctypes.data)
     assert n == -1 and out[0] == -7
+
+
+# ------------------------------------------------------------- sparse attention --
+
+def _bf16_bits(a: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16) \
+        .numpy().view(np.uint16)
+
+
+def _bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+
+
+def _attn_case(R, Hq, D, N, K, seed, bs=4):
+    rng = np.random.default_rng(seed)
+    q = _bf16_bits(rng.standard_normal((R, Hq, D)))
+    k = _bf16_bits(rng.standard_normal((N * bs, D)))
+    v = _bf16_bits(rng.standard_normal((N * bs, D)))
+    sel = np.full((R, K), -1, np.int32)
+    for r in range(R):
+        n = int(rng.integers(1, K + 1))
+        sel[r, :n] = np.sort(rng.choice(N, size=n, replace=False))
+    return q, k, v, sel
+
+
+def test_sparse_attention_matches_a_dense_masked_softmax():
+    # an independent restatement: gather the selected tokens, scipy's softmax over
+    # q.k / sqrt(D), weighted sum of the values
+    from scipy.special import softmax
+    R, Hq, D, N, K = 3, 4, 32, 40, 9
+    q, k, v, sel = _attn_case(R, Hq, D, N, K, seed=1)
+    o, ob = oracle.sparse_attention(q, k, v, sel)
+    qf, kf, vf = _bits_to_f64(q), _bits_to_f64(k), _bits_to_f64(v)
+    for r in range(R):
+        toks = np.concatenate([np.arange(4 * b, 4 * b + 4) for b in sel[r] if b >= 0])
+        s = qf[r] @ kf[toks].T / np.sqrt(D)
+        want = softmax(s, axis=1) @ vf[toks]
+        assert np.allclose(o[r], want, rtol=1e-12, atol=1e-14)
+    # one bf16 rounding of the fp64 result (torch rounds fp64 -> bf16 once)
+    want_b = torch.from_numpy(o).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ob, want_b)
+
+
+def test_sparse_attention_equal_keys_give_the_mean_value():
+    # every selected token has the same key: the weights are uniform and the output is the
+    # plain mean of the selected tokens' values
+    R, Hq, D, N, K = 2, 3, 16, 12, 4
+    q, k, v, sel = _attn_case(R, Hq, D, N, K, seed=2)
+    k[:] = k[0]
+    o, _ = oracle.sparse_attention(q, k, v, sel)
+    vf = _bits_to_f64(v)
+    for r in range(R):
+        toks = np.concatenate([np.arange(4 * b, 4 * b + 4) for b in sel[r] if b >= 0])
+        for h in range(Hq):
+            assert np.allclose(o[r, h], vf[toks].mean(axis=0), rtol=1e-13, atol=1e-15)
+
+
+def test_sparse_attention_one_dominant_token():
+    # a key equal to 16 x the query: its score exceeds every other by far more than 40, so
+    # the output is that token's value to within e^-40
+    R, Hq, D, N, K = 1, 1, 32, 8, 3
+    q, k, v, sel = _attn_case(R, Hq, D, N, K, seed=3)
+    sel[0] = [1, 4, 6]
+    kf = _bits_to_f64(k)
+    k[4 * 4 + 2] = _bf16_bits(16.0 * _bits_to_f64(q[0, 0]))
+    o, _ = oracle.sparse_attention(q, k, v, sel)
+    assert np.allclose(o[0, 0], _bits_to_f64(v)[4 * 4 + 2], rtol=1e-12, atol=1e-12)
+    del kf
+
+
+def test_sparse_attention_padding_empty_rows_and_range():
+    R, Hq, D, N, K = 2, 2, 8, 6, 3
+    q, k, v, sel = _attn_case(R, Hq, D, N, K, seed=4)
+    sel[1] = -1
+    o, ob = oracle.sparse_attention(q, k, v, sel)
+    assert (o[1] == 0).all() and (ob[1] == 0).all()
+    # the same selection with extra -1 entries gives the same output
+    wide = np.concatenate([sel, np.full((R, 5), -1, np.int32)], axis=1)
+    o2, _ = oracle.sparse_attention(q, k, v, wide)
+    assert np.array_equal(o, o2)
+    bad = sel.copy()
+    bad[0, 0] = N
+    with pytest.raises(ValueError):
+        oracle.sparse_attention(q, k, v, bad)
