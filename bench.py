@@ -743,6 +743,35 @@ def decode_step_sweep(args, lib, dsm, dev, stream) -> dict:
                                          "gbs": round(65536 * 4096 * 1.0625 / (us * 1e-6) / 1e9, 1)}
     del big
     assert dsm.workspace_status(q8_ws) == 0 and st_ == 256
+    # sparse attention over the selected blocks: 43 layers x 6 rows x 16 heads, 512 blocks
+    # of 4 tokens per row (keys and values of the selected tokens: 1 MB per row), at 300k
+    # context (75,000 blocks per layer; the selection is random, ascending)
+    T = 75000 * 4
+    ai = synth.attention_inputs(43, 6, 16, T, seed=args.seed + 900, device=dev)
+    rng = np.random.default_rng(args.seed + 901)
+    sel_np = np.sort(np.stack([rng.choice(75000, size=512, replace=False)
+                               for _ in range(43 * 6)]), axis=1).astype(np.int32)
+    sel_a = torch.from_numpy(sel_np.reshape(43, 6, 512)).to(dev)
+    a_out = torch.empty_like(ai["q"])
+    a_args = NB.DsAttnArgs(43, 6, 16, 128, 75000, 4, 512, ai["q"].data_ptr(), ai["k"].data_ptr(),
+                           ai["v"].data_ptr(), T * 128, sel_a.data_ptr())
+    a_ws = torch.empty(lib.ds_attn_workspace_size(a_args), dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(warm + 20):
+        a, b = ev(), ev()
+        a.record(stream)
+        st = lib.ds_sparse_attention(a_args, a_out.data_ptr(), a_ws.data_ptr(), a_ws.numel(), sptr)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if st:
+            raise RuntimeError(f"ds_sparse_attention: status {st}")
+        if i >= warm:
+            ts.append(a.elapsed_time(b))
+    us = 1e3 * statistics.median(ts)
+    a_bytes = 43 * 6 * 512 * 4 * 256 * 2 + 43 * 6 * 16 * 128 * 2 * 2
+    out["attention"] = {"layers": 43, "rows": 6, "heads": 16, "blocks": 512, "us": round(us, 1),
+                        "bytes": a_bytes, "gbs": round(a_bytes / (us * 1e-6) / 1e9, 1)}
+    del ai, a_out, a_ws, sel_a
     # the acceptance step after the verify: R = 6 rows over the vocabulary, one step and a
     # batch of 64 independent steps, greedy and exact speculative sampling at T = 1
     out["accept"] = {}

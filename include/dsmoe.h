@@ -302,6 +302,41 @@ size_t ds_select_workspace_offset(const ds_select_args* args, int32_t with_compa
                                   int32_t part);
 
 /* ------------------------------------------------------------------------------------
+ * Sparse attention over the selected blocks (page "DeepSeek V4.1F Q4 on M3 Ultra with
+ * native DSpark MTP (40tps / 800tps)", paragraph "Decode at depth": each layer attends to
+ * the 512 blocks its selection picks). The pages stop at the selection; the arithmetic is
+ * the plain reading: for layer l, row r and query head h,
+ *   s_t = q_{l,r,h} . k_{l,t} / sqrt(D) over the tokens t of the row's selected blocks
+ *         (tokens block_tokens * b .. block_tokens * b + block_tokens - 1 of block b),
+ *   p = softmax(s),  out_{l,r,h} = bf16_RNE(sum_t p_t v_{l,t}),
+ * all heads of a row sharing each token's key and value; a row with no selected block
+ * gets 0. Sums in fp32 on the tensor cores (bf16 products exact; p carried as a bf16 high
+ * and low part), so the result is not bit-exact with an fp64 evaluation. */
+typedef struct {
+  int32_t n_layers;       /* L                                                       */
+  int32_t n_rows;         /* R, 1 .. 8                                               */
+  int32_t n_heads;        /* Hq query heads, 1 .. 16                                 */
+  int32_t head_dim;       /* D, 128                                                  */
+  int32_t n_blocks;       /* N blocks per layer                                      */
+  int32_t block_tokens;   /* tokens per block: 1, 2, 4, 8 or 16                      */
+  int32_t top_k;          /* entries of sel per row, 1 .. 2048                       */
+  const uint16_t* q;      /* bf16 [L][R][Hq][D]                                      */
+  const uint16_t* k;      /* bf16 [L][N * block_tokens][D], layer stride below        */
+  const uint16_t* v;      /* same layout as k                                        */
+  int64_t kv_layer_stride;   /* values between layers of k and v (>= N*block_tokens*D) */
+  const int32_t* sel;     /* int32 [L][R][top_k]: block ids (as written by
+                             ds_select_blocks), -1 for none; ids >= N are skipped     */
+} ds_attn_args;
+
+/* Workspace bytes for these arguments (0 when they are invalid). Host-only. */
+size_t ds_attn_workspace_size(const ds_attn_args* args);
+/* out: bf16 [L][R][Hq][D] (device, 16-byte aligned); q, k, v 16-byte aligned; workspace
+ * 256-byte aligned of ds_attn_workspace_size bytes. DS_ERR_INVALID_ARG outside the limits
+ * above, DS_ERR_UNSUPPORTED for head_dim != 128. */
+ds_status ds_sparse_attention(const ds_attn_args* args, uint16_t* out, void* workspace,
+                              size_t ws_bytes, ds_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * Paired Q8 projections (page "DeepSeek V4.1F Q4 on M3 Ultra with native DSpark MTP
  * (40tps / 800tps)", paragraph "DSpark": the 6 verify rows share one weight stream
  * through paired Q8 projections). Format as defined for this workload: a logical

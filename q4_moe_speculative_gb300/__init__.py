@@ -15,7 +15,7 @@ from . import _native as N
 __all__ = [
     "MoeLayer", "q4_tile", "moe_workspace_size", "moe_verify_forward", "select_workspace_size",
     "select_blocks", "workspace_status", "version", "DsmoeError", "verify_greedy",
-    "verify_sample", "q8_tile", "q8_project",
+    "verify_sample", "q8_tile", "q8_project", "sparse_attention",
 ]
 
 DsmoeError = N.DsmoeError
@@ -351,6 +351,34 @@ def verify_sample(logits: torch.Tensor, T: float, qd: torch.Tensor | None,
         _stream(stream))
     _check(st, "ds_verify_sample")
     return out, n_out
+
+
+def sparse_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, sel: torch.Tensor,
+                     block_tokens: int = 4, *, out=None, workspace=None, stream=None):
+    """Attention of each row's query heads over the tokens of its selected blocks:
+    q bf16 [L, R, Hq, 128], k and v bf16 [L, T, 128] (T = blocks x block_tokens), sel int32
+    [L, R, K] (block ids, -1 for none) -> bf16 [L, R, Hq, 128] (ds_sparse_attention)."""
+    lib = N.load()
+    _need(q, "q", torch.bfloat16)
+    L, R, Hq, D = q.shape
+    _need(k, "k", torch.bfloat16)
+    _need(v, "v", torch.bfloat16, tuple(k.shape))
+    _need(sel, "sel", torch.int32)
+    if k.shape[0] != L or k.shape[2] != D or sel.shape[:2] != (L, R):
+        raise ValueError("k, v must be [L, T, D] and sel [L, R, K] for q [L, R, Hq, D]")
+    T = k.shape[1]
+    args = N.DsAttnArgs(L, R, Hq, D, T // block_tokens, block_tokens, sel.shape[2], _ptr(q),
+                        _ptr(k), _ptr(v), T * D, _ptr(sel))
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", torch.bfloat16, tuple(q.shape))
+    need = lib.ds_attn_workspace_size(args)
+    if need == 0:
+        raise ValueError("invalid sparse attention arguments")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(lib.ds_sparse_attention(args, _ptr(out), _ptr(workspace), workspace.numel(),
+                                   _stream(stream)), "ds_sparse_attention")
+    return out
 
 
 def noalloc_status(stream=None) -> int:

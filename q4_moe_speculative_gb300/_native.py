@@ -24,7 +24,7 @@ EXPORTS = (
     "ds_moe_verify_forward_noalloc", "ds_noalloc_status", "ds_q4_tiled_bytes", "ds_q4_tile",
     "ds_select_workspace_offset", "ds_verify_workspace_size", "ds_verify_greedy",
     "ds_verify_sample", "ds_q8_tiled_bytes", "ds_q8_tile", "ds_q8_workspace_size",
-    "ds_q8_project",
+    "ds_q8_project", "ds_attn_workspace_size", "ds_sparse_attention",
 )
 SELECT_WS_PARTS = {"union": 0, "union_count": 1, "scores": 2, "key_norms": 3, "row_scales": 4}
 
@@ -71,6 +71,15 @@ class DsSelectArgs(C.Structure):
         ("keys", C.c_void_p), ("key_layer_stride", C.c_int64),
         ("q", C.c_void_p), ("head_w", C.c_void_p),
         ("mask", C.c_void_p), ("limit", C.c_void_p), ("flags", C.c_int32),
+    ]
+
+
+class DsAttnArgs(C.Structure):
+    _fields_ = [
+        ("n_layers", C.c_int32), ("n_rows", C.c_int32), ("n_heads", C.c_int32),
+        ("head_dim", C.c_int32), ("n_blocks", C.c_int32), ("block_tokens", C.c_int32),
+        ("top_k", C.c_int32), ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p),
+        ("kv_layer_stride", C.c_int64), ("sel", C.c_void_p),
     ]
 
 
@@ -124,6 +133,11 @@ def load() -> C.CDLL:
     lib.ds_select_blocks.restype = C.c_int
     lib.ds_select_blocks_marked.argtypes = lib.ds_select_blocks.argtypes + [C.c_void_p]
     lib.ds_select_blocks_marked.restype = C.c_int
+    lib.ds_attn_workspace_size.argtypes = [C.POINTER(DsAttnArgs)]
+    lib.ds_attn_workspace_size.restype = C.c_size_t
+    lib.ds_sparse_attention.argtypes = [C.POINTER(DsAttnArgs), C.c_void_p, C.c_void_p,
+                                        C.c_size_t, C.c_void_p]
+    lib.ds_sparse_attention.restype = C.c_int
     lib.ds_q8_tiled_bytes.argtypes = [C.c_int64, C.c_int32]
     lib.ds_q8_tiled_bytes.restype = C.c_size_t
     lib.ds_q8_tile.argtypes = [C.POINTER(DsQ8), C.c_int64, C.c_int32, C.c_void_p, C.c_size_t,

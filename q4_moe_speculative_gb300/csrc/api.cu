@@ -246,6 +246,50 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
 
 namespace {
 
+ds_status check_attn(const ds_attn_args* a) {
+  if (!a) return DS_ERR_INVALID_ARG;
+  if (a->n_layers < 1 || a->n_rows < 1 || a->n_rows > 8 || a->n_heads < 1 || a->n_heads > 16)
+    return DS_ERR_INVALID_ARG;
+  const int bs = a->block_tokens;
+  if (!(bs == 1 || bs == 2 || bs == 4 || bs == 8 || bs == 16)) return DS_ERR_INVALID_ARG;
+  if (a->n_blocks < 1 || a->n_blocks > (1 << 24) || a->top_k < 1 || a->top_k > 2048)
+    return DS_ERR_INVALID_ARG;
+  if (a->head_dim < 1) return DS_ERR_INVALID_ARG;
+  if (a->head_dim != 128) return DS_ERR_UNSUPPORTED;
+  if ((long long)a->n_layers * a->n_rows > 65535) return DS_ERR_INVALID_ARG;
+  if (a->kv_layer_stride < (int64_t)a->n_blocks * bs * a->head_dim) return DS_ERR_INVALID_ARG;
+  if (!a->q || !a->k || !a->v || !a->sel) return DS_ERR_INVALID_ARG;
+  if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->sel, 4))
+    return DS_ERR_INVALID_ARG;
+  if (a->kv_layer_stride % 8) return DS_ERR_INVALID_ARG;   // 16-byte aligned layers
+  return DS_OK;
+}
+
+}  // namespace
+
+size_t ds_attn_workspace_size(const ds_attn_args* a) {
+  if (check_attn(a) != DS_OK) return 0;
+  return attn_layout(a->n_layers, a->n_rows, attn_splits(a->n_layers, a->n_rows)).total;
+}
+
+ds_status ds_sparse_attention(const ds_attn_args* a, uint16_t* out, void* workspace,
+                              size_t ws_bytes, ds_stream_t stream) {
+  const ds_status st = check_attn(a);
+  if (st != DS_OK) return st;
+  if (!out || !aligned(out, 16)) return DS_ERR_INVALID_ARG;
+  const int splits = attn_splits(a->n_layers, a->n_rows);
+  const AttnLayout Ly = attn_layout(a->n_layers, a->n_rows, splits);
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < Ly.total) return DS_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(base, 0, Ly.part, s) != cudaSuccess) return DS_ERR_CUDA;   // header, counts
+  AttnProblem p{a->n_layers, a->n_rows, a->n_heads, a->n_blocks, a->block_tokens, a->top_k,
+                a->kv_layer_stride, a->q, a->k, a->v, a->sel, out};
+  return launch_attn(p, base, s) == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
+namespace {
+
 bool q8_sizes_ok(int64_t rows, int32_t K) {
   return rows >= 16 && rows <= (1 << 24) && rows % 16 == 0 && K >= 32 && K <= 65536 &&
          K % 32 == 0;

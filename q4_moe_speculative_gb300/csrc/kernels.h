@@ -118,6 +118,23 @@ bool q8_plan(int R, int K, int* stages, int* slots, size_t* smem);
 cudaError_t launch_q8_project(const void* tiles, int rows, int K, const uint16_t* x, int R,
                               uint16_t* y, uint32_t* status, cudaStream_t s);
 
+// ---- sparse attention over the selected blocks (attn.cu)
+struct AttnProblem {
+  int L, R, Hq, N, bs, K;
+  int64_t kv_stride;
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  const int32_t* sel;
+  uint16_t* out;
+};
+struct AttnLayout {
+  size_t header, count, part, total;
+};
+int attn_splits(int L, int R);
+AttnLayout attn_layout(int L, int R, int splits);
+cudaError_t launch_attn(const AttnProblem& p, uint8_t* ws, cudaStream_t s);
+
 // ---- verify acceptance (accept.cu)
 constexpr int kAcceptChunk = 4096;    // tokens of a row per CTA
 constexpr int kAcceptMaxRows = 16;

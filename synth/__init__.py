@@ -17,6 +17,9 @@ distributions of the workload definitions):
   - Paired Q8 projections: int8 values uniform in [-128, 127], fp16 scales
     uniform(0.5, 2) x 2^-7 (so |W| is about 0.5 at most, comparable to a trained layer's
     weights), verify rows bf16 N(0, 1).
+  - Sparse attention over the selected blocks: queries bf16 N(0, sigma^2) [L][R][Hq][128]
+    (sigma 1, or larger for peaked attention), keys and values bf16 N(0, 1) per token
+    [L][T][128], T = 4 x blocks.
   - Speculative acceptance: Bernoulli(a) per draft, seeded (the sweep); and, for the
     acceptance step itself, target logits N(0, 1.5^2) per token with one planted strong
     token per row (its logit raised by `peak` x U(0.5, 1.5)), a drafter distribution that
@@ -232,3 +235,13 @@ def q8_matrix(rows: int, K: int, seed: int = 0, device="cpu"):
     qs = torch.randint(-128, 128, (rows, K), dtype=torch.int8, generator=g, device=device)
     sc = torch.rand((rows, K // 32), generator=g, device=device).mul_(1.5).add_(0.5)
     return qs, sc.mul_(2.0 ** -7).to(torch.float16)
+
+
+def attention_inputs(L: int, R: int, Hq: int, T: int, seed: int = 0, sigma: float = 1.0,
+                     device="cpu") -> dict:
+    """Queries bf16 N(0, sigma^2) [L][R][Hq][128]; keys and values bf16 N(0, 1) [L][T][128]."""
+    g = _gen(seed, device)
+    q = torch.randn((L, R, Hq, 128), generator=g, device=device).mul_(sigma)
+    k = torch.randn((L, T, 128), generator=g, device=device)
+    v = torch.randn((L, T, 128), generator=g, device=device)
+    return {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}

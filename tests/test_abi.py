@@ -258,3 +258,26 @@ def test_q8_sizes_and_argument_checks(lib):
     assert p(w, 48, 512, FAKE, 6, FAKE + 8, FAKE, 256, None) == 1   # x alignment
     assert p(w, 64, 544, FAKE, 6, FAKE, FAKE, 256, None) == 2       # K % 512: unsupported
     assert p(w, 64, 1056, FAKE, 6, FAKE, FAKE, 256, None) == 2
+
+
+def test_attention_argument_checks(lib):
+    from q4_moe_speculative_gb300 import _native as N
+
+    def args(**kw):
+        d = dict(n_layers=2, n_rows=6, n_heads=16, head_dim=128, n_blocks=2048, block_tokens=4,
+                 top_k=512, q=FAKE, k=FAKE, v=FAKE, kv_layer_stride=2048 * 4 * 128, sel=FAKE)
+        d.update(kw)
+        return N.DsAttnArgs(*[d[f] for f, _ in N.DsAttnArgs._fields_])
+
+    good = args()
+    ws = lib.ds_attn_workspace_size(good)
+    assert ws > 0 and ws % 256 == 0
+    for kw, code in (({"n_rows": 9}, 1), ({"n_heads": 17}, 1), ({"block_tokens": 3}, 1),
+                     ({"top_k": 2049}, 1), ({"head_dim": 64}, 2), ({"q": None}, 1),
+                     ({"k": FAKE + 8}, 1), ({"kv_layer_stride": 100}, 1), ({"n_blocks": 0}, 1)):
+        a = args(**kw)
+        assert lib.ds_attn_workspace_size(a) == 0
+        assert lib.ds_sparse_attention(a, FAKE, FAKE, ws, None) == code, kw
+    assert lib.ds_sparse_attention(good, None, FAKE, ws, None) == 1
+    assert lib.ds_sparse_attention(good, FAKE, FAKE, ws - 1, None) == 3
+    assert lib.ds_sparse_attention(good, FAKE, FAKE + 16, ws, None) == 3
