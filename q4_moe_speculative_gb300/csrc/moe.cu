@@ -512,6 +512,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
       }
       consumer_sync();
     }
+    // the prologue (zeroed header) is complete and visible from here on
+    pdl_wait();
     // (2) every CTA's scores are written: count this one (the barrier orders its scores
     // before the fence), wait for all, then each CTA builds the route from all scores
     if (tid == 0) {
@@ -779,6 +781,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
     // order, h = bf16_rne(silu(g) * u) is written for the expert's rows, and the unit is
     // counted against its expert slot.
     const int rtid = tid - kReducer0;
+    pdl_wait();   // the prologue (zeroed header) is complete
     if (!pipe_wait(&s_route, 0)) timed_out = true;
     const int n_union = s_nunion;
     const int n_units = (1 + n_union) * RTg;
@@ -855,24 +858,38 @@ int moe_ring(const MoeDims& d) {
 
 template <int KPER>
 cudaError_t launch_moe_k(const MoeArgs& a, size_t smem, cudaStream_t s) {
-  cudaError_t err = cudaFuncSetAttribute(k_moe<KPER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+  // the shared-memory attribute and the one-CTA-per-SM check, once per device and size
+  static thread_local int set_dev = -1;
+  static thread_local size_t set_smem = 0;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_moe<KPER>, kMoeThreads, smem);
-  if (err != cudaSuccess) return err;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  // one CTA per SM, all resident at once (cooperative launch)
+  if (dev != set_dev || smem != set_smem) {
+    err = cudaFuncSetAttribute(k_moe<KPER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_moe<KPER>, kMoeThreads, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    set_dev = dev;
+    set_smem = smem;
+  }
+  // one CTA per SM, all resident at once (cooperative launch), allowed to start while the
+  // prologue before it finishes (programmatic dependent launch: the kernel waits for the
+  // prologue before it touches the workspace header)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(device_sm_count());
   cfg.blockDim = dim3(kMoeThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k_moe<KPER>, a);
 }
 
