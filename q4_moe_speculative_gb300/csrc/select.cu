@@ -87,14 +87,13 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) 
   return res;
 }
 
-// Admitted bits of mask word wi for a row with limit lim (bits at b >= lim cleared).
+// Admitted bits of mask word wi for a row with limit lim (bits at b >= lim cleared). The
+// load is predicated rather than branched around, so that a thread's loads of several
+// words and rows are all in flight together.
 __device__ __forceinline__ uint32_t admitted_word(const uint32_t* m, int wi, int lim) {
-  const int b0 = wi * 32;
-  if (b0 >= lim) return 0u;
-  uint32_t w = m[wi];
-  const int rem = lim - b0;
-  if (rem < 32) w &= (1u << rem) - 1u;
-  return w;
+  const int rem = lim - wi * 32;
+  const uint32_t w = rem > 0 ? __ldg(m + wi) : 0u;
+  return rem >= 32 ? w : (rem > 0 ? w & ((1u << rem) - 1u) : 0u);
 }
 
 // d + q_lo k_lo, then + q_hi k_hi, for two packed bf16 pairs: each step is one fused
@@ -249,62 +248,67 @@ __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) 
     c_first = uchunk * kCompactThreads;
     c_last = min(W, c_first + kCompactThreads);
     int c = 0;
+#pragma unroll 2
     for (int wi = tid; wi < c_first; wi += kCompactThreads) {
       uint32_t mw = 0;
-      for (int r = 0; r < R; ++r) mw |= admitted_word(a.mask + ((size_t)l * R + r) * W, wi, s_lim[r]);
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r < R) mw |= admitted_word(a.mask + ((size_t)l * R + r) * W, wi, s_lim[r]);
       c += __popc(mw);
     }
     block_excl_scan(c, scratch, &base);
   }
   for (int c0 = c_first; c0 < c_last; c0 += kCompactThreads) {
+    // word wi = c0 + tid of each row read (per row for the union): its admitted bits
     const int wi = c0 + tid;
-    uint32_t mw = 0;
+    uint32_t mine[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) mine[r] = 0u;
     if (wi < W) {
       if (union_cta) {
-        for (int r = 0; r < R; ++r)
-          mw |= admitted_word(a.mask + ((size_t)l * R + r) * W, wi, s_lim[r]);
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r < R) mine[r] = admitted_word(a.mask + ((size_t)l * R + r) * W, wi, s_lim[r]);
       } else {
-        mw = admitted_word(mrow, wi, lim_row);
+        mine[0] = admitted_word(mrow, wi, lim_row);
       }
     }
+    uint32_t mw = 0;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) mw |= mine[r];
+    // a word whose admitted bits are the same in every row (a shared mask away from the
+    // limits): each of its union entries is admitted by every row
+    bool same = true;
+#pragma unroll
+    for (int r = 1; r < 8; ++r)
+      if (r < R) same = same && mine[r] == mine[0];
     int total;
     const int excl = base + block_excl_scan(__popc(mw), scratch, &total);
     s_off[tid] = excl;
     if (union_cta && wi < W) a.uwordoff[(size_t)l * W + wi] = excl;
     __syncthreads();
-    // Warp `warp` scatters the words c0 + 32*warp .. c0 + 32*warp + 31 of this chunk: lane
-    // j first loads word j's admitted bits (per row for the union), then the words are
-    // taken one by one with the bits broadcast by shuffles (loads all in flight at once).
+    // Warp `warp` scatters the words c0 + 32*warp .. c0 + 32*warp + 31 of this chunk, whose
+    // bits sit in its lanes 0..31, one word at a time with the bits broadcast by shuffles.
     {
       const int wbase = c0 + warp * 32;
-      const int wl = wbase + lane;
-      uint32_t mine[8];
-#pragma unroll
-      for (int r = 0; r < 8; ++r) mine[r] = 0u;
-      if (wl < W) {
-        if (union_cta) {
-#pragma unroll
-          for (int r = 0; r < 8; ++r)
-            if (r < R) mine[r] = admitted_word(a.mask + ((size_t)l * R + r) * W, wl, s_lim[r]);
-        } else {
-          mine[0] = admitted_word(mrow, wl, lim_row);
-        }
-      }
-      for (int jw = 0; jw < 32 && wbase + jw < W && warp * 32 + jw < kCompactThreads; ++jw) {
+      const uint32_t all_rows = (1u << R) - 1u;
+      for (int jw = 0; jw < 32 && wbase + jw < W; ++jw) {
         const int w = wbase + jw;
         const int b = w * 32 + lane;
+        const uint32_t wv = __shfl_sync(0xffffffffu, mw, jw);
+        const bool pred = (wv >> lane) & 1u;
         uint32_t rows = 0;
         if (union_cta) {
+          if (__shfl_sync(0xffffffffu, same ? 1 : 0, jw)) {
+            rows = pred ? all_rows : 0u;
+          } else {
 #pragma unroll
-          for (int r = 0; r < 8; ++r)
-            if (r < R && ((__shfl_sync(0xffffffffu, mine[r], jw) >> lane) & 1u)) rows |= 1u << r;
-        } else {
-          rows = (__shfl_sync(0xffffffffu, mine[0], jw) >> lane) & 1u;
+            for (int r = 0; r < 8; ++r)
+              if (r < R && ((__shfl_sync(0xffffffffu, mine[r], jw) >> lane) & 1u)) rows |= 1u << r;
+          }
         }
-        const bool pred = rows != 0;
-        const uint32_t bal = __ballot_sync(0xffffffffu, pred);
         if (pred) {
-          const int off = s_off[warp * 32 + jw] + __popc(bal & ((1u << lane) - 1u));
+          const int off = s_off[warp * 32 + jw] + __popc(wv & ((1u << lane) - 1u));
           if (union_cta) {
             a.uidx[(size_t)l * N + off] = b;
             a.urows[(size_t)l * N + off] = (uint8_t)rows;
