@@ -79,15 +79,20 @@ struct SelWorkspace {
   float* cscore;      // [L][R][NS] by union entry: canonical or tensor-core scores
                       // (-inf where the row does not admit the entry)
   float* knorm;       // [L][NS] by union entry: key norm bound (tensor-core scoring)
+  float* kmax;        // [L][NC] the largest knorm of each 32 union entries (NC = NS / 32
+                      // rounded up; tensor-core scoring)
   float* qnorm;       // [L][R] sum_h |w_h| ||q_h|| bound (tensor-core scoring)
 };
 
 // Row stride of the score arrays (cscore, knorm): N rounded up to a multiple of 4, so that
 // every row starts 16-byte aligned.
 inline int score_stride(int N) { return (N + 3) & ~3; }
+// Row stride of kmax: one value per 32 union entries.
+inline int chunk_stride(int N) { return (score_stride(N) + 31) / 32; }
 
 struct SelLayout {
-  size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, knorm, qnorm, total;
+  size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, knorm, kmax, qnorm,
+      total;
 };
 SelLayout sel_layout(const SelDims& d, bool caller_cidx);
 bool tc_scoring_supported(const SelDims& d, const uint16_t* keys, const uint16_t* q);

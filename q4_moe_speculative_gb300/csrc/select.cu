@@ -96,6 +96,25 @@ __device__ __forceinline__ uint32_t admitted_word(const uint32_t* m, int wi, int
   return rem >= 32 ? w : (rem > 0 ? w & ((1u << rem) - 1u) : 0u);
 }
 
+// d0 + qa k, d1 + qb k for the bf16 pair (qa, qb) of qw and the bf16 k in the low (HI =
+// false) or high half of kw: fused multiply-adds of bf16 operands into fp32 (exact
+// product, one rounding), the same values as fmaf on the operands widened to fp32.
+template <bool HI>
+__device__ __forceinline__ void fma_pair_bf16(float& d0, float& d1, uint32_t qw, uint32_t kw) {
+  if (HI)
+    asm("{\n\t.reg .b16 qa, qb, kl, kh;\n\t"
+        "mov.b32 {qa, qb}, %2;\n\tmov.b32 {kl, kh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, qa, kh, %0;\n\tfma.rn.f32.bf16 %1, qb, kh, %1;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "r"(qw), "r"(kw));
+  else
+    asm("{\n\t.reg .b16 qa, qb, kl, kh;\n\t"
+        "mov.b32 {qa, qb}, %2;\n\tmov.b32 {kl, kh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, qa, kl, %0;\n\tfma.rn.f32.bf16 %1, qb, kl, %1;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "r"(qw), "r"(kw));
+}
+
 // d + q_lo k_lo, then + q_hi k_hi, for two packed bf16 pairs: each step is one fused
 // multiply-add of bf16 operands into fp32 (the product is exact, one rounding), the same
 // value as fmaf on the operands widened to fp32.
@@ -342,10 +361,12 @@ struct ScoreArgs {
   uint32_t* sc0;      // [L][R][NS] by union entry: fp32 scores (-inf: not admitted)
   float* knorm;       // [L][NS] by union entry: key norm bound (tensor-core mode)
   float* qnorm;       // [L][R] 2^-13 sum_h |w_h| ||q_h|| bound (tensor-core mode)
+  float* kmax;        // [L][NC] the largest knorm of each 32 union entries (tensor-core mode)
   uint32_t* status;
   int tma;            // kmap is valid: tiles of 128 consecutive blocks come by TMA
   CUtensorMap kmap;   // keys [L][N][128] bf16, boxes of 64 values x 128 blocks, 128B swizzle
   int NS;             // row stride of sc0 / knorm (N rounded up to a multiple of 4)
+  int NC;             // row stride of kmax
 };
 
 // ---------------------------------------------------------------------------------
@@ -447,6 +468,28 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+// Scores and key norms written by K5 are read back by K7 right after: kept in L2 ahead of
+// the streamed keys, then read with evict_first so that they leave first once read.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void st_hint(uint32_t* p, uint32_t v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void st_hint(float* p, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_hint_v4(const uint32_t* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
 }
 __device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, bool valid,
                                                 uint64_t policy) {
@@ -811,6 +854,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
     const int bar_id = 1 + g;
     const uint32_t tbuf = tmem + (uint32_t)g * kCols;
     uint32_t mphase = 0;
+    const uint64_t spol = l2_evict_last_policy();   // scores stay in L2 for K7
     bool issued = false;    // this group has MMAs whose commit it has not observed
     int wlayer = -1;        // layer whose head weights s_wg[g] holds
     for (int i = g; i < n; i += kTcGroups) {
@@ -887,13 +931,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
       for (int c = 0; c < NCH; ++c) sm100::tmem_ld16(lane_base + (uint32_t)(c * 16), d + c * 16);
       sm100::tc_fence_before();   // the group barrier of the next tile orders the next MMA
       const int e = e0 + row;
+      {
+        // the largest key norm bound of this warp's 32 entries (a tile starts at a multiple
+        // of 128 entries): K7's first test takes it in place of each entry's own
+        const float kc = warp_max(e < ucnt ? kn : 0.0f);
+        if (lane == 0 && e < ucnt) st_hint(a.kmax + (size_t)l * a.NC + (e >> 5), kc, spol);
+      }
       if (e < ucnt) {
         // row r's tensor-core score; its interval comes from kn and the row's scale
         // (tc_lo / tc_hi) wherever it is used
-        a.knorm[(size_t)l * a.NS + e] = kn;
+        st_hint(a.knorm + (size_t)l * a.NS + e, kn, spol);
         auto emit = [&](int r, float sc) {
           const size_t out = ((size_t)l * R + r) * a.NS + e;
-          a.sc0[out] = (rows & (1u << r)) ? __float_as_uint(sc) : kMinusInfBits;
+          st_hint(a.sc0 + out, (rows & (1u << r)) ? __float_as_uint(sc) : kMinusInfBits, spol);
         };
         if constexpr (HH > 0) {   // head count known at compile time: static indices
 #pragma unroll
@@ -987,21 +1037,24 @@ __device__ __forceinline__ void hist_pass(int n, bool resid, const uint32_t* r_k
 // while this one fills), one after warp 0 has found the bucket (8 bins per lane, a warp
 // scan). *need_out = how many elements equal to the threshold belong to the selection.
 // All threads must call it.
+// With start > 0 the first `start` digits are given (prefix0): every element that can
+// reach the threshold has them, and the elements that do not are counted below it.
 template <typename KeyAt>
 __device__ uint32_t radix_threshold(int n, int need, KeyAt key_at, int* hist, int* scratch,
                                     uint32_t* r_key, int* s_misc, uint32_t* status,
-                                    int* need_out, int passes = 4) {
+                                    int* need_out, int passes = 4, int start = 0,
+                                    uint32_t prefix0 = 0u) {
   (void)scratch;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int& s_bucket = s_misc[0];
   int& s_need = s_misc[1];
   int& s_rn = s_misc[2];
   int& s_cnt = s_misc[3];   // elements in the chosen bucket
-  uint32_t prefix = 0;
+  uint32_t prefix = prefix0;
   bool resid = false;
-  for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+  for (int i = tid; i < 256; i += blockDim.x) hist[(start & 1) * 256 + i] = 0;
   __syncthreads();
-  for (int pass = 0; pass < passes; ++pass) {
+  for (int pass = start; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
     int* h = hist + (pass & 1) * 256;
     if (tid == 0 && pass == 1) s_rn = 0;
@@ -1177,27 +1230,58 @@ struct TopkArgs {
   uint32_t* sc0;
   const float* knorm;
   const float* qnorm;
+  const float* kmax;
   int32_t* sel;
   int32_t* nsel;
   uint32_t* status;
   int tc_mode;
   int NS;             // row stride of sc0 / knorm (N rounded up to a multiple of 4)
+  int NC;             // row stride of kmax
 };
 
+// Bitonic sort, descending, of one 64-bit value per thread over threads 0 .. P - 1 (P a
+// power of two <= the block size; the other threads sort their own values among
+// themselves): returns the value of this thread's rank. Exchanges within a warp go by
+// shuffles, wider ones through buf (2 x blockDim.x values, alternating, one barrier each).
+// All threads must call it.
+__device__ uint64_t block_sort_desc(uint64_t v, int P, uint64_t* buf) {
+  const int tid = threadIdx.x;
+  int step = 0;
+  for (int k = 2; k <= P; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      uint64_t o;
+      if (j >= 32) {
+        uint64_t* b = buf + (step & 1) * blockDim.x;
+        b[tid] = v;
+        __syncthreads();
+        o = b[tid ^ j];
+        ++step;
+      } else {
+        o = __shfl_xor_sync(0xffffffffu, v, j);
+      }
+      const bool lower = (tid & j) == 0, first_half_up = (tid & k) == 0;
+      v = (lower == first_half_up) ? (v > o ? v : o) : (v < o ? v : o);
+    }
+  }
+  return v;
+}
+
 constexpr int kWarpBuf = 256;   // collected entries a warp keeps before the lists merge
-constexpr int kRescoreRound = kTopkThreads / 4;   // uncertain candidates re-scored per round
-constexpr int kRescorePitch = 272;   // bytes per staged key row (16-byte reads spread over banks)
+constexpr int kRescoreRound = 96;    // uncertain candidates re-scored per round (<= threads / 4)
+constexpr int kRescoreBuf = kRescoreRound * 256;   // one round's staged keys (two alternate)
 // dynamic shared memory of K7: residual keys, candidates and their keys, the row's queries
-// (fp32, [i][head]) and head weights, the collection (block id, lower and upper bound key)
+// (fp32, [i][head]) and head weights, the collection (block id, lower and upper bound key),
+// the queries again as bf16 pairs for up to 8 heads
 constexpr size_t kTopkSmem = sizeof(uint32_t) * kResidCap + sizeof(int32_t) * 2 * kCandCap +
                              sizeof(float) * (kScoreMaxHeads * 128 + kScoreMaxHeads) +
-                             sizeof(int32_t) * 3 * kCollectCap;
+                             sizeof(int32_t) * 3 * kCollectCap + sizeof(uint32_t) * 4 * 128;
 // the warps' collection lists live over the residual keys and the candidates
 static_assert((size_t)3 * kTopkWarps * kWarpBuf <= (size_t)kResidCap + 2 * kCandCap,
               "collection lists overlap the queries");
 static_assert(kCollectCap >= 2048, "the tau sample lives over the collection");
-static_assert((size_t)kRescoreRound * kRescorePitch <= sizeof(int32_t) * 3 * kCollectCap,
+static_assert((size_t)2 * kRescoreBuf <= sizeof(int32_t) * 3 * kCollectCap,
               "key staging overlaps past the collection");
+static_assert(4 * kRescoreRound <= kTopkThreads, "four threads per candidate");
 static_assert(kScoreMaxHeads == 16, "four threads of four heads each per candidate");
 
 __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
@@ -1206,7 +1290,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   __shared__ int s_misc[4];
   __shared__ int s_eq[kTopkWarps], s_gt[kTopkWarps];
   __shared__ int s_cnt[kTopkWarps], s_lo[kTopkWarps];
-  __shared__ unsigned s_dmax;
+  __shared__ unsigned s_dmax, s_maxlo;
   extern __shared__ __align__(16) uint8_t dsm[];
   uint32_t* r_key = reinterpret_cast<uint32_t*>(dsm);              // [kResidCap]
   int32_t* cand = reinterpret_cast<int32_t*>(r_key + kResidCap);   // [kCandCap]
@@ -1216,11 +1300,14 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   int32_t* col_i = reinterpret_cast<int32_t*>(wf + kScoreMaxHeads);
   uint32_t* col_lo = reinterpret_cast<uint32_t*>(col_i + kCollectCap);
   uint32_t* col_hi = col_lo + kCollectCap;
+  // [i / 4][t][i % 4]: bf16 pair (head t, head t + 4) of query value i, t = 0..3
+  uint32_t* qb = col_hi + kCollectCap;
   uint32_t* const wbuf = r_key;                                    // [warp][3][kWarpBuf]
   uint32_t* const samp = reinterpret_cast<uint32_t*>(col_i);       // [2048]
 
   pdl_wait();   // the scores and the compaction are complete
   pdl_trigger();
+  if (threadIdx.x == 0) s_maxlo = 0u;
   const int lr = blockIdx.x;
   const int l = lr / a.R;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1249,6 +1336,14 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
     const uint16_t* qrow = a.q + (size_t)lr * a.Hh * 128;
     for (int i = tid; i < a.Hh * 128; i += blockDim.x)
       qf[(i & 127) * kScoreMaxHeads + qslot(i >> 7)] = bf16_bits_to_f32(qrow[i]);
+    if (a.Hh <= 8) {
+      for (int w = tid; w < 4 * 128; w += blockDim.x) {
+        const int i = w & 127, t = w >> 7;   // value i of heads t (low half) and t + 4
+        const uint32_t lo = t < a.Hh ? qrow[t * 128 + i] : 0u;
+        const uint32_t hi = t + 4 < a.Hh ? qrow[(t + 4) * 128 + i] : 0u;
+        qb[((i >> 2) * 4 + t) * 4 + (i & 3)] = lo | (hi << 16);
+      }
+    }
   };
 
   if (a.tc_mode) {
@@ -1259,114 +1354,150 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
     if (n > kCollectCap) {
       constexpr int kChunks = 64, kS = kChunks * 32;
       const int spacing = n / kChunks;
-      for (int j = tid; j < kS; j += blockDim.x) {
+      static_assert(kS % kTopkThreads == 0, "whole sample rounds");
+      constexpr int kPer = kS / kTopkThreads;
+      uint32_t sb[kPer];
+      float kb[kPer];
+#pragma unroll
+      for (int t = 0; t < kPer; ++t) {   // every load in flight, then the stores
+        const int j = tid + t * kTopkThreads;
         const int i = (j >> 5) * spacing + (j & 31);
-        samp[j] = tc_lo(s0[i], kn[i], G);
+        sb[t] = s0[i];
+        kb[t] = kn[i];
       }
+#pragma unroll
+      for (int t = 0; t < kPer; ++t) samp[tid + t * kTopkThreads] = tc_lo(sb[t], kb[t], G);
       __syncthreads();
       const int rank = min(kS, (int)(((long long)K * kS + n - 1) / n) + 16);
       int need;
       tau = radix_threshold(kS, rank, [&](int j) { return samp[j]; }, hist, scratch, nullptr,
                             s_misc, a.status, &need, 2);
     }
-    // ---- 2. collection. Each lane takes 4 consecutive entries of a group of 128 (16-byte
-    // loads; warp segments start at multiples of 128 entries, and entries past `end` in the
-    // last group lie inside the row's padded stride and are masked). U groups per batch;
-    // the next batch's loads are in flight while this one is classified. The taken entries
-    // keep index order: a lane's place is the prefix over the lanes of their counts
-    // (bit-sliced ballots).
-    //   First test, in round-to-nearest arithmetic: x = fmaf(kn, G, s) must reach t*, the
-    // smallest score whose key reaches tau, less a margin. If the exact test passes (the
-    // upper bound RU(s + RU(kn G)) >= t*), then s + kn G >= t* - 2^-23 (|s + RU(kn G)| +
-    // kn G) less a subnormal quantum, and x lies within 2^-24 |x| of s + kn G, so
-    // t* - x <= 2^-22 (|x| + kn G) + 2^-126: the margin 2^-21 (|x| + kn G) + 2^-126 keeps
-    // every entry the exact test takes (and an entry the row does not admit, s = -inf,
-    // never passes). tau at or below the key of -inf takes every entry: no first test.
+    // ---- 2. collection, in two passes per warp. Each warp walks a contiguous segment
+    // (starting at a multiple of 128 entries); entries past `end` in the last group lie
+    // inside the row's padded stride and are masked.
+    //   Pass 1 reads only the scores: lane L takes 16 consecutive entries of a batch of
+    // 512 (four 16-byte loads, the next batch in flight) and keeps those with s >= theta,
+    // theta = RD(RD(t* - A) - RU(2^-22 |t*| + 2^-126)), A = RU(kc G), where kc >= kn is the
+    // largest key norm bound of the entry's 32 and t* the smallest score whose key reaches
+    // tau. This keeps every entry the exact test takes: if RU(z) >= t* for
+    // z = s + RU(kn G), then z >= t* - ulp(z) >= t* - 2^-22 |t*| - 2^-149, and
+    // RU(kn G) <= A, so s >= t* - A - 2^-22 |t*| - 2^-149 >= theta. An entry the row does
+    // not admit (s = -inf) never passes; tau at or below the key of -inf takes every
+    // entry. The passing entries' positions are listed in order (a lane's place is the
+    // prefix over the lanes of their counts, by bit-sliced ballots).
+    //   Pass 2 takes the listed entries 32 at a time (all loads of a lane issued first),
+    // forms their exact bounds from the entry's own kn and keeps, in order and in place,
+    // the ones whose upper bound reaches tau, with their block ids and both bounds,
+    // counting the lower bounds that reach tau.
     int m = -1;
+    __syncthreads();   // s_maxlo is zero
     {
       const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 127) & ~127;
       const int beg = min(n, warp * seg), end = min(n, beg + seg);
       uint32_t* const b_i = wbuf + (size_t)warp * 3 * kWarpBuf;
       uint32_t* const b_lo = b_i + kWarpBuf;
       uint32_t* const b_hi = b_lo + kWarpBuf;
-      constexpr int U = 2;
+      const float* kc_row = a.kmax + (size_t)l * a.NC;
       const bool take_all = tau <= 0x007FFFFFu;
       const float tstar = key_score(tau);
-      const float crow = __fmaf_rn(0.000000476837158203125f, fabsf(tstar), 1.17549435e-38f);
-      int cnt = 0, nlo = 0;
-      uint4 sv[U];
-      float4 kv[U];
-      const uint4 kNone = make_uint4(kMinusInfBits, kMinusInfBits, kMinusInfBits, kMinusInfBits);
-      const float4 kZero = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = beg + u * 128 + 4 * lane;
-        sv[u] = i < end ? *reinterpret_cast<const uint4*>(s0 + i) : kNone;
-        kv[u] = i < end ? *reinterpret_cast<const float4*>(kn + i) : kZero;
-      }
       const unsigned lt = (1u << lane) - 1u;
-      for (int g0 = beg; g0 < end; g0 += 128 * U) {
-        uint4 sn[U];
-        float4 kx[U];
+      int c1 = 0;   // entries that pass the first test (listed while c1 < kWarpBuf)
+      {
+        const uint64_t rpol = l2_evict_first_policy();   // each score is read once here
+        // the first test's margin (see above), formed rounding upward
+        const float mt = __fmaf_ru(0.0000002384185791015625f, fabsf(tstar), 1.17549435e-38f);
+        const uint32_t all16 = take_all ? 0xFFFFu : 0u;
+        const uint4 kNone = make_uint4(kMinusInfBits, kMinusInfBits, kMinusInfBits, kMinusInfBits);
+        // lane L takes entries g + 16 L .. g + 16 L + 15 of a batch of 512 (four 16-byte
+        // loads; their 32-entry chunk is one kc)
+        auto load = [&](int g, uint4* v, float& k) {
+          const int i = g + 16 * lane;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int i = g0 + 128 * U + u * 128 + 4 * lane;
-          sn[u] = i < end ? *reinterpret_cast<const uint4*>(s0 + i) : kNone;
-          kx[u] = i < end ? *reinterpret_cast<const float4*>(kn + i) : kZero;
-        }
+          for (int j = 0; j < 4; ++j) v[j] = i + 4 * j < end ? ld_hint_v4(s0 + i + 4 * j, rpol) : kNone;
+          k = i < end ? kc_row[i >> 5] : 0.0f;
+        };
+        uint4 sv[4];
+        float kc;
+        load(beg, sv, kc);
+        for (int g0 = beg; g0 < end; g0 += 512) {
+          uint4 sn[4];
+          float kx;
+          load(g0 + 512, sn, kx);
+          const int i = g0 + 16 * lane;
+          const float th = __fsub_rd(__fsub_rd(tstar, __fmul_ru(kc, G)), mt);
+          uint32_t pm = all16;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int i = g0 + u * 128 + 4 * lane;
-          const uint32_t sb[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
-          const float k4[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-          unsigned pm = 0u;   // entries that pass the first test
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float sf = __uint_as_float(sb[e]);
-            const float ke = __fmul_rn(k4[e], G);
-            const float x = __fmaf_rn(k4[e], G, sf);
-            const bool pass =
-                take_all || __fsub_rn(tstar, x) <= __fmaf_rn(0.000000476837158203125f,
-                                                           __fadd_rn(fabsf(x), ke), crow);
-            pm |= (i + e < end && pass) ? 1u << e : 0u;
+          for (int j = 0; j < 4; ++j) {
+            pm |= __uint_as_float(sv[j].x) >= th ? 1u << (4 * j) : 0u;
+            pm |= __uint_as_float(sv[j].y) >= th ? 2u << (4 * j) : 0u;
+            pm |= __uint_as_float(sv[j].z) >= th ? 4u << (4 * j) : 0u;
+            pm |= __uint_as_float(sv[j].w) >= th ? 8u << (4 * j) : 0u;
           }
-          if (!__ballot_sync(0xffffffffu, pm != 0u)) continue;
-          uint32_t hk[4] = {0u, 0u, 0u, 0u};
-          unsigned tm = 0u;
+          const int lim = end - i;   // entries of this lane inside the segment
+          pm &= lim >= 16 ? 0xFFFFu : (lim > 0 ? (1u << lim) - 1u : 0u);
+          if (__ballot_sync(0xffffffffu, pm != 0u)) {
+            const int c = __popc(pm);   // 0..16: five bit slices
+            int p = c1, tot = 0;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (pm & (1u << e)) {
-              hk[e] = tc_hi(sb[e], k4[e], G);
-              tm |= hk[e] >= tau ? 1u << e : 0u;
+            for (int bit = 0; bit < 5; ++bit) {
+              const unsigned sl = __ballot_sync(0xffffffffu, (c >> bit) & 1);
+              p += __popc(sl & lt) << bit;
+              tot += __popc(sl) << bit;
             }
-          }
-          if (__ballot_sync(0xffffffffu, tm != 0u)) {   // lo <= hi: only taken entries count
-            const int c = __popc(tm);
-            const unsigned c0 = __ballot_sync(0xffffffffu, c & 1);
-            const unsigned c1 = __ballot_sync(0xffffffffu, c & 2);
-            const unsigned c2 = __ballot_sync(0xffffffffu, c & 4);
-            int p = cnt + __popc(c0 & lt) + 2 * __popc(c1 & lt) + 4 * __popc(c2 & lt);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (tm & (1u << e)) {
-                const uint32_t lk = tc_lo(sb[e], k4[e], G);
-                nlo += lk >= tau ? 1 : 0;
-                if (p < kWarpBuf) {
-                  b_i[p] = (uint32_t)(i + e);
-                  b_lo[p] = lk;
-                  b_hi[p] = hk[e];
-                }
-                ++p;
-              }
+            while (pm) {
+              const int e = __ffs(pm) - 1;
+              pm &= pm - 1u;
+              if (p < kWarpBuf) b_i[p] = (uint32_t)(i + e);
+              ++p;
             }
-            cnt += __popc(c0) + 2 * __popc(c1) + 4 * __popc(c2);
+            c1 += tot;
           }
-        }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          sv[u] = sn[u];
-          kv[u] = kx[u];
+          for (int j = 0; j < 4; ++j) sv[j] = sn[j];
+          kc = kx;
         }
+      }
+      __syncwarp();
+      int cnt = 0, nlo = 0;
+      if (c1 > kWarpBuf) {
+        cnt = c1;   // the list overflowed: the slow path below
+      } else {
+        constexpr int P = kWarpBuf / 32;
+        uint32_t ii[P], sb[P];
+        float kk[P];
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+          const int p = 32 * j + lane;
+          const uint32_t e = p < c1 ? b_i[p] : 0u;
+          sb[j] = p < c1 ? s0[e] : kMinusInfBits;
+          kk[j] = p < c1 ? kn[e] : 0.0f;
+          ii[j] = p < c1 ? (uint32_t)ui[e] : 0u;   // the entry's block id
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < P; ++j) {
+          if (32 * j >= c1) break;
+          const bool valid = 32 * j + lane < c1;
+          const uint32_t hk = valid ? tc_hi(sb[j], kk[j], G) : 0u;
+          const bool take = valid && hk >= tau;
+          const unsigned bal = __ballot_sync(0xffffffffu, take);
+          if (take) {
+            const uint32_t lk = tc_lo(sb[j], kk[j], G);
+            const int w = cnt + __popc(bal & lt);
+            b_i[w] = ii[j];
+            b_lo[w] = lk;
+            b_hi[w] = hk;
+            nlo += lk >= tau ? 1 : 0;
+          }
+          cnt += __popc(bal);
+        }
+        // the largest lower bound collected
+        __syncwarp();
+        uint32_t ml = 0u;
+        for (int p = lane; p < cnt; p += 32) ml = max(ml, b_lo[p]);
+        ml = __reduce_max_sync(0xffffffffu, ml);
+        if (lane == 0 && ml) atomicMax(&s_maxlo, ml);
       }
       nlo = __reduce_add_sync(0xffffffffu, nlo);
       if (lane == 0) { s_cnt[warp] = cnt; s_lo[warp] = nlo; }
@@ -1382,16 +1513,22 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       const bool fast = !over && total <= kCollectCap && lo_total >= K;
       if (fast)
         for (int p = lane; p < cnt; p += 32) {
-          col_i[off + p] = ui[b_i[p]];   // the entry's block id
+          col_i[off + p] = b_i[p];   // the entry's block id
           col_lo[off + p] = b_lo[p];
           col_hi[off + p] = b_hi[p];
         }
       __syncthreads();
       // ---- 3./4. over the collection: T, the candidates and the certain ones
       if (fast) {
+        // At least K lower bounds reach tau, so T >= tau, and every lower bound at or
+        // above tau shares the leading bytes of tau and of the largest lower bound: those
+        // digits are given.
+        const uint32_t dx = tau ^ s_maxlo;
+        const int start = min(3, dx == 0u ? 4 : __clz((int)dx) >> 3);
         int need;
-        const uint32_t T = radix_threshold(total, K, [&](int j) { return col_lo[j]; }, hist,
-                                           scratch, r_key, s_misc, a.status, &need);
+        const uint32_t T = radix_threshold(
+            total, K, [&](int j) { return col_lo[j]; }, hist, scratch, r_key, s_misc, a.status,
+            &need, 4, start, start > 0 ? tau >> (32 - 8 * start) : 0u);
         // H = T + max over the candidates of (upper - lower), rounded upward, is at least
         // the (K+1)-th largest upper bound of the row (the K+1 largest upper bounds each
         // exceed their lower bound by at most that much, and at most K lower bounds reach
@@ -1441,18 +1578,18 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
           s_eq, s_gt);
     }
     __syncthreads();
-    stage_queries();
     if (m <= kCandCap) {
       if (cand_entries)
         for (int j = tid; j < m; j += blockDim.x) cand[j] = ui[cand[j]];
       __syncthreads();
       // ---- 4. canonical scores of the uncertain candidates. Their positions are listed
-      // (over the residual keys); rounds of 128 stage their keys in shared memory (rows of
-      // 272 bytes, over the collection), and four threads take a candidate: thread t runs
+      // (over the residual keys); rounds of 96 stage their keys in shared memory (two
+      // alternating buffers over the collection), and four threads take a candidate: thread t runs
       // the chains of heads t, t + 4, t + 8, t + 12 over i ascending (a fused multiply-add
       // per step), and the first of the four sums the heads' ReLU terms in head order.
+      int32_t* const ulist = reinterpret_cast<int32_t*>(r_key);
+      int mu = 0;
       {
-        int32_t* const ulist = reinterpret_cast<int32_t*>(r_key);
         if (tid == 0) s_misc[0] = 0;
         __syncthreads();
         for (int j0 = 0; j0 < m; j0 += blockDim.x) {
@@ -1462,30 +1599,66 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
           int wb = 0;
           if (lane == 0 && bal) wb = atomicAdd(&s_misc[0], __popc(bal));
           wb = __shfl_sync(0xffffffffu, wb, 0);
-          if (u) ulist[wb + __popc(bal & ((1u << lane) - 1u))] = j;
+          if (u) {
+            ulist[wb + __popc(bal & ((1u << lane) - 1u))] = j;
+            // its key to L2 now: the rounds below copy it from there
+            const uint8_t* kp = reinterpret_cast<const uint8_t*>(kbase) + (size_t)cand[j] * 256;
+            asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(kp));
+            asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(kp + 128));
+          }
         }
+        stage_queries();
         __syncthreads();
-        const int mu = s_misc[0];
+        mu = s_misc[0];
         uint8_t* const stg = reinterpret_cast<uint8_t*>(col_i);
         const uint32_t stg_addr = static_cast<uint32_t>(__cvta_generic_to_shared(stg));
         const uint8_t* kb8 = reinterpret_cast<const uint8_t*>(kbase);
         const int sub = tid & 3, slot = tid >> 2;
-        for (int u0 = 0; u0 < mu; u0 += kRescoreRound) {
-          const int nr = min(kRescoreRound, mu - u0);
+        const int rounds = (mu + kRescoreRound - 1) / kRescoreRound;
+        // round r's keys go to buffer r & 1 (rows of 256 bytes, 16-byte granule c of row
+        // j at c ^ (j & 15)); the next round's copies are in flight while this one is
+        // scored
+        auto stage = [&](int r) {
+          const int u0 = r * kRescoreRound, nr = min(kRescoreRound, mu - u0);
+          const uint32_t dst = stg_addr + (uint32_t)((r & 1) * kRescoreBuf);
           for (int t = tid; t < nr * 16; t += blockDim.x) {
-            const int r = t >> 4, c = t & 15;
-            cp_async16(stg_addr + (uint32_t)(r * kRescorePitch + c * 16),
-                       kb8 + (size_t)cand[ulist[u0 + r]] * 256 + c * 16, true);
+            const int j = t >> 4, c = t & 15;
+            cp_async16(dst + (uint32_t)(j * 256 + ((c ^ (j & 15)) << 4)),
+                       kb8 + (size_t)cand[ulist[u0 + j]] * 256 + c * 16, true);
           }
           cp_async_commit();
-          cp_async_wait<0>();
-          __syncthreads();
+        };
+        if (rounds > 0) stage(0);
+        for (int r = 0; r < rounds; ++r) {
+          if (r + 1 < rounds) stage(r + 1);
+          else cp_async_commit();   // an empty group: the wait below keeps one group open
+          cp_async_wait<1>();
+          __syncthreads();          // round r's keys are in shared memory
+          const int u0 = r * kRescoreRound, nr = min(kRescoreRound, mu - u0);
+          const uint8_t* kr = stg + (r & 1) * kRescoreBuf + slot * 256;
+          const int sw = slot & 15;
           float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          if (slot < nr) {
-            const uint8_t* kr = stg + slot * kRescorePitch;
+          if (slot < nr && a.Hh <= 8) {
+            // heads t + 8, t + 12 are absent: two chains per thread on bf16 operands
+            const uint32_t* qt = qb + sub * 4;
 #pragma unroll 2
             for (int c = 0; c < 16; ++c) {
-              const uint4 kv = *reinterpret_cast<const uint4*>(kr + c * 16);
+              const uint4 kv = *reinterpret_cast<const uint4*>(kr + ((c ^ sw) << 4));
+              const uint4 q0 = *reinterpret_cast<const uint4*>(qt + (2 * c) * 16);
+              const uint4 q1 = *reinterpret_cast<const uint4*>(qt + (2 * c + 1) * 16);
+              fma_pair_bf16<false>(d[0], d[1], q0.x, kv.x);
+              fma_pair_bf16<true>(d[0], d[1], q0.y, kv.x);
+              fma_pair_bf16<false>(d[0], d[1], q0.z, kv.y);
+              fma_pair_bf16<true>(d[0], d[1], q0.w, kv.y);
+              fma_pair_bf16<false>(d[0], d[1], q1.x, kv.z);
+              fma_pair_bf16<true>(d[0], d[1], q1.y, kv.z);
+              fma_pair_bf16<false>(d[0], d[1], q1.z, kv.w);
+              fma_pair_bf16<true>(d[0], d[1], q1.w, kv.w);
+            }
+          } else if (slot < nr) {
+#pragma unroll 2
+            for (int c = 0; c < 16; ++c) {
+              const uint4 kv = *reinterpret_cast<const uint4*>(kr + ((c ^ sw) << 4));
               const float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
                                    bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
 #pragma unroll
@@ -1512,17 +1685,51 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
               if (h < a.Hh) sc = __fmaf_rn(wf[h], dh[h] > 0.0f ? dh[h] : 0.0f, sc);
             ckey[ulist[u0 + slot]] = score_key(sc);
           }
-          __syncthreads();   // the staging is free for the next round
+          __syncthreads();   // buffer r & 1 is free for round r + 2
         }
+        cp_async_wait<0>();
       }
-      // ---- 5. the exact select among the candidates
-      int need;
-      const uint32_t T = radix_threshold(
-          m, K, [&](int j) { return ckey[j]; }, hist, scratch, r_key, s_misc, a.status, &need);
-      const int taken = ordered_take(
-          m, need,
-          [&](int j) { const uint32_t k = ckey[j]; return k > T ? 2 : (k == T ? 1 : 0); },
-          [&](int p, int j) { if (p < K) out[p] = cand[j]; }, s_eq, s_gt);
+      // ---- 5. the exact select among the candidates: the first K by (key desc,
+      // position asc). The certain ones all belong to it. When at most one uncertain
+      // candidate per thread remains (none with the certain key), the uncertain ones are
+      // sorted by (key desc, position asc) and the first K - (m - mu) take the certain
+      // key; otherwise a radix threshold over all candidates.
+      const int need_u = K - (m - mu);
+      if (tid == 0) s_misc[1] = 0;
+      __syncthreads();
+      uint32_t myk = 0u;
+      int myj = -1;
+      if (tid < mu && mu <= kTopkThreads) {
+        myj = ulist[tid];
+        myk = ckey[myj];
+        if (myk == kCertainKey) s_misc[1] = 1;
+      }
+      __syncthreads();
+      const bool direct = mu <= kTopkThreads && need_u >= 0 && need_u <= mu && !s_misc[1];
+      int taken;
+      if (direct) {
+        if (mu > 0) {
+          int P = 2;
+          while (P < mu) P <<= 1;
+          // (key, complement of the position): descending order is (key desc, position
+          // asc); padding (0) sorts after every candidate
+          const uint64_t v = tid < mu ? ((uint64_t)myk << 32) | (uint32_t)~(uint32_t)myj : 0ull;
+          const uint64_t r = block_sort_desc(v, P, reinterpret_cast<uint64_t*>(col_lo));
+          if (tid < mu) ckey[(int)~(uint32_t)r] = tid < need_u ? kCertainKey : 0u;
+          __syncthreads();
+        }
+        taken = ordered_take(
+            m, 0, [&](int j) { return ckey[j] == kCertainKey ? 2 : 0; },
+            [&](int p, int j) { if (p < K) out[p] = cand[j]; }, s_eq, s_gt);
+      } else {
+        int need;
+        const uint32_t T = radix_threshold(
+            m, K, [&](int j) { return ckey[j]; }, hist, scratch, r_key, s_misc, a.status, &need);
+        taken = ordered_take(
+            m, need,
+            [&](int j) { const uint32_t k = ckey[j]; return k > T ? 2 : (k == T ? 1 : 0); },
+            [&](int p, int j) { if (p < K) out[p] = cand[j]; }, s_eq, s_gt);
+      }
       if (tid == 0) {
         a.nsel[lr] = K;
         if (taken != K) flag_status(a.status, kStatusCheck);
@@ -1530,6 +1737,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       return;
     }
     // Too many candidates (e.g. heavy ties): canonical scores for the whole row.
+    stage_queries();
     __syncthreads();
     for (int i = tid; i < n; i += blockDim.x) {
       const bool adm = s0[i] != kMinusInfBits;
@@ -1595,6 +1803,7 @@ SelLayout sel_layout(const SelDims& d, bool caller_cidx) {
   L.urows = off; off += up((size_t)d.L * d.N);
   L.cscore = off; off += up(sizeof(float) * LR * (size_t)score_stride(d.N));
   L.knorm = off; off += up(sizeof(float) * (size_t)d.L * score_stride(d.N));
+  L.kmax = off; off += up(sizeof(float) * (size_t)d.L * chunk_stride(d.N));
   L.qnorm = off; off += up(sizeof(float) * LR);
   L.total = off;
   return L;
@@ -1621,8 +1830,9 @@ cudaError_t launch_score(const SelDims& d, const uint16_t* keys, const uint16_t*
                          const SelWorkspace& ws, bool tc, cudaStream_t s) {
   ScoreArgs a{d.L, d.R, d.Hh, d.N, d.key_stride, keys, q, head_w, mask, limit, ws.uidx,
               ws.ucount, ws.urows, ws.wordoff, reinterpret_cast<uint32_t*>(ws.cscore), ws.knorm,
-              ws.qnorm, ws.header};
+              ws.qnorm, ws.kmax, ws.header};
   a.NS = score_stride(d.N);
+  a.NC = chunk_stride(d.N);
   if (!tc) {
     const int RH = d.R * d.Hh;
     const size_t smem = sizeof(float) * ((size_t)RH * 128 + ((RH + 3) & ~3)) +
@@ -1662,9 +1872,10 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
                         const float* head_w, int32_t* sel, int32_t* nsel,
                         const SelWorkspace& ws, bool tc, cudaStream_t s) {
   TopkArgs a{d.R, d.Hh, d.N, d.topk, d.key_stride, keys, q, head_w, ws.cidx, ws.ccount,
-             ws.uidx, ws.ucount, reinterpret_cast<uint32_t*>(ws.cscore), ws.knorm, ws.qnorm, sel,
-             nsel, ws.header, tc ? 1 : 0};
+             ws.uidx, ws.ucount, reinterpret_cast<uint32_t*>(ws.cscore), ws.knorm, ws.qnorm,
+             ws.kmax, sel, nsel, ws.header, tc ? 1 : 0};
   a.NS = score_stride(d.N);
+  a.NC = chunk_stride(d.N);
   cudaError_t err =
       cudaFuncSetAttribute(k7_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
   if (err != cudaSuccess) return err;
