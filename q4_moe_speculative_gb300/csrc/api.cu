@@ -219,6 +219,7 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
   char* base = static_cast<char*>(workspace);
   SelWorkspace ws{};
   ws.header = reinterpret_cast<uint32_t*>(base + L.header);
+  ws.uagg = reinterpret_cast<uint32_t*>(base + L.uagg);
   ws.wordoff = reinterpret_cast<int32_t*>(base + L.wordoff);
   ws.cidx = caller ? cidx : reinterpret_cast<int32_t*>(base + L.cidx);
   ws.ccount = caller ? ccount : reinterpret_cast<int32_t*>(base + L.ccount);
@@ -233,7 +234,7 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
                   tc_scoring_supported(d, a->keys, a->q);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(base, 0, 256, s) != cudaSuccess) return DS_ERR_CUDA;
+  if (cudaMemsetAsync(base, 0, L.zero_bytes, s) != cudaSuccess) return DS_ERR_CUDA;
   if (launch_compact(d, a->mask, a->limit, ws, caller, s) != cudaSuccess) return DS_ERR_CUDA;
   if (!mark(marks, 0, s)) return DS_ERR_CUDA;
   if (launch_score(d, a->keys, a->q, a->head_w, a->mask, a->limit, ws, tc, s) != cudaSuccess)

@@ -70,6 +70,8 @@ struct SelDims {
 
 struct SelWorkspace {
   uint32_t* header;
+  uint32_t* uagg;     // [L][P] union count of each chunk of kCompactChunk mask words, with
+                      // bit 31 set once published (zeroed with the header by every call)
   int32_t* wordoff;   // [L][W] exclusive prefix of union-admitted counts per mask word
   int32_t* cidx;      // [L][R][N] (caller's array or workspace)
   int32_t* ccount;    // [L][R]
@@ -91,8 +93,8 @@ inline int score_stride(int N) { return (N + 3) & ~3; }
 inline int chunk_stride(int N) { return (score_stride(N) + 31) / 32; }
 
 struct SelLayout {
-  size_t header, wordoff, cidx, ccount, uidx, ucount, urows, cscore, knorm, kmax, qnorm,
-      total;
+  size_t header, uagg, zero_bytes, wordoff, cidx, ccount, uidx, ucount, urows, cscore, knorm,
+      kmax, qnorm, total;
 };
 SelLayout sel_layout(const SelDims& d, bool caller_cidx);
 bool tc_scoring_supported(const SelDims& d, const uint16_t* keys, const uint16_t* q);

@@ -212,6 +212,12 @@ __device__ __forceinline__ float canonical_score(const float* q, const uint16_t*
 // counts first and scatters only when its compacted index is wanted: when the caller
 // asked for it, or when the row admits at most top_k blocks (the top-k then copies it).
 // ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 struct CompactArgs {
   int L, R, N;
   const uint32_t* mask;
@@ -222,6 +228,8 @@ struct CompactArgs {
   int32_t* ucount;     // [L]
   uint8_t* urows;      // [L][N]
   int32_t* uwordoff;   // [L][W]
+  uint32_t* uagg;      // [L][P] published union counts of the chunks
+  uint32_t* status;
   int topk;
   int want_cidx;       // the caller passed cidx / ccount
 };
@@ -229,7 +237,7 @@ struct CompactArgs {
 __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) {
   __shared__ int scratch[33];
   __shared__ int s_off[kCompactThreads];
-  __shared__ int s_lim[8];
+  __shared__ int s_base;
   const int R = a.R, N = a.N;
   const int W = (N + 31) >> 5;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -242,12 +250,19 @@ __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) 
   const int l = union_cta ? uc / P : lr / R;
   const int uchunk = union_cta ? uc - l * P : 0;
   const uint32_t* mrow = a.mask + (size_t)(union_cta ? l * R : lr) * W;
-  if (tid < R) {
-    const int lim = a.limit[(size_t)l * R + tid];
-    s_lim[tid] = lim < 0 ? 0 : (lim > N ? N : lim);
+  // the rows' causal limits, read by every thread (no barrier before the mask loads); a
+  // word's bits at or past the limit are cleared after it is loaded
+  int lims[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int lim = r < R ? __ldg(a.limit + (size_t)l * R + r) : 0;
+    lims[r] = lim < 0 ? 0 : (lim > N ? N : lim);
   }
-  __syncthreads();
-  const int lim_row = union_cta ? 0 : s_lim[lr - l * R];
+  const int lim_row = union_cta ? 0 : min(max(__ldg(a.limit + lr), 0), N);
+  auto limited = [](uint32_t w, int wi, int lim) {
+    const int rem = lim - wi * 32;
+    return rem >= 32 ? w : (rem > 0 ? w & ((1u << rem) - 1u) : 0u);
+  };
 
   if (!union_cta && !a.want_cidx) {
     int c = 0;
@@ -262,20 +277,9 @@ __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) 
 
   int base = 0;
   int c_first = 0, c_last = W;
-  if (union_cta) {
-    // this CTA's chunk, and the union entries of the words before it
+  if (union_cta) {   // this CTA's chunk (one pass of the loop below)
     c_first = uchunk * kCompactThreads;
     c_last = min(W, c_first + kCompactThreads);
-    int c = 0;
-#pragma unroll 2
-    for (int wi = tid; wi < c_first; wi += kCompactThreads) {
-      uint32_t mw = 0;
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-        if (r < R) mw |= admitted_word(a.mask + ((size_t)l * R + r) * W, wi, s_lim[r]);
-      c += __popc(mw);
-    }
-    block_excl_scan(c, scratch, &base);
   }
   for (int c0 = c_first; c0 < c_last; c0 += kCompactThreads) {
     // word wi = c0 + tid of each row read (per row for the union): its admitted bits
@@ -287,7 +291,9 @@ __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) 
       if (union_cta) {
 #pragma unroll
         for (int r = 0; r < 8; ++r)
-          if (r < R) mine[r] = admitted_word(a.mask + ((size_t)l * R + r) * W, wi, s_lim[r]);
+          if (r < R) mine[r] = __ldg(a.mask + ((size_t)l * R + r) * W + wi);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) mine[r] = limited(mine[r], wi, lims[r]);
       } else {
         mine[0] = admitted_word(mrow, wi, lim_row);
       }
@@ -302,7 +308,34 @@ __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) 
     for (int r = 1; r < 8; ++r)
       if (r < R) same = same && mine[r] == mine[0];
     int total;
-    const int excl = base + block_excl_scan(__popc(mw), scratch, &total);
+    const int lexcl = block_excl_scan(__popc(mw), scratch, &total);
+    if (union_cta) {
+      // publish this chunk's count, then add up those of the chunks before it in the
+      // layer: lower block indices, started earlier, and none of them waits on this one
+      uint32_t* agg = a.uagg + (size_t)l * P;
+      if (tid == 0) {
+        __threadfence();
+        atomicExch(agg + uchunk, 0x80000000u | (uint32_t)total);
+      }
+      if (warp == 0) {
+        int v = 0;
+        for (int j = lane; j < uchunk; j += 32) {
+          uint32_t x = 0;
+          for (uint32_t it = 0; it < (1u << 22); ++it) {
+            x = ld_acquire_u32(agg + j);
+            if (x & 0x80000000u) break;
+            __nanosleep(64);
+          }
+          if (!(x & 0x80000000u)) flag_status(a.status, kStatusTimeout);
+          v += (int)(x & 0x7FFFFFFFu);
+        }
+        v = __reduce_add_sync(0xffffffffu, v);
+        if (lane == 0) s_base = v;
+      }
+      __syncthreads();
+      base = s_base;
+    }
+    const int excl = base + lexcl;
     s_off[tid] = excl;
     if (union_cta && wi < W) a.uwordoff[(size_t)l * W + wi] = excl;
     __syncthreads();
@@ -311,7 +344,12 @@ __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) 
     {
       const int wbase = c0 + warp * 32;
       const uint32_t all_rows = (1u << R) - 1u;
-      for (int jw = 0; jw < 32 && wbase + jw < W; ++jw) {
+      const int nw = min(32, W - wbase);
+      int32_t* const uo = a.uidx + (size_t)l * N;
+      uint8_t* const ro = a.urows + (size_t)l * N;
+      int32_t* const co = union_cta ? nullptr : a.cidx + (size_t)lr * N;
+#pragma unroll 4
+      for (int jw = 0; jw < nw; ++jw) {
         const int w = wbase + jw;
         const int b = w * 32 + lane;
         const uint32_t wv = __shfl_sync(0xffffffffu, mw, jw);
@@ -329,10 +367,10 @@ __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) 
         if (pred) {
           const int off = s_off[warp * 32 + jw] + __popc(wv & ((1u << lane) - 1u));
           if (union_cta) {
-            a.uidx[(size_t)l * N + off] = b;
-            a.urows[(size_t)l * N + off] = (uint8_t)rows;
+            uo[off] = b;
+            ro[off] = (uint8_t)rows;
           } else {
-            a.cidx[(size_t)lr * N + off] = b;
+            co[off] = b;
           }
         }
       }
@@ -1791,6 +1829,8 @@ SelLayout sel_layout(const SelDims& d, bool caller_cidx) {
   SelLayout L{};
   size_t off = 0;
   L.header = off; off += 256;
+  L.uagg = off; off += up(sizeof(uint32_t) * (size_t)d.L * ((W + kCompactThreads - 1) / kCompactThreads));
+  L.zero_bytes = off;
   L.wordoff = off; off += up(sizeof(int32_t) * (size_t)d.L * W);
   if (!caller_cidx) {
     L.cidx = off; off += up(sizeof(int32_t) * LR * (size_t)d.N);
@@ -1818,7 +1858,7 @@ bool tc_scoring_supported(const SelDims& d, const uint16_t* keys, const uint16_t
 cudaError_t launch_compact(const SelDims& d, const uint32_t* mask, const int32_t* limit,
                            const SelWorkspace& ws, bool want_cidx, cudaStream_t s) {
   CompactArgs a{d.L, d.R, d.N, mask, limit, ws.cidx, ws.ccount, ws.uidx, ws.ucount, ws.urows,
-                ws.wordoff, d.topk, want_cidx ? 1 : 0};
+                ws.wordoff, ws.uagg, ws.header, d.topk, want_cidx ? 1 : 0};
   const int W = (d.N + 31) / 32;
   const int P = (W + kCompactThreads - 1) / kCompactThreads;
   k6_compact<<<d.L * d.R + d.L * P, kCompactThreads, 0, s>>>(a);
