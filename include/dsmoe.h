@@ -173,8 +173,10 @@ ds_status ds_moe_verify_forward_marked(const ds_moe_layer* layer, const uint16_t
 /* Byte offset, inside a workspace sized by ds_moe_workspace_size(layer, R), of the bf16
  * array h [R][1 + k][I] that ds_moe_verify_forward leaves there (slot 0 = shared expert,
  * slot j + 1 = the row's rank-j expert): the rounded SwiGLU activations, kept for
- * inspection. Valid once the call has completed on its stream and until the workspace is
- * reused. Returns (size_t)-1 when the layer or R is invalid. */
+ * inspection. Within each group of 8 consecutive values the order is the tensor-core
+ * operand order v0, v4, v1, v5, v2, v6, v3, v7. Valid once the call has completed on its
+ * stream and until the workspace is reused. Returns (size_t)-1 when the layer or R is
+ * invalid. */
 size_t ds_moe_workspace_h_offset(const ds_moe_layer* layer, int32_t R);
 
 /* Bytes of the scratch array that ds_moe_verify_forward_noalloc uses, one per device,
@@ -243,13 +245,17 @@ typedef struct {
   const float* head_w;   /* fp32 [L][R][Hh]        */
   const uint32_t* mask;  /* uint32 [L][R][ceil(N/32)] */
   const int32_t* limit;  /* int32 [L][R]           */
-  int32_t flags;         /* 0, or DS_SELECT_CANONICAL_SCORES                        */
+  int32_t flags;         /* 0, or DS_SELECT_CANONICAL_SCORES | DS_SELECT_KEEP_WORKSPACE */
 } ds_select_args;
 
 /* ds_select_args.flags: compute every admitted block's score in the canonical order on
  * CUDA cores instead of the default tensor-core scoring with exact re-scoring of the
  * candidates near the threshold. Both give the same selection; the default is faster. */
 #define DS_SELECT_CANONICAL_SCORES 1
+/* ds_select_args.flags: leave the scores, key norms and union lists in the workspace for
+ * inspection (below). Without it the top-k drops them from L2 once it has read them (no
+ * write-back to memory), and their workspace bytes are undefined after the call. */
+#define DS_SELECT_KEEP_WORKSPACE 2
 
 /* Bytes of workspace ds_select_blocks needs, or 0 when the arguments are invalid. */
 size_t ds_select_workspace_size(const ds_select_args* args);
@@ -275,9 +281,9 @@ ds_status ds_select_blocks_marked(const ds_select_args* args, int32_t* sel, int3
                                   size_t ws_bytes, ds_stream_t stream,
                                   const ds_event_t marks[3]);
 
-/* Parts of a select workspace that a completed tensor-core-mode call (flags 0) leaves for
- * inspection, at the byte offsets ds_select_workspace_offset returns (NS = N rounded up
- * to a multiple of 4):
+/* Parts of a select workspace that a completed tensor-core-mode call with
+ * DS_SELECT_KEEP_WORKSPACE leaves for inspection, at the byte offsets
+ * ds_select_workspace_offset returns (NS = N rounded up to a multiple of 32):
  *   DS_SELECT_WS_UNION       int32 [L][N]: per layer, the blocks some row admits, ascending
  *                            (the first count entries are valid);
  *   DS_SELECT_WS_UNION_COUNT int32 [L]: that count;

@@ -223,11 +223,12 @@ def moe_verify_forward_noalloc(layer: MoeLayer, x: torch.Tensor, y: torch.Tensor
 
 
 def _select_struct(keys, q, head_w, mask, limit, top_k, key_layer_stride=None,
-                   canonical: bool = False) -> N.DsSelectArgs:
+                   canonical: bool = False, keep_workspace: bool = False) -> N.DsSelectArgs:
     L, Nb, D = keys.shape
     _, R, Hh, _ = q.shape
     stride = keys.stride(0) if key_layer_stride is None else key_layer_stride
-    flags = N.DS_SELECT_CANONICAL_SCORES if canonical else 0
+    flags = (N.DS_SELECT_CANONICAL_SCORES if canonical else 0) | \
+        (N.DS_SELECT_KEEP_WORKSPACE if keep_workspace else 0)
     return N.DsSelectArgs(L, R, Hh, D, Nb, top_k, _ptr(keys), stride, _ptr(q), _ptr(head_w),
                           _ptr(mask), _ptr(limit), flags)
 
@@ -238,12 +239,14 @@ def select_workspace_size(keys, q, head_w, mask, limit, top_k: int) -> int:
 
 def select_blocks(keys, q, head_w, mask, limit, top_k: int = 512, *, sel=None, nsel=None,
                   cidx=None, ccount=None, want_compacted: bool = False, workspace=None,
-                  stream=None, validate: bool = True, canonical: bool = False):
+                  stream=None, validate: bool = True, canonical: bool = False,
+                  keep_workspace: bool = False):
     """Block selection for L layers x R rows.
     keys bf16 [L,N,128]; q bf16 [L,R,Hh,128]; head_w fp32 [L,R,Hh]; mask int32 [L,R,ceil(N/32)]
     (bit patterns); limit int32 [L,R]. Returns (sel [L,R,top_k], nsel [L,R], cidx, ccount),
     the last two None unless want_compacted or passed in. canonical=True scores every admitted
-    block in the canonical order on CUDA cores (same selection, slower)."""
+    block in the canonical order on CUDA cores (same selection, slower); keep_workspace=True
+    leaves the scores, key norms and union lists in `workspace` for select_workspace_views."""
     lib = N.load()
     L, Nb, D = keys.shape
     R, Hh = q.shape[1], q.shape[2]
@@ -260,7 +263,8 @@ def select_blocks(keys, q, head_w, mask, limit, top_k: int = 512, *, sel=None, n
     if want_compacted and cidx is None:
         cidx = torch.empty((L, R, Nb), dtype=torch.int32, device=dev)
         ccount = torch.empty((L, R), dtype=torch.int32, device=dev)
-    args = _select_struct(keys, q, head_w, mask, limit, top_k, canonical=canonical)
+    args = _select_struct(keys, q, head_w, mask, limit, top_k, canonical=canonical,
+                          keep_workspace=keep_workspace)
     if workspace is None:
         workspace = torch.empty(int(lib.ds_select_workspace_size(args)), dtype=torch.uint8, device=dev)
     status = lib.ds_select_blocks(args, _ptr(sel), _ptr(nsel), _ptr(cidx), _ptr(ccount),
@@ -271,13 +275,14 @@ def select_blocks(keys, q, head_w, mask, limit, top_k: int = 512, *, sel=None, n
 
 def select_workspace_views(keys, q, head_w, mask, limit, top_k: int, workspace: torch.Tensor,
                            with_compacted: bool = False) -> dict:
-    """Views of what a completed tensor-core-mode select call left in `workspace`
+    """Views of what a completed tensor-core-mode select call with keep_workspace=True left
+    in `workspace`
     (include/dsmoe.h): union [L,N] int32 and union_count [L]; scores [L,R,NS] fp32 by union
     entry (-inf where the row does not admit it); key_norms [L,NS]; row_scales [L,R]."""
     lib = N.load()
     L, Nb, _ = keys.shape
     R = q.shape[1]
-    NS = (Nb + 3) & ~3
+    NS = (Nb + 31) & ~31
     args = _select_struct(keys, q, head_w, mask, limit, top_k)
     shapes = {"union": ((L, Nb), torch.int32), "union_count": ((L,), torch.int32),
               "scores": ((L, R, NS), torch.float32), "key_norms": ((L, NS), torch.float32),
@@ -293,12 +298,20 @@ def select_workspace_views(keys, q, head_w, mask, limit, top_k: int, workspace: 
     return out
 
 
+# position of value v (0..7) of a group of 8 in the workspace's h: v0, v4, v1, v5, ...
+_H_PAIR_POS = (0, 2, 4, 6, 1, 3, 5, 7)
+
+
 def moe_workspace_h(layer: MoeLayer, R: int, workspace: torch.Tensor) -> torch.Tensor:
-    """View of the bf16 SwiGLU activations h [R, 1+k, I] that the last call left in
-    `workspace` (slot 0 = shared expert, slot j+1 = the row's rank-j expert)."""
+    """The bf16 SwiGLU activations h [R, 1+k, I] that the last call left in `workspace`
+    (slot 0 = shared expert, slot j+1 = the row's rank-j expert), in natural order (the
+    workspace keeps each group of 8 values in tensor-core operand order)."""
     off = int(N.load().ds_moe_workspace_h_offset(layer.struct(), R))
     n = R * (1 + layer.top_k) * layer.inter
-    return workspace[off: off + 2 * n].view(torch.bfloat16).view(R, 1 + layer.top_k, layer.inter)
+    h = workspace[off: off + 2 * n].view(torch.bfloat16).view(R, 1 + layer.top_k, layer.inter)
+    pos = torch.tensor(_H_PAIR_POS, device=h.device)
+    idx = (torch.arange(layer.inter, device=h.device) & ~7) + pos[torch.arange(layer.inter, device=h.device) & 7]
+    return h[..., idx]
 
 
 def _verify_common(logits, draft, out, n_out, workspace):

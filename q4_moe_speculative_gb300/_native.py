@@ -29,6 +29,7 @@ EXPORTS = (
 SELECT_WS_PARTS = {"union": 0, "union_count": 1, "scores": 2, "key_norms": 3, "row_scales": 4}
 
 DS_SELECT_CANONICAL_SCORES = 1
+DS_SELECT_KEEP_WORKSPACE = 2
 DS_NOALLOC_SCRATCH_BYTES = 4 << 20  # same value as the C header's macro
 
 

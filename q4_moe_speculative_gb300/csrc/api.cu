@@ -84,7 +84,7 @@ ds_status check_select(const ds_select_args* a) {
   if (!a->keys || !aligned(a->keys, 16) || !a->q || !aligned(a->q, 4) || !a->head_w ||
       !a->mask || !a->limit)
     return DS_ERR_INVALID_ARG;
-  if (a->flags & ~DS_SELECT_CANONICAL_SCORES) return DS_ERR_INVALID_ARG;
+  if (a->flags & ~(DS_SELECT_CANONICAL_SCORES | DS_SELECT_KEEP_WORKSPACE)) return DS_ERR_INVALID_ARG;
   return DS_OK;
 }
 
@@ -220,6 +220,7 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
   SelWorkspace ws{};
   ws.header = reinterpret_cast<uint32_t*>(base + L.header);
   ws.uagg = reinterpret_cast<uint32_t*>(base + L.uagg);
+  ws.ldone = reinterpret_cast<uint32_t*>(base + L.ldone);
   ws.wordoff = reinterpret_cast<int32_t*>(base + L.wordoff);
   ws.cidx = caller ? cidx : reinterpret_cast<int32_t*>(base + L.cidx);
   ws.ccount = caller ? ccount : reinterpret_cast<int32_t*>(base + L.ccount);
@@ -240,7 +241,8 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
   if (launch_score(d, a->keys, a->q, a->head_w, a->mask, a->limit, ws, tc, s) != cudaSuccess)
     return DS_ERR_CUDA;
   if (!mark(marks, 1, s)) return DS_ERR_CUDA;
-  if (launch_topk(d, a->keys, a->q, a->head_w, sel, nsel, ws, tc, s) != cudaSuccess)
+  if (launch_topk(d, a->keys, a->q, a->head_w, sel, nsel, ws, tc,
+                  (a->flags & DS_SELECT_KEEP_WORKSPACE) != 0, s) != cudaSuccess)
     return DS_ERR_CUDA;
   if (!mark(marks, 2, s)) return DS_ERR_CUDA;
   return DS_OK;

@@ -70,6 +70,7 @@ struct SelDims {
 
 struct SelWorkspace {
   uint32_t* header;
+  uint32_t* ldone;    // [L] rows of the layer whose top-k is done (zeroed with the header)
   uint32_t* uagg;     // [L][P] union count of each chunk of kCompactChunk mask words, with
                       // bit 31 set once published (zeroed with the header by every call)
   int32_t* wordoff;   // [L][W] exclusive prefix of union-admitted counts per mask word
@@ -86,14 +87,14 @@ struct SelWorkspace {
   float* qnorm;       // [L][R] sum_h |w_h| ||q_h|| bound (tensor-core scoring)
 };
 
-// Row stride of the score arrays (cscore, knorm): N rounded up to a multiple of 4, so that
-// every row starts 16-byte aligned.
-inline int score_stride(int N) { return (N + 3) & ~3; }
+// Row stride of the score arrays (cscore, knorm): N rounded up to a multiple of 32, so that
+// every row starts on a 128-byte line (rows are dropped from L2 line by line once read).
+inline int score_stride(int N) { return (N + 31) & ~31; }
 // Row stride of kmax: one value per 32 union entries.
 inline int chunk_stride(int N) { return (score_stride(N) + 31) / 32; }
 
 struct SelLayout {
-  size_t header, uagg, zero_bytes, wordoff, cidx, ccount, uidx, ucount, urows, cscore, knorm,
+  size_t header, uagg, ldone, zero_bytes, wordoff, cidx, ccount, uidx, ucount, urows, cscore, knorm,
       kmax, qnorm, total;
 };
 SelLayout sel_layout(const SelDims& d, bool caller_cidx);
@@ -106,7 +107,7 @@ cudaError_t launch_score(const SelDims& d, const uint16_t* keys, const uint16_t*
                          const SelWorkspace& ws, bool tc, cudaStream_t s);
 cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* q,
                         const float* head_w, int32_t* sel, int32_t* nsel,
-                        const SelWorkspace& ws, bool tc, cudaStream_t s);
+                        const SelWorkspace& ws, bool tc, bool keep, cudaStream_t s);
 
 // TMA tensor map (cached by its parameters) of bf16 block keys [L][N][128] (layer stride
 // key_stride values, a multiple of 8) in boxes of 64 values x box_rows blocks, 128-byte

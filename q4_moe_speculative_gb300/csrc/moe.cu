@@ -70,18 +70,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-// 16-byte async copy global -> shared.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 // 1D bulk copy global -> shared of `bytes` (multiple of 16, both addresses 16-aligned),
 // completing `bytes` of the transaction count of `bar`.
 __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,
@@ -235,22 +223,27 @@ __global__ void __launch_bounds__(256) k0_clear(uint32_t* __restrict__ p, int nw
 //     experts with each one's rows and rank slots, in shared memory. Meanwhile the
 //     producer already streams the shared expert.
 //  2. Gate + up + SwiGLU. A unit is (expert slot u, tile row of I = 16 rows): slot 0 is
-//     the shared expert (all rows), slot u >= 1 the u-th expert of the union (its rows);
-//     CTA b takes units b, b + G, ... A stage is one K chunk of a unit: 32 tiles of the
-//     gate tile row and 32 of the up tile row, two bulk copies. Consumer warp w takes
-//     tiles 2w, 2w + 1 of each chunk for both matrices and keeps its partial sums across
-//     the unit's chunks; its activation fragments for those tiles sit in tensor memory
-//     (written once, read back with tcgen05.ld), which leaves shared memory to the ring.
-//     At the end of a unit the 16 warps' partials meet in shared memory; the reducer warps
-//     add them in warp order, write h = bf16_rne(silu(g) * u) and count the unit against
-//     its expert slot.
+//     the shared expert (all rows), slot u >= 1 the u-th expert of the union (its rows).
+//     A stage is one K chunk of a unit: 32 tiles of the gate tile row and 32 of the up
+//     tile row, two bulk copies. Consumer warp w takes tiles 2w, 2w + 1 of each chunk for
+//     both matrices and keeps its partial sums across the unit's chunks; its activation
+//     fragments for those tiles sit in tensor memory (written once, read back with
+//     tcgen05.ld), which leaves shared memory to the ring. At the end of a unit the 16
+//     warps' partials meet in shared memory; the reducer warps add them in warp order,
+//     write h = bf16_rne(silu(g) * u) (each group of 8 values in MMA pair order) and count
+//     the unit against its expert slot.
 //  3. Down projection. A unit is (expert slot u, row group of 16 tile rows = 256 rows of
 //     H); consumer warp w owns tile row w of the group for all of K (two accumulation
 //     chains, even and odd tiles), so no reduction with other warps follows. A stage is 4
 //     K tiles of the group's 16 tile rows, one contiguous bulk copy (the down matrices keep
-//     their tile rows in groups of 16). CTA b takes a contiguous range of units, so its h
-//     (the B operand, in shared memory) is reloaded only when the expert changes, once
-//     every gate/up unit of that expert is counted. Each warp writes o[row][slot] (fp32).
+//     their tile rows in groups of 16). The expert's h (the B operand) is brought into one
+//     of two shared buffers by the producer, with bulk copies, once every gate/up unit of
+//     the expert is counted. Each warp writes o[row][slot] (fp32).
+//  Units are handed out by one atomic counter in a fixed order: every gate/up unit (the
+//  shared expert's first), then every down unit, expert slot by expert slot. A CTA's
+//  producer takes its next unit when the ring has room and records it with each stage, so
+//  the CTAs stay busy until the last unit whatever their units' timing, and the gate/up
+//  units of an expert are long done when its down units come up.
 //  4. Combine. Once every CTA's down units are done (a count), CTA b writes y =
 //     bf16_rne(o_shared + sum_j w_j o_j), j in rank order, for its share of H.
 // ---------------------------------------------------------------------------------
@@ -274,8 +267,9 @@ constexpr int kRouterBatch = 4;                          // experts per CTA per 
 
 // Words of the workspace's zeroed area (the prologue clears it before every call): the
 // status word, the router arrival count, the count of CTAs whose down outputs are written,
-// and from word kHdrUnits on, per expert slot, the gate/up units whose h is written.
-enum : int { kHdrStatus = 0, kHdrArrivals = 1, kHdrDDone = 2, kHdrUnits = 64 };
+// the next unit to hand out, and from word kHdrUnits on, per expert slot, the gate/up units
+// whose h is written.
+enum : int { kHdrStatus = 0, kHdrArrivals = 1, kHdrDDone = 2, kHdrNext = 3, kHdrUnits = 64 };
 constexpr int kMoeZeroBytes = 4 * (kHdrUnits + 128);
 static_assert(kMaxUnion + 1 <= 128, "unit counts fit the zeroed area");
 
@@ -304,6 +298,19 @@ __device__ __forceinline__ void consumer_sync() {
 __device__ __forceinline__ void reducer_sync() {
   asm volatile("bar.sync %0, %1;" ::"n"(kReducerBarrier), "n"(32 * kReducerWarps) : "memory");
 }
+// The reducer barrier, returning whether `pred` held in every reducer thread.
+__device__ __forceinline__ bool reducer_all(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "n"(kReducerBarrier), "n"(32 * kReducerWarps)
+      : "memory");
+  return r != 0;
+}
 
 struct MoeArgs {
   const uint16_t* x;          // bf16 [R][H]
@@ -328,7 +335,8 @@ struct MoeArgs {
 __host__ __device__ constexpr size_t moe_red_bytes(int R) {
   return (size_t)kConsumerWarps * 2 * 16 * R * 4;
 }
-__host__ __device__ constexpr size_t moe_h_bytes(int I) { return (size_t)8 * (2 * I + kXPad); }
+// one staged h: the rows of one expert slot, rows of 2 I bytes + pad
+__host__ __device__ constexpr size_t moe_h_bytes(int I, int R) { return (size_t)R * (2 * I + kXPad); }
 // TMEM columns of the activation fragments: 16 per K chunk per warp, 4 warps per lane quarter.
 __host__ __device__ constexpr uint32_t moe_tmem_cols(int H) {
   const int kc = (H / 64 + kGuCT - 1) / kGuCT;
@@ -344,6 +352,10 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
   // the partial sums of one gate/up unit: written by the 16 consumer warps (pfull), read by
   // the reducer warps (pempty); the route is built (s_route)
   __shared__ __align__(8) uint64_t s_pfull, s_pempty, s_route;
+  // the two staged h buffers: filled by the producer (hfull), released by the consumers
+  __shared__ __align__(8) uint64_t hfull[2], hempty[2];
+  __shared__ int s_meta[kMaxRing];   // unit of each ring stage (-1: no unit left)
+  __shared__ int s_red_unit[2];      // unit of the partials handed to the reducers (-1: end)
   __shared__ uint32_t s_tmem;
   __shared__ float s_part[kRouterBatch][kConsumerWarps][kMaxRows];
   __shared__ int32_t sel_e[kMaxRows][kMaxTopK];
@@ -364,9 +376,9 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
   uint32_t* ucount = a.hdr + kHdrUnits;
 
   uint8_t* stages = smem;
-  uint8_t* region = smem + (size_t)ring * kStage;   // gate/up: red; down: hs
-  float* red = reinterpret_cast<float*>(region);
-  uint8_t* hs = region;
+  const size_t hbytes = moe_h_bytes(I, R);
+  uint8_t* hbuf = smem + (size_t)ring * kStage;                    // [2][R][2 I + pad]
+  float* red = reinterpret_cast<float*>(hbuf + 2 * hbytes);
 
   // gate/up geometry (K = H)
   const int Tg = H >> 6, KCg = (Tg + kGuCT - 1) / kGuCT, RTg = I >> 4;
@@ -386,6 +398,10 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
     mbar_init(&s_pfull, kConsumerWarps);
     mbar_init(&s_pempty, kReducerWarps);
     mbar_init(&s_route, 1);
+    for (int b2 = 0; b2 < 2; ++b2) {
+      mbar_init(&hfull[b2], 1);
+      mbar_init(&hempty[b2], kConsumerWarps);
+    }
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -417,45 +433,93 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
       ++f;
       if (++slot == ring) { slot = 0; phase ^= 1u; }
     };
-    // gate/up units b, b + G, ...: the shared expert's need nothing from the router
-    for (int n = b;; n += G) {
-      const int u = n / RTg, rt = n - u * RTg;
-      if (u > 0) routed();
-      if (n_union >= 0 && n >= (1 + n_union) * RTg) break;
-      const size_t e = u > 0 ? (size_t)u_expert[u - 1] : 0;
-      const uint8_t* gb = u > 0 ? a.gate + e * gu_expert : a.sh_gate;
-      const uint8_t* ub = u > 0 ? a.up + e * gu_expert : a.sh_up;
-      for (int c = 0; c < KCg; ++c) {
-        uint8_t* st = next_slot();
-        if (lane == 0) {
-          const size_t off = ((size_t)rt * Tg + (size_t)c * kGuCT) * kTile;
-          const uint32_t bytes = (uint32_t)min(kGuCT, Tg - c * kGuCT) * kTile;
-          mbar_arrive_expect_tx(&full[slot], 2u * bytes);
-          bulk_copy(st, gb + off, bytes, &full[slot]);
-          bulk_copy(st + kGuCT * kTile, ub + off, bytes, &full[slot]);
+    // Units are handed out in one order to all CTAs (an atomic counter): every gate/up unit
+    // (the shared expert's first: they need nothing from the router), then every down
+    // unit, expert slot by expert slot. A CTA takes its next unit when its ring has room,
+    // so the CTAs finish together whatever their units' timing; each stage records its
+    // unit for the consumers, and after the last unit a stage carries the end marker.
+    // The shared expert's unit b (b < S0 = min(G, RTg)) is taken first without the
+    // counter: it needs neither the router nor the zeroed header, so it streams from the
+    // start; the counter hands out the units from S0 on.
+    const int S0 = min(G, RTg);
+    int dn = 0;   // down units taken by this CTA (their h alternates between two buffers)
+    bool own_first = b < S0, header_ready = false;
+    for (;;) {
+      int n = b;
+      if (!own_first) {
+        if (!header_ready) {
+          pdl_wait();   // the prologue has zeroed the counter
+          header_ready = true;
         }
-        __syncwarp();
-        advance();
+        if (lane == 0) n = S0 + (int)atomicAdd(a.hdr + kHdrNext, 1u);
+        n = __shfl_sync(0xffffffffu, n, 0);
       }
-    }
-    routed();
-    // down units: a contiguous range
-    const int nd = (1 + n_union) * NGR;
-    const int d0 = (int)(((long long)b * nd) / G), d1 = (int)(((long long)(b + 1) * nd) / G);
-    for (int n = d0; n < d1; ++n) {
-      const int u = n / NGR, rg = n - u * NGR;
-      const int rig = min(kGroupRows, RTd - rg * kGroupRows);   // tile rows in the group
-      const uint8_t* gbase = (u > 0 ? a.down + (size_t)u_expert[u - 1] * dn_expert : a.sh_down) +
-                             (size_t)rg * kGroupRows * Td * kTile;
-      for (int c = 0; c < KCd; ++c) {
-        uint8_t* st = next_slot();
+      own_first = false;
+      if (n >= RTg) routed();
+      const int NG = n_union >= 0 ? (1 + n_union) * RTg : RTg;
+      const int ND = n_union >= 0 ? (1 + n_union) * NGR : 0;
+      if (n >= NG + ND) {
+        next_slot();
         if (lane == 0) {
-          const uint32_t bytes = (uint32_t)(min(kDownKT, Td - c * kDownKT) * rig * kTile);
-          mbar_arrive_expect_tx(&full[slot], bytes);
-          bulk_copy(st, gbase + (size_t)c * kDownKT * rig * kTile, bytes, &full[slot]);
+          s_meta[slot] = -1;
+          mbar_arrive(&full[slot]);
         }
         __syncwarp();
-        advance();
+        break;
+      }
+      if (n < NG) {
+        const int u = n / RTg, rt = n - u * RTg;
+        const size_t e = u > 0 ? (size_t)u_expert[u - 1] : 0;
+        const uint8_t* gb = u > 0 ? a.gate + e * gu_expert : a.sh_gate;
+        const uint8_t* ub = u > 0 ? a.up + e * gu_expert : a.sh_up;
+        for (int c = 0; c < KCg; ++c) {
+          uint8_t* st = next_slot();
+          if (lane == 0) {
+            const size_t off = ((size_t)rt * Tg + (size_t)c * kGuCT) * kTile;
+            const uint32_t bytes = (uint32_t)min(kGuCT, Tg - c * kGuCT) * kTile;
+            s_meta[slot] = n;
+            mbar_arrive_expect_tx(&full[slot], 2u * bytes);
+            bulk_copy(st, gb + off, bytes, &full[slot]);
+            bulk_copy(st + kGuCT * kTile, ub + off, bytes, &full[slot]);
+          }
+          __syncwarp();
+          advance();
+        }
+      } else {
+        const int m = n - NG, u = m / NGR, rg = m - u * NGR;
+        const int hb = dn & 1;
+        if (lane == 0) {
+          // h of the expert's rows, once every gate/up unit of the expert is counted and
+          // the buffer's previous unit is done; h is stored in MMA pair order
+          if (!wait_count(ucount + u, (uint32_t)RTg)) timed_out = true;
+          if (dn >= 2 && !pipe_wait(&hempty[hb], ((dn >> 1) - 1) & 1)) timed_out = true;
+          asm volatile("fence.proxy.async;" ::: "memory");   // h was written by other SMs
+          const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : u_rowmask[u - 1];
+          mbar_arrive_expect_tx(&hfull[hb], (uint32_t)__popc(rowmask) * 2u * (uint32_t)I);
+          for (int rr = 0; rr < R; ++rr) {
+            if ((rowmask >> rr) & 1u) {
+              const int slot_r = (u == 0) ? 0 : u_slot[u - 1][rr];
+              bulk_copy(hbuf + hb * hbytes + (size_t)rr * hpitch,
+                        a.h + ((size_t)rr * (1 + k) + slot_r) * I, 2u * (uint32_t)I, &hfull[hb]);
+            }
+          }
+        }
+        __syncwarp();
+        ++dn;
+        const int rig = min(kGroupRows, RTd - rg * kGroupRows);   // tile rows in the group
+        const uint8_t* gbase = (u > 0 ? a.down + (size_t)u_expert[u - 1] * dn_expert : a.sh_down) +
+                               (size_t)rg * kGroupRows * Td * kTile;
+        for (int c = 0; c < KCd; ++c) {
+          uint8_t* st = next_slot();
+          if (lane == 0) {
+            const uint32_t bytes = (uint32_t)(min(kDownKT, Td - c * kDownKT) * rig * kTile);
+            s_meta[slot] = n;
+            mbar_arrive_expect_tx(&full[slot], bytes);
+            bulk_copy(st, gbase + (size_t)c * kDownKT * rig * kTile, bytes, &full[slot]);
+          }
+          __syncwarp();
+          advance();
+        }
       }
     }
   } else if (warp < kProducerWarp) {
@@ -643,132 +707,121 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
       }
       if (tid == 0) a.route->n_union = n_union;
     }
-    // (3) gate/up units
-    const int n_units = (1 + n_union) * RTg;
-    const int n_mine = b < n_units ? (n_units - b + G - 1) / G : 0;
+    // (3) / (4) the units the producer took, in its order
+    const int NG = (1 + n_union) * RTg;
+    const uint8_t* const hrow0 = hbuf + (size_t)min(g, R - 1) * hpitch + q * 16;   // rows >= R: a copy
     float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
+    // down: two chains, even (acc) and odd (acc2) tiles of the row, added at the unit end
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
     int slot = 0;
     uint32_t phase = 0;
-    for (int unit = 0; unit < n_mine; ++unit) {
-      for (int c = 0; c < KCg; ++c) {
-        if (!pipe_wait(&full[slot], phase)) timed_out = true;
-        const uint8_t* st = stages + (size_t)slot * kStage;
-        const int ct = min(kGuCT, Tg - c * kGuCT);
+    int gu_k = 0;   // gate/up units handed to the reducers
+    int dn = 0;     // down units done
+    for (;;) {
+      if (!pipe_wait(&full[slot], phase)) { timed_out = true; break; }
+      const int n = s_meta[slot];
+      if (n < 0) break;
+      if (n < NG) {
+        // gate/up: KCg stages; warp w takes tiles 2w, 2w + 1 of each
+        for (int c = 0; c < KCg; ++c) {
+          if (c > 0 && !pipe_wait(&full[slot], phase)) timed_out = true;
+          const uint8_t* st = stages + (size_t)slot * kStage;
+          const int ct = min(kGuCT, Tg - c * kGuCT);
 #pragma unroll
-        for (int tt = 0; tt < 2; ++tt) {
-          const int t = warp * 2 + tt;
-          if (t < ct) {
-            uint32_t xw[8];   // blocks 2t, 2t + 1 of the chunk
-            tmem_ld8(tw + (uint32_t)(c * 16 + tt * 8), xw);
-            const uint4 X0 = make_uint4(xw[0], xw[1], xw[2], xw[3]);
-            const uint4 X1 = make_uint4(xw[4], xw[5], xw[6], xw[7]);
-            const uint8_t* tg = st + t * kTile;
-            const uint8_t* tu = st + (kGuCT + t) * kTile;
-            const uint4 Wg = lds128(tg + lane * 16), Wu = lds128(tu + lane * 16);
-            const uint2 Sg = lds64(tg + kTileNib + g * 8), Su = lds64(tu + kTileNib + g * 8);
-            q4_tile_mma(Wg, Sg, X0, X1, ag);
-            q4_tile_mma(Wu, Su, X0, X1, au);
+          for (int tt = 0; tt < 2; ++tt) {
+            const int t = warp * 2 + tt;
+            if (t < ct) {
+              uint32_t xw[8];   // blocks 2t, 2t + 1 of the chunk
+              tmem_ld8(tw + (uint32_t)(c * 16 + tt * 8), xw);
+              const uint4 X0 = make_uint4(xw[0], xw[1], xw[2], xw[3]);
+              const uint4 X1 = make_uint4(xw[4], xw[5], xw[6], xw[7]);
+              const uint8_t* tg = st + t * kTile;
+              const uint8_t* tu = st + (kGuCT + t) * kTile;
+              const uint4 Wg = lds128(tg + lane * 16), Wu = lds128(tu + lane * 16);
+              const uint2 Sg = lds64(tg + kTileNib + g * 8), Su = lds64(tu + kTileNib + g * 8);
+              q4_tile_mma(Wg, Sg, X0, X1, ag);
+              q4_tile_mma(Wu, Su, X0, X1, au);
+            }
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the slot
+          if (++slot == ring) { slot = 0; phase ^= 1u; }
+        }
+        // partials [warp][gate/up][row][col] (cols < R only), once the reducers are done
+        // with the unit before
+        if (gu_k >= 1 && !pipe_wait(&s_pempty, (gu_k - 1) & 1)) timed_out = true;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int col = 2 * q + (e & 1), row = g + ((e & 2) ? 8 : 0);
+          if (col < R) {
+            red[((warp * 2 + 0) * 16 + row) * R + col] = ag[e];
+            red[((warp * 2 + 1) * 16 + row) * R + col] = au[e];
+          }
+          ag[e] = 0.f;
+          au[e] = 0.f;
+        }
+        if (tid == 0) s_red_unit[gu_k & 1] = n;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_pfull);
+        ++gu_k;
+      } else {
+        // down: warp w owns tile row w of the group for all of K
+        const int m = n - NG, u = m / NGR, rg = m - u * NGR;
+        const int rig = min(kGroupRows, RTd - rg * kGroupRows);
+        const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : u_rowmask[u - 1];
+        const int hb = dn & 1;
+        if (!pipe_wait(&hfull[hb], (dn >> 1) & 1)) timed_out = true;
+        const uint8_t* hrow = hrow0 + hb * hbytes;
+        const int tr = rg * kGroupRows + warp;              // this warp's tile row
+        for (int c = 0; c < KCd; ++c) {
+          if (c > 0 && !pipe_wait(&full[slot], phase)) timed_out = true;
+          const uint8_t* st = stages + (size_t)slot * kStage;
+          const int kt = min(kDownKT, Td - c * kDownKT);
+          if (warp < rig) {
+            const uint8_t* xc = hrow + (size_t)c * kDownKT * 128;
+#pragma unroll
+            for (int jj = 0; jj < kDownKT; ++jj) {
+              if (jj < kt) {
+                const uint8_t* tp = st + (jj * rig + warp) * kTile;
+                const uint4 W = lds128(tp + lane * 16);
+                const uint2 S = lds64(tp + kTileNib + g * 8);
+                const uint8_t* xb = xc + jj * 128;   // blocks 2t, 2t + 1
+                if (jj & 1)
+                  q4_tile_mma(W, S, lds128(xb), lds128(xb + 64), acc2);
+                else
+                  q4_tile_mma(W, S, lds128(xb), lds128(xb + 64), acc);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+          if (++slot == ring) { slot = 0; phase ^= 1u; }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the slot
-        if (++slot == ring) { slot = 0; phase ^= 1u; }
-      }
-      // partials [warp][gate/up][row][col] (cols < R only), once the reducers are done
-      // with the unit before
-      if (unit >= 1 && !pipe_wait(&s_pempty, (unit - 1) & 1)) timed_out = true;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int col = 2 * q + (e & 1), row = g + ((e & 2) ? 8 : 0);
-        if (col < R) {
-          red[((warp * 2 + 0) * 16 + row) * R + col] = ag[e];
-          red[((warp * 2 + 1) * 16 + row) * R + col] = au[e];
-        }
-        ag[e] = 0.f;
-        au[e] = 0.f;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_pfull);
-    }
-    tc_fence_before();   // this warp's tensor-memory reads are done
-    // (4) down units. The partial buffer shares shared memory with h: the reducers must be
-    // done with it first.
-    if (n_mine > 0 && !pipe_wait(&s_pempty, (n_mine - 1) & 1)) timed_out = true;
-    const int nd = (1 + n_union) * NGR;
-    const int d0 = (int)(((long long)b * nd) / G), d1 = (int)(((long long)(b + 1) * nd) / G);
-    const uint8_t* hrow = hs + g * hpitch + q * 16;   // rows >= R or unused: never read out
-    int h_u = -1;       // expert slot whose h is staged
-    // two chains: even (acc) and odd (acc2) tiles of the row, added once at the unit end
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int n = d0; n < d1; ++n) {
-      const int u = n / NGR, rg = n - u * NGR;
-      const int rig = min(kGroupRows, RTd - rg * kGroupRows);
-      const uint32_t rowmask = (u == 0) ? ((1u << R) - 1u) : u_rowmask[u - 1];
-      if (u != h_u) {
-        // h of the expert's rows, once every gate/up unit of the expert is counted:
-        // [verify row][values], 16-byte pieces, then each piece put in MMA pair order in
-        // place. Rows that do not use the expert keep stale values; their MMA columns are
-        // never read.
-        if (tid == 0 && !wait_count(ucount + u, (uint32_t)RTg)) timed_out = true;
-        consumer_sync();   // every consumer is done with the previous h
-        const int per_row = I / 8;
-        for (int p = tid; p < R * per_row; p += kConsumers) {
-          const int rr = p / per_row, pp = p - rr * per_row;
-          if ((rowmask >> rr) & 1u) {
-            const int slot_r = (u == 0) ? 0 : u_slot[u - 1][rr];
-            cp_async16(hs + rr * hpitch + pp * 16, a.h + ((size_t)rr * (1 + k) + slot_r) * I + pp * 8);
-          }
-        }
-        cp_async_commit();
-        cp_async_wait<0>();
-        for (int p = tid; p < R * per_row; p += kConsumers) {
-          const int rr = p / per_row, pp = p - rr * per_row;
-          if ((rowmask >> rr) & 1u) {
-            uint4* hp = reinterpret_cast<uint4*>(hs + rr * hpitch + pp * 16);
-            *hp = pair_order(*hp);
-          }
-        }
-        consumer_sync();
-        h_u = u;
-      }
-      const int tr = rg * kGroupRows + warp;              // this warp's tile row
-      for (int c = 0; c < KCd; ++c) {
-        if (!pipe_wait(&full[slot], phase)) timed_out = true;
-        const uint8_t* st = stages + (size_t)slot * kStage;
-        const int kt = min(kDownKT, Td - c * kDownKT);
+        if (lane == 0) mbar_arrive(&hempty[hb]);   // this warp is done with the staged h
+        ++dn;
         if (warp < rig) {
-          const uint8_t* xc = hrow + (size_t)c * kDownKT * 128;
 #pragma unroll
-          for (int jj = 0; jj < kDownKT; ++jj) {
-            if (jj < kt) {
-              const uint8_t* tp = st + (jj * rig + warp) * kTile;
-              const uint4 W = lds128(tp + lane * 16);
-              const uint2 S = lds64(tp + kTileNib + g * 8);
-              const uint8_t* xb = xc + jj * 128;   // blocks 2t, 2t + 1
-              if (jj & 1)
-                q4_tile_mma(W, S, lds128(xb), lds128(xb + 64), acc2);
-              else
-                q4_tile_mma(W, S, lds128(xb), lds128(xb + 64), acc);
+          for (int e = 0; e < 4; ++e) {
+            const int col = 2 * q + (e & 1), row = tr * 16 + g + ((e & 2) ? 8 : 0);
+            if (col < R && ((rowmask >> col) & 1u)) {
+              const int slot_c = (u == 0) ? 0 : u_slot[u - 1][col];
+              a.opart[((size_t)col * (1 + k) + slot_c) * H + row] = __fadd_rn(acc[e], acc2[e]);
             }
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        if (++slot == ring) { slot = 0; phase ^= 1u; }
-      }
-      if (warp < rig) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int col = 2 * q + (e & 1), row = tr * 16 + g + ((e & 2) ? 8 : 0);
-          if (col < R && ((rowmask >> col) & 1u)) {
-            const int slot_c = (u == 0) ? 0 : u_slot[u - 1][col];
-            a.opart[((size_t)col * (1 + k) + slot_c) * H + row] = __fadd_rn(acc[e], acc2[e]);
-          }
-        }
+        for (int e = 0; e < 4; ++e) acc[e] = acc2[e] = 0.f;
       }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[e] = acc2[e] = 0.f;
     }
+    tc_fence_before();   // this warp's tensor-memory reads are done
+    // the reducers stop at an end marker in place of a unit. It is handed over only once
+    // they are done with the last unit, as every unit is: a waiter on a parity must not
+    // see two phases complete while it looks away.
+    if (gu_k >= 1 && !pipe_wait(&s_pempty, (gu_k - 1) & 1)) timed_out = true;
+    if (tid == 0) s_red_unit[gu_k & 1] = -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_pfull);
     // this CTA's outputs are written: count it (the barrier orders them before the fence)
     consumer_sync();
     if (tid == 0) {
@@ -783,11 +836,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
     const int rtid = tid - kReducer0;
     pdl_wait();   // the prologue (zeroed header) is complete
     if (!pipe_wait(&s_route, 0)) timed_out = true;
-    const int n_union = s_nunion;
-    const int n_units = (1 + n_union) * RTg;
-    int unit = 0;
-    for (int n = b; n < n_units; n += G, ++unit) {
-      if (!pipe_wait(&s_pfull, unit & 1)) timed_out = true;
+    for (int unit = 0;; ++unit) {
+      // the three warps leave together on a give-up (they meet at a named barrier below)
+      if (!reducer_all(pipe_wait(&s_pfull, unit & 1))) { timed_out = true; break; }
+      const int n = s_red_unit[unit & 1];
+      if (n < 0) break;
       const int u = n / RTg, rti = n - u * RTg;
       if (rtid < 16 * R) {
         const int row = rtid / R, col = rtid - row * R;
@@ -800,8 +853,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
           }
           const int slot_c = (u == 0) ? 0 : u_slot[u - 1][col];
           const float silu = __fdiv_rn(gs, __fadd_rn(1.0f, expf(-gs)));
-          a.h[((size_t)col * (1 + k) + slot_c) * I + rti * 16 + row] =
-              f32_to_bf16_rne(__fmul_rn(silu, us));
+          // value i = rti * 16 + row, stored in MMA pair order within its group of 8
+          // (v0, v4, v1, v5, v2, v6, v3, v7)
+          const int i = rti * 16 + row, i8 = i & 7;
+          const int pos = (i & ~7) | (i8 < 4 ? 2 * i8 : 2 * (i8 - 4) + 1);
+          a.h[((size_t)col * (1 + k) + slot_c) * I + pos] = f32_to_bf16_rne(__fmul_rn(silu, us));
         }
       }
       __syncwarp();
@@ -844,8 +900,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
 }
 
 size_t moe_smem(const MoeDims& d, int ring) {
-  const size_t region = std::max(moe_red_bytes(d.R), moe_h_bytes(d.I));
-  return 1024 + (size_t)ring * kStage + region;
+  return 1024 + (size_t)ring * kStage + 2 * moe_h_bytes(d.I, d.R) + moe_red_bytes(d.R);
 }
 
 // Deepest ring (kMaxRing .. 2 stages) whose shared memory fits beside the kernel's static

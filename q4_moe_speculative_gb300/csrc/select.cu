@@ -1273,9 +1273,21 @@ struct TopkArgs {
   int32_t* nsel;
   uint32_t* status;
   int tc_mode;
-  int NS;             // row stride of sc0 / knorm (N rounded up to a multiple of 4)
+  int NS;             // row stride of sc0 / knorm (N rounded up to a multiple of 32)
   int NC;             // row stride of kmax
+  uint32_t* ldone;    // [L] rows done per layer
+  const uint8_t* urows;
+  int keep;           // leave the scores, key norms and union lists in the workspace
 };
+
+// Drops the 128-byte lines that lie wholly inside [p, p + bytes) from L2 without writing
+// them back (their contents become undefined), spread over the block's threads.
+__device__ __forceinline__ void discard_lines(const void* p, size_t bytes) {
+  const uintptr_t a0 = (reinterpret_cast<uintptr_t>(p) + 127) & ~(uintptr_t)127;
+  const uintptr_t a1 = (reinterpret_cast<uintptr_t>(p) + bytes) & ~(uintptr_t)127;
+  for (uintptr_t x = a0 + 128 * threadIdx.x; x < a1; x += 128 * (uintptr_t)blockDim.x)
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(x) : "memory");
+}
 
 // Bitonic sort, descending, of one 64-bit value per thread over threads 0 .. P - 1 (P a
 // power of two <= the block size; the other threads sort their own values among
@@ -1352,11 +1364,28 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   const int count = a.ccount[lr];
   const int K = a.K;
   int32_t* out = a.sel + (size_t)lr * K;
+  // At the end of the row: its scores are dead, and once the layer's last row is done, so
+  // are the layer's key norms and union lists. They are dropped from L2 rather than left
+  // dirty there (the next kernels would pay for writing them back), unless the caller keeps
+  // the workspace for inspection.
+  auto finish = [&]() {
+    if (a.keep) return;
+    __syncthreads();   // every read of this row's data is done
+    discard_lines(a.sc0 + (size_t)lr * a.NS, sizeof(uint32_t) * (size_t)a.NS);
+    if (tid == 0) s_misc[0] = atomicAdd(a.ldone + l, 1u) == (uint32_t)(a.R - 1) ? 1 : 0;
+    __syncthreads();
+    if (s_misc[0]) {
+      discard_lines(a.knorm + (size_t)l * a.NS, sizeof(float) * (size_t)a.NS);
+      discard_lines(a.uidx + (size_t)l * a.N, sizeof(int32_t) * (size_t)a.N);
+      discard_lines(a.urows + (size_t)l * a.N, (size_t)a.N);
+    }
+  };
 
   if (count <= K) {
     const int32_t* ci = a.cidx + (size_t)lr * a.N;
     for (int i = tid; i < K; i += blockDim.x) out[i] = i < count ? ci[i] : -1;
     if (tid == 0) a.nsel[lr] = count;
+    finish();
     return;
   }
 
@@ -1772,6 +1801,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
         a.nsel[lr] = K;
         if (taken != K) flag_status(a.status, kStatusCheck);
       }
+      finish();
       return;
     }
     // Too many candidates (e.g. heavy ties): canonical scores for the whole row.
@@ -1801,6 +1831,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       if (taken != K) flag_status(a.status, kStatusCheck);
     }
   }
+  finish();
 }
 
 template <int NCH, int HH>
@@ -1830,6 +1861,7 @@ SelLayout sel_layout(const SelDims& d, bool caller_cidx) {
   size_t off = 0;
   L.header = off; off += 256;
   L.uagg = off; off += up(sizeof(uint32_t) * (size_t)d.L * ((W + kCompactThreads - 1) / kCompactThreads));
+  L.ldone = off; off += up(sizeof(uint32_t) * (size_t)d.L);
   L.zero_bytes = off;
   L.wordoff = off; off += up(sizeof(int32_t) * (size_t)d.L * W);
   if (!caller_cidx) {
@@ -1910,12 +1942,15 @@ cudaError_t launch_score(const SelDims& d, const uint16_t* keys, const uint16_t*
 
 cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* q,
                         const float* head_w, int32_t* sel, int32_t* nsel,
-                        const SelWorkspace& ws, bool tc, cudaStream_t s) {
+                        const SelWorkspace& ws, bool tc, bool keep, cudaStream_t s) {
   TopkArgs a{d.R, d.Hh, d.N, d.topk, d.key_stride, keys, q, head_w, ws.cidx, ws.ccount,
              ws.uidx, ws.ucount, reinterpret_cast<uint32_t*>(ws.cscore), ws.knorm, ws.qnorm,
              ws.kmax, sel, nsel, ws.header, tc ? 1 : 0};
   a.NS = score_stride(d.N);
   a.NC = chunk_stride(d.N);
+  a.ldone = ws.ldone;
+  a.urows = ws.urows;
+  a.keep = keep ? 1 : 0;
   cudaError_t err =
       cudaFuncSetAttribute(k7_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
   if (err != cudaSuccess) return err;

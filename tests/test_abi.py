@@ -124,7 +124,7 @@ def test_select_workspace_size_host_only(lib):
     dict(head_dim=64), dict(n_rows=0), dict(n_rows=9), dict(n_heads=17), dict(n_blocks=0),
     dict(top_k=0), dict(top_k=4096), dict(key_layer_stride=100), dict(keys=FAKE + 8),
     dict(keys=None), dict(mask=None), dict(limit=None), dict(head_w=None), dict(q=None),
-    dict(flags=2), dict(flags=-1),
+    dict(flags=4), dict(flags=-1),
 ])
 def test_select_rejects_bad_arguments(lib, kw):
     a = fake_select(**kw)

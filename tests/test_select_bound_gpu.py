@@ -73,7 +73,7 @@ def check_bound_and_selection(dsm, inp, topk, layers, sample=None, seed=0):
     dv = {k: v.to("cuda") for k, v in inp.items()}
     args = (dv["keys"], dv["q"], dv["head_w"], dv["mask"], dv["limit"], topk)
     ws = torch.empty(dsm.select_workspace_size(*args), dtype=torch.uint8, device="cuda")
-    sel, nsel, _, _ = dsm.select_blocks(*args, workspace=ws)
+    sel, nsel, _, _ = dsm.select_blocks(*args, workspace=ws, keep_workspace=True)
     torch.cuda.synchronize()
     assert dsm.workspace_status(ws) == 0
     views = {k: v.cpu().numpy() for k, v in dsm.select_workspace_views(*args, ws).items()}
