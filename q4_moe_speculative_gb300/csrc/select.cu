@@ -236,7 +236,6 @@ struct CompactArgs {
 
 __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) {
   __shared__ int scratch[33];
-  __shared__ int s_off[kCompactThreads];
   __shared__ int s_base;
   const int R = a.R, N = a.N;
   const int W = (N + 31) >> 5;
@@ -336,11 +335,10 @@ __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) 
       base = s_base;
     }
     const int excl = base + lexcl;
-    s_off[tid] = excl;
     if (union_cta && wi < W) a.uwordoff[(size_t)l * W + wi] = excl;
-    __syncthreads();
     // Warp `warp` scatters the words c0 + 32*warp .. c0 + 32*warp + 31 of this chunk, whose
-    // bits sit in its lanes 0..31, one word at a time with the bits broadcast by shuffles.
+    // bits and offsets sit in its lanes 0..31, one word at a time, broadcast by shuffles
+    // (nothing goes through shared memory, so the words' stores overlap).
     {
       const int wbase = c0 + warp * 32;
       const uint32_t all_rows = (1u << R) - 1u;
@@ -353,6 +351,7 @@ __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) 
         const int w = wbase + jw;
         const int b = w * 32 + lane;
         const uint32_t wv = __shfl_sync(0xffffffffu, mw, jw);
+        const int off0 = __shfl_sync(0xffffffffu, excl, jw);
         const bool pred = (wv >> lane) & 1u;
         uint32_t rows = 0;
         if (union_cta) {
@@ -365,7 +364,7 @@ __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) 
           }
         }
         if (pred) {
-          const int off = s_off[warp * 32 + jw] + __popc(wv & ((1u << lane) - 1u));
+          const int off = off0 + __popc(wv & ((1u << lane) - 1u));
           if (union_cta) {
             uo[off] = b;
             ro[off] = (uint8_t)rows;
