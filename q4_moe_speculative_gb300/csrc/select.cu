@@ -235,6 +235,7 @@ struct CompactArgs {
 };
 
 __global__ void __launch_bounds__(kCompactThreads, 3) k6_compact(CompactArgs a) {
+  pdl_trigger();   // the scorer may launch as soon as every CTA of this grid has started
   __shared__ int scratch[33];
   __shared__ int s_base;
   const int R = a.R, N = a.N;
@@ -665,15 +666,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
   uint8_t* const base_ptr = smem_raw + (base - raw);
   const uint32_t qslot_addr = base + (uint32_t)S * kKeyBytes;
 
-  // This CTA's tile range [t0, t1) and the cursor of t0 (same in every warp).
-  int total = 0, cl = 0, ce = 0;
-  tile_cursor(a.ucount, a.L, 0, &cl, &ce, &total);
-  const int t0 = (int)(((long long)blockIdx.x * total) / gridDim.x);
-  const int t1 = (int)(((long long)(blockIdx.x + 1) * total) / gridDim.x);
-  if (t0 >= t1) return;
-  if (t0 > 0) tile_cursor(a.ucount, a.L, t0, &cl, &ce, &total);
-  const int n = t1 - t0;
-
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       sm100::mbar_init(&bar_full[s], kTcProducerWarps);
@@ -691,6 +683,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
   __syncthreads();
   sm100::tc_fence_after();
   const uint32_t tmem = s_tmem;
+
+  // Set up while the compaction finishes (programmatic launch); its union lists and counts
+  // are read from here on.
+  pdl_wait();
+  pdl_trigger();   // the top-k may start launching on SMs this grid leaves
+  // This CTA's tile range [t0, t1) and the cursor of t0 (same in every warp).
+  int total = 0, cl = 0, ce = 0;
+  tile_cursor(a.ucount, a.L, 0, &cl, &ce, &total);
+  const int t0 = (int)(((long long)blockIdx.x * total) / gridDim.x);
+  const int t1 = (int)(((long long)(blockIdx.x + 1) * total) / gridDim.x);
+  if (t0 >= t1) {
+    if (warp == 0) sm100::tmem_dealloc(tmem, G::kTmemCols);
+    return;
+  }
+  if (t0 > 0) tile_cursor(a.ucount, a.L, t0, &cl, &ce, &total);
+  const int n = t1 - t0;
 
   auto give_up = [&]() {
     if (lane == 0) {
@@ -1846,8 +1854,8 @@ cudaError_t launch_tc(const SelDims& d, const ScoreArgs& a, cudaStream_t s) {
   int grid = device_sm_count();
   if (tiles < grid) grid = (int)tiles;
   if (grid < 1) grid = 1;
-  k5_score_tc<NCH, HH><<<grid, kTcThreads, smem, s>>>(ta);
-  return cudaGetLastError();
+  // a programmatic dependent of the compaction: the CTAs set up while it finishes
+  return launch_pdl(k5_score_tc<NCH, HH>, dim3(grid), kTcThreads, smem, s, ta);
 }
 
 }  // namespace
