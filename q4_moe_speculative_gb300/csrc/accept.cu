@@ -20,7 +20,8 @@
 //    weight (token order) exceeds u * sum(w), else the last x with w[x] > 0.
 //
 // Every decision is taken in fp64 (on GB300 the fp64 exponentials of the softmax are the
-// cost of sampling). The rows are split into chunks of kAcceptChunk tokens over the GPU:
+// cost of sampling). The rows are split into chunks of kAcceptChunk tokens (kAcceptChunkSmall
+// for small batches) over the GPU:
 //   K_stats   per (chunk, row): greedy: the chunk's (max, lowest id); sampling: the
 //             chunk's max m_c and sum_v exp(z_v / T - m_c / T).
 //   K_decide  per step: each row's max M and normaliser s = sum_c s_c exp(m_c/T - M)
@@ -36,7 +37,6 @@ namespace dsmoe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kPer = kAcceptChunk / kThreads;   // tokens per thread in a chunk
 constexpr int kModeResidual = 0;                // draw from max(p - q, 0)
 constexpr int kModeTarget = 1;                  // draw from p (bonus token)
 
@@ -86,15 +86,16 @@ __device__ __forceinline__ void better(float& v, int& i, float v2, int i2) {
 // K_stats: one CTA per (chunk, row of a step); thread t reads tokens t, t + 256, ... of
 // the chunk (coalesced), in ascending order.
 // ---------------------------------------------------------------------------------
-template <bool kGreedy>
+template <bool kGreedy, int CH>
 __global__ void __launch_bounds__(kThreads) k_acc_stats(AcceptArgs a) {
+  constexpr int kPer = CH / kThreads;   // tokens per thread in a chunk
   __shared__ double sh[32];
   __shared__ float shf[kThreads / 32];
   __shared__ int shi[kThreads / 32];
   const int c = blockIdx.x, br = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float* z = a.z + (size_t)br * a.V;
-  const int v0 = c * kAcceptChunk, v1 = min(a.V, v0 + kAcceptChunk);
+  const int v0 = c * CH, v1 = min(a.V, v0 + CH);
   pdl_trigger();
   float best = -INFINITY;
   int bid = 0x7FFFFFFF;
@@ -250,7 +251,9 @@ __device__ __forceinline__ void weights(const AcceptArgs& a, const AcceptDecisio
 // K_part: one CTA per (chunk, step): sums of both weights over the chunk and the last
 // token of the chunk with a positive weight of each kind.
 // ---------------------------------------------------------------------------------
+template <int CH>
 __global__ void __launch_bounds__(kThreads) k_acc_part(AcceptArgs a) {
+  constexpr int kPer = CH / kThreads;
   __shared__ double sh[32];
   __shared__ int shl[2];
   const int c = blockIdx.x, b = blockIdx.y;
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads) k_acc_part(AcceptArgs a) {
   const float* z = a.z + ((size_t)b * a.R + D.row) * a.V;
   const double* q =
       D.mode == kModeResidual ? a.qd + ((size_t)b * (a.R - 1) + D.row) * a.V : nullptr;
-  const int v0 = c * kAcceptChunk, v1 = min(a.V, v0 + kAcceptChunk);
+  const int v0 = c * CH, v1 = min(a.V, v0 + CH);
   if (threadIdx.x == 0) { shl[0] = -1; shl[1] = -1; }
   __syncthreads();
   double sp = 0.0, sr = 0.0;
@@ -295,7 +298,9 @@ __global__ void __launch_bounds__(kThreads) k_acc_part(AcceptArgs a) {
 // consecutive tokens (sequential partial sums) and a block scan of the threads' totals
 // gives every token's cumulative weight; the smallest token past the target is drawn.
 // ---------------------------------------------------------------------------------
+template <int CH>
 __global__ void __launch_bounds__(kThreads) k_acc_pick(AcceptArgs a) {
+  constexpr int kPer = CH / kThreads;
   __shared__ double sh[kThreads / 32];
   __shared__ int s_chunk, s_tok, s_use_res, s_last;
   __shared__ double s_target, s_pre;
@@ -334,7 +339,7 @@ __global__ void __launch_bounds__(kThreads) k_acc_pick(AcceptArgs a) {
     const float* z = a.z + ((size_t)b * a.R + D.row) * a.V;
     const double* q =
         D.mode == kModeResidual ? a.qd + ((size_t)b * (a.R - 1) + D.row) * a.V : nullptr;
-    const int v0 = c * kAcceptChunk + tid * kPer, v1 = min(a.V, c * kAcceptChunk + kAcceptChunk);
+    const int v0 = c * CH + tid * kPer, v1 = min(a.V, c * CH + CH);
     double w[kPer];
     double mine = 0.0;
     for (int k = 0; k < kPer; ++k) {
@@ -385,7 +390,8 @@ __global__ void __launch_bounds__(kThreads) k_acc_pick(AcceptArgs a) {
 
 AcceptLayout accept_layout(int B, int R, int V) {
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
-  const size_t C = (size_t)(V + kAcceptChunk - 1) / kAcceptChunk;
+  // sized for the smaller chunk
+  const size_t C = (size_t)(V + kAcceptChunkSmall - 1) / kAcceptChunkSmall;
   AcceptLayout L{};
   size_t off = 0;
   L.header = off; off += 256;
@@ -396,12 +402,30 @@ AcceptLayout accept_layout(int B, int R, int V) {
   return L;
 }
 
+template <int CH>
+cudaError_t launch_accept_ch(AcceptArgs a, bool greedy, cudaStream_t s) {
+  a.C = (a.V + CH - 1) / CH;
+  const dim3 g1(a.C, a.B * a.R);
+  if (greedy) {
+    k_acc_stats<true, CH><<<g1, kThreads, 0, s>>>(a);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return launch_pdl(k_acc_decide<true>, a.B, 32, 0, s, a);
+  }
+  k_acc_stats<false, CH><<<g1, kThreads, 0, s>>>(a);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if ((err = launch_pdl(k_acc_decide<false>, a.B, 32, 0, s, a)) != cudaSuccess) return err;
+  if ((err = launch_pdl(k_acc_part<CH>, dim3(a.C, a.B), kThreads, 0, s, a)) != cudaSuccess)
+    return err;
+  return launch_pdl(k_acc_pick<CH>, a.B, kThreads, 0, s, a);
+}
+
 cudaError_t launch_accept(const AcceptProblem& pr, uint8_t* ws, cudaStream_t s) {
   const AcceptLayout L = accept_layout(pr.B, pr.R, pr.V);
   AcceptArgs a{};
   a.z = pr.logits;
   a.B = pr.B; a.R = pr.R; a.V = pr.V;
-  a.C = (pr.V + kAcceptChunk - 1) / kAcceptChunk;
   a.T = pr.T;
   a.qd = pr.qd; a.draft = pr.draft; a.u_acc = pr.u_acc; a.u_res = pr.u_res;
   a.out = pr.out; a.n_out = pr.n_out;
@@ -409,20 +433,12 @@ cudaError_t launch_accept(const AcceptProblem& pr, uint8_t* ws, cudaStream_t s) 
   a.dec = reinterpret_cast<AcceptDecision*>(ws + L.dec);
   a.spart = reinterpret_cast<AcceptPart*>(ws + L.spart);
   a.status = reinterpret_cast<uint32_t*>(ws + L.header);
-  const dim3 g1(a.C, a.B * a.R);
-  if (pr.greedy) {
-    k_acc_stats<true><<<g1, kThreads, 0, s>>>(a);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    return launch_pdl(k_acc_decide<true>, a.B, 32, 0, s, a);
-  }
-  k_acc_stats<false><<<g1, kThreads, 0, s>>>(a);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  if ((err = launch_pdl(k_acc_decide<false>, a.B, 32, 0, s, a)) != cudaSuccess) return err;
-  if ((err = launch_pdl(k_acc_part, dim3(a.C, a.B), kThreads, 0, s, a)) != cudaSuccess)
-    return err;
-  return launch_pdl(k_acc_pick, a.B, kThreads, 0, s, a);
+  // Chunks of kAcceptChunk tokens, or of kAcceptChunkSmall when that leaves fewer than
+  // two CTAs per SM (few steps): the later kernels work on one row per step and the draw
+  // scans one chunk, so small batches want short chunks.
+  const long long ctas = (long long)pr.B * pr.R * ((pr.V + kAcceptChunk - 1) / kAcceptChunk);
+  if (ctas < 2LL * device_sm_count()) return launch_accept_ch<kAcceptChunkSmall>(a, pr.greedy, s);
+  return launch_accept_ch<kAcceptChunk>(a, pr.greedy, s);
 }
 
 }  // namespace dsmoe

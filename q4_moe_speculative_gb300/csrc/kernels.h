@@ -145,6 +145,7 @@ cudaError_t launch_attn(const AttnProblem& p, uint8_t* ws, cudaStream_t s);
 
 // ---- verify acceptance (accept.cu)
 constexpr int kAcceptChunk = 4096;    // tokens of a row per CTA
+constexpr int kAcceptChunkSmall = 1024;   // the same for batches of few steps
 constexpr int kAcceptMaxRows = 16;
 struct AcceptChunk {      // per (step, row, chunk)
   float m;                // greedy / sampling: the chunk's largest logit

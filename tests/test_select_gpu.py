@@ -221,3 +221,26 @@ def test_twelve_heads_odd_block_count(dsm, canonical):
     shape = synth.SelectShape(L=2, R=3, Hh=12, N=12345, topk=300)
     inp = synth.select_inputs(shape, seed=21)
     check(dsm, inp, shape.topk, canonical=canonical)
+
+
+def test_dropped_workspace_is_rewritten_by_the_next_call(dsm):
+    # By default the top-k drops the scores, key norms and union lists from L2 once read
+    # (their workspace bytes become undefined); the next call on the same workspace must
+    # rebuild everything it reads. Three calls on one workspace (dropping, keeping,
+    # dropping) and a call on a fresh workspace give the same selection, bit for bit.
+    shape = synth.SelectShape(L=6, R=6, Hh=8, N=20000, topk=512)
+    inp = to_dev(synth.select_inputs(shape, seed=21))
+    args = (inp["keys"], inp["q"], inp["head_w"], inp["mask"], inp["limit"], 512)
+    ws = torch.empty(dsm.select_workspace_size(*args), dtype=torch.uint8, device="cuda")
+    outs = []
+    for keep in (False, True, False):
+        sel, nsel, _, _ = dsm.select_blocks(*args, workspace=ws, keep_workspace=keep)
+        torch.cuda.synchronize()
+        assert dsm.workspace_status(ws) == 0
+        outs.append((sel.cpu().clone(), nsel.cpu().clone()))
+    fresh = dsm.select_blocks(*args)
+    torch.cuda.synchronize()
+    for sel, nsel in outs:
+        assert torch.equal(sel, fresh[0].cpu()) and torch.equal(nsel, fresh[1].cpu())
+    ref = run_ref(inp, 512, layers=(0, 2))
+    assert np.array_equal(outs[2][0].numpy()[:2], ref["sel"][:2])
