@@ -140,13 +140,16 @@ __global__ void __launch_bounds__(kThreads) k_acc_stats(AcceptArgs a) {
     }
     return;
   }
-  // sum of exp(z / T - m_c / T) over the chunk, in fp64
-  const double Mc = (double)shf[0] / a.T;
+  // sum of exp(z / T - m_c / T) over the chunk, in fp64 (z / T as z times 1 / T: within
+  // an ulp of the quotient, far inside the decisions' rounding margin, and no fp64
+  // division per token)
+  const double invT = 1.0 / a.T;
+  const double Mc = (double)shf[0] * invT;
   double s = 0.0;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int v = v0 + k * kThreads + (int)threadIdx.x;
-    if (v < v1) s += exp((double)zv[k] / a.T - Mc);
+    if (v < v1) s += exp(fma((double)zv[k], invT, -Mc));
   }
   s = block_sum_d(s, sh);
   if (threadIdx.x == 0) {
@@ -182,12 +185,13 @@ __global__ void __launch_bounds__(32) k_acc_decide(AcceptArgs a) {
       }
       if (lane == 0) sBest[r] = bid;
     } else {
+      const double invT = 1.0 / a.T;   // z / T as z times 1 / T, as in the other kernels
       double M = -INFINITY;
-      for (int c = lane; c < C; c += 32) M = fmax(M, (double)cs[c].m / a.T);
+      for (int c = lane; c < C; c += 32) M = fmax(M, (double)cs[c].m * invT);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) M = fmax(M, __shfl_xor_sync(0xffffffffu, M, o));
       double s = 0.0;
-      for (int c = lane; c < C; c += 32) s += cs[c].s * exp((double)cs[c].m / a.T - M);
+      for (int c = lane; c < C; c += 32) s += cs[c].s * exp(fma((double)cs[c].m, invT, -M));
       s = warp_sum_d(s);
       if (lane == 0) { sM[r] = M; sS[r] = s; }
     }
@@ -210,7 +214,7 @@ __global__ void __launch_bounds__(32) k_acc_decide(AcceptArgs a) {
       bool keep = false;
       if (d >= 0 && d < a.V) {
         const double pd =
-            exp((double)a.z[((size_t)b * R + r) * a.V + d] / a.T - sM[r]) / sS[r];
+            exp(fma((double)a.z[((size_t)b * R + r) * a.V + d], 1.0 / a.T, -sM[r])) / sS[r];
         const double qv = a.qd[((size_t)b * (R - 1) + r) * a.V + d];
         keep = a.u_acc[(size_t)b * (R - 1) + r] * qv < pd;
       } else {
@@ -235,10 +239,12 @@ __global__ void __launch_bounds__(32) k_acc_decide(AcceptArgs a) {
 }
 
 // The target weight p_v and the residual weight max(p_v - q_v, 0) of token v.
-__device__ __forceinline__ void weights(const AcceptArgs& a, const AcceptDecision& D,
+// invT = 1 / T and inv_s = 1 / D.s are formed once per thread: a product within an ulp of
+// the quotient, far inside the decisions' rounding margin.
+__device__ __forceinline__ void weights(const AcceptDecision& D, double invT, double inv_s,
                                         const float* z, const double* q, int v, double* p,
                                         double* res) {
-  *p = exp((double)z[v] / a.T - D.M) / D.s;
+  *p = exp(fma((double)z[v], invT, -D.M)) * inv_s;
   if (D.mode == kModeResidual) {
     const double qv = q[v];
     *res = *p > qv ? *p - qv : 0.0;
@@ -260,6 +266,7 @@ __global__ void __launch_bounds__(kThreads) k_acc_part(AcceptArgs a) {
   pdl_wait();   // the decisions are complete
   pdl_trigger();
   const AcceptDecision D = a.dec[b];
+  const double invT = 1.0 / a.T, inv_s = 1.0 / D.s;
   const float* z = a.z + ((size_t)b * a.R + D.row) * a.V;
   const double* q =
       D.mode == kModeResidual ? a.qd + ((size_t)b * (a.R - 1) + D.row) * a.V : nullptr;
@@ -272,7 +279,7 @@ __global__ void __launch_bounds__(kThreads) k_acc_part(AcceptArgs a) {
     const int v = v0 + k * kThreads + (int)threadIdx.x;
     if (v < v1) {
       double p, r;
-      weights(a, D, z, q, v, &p, &r);
+      weights(D, invT, inv_s, z, q, v, &p, &r);
       sp += p;
       sr += r;
       if (p > 0.0) lp = v;
@@ -336,6 +343,7 @@ __global__ void __launch_bounds__(kThreads) k_acc_pick(AcceptArgs a) {
   __syncthreads();
   if (s_chunk >= 0) {
     const int c = s_chunk;
+    const double invT = 1.0 / a.T, inv_s = 1.0 / D.s;
     const float* z = a.z + ((size_t)b * a.R + D.row) * a.V;
     const double* q =
         D.mode == kModeResidual ? a.qd + ((size_t)b * (a.R - 1) + D.row) * a.V : nullptr;
@@ -345,7 +353,7 @@ __global__ void __launch_bounds__(kThreads) k_acc_pick(AcceptArgs a) {
     for (int k = 0; k < kPer; ++k) {
       const int v = v0 + k;
       double p = 0.0, r = 0.0;
-      if (v < v1) weights(a, D, z, q, v, &p, &r);
+      if (v < v1) weights(D, invT, inv_s, z, q, v, &p, &r);
       w[k] = s_use_res ? r : p;
       mine += w[k];
     }
