@@ -333,7 +333,7 @@ ds_status ds_q8_project(const ds_q8_tiled* w, int64_t rows, int32_t K, const uin
   if (!q8_plan(R, K, &S, &P, &smem)) return DS_ERR_UNSUPPORTED;
   if (!workspace || !aligned(workspace, 256) || ws_bytes < 256) return DS_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, 256, s) != cudaSuccess) return DS_ERR_CUDA;
+  // (the kernel resets the status word itself, so that consecutive projections overlap)
   return launch_q8_project(w->tiles, (int)rows, K, x, R, y, static_cast<uint32_t*>(workspace), s) ==
                  cudaSuccess
              ? DS_OK

@@ -162,7 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_q8_proj(const __grid_constant__
   }
   for (int i = tid; i < P; i += blockDim.x) s_cnt[i] = 0;
   __syncthreads();
+  pdl_trigger();   // the next grid may start launching (it waits for this one's outputs)
   if (warp == kWarps) {
+    // The weights do not come from the grid before this one (a programmatic launch): the
+    // ring fills while it finishes.
     // ------------------------------------------------------------- producer ------
     if (lane == 0) {
       const uint8_t* src = a.tiles + (size_t)u0 * Tk * kQ8TileBytes;
@@ -187,6 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_q8_proj(const __grid_constant__
   }
 
   // --------------------------------------------------------------- consumers -------
+  // The activations may come from the grid before this one: wait for it. The call's
+  // status word is reset here (a give-up is flagged only after a wait of about 1 s).
+  pdl_wait();
+  if (blockIdx.x == 0 && tid == 0) *a.status = 0u;
   // activations of verify row g, block b, lane q: (x[4q], x[4q+2]), (x[4q+1], x[4q+3]) of
   // the block's first 16 values, then the same for its last 16 (bf16 pairs); staged by the
   // consumer warps while the producer starts the weight stream
@@ -344,8 +351,8 @@ cudaError_t launch_q8_project(const void* tiles, int rows, int K, const uint16_t
   if (err != cudaSuccess) return err;
   int grid = device_sm_count();
   if (grid > rows / 16) grid = rows / 16;
-  k_q8_proj<<<grid, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  // a programmatic dependent of the grid before it: the weight stream starts early
+  return launch_pdl(k_q8_proj, dim3(grid), kThreads, smem, s, a);
 }
 
 }  // namespace dsmoe
