@@ -1250,17 +1250,21 @@ __device__ int ordered_take(int n, int need, Cls cls, Emit emit, int* s_eq, int*
 //     entries lie above it at 300k context), to two digits (the bucket's lower bound).
 //     Rows that fit the collection whole take tau = 0.
 //  2. collection: the entries whose upper bound reaches tau, in index order, with their
-//     bounds, and how many of them have a lower bound >= tau. Each warp walks a contiguous
-//     segment and keeps its matches in shared memory; the warps' lists are concatenated.
+//     bounds and block ids, and how many of them have a lower bound >= tau. Each warp walks
+//     a contiguous segment in two passes (the scores alone against a threshold per 32
+//     entries, then the exact bounds of the entries that pass) and keeps its matches in
+//     shared memory; the warps' lists are concatenated.
 //  3. If at least K lower bounds reach tau, the K-th largest lower bound T of the row is
 //     among the collected entries and so is every candidate (upper bound >= T). Otherwise
 //     (or on overflow) T and the candidates come from two passes over the whole row.
 //  4. Candidates whose lower bound exceeds H (below) are selected whatever the exact scores;
 //     the others are re-scored in the canonical order.
-//  5. The exact select among the candidates: threshold over their keys (the certain ones
-//     carry the largest key) and the ordered take, ties to the lowest index.
+//  5. The exact select among the candidates, ties to the lowest index: the uncertain ones
+//     sorted by (key, position) when at most one per thread remains, else a threshold over
+//     all candidates' keys (the certain ones carry the largest key); the ordered take.
 // With more candidates than the CTA keeps: canonical re-score of every admitted entry of
-// the row, then the canonical-mode path.
+// the row, then the canonical-mode path. At the end the row's scores (and, after the
+// layer's last row, the layer's key norms and union lists) are dropped from L2.
 // ---------------------------------------------------------------------------------
 struct TopkArgs {
   int R, Hh, N, K;
