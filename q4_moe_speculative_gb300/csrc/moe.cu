@@ -79,6 +79,21 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
       ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+// The same with an L2 eviction-priority hint: the weights are read once per call, so they
+// leave L2 first.
+__device__ __forceinline__ void bulk_copy_hint(void* dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
@@ -418,6 +433,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
     // ------------------------------------------------------------- producer ----------
     int slot = 0, f = 0;
     uint32_t phase = 0;    // ring cursor: stage f sits in `slot`, pass parity `phase`
+    const uint64_t wpol = l2_evict_first();   // weights: read once per call
     int n_union = -1;      // known once this CTA has built the route
     auto routed = [&]() {
       if (n_union < 0) {
@@ -479,8 +495,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
             const uint32_t bytes = (uint32_t)min(kGuCT, Tg - c * kGuCT) * kTile;
             s_meta[slot] = n;
             mbar_arrive_expect_tx(&full[slot], 2u * bytes);
-            bulk_copy(st, gb + off, bytes, &full[slot]);
-            bulk_copy(st + kGuCT * kTile, ub + off, bytes, &full[slot]);
+            bulk_copy_hint(st, gb + off, bytes, &full[slot], wpol);
+            bulk_copy_hint(st + kGuCT * kTile, ub + off, bytes, &full[slot], wpol);
           }
           __syncwarp();
           advance();
@@ -515,7 +531,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
             const uint32_t bytes = (uint32_t)(min(kDownKT, Td - c * kDownKT) * rig * kTile);
             s_meta[slot] = n;
             mbar_arrive_expect_tx(&full[slot], bytes);
-            bulk_copy(st, gbase + (size_t)c * kDownKT * rig * kTile, bytes, &full[slot]);
+            bulk_copy_hint(st, gbase + (size_t)c * kDownKT * rig * kTile, bytes, &full[slot], wpol);
           }
           __syncwarp();
           advance();
