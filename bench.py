@@ -37,9 +37,9 @@ import synth  # noqa: E402
 
 # Kernels one step launches: the MoE verify call (a prologue that zeroes the workspace
 # header, then one kernel: router, gate/up/SwiGLU, down projection, combine) and the
-# tensor-core select (compact, score, tau, collect, top-k, re-score, final select).
+# tensor-core select (compact, score, top-k).
 MOE_KERNELS = 2
-SELECT_KERNELS = 7
+SELECT_KERNELS = 3
 METRIC = "Q4 MoE verify weight GB/s (% of HBM peak) at R=1/6; top-512 select µs @300k ctx"
 UNIT = "GB/s"
 Q4_BYTES_PER_WEIGHT = 0.5625          # 4 bits + one fp16 scale per 32 values
