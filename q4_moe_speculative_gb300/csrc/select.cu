@@ -1366,6 +1366,29 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   uint32_t* const wbuf = r_key;                                    // [warp][3][kWarpBuf]
   uint32_t* const samp = reinterpret_cast<uint32_t*>(col_i);       // [2048]
 
+  // the row's queries as fp32 in the [i][head] layout (heads at qslot(h), heads past Hh
+  // zero) and its head weights
+  auto stage_queries = [&]() {
+    const int tid = threadIdx.x;
+    for (int i = tid; i < a.Hh; i += blockDim.x) wf[i] = a.hw[(size_t)blockIdx.x * a.Hh + i];
+    for (int i = a.Hh * 128 + tid; i < kScoreMaxHeads * 128; i += blockDim.x)
+      qf[(i & 127) * kScoreMaxHeads + qslot(i >> 7)] = 0.0f;
+    const uint16_t* qrow = a.q + (size_t)blockIdx.x * a.Hh * 128;
+    for (int i = tid; i < a.Hh * 128; i += blockDim.x)
+      qf[(i & 127) * kScoreMaxHeads + qslot(i >> 7)] = bf16_bits_to_f32(qrow[i]);
+    if (a.Hh <= 8) {
+      for (int w = tid; w < 4 * 128; w += blockDim.x) {
+        const int i = w & 127, t = w >> 7;   // value i of heads t (low half) and t + 4
+        const uint32_t lo = t < a.Hh ? qrow[t * 128 + i] : 0u;
+        const uint32_t hi = t + 4 < a.Hh ? qrow[(t + 4) * 128 + i] : 0u;
+        qb[((i >> 2) * 4 + t) * 4 + (i & 3)] = lo | (hi << 16);
+      }
+    }
+  };
+
+  // The queries are inputs of the call: staged (for the re-scores of tensor-core mode)
+  // while the scoring grid finishes.
+  if (a.tc_mode) stage_queries();
   pdl_wait();   // the scores and the compaction are complete
   pdl_trigger();
   if (threadIdx.x == 0) s_maxlo = 0u;
@@ -1405,25 +1428,6 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   uint32_t* s0 = a.sc0 + (size_t)lr * a.NS;
   const uint16_t* kbase = a.keys + (size_t)l * a.key_stride;
   bool canonical = !a.tc_mode;
-  // the row's queries as fp32 in the [i][head] layout (heads at qslot(h), heads past Hh
-  // zero) and its head weights
-  auto stage_queries = [&]() {
-    for (int i = tid; i < a.Hh; i += blockDim.x) wf[i] = a.hw[(size_t)lr * a.Hh + i];
-    for (int i = a.Hh * 128 + tid; i < kScoreMaxHeads * 128; i += blockDim.x)
-      qf[(i & 127) * kScoreMaxHeads + qslot(i >> 7)] = 0.0f;
-    const uint16_t* qrow = a.q + (size_t)lr * a.Hh * 128;
-    for (int i = tid; i < a.Hh * 128; i += blockDim.x)
-      qf[(i & 127) * kScoreMaxHeads + qslot(i >> 7)] = bf16_bits_to_f32(qrow[i]);
-    if (a.Hh <= 8) {
-      for (int w = tid; w < 4 * 128; w += blockDim.x) {
-        const int i = w & 127, t = w >> 7;   // value i of heads t (low half) and t + 4
-        const uint32_t lo = t < a.Hh ? qrow[t * 128 + i] : 0u;
-        const uint32_t hi = t + 4 < a.Hh ? qrow[(t + 4) * 128 + i] : 0u;
-        qb[((i >> 2) * 4 + t) * 4 + (i & 3)] = lo | (hi << 16);
-      }
-    }
-  };
-
   if (a.tc_mode) {
     const float* kn = a.knorm + (size_t)l * a.NS;
     const float G = a.qnorm[lr];   // eps per unit key norm
@@ -1685,7 +1689,6 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
             asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(kp + 128));
           }
         }
-        stage_queries();
         __syncthreads();
         mu = s_misc[0];
         uint8_t* const stg = reinterpret_cast<uint8_t*>(col_i);
@@ -1816,7 +1819,6 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       return;
     }
     // Too many candidates (e.g. heavy ties): canonical scores for the whole row.
-    stage_queries();
     __syncthreads();
     for (int i = tid; i < n; i += blockDim.x) {
       const bool adm = s0[i] != kMinusInfBits;
