@@ -231,6 +231,7 @@ ds_status ds_select_blocks_marked(const ds_select_args* a, int32_t* sel, int32_t
   ws.knorm = reinterpret_cast<float*>(base + L.knorm);
   ws.kmax = reinterpret_cast<float*>(base + L.kmax);
   ws.qnorm = reinterpret_cast<float*>(base + L.qnorm);
+  ws.smax = reinterpret_cast<float*>(base + L.smax);
   const bool tc = !(a->flags & DS_SELECT_CANONICAL_SCORES) &&
                   tc_scoring_supported(d, a->keys, a->q);
 

@@ -85,6 +85,8 @@ struct SelWorkspace {
   float* kmax;        // [L][NC] the largest knorm of each 32 union entries (NC = NS / 32
                       // rounded up; tensor-core scoring)
   float* qnorm;       // [L][R] sum_h |w_h| ||q_h|| bound (tensor-core scoring)
+  float* smax;        // [L][NC][R] per 32 union entries, the largest score each row gives
+                      // them (-inf: none admitted; tensor-core scoring)
 };
 
 // Row stride of the score arrays (cscore, knorm): N rounded up to a multiple of 32, so that
@@ -95,7 +97,7 @@ inline int chunk_stride(int N) { return (score_stride(N) + 31) / 32; }
 
 struct SelLayout {
   size_t header, uagg, ldone, zero_bytes, wordoff, cidx, ccount, uidx, ucount, urows, cscore, knorm,
-      kmax, qnorm, total;
+      kmax, qnorm, smax, total;
 };
 SelLayout sel_layout(const SelDims& d, bool caller_cidx);
 bool tc_scoring_supported(const SelDims& d, const uint16_t* keys, const uint16_t* q);

@@ -155,6 +155,23 @@ __device__ __forceinline__ uint32_t tc_hi(uint32_t sbits, float kn, float G) {
   return score_key(__fadd_ru(__uint_as_float(sbits), __fmul_ru(kn, G)));
 }
 
+// Max over the warp of eight values per lane, reduce-scatter style (nine shuffles): lane L
+// ends with the maximum of value 4 b4 + 2 b3 + b2 (b = the bits of L) over all lanes.
+__device__ __forceinline__ float warp_max8(const float (&v)[8]) {
+  const int lane = threadIdx.x & 31;
+  float a[4], b[2];
+  const bool h4 = lane & 16, h3 = lane & 8, h2 = lane & 4;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)   // keep values 4 h4 + j, send the partner's half
+    a[j] = fmaxf(h4 ? v[4 + j] : v[j], __shfl_xor_sync(0xffffffffu, h4 ? v[j] : v[4 + j], 16));
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+    b[j] = fmaxf(h3 ? a[2 + j] : a[j], __shfl_xor_sync(0xffffffffu, h3 ? a[j] : a[2 + j], 8));
+  float c = fmaxf(h2 ? b[1] : b[0], __shfl_xor_sync(0xffffffffu, h2 ? b[0] : b[1], 4));
+  c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, 2));
+  return fmaxf(c, __shfl_xor_sync(0xffffffffu, c, 1));
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -405,6 +422,8 @@ struct ScoreArgs {
   CUtensorMap kmap;   // keys [L][N][128] bf16, boxes of 64 values x 128 blocks, 128B swizzle
   int NS;             // row stride of sc0 / knorm (N rounded up to a multiple of 4)
   int NC;             // row stride of kmax
+  float* smax;        // [L][NC][R] per 32 union entries, each row's largest score
+                      // (-inf: none admitted; tensor-core mode)
 };
 
 // ---------------------------------------------------------------------------------
@@ -976,47 +995,69 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
       for (int c = 0; c < NCH; ++c) sm100::tmem_ld16(lane_base + (uint32_t)(c * 16), d + c * 16);
       sm100::tc_fence_before();   // the group barrier of the next tile orders the next MMA
       const int e = e0 + row;
-      {
-        // the largest key norm bound of this warp's 32 entries (a tile starts at a multiple
-        // of 128 entries): K7's first test takes it in place of each entry's own
-        const float kc = warp_max(e < ucnt ? kn : 0.0f);
-        if (lane == 0 && e < ucnt) st_hint(a.kmax + (size_t)l * a.NC + (e >> 5), kc, spol);
-      }
-      if (e < ucnt) {
-        // row r's tensor-core score; its interval comes from kn and the row's scale
-        // (tc_lo / tc_hi) wherever it is used
-        st_hint(a.knorm + (size_t)l * a.NS + e, kn, spol);
-        auto emit = [&](int r, float sc) {
-          const size_t out = ((size_t)l * R + r) * a.NS + e;
-          st_hint(a.sc0 + out, (rows & (1u << r)) ? __float_as_uint(sc) : kMinusInfBits, spol);
-        };
-        if constexpr (HH > 0) {   // head count known at compile time: static indices
+      // Per row: the score (every lane forms it; keys past the layer's union are zero
+      // rows), stored for the entries of the union. Per chunk of 32 entries (this warp's;
+      // a tile starts at a multiple of 128 entries): the largest key norm bound kc, which
+      // K7's first test takes in place of each entry's own, and per row the largest
+      // admitted score (-inf: none), which with kc bounds the chunk's intervals for K7's
+      // threshold and first test. The chunk's values leave in one store (lane r < R: row
+      // r's maximum, lane R: kc), next to the gather's copies in the memory pipe.
+      const bool live = e < ucnt;
+      const bool chunk_live = e0 + (warp & 3) * 32 < ucnt;   // warp-uniform
+      if (live) st_hint(a.knorm + (size_t)l * a.NS + e, kn, spol);
+      auto emit = [&](int r, float sc) {
+        const bool adm = live && (rows & (1u << r));
+        if (live)
+          st_hint(a.sc0 + ((size_t)l * R + r) * a.NS + e,
+                  adm ? __float_as_uint(sc) : kMinusInfBits, spol);
+        return adm ? sc : -INFINITY;
+      };
+      const size_t cidx = (size_t)l * a.NC + (e0 >> 5) + (warp & 3);   // the chunk
+      if constexpr (HH > 0) {   // head count known at compile time: static indices
+        constexpr int NR = NPAD / HH < 8 ? NPAD / HH : 8;
+        // values 0 .. R-1: the rows' scores, value R (R < 8): kn; reduced together
+        float v[8];
 #pragma unroll
-          for (int r = 0; r < NPAD / HH; ++r) {
-            if (r < R) {
-              float sc = 0.0f;
+        for (int r = 0; r < 8; ++r) v[r] = -INFINITY;
 #pragma unroll
-              for (int h = 0; h < HH; ++h) {
-                const float v = d[r * HH + h];
-                sc = __fmaf_rn(s_wg[g][r * HH + h], v > 0.0f ? v : 0.0f, sc);
-              }
-              emit(r, sc);
-            }
-          }
-        } else {                  // any head count: each row picks its columns by predicate
-#pragma unroll 1
-          for (int r = 0; r < R; ++r) {
-            const int p0 = r * Hh, p1 = p0 + Hh;
+        for (int r = 0; r < NR; ++r) {
+          if (r < R) {
             float sc = 0.0f;
 #pragma unroll
-            for (int p = 0; p < NPAD; ++p) {
-              const float v = d[p];
-              const float t = __fmaf_rn(s_wg[g][p], v > 0.0f ? v : 0.0f, sc);
-              sc = (p >= p0 && p < p1) ? t : sc;
+            for (int h = 0; h < HH; ++h) {
+              const float x = d[r * HH + h];
+              sc = __fmaf_rn(s_wg[g][r * HH + h], x > 0.0f ? x : 0.0f, sc);
             }
-            emit(r, sc);
+            v[r] = emit(r, sc);
           }
         }
+        const float knv = live ? kn : 0.0f;
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r == R) v[r] = knv;
+        const float kc8 = R < 8 ? 0.0f : warp_max(knv);
+        const float mine = warp_max8(v);
+        const int slot = (lane >> 2) & 7;   // the value this lane holds: 4 b4 + 2 b3 + b2
+        const int which = (lane & 3) == 0 ? slot : 8;
+        if (chunk_live && which < R) st_hint(a.smax + cidx * R + which, mine, spol);
+        if (chunk_live && (R < 8 ? which == R : lane == 0))
+          st_hint(a.kmax + cidx, R < 8 ? mine : kc8, spol);
+      } else {                  // any head count: each row picks its columns by predicate
+        float mine = warp_max(live ? kn : 0.0f);   // lane r < R: row r's largest; lane R: kc
+#pragma unroll 1
+        for (int r = 0; r < R; ++r) {
+          const int p0 = r * Hh, p1 = p0 + Hh;
+          float sc = 0.0f;
+#pragma unroll
+          for (int p = 0; p < NPAD; ++p) {
+            const float x = d[p];
+            const float t = __fmaf_rn(s_wg[g][p], x > 0.0f ? x : 0.0f, sc);
+            sc = (p >= p0 && p < p1) ? t : sc;
+          }
+          const float mx = warp_max(emit(r, sc));
+          if (lane == r) mine = mx;
+        }
+        if (chunk_live && lane <= R) st_hint(lane < R ? a.smax + cidx * R + lane : a.kmax + cidx, mine, spol);
       }
     }
     // MMAs issued but never observed complete: wait (bounded) before TMEM is freed
@@ -1289,6 +1330,8 @@ struct TopkArgs {
   uint32_t* ldone;    // [L] rows done per layer
   const uint8_t* urows;
   int keep;           // leave the scores, key norms and union lists in the workspace
+  const float* smax;  // [L][NC][R] per 32 union entries, each row's largest score
+                      // (-inf: none admitted; tensor-core mode)
 };
 
 // Drops the 128-byte lines that lie wholly inside [p, p + bytes) from L2 without writing
@@ -1410,6 +1453,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
     __syncthreads();
     if (s_misc[0]) {
       discard_lines(a.knorm + (size_t)l * a.NS, sizeof(float) * (size_t)a.NS);
+      if (a.tc_mode) discard_lines(a.smax + (size_t)l * a.NC * a.R, sizeof(float) * a.NC * a.R);
       discard_lines(a.uidx + (size_t)l * a.N, sizeof(int32_t) * (size_t)a.N);
       discard_lines(a.urows + (size_t)l * a.N, (size_t)a.N);
     }
@@ -1431,9 +1475,43 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   if (a.tc_mode) {
     const float* kn = a.knorm + (size_t)l * a.NS;
     const float G = a.qnorm[lr];   // eps per unit key norm
-    // ---- 1. tau
+    // ---- 1. tau: a key that (at least, or very likely) K lower bounds of the row reach.
+    // Each chunk of 32 entries carries its largest score smax (K5) and largest key norm
+    // bound kc, so the entry holding smax has a lower bound of at least
+    // v = RD(smax - RU(kc G)) (its own kn is at most kc). At least K chunks, each through
+    // one of its entries, reach the K-th largest v, so that value, or a lower one (its
+    // first two radix digits), is a tau. When fewer than K chunks hold an admitted entry
+    // it is zero; a sample of the entries' lower bounds then estimates one (rank a little
+    // above K; the collection checks the count).
     uint32_t tau = 0u;
-    if (n > kCollectCap) {
+    const int nc = (n + 31) >> 5;
+    const float* kc_row = a.kmax + (size_t)l * a.NC;
+    // smax of chunk c for this row: sm_row[c * R]
+    const uint32_t* sm_row =
+        reinterpret_cast<const uint32_t*>(a.smax) + (size_t)l * a.NC * a.R + (lr - l * a.R);
+    if (n > kCollectCap && nc >= K) {
+      int need;
+      if (nc <= kCollectCap) {
+        constexpr int kPer = kCollectCap / kTopkThreads;
+        uint32_t sv[kPer];
+        float kv[kPer];
+#pragma unroll
+        for (int t = 0; t < kPer; ++t) {   // every load in flight, then the stores
+          const int c = tid + t * kTopkThreads;
+          sv[t] = c < nc ? sm_row[(size_t)c * a.R] : kMinusInfBits;
+          kv[t] = c < nc ? kc_row[c] : 0.0f;
+        }
+#pragma unroll
+        for (int t = 0; t < kPer; ++t) samp[tid + t * kTopkThreads] = tc_lo(sv[t], kv[t], G);
+        __syncthreads();
+        tau = radix_threshold(nc, K, [&](int c) { return samp[c]; }, hist, scratch, nullptr,
+                              s_misc, a.status, &need, 2);
+      } else {
+        tau = radix_threshold(nc, K, [&](int c) { return tc_lo(sm_row[(size_t)c * a.R], kc_row[c], G); },
+                              hist, scratch, nullptr, s_misc, a.status, &need, 2);
+      }
+    }
+    if (n > kCollectCap && tau == 0u) {
       constexpr int kChunks = 64, kS = kChunks * 32;
       const int spacing = n / kChunks;
       static_assert(kS % kTopkThreads == 0, "whole sample rounds");
@@ -1458,8 +1536,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
     // ---- 2. collection, in two passes per warp. Each warp walks a contiguous segment
     // (starting at a multiple of 128 entries); entries past `end` in the last group lie
     // inside the row's padded stride and are masked.
-    //   Pass 1 reads only the scores: lane L takes 16 consecutive entries of a batch of
-    // 512 (four 16-byte loads, the next batch in flight) and keeps those with s >= theta,
+    //   Pass 1 reads only the chunks' largest upper bounds and, in the chunks where one
+    // reaches tau, the scores: 16 consecutive entries per lane, and keeps those with
+    // s >= theta,
     // theta = RD(RD(t* - A) - RU(2^-22 |t*| + 2^-126)), A = RU(kc G), where kc >= kn is the
     // largest key norm bound of the entry's 32 and t* the smallest score whose key reaches
     // tau. This keeps every entry the exact test takes: if RU(z) >= t* for
@@ -1480,7 +1559,6 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
       uint32_t* const b_i = wbuf + (size_t)warp * 3 * kWarpBuf;
       uint32_t* const b_lo = b_i + kWarpBuf;
       uint32_t* const b_hi = b_lo + kWarpBuf;
-      const float* kc_row = a.kmax + (size_t)l * a.NC;
       const bool take_all = tau <= 0x007FFFFFu;
       const float tstar = key_score(tau);
       const unsigned lt = (1u << lane) - 1u;
@@ -1491,53 +1569,65 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
         const float mt = __fmaf_ru(0.0000002384185791015625f, fabsf(tstar), 1.17549435e-38f);
         const uint32_t all16 = take_all ? 0xFFFFu : 0u;
         const uint4 kNone = make_uint4(kMinusInfBits, kMinusInfBits, kMinusInfBits, kMinusInfBits);
-        // lane L takes entries g + 16 L .. g + 16 L + 15 of a batch of 512 (four 16-byte
-        // loads; their 32-entry chunk is one kc)
-        auto load = [&](int g, uint4* v, float& k) {
-          const int i = g + 16 * lane;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = i + 4 * j < end ? ld_hint_v4(s0 + i + 4 * j, rpol) : kNone;
-          k = i < end ? kc_row[i >> 5] : 0.0f;
-        };
-        uint4 sv[4];
-        float kc;
-        load(beg, sv, kc);
-        for (int g0 = beg; g0 < end; g0 += 512) {
-          uint4 sn[4];
-          float kx;
-          load(g0 + 512, sn, kx);
-          const int i = g0 + 16 * lane;
-          const float th = __fsub_rd(__fsub_rd(tstar, __fmul_ru(kc, G)), mt);
-          uint32_t pm = all16;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            pm |= __uint_as_float(sv[j].x) >= th ? 1u << (4 * j) : 0u;
-            pm |= __uint_as_float(sv[j].y) >= th ? 2u << (4 * j) : 0u;
-            pm |= __uint_as_float(sv[j].z) >= th ? 4u << (4 * j) : 0u;
-            pm |= __uint_as_float(sv[j].w) >= th ? 8u << (4 * j) : 0u;
+        // The chunks of 32 entries (one kc each) where an entry passes, i.e. whose largest
+        // score reaches theta (all of them when every entry is taken), are listed in order,
+        // 32 chunks at a time (the next 32 chunks' smax and kc in flight); lane L then takes
+        // half L & 1 (16 consecutive entries, four 16-byte loads) of listed chunk L >> 1,
+        // 16 listed chunks per batch.
+        uint32_t* const clist = b_lo;   // free until the second pass
+        const int cbeg = beg >> 5, cend = beg < end ? (end + 31) >> 5 : cbeg;   // none: empty
+        float hs = cbeg + lane < cend ? __uint_as_float(sm_row[(size_t)(cbeg + lane) * a.R]) : -INFINITY;
+        float hk = cbeg + lane < cend ? kc_row[cbeg + lane] : 0.0f;
+        for (int c0 = cbeg; c0 < cend; c0 += 32) {
+          const int c = c0 + lane;
+          const bool cp = c < cend &&
+                          (take_all || hs >= __fsub_rd(__fsub_rd(tstar, __fmul_ru(hk, G)), mt));
+          if (c0 + 32 < cend) {
+            hs = c + 32 < cend ? __uint_as_float(sm_row[(size_t)(c + 32) * a.R]) : -INFINITY;
+            hk = c + 32 < cend ? kc_row[c + 32] : 0.0f;
           }
-          const int lim = end - i;   // entries of this lane inside the segment
-          pm &= lim >= 16 ? 0xFFFFu : (lim > 0 ? (1u << lim) - 1u : 0u);
-          if (__ballot_sync(0xffffffffu, pm != 0u)) {
-            const int c = __popc(pm);   // 0..16: five bit slices
-            int p = c1, tot = 0;
+          const unsigned M = __ballot_sync(0xffffffffu, cp);
+          if (cp) clist[__popc(M & lt)] = (uint32_t)c;
+          __syncwarp();
+          const int np = __popc(M);
+          for (int j0 = 0; j0 < np; j0 += 16) {
+            const int j = j0 + (lane >> 1);
+            const int cc = j < np ? (int)clist[j] : -1;
+            const int i = cc * 32 + 16 * (lane & 1);
+            const int lim = cc < 0 ? 0 : end - i;   // entries of this lane inside the segment
+            uint4 sv[4];
 #pragma unroll
-            for (int bit = 0; bit < 5; ++bit) {
-              const unsigned sl = __ballot_sync(0xffffffffu, (c >> bit) & 1);
-              p += __popc(sl & lt) << bit;
-              tot += __popc(sl) << bit;
+            for (int q = 0; q < 4; ++q) sv[q] = 4 * q < lim ? ld_hint_v4(s0 + i + 4 * q, rpol) : kNone;
+            const float kc = cc >= 0 ? kc_row[cc] : 0.0f;
+            const float th = __fsub_rd(__fsub_rd(tstar, __fmul_ru(kc, G)), mt);
+            uint32_t pm = all16;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              pm |= __uint_as_float(sv[q].x) >= th ? 1u << (4 * q) : 0u;
+              pm |= __uint_as_float(sv[q].y) >= th ? 2u << (4 * q) : 0u;
+              pm |= __uint_as_float(sv[q].z) >= th ? 4u << (4 * q) : 0u;
+              pm |= __uint_as_float(sv[q].w) >= th ? 8u << (4 * q) : 0u;
             }
-            while (pm) {
-              const int e = __ffs(pm) - 1;
-              pm &= pm - 1u;
-              if (p < kWarpBuf) b_i[p] = (uint32_t)(i + e);
-              ++p;
+            pm &= lim >= 16 ? 0xFFFFu : (lim > 0 ? (1u << lim) - 1u : 0u);
+            if (__ballot_sync(0xffffffffu, pm != 0u)) {
+              const int cn = __popc(pm);   // 0..16: five bit slices
+              int p = c1, tot = 0;
+#pragma unroll
+              for (int bit = 0; bit < 5; ++bit) {
+                const unsigned sl = __ballot_sync(0xffffffffu, (cn >> bit) & 1);
+                p += __popc(sl & lt) << bit;
+                tot += __popc(sl) << bit;
+              }
+              while (pm) {
+                const int e = __ffs(pm) - 1;
+                pm &= pm - 1u;
+                if (p < kWarpBuf) b_i[p] = (uint32_t)(i + e);
+                ++p;
+              }
+              c1 += tot;
             }
-            c1 += tot;
           }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) sv[j] = sn[j];
-          kc = kx;
+          __syncwarp();   // the list is rewritten by the next step
         }
       }
       __syncwarp();
@@ -1890,6 +1980,7 @@ SelLayout sel_layout(const SelDims& d, bool caller_cidx) {
   L.knorm = off; off += up(sizeof(float) * (size_t)d.L * score_stride(d.N));
   L.kmax = off; off += up(sizeof(float) * (size_t)d.L * chunk_stride(d.N));
   L.qnorm = off; off += up(sizeof(float) * LR);
+  L.smax = off; off += up(sizeof(float) * LR * (size_t)chunk_stride(d.N));
   L.total = off;
   return L;
 }
@@ -1918,6 +2009,7 @@ cudaError_t launch_score(const SelDims& d, const uint16_t* keys, const uint16_t*
               ws.qnorm, ws.kmax, ws.header};
   a.NS = score_stride(d.N);
   a.NC = chunk_stride(d.N);
+  a.smax = ws.smax;
   if (!tc) {
     const int RH = d.R * d.Hh;
     const size_t smem = sizeof(float) * ((size_t)RH * 128 + ((RH + 3) & ~3)) +
@@ -1964,6 +2056,7 @@ cudaError_t launch_topk(const SelDims& d, const uint16_t* keys, const uint16_t* 
   a.ldone = ws.ldone;
   a.urows = ws.urows;
   a.keep = keep ? 1 : 0;
+  a.smax = ws.smax;
   cudaError_t err =
       cudaFuncSetAttribute(k7_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
   if (err != cudaSuccess) return err;
