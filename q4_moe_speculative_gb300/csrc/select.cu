@@ -1111,7 +1111,8 @@ __device__ __forceinline__ void hist_pass(int n, bool resid, const uint32_t* r_k
         k[u] = i < end ? key_at(i) : 0u;
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) add(k[u], i0 + u * 32 + lane < end);
+      for (int u = 0; u < U; ++u)   // (warp-uniform) groups past the segment are skipped
+        if (i0 + u * 32 < end) add(k[u], i0 + u * 32 + lane < end);
     }
   }
 }
@@ -1243,7 +1244,8 @@ __device__ int ordered_take(int n, int need, Cls cls, Emit emit, int* s_eq, int*
       c[u] = i < end ? cls(i) : 0;        // 2 = greater, 1 = equal, 0 = below
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int u = 0; u < U; ++u) {   // (warp-uniform) groups past the segment are skipped
+      if (i0 + u * 32 >= end) break;
       gt_w += __popc(__ballot_sync(0xffffffffu, c[u] == 2));
       eq_w += __popc(__ballot_sync(0xffffffffu, c[u] == 1));
     }
@@ -1266,6 +1268,7 @@ __device__ int ordered_take(int n, int need, Cls cls, Emit emit, int* s_eq, int*
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
+      if (i0 + u * 32 >= end) break;
       const int i = i0 + u * 32 + lane;
       const uint32_t eqm = __ballot_sync(0xffffffffu, c[u] == 1);
       const int eq_rank = eq_seen + __popc(eqm & ((1u << lane) - 1u));
@@ -1285,15 +1288,16 @@ __device__ int ordered_take(int n, int need, Cls cls, Emit emit, int* s_eq, int*
 // entries (entries the row does not admit carry the sentinel and never qualify).
 // Canonical mode: threshold and ordered take over the canonical scores.
 // Tensor-core mode, all inside the CTA:
-//  1. tau, a collection threshold at or below the K-th largest lower bound: from a sample
-//     of 2048 entries (64 chunks of 32, evenly spaced), the key of the sample's rank-th
-//     largest lower bound, rank = K scaled to the sample plus 16 (about 800 of the row's
-//     entries lie above it at 300k context), to two digits (the bucket's lower bound).
-//     Rows that fit the collection whole take tau = 0.
+//  1. tau, a collection threshold at or below the K-th largest lower bound: the K-th largest
+//     of the per-chunk bounds RD(smax - RU(kc G)) (each reached by a lower bound in its
+//     chunk), to two digits (the bucket's lower bound); when fewer than K chunks hold an
+//     admitted entry, from a sample of 2048 entries (64 chunks of 32, evenly spaced) at
+//     rank K scaled to the sample plus 16. Rows that fit the collection whole take tau = 0.
 //  2. collection: the entries whose upper bound reaches tau, in index order, with their
 //     bounds and block ids, and how many of them have a lower bound >= tau. Each warp walks
 //     a contiguous segment in two passes (the scores alone against a threshold per 32
-//     entries, then the exact bounds of the entries that pass) and keeps its matches in
+//     entries, in the chunks whose largest score reaches it; then the exact bounds of the
+//     entries that pass) and keeps its matches in
 //     shared memory; the warps' lists are concatenated.
 //  3. If at least K lower bounds reach tau, the K-th largest lower bound T of the row is
 //     among the collected entries and so is every candidate (upper bound >= T). Otherwise
@@ -1438,7 +1442,11 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
   const int lr = blockIdx.x;
   const int l = lr / a.R;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the row's admitted count, the layer's union count and the row's interval scale, loaded
+  // together
   const int count = a.ccount[lr];
+  const int n = a.ucount[l];
+  const float G = a.tc_mode ? a.qnorm[lr] : 0.0f;   // eps per unit key norm
   const int K = a.K;
   int32_t* out = a.sel + (size_t)lr * K;
   // At the end of the row: its scores are dead, and once the layer's last row is done, so
@@ -1467,14 +1475,12 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k7_topk(TopkArgs a) {
     return;
   }
 
-  const int n = a.ucount[l];
   const int32_t* ui = a.uidx + (size_t)l * a.N;
   uint32_t* s0 = a.sc0 + (size_t)lr * a.NS;
   const uint16_t* kbase = a.keys + (size_t)l * a.key_stride;
   bool canonical = !a.tc_mode;
   if (a.tc_mode) {
     const float* kn = a.knorm + (size_t)l * a.NS;
-    const float G = a.qnorm[lr];   // eps per unit key norm
     // ---- 1. tau: a key that (at least, or very likely) K lower bounds of the row reach.
     // Each chunk of 32 entries carries its largest score smax (K5) and largest key norm
     // bound kc, so the entry holding smax has a lower bound of at least
