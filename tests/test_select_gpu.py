@@ -214,6 +214,31 @@ def test_mixed_density_and_empty_layers(dsm, canonical):
     assert np.all(dev[1][1] == 0)
 
 
+def test_chunk_threshold_paths(dsm):
+    # Rows long enough (at least K chunks of 32 union entries) that the top-k takes its
+    # collection threshold from the per-chunk score maxima. Layer 0: row 0 admits one
+    # window of 3000 blocks (fewer than K chunks hold an admitted entry: the sampled
+    # threshold), row 1 70%, row 2 every block; layer 1: 5% per row (most chunks hold one
+    # or two admitted entries); layer 2: a shared 70% mask with a causal limit inside a
+    # chunk on row 2.
+    shape = synth.SelectShape(L=3, R=3, Hh=8, N=40000, topk=512)
+    inp = synth.select_inputs(shape, seed=31, shared_mask=False)
+    rng = np.random.default_rng(31)
+    N = shape.N
+    bits = np.zeros((3, 3, N), bool)
+    bits[0, 0, 20000:23000] = True
+    bits[0, 1] = rng.random(N) < 0.7
+    bits[0, 2] = True
+    bits[1] = rng.random((3, N)) < 0.05
+    bits[2] = (rng.random(N) < 0.7)[None, :]
+    limit = np.full((3, 3), N, dtype=np.int32)
+    limit[2, 2] = 30017
+    inp["mask"] = torch.from_numpy(synth.pack_bits(bits).view(np.int32).copy())
+    inp["limit"] = torch.from_numpy(limit)
+    dev, _ = check(dsm, inp, shape.topk)
+    assert np.all(dev[1] == shape.topk)
+
+
 @pytest.mark.parametrize("canonical", [False, True])
 def test_twelve_heads_odd_block_count(dsm, canonical):
     # Hh = 12 (the generic scoring and re-score paths), 3 rows, an odd block count (score
