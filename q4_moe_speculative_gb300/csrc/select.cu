@@ -14,8 +14,8 @@
 //      position [layer][row][entry]. Rows that do not admit an entry get a sentinel that
 //      sorts below every score.
 //  K7  per (layer, row): bounded radix top-k over the union entries, in one CTA (tensor-core
-//      mode: sampled threshold, collection, candidates, canonical re-score of the uncertain
-//      ones, final select).
+//      mode: a collection threshold from per-chunk maxima, collection, candidates, canonical
+//      re-score of the uncertain ones, final select).
 //
 // Two scoring modes give the same selection:
 //  * canonical: every score in the canonical fp32 order (fmaf over i ascending, then over
@@ -31,7 +31,8 @@
 //    that sum per group (far more than the hardware loses) stay below 2^-16 of it. The
 //    two sums over the heads add 2 x 8 roundings of terms below |w_h| ||q_h|| ||k|| (2^-20).
 //    In all at most 2^-15.2 of ||k|| sum_h |w_h| ||q_h||, so 2^-13 leaves a margin above 4.
-//    K5 stores s_tc per admitting row and ||k|| per entry; every consumer derives [lo, hi]
+//    K5 stores s_tc per admitting row and ||k|| per entry (and, per 32 entries, the largest
+//    ||k|| and each row's largest s_tc); every consumer derives [lo, hi]
 //    with the same function (tc_lo / tc_hi), so the bounds agree bit for bit. K7 takes
 //    T = k-th largest lo; every block of the canonical top-k has hi >= T, so only the
 //    candidates with hi >= T are re-scored in the canonical order and selected among
@@ -50,7 +51,7 @@ constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kResidCap = 4096;      // residual radix bucket kept in shared memory
 constexpr int kCandCap = 4096;       // re-score candidates kept in shared memory
-constexpr int kCollectCap = 4096;    // entries collected by the sampled-threshold pass
+constexpr int kCollectCap = 4096;    // entries the threshold-tau collection keeps
 constexpr uint32_t kWaitPolls = 1u << 17;   // bounded mbarrier polling (<= ~0.13 s)
 constexpr float kEpsRel = 0.0001220703125f;  // 2^-13
 constexpr uint32_t kNoScoreKey = 0u;        // sorts below the key of every score
