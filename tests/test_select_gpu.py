@@ -126,6 +126,15 @@ def test_many_heads_and_rows(dsm):
     check(dsm, inp, shape.topk)
 
 
+def test_eight_rows_eight_heads_long_rows(dsm):
+    # R = 8 at 8 heads (the static epilogue with every row slot used: the key-norm bound of
+    # each 32 entries takes its own reduction), rows long enough for the chunk-maxima
+    # threshold and the chunk-level first test
+    shape = synth.SelectShape(L=2, R=8, Hh=8, N=30000, topk=512)
+    inp = synth.select_inputs(shape, seed=14, shared_mask=False)
+    check(dsm, inp, shape.topk)
+
+
 def test_candidate_band_overflow_falls_back(dsm):
     # keys in 3 distinct values: thousands of near-equal tensor-core scores around the
     # threshold overflow the candidate bound; the row is re-scored canonically.
