@@ -504,6 +504,25 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
       } else {
         const int m = n - NG, u = m / NGR, rg = m - u * NGR;
         const int hb = dn & 1;
+        const int rig = min(kGroupRows, RTd - rg * kGroupRows);   // tile rows in the group
+        const uint8_t* gbase = (u > 0 ? a.down + (size_t)u_expert[u - 1] * dn_expert : a.sh_down) +
+                               (size_t)rg * kGroupRows * Td * kTile;
+        auto issue = [&](int c) {
+          uint8_t* st = next_slot();
+          if (lane == 0) {
+            const uint32_t bytes = (uint32_t)(min(kDownKT, Td - c * kDownKT) * rig * kTile);
+            s_meta[slot] = n;
+            mbar_arrive_expect_tx(&full[slot], bytes);
+            bulk_copy_hint(st, gbase + (size_t)c * kDownKT * rig * kTile, bytes, &full[slot], wpol);
+          }
+          __syncwarp();
+          advance();
+        };
+        // The unit's first `ring` stages need no h: their weights are on their way while
+        // the expert's gate/up units finish (each takes a slot that an earlier unit's stage
+        // frees, so none waits on this unit's h).
+        const int pre = min(KCd, ring);
+        for (int c = 0; c < pre; ++c) issue(c);
         if (lane == 0) {
           // h of the expert's rows, once every gate/up unit of the expert is counted and
           // the buffer's previous unit is done; h is stored in MMA pair order
@@ -522,20 +541,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(const MoeArgs a) {
         }
         __syncwarp();
         ++dn;
-        const int rig = min(kGroupRows, RTd - rg * kGroupRows);   // tile rows in the group
-        const uint8_t* gbase = (u > 0 ? a.down + (size_t)u_expert[u - 1] * dn_expert : a.sh_down) +
-                               (size_t)rg * kGroupRows * Td * kTile;
-        for (int c = 0; c < KCd; ++c) {
-          uint8_t* st = next_slot();
-          if (lane == 0) {
-            const uint32_t bytes = (uint32_t)(min(kDownKT, Td - c * kDownKT) * rig * kTile);
-            s_meta[slot] = n;
-            mbar_arrive_expect_tx(&full[slot], bytes);
-            bulk_copy_hint(st, gbase + (size_t)c * kDownKT * rig * kTile, bytes, &full[slot], wpol);
-          }
-          __syncwarp();
-          advance();
-        }
+        for (int c = pre; c < KCd; ++c) issue(c);
       }
     }
   } else if (warp < kProducerWarp) {
