@@ -571,8 +571,8 @@ __device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, b
 //    memory beside the stage, so the epilogue reads nothing from global memory. Producer
 //    warp 0 also stages each layer's queries (one of two slots, by layer parity) with their
 //    norm bounds and head weights;
-//  * two epilogue groups of 4 warps take alternate tiles; each has its own TMEM
-//    accumulator. The group's first thread issues the 8 tcgen05.mma (M = 128 keys,
+//  * three epilogue groups of 4 warps (two when N > 64) take the tiles in turn; each has
+//    its own TMEM accumulator. The group's first thread issues the 8 tcgen05.mma (M = 128 keys,
 //    N = NPAD >= R*Hh, K = 16 each) and commits to the group's mbarrier; each warp then
 //    reads its 32 lanes (one key per thread), writes the score for every admitting row and
 //    the key's norm bound, and releases the stage on its `empty` barrier.
@@ -582,22 +582,25 @@ __device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, b
 // ---------------------------------------------------------------------------------
 constexpr int kTcProducerWarps = 4;
 constexpr int kTcRowsPerProducer = 128 / kTcProducerWarps;   // 32: one block id per lane
-constexpr int kTcGroups = 2;
-constexpr int kTcThreads = 32 * (kTcProducerWarps + 4 * kTcGroups);
 
 template <int NCH>
 struct TcGeom {
   static constexpr int NPAD = NCH * 16;
   static constexpr uint32_t kCols = NPAD <= 32 ? 32 : (NPAD <= 64 ? 64 : 128);  // per group
+  // epilogue groups of 4 warps, each with its own accumulator: three while the epilogue's
+  // registers fit 512 threads (N <= 64), else two
+  static constexpr int kGroups = NPAD <= 64 ? 3 : 2;
+  static constexpr int kThreads = 32 * (kTcProducerWarps + 4 * kGroups);
   static constexpr uint32_t kKeyBytes = 128 * 256;   // one tile of keys
   static constexpr uint32_t kQBytes = NPAD * 256;    // one layer's queries
   static constexpr int kFit = (int)((227u * 1024u - 4096u - 2u * kQBytes) / kKeyBytes);
   static constexpr int kStages = kFit < 6 ? kFit : 6;
-  static constexpr int kLag = kStages - kTcGroups;   // tiles in flight behind the newest
+  static constexpr int kLag = kStages - kGroups;     // tiles in flight behind the newest
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kKeyBytes + 2 * (size_t)kQBytes;
   static_assert(kLag >= 1, "stage ring too small");
   // tcgen05.alloc takes a power of two of at least 32 columns
-  static constexpr uint32_t kTmemCols = kTcGroups * kCols;
+  static constexpr uint32_t kTmemCols =
+      kGroups * kCols <= 128 ? 128 : (kGroups * kCols <= 256 ? 256 : 512);
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
                 "TMEM allocation must be a power of two");
 };
@@ -661,18 +664,18 @@ __device__ __forceinline__ void tile_cursor(const int32_t* ucount, int L, int t,
 }
 
 template <int NCH, int HH>
-__global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_constant__ ScoreArgs a) {
+__global__ void __launch_bounds__(TcGeom<NCH>::kThreads, 1) k5_score_tc(const __grid_constant__ ScoreArgs a) {
   using G = TcGeom<NCH>;
   constexpr int NPAD = G::NPAD, S = G::kStages, D = G::kLag;
   constexpr uint32_t kCols = G::kCols, kKeyBytes = G::kKeyBytes, kQBytes = G::kQBytes;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[S];
   __shared__ __align__(8) uint64_t bar_empty[S];
-  __shared__ __align__(8) uint64_t bar_mma[kTcGroups];
+  __shared__ __align__(8) uint64_t bar_mma[G::kGroups];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ float s_w[2][NPAD];
-  __shared__ float s_wg[kTcGroups][NPAD];       // each epilogue group's copy of its layer's w
+  __shared__ float s_wg[G::kGroups][NPAD];      // each epilogue group's copy of its layer's w
   __shared__ float s_F[2][8];
   __shared__ float s_qn[NPAD];
   __shared__ int s_tl[S], s_te[S], s_tn[S];     // per stage: layer, first entry, entry count
@@ -691,7 +694,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
       sm100::mbar_init(&bar_full[s], kTcProducerWarps);
       sm100::mbar_init(&bar_empty[s], 4);
     }
-    for (int g = 0; g < kTcGroups; ++g) sm100::mbar_init(&bar_mma[g], 1);
+    for (int g = 0; g < G::kGroups; ++g) sm100::mbar_init(&bar_mma[g], 1);
     s_abort = 0;
     sm100::fence_mbar_init();
   }
@@ -922,7 +925,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k5_score_tc(const __grid_consta
     const uint64_t spol = l2_evict_last_policy();   // scores stay in L2 for K7
     bool issued = false;    // this group has MMAs whose commit it has not observed
     int wlayer = -1;        // layer whose head weights s_wg[g] holds
-    for (int i = g; i < n; i += kTcGroups) {
+    for (int i = g; i < n; i += G::kGroups) {
       const int s = i % S;
       bool ok = !s_abort && sm100::mbar_wait(&bar_full[s], (i / S) & 1, kWaitPolls);
       ok = bar_and(bar_id, 128, ok);
@@ -1958,7 +1961,7 @@ cudaError_t launch_tc(const SelDims& d, const ScoreArgs& a, cudaStream_t s) {
   if (tiles < grid) grid = (int)tiles;
   if (grid < 1) grid = 1;
   // a programmatic dependent of the compaction: the CTAs set up while it finishes
-  return launch_pdl(k5_score_tc<NCH, HH>, dim3(grid), kTcThreads, smem, s, ta);
+  return launch_pdl(k5_score_tc<NCH, HH>, dim3(grid), TcGeom<NCH>::kThreads, smem, s, ta);
 }
 
 }  // namespace
